@@ -1,0 +1,363 @@
+// gdn_api.cu -- host side of libgdn: argument validation, launch planning, the C ABI.
+//
+// The operation and its citations are stated in include/gdn.h.  Nothing here computes
+// any part of the recurrence: every step runs in the kernels of gdn_fwd.cu / gdn_bwd.cu.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+gdn_status_t fail(gdn_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+gdn_status_t fail(gdn_status_t s, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+int64_t ceil_sqrt(int64_t T)
+{
+    if (T <= 1) return 1;
+    int64_t r = 1;
+    while (r * r < T) ++r;
+    return r;
+}
+
+// Launch plan: everything the kernels and the workspace size depend on.
+struct Plan {
+    int D = 0, RT = 1, W = 4, R = 16, P = 1, tc = 32, c2 = 1, nsub_max = 1;
+    bool kda = false;
+    int64_t C = 1, n_ck = 0;
+    size_t off_sub = 0, off_col = 0, off_sc = 0, ws_bytes = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+gdn_status_t check_sizes(const gdn_params_t* p)
+{
+    if (!p) return fail(GDN_ERR_INVALID_ARG, "params is NULL");
+    if (p->reserved0 != 0 || p->reserved1 != 0.0f)
+        return fail(GDN_ERR_INVALID_ARG, "reserved fields must be zero");
+    if (p->n_seq < 0 || p->T < 0) return fail(GDN_ERR_INVALID_ARG, "negative n_seq or T");
+    if (p->H_k < 1 || p->H_v < 1) return fail(GDN_ERR_INVALID_ARG, "H_k and H_v must be >= 1");
+    if (p->H_v % p->H_k != 0)
+        return fail(GDN_ERR_INVALID_ARG, "H_v (%lld) is not a multiple of H_k (%lld)",
+                    (long long)p->H_v, (long long)p->H_k);
+    if (p->gate != GDN_GATE_SCALAR && p->gate != GDN_GATE_KDA)
+        return fail(GDN_ERR_INVALID_ARG, "unknown gate kind %d", (int)p->gate);
+    if (p->S_k < 1 || p->S_v < 1) return fail(GDN_ERR_INVALID_ARG, "head sizes must be >= 1");
+    if (p->S_k != p->S_v)
+        return fail(GDN_ERR_UNSUPPORTED, "S_k (%lld) != S_v (%lld) is not supported",
+                    (long long)p->S_k, (long long)p->S_v);
+    if (p->S_k != 32 && p->S_k != 64 && p->S_k != 128)
+        return fail(GDN_ERR_UNSUPPORTED, "head size %lld is not supported (32, 64, 128)",
+                    (long long)p->S_k);
+    if (p->T > INT_MAX / 2 || p->H_v > 65535 || p->n_seq > 65535)
+        return fail(GDN_ERR_UNSUPPORTED, "sizes beyond the kernels' index range");
+    for (int i = 0; i < 3; ++i)
+        if (p->q_s[i] < 0 || p->k_s[i] < 0 || p->v_s[i] < 0 || p->gy_s[i] < 0)
+            return fail(GDN_ERR_INVALID_ARG, "negative stride");
+    return GDN_OK;
+}
+
+Plan make_plan(const gdn_params_t* p)
+{
+    Plan pl;
+    pl.D = (int)p->S_k;
+    pl.kda = p->gate == GDN_GATE_KDA;
+    pl.C = p->C > 0 ? p->C : ceil_sqrt(p->T);
+    if (pl.C > INT_MAX / 2) pl.C = INT_MAX / 2;
+    pl.n_ck = p->T > 0 ? (p->T + pl.C - 1) / pl.C : 0;
+    pl.RT = 1;
+    pl.W = 4;
+    pl.R = 4 * pl.RT * pl.W;
+    pl.P = pl.D / pl.R;
+    pl.tc = 32;
+    // Sub-segment length c2: as many ring slots as fit the shared memory of the number
+    // of CTAs each SM must hold for the whole grid to be resident (at most 4 per SM).
+    const long long ctas = (long long)p->n_seq * p->H_v * pl.P;
+    long long per_sm = (ctas + gdn::kNumSMs - 1) / gdn::kNumSMs;
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > 4) per_sm = 4;
+    long long budget = gdn::kSmemPerSM / per_sm - gdn::kSmemReservePerCta;
+    if (budget > gdn::kSmemPerCtaMax) budget = gdn::kSmemPerCtaMax;
+    const int cmax = (int)(pl.C < 64 ? pl.C : 64);
+    int c2 = 1;
+    for (int c = cmax; c >= 1; --c) {
+        const gdn::BwdSmem L = gdn::bwd_smem_layout(pl.D, pl.RT, pl.W, c, pl.kda);
+        if ((long long)L.total * 4 <= budget) { c2 = c; break; }
+    }
+    pl.c2 = c2;
+    pl.nsub_max = (int)((pl.C + c2 - 1) / c2);
+    if (p->T > 0 && pl.nsub_max > (p->T + c2 - 1) / c2) pl.nsub_max = (int)((p->T + c2 - 1) / c2);
+    // workspace: sub-checkpoints | column partials | scalar partials
+    const size_t NQ = pl.kda ? 3 : 2;
+    const size_t cta_state = (size_t)pl.R * pl.D;  // floats per CTA per stored state
+    const size_t sub_f = (size_t)ctas * (pl.nsub_max > 1 ? pl.nsub_max - 1 : 0) * cta_state;
+    const size_t toks = (size_t)p->n_seq * p->T * p->H_v;
+    const size_t col_f = toks * pl.P * NQ * pl.D;
+    const size_t sc_f = toks * pl.P * 2;
+    pl.off_sub = 0;
+    pl.off_col = align256(sub_f * 4);
+    pl.off_sc = pl.off_col + align256(col_f * 4);
+    pl.ws_bytes = pl.off_sc + align256(sc_f * 4);
+    return pl;
+}
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+// Byte extent of a [N][T][H][D] tensor with element strides {s0, s1, s2, 1}.
+Range extent4(const void* ptr, int64_t N, int64_t T, int64_t H, int64_t D, const int64_t s[3])
+{
+    const uintptr_t lo = (uintptr_t)ptr;
+    if (!ptr || N == 0 || T == 0 || H == 0 || D == 0) return {lo, lo};
+    const uint64_t last = (uint64_t)(s[0] * (N - 1) + s[1] * (T - 1) + s[2] * (H - 1) + D);
+    return {lo, lo + last * 4};
+}
+
+Range extent_dense(const void* ptr, size_t elems)
+{
+    const uintptr_t lo = (uintptr_t)ptr;
+    return {lo, ptr ? lo + elems * 4 : lo};
+}
+
+bool overlap(Range a, Range b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+bool vec_ok(const void* ptr, const int64_t s[3])
+{
+    return aligned(ptr, 16) && s[0] % 4 == 0 && s[1] % 4 == 0 && s[2] % 4 == 0;
+}
+
+void packed_offsets(const gdn_params_t* p, size_t off[7])
+{
+    const size_t N = (size_t)p->n_seq, T = (size_t)p->T, Hk = (size_t)p->H_k, Hv = (size_t)p->H_v;
+    const size_t Sk = (size_t)p->S_k, Sv = (size_t)p->S_v;
+    off[0] = 0;
+    off[1] = off[0] + N * T * Hk * Sk;
+    off[2] = off[1] + N * T * Hk * Sk;
+    off[3] = off[2] + N * T * Hv * Sv;
+    off[4] = off[3] + N * T * Hv * (p->gate == GDN_GATE_KDA ? Sk : 1);
+    off[5] = off[4] + N * T * Hv;
+    off[6] = off[5] + N * Hv * Sv * Sk;
+}
+
+gdn_status_t cuda_status(int err, const char* what)
+{
+    if (err == 0) return GDN_OK;
+    return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)err));
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t gdn_checkpoint_interval(const gdn_params_t* p)
+{
+    if (!p) return 0;
+    return p->C > 0 ? p->C : ceil_sqrt(p->T);
+}
+
+int64_t gdn_num_checkpoints(const gdn_params_t* p)
+{
+    if (!p || p->T <= 0) return 0;
+    const int64_t C = gdn_checkpoint_interval(p);
+    return (p->T + C - 1) / C;
+}
+
+size_t gdn_ckpt_elems(const gdn_params_t* p)
+{
+    if (!p) return 0;
+    return (size_t)p->n_seq * p->H_v * gdn_num_checkpoints(p) * p->S_v * p->S_k;
+}
+
+size_t gdn_packed_grad_elems(const gdn_params_t* p)
+{
+    if (!p) return 0;
+    size_t off[7];
+    packed_offsets(p, off);
+    return off[6];
+}
+
+void gdn_packed_grad_offsets(const gdn_params_t* p, size_t off[6])
+{
+    if (!p || !off) return;
+    size_t o[7];
+    packed_offsets(p, o);
+    for (int i = 0; i < 6; ++i) off[i] = o[i];
+}
+
+size_t gdn_backward_workspace_bytes(const gdn_params_t* p)
+{
+    if (check_sizes(p) != GDN_OK) return 0;
+    return make_plan(p).ws_bytes;
+}
+
+int gdn_forward_launches(const gdn_params_t* p)
+{
+    if (check_sizes(p) != GDN_OK) return 0;
+    return p->n_seq > 0 ? 1 : 0;
+}
+
+int gdn_backward_launches(const gdn_params_t* p)
+{
+    if (check_sizes(p) != GDN_OK) return 0;
+    if (p->n_seq == 0) return 0;
+    return p->T > 0 ? 2 : 1;
+}
+
+const char* gdn_status_str(gdn_status_t s)
+{
+    switch (s) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+        case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS";
+        case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    }
+    return "unknown gdn status";
+}
+
+const char* gdn_last_error(void) { return g_last_error.c_str(); }
+
+gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, const float* v,
+                         const float* g, const float* beta, const float* state0, float* y,
+                         float* state_T, float* ckpt, void* stream)
+{
+    gdn_status_t st = check_sizes(p);
+    if (st != GDN_OK) return st;
+    g_last_error.clear();
+    const Plan pl = make_plan(p);
+    const int64_t N = p->n_seq, T = p->T, Hk = p->H_k, Hv = p->H_v, D = p->S_k;
+    if (N == 0) return GDN_OK;
+    const bool tok = T > 0;
+    if (tok && (!q || !k || !v || !g || !beta))
+        return fail(GDN_ERR_INVALID_ARG, "q, k, v, g and beta must be non-NULL");
+    if (!state0 || !state_T) return fail(GDN_ERR_INVALID_ARG, "state0 and state_T must be non-NULL");
+    if (tok && (!y || !ckpt)) return fail(GDN_ERR_INVALID_ARG, "y and ckpt must be non-NULL");
+    for (const void* ptr : {(const void*)q, (const void*)k, (const void*)v, (const void*)g,
+                            (const void*)beta, (const void*)y})
+        if (!aligned(ptr, 4)) return fail(GDN_ERR_INVALID_ARG, "pointer not 4-byte aligned");
+    if (!aligned(state0, 16) || !aligned(state_T, 16) || !aligned(ckpt, 16))
+        return fail(GDN_ERR_INVALID_ARG, "state0, state_T and ckpt must be 16-byte aligned");
+
+    const int64_t gw = pl.kda ? D : 1;
+    const Range rq = extent4(q, N, T, Hk, D, p->q_s), rk = extent4(k, N, T, Hk, D, p->k_s);
+    const Range rv = extent4(v, N, T, Hv, D, p->v_s);
+    const Range rg = extent_dense(g, (size_t)(N * T * Hv * gw));
+    const Range rb = extent_dense(beta, (size_t)(N * T * Hv));
+    const Range rs0 = extent_dense(state0, (size_t)(N * Hv * D * D));
+    const Range ry = extent_dense(y, (size_t)(N * T * Hv * D));
+    const Range rsT = extent_dense(state_T, (size_t)(N * Hv * D * D));
+    const Range rck = extent_dense(ckpt, (size_t)(N * Hv * pl.n_ck * D * D));
+    for (Range out : {ry, rsT, rck})
+        for (Range in : {rq, rk, rv, rg, rb, rs0})
+            if (overlap(out, in)) return fail(GDN_ERR_ALIAS, "a forward output overlaps an input");
+    if (overlap(ry, rsT) || overlap(ry, rck) || overlap(rsT, rck))
+        return fail(GDN_ERR_ALIAS, "forward outputs overlap one another");
+
+    gdn::FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state0 = state0;
+    a.y = y; a.state_T = state_T; a.ckpt = ckpt;
+    a.qs0 = p->q_s[0]; a.qs1 = p->q_s[1]; a.qs2 = p->q_s[2];
+    a.ks0 = p->k_s[0]; a.ks1 = p->k_s[1]; a.ks2 = p->k_s[2];
+    a.vs0 = p->v_s[0]; a.vs1 = p->v_s[1]; a.vs2 = p->v_s[2];
+    a.N = (int)N; a.T = (int)T; a.H_k = (int)Hk; a.H_v = (int)Hv;
+    a.C = (int)pl.C; a.n_ck = (int)pl.n_ck; a.scale = p->scale; a.tc = pl.tc;
+    a.vec_q = vec_ok(q, p->q_s); a.vec_k = vec_ok(k, p->k_s); a.vec_v = vec_ok(v, p->v_s);
+    a.vec_g = aligned(g, 16);
+    return cuda_status(gdn::launch_forward(a, pl.D, pl.RT, pl.W, pl.kda, stream), "forward launch");
+}
+
+gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k, const float* v,
+                          const float* g, const float* beta, const float* ckpt, const float* gy,
+                          const float* dstate_T, float* packed, void* workspace,
+                          size_t workspace_bytes, void* stream)
+{
+    gdn_status_t st = check_sizes(p);
+    if (st != GDN_OK) return st;
+    g_last_error.clear();
+    const Plan pl = make_plan(p);
+    const int64_t N = p->n_seq, T = p->T, Hk = p->H_k, Hv = p->H_v, D = p->S_k;
+    if (N == 0) return GDN_OK;
+    const bool tok = T > 0;
+    if (tok && (!q || !k || !v || !g || !beta || !ckpt || !gy))
+        return fail(GDN_ERR_INVALID_ARG, "q, k, v, g, beta, ckpt and gy must be non-NULL");
+    if (!packed) return fail(GDN_ERR_INVALID_ARG, "packed_grads must be non-NULL");
+    for (const void* ptr : {(const void*)q, (const void*)k, (const void*)v, (const void*)g,
+                            (const void*)beta, (const void*)gy})
+        if (!aligned(ptr, 4)) return fail(GDN_ERR_INVALID_ARG, "pointer not 4-byte aligned");
+    if (!aligned(ckpt, 16) || !aligned(dstate_T, 16) || !aligned(packed, 16))
+        return fail(GDN_ERR_INVALID_ARG, "ckpt, dstate_T and packed_grads must be 16-byte aligned");
+    if (workspace_bytes < pl.ws_bytes)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    pl.ws_bytes);
+    if (pl.ws_bytes > 0 && (!workspace || !aligned(workspace, 256)))
+        return fail(GDN_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+
+    size_t off[7];
+    packed_offsets(p, off);
+    const int64_t gw = pl.kda ? D : 1;
+    const Range rq = extent4(q, N, T, Hk, D, p->q_s), rk = extent4(k, N, T, Hk, D, p->k_s);
+    const Range rv = extent4(v, N, T, Hv, D, p->v_s), rgy = extent4(gy, N, T, Hv, D, p->gy_s);
+    const Range rg = extent_dense(g, (size_t)(N * T * Hv * gw));
+    const Range rb = extent_dense(beta, (size_t)(N * T * Hv));
+    const Range rck = extent_dense(ckpt, (size_t)(N * Hv * pl.n_ck * D * D));
+    const Range rdsT = extent_dense(dstate_T, (size_t)(N * Hv * D * D));
+    const Range rpk = extent_dense(packed, off[6]);
+    const Range rws = {(uintptr_t)workspace, (uintptr_t)workspace + (workspace ? pl.ws_bytes : 0)};
+    for (Range out : {rpk, rws})
+        for (Range in : {rq, rk, rv, rgy, rg, rb, rck, rdsT})
+            if (overlap(out, in)) return fail(GDN_ERR_ALIAS, "a backward output overlaps an input");
+    if (overlap(rpk, rws)) return fail(GDN_ERR_ALIAS, "workspace overlaps packed_grads");
+
+    char* ws = (char*)workspace;
+    gdn::BwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.ckpt = ckpt; a.gy = gy;
+    a.dstate_T = dstate_T;
+    a.dv = packed + off[2];
+    a.dstate0 = packed + off[5];
+    a.sub = (float*)(ws + pl.off_sub);
+    a.ws_col = (float*)(ws + pl.off_col);
+    a.ws_sc = (float*)(ws + pl.off_sc);
+    a.qs0 = p->q_s[0]; a.qs1 = p->q_s[1]; a.qs2 = p->q_s[2];
+    a.ks0 = p->k_s[0]; a.ks1 = p->k_s[1]; a.ks2 = p->k_s[2];
+    a.vs0 = p->v_s[0]; a.vs1 = p->v_s[1]; a.vs2 = p->v_s[2];
+    a.gys0 = p->gy_s[0]; a.gys1 = p->gy_s[1]; a.gys2 = p->gy_s[2];
+    a.N = (int)N; a.T = (int)T; a.H_k = (int)Hk; a.H_v = (int)Hv;
+    a.C = (int)pl.C; a.n_ck = (int)pl.n_ck; a.c2 = pl.c2; a.nsub_max = pl.nsub_max;
+    a.scale = p->scale;
+    a.vec_q = vec_ok(q, p->q_s); a.vec_k = vec_ok(k, p->k_s); a.vec_v = vec_ok(v, p->v_s);
+    a.vec_gy = vec_ok(gy, p->gy_s); a.vec_g = aligned(g, 16);
+    a.vec_ds0 = aligned(packed + off[5], 16);
+    st = cuda_status(gdn::launch_backward(a, pl.D, pl.RT, pl.W, pl.kda, stream), "backward launch");
+    if (st != GDN_OK || !tok) return st;
+
+    gdn::ReduceArgs r{};
+    r.ws_col = a.ws_col; r.ws_sc = a.ws_sc;
+    r.dq = packed + off[0]; r.dk = packed + off[1]; r.dg = packed + off[3]; r.dbeta = packed + off[4];
+    r.N = (int)N; r.T = (int)T; r.H_k = (int)Hk; r.H_v = (int)Hv; r.D = (int)D; r.P = pl.P;
+    r.NQ = pl.kda ? 3 : 2; r.kda = pl.kda;
+    return cuda_status(gdn::launch_reduce(r, stream), "reduce launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,151 @@
+// gdn_fwd.cu -- forward of the gated delta rule (sm_103a).
+//
+// Grid (P, H_v, N): CTA p owns rows [p R, p R + R) of M = S^T for one (sequence, value
+// head).  Rows are independent in the forward (every term of the step is row-local:
+// "metal: GATED_DELTA_NET_BACK", PR #16 review "APPROVED at 739b9bf", "Thread j owns
+// row j of M"), so CTAs never communicate and warps never wait on one another inside
+// a tile: each warp runs its own chain of tokens over its rows.
+//
+// Per tile of tc tokens the CTA stages k, q, a = exp(g), beta and its own rows of v in
+// shared memory; the state lives in registers (RT rows x S/8 columns per lane).  The
+// state entering token c*C is written to ckpt[c] (PR #16 body: checkpointed recompute).
+#include <cuda_runtime.h>
+
+#include "gdn_device.cuh"
+
+namespace gdn {
+
+template <int D, int RT, bool KDA>
+__global__ void __launch_bounds__(256) gdn_fwd_kernel(const FwdArgs A)
+{
+    constexpr int NV = D / 32;
+    const int NT = blockDim.x, W = NT >> 5;
+    const int R = 4 * RT * W;
+    const int p = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int hk = h % A.H_k;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int grp = lane >> 3, cl = lane & 7;
+    const int lrow0 = warp * 4 * RT + grp * RT;
+    const int row0 = p * R + lrow0;
+    const int tc = A.tc;
+
+    extern __shared__ __align__(16) float sm[];
+    const FwdSmem L = fwd_smem_layout(D, RT, W, tc, KDA);
+    float* sk = sm + L.sk;
+    float* sq = sm + L.sq;
+    float* sa = sm + L.sa;
+    float* sb = sm + L.sb;
+    float* sv = sm + L.sv;
+    float* sy = sm + L.sy;
+
+    const long long head = (long long)n * A.H_v + h;
+    float4 m[RT][NV];
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+            m[r][v] = __ldg(reinterpret_cast<const float4*>(A.state0 + (head * D + row0 + r) * D) +
+                            8 * v + cl);
+
+    for (int t0 = 0; t0 < A.T; t0 += tc) {
+        const int nt = min(tc, A.T - t0);
+        __syncthreads();
+        load_rows(sk, A.k + n * A.ks0 + (long long)t0 * A.ks1 + hk * A.ks2, A.ks1, nt, D,
+                  A.vec_k, tid, NT);
+        load_rows(sq, A.q + n * A.qs0 + (long long)t0 * A.qs1 + hk * A.qs2, A.qs1, nt, D,
+                  A.vec_q, tid, NT);
+        const long long tok0 = (long long)n * A.T + t0;
+        if (KDA) {
+            load_rows_exp(sa, A.g + (tok0 * A.H_v + h) * D, (long long)A.H_v * D, nt, D,
+                          A.vec_g, tid, NT);
+        } else {
+            for (int tt = tid; tt < nt; tt += NT) sa[tt] = expf(__ldg(A.g + (tok0 + tt) * A.H_v + h));
+        }
+        for (int tt = tid; tt < nt; tt += NT) sb[tt] = __ldg(A.beta + (tok0 + tt) * A.H_v + h);
+        load_rows(sv, A.v + n * A.vs0 + (long long)t0 * A.vs1 + h * A.vs2 + p * R, A.vs1, nt, R,
+                  A.vec_v, tid, NT);
+        __syncthreads();
+
+        for (int tt = 0; tt < nt; ++tt) {
+            const int t = t0 + tt;
+            if (t % A.C == 0) {
+                float* ck = A.ckpt + ((head * A.n_ck + t / A.C) * D + row0) * D;
+#pragma unroll
+                for (int r = 0; r < RT; ++r)
+#pragma unroll
+                    for (int v = 0; v < NV; ++v)
+                        reinterpret_cast<float4*>(ck + r * D)[8 * v + cl] = m[r][v];
+            }
+            float4 kv[NV], qv[NV], av[NV];
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                kv[v] = lds_cols<D>(sk + tt * D, v, cl);
+                qv[v] = lds_cols<D>(sq + tt * D, v, cl);
+                if (KDA) av[v] = lds_cols<D>(sa + tt * D, v, cl);
+            }
+            const float as = KDA ? 0.f : sa[tt];
+            float vj[RT], u[RT], delta[RT];
+#pragma unroll
+            for (int r = 0; r < RT; ++r) vj[r] = sv[tt * R + lrow0 + r];
+            float4 sp[RT][NV];
+            recurrence_step<NV, RT, KDA>(m, sp, kv, av, as, sb[tt], vj, u, delta);
+            // y_j = scale * sum_i M_t[j][i] q_i  (meTile: output = scale * state^T query)
+            float w[RT];
+#pragma unroll
+            for (int r = 0; r < RT; ++r) w[r] = dot_part<NV>(m[r], qv);
+#pragma unroll
+            for (int r = 0; r < RT; ++r) w[r] = rowsum8(w[r]);
+            if (cl == 0) {
+#pragma unroll
+                for (int r = 0; r < RT; ++r) sy[tt * R + lrow0 + r] = __fmul_rn(A.scale, w[r]);
+            }
+        }
+        __syncthreads();
+        // y rows of this CTA for the tile: R contiguous floats per token
+        float* ydst = A.y + (tok0 * A.H_v + h) * D + p * R;
+        const long long ystride = (long long)A.H_v * D;
+        for (int idx = tid; idx < nt * R; idx += NT) {
+            const int tt = idx / R, j = idx - tt * R;
+            ydst[tt * ystride + j] = sy[tt * R + j];
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+            reinterpret_cast<float4*>(A.state_T + (head * D + row0 + r) * D)[8 * v + cl] = m[r][v];
+}
+
+template <int D, int RT, bool KDA>
+static int launch_fwd_t(const FwdArgs& a, int W, void* stream)
+{
+    const int R = 4 * RT * W;
+    const FwdSmem L = fwd_smem_layout(D, RT, W, a.tc, KDA);
+    const size_t smem = (size_t)L.total * sizeof(float);
+    auto kern = gdn_fwd_kernel<D, RT, KDA>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    dim3 grid(D / R, a.H_v, a.N);
+    kern<<<grid, 32 * W, smem, (cudaStream_t)stream>>>(a);
+    return (int)cudaGetLastError();
+}
+
+int launch_forward(const FwdArgs& a, int D, int RT, int W, bool kda, void* stream)
+{
+#define GDN_FWD_CASE(DD, RR)                                                          \
+    if (D == DD && RT == RR)                                                          \
+        return kda ? launch_fwd_t<DD, RR, true>(a, W, stream)                         \
+                   : launch_fwd_t<DD, RR, false>(a, W, stream);
+    GDN_FWD_CASE(32, 1)
+    GDN_FWD_CASE(64, 1)
+    GDN_FWD_CASE(128, 1)
+    GDN_FWD_CASE(32, 2)
+    GDN_FWD_CASE(64, 2)
+    GDN_FWD_CASE(128, 2)
+#undef GDN_FWD_CASE
+    return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace gdn

@@ -1,0 +1,126 @@
+// gdn_internal.h -- host/device shared declarations of libgdn (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define GDN_HD __host__ __device__
+#else
+#define GDN_HD
+#endif
+
+namespace gdn {
+
+// Thread layout shared by every recurrence kernel: a warp holds 4 row groups of 8
+// column lanes; lane = 8 * group + column_lane.  Column lane c owns the float4 blocks
+// starting at columns 32 v + 4 c (v < S/32) of each row the thread holds.
+constexpr int kColLanes = 8;
+constexpr int kGroups = 4;
+
+// GB300 facts the launch planner sizes for.
+constexpr int kNumSMs = 152;
+constexpr int kSmemPerSM = 228 * 1024;     // shared memory per SM
+constexpr int kSmemPerCtaMax = 227 * 1024; // opt-in maximum per CTA
+constexpr int kSmemReservePerCta = 1024;   // driver-reserved per resident CTA
+
+struct FwdArgs {
+    const float* q;
+    const float* k;
+    const float* v;
+    const float* g;
+    const float* beta;
+    const float* state0;
+    float* y;
+    float* state_T;
+    float* ckpt;
+    long long qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2;
+    int N, T, H_k, H_v, C, n_ck;
+    float scale;
+    int tc;  // tokens per shared-memory tile
+    int vec_q, vec_k, vec_v, vec_g;
+};
+
+struct BwdArgs {
+    const float* q;
+    const float* k;
+    const float* v;
+    const float* g;
+    const float* beta;
+    const float* ckpt;
+    const float* gy;
+    const float* dstate_T;  // may be null
+    float* dv;              // packed dv region
+    float* dstate0;         // packed dstate region
+    float* sub;             // workspace: level-1 sub-checkpoints
+    float* ws_col;          // workspace: per-CTA column partials [N*T*H_v][P][NQ*D]
+    float* ws_sc;           // workspace: per-CTA scalar partials [N*T*H_v][P][2]
+    long long qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2, gys0, gys1, gys2;
+    int N, T, H_k, H_v, C, n_ck, c2, nsub_max;
+    float scale;
+    int vec_q, vec_k, vec_v, vec_gy, vec_g, vec_ds0;
+};
+
+struct ReduceArgs {
+    const float* ws_col;
+    const float* ws_sc;
+    float* dq;
+    float* dk;
+    float* dg;
+    float* dbeta;
+    int N, T, H_k, H_v, D, P, NQ, kda;
+};
+
+// Shared-memory layout of the backward kernel, in floats (every offset a multiple of 4).
+struct BwdSmem {
+    int ring, sk, sq, sa, sb, sv, sgy, sdel, svmu, sdd, scol, sdg, total;
+};
+
+GDN_HD inline int round4(int x) { return (x + 3) & ~3; }
+
+GDN_HD inline BwdSmem bwd_smem_layout(int D, int RT, int W, int c2, bool kda)
+{
+    const int NT = 32 * W, R = 4 * RT * W, NV = D / 32, NQ = kda ? 3 : 2;
+    BwdSmem s;
+    int o = 0;
+    s.ring = o; o += c2 * RT * NV * NT * 4;
+    s.sk = o;   o += c2 * D;
+    s.sq = o;   o += c2 * D;
+    s.sa = o;   o += kda ? c2 * D : round4(c2);
+    s.sb = o;   o += round4(c2);
+    s.sv = o;   o += round4(c2 * R);
+    s.sgy = o;  o += round4(c2 * R);
+    s.sdel = o; o += round4(c2 * R);
+    s.svmu = o; o += round4(c2 * R);
+    s.sdd = o;  o += round4(c2 * R);
+    s.scol = o; o += W * c2 * NQ * D;
+    s.sdg = o;  o += kda ? 0 : W * c2 * 32;
+    s.total = o;
+    return s;
+}
+
+struct FwdSmem {
+    int sk, sq, sa, sb, sv, sy, total;
+};
+
+GDN_HD inline FwdSmem fwd_smem_layout(int D, int RT, int W, int tc, bool kda)
+{
+    const int R = 4 * RT * W;
+    FwdSmem s;
+    int o = 0;
+    s.sk = o; o += tc * D;
+    s.sq = o; o += tc * D;
+    s.sa = o; o += kda ? tc * D : round4(tc);
+    s.sb = o; o += round4(tc);
+    s.sv = o; o += round4(tc * R);
+    s.sy = o; o += round4(tc * R);
+    s.total = o;
+    return s;
+}
+
+// Launchers (defined in gdn_fwd.cu / gdn_bwd.cu).  Return a cudaError_t as int.
+int launch_forward(const FwdArgs& a, int D, int RT, int W, bool kda, void* stream);
+int launch_backward(const BwdArgs& a, int D, int RT, int W, bool kda, void* stream);
+int launch_reduce(const ReduceArgs& a, void* stream);
+
+}  // namespace gdn

@@ -1,0 +1,216 @@
+"""ctypes binding of libgdn (include/gdn.h): argument marshalling only.
+
+Every step of the gated delta rule runs in the CUDA kernels behind the C ABI; this
+module builds the parameter struct from tensors, allocates outputs with PyTorch (device
+memory and streams are all PyTorch is used for) and raises on a non-OK status.  There is
+no fallback: importing this module fails loudly when libgdn.so has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libgdn.so not found at {LIB_PATH}; build it first "
+        "(python -c 'import __graft_entry__ as g; g.build()')")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+GDN_OK = 0
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIAS",
+          4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT"}
+GATE_SCALAR, GATE_KDA = 0, 1
+
+# Every symbol include/gdn.h declares.
+EXPORTS = ["gdn_checkpoint_interval", "gdn_num_checkpoints", "gdn_ckpt_elems", "gdn_forward",
+           "gdn_packed_grad_elems", "gdn_packed_grad_offsets", "gdn_backward_workspace_bytes",
+           "gdn_backward", "gdn_status_str", "gdn_last_error", "gdn_forward_launches",
+           "gdn_backward_launches"]
+
+
+class GdnParams(ctypes.Structure):
+    _fields_ = [
+        ("n_seq", ctypes.c_int64), ("T", ctypes.c_int64), ("H_k", ctypes.c_int64),
+        ("H_v", ctypes.c_int64), ("S_k", ctypes.c_int64), ("S_v", ctypes.c_int64),
+        ("gate", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("C", ctypes.c_int64),
+        ("scale", ctypes.c_float), ("reserved1", ctypes.c_float),
+        ("q_s", ctypes.c_int64 * 3), ("k_s", ctypes.c_int64 * 3),
+        ("v_s", ctypes.c_int64 * 3), ("gy_s", ctypes.c_int64 * 3),
+    ]
+
+
+_P = ctypes.POINTER(GdnParams)
+_vp = ctypes.c_void_p
+_lib.gdn_checkpoint_interval.argtypes = [_P]
+_lib.gdn_checkpoint_interval.restype = ctypes.c_int64
+_lib.gdn_num_checkpoints.argtypes = [_P]
+_lib.gdn_num_checkpoints.restype = ctypes.c_int64
+_lib.gdn_ckpt_elems.argtypes = [_P]
+_lib.gdn_ckpt_elems.restype = ctypes.c_size_t
+_lib.gdn_packed_grad_elems.argtypes = [_P]
+_lib.gdn_packed_grad_elems.restype = ctypes.c_size_t
+_lib.gdn_packed_grad_offsets.argtypes = [_P, ctypes.POINTER(ctypes.c_size_t)]
+_lib.gdn_packed_grad_offsets.restype = None
+_lib.gdn_backward_workspace_bytes.argtypes = [_P]
+_lib.gdn_backward_workspace_bytes.restype = ctypes.c_size_t
+_lib.gdn_forward.argtypes = [_P] + [_vp] * 10
+_lib.gdn_forward.restype = ctypes.c_int
+_lib.gdn_backward.argtypes = [_P] + [_vp] * 10 + [ctypes.c_size_t, _vp]
+_lib.gdn_backward.restype = ctypes.c_int
+_lib.gdn_status_str.argtypes = [ctypes.c_int]
+_lib.gdn_status_str.restype = ctypes.c_char_p
+_lib.gdn_last_error.argtypes = []
+_lib.gdn_last_error.restype = ctypes.c_char_p
+_lib.gdn_forward_launches.argtypes = [_P]
+_lib.gdn_forward_launches.restype = ctypes.c_int
+_lib.gdn_backward_launches.argtypes = [_P]
+_lib.gdn_backward_launches.restype = ctypes.c_int
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        detail = _lib.gdn_last_error().decode()
+        super().__init__(f"{what}: {STATUS.get(status, status)}: {detail}")
+
+
+def library():
+    return _lib
+
+
+def make_params(N, T, H_k, H_v, S, kda, C=None, scale=None, q_s=None, k_s=None, v_s=None,
+                gy_s=None) -> GdnParams:
+    """Parameter struct; strides default to the contiguous [N,T,H,S] layout."""
+    p = GdnParams()
+    p.n_seq, p.T, p.H_k, p.H_v, p.S_k, p.S_v = N, T, H_k, H_v, S, S
+    p.gate = GATE_KDA if kda else GATE_SCALAR
+    p.reserved0, p.reserved1 = 0, 0.0
+    p.C = 0 if C is None else int(C)
+    p.scale = (1.0 / math.sqrt(S)) if scale is None else float(scale)
+    p.q_s[:] = q_s or (T * H_k * S, H_k * S, S)
+    p.k_s[:] = k_s or (T * H_k * S, H_k * S, S)
+    p.v_s[:] = v_s or (T * H_v * S, H_v * S, S)
+    p.gy_s[:] = gy_s or (T * H_v * S, H_v * S, S)
+    return p
+
+
+def strides3(t):
+    """Element strides of a [N,T,H,S] tensor view (its last dim must be contiguous)."""
+    if t.stride(-1) != 1:
+        raise ValueError("the head dimension must be contiguous")
+    return tuple(int(s) for s in t.stride()[:3])
+
+
+def params_for(q, k, v, g, gy=None, C=None, scale=None) -> GdnParams:
+    N, T, H_k, S = q.shape
+    H_v = v.shape[2]
+    kda = g.dim() == 4
+    return make_params(N, T, H_k, H_v, S, kda, C=C, scale=scale, q_s=strides3(q),
+                       k_s=strides3(k), v_s=strides3(v),
+                       gy_s=strides3(gy) if gy is not None else None)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def num_checkpoints(p: GdnParams) -> int:
+    return int(_lib.gdn_num_checkpoints(ctypes.byref(p)))
+
+
+def checkpoint_interval(p: GdnParams) -> int:
+    return int(_lib.gdn_checkpoint_interval(ctypes.byref(p)))
+
+
+def packed_grad_elems(p: GdnParams) -> int:
+    return int(_lib.gdn_packed_grad_elems(ctypes.byref(p)))
+
+
+def packed_grad_offsets(p: GdnParams):
+    off = (ctypes.c_size_t * 6)()
+    _lib.gdn_packed_grad_offsets(ctypes.byref(p), off)
+    return [int(x) for x in off]
+
+
+def backward_workspace_bytes(p: GdnParams) -> int:
+    return int(_lib.gdn_backward_workspace_bytes(ctypes.byref(p)))
+
+
+def launches(p: GdnParams):
+    """(forward kernels, backward kernels) one call of each enqueues."""
+    return (int(_lib.gdn_forward_launches(ctypes.byref(p))),
+            int(_lib.gdn_backward_launches(ctypes.byref(p))))
+
+
+def gdn_forward(p: GdnParams, q, k, v, g, beta, state0, y, state_T, ckpt, stream=None):
+    """Raw C-ABI call on caller-provided tensors (all on the current CUDA device)."""
+    st = _lib.gdn_forward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                          _ptr(state0), _ptr(y), _ptr(state_T), _ptr(ckpt),
+                          _stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_forward")
+
+
+def gdn_backward(p: GdnParams, q, k, v, g, beta, ckpt, gy, dstate_T, packed, workspace,
+                 stream=None):
+    st = _lib.gdn_backward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           _ptr(ckpt), _ptr(gy), _ptr(dstate_T), _ptr(packed),
+                           _ptr(workspace),
+                           ctypes.c_size_t(0 if workspace is None else workspace.numel()),
+                           _stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_backward")
+
+
+def forward(q, k, v, g, beta, state0, C=None, scale=None, stream=None):
+    """Allocate y, state_T, ckpt and run gdn_forward.  Returns (y, state_T, ckpt, params)."""
+    import torch
+    p = params_for(q, k, v, g, C=C, scale=scale)
+    N, T, H_k, S = q.shape
+    H_v = v.shape[2]
+    dev = q.device
+    y = torch.empty((N, T, H_v, S), dtype=torch.float32, device=dev)
+    state_T = torch.empty((N, H_v, S, S), dtype=torch.float32, device=dev)
+    ckpt = torch.empty((N, H_v, num_checkpoints(p), S, S), dtype=torch.float32, device=dev)
+    gdn_forward(p, q, k, v, g, beta, state0, y, state_T, ckpt, stream)
+    return y, state_T, ckpt, p
+
+
+def split_packed(p: GdnParams, packed):
+    """Views of the six regions of a packed gradient buffer."""
+    N, T, H_k, H_v, S = p.n_seq, p.T, p.H_k, p.H_v, p.S_k
+    off = packed_grad_offsets(p) + [packed_grad_elems(p)]
+    shapes = [(N, T, H_k, S), (N, T, H_k, S), (N, T, H_v, S),
+              (N, T, H_v, S) if p.gate == GATE_KDA else (N, T, H_v), (N, T, H_v),
+              (N, H_v, S, S)]
+    names = ["dq", "dk", "dv", "dg", "dbeta", "dstate0"]
+    return {nm: packed[off[i]:off[i + 1]].view(shapes[i]) for i, nm in enumerate(names)}
+
+
+def backward(p: GdnParams, q, k, v, g, beta, ckpt, gy, dstate_T=None, stream=None,
+             workspace=None):
+    """Allocate the packed buffer (and workspace unless given) and run gdn_backward.
+
+    Returns (packed, views) where views maps dq, dk, dv, dg, dbeta, dstate0 to regions."""
+    import torch
+    dev = q.device
+    if tuple(int(s) for s in p.gy_s) != strides3(gy):
+        p.gy_s[:] = strides3(gy)
+    packed = torch.empty(packed_grad_elems(p), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(backward_workspace_bytes(p), 1), dtype=torch.uint8,
+                                device=dev)
+    gdn_backward(p, q, k, v, g, beta, ckpt, gy, dstate_T, packed, workspace, stream)
+    return packed, split_packed(p, packed)

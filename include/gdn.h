@@ -1,0 +1,144 @@
+/*
+ * gdn.h -- C ABI of libgdn: the gated delta rule (Gated DeltaNet with a scalar gate,
+ * Kimi Delta Attention with a per-key-column gate), forward and backward, as CUDA
+ * kernels for sm_103a (GB300).
+ *
+ * The operation
+ * -------------
+ * Per sequence n and value head h (its key head is h mod H_k), with the state kept as
+ * M = S^T (S_v rows j = value index, S_k columns i = key index) and a = exp(g):
+ *     S'      = a (.) M_{t-1}                 (S'[j][i] = a_i M_{t-1}[j][i])
+ *     u_j     = sum_i S'[j][i] k_i,   delta_j = beta (v_j - u_j)
+ *     M_t     = S' + k delta^T        (M_t[j][i] = S'[j][i] + k_i delta_j)
+ *     y_j     = scale sum_i M_t[j][i] q_i
+ * Sources: "metal: GATED_DELTA_NET_BACK" (llama.cpp fork PR #16), review comment
+ * "APPROVED at 739b9bf" (row form); meTile "Training kernels and gradients", section
+ * "Recurrent delta attention" (matrix form, decay before correction).
+ *
+ * The backward walks the tokens in reverse from dM = dstate_T (PR #16 review "Math,
+ * read term by term"): dM += scale gy q^T; dq = scale M_t^T gy; dd = dM k;
+ * dv = beta dd; du = -beta dd; dbeta = sum_j dd_j (v_j - u_j);
+ * dk = dM^T delta + S'^T du (dM read before the du update); dM += k du^T (= dS');
+ * dg = sum_j dS' (.) S' per key column (KDA) or summed (scalar gate); dM = a (.) dS'.
+ * dq/dk are summed over the H_v/H_k value heads that share a key head, in ascending
+ * value-head order, without atomics.
+ *
+ * Checkpointed recompute (PR #16 body: "checkpointed recompute (C ~ sqrt(T))"): the
+ * forward stores ckpt[c] = the state entering token c*C for c = 0..n_ck-1,
+ * n_ck = ceil(T/C); the backward recomputes every segment from its checkpoint.  The
+ * backward returns one packed buffer [dq|dk|dv|dg|dbeta|dstate] (PR #16 body).
+ *
+ * Layouts (fp32, M = S^T)
+ * -----------------------
+ *   q, k      [N][T][H_k][S_k]  element strides q_s/k_s = {seq, token, head}; the
+ *                               S_k elements of one (seq, token, head) are contiguous
+ *                               (so q, k may be row views of a packed qkv buffer)
+ *   v         [N][T][H_v][S_v]  strides v_s, last dim contiguous
+ *   gy        [N][T][H_v][S_v]  strides gy_s, last dim contiguous
+ *   g         [N][T][H_v] (scalar gate) or [N][T][H_v][S_k] (KDA), contiguous
+ *   beta      [N][T][H_v] contiguous
+ *   state0, state_T, dstate_T    [N][H_v][S_v][S_k] contiguous
+ *   y         [N][T][H_v][S_v] contiguous
+ *   ckpt      [N][H_v][n_ck][S_v][S_k] contiguous
+ *   packed    dq [N][T][H_k][S_k] | dk [N][T][H_k][S_k] | dv [N][T][H_v][S_v] |
+ *             dg (like g) | dbeta [N][T][H_v] | dstate [N][H_v][S_v][S_k], back to back
+ *             (element offsets from gdn_packed_grad_offsets)
+ *
+ * Ownership and ordering
+ * ----------------------
+ * The caller owns every buffer and the stream; the library allocates nothing and keeps
+ * no pointer after a call returns.  Work is enqueued on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream): GDN_OK means "validated and launched".  The inputs and
+ * ckpt must stay unchanged between gdn_forward and gdn_backward; the backward never
+ * writes its inputs.  Inputs must be finite.
+ *
+ * Errors (no call ever writes an output when it returns an error)
+ * ------
+ *   GDN_ERR_INVALID_ARG  NULL pointer, negative size, H_v % H_k != 0, a stride that is
+ *                        negative, a pointer that is not 4-byte aligned, a state or
+ *                        output buffer that is not 16-byte aligned, bad gate kind
+ *   GDN_ERR_UNSUPPORTED  S_k != S_v, or a head size other than 32, 64, 128
+ *   GDN_ERR_ALIAS        an output overlaps an input (state_T over state0 included)
+ *   GDN_ERR_WORKSPACE    workspace smaller than gdn_backward_workspace_bytes()
+ *   GDN_ERR_CUDA         a CUDA launch failed (text in gdn_last_error())
+ * gdn_last_error() returns a description of the last failure on the calling thread.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,
+    GDN_ERR_UNSUPPORTED = 2,
+    GDN_ERR_ALIAS = 3,
+    GDN_ERR_WORKSPACE = 4,
+    GDN_ERR_CUDA = 5,
+    GDN_ERR_TIMEOUT = 6
+} gdn_status_t;
+
+typedef enum { GDN_GATE_SCALAR = 0, GDN_GATE_KDA = 1 } gdn_gate_t;
+
+typedef struct {
+    int64_t n_seq, T, H_k, H_v, S_k, S_v; /* sizes; H_v = r H_k, key head = h_v mod H_k */
+    int32_t gate;                         /* gdn_gate_t */
+    int32_t reserved0;                    /* must be 0 */
+    int64_t C;                            /* checkpoint interval; <= 0: ceil(sqrt(T)) */
+    float scale;                          /* output scale, usually 1/sqrt(S_k) */
+    float reserved1;                      /* must be 0 */
+    int64_t q_s[3], k_s[3], v_s[3], gy_s[3]; /* element strides of {seq, token, head} */
+} gdn_params_t;
+
+/* Effective checkpoint interval (C, or ceil(sqrt(T)) when C <= 0) and count ceil(T/C). */
+int64_t gdn_checkpoint_interval(const gdn_params_t* p);
+int64_t gdn_num_checkpoints(const gdn_params_t* p);
+/* Elements of the ckpt buffer: N * H_v * n_ck * S_v * S_k. */
+size_t gdn_ckpt_elems(const gdn_params_t* p);
+
+/* Forward (meTile "Recurrent delta attention"; PR #16 row form).  Reads q, k, v, g,
+ * beta, state0; writes y, state_T and ckpt (each must be non-NULL unless its size is
+ * zero).  state_T may not overlap state0 (llama.cpp PR #26: an in-place state update
+ * destroyed the initial state the backward needed). */
+gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k,
+                         const float* v, const float* g, const float* beta,
+                         const float* state0, float* y, float* state_T, float* ckpt,
+                         void* stream);
+
+/* Packed gradient buffer: total elements, and the element offsets of its six regions
+ * in the order dq, dk, dv, dg, dbeta, dstate (PR #16 body: "[dq|dk|dv|dg|dbeta|dstate]"). */
+size_t gdn_packed_grad_elems(const gdn_params_t* p);
+void gdn_packed_grad_offsets(const gdn_params_t* p, size_t off[6]);
+
+/* Device workspace the backward needs (bytes, 256-byte aligned start required). */
+size_t gdn_backward_workspace_bytes(const gdn_params_t* p);
+
+/* Backward (PR #16, GATED_DELTA_NET_BACK).  Reads q, k, v, g, beta, ckpt (from
+ * gdn_forward with the same params), gy and dstate_T (NULL = zero cotangent for the
+ * final state); writes every element of packed_grads.  The workspace is scratch owned
+ * by the caller for the duration of the enqueued work. */
+gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
+                          const float* v, const float* g, const float* beta,
+                          const float* ckpt, const float* gy, const float* dstate_T,
+                          float* packed_grads, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Static text of a status code, and the detail of the calling thread's last error. */
+const char* gdn_status_str(gdn_status_t s);
+const char* gdn_last_error(void);
+
+/* Kernels a forward / backward call with these params launches (0 when the call would
+ * fail validation).  Lets callers account for the work they enqueue. */
+int gdn_forward_launches(const gdn_params_t* p);
+int gdn_backward_launches(const gdn_params_t* p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

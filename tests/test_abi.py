@@ -1,0 +1,147 @@
+"""libgdn's C ABI on the host (no GPU needed): it loads, exports every symbol that
+include/gdn.h declares, sizes its buffers as documented, and rejects bad arguments
+with the documented status codes before touching the device."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_backward_gb300 import gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, ALIAS, WORKSPACE = 0, 1, 2, 3, 4
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = header_functions()
+    assert len(names) >= 12
+    lib = gdn.library()
+    for nm in names:
+        assert hasattr(lib, nm), nm
+    assert sorted(gdn.EXPORTS) == names
+
+
+def test_status_strings():
+    lib = gdn.library()
+    for code, name in gdn.STATUS.items():
+        assert lib.gdn_status_str(code).decode() == name
+
+
+def test_packed_layout_and_sizes():
+    for kda in (False, True):
+        p = gdn.make_params(3, 61, 4, 12, 64, kda, C=8)
+        off = gdn.packed_grad_offsets(p)
+        N, T, Hk, Hv, S = 3, 61, 4, 12, 64
+        sizes = [N * T * Hk * S, N * T * Hk * S, N * T * Hv * S,
+                 N * T * Hv * (S if kda else 1), N * T * Hv, N * Hv * S * S]
+        exp = [0]
+        for s in sizes[:-1]:
+            exp.append(exp[-1] + s)
+        assert off == exp
+        assert gdn.packed_grad_elems(p) == sum(sizes)
+        assert gdn.num_checkpoints(p) == 8                        # ceil(61 / 8)
+        assert gdn.library().gdn_ckpt_elems(ctypes.byref(p)) == N * Hv * 8 * S * S
+        assert gdn.backward_workspace_bytes(p) > 0
+        assert gdn.launches(p) == (1, 2)
+
+
+def test_default_checkpoint_interval_matches_pages():
+    gold = json.load(open(os.path.join(ROOT, "tests", "golden", "checkpoint_interval.json")))
+    for case in gold["cases"]:
+        p = gdn.make_params(1, case["T"], 1, 1, 32, False, C=None)
+        assert gdn.checkpoint_interval(p) == case["C"]
+    p = gdn.make_params(1, 2048, 16, 48, 128, False)
+    assert gdn.checkpoint_interval(p) == 46 and gdn.num_checkpoints(p) == 45
+
+
+def test_empty_batch_launches_nothing():
+    p = gdn.make_params(0, 16, 1, 1, 32, False)
+    assert gdn.launches(p) == (0, 0)
+    p = gdn.make_params(2, 0, 1, 1, 32, False)
+    assert gdn.launches(p) == (1, 1)
+    assert gdn.num_checkpoints(p) == 0
+
+
+# ---- argument validation: every case below fails before any device work ----
+
+BASE = 0x7f0000000000  # fake, 256-byte aligned device addresses
+
+
+def fake(i):
+    return ctypes.c_void_p(BASE + i * (1 << 32))
+
+
+def call_forward(p, ptrs=None):
+    ptrs = ptrs or [fake(i) for i in range(9)]
+    return gdn.library().gdn_forward(ctypes.byref(p), *ptrs, None)
+
+
+def call_backward(p, ws_bytes, ptrs=None):
+    ptrs = ptrs or [fake(i) for i in range(10)]
+    return gdn.library().gdn_backward(ctypes.byref(p), *ptrs[:10], ctypes.c_size_t(ws_bytes), None)
+
+
+def test_unsupported_head_sizes():
+    assert call_forward(gdn.make_params(1, 8, 1, 1, 48, False)) == UNSUPPORTED
+    assert call_forward(gdn.make_params(1, 8, 1, 1, 16, False)) == UNSUPPORTED
+    p = gdn.make_params(1, 8, 1, 1, 64, False)
+    p.S_v = 32
+    assert call_forward(p) == UNSUPPORTED
+    assert b"S_k" in gdn.library().gdn_last_error()
+
+
+def test_invalid_arguments():
+    assert call_forward(gdn.make_params(1, 8, 2, 3, 32, False)) == INVALID  # H_v % H_k
+    p = gdn.make_params(1, 8, 1, 1, 32, False)
+    p.q_s[1] = -32
+    assert call_forward(p) == INVALID                                       # negative stride
+    p = gdn.make_params(1, 8, 1, 1, 32, False)
+    p.gate = 7
+    assert call_forward(p) == INVALID
+    p = gdn.make_params(1, 8, 1, 1, 32, False)
+    p.reserved0 = 1
+    assert call_forward(p) == INVALID
+    p = gdn.make_params(-1, 8, 1, 1, 32, False)
+    assert call_forward(p) == INVALID
+    assert gdn.library().gdn_forward(None, *[fake(i) for i in range(9)], None) == INVALID
+    p = gdn.make_params(1, 8, 1, 1, 32, False)
+    ptrs = [fake(i) for i in range(9)]
+    ptrs[0] = ctypes.c_void_p(BASE + 2)                                     # q not 4-byte aligned
+    assert call_forward(p, ptrs) == INVALID
+    ptrs = [fake(i) for i in range(9)]
+    ptrs[7] = ctypes.c_void_p(BASE + 7 * (1 << 32) + 4)                     # state_T not 16-aligned
+    assert call_forward(p, ptrs) == INVALID
+    ptrs = [fake(i) for i in range(9)]
+    ptrs[0] = None                                                          # q missing
+    assert call_forward(p, ptrs) == INVALID
+
+
+def test_alias_is_rejected():
+    p = gdn.make_params(1, 8, 1, 1, 32, False)
+    ptrs = [fake(i) for i in range(9)]
+    ptrs[7] = ptrs[5]                                                       # state_T == state0
+    assert call_forward(p, ptrs) == ALIAS
+    ptrs = [fake(i) for i in range(9)]
+    ptrs[6] = ctypes.c_void_p(BASE + 2 * (1 << 32) + 64)                    # y inside v
+    assert call_forward(p, ptrs) == ALIAS
+    ws = gdn.backward_workspace_bytes(p)
+    ptrs = [fake(i) for i in range(10)]
+    ptrs[8] = ptrs[6]                                                       # packed over gy
+    assert call_backward(p, ws, ptrs) == ALIAS
+
+
+def test_workspace_too_small():
+    p = gdn.make_params(1, 64, 1, 3, 64, True)
+    ws = gdn.backward_workspace_bytes(p)
+    assert call_backward(p, ws - 256) == WORKSPACE
+    ptrs = [fake(i) for i in range(10)]
+    ptrs[9] = ctypes.c_void_p(BASE + 9 * (1 << 32) + 16)                    # not 256-aligned
+    assert call_backward(p, ws, ptrs) == WORKSPACE

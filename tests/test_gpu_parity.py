@@ -1,0 +1,159 @@
+"""libgdn (CUDA, sm_103a) against the float64 oracle, element by element.
+
+Tolerance (fp32 kernels vs float64 oracle): max |err| <= 2e-4 (1 + |ref|) for T <= 2048
+and <= 1e-3 (1 + |ref|) beyond, on every output: y, state_T, the checkpoints and every
+region of the packed gradient.  Small and mid-size problems are checked in full (they
+span several tiles, several sub-segments and a ragged last segment); the full-size
+workloads are checked on sampled (sequence, key-head group) units, each a complete
+independent problem the oracle solves on its own.
+"""
+import numpy as np
+import pytest
+
+import gpu_helpers as H
+from gated_delta_rule_backward_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+def full_check(prob, C=None):
+    gpu, _ = H.run_gpu(prob, C=C)
+    ref = H.run_oracle(H.problem_dict(prob), prob.scale, C if C is not None else prob.C)
+    return H.compare_all(gpu, ref, H.tolerance(prob.T))
+
+
+def test_tiny_d32_T16_scalar():
+    prob = synth.workload("tiny_d32_T16")
+    full_check(prob)
+
+
+def test_tiny_d32_T16_scalar_with_final_state_cotangent():
+    prob = synth.workload("tiny_d32_T16", dstate_T=True)
+    full_check(prob)
+
+
+def test_kda_d64_T61_partial_last_segment():
+    prob = synth.workload("kda_d64_T61")
+    full_check(prob)
+
+
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_mid_size_full(kda, d):
+    # 2 seqs, H_k=2 -> H_v=6 broadcast, packed qkv views, T=300 with C=17 (ragged tail)
+    prob = synth.make_problem(2, 300, 2, 6, d, kda=kda, seed=31 + d, C=17, packed=True,
+                              dstate_T=True)
+    full_check(prob)
+
+
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+@pytest.mark.parametrize("d", [32, 64])
+def test_sweep_T512(kda, d):
+    prob = synth.make_problem(1, 512, 16, 48, d, kda=kda, seed=2100 + d + kda, packed=True)
+    full_check(prob)
+
+
+def test_bcast_d128_T2048_sampled():
+    prob = synth.workload("bcast_d128_T2048")
+    gpu, _ = H.run_gpu(prob)
+    for n, hk in ((0, 0), (3, 15), (1, 7)):
+        H.compare_group(gpu, prob, n, hk, prob.C)
+
+
+def test_bench_d128_T4096_sampled():
+    prob = synth.workload("bench_d128_T4096")
+    gpu, _ = H.run_gpu(prob)
+    for n, hk in ((0, 0), (0, 11)):
+        H.compare_group(gpu, prob, n, hk, prob.C)
+
+
+def test_kda_d128_T16384_sampled():
+    prob = synth.workload("kda_d128_T16384")
+    gpu, _ = H.run_gpu(prob)
+    for n, hk in ((0, 5),):
+        H.compare_group(gpu, prob, n, hk, prob.C)
+
+
+def test_run_to_run_bit_identical():
+    prob = synth.make_problem(2, 300, 2, 6, 128, kda=True, seed=41, C=17, packed=True,
+                              dstate_T=True)
+    dev = H.upload(prob)
+    a, pa = H.run_gpu(prob, dev=dev)
+    b, pb = H.run_gpu(prob, dev=dev)
+    assert torch.equal(pa, pb)
+    for k in ("y", "state_T", "ckpt"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+def test_checkpoint_interval_invariance(kda):
+    """States are recomputed bit-exactly, so gradients do not depend on C."""
+    prob = synth.make_problem(2, 300, 2, 6, 64, kda=kda, seed=42, packed=True, dstate_T=True)
+    dev = H.upload(prob)
+    base, pbase = H.run_gpu(prob, C=17, dev=dev)
+    for C in (1, 5, 64, 300, 1000):
+        got, pk = H.run_gpu(prob, C=C, dev=dev)
+        assert torch.equal(pk, pbase), C
+        assert np.array_equal(got["y"], base["y"]) and np.array_equal(got["state_T"], base["state_T"])
+
+
+def test_strided_views_equal_contiguous_copies():
+    prob = synth.make_problem(2, 100, 2, 6, 64, kda=False, seed=43, C=9, packed=True,
+                              dstate_T=True)
+    dev = H.upload(prob)
+    a, pa = H.run_gpu(prob, dev=dev)
+    dev2 = dict(dev)
+    for k in ("q", "k", "v"):
+        dev2[k] = dev[k].contiguous()
+    gy_wide = torch.zeros((2, 100, 6, 80), device="cuda")
+    gy_wide[..., :64] = dev["gy"]
+    dev2["gy"] = gy_wide[..., :64]                 # a strided gy view as well
+    b, pb = H.run_gpu(prob, dev=dev2)
+    assert torch.equal(pa, pb)
+    assert np.array_equal(a["y"], b["y"])
+
+
+def test_broadcast_equals_explicit_replication():
+    prob = synth.make_problem(1, 120, 2, 6, 64, kda=True, seed=44, C=11, dstate_T=True)
+    dev = H.upload(prob)
+    a, _ = H.run_gpu(prob, dev=dev)
+    hk = torch.arange(6, device="cuda") % 2
+    rep = dict(dev)
+    rep["q"] = dev["q"][:, :, hk].contiguous()
+    rep["k"] = dev["k"][:, :, hk].contiguous()
+    b, _ = H.run_gpu(prob, dev=rep)
+    for k in ("y", "state_T", "ckpt", "dv", "dg", "dbeta", "dstate0"):
+        assert np.array_equal(a[k], b[k]), k
+    for k in ("dq", "dk"):
+        for h in range(2):
+            acc = np.zeros_like(b[k][:, :, 0])
+            for hv in range(h, 6, 2):                  # ascending value heads, fp32 adds
+                acc = (acc + b[k][:, :, hv]).astype(np.float32)
+            assert np.array_equal(acc, a[k][:, :, h]), (k, h)
+
+
+def test_single_token():
+    prob = synth.make_problem(1, 1, 1, 2, 32, kda=True, seed=45, dstate_T=True)
+    full_check(prob)
+
+
+def test_empty_sequence():
+    prob = synth.make_problem(2, 0, 1, 2, 32, kda=False, seed=46, dstate_T=True)
+    gpu, _ = H.run_gpu(prob)
+    assert np.array_equal(gpu["state_T"], prob.state0)
+    assert np.array_equal(gpu["dstate0"], prob.dstate_T)
+    assert gpu["y"].size == 0 and gpu["ckpt"].size == 0
+
+
+def test_empty_batch_is_a_no_op():
+    from gated_delta_rule_backward_gb300 import gdn
+    prob = synth.make_problem(1, 4, 1, 1, 32, seed=47)
+    dev = H.upload(prob)
+    p = gdn.make_params(0, 4, 1, 1, 32, False)
+    e = torch.empty(0, device="cuda")
+    gdn.gdn_forward(p, e, e, e, e, e, e, e, e, e)
+    gdn.gdn_backward(p, e, e, e, e, e, e, e, None, e, None)
+    torch.cuda.synchronize()
