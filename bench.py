@@ -1,0 +1,386 @@
+"""Throughput of the gated delta rule forward + backward (libgdn, sm_103a).
+
+One step = gdn_forward + gdn_backward over one batch: 1 sequence, H_k = 16 key heads
+broadcast to H_v = 48 value heads, head size 128, T = 4096 tokens, scalar gate, default
+checkpoint interval C = ceil(sqrt(T)) = 64, q/k/v as row views of a packed qkv buffer.
+Metric: head-tokens/s = N * H_v * T / step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  --impl reference times the float64 CPU oracle (the only other
+implementation of this path) on the host cores, on a bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN fwd+bwd head-tokens/s at d=128,H_v=48,T=4096; % of FP32/HBM roofline"
+UNIT = "head-tokens/s"
+WORKLOAD = "bench_d128_T4096"
+
+# FP32 CUDA-core peak of GB300: 152 SMs x 128 FP32 lanes x 2 flop (FMA) x 2.070 GHz.
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+# Algorithmic flops per head-token (FMA = 2): forward 7 d^2; backward call = one
+# recompute 5 d^2 + reverse step 15 d^2.
+FWD_FLOPS = lambda d: 7 * d * d
+BWD_FLOPS = lambda d: 20 * d * d
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def _dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- traffic
+def _kernel_sha():
+    h = hashlib.sha256()
+    for f in ("gdn_bwd.cu", "gdn_device.cuh", "gdn_internal.h", "gdn_api.cu"):
+        h.update(open(os.path.join(ROOT, "gated_delta_rule_backward_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _recorded_traffic():
+    """DRAM bytes per backward launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "gdn_bwd_kernel_bench_d128_T4096.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_sources_sha") != _kernel_sha():
+        return None
+    try:
+        return float(vals["dram_bytes_per_backward_call"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------- oracle
+def _oracle_sample(prob, groups, lib=None):
+    """Run the oracle forward+backward on `groups` (n, hk) key-head groups of prob.
+    Returns (head_tokens, seconds)."""
+    import numpy as np
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import gpu_helpers as H
+    qs, ks, vs, gs, bs, s0, gys = [], [], [], [], [], [], []
+    for n, hk in groups:
+        sub, heads = H.group_problem(prob, n, hk)
+        qs.append(np.repeat(sub["q"], len(heads), axis=2))  # one unit per value head
+        ks.append(np.repeat(sub["k"], len(heads), axis=2))
+        vs.append(sub["v"]); gs.append(sub["g"]); bs.append(sub["beta"])
+        s0.append(sub["state0"]); gys.append(sub["gy"])
+    cat = lambda xs, ax: np.ascontiguousarray(np.concatenate(xs, axis=ax), dtype=np.float64)
+    q, k, v, g, b = cat(qs, 2), cat(ks, 2), cat(vs, 2), cat(gs, 2), cat(bs, 2)
+    st0, gy = cat(s0, 1), cat(gys, 2)
+    t0 = time.perf_counter()
+    _, _, ck = oracle.forward(q, k, v, g, b, st0, prob.scale, C=prob.C, lib=lib)
+    oracle.backward(q, k, v, g, b, st0, gy, None, prob.scale, C=prob.C, ckpt=ck, lib=lib)
+    dt = time.perf_counter() - t0
+    return q.shape[2] * prob.T, dt
+
+
+def _sample_groups(prob, cores):
+    r = prob.H_v // prob.H_k
+    n_groups = max(1, min(prob.H_k, cores // r))
+    return [(0, hk) for hk in range(n_groups)]
+
+
+def cpu_baseline(prob):
+    import oracle
+    lib = oracle.load()
+    cores = oracle.max_threads(lib)
+    groups = _sample_groups(prob, cores)
+    ht, dt = _oracle_sample(prob, groups, lib)
+    r = prob.H_v // prob.H_k
+    return {"value": ht / dt, "unit": UNIT, "cores": min(cores, len(groups) * r),
+            "kind": "oracle",
+            "sample": f"{len(groups) * r} of {prob.N * prob.H_v} value heads (sequence 0, key "
+                      f"heads 0..{len(groups) - 1}) over all {prob.T} tokens, forward + "
+                      f"checkpointed backward, float64, {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = _dist_env()
+    if rank != 0:
+        return
+    from gated_delta_rule_backward_gb300 import synth
+    import oracle
+    prob = synth.workload(args.workload)
+    lib = oracle.load()
+    cores = oracle.max_threads(lib)
+    groups = _sample_groups(prob, cores)
+    for _ in range(args.warmup):
+        _oracle_sample(prob, groups[:1], lib)
+    tot_ht, tot_s = 0, 0.0
+    for _ in range(args.steps):
+        ht, dt = _oracle_sample(prob, groups, lib)
+        tot_ht += ht
+        tot_s += dt
+    value = tot_ht / tot_s
+    r = prob.H_v // prob.H_k
+    sample = (f"per step {len(groups) * r} of {prob.N * prob.H_v} value heads (sequence 0) over "
+              f"all {prob.T} tokens, forward + checkpointed backward, float64 C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "N": prob.N, "T": prob.T, "H_k": prob.H_k,
+                   "H_v": prob.H_v, "d": prob.d, "gate": "kda" if prob.kda else "scalar",
+                   "C": prob.C or math.isqrt(prob.T - 1) + 1, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, len(groups) * r),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- ours
+def run_ours(args):
+    import torch
+    from gated_delta_rule_backward_gb300 import gdn, synth
+
+    rank, world, local = _dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    prob = synth.workload(args.workload)
+    N, T, H_k, H_v, d = prob.N, prob.T, prob.H_k, prob.H_v, prob.d
+    qkv = torch.from_numpy(prob.qkv).to(dev)
+    q = qkv[:, :, : H_k * d].view(N, T, H_k, d)
+    k = qkv[:, :, H_k * d: 2 * H_k * d].view(N, T, H_k, d)
+    v = qkv[:, :, 2 * H_k * d:].view(N, T, H_v, d)
+    g = torch.from_numpy(prob.g).to(dev)
+    beta = torch.from_numpy(prob.beta).to(dev)
+    state0 = torch.from_numpy(prob.state0).to(dev)
+    gy = torch.from_numpy(prob.gy).to(dev)
+    p = gdn.params_for(q, k, v, g, gy=gy, C=prob.C, scale=prob.scale)
+    C = gdn.checkpoint_interval(p)
+    y = torch.empty((N, T, H_v, d), device=dev)
+    sT = torch.empty((N, H_v, d, d), device=dev)
+    ck = torch.empty((N, H_v, gdn.num_checkpoints(p), d, d), device=dev)
+    packed = torch.empty(gdn.packed_grad_elems(p), device=dev)
+    ws = torch.empty(max(gdn.backward_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)  # 256 MiB > 129 MB of L2
+    stream = torch.cuda.current_stream(dev)
+    n_fwd, n_bwd = gdn.launches(p)
+
+    def step():
+        gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, stream)
+        gdn.gdn_backward(p, q, k, v, g, beta, ck, gy, None, packed, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps (not inside the events)
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, stream)
+        e1.record(stream)
+        gdn.gdn_backward(p, q, k, v, g, beta, ck, gy, None, packed, ws, stream)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) / args.steps
+    if dist:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    head_tokens = N * H_v * T
+    value = world * head_tokens / (step_ms * 1e-3)
+
+    # end to end through the public API: pinned host inputs in, results back out
+    e2e = None
+    if not args.no_e2e:
+        host = {nm: torch.from_numpy(getattr(prob, nm)).pin_memory()
+                for nm in ("g", "beta", "state0", "gy")}
+        host["qkv"] = torch.from_numpy(prob.qkv).pin_memory()
+        out_h = {"y": torch.empty(y.shape).pin_memory(), "sT": torch.empty(sT.shape).pin_memory(),
+                 "packed": torch.empty(packed.shape).pin_memory()}
+        d_in = {nm: torch.empty(t.shape, device=dev) for nm, t in host.items()}
+        h2d = sum(t.numel() * 4 for t in host.values())
+        d2h = sum(t.numel() * 4 for t in out_h.values())
+        qv = d_in["qkv"]
+        q2 = qv[:, :, : H_k * d].view(N, T, H_k, d)
+        k2 = qv[:, :, H_k * d: 2 * H_k * d].view(N, T, H_k, d)
+        v2 = qv[:, :, 2 * H_k * d:].view(N, T, H_v, d)
+
+        def e2e_step():
+            for nm, t in host.items():
+                d_in[nm].copy_(t, non_blocking=True)
+            gdn.gdn_forward(p, q2, k2, v2, d_in["g"], d_in["beta"], d_in["state0"], y, sT, ck, stream)
+            gdn.gdn_backward(p, q2, k2, v2, d_in["g"], d_in["beta"], ck, d_in["gy"], None, packed,
+                             ws, stream)
+            out_h["y"].copy_(y, non_blocking=True)
+            out_h["sT"].copy_(sT, non_blocking=True)
+            out_h["packed"].copy_(packed, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        k_e2e = max(3, min(args.steps, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / k_e2e
+        e2e = {"value": world * head_tokens / (e2e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    bwd_avg = sum(bwd_ms) / len(bwd_ms)
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    bwd_flops = BWD_FLOPS(d) * head_tokens
+    achieved = bwd_flops / (bwd_avg * 1e-3) / 1e12
+    path_tflops = (FWD_FLOPS(d) + BWD_FLOPS(d)) * head_tokens / (step_ms * 1e-3) / 1e12
+    traffic = _recorded_traffic()
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(prob)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "N": N, "T": T, "H_k": H_k, "H_v": H_v, "d": d,
+                   "gate": "kda" if prob.kda else "scalar", "C": C, "qkv": "packed row views",
+                   "l2": "flushed between timed steps (256 MiB write outside the events)",
+                   "per_rank": "each rank runs the whole workload on its own GPU"},
+        "roofline": {"bound": "alu", "kernel": "gdn_backward call (gdn_bwd_kernel + gdn_reduce_kernel)",
+                     "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                     "frac": achieved / FP32_PEAK_TFLOPS, "traffic": traffic,
+                     "flops_per_head_token": BWD_FLOPS(d), "launch_ms": bwd_avg,
+                     "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.070 GHz (nominal)"},
+        "roofline_path": {"achieved": path_tflops, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                          "frac": path_tflops / FP32_PEAK_TFLOPS,
+                          "flops_per_head_token": FWD_FLOPS(d) + BWD_FLOPS(d),
+                          "fwd_ms": fwd_avg, "bwd_ms": bwd_avg},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": (n_fwd + n_bwd) * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -102,6 +102,9 @@ def make_params(N, T, H_k, H_v, S, kda, C=None, scale=None, q_s=None, k_s=None, 
 
 def strides3(t):
     """Element strides of a [N,T,H,S] tensor view (its last dim must be contiguous)."""
+    if t.numel() == 0:  # empty views carry no meaningful strides
+        N, T, H, S = t.shape
+        return (T * H * S, H * S, S)
     if t.stride(-1) != 1:
         raise ValueError("the head dimension must be contiguous")
     return tuple(int(s) for s in t.stride()[:3])
