@@ -135,7 +135,7 @@ def _recorded_traffic():
     if vals.get("kernel_sources_sha") != _kernel_sha():
         return None
     try:
-        return float(vals["dram_bytes_per_backward_call"])
+        return float(vals["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
 
@@ -222,6 +222,14 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- ours
+def max_over_ranks(x, dist, device):
+    """The slowest rank's value (whole-job time is the max over ranks)."""
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args):
     import torch
     from gated_delta_rule_backward_gb300 import gdn, synth
@@ -263,8 +271,12 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # per step: [step start, fwd end, bwd start, bwd recurrence end, bwd reduction end]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for es in ev:
+        for e in es:
+            e.record(stream)  # materialise the event handles
+    torch.cuda.synchronize()
     clocks = ClockSampler(local)
     if dist:
         dist.barrier()
@@ -273,23 +285,24 @@ def run_ours(args):
     time.sleep(0.3)
     for i in range(args.steps):
         flush.zero_()  # L2 flush between timed steps (not inside the events)
-        e0, e1, e2 = ev[i]
+        e0, e1, b0, b1, b2 = ev[i]
         e0.record(stream)
         gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, stream)
         e1.record(stream)
+        gdn.set_backward_timing_events((b0, b1, b2))
         gdn.gdn_backward(p, q, k, v, g, beta, ck, gy, None, packed, ws, stream)
-        e2.record(stream)
+    gdn.set_backward_timing_events(None)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
-    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
-    step_ms = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) / args.steps
+    fwd_ms = [es[0].elapsed_time(es[1]) for es in ev]
+    bwdk_ms = [es[2].elapsed_time(es[3]) for es in ev]
+    red_ms = [es[3].elapsed_time(es[4]) for es in ev]
+    bwd_ms = [es[1].elapsed_time(es[4]) for es in ev]
+    step_ms = sum(es[0].elapsed_time(es[4]) for es in ev) / args.steps
     if dist:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+        step_ms = max_over_ranks(step_ms, dist, dev)
     head_tokens = N * H_v * T
     value = world * head_tokens / (step_ms * 1e-3)
 
@@ -339,9 +352,10 @@ def run_ours(args):
         return
 
     bwd_avg = sum(bwd_ms) / len(bwd_ms)
+    bwdk_avg = sum(bwdk_ms) / len(bwdk_ms)
+    red_avg = sum(red_ms) / len(red_ms)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    bwd_flops = BWD_FLOPS(d) * head_tokens
-    achieved = bwd_flops / (bwd_avg * 1e-3) / 1e12
+    achieved = BWD_FLOPS(d) * head_tokens / (bwdk_avg * 1e-3) / 1e12
     path_tflops = (FWD_FLOPS(d) + BWD_FLOPS(d)) * head_tokens / (step_ms * 1e-3) / 1e12
     traffic = _recorded_traffic()
     cpu = None
@@ -355,15 +369,16 @@ def run_ours(args):
                    "gate": "kda" if prob.kda else "scalar", "C": C, "qkv": "packed row views",
                    "l2": "flushed between timed steps (256 MiB write outside the events)",
                    "per_rank": "each rank runs the whole workload on its own GPU"},
-        "roofline": {"bound": "alu", "kernel": "gdn_backward call (gdn_bwd_kernel + gdn_reduce_kernel)",
+        "roofline": {"bound": "alu", "kernel": "gdn_bwd_kernel",
                      "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                      "frac": achieved / FP32_PEAK_TFLOPS, "traffic": traffic,
-                     "flops_per_head_token": BWD_FLOPS(d), "launch_ms": bwd_avg,
-                     "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.070 GHz (nominal)"},
+                     "flops_per_head_token": BWD_FLOPS(d), "launch_ms": bwdk_avg,
+                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.070 GHz"},
         "roofline_path": {"achieved": path_tflops, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                           "frac": path_tflops / FP32_PEAK_TFLOPS,
                           "flops_per_head_token": FWD_FLOPS(d) + BWD_FLOPS(d),
-                          "fwd_ms": fwd_avg, "bwd_ms": bwd_avg},
+                          "fwd_ms": fwd_avg, "bwd_ms": bwd_avg, "bwd_kernel_ms": bwdk_avg,
+                          "reduce_kernel_ms": red_avg},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": (n_fwd + n_bwd) * args.steps,

@@ -16,6 +16,7 @@
 namespace {
 
 thread_local std::string g_last_error;
+thread_local void* const* g_bwd_events = nullptr;
 
 gdn_status_t fail(gdn_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 gdn_status_t fail(gdn_status_t s, const char* fmt, ...)
@@ -239,6 +240,8 @@ const char* gdn_status_str(gdn_status_t s)
 
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
+void gdn_set_backward_timing_events(void* const* events) { g_bwd_events = events; }
+
 gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, const float* v,
                          const float* g, const float* beta, const float* state0, float* y,
                          float* state_T, float* ckpt, void* stream)
@@ -349,15 +352,24 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
     a.vec_q = vec_ok(q, p->q_s); a.vec_k = vec_ok(k, p->k_s); a.vec_v = vec_ok(v, p->v_s);
     a.vec_gy = vec_ok(gy, p->gy_s); a.vec_g = aligned(g, 16);
     a.vec_ds0 = aligned(packed + off[5], 16);
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (g_bwd_events) cudaEventRecord((cudaEvent_t)g_bwd_events[0], cs);
     st = cuda_status(gdn::launch_backward(a, pl.D, pl.RT, pl.W, pl.kda, stream), "backward launch");
-    if (st != GDN_OK || !tok) return st;
+    if (g_bwd_events) cudaEventRecord((cudaEvent_t)g_bwd_events[1], cs);
+    if (st != GDN_OK) return st;
+    if (!tok) {
+        if (g_bwd_events) cudaEventRecord((cudaEvent_t)g_bwd_events[2], cs);
+        return st;
+    }
 
     gdn::ReduceArgs r{};
     r.ws_col = a.ws_col; r.ws_sc = a.ws_sc;
     r.dq = packed + off[0]; r.dk = packed + off[1]; r.dg = packed + off[3]; r.dbeta = packed + off[4];
     r.N = (int)N; r.T = (int)T; r.H_k = (int)Hk; r.H_v = (int)Hv; r.D = (int)D; r.P = pl.P;
     r.NQ = pl.kda ? 3 : 2; r.kda = pl.kda;
-    return cuda_status(gdn::launch_reduce(r, stream), "reduce launch");
+    st = cuda_status(gdn::launch_reduce(r, stream), "reduce launch");
+    if (g_bwd_events) cudaEventRecord((cudaEvent_t)g_bwd_events[2], cs);
+    return st;
 }
 
 }  // extern "C"

@@ -30,7 +30,7 @@ GATE_SCALAR, GATE_KDA = 0, 1
 EXPORTS = ["gdn_checkpoint_interval", "gdn_num_checkpoints", "gdn_ckpt_elems", "gdn_forward",
            "gdn_packed_grad_elems", "gdn_packed_grad_offsets", "gdn_backward_workspace_bytes",
            "gdn_backward", "gdn_status_str", "gdn_last_error", "gdn_forward_launches",
-           "gdn_backward_launches"]
+           "gdn_backward_launches", "gdn_set_backward_timing_events"]
 
 
 class GdnParams(ctypes.Structure):
@@ -71,6 +71,8 @@ _lib.gdn_forward_launches.argtypes = [_P]
 _lib.gdn_forward_launches.restype = ctypes.c_int
 _lib.gdn_backward_launches.argtypes = [_P]
 _lib.gdn_backward_launches.restype = ctypes.c_int
+_lib.gdn_set_backward_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+_lib.gdn_set_backward_timing_events.restype = None
 
 
 class GdnError(RuntimeError):
@@ -155,6 +157,21 @@ def launches(p: GdnParams):
     """(forward kernels, backward kernels) one call of each enqueues."""
     return (int(_lib.gdn_forward_launches(ctypes.byref(p))),
             int(_lib.gdn_backward_launches(ctypes.byref(p))))
+
+
+_EVENTS = None
+
+
+def set_backward_timing_events(events):
+    """Three recorded torch.cuda.Event(enable_timing=True) objects, or None.  gdn_backward
+    then records them around its recurrence and reduction kernels."""
+    global _EVENTS
+    if events is None:
+        _EVENTS = None
+        _lib.gdn_set_backward_timing_events(None)
+        return
+    _EVENTS = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _lib.gdn_set_backward_timing_events(_EVENTS)
 
 
 def gdn_forward(p: GdnParams, q, k, v, g, beta, state0, y, state_T, ckpt, stream=None):

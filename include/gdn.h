@@ -132,6 +132,13 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
 const char* gdn_status_str(gdn_status_t s);
 const char* gdn_last_error(void);
 
+/* Optional per-kernel timing for the calling thread: when `events` is non-NULL,
+ * gdn_backward records events[0] before its first kernel, events[1] after the
+ * recurrence kernel and events[2] after the reduction kernel, all on the call's stream;
+ * the events are cudaEvent_t handles the caller created (and owns).  NULL turns it off.
+ * Not part of the operation: it lets a caller time the two kernels separately. */
+void gdn_set_backward_timing_events(void* const* events);
+
 /* Kernels a forward / backward call with these params launches (0 when the call would
  * fail validation).  Lets callers account for the work they enqueue. */
 int gdn_forward_launches(const gdn_params_t* p);
