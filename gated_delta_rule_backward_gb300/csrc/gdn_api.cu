@@ -168,6 +168,8 @@ gdn_status_t cuda_status(int err, const char* what)
 
 }  // namespace
 
+void gdn::set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
 extern "C" {
 
 int64_t gdn_checkpoint_interval(const gdn_params_t* p)

@@ -123,4 +123,7 @@ int launch_forward(const FwdArgs& a, int D, int RT, int W, bool kda, void* strea
 int launch_backward(const BwdArgs& a, int D, int RT, int W, bool kda, void* stream);
 int launch_reduce(const ReduceArgs& a, void* stream);
 
+// Sets the text gdn_last_error() returns on the calling thread.
+void set_last_error(const char* msg);
+
 }  // namespace gdn

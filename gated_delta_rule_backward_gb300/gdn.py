@@ -30,7 +30,8 @@ GATE_SCALAR, GATE_KDA = 0, 1
 EXPORTS = ["gdn_checkpoint_interval", "gdn_num_checkpoints", "gdn_ckpt_elems", "gdn_forward",
            "gdn_packed_grad_elems", "gdn_packed_grad_offsets", "gdn_backward_workspace_bytes",
            "gdn_backward", "gdn_status_str", "gdn_last_error", "gdn_forward_launches",
-           "gdn_backward_launches", "gdn_set_backward_timing_events"]
+           "gdn_backward_launches", "gdn_set_backward_timing_events",
+           "gdn_backward_noalloc"]
 
 
 class GdnParams(ctypes.Structure):
@@ -71,6 +72,8 @@ _lib.gdn_forward_launches.argtypes = [_P]
 _lib.gdn_forward_launches.restype = ctypes.c_int
 _lib.gdn_backward_launches.argtypes = [_P]
 _lib.gdn_backward_launches.restype = ctypes.c_int
+_lib.gdn_backward_noalloc.argtypes = [_P] + [_vp] * 10
+_lib.gdn_backward_noalloc.restype = ctypes.c_int
 _lib.gdn_set_backward_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
 _lib.gdn_set_backward_timing_events.restype = None
 
@@ -192,6 +195,16 @@ def gdn_backward(p: GdnParams, q, k, v, g, beta, ckpt, gy, dstate_T, packed, wor
                            _stream_handle(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_backward")
+
+
+def gdn_backward_noalloc(p: GdnParams, q, k, v, g, beta, ckpt, gy, dstate_T, packed,
+                         stream=None):
+    """gdn_backward with the library's fixed device scratch instead of a workspace."""
+    st = _lib.gdn_backward_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                   _ptr(beta), _ptr(ckpt), _ptr(gy), _ptr(dstate_T),
+                                   _ptr(packed), _stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_backward_noalloc")
 
 
 def forward(q, k, v, g, beta, state0, C=None, scale=None, stream=None):

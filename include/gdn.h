@@ -128,6 +128,24 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
                           float* packed_grads, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/* Backward without a caller workspace.  The paper has no counterpart: this entry point
+ * exists for callers that cannot allocate device memory when they run the backward (a
+ * host framework that has already handed out its whole memory budget, a plugin host
+ * that gives extensions no device allocator, a call site that must not trigger an
+ * allocator).  Its scratch is one fixed 64 MiB array in device memory that every GPU
+ * which loads libgdn holds until the process exits; it allocates nothing itself.
+ * Arguments and results are those of gdn_backward, less the workspace.  Problems whose
+ * gdn_backward_workspace_bytes() exceeds 64 MiB return GDN_ERR_WORKSPACE (text in
+ * gdn_last_error()) before any work is enqueued.  The first call on a device, with that
+ * device current, looks up the array's address; make it before any stream capture.  All
+ * calls on a device share the array (no call needs it zeroed: every scratch element a
+ * call reads, it wrote first), so calls whose work overlaps on the GPU race on it:
+ * order them on one stream or with events. */
+gdn_status_t gdn_backward_noalloc(const gdn_params_t* p, const float* q, const float* k,
+                                  const float* v, const float* g, const float* beta,
+                                  const float* ckpt, const float* gy, const float* dstate_T,
+                                  float* packed_grads, void* stream);
+
 /* Static text of a status code, and the detail of the calling thread's last error. */
 const char* gdn_status_str(gdn_status_t s);
 const char* gdn_last_error(void);
