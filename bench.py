@@ -32,10 +32,32 @@ WORKLOAD = "bench_d128_T4096"
 
 # FP32 CUDA-core peak of GB300: 152 SMs x 128 FP32 lanes x 2 flop (FMA) x 2.070 GHz.
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
-# Algorithmic flops per head-token (FMA = 2): forward 7 d^2; backward call = one
+# Algorithmic flops per head-token of the path (FMA = 2): forward 7 d^2; backward = one
 # recompute 5 d^2 + reverse step 15 d^2.
 FWD_FLOPS = lambda d: 7 * d * d
 BWD_FLOPS = lambda d: 20 * d * d
+BC = 32  # chunk length of the chunked (scalar-gate) kernels
+
+
+def chunk_kernel_flops(N, T, H_v, d, C, which):
+    """Flops (FMA = 2) each chunked kernel executes per launch: the dense products of the
+    WY form per (sequence, value head, 32-token chunk); see the design doc."""
+    cps = -(-C // BC)
+    n_ck = -(-T // C)
+    last = T - (n_ck - 1) * C
+    n_chunks = (n_ck - 1) * cps + -(-last // BC)
+    ch = N * H_v * n_chunks
+    recomputed = N * H_v * (n_chunks - n_ck)
+    b2d, bd2 = BC * BC * d, BC * d * d
+    fma = {
+        "prep_fwd": ch * 4 * b2d,
+        "state_fwd": ch * (3 * bd2 + b2d),
+        "prep_bwd": ch * (4 if cps > 1 else 2) * b2d,
+        "recompute": recomputed * 2 * bd2,
+        "dstate": ch * (3 * bd2 + 2 * b2d),
+        "grad": ch * (4 * bd2 + 8 * b2d + 2 * BC ** 3),
+    }[which]
+    return 2.0 * fma
 
 
 def _args():
@@ -116,15 +138,16 @@ class ClockSampler:
 # --------------------------------------------------------------------------- traffic
 def _kernel_sha():
     h = hashlib.sha256()
-    for f in ("gdn_bwd.cu", "gdn_device.cuh", "gdn_internal.h", "gdn_api.cu"):
+    for f in ("gdn_chunk.cu", "gdn_gemm.cuh", "gdn_bwd.cu", "gdn_fwd.cu", "gdn_device.cuh",
+              "gdn_internal.h", "gdn_api.cu"):
         h.update(open(os.path.join(ROOT, "gated_delta_rule_backward_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def _recorded_traffic():
-    """DRAM bytes per backward launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "gdn_bwd_kernel_bench_d128_T4096.md")
+def _recorded_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel.split('(')[0]}_bench_d128_T4096.md")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -259,22 +282,35 @@ def run_ours(args):
     ck = torch.empty((N, H_v, gdn.num_checkpoints(p), d, d), device=dev)
     packed = torch.empty(gdn.packed_grad_elems(p), device=dev)
     ws = torch.empty(max(gdn.backward_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
+    fws_n = gdn.forward_workspace_bytes(p)
+    fws = torch.empty(fws_n, dtype=torch.uint8, device=dev) if fws_n else None
     flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)  # 256 MiB > 129 MB of L2
     stream = torch.cuda.current_stream(dev)
     n_fwd, n_bwd = gdn.launches(p)
+    chunked = not prob.kda
+    fwd_names = ["gdn_chunk_prep_kernel", "gdn_chunk_state_kernel"] if chunked else ["gdn_fwd_kernel"]
+    bwd_names = (["gdn_chunk_prep_kernel", "gdn_chunk_state_kernel(recompute)",
+                  "gdn_chunk_dstate_kernel", "gdn_chunk_grad_kernel"] if n_bwd == 4 else
+                 ["gdn_chunk_prep_kernel", "gdn_chunk_dstate_kernel", "gdn_chunk_grad_kernel"]
+                 if chunked else ["gdn_bwd_kernel", "gdn_reduce_kernel"])
+    kinds = (["prep_fwd", "state_fwd"] + (["prep_bwd", "recompute", "dstate", "grad"]
+                                          if n_bwd == 4 else ["prep_bwd", "dstate", "grad"])
+             if chunked else None)
 
     def step():
-        gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, stream)
+        gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, fws, stream)
         gdn.gdn_backward(p, q, k, v, g, beta, ck, gy, None, packed, ws, stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
 
-    # per step: [step start, fwd end, bwd start, bwd recurrence end, bwd reduction end]
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    for es in ev:
-        for e in es:
+    # per step: forward events (before + after each kernel), backward events likewise
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [([mk() for _ in range(n_fwd + 1)], [mk() for _ in range(n_bwd + 1)])
+          for _ in range(args.steps)]
+    for fe, be in ev:
+        for e in fe + be:
             e.record(stream)  # materialise the event handles
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
@@ -285,22 +321,27 @@ def run_ours(args):
     time.sleep(0.3)
     for i in range(args.steps):
         flush.zero_()  # L2 flush between timed steps (not inside the events)
-        e0, e1, b0, b1, b2 = ev[i]
-        e0.record(stream)
-        gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, stream)
-        e1.record(stream)
-        gdn.set_backward_timing_events((b0, b1, b2))
+        fe, be = ev[i]
+        gdn.set_timing_events(fe)
+        gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, fws, stream)
+        gdn.set_timing_events(be)
         gdn.gdn_backward(p, q, k, v, g, beta, ck, gy, None, packed, ws, stream)
-    gdn.set_backward_timing_events(None)
+    gdn.set_timing_events(None)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    fwd_ms = [es[0].elapsed_time(es[1]) for es in ev]
-    bwdk_ms = [es[2].elapsed_time(es[3]) for es in ev]
-    red_ms = [es[3].elapsed_time(es[4]) for es in ev]
-    bwd_ms = [es[1].elapsed_time(es[4]) for es in ev]
-    step_ms = sum(es[0].elapsed_time(es[4]) for es in ev) / args.steps
+    kern_ms = [0.0] * (n_fwd + n_bwd)
+    fwd_ms, bwd_ms, steps_ms = [], [], []
+    for fe, be in ev:
+        for j in range(n_fwd):
+            kern_ms[j] += fe[j].elapsed_time(fe[j + 1]) / args.steps
+        for j in range(n_bwd):
+            kern_ms[n_fwd + j] += be[j].elapsed_time(be[j + 1]) / args.steps
+        fwd_ms.append(fe[0].elapsed_time(fe[-1]))
+        bwd_ms.append(be[0].elapsed_time(be[-1]))
+        steps_ms.append(fe[0].elapsed_time(be[-1]))
+    step_ms = sum(steps_ms) / args.steps
     if dist:
         step_ms = max_over_ranks(step_ms, dist, dev)
     head_tokens = N * H_v * T
@@ -325,7 +366,8 @@ def run_ours(args):
         def e2e_step():
             for nm, t in host.items():
                 d_in[nm].copy_(t, non_blocking=True)
-            gdn.gdn_forward(p, q2, k2, v2, d_in["g"], d_in["beta"], d_in["state0"], y, sT, ck, stream)
+            gdn.gdn_forward(p, q2, k2, v2, d_in["g"], d_in["beta"], d_in["state0"], y, sT, ck,
+                            fws, stream)
             gdn.gdn_backward(p, q2, k2, v2, d_in["g"], d_in["beta"], ck, d_in["gy"], None, packed,
                              ws, stream)
             out_h["y"].copy_(y, non_blocking=True)
@@ -352,12 +394,19 @@ def run_ours(args):
         return
 
     bwd_avg = sum(bwd_ms) / len(bwd_ms)
-    bwdk_avg = sum(bwdk_ms) / len(bwdk_ms)
-    red_avg = sum(red_ms) / len(red_ms)
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    achieved = BWD_FLOPS(d) * head_tokens / (bwdk_avg * 1e-3) / 1e12
+    names = fwd_names + bwd_names
+    top = max(range(len(kern_ms)), key=lambda j: kern_ms[j])
+    if chunked:
+        top_flops = chunk_kernel_flops(N, T, H_v, d, C, kinds[top])
+    else:
+        top_flops = (FWD_FLOPS(d) if top < n_fwd else BWD_FLOPS(d)) * head_tokens
+    achieved = top_flops / (kern_ms[top] * 1e-3) / 1e12
     path_tflops = (FWD_FLOPS(d) + BWD_FLOPS(d)) * head_tokens / (step_ms * 1e-3) / 1e12
-    traffic = _recorded_traffic()
+    kernels = [{"kernel": nm, "ms": kern_ms[j],
+                "tflops": (chunk_kernel_flops(N, T, H_v, d, C, kinds[j]) / (kern_ms[j] * 1e-3) / 1e12)
+                if chunked else None} for j, nm in enumerate(names)]
+    traffic = _recorded_traffic(names[top])
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(prob)
@@ -369,16 +418,16 @@ def run_ours(args):
                    "gate": "kda" if prob.kda else "scalar", "C": C, "qkv": "packed row views",
                    "l2": "flushed between timed steps (256 MiB write outside the events)",
                    "per_rank": "each rank runs the whole workload on its own GPU"},
-        "roofline": {"bound": "alu", "kernel": "gdn_bwd_kernel",
+        "roofline": {"bound": "alu", "kernel": names[top],
                      "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                      "frac": achieved / FP32_PEAK_TFLOPS, "traffic": traffic,
-                     "flops_per_head_token": BWD_FLOPS(d), "launch_ms": bwdk_avg,
+                     "flops_per_launch": top_flops, "launch_ms": kern_ms[top],
                      "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.070 GHz"},
         "roofline_path": {"achieved": path_tflops, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                           "frac": path_tflops / FP32_PEAK_TFLOPS,
                           "flops_per_head_token": FWD_FLOPS(d) + BWD_FLOPS(d),
-                          "fwd_ms": fwd_avg, "bwd_ms": bwd_avg, "bwd_kernel_ms": bwdk_avg,
-                          "reduce_kernel_ms": red_avg},
+                          "fwd_ms": fwd_avg, "bwd_ms": bwd_avg},
+        "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": (n_fwd + n_bwd) * args.steps,

@@ -16,7 +16,8 @@
 namespace {
 
 thread_local std::string g_last_error;
-thread_local void* const* g_bwd_events = nullptr;
+thread_local void* const* g_events = nullptr;
+thread_local int g_n_events = 0;
 
 gdn_status_t fail(gdn_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 gdn_status_t fail(gdn_status_t s, const char* fmt, ...)
@@ -38,12 +39,21 @@ int64_t ceil_sqrt(int64_t T)
     return r;
 }
 
-// Launch plan: everything the kernels and the workspace size depend on.
+// Launch plan: everything the kernels and the workspace sizes depend on.  The scalar
+// gate runs the chunked (WY) kernels; the per-key-column (KDA) gate and the degenerate
+// T = 0 case run the token recurrence kernels.
 struct Plan {
     int D = 0, RT = 1, W = 4, R = 16, P = 1, tc = 32, c2 = 1, nsub_max = 1;
     bool kda = false;
+    bool chunked = false;
     int64_t C = 1, n_ck = 0;
-    size_t off_sub = 0, off_col = 0, off_sc = 0, ws_bytes = 0;
+    size_t off_sub = 0, off_col = 0, off_sc = 0, ws_bytes = 0;  // recurrence backward
+    // chunked form
+    int cps = 1;          // chunks per checkpoint segment
+    int64_t n_chunks = 0; // chunks per (sequence, value head)
+    long long o_T = 0, o_QKD = 0, o_gam = 0, o_r = 0, o_W = 0, o_U = 0, o_Mc = 0, o_dM = 0,
+              o_dDel = 0, o_dX = 0;
+    size_t fwd_ws_bytes = 0, bwd_ws_bytes = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -116,6 +126,38 @@ Plan make_plan(const gdn_params_t* p)
     pl.off_col = align256(sub_f * 4);
     pl.off_sc = pl.off_col + align256(col_f * 4);
     pl.ws_bytes = pl.off_sc + align256(sc_f * 4);
+
+    pl.chunked = !pl.kda && p->T > 0;
+    if (pl.chunked) {
+        const int64_t BC = gdn::BC;
+        pl.cps = (int)((pl.C + BC - 1) / BC);
+        const int64_t last_len = p->T - (pl.n_ck - 1) * pl.C;
+        pl.n_chunks = (pl.n_ck - 1) * pl.cps + (last_len + BC - 1) / BC;
+        const int64_t CH = p->n_seq * p->H_v * pl.n_chunks;
+        const int64_t D = pl.D;
+        // float offsets, each sub-array 256-byte aligned
+        auto al = [](int64_t f) { return (long long)((f + 63) & ~int64_t(63)); };
+        long long o = 0;
+        pl.o_T = o;   o += al(CH * BC * BC);
+        pl.o_QKD = o; o += al(CH * BC * BC);
+        pl.o_gam = o; o += al(CH * BC);
+        pl.o_r = o;   o += al(CH * BC);
+        const long long common = o;
+        pl.o_W = o;   o += al(CH * BC * D);
+        pl.o_U = o;   o += al(CH * BC * D);
+        pl.fwd_ws_bytes = (size_t)o * 4;
+        // backward: W, U and the chunk-entry states only when segments hold several chunks
+        if (pl.cps > 1) {
+            pl.o_Mc = o; o += al(CH * D * D);
+        } else {
+            o = common;
+        }
+        pl.o_dM = o;   o += al(CH * D * D);
+        pl.o_dDel = o; o += al(CH * BC * D);
+        pl.o_dX = o;   o += al(CH * BC * D);
+        pl.bwd_ws_bytes = (size_t)o * 4;
+        pl.ws_bytes = pl.bwd_ws_bytes;
+    }
     return pl;
 }
 
@@ -166,9 +208,28 @@ gdn_status_t cuda_status(int err, const char* what)
     return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)err));
 }
 
+void fill_chunk_common(gdn::ChunkArgs& c, const gdn_params_t* p, const Plan& pl)
+{
+    c.qs0 = p->q_s[0]; c.qs1 = p->q_s[1]; c.qs2 = p->q_s[2];
+    c.ks0 = p->k_s[0]; c.ks1 = p->k_s[1]; c.ks2 = p->k_s[2];
+    c.vs0 = p->v_s[0]; c.vs1 = p->v_s[1]; c.vs2 = p->v_s[2];
+    c.gys0 = p->gy_s[0]; c.gys1 = p->gy_s[1]; c.gys2 = p->gy_s[2];
+    c.N = (int)p->n_seq; c.T = (int)p->T; c.H_k = (int)p->H_k; c.H_v = (int)p->H_v;
+    c.C = (int)pl.C; c.n_ck = (int)pl.n_ck; c.cps = pl.cps; c.n_chunks = (int)pl.n_chunks;
+    c.scale = p->scale;
+    c.o_T = pl.o_T; c.o_QKD = pl.o_QKD; c.o_gam = pl.o_gam; c.o_r = pl.o_r; c.o_W = pl.o_W;
+    c.o_U = pl.o_U; c.o_Mc = pl.o_Mc; c.o_dM = pl.o_dM; c.o_dDel = pl.o_dDel; c.o_dX = pl.o_dX;
+}
+
 }  // namespace
 
 void gdn::set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
+void gdn::EventTap::mark(void* stream)
+{
+    if (ev && i < n) cudaEventRecord((cudaEvent_t)ev[i], (cudaStream_t)stream);
+    ++i;
+}
 
 extern "C" {
 
@@ -213,16 +274,26 @@ size_t gdn_backward_workspace_bytes(const gdn_params_t* p)
     return make_plan(p).ws_bytes;
 }
 
+size_t gdn_forward_workspace_bytes(const gdn_params_t* p)
+{
+    if (check_sizes(p) != GDN_OK) return 0;
+    const Plan pl = make_plan(p);
+    return pl.chunked ? pl.fwd_ws_bytes : 0;
+}
+
 int gdn_forward_launches(const gdn_params_t* p)
 {
     if (check_sizes(p) != GDN_OK) return 0;
-    return p->n_seq > 0 ? 1 : 0;
+    if (p->n_seq == 0) return 0;
+    return make_plan(p).chunked ? 2 : 1;
 }
 
 int gdn_backward_launches(const gdn_params_t* p)
 {
     if (check_sizes(p) != GDN_OK) return 0;
     if (p->n_seq == 0) return 0;
+    const Plan pl = make_plan(p);
+    if (pl.chunked) return pl.cps > 1 ? 4 : 3;
     return p->T > 0 ? 2 : 1;
 }
 
@@ -242,11 +313,16 @@ const char* gdn_status_str(gdn_status_t s)
 
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
-void gdn_set_backward_timing_events(void* const* events) { g_bwd_events = events; }
+void gdn_set_timing_events(void* const* events, int n_events)
+{
+    g_events = events;
+    g_n_events = events ? n_events : 0;
+}
 
 gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, const float* v,
                          const float* g, const float* beta, const float* state0, float* y,
-                         float* state_T, float* ckpt, void* stream)
+                         float* state_T, float* ckpt, void* workspace, size_t workspace_bytes,
+                         void* stream)
 {
     gdn_status_t st = check_sizes(p);
     if (st != GDN_OK) return st;
@@ -279,6 +355,25 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, 
             if (overlap(out, in)) return fail(GDN_ERR_ALIAS, "a forward output overlaps an input");
     if (overlap(ry, rsT) || overlap(ry, rck) || overlap(rsT, rck))
         return fail(GDN_ERR_ALIAS, "forward outputs overlap one another");
+    const size_t need = pl.chunked ? pl.fwd_ws_bytes : 0;
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    if (need > 0 && (!workspace || !aligned(workspace, 256)))
+        return fail(GDN_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+    const Range rws = {(uintptr_t)workspace, (uintptr_t)workspace + (workspace ? need : 0)};
+    for (Range other : {rq, rk, rv, rg, rb, rs0, ry, rsT, rck})
+        if (overlap(rws, other)) return fail(GDN_ERR_ALIAS, "workspace overlaps a tensor");
+
+    gdn::EventTap tap{g_events, g_n_events, 0};
+    if (pl.chunked) {
+        gdn::ChunkArgs c{};
+        c.q = q; c.k = k; c.v = v; c.g = g; c.beta = beta; c.state0 = state0;
+        c.y = y; c.state_T = state_T; c.ckpt_out = ckpt; c.ws = (float*)workspace;
+        fill_chunk_common(c, p, pl);
+        c.want_wu = 1;
+        c.vec_q = vec_ok(q, p->q_s); c.vec_k = vec_ok(k, p->k_s); c.vec_v = vec_ok(v, p->v_s);
+        return cuda_status(gdn::launch_chunk_forward(c, pl.D, stream, tap), "forward launch");
+    }
 
     gdn::FwdArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state0 = state0;
@@ -290,7 +385,10 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, 
     a.C = (int)pl.C; a.n_ck = (int)pl.n_ck; a.scale = p->scale; a.tc = pl.tc;
     a.vec_q = vec_ok(q, p->q_s); a.vec_k = vec_ok(k, p->k_s); a.vec_v = vec_ok(v, p->v_s);
     a.vec_g = aligned(g, 16);
-    return cuda_status(gdn::launch_forward(a, pl.D, pl.RT, pl.W, pl.kda, stream), "forward launch");
+    tap.mark(stream);
+    st = cuda_status(gdn::launch_forward(a, pl.D, pl.RT, pl.W, pl.kda, stream), "forward launch");
+    tap.mark(stream);
+    return st;
 }
 
 gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k, const float* v,
@@ -335,6 +433,20 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
             if (overlap(out, in)) return fail(GDN_ERR_ALIAS, "a backward output overlaps an input");
     if (overlap(rpk, rws)) return fail(GDN_ERR_ALIAS, "workspace overlaps packed_grads");
 
+    gdn::EventTap tap{g_events, g_n_events, 0};
+    if (pl.chunked) {
+        gdn::ChunkArgs c{};
+        c.q = q; c.k = k; c.v = v; c.g = g; c.beta = beta; c.ckpt = ckpt; c.gy = gy;
+        c.dstate_T = dstate_T; c.ws = (float*)workspace;
+        c.dq = packed + off[0]; c.dk = packed + off[1]; c.dv = packed + off[2];
+        c.dg = packed + off[3]; c.dbeta = packed + off[4]; c.dstate0 = packed + off[5];
+        fill_chunk_common(c, p, pl);
+        c.want_wu = pl.cps > 1;
+        c.vec_q = vec_ok(q, p->q_s); c.vec_k = vec_ok(k, p->k_s); c.vec_v = vec_ok(v, p->v_s);
+        c.vec_gy = vec_ok(gy, p->gy_s);
+        return cuda_status(gdn::launch_chunk_backward(c, pl.D, stream, tap), "backward launch");
+    }
+
     char* ws = (char*)workspace;
     gdn::BwdArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.ckpt = ckpt; a.gy = gy;
@@ -354,15 +466,10 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
     a.vec_q = vec_ok(q, p->q_s); a.vec_k = vec_ok(k, p->k_s); a.vec_v = vec_ok(v, p->v_s);
     a.vec_gy = vec_ok(gy, p->gy_s); a.vec_g = aligned(g, 16);
     a.vec_ds0 = aligned(packed + off[5], 16);
-    cudaStream_t cs = (cudaStream_t)stream;
-    if (g_bwd_events) cudaEventRecord((cudaEvent_t)g_bwd_events[0], cs);
+    tap.mark(stream);
     st = cuda_status(gdn::launch_backward(a, pl.D, pl.RT, pl.W, pl.kda, stream), "backward launch");
-    if (g_bwd_events) cudaEventRecord((cudaEvent_t)g_bwd_events[1], cs);
-    if (st != GDN_OK) return st;
-    if (!tok) {
-        if (g_bwd_events) cudaEventRecord((cudaEvent_t)g_bwd_events[2], cs);
-        return st;
-    }
+    tap.mark(stream);
+    if (st != GDN_OK || !tok) return st;
 
     gdn::ReduceArgs r{};
     r.ws_col = a.ws_col; r.ws_sc = a.ws_sc;
@@ -370,7 +477,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
     r.N = (int)N; r.T = (int)T; r.H_k = (int)Hk; r.H_v = (int)Hv; r.D = (int)D; r.P = pl.P;
     r.NQ = pl.kda ? 3 : 2; r.kda = pl.kda;
     st = cuda_status(gdn::launch_reduce(r, stream), "reduce launch");
-    if (g_bwd_events) cudaEventRecord((cudaEvent_t)g_bwd_events[2], cs);
+    tap.mark(stream);
     return st;
 }
 

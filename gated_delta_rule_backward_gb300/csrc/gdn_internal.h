@@ -71,6 +71,50 @@ struct ReduceArgs {
     int N, T, H_k, H_v, D, P, NQ, kda;
 };
 
+// Chunked (WY) form, scalar gate: chunk length and the arguments of its kernels.
+constexpr int BC = 32;
+
+struct ChunkArgs {
+    const float* q;
+    const float* k;
+    const float* v;
+    const float* g;
+    const float* beta;
+    const float* state0;    // forward input
+    const float* ckpt;      // backward input (checkpoints of the forward)
+    const float* gy;        // backward input
+    const float* dstate_T;  // backward input, may be null
+    float* y;               // forward outputs
+    float* state_T;
+    float* ckpt_out;
+    float* dq;              // backward outputs (packed regions)
+    float* dk;
+    float* dv;
+    float* dg;
+    float* dbeta;
+    float* dstate0;
+    float* ws;              // workspace base
+    long long qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2, gys0, gys1, gys2;
+    int N, T, H_k, H_v, C, n_ck, cps, n_chunks;
+    float scale;
+    // workspace sub-arrays (float offsets from ws), per (sequence, value head, chunk)
+    long long o_T, o_QKD, o_gam, o_r, o_W, o_U, o_Mc, o_dM, o_dDel, o_dX;
+    int want_wu;
+    int vec_q, vec_k, vec_v, vec_gy;
+};
+
+// Records caller-provided timing events around the kernels of one call: mark() before
+// the first kernel and after each one, while events remain.
+struct EventTap {
+    void* const* ev;
+    int n;
+    int i;
+    void mark(void* stream);
+};
+
+int launch_chunk_forward(const ChunkArgs& a, int D, void* stream, EventTap& tap);
+int launch_chunk_backward(const ChunkArgs& a, int D, void* stream, EventTap& tap);
+
 // Shared-memory layout of the backward kernel, in floats (every offset a multiple of 4).
 struct BwdSmem {
     int ring, sk, sq, sa, sb, sv, sgy, sdel, svmu, sdd, scol, sdg, total;

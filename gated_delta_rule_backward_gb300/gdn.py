@@ -30,8 +30,8 @@ GATE_SCALAR, GATE_KDA = 0, 1
 EXPORTS = ["gdn_checkpoint_interval", "gdn_num_checkpoints", "gdn_ckpt_elems", "gdn_forward",
            "gdn_packed_grad_elems", "gdn_packed_grad_offsets", "gdn_backward_workspace_bytes",
            "gdn_backward", "gdn_status_str", "gdn_last_error", "gdn_forward_launches",
-           "gdn_backward_launches", "gdn_set_backward_timing_events",
-           "gdn_backward_noalloc"]
+           "gdn_backward_launches", "gdn_set_timing_events", "gdn_backward_noalloc",
+           "gdn_forward_workspace_bytes"]
 
 
 class GdnParams(ctypes.Structure):
@@ -60,7 +60,7 @@ _lib.gdn_packed_grad_offsets.argtypes = [_P, ctypes.POINTER(ctypes.c_size_t)]
 _lib.gdn_packed_grad_offsets.restype = None
 _lib.gdn_backward_workspace_bytes.argtypes = [_P]
 _lib.gdn_backward_workspace_bytes.restype = ctypes.c_size_t
-_lib.gdn_forward.argtypes = [_P] + [_vp] * 10
+_lib.gdn_forward.argtypes = [_P] + [_vp] * 10 + [ctypes.c_size_t, _vp]
 _lib.gdn_forward.restype = ctypes.c_int
 _lib.gdn_backward.argtypes = [_P] + [_vp] * 10 + [ctypes.c_size_t, _vp]
 _lib.gdn_backward.restype = ctypes.c_int
@@ -74,8 +74,10 @@ _lib.gdn_backward_launches.argtypes = [_P]
 _lib.gdn_backward_launches.restype = ctypes.c_int
 _lib.gdn_backward_noalloc.argtypes = [_P] + [_vp] * 10
 _lib.gdn_backward_noalloc.restype = ctypes.c_int
-_lib.gdn_set_backward_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
-_lib.gdn_set_backward_timing_events.restype = None
+_lib.gdn_set_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+_lib.gdn_set_timing_events.restype = None
+_lib.gdn_forward_workspace_bytes.argtypes = [_P]
+_lib.gdn_forward_workspace_bytes.restype = ctypes.c_size_t
 
 
 class GdnError(RuntimeError):
@@ -165,22 +167,29 @@ def launches(p: GdnParams):
 _EVENTS = None
 
 
-def set_backward_timing_events(events):
-    """Three recorded torch.cuda.Event(enable_timing=True) objects, or None.  gdn_backward
-    then records them around its recurrence and reduction kernels."""
+def set_timing_events(events):
+    """A list of recorded torch.cuda.Event(enable_timing=True) objects, or None.  Each
+    gdn_forward / gdn_backward call then records events[0] before its first kernel and
+    events[i] after its i-th kernel."""
     global _EVENTS
     if events is None:
         _EVENTS = None
-        _lib.gdn_set_backward_timing_events(None)
+        _lib.gdn_set_timing_events(None, 0)
         return
-    _EVENTS = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) for e in events])
-    _lib.gdn_set_backward_timing_events(_EVENTS)
+    _EVENTS = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _lib.gdn_set_timing_events(_EVENTS, len(events))
 
 
-def gdn_forward(p: GdnParams, q, k, v, g, beta, state0, y, state_T, ckpt, stream=None):
+def forward_workspace_bytes(p: GdnParams) -> int:
+    return int(_lib.gdn_forward_workspace_bytes(ctypes.byref(p)))
+
+
+def gdn_forward(p: GdnParams, q, k, v, g, beta, state0, y, state_T, ckpt, workspace=None,
+                stream=None):
     """Raw C-ABI call on caller-provided tensors (all on the current CUDA device)."""
     st = _lib.gdn_forward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                          _ptr(state0), _ptr(y), _ptr(state_T), _ptr(ckpt),
+                          _ptr(state0), _ptr(y), _ptr(state_T), _ptr(ckpt), _ptr(workspace),
+                          ctypes.c_size_t(0 if workspace is None else workspace.numel()),
                           _stream_handle(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_forward")
@@ -217,7 +226,9 @@ def forward(q, k, v, g, beta, state0, C=None, scale=None, stream=None):
     y = torch.empty((N, T, H_v, S), dtype=torch.float32, device=dev)
     state_T = torch.empty((N, H_v, S, S), dtype=torch.float32, device=dev)
     ckpt = torch.empty((N, H_v, num_checkpoints(p), S, S), dtype=torch.float32, device=dev)
-    gdn_forward(p, q, k, v, g, beta, state0, y, state_T, ckpt, stream)
+    nws = forward_workspace_bytes(p)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
+    gdn_forward(p, q, k, v, g, beta, state0, y, state_T, ckpt, ws, stream)
     return y, state_T, ckpt, p
 
 

@@ -101,14 +101,20 @@ int64_t gdn_num_checkpoints(const gdn_params_t* p);
 /* Elements of the ckpt buffer: N * H_v * n_ck * S_v * S_k. */
 size_t gdn_ckpt_elems(const gdn_params_t* p);
 
+/* Device workspace the forward needs (bytes; 0 when it needs none).  Scratch owned by
+ * the caller for the duration of the enqueued work; 256-byte aligned start required. */
+size_t gdn_forward_workspace_bytes(const gdn_params_t* p);
+
 /* Forward (meTile "Recurrent delta attention"; PR #16 row form).  Reads q, k, v, g,
  * beta, state0; writes y, state_T and ckpt (each must be non-NULL unless its size is
  * zero).  state_T may not overlap state0 (llama.cpp PR #26: an in-place state update
- * destroyed the initial state the backward needed). */
+ * destroyed the initial state the backward needed).  The scalar gate runs the chunked
+ * (WY) regrouping of the recurrence (exact, chunks of 32 tokens aligned to the
+ * checkpoint segments); the per-key-column gate runs the token recurrence. */
 gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k,
                          const float* v, const float* g, const float* beta,
                          const float* state0, float* y, float* state_T, float* ckpt,
-                         void* stream);
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* Packed gradient buffer: total elements, and the element offsets of its six regions
  * in the order dq, dk, dv, dg, dbeta, dstate (PR #16 body: "[dq|dk|dv|dg|dbeta|dstate]"). */
@@ -150,12 +156,12 @@ gdn_status_t gdn_backward_noalloc(const gdn_params_t* p, const float* q, const f
 const char* gdn_status_str(gdn_status_t s);
 const char* gdn_last_error(void);
 
-/* Optional per-kernel timing for the calling thread: when `events` is non-NULL,
- * gdn_backward records events[0] before its first kernel, events[1] after the
- * recurrence kernel and events[2] after the reduction kernel, all on the call's stream;
- * the events are cudaEvent_t handles the caller created (and owns).  NULL turns it off.
- * Not part of the operation: it lets a caller time the two kernels separately. */
-void gdn_set_backward_timing_events(void* const* events);
+/* Optional per-kernel timing for the calling thread: while `events` is non-NULL, every
+ * gdn_forward / gdn_backward call records events[0] on its stream before its first
+ * kernel and events[i] after its i-th kernel, for i < n_events.  The events are
+ * cudaEvent_t handles the caller created and owns; NULL turns the recording off.  Not
+ * part of the operation: it lets a caller time each kernel of a call. */
+void gdn_set_timing_events(void* const* events, int n_events);
 
 /* Kernels a forward / backward call with these params launches (0 when the call would
  * fail validation).  Lets callers account for the work they enqueue. */

@@ -50,7 +50,10 @@ def test_packed_layout_and_sizes():
         assert gdn.num_checkpoints(p) == 8                        # ceil(61 / 8)
         assert gdn.library().gdn_ckpt_elems(ctypes.byref(p)) == N * Hv * 8 * S * S
         assert gdn.backward_workspace_bytes(p) > 0
-        assert gdn.launches(p) == (1, 2)
+        # scalar gate: chunked kernels (prep + state chain; prep + dM chain + gradients),
+        # KDA gate: token recurrence (forward; backward + reduction)
+        assert gdn.launches(p) == ((1, 2) if kda else (2, 3))
+        assert (gdn.forward_workspace_bytes(p) == 0) == kda
 
 
 def test_default_checkpoint_interval_matches_pages():
@@ -70,6 +73,20 @@ def test_empty_batch_launches_nothing():
     assert gdn.num_checkpoints(p) == 0
 
 
+def test_chunked_launch_count_with_several_chunks_per_segment():
+    # C = 64 > 32-token chunks: the backward also rebuilds the chunk-entry states
+    p = gdn.make_params(1, 4096, 16, 48, 128, False)
+    assert gdn.checkpoint_interval(p) == 64
+    assert gdn.launches(p) == (2, 4)
+
+
+def test_forward_workspace_checks():
+    p = gdn.make_params(1, 64, 1, 3, 64, False)
+    need = gdn.forward_workspace_bytes(p)
+    assert need > 0
+    assert call_forward(p, ws_bytes=need - 256) == WORKSPACE
+
+
 # ---- argument validation: every case below fails before any device work ----
 
 BASE = 0x7f0000000000  # fake, 256-byte aligned device addresses
@@ -79,9 +96,12 @@ def fake(i):
     return ctypes.c_void_p(BASE + i * (1 << 32))
 
 
-def call_forward(p, ptrs=None):
+def call_forward(p, ptrs=None, ws_bytes=None):
     ptrs = ptrs or [fake(i) for i in range(9)]
-    return gdn.library().gdn_forward(ctypes.byref(p), *ptrs, None)
+    if ws_bytes is None:
+        ws_bytes = gdn.forward_workspace_bytes(p)
+    return gdn.library().gdn_forward(ctypes.byref(p), *ptrs, fake(10), ctypes.c_size_t(ws_bytes),
+                                     None)
 
 
 def call_backward(p, ws_bytes, ptrs=None):
@@ -111,7 +131,8 @@ def test_invalid_arguments():
     assert call_forward(p) == INVALID
     p = gdn.make_params(-1, 8, 1, 1, 32, False)
     assert call_forward(p) == INVALID
-    assert gdn.library().gdn_forward(None, *[fake(i) for i in range(9)], None) == INVALID
+    assert gdn.library().gdn_forward(None, *[fake(i) for i in range(10)], ctypes.c_size_t(0),
+                                     None) == INVALID
     p = gdn.make_params(1, 8, 1, 1, 32, False)
     ptrs = [fake(i) for i in range(9)]
     ptrs[0] = ctypes.c_void_p(BASE + 2)                                     # q not 4-byte aligned
