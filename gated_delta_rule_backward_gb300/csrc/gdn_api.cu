@@ -51,8 +51,8 @@ struct Plan {
     // chunked form
     int cps = 1;          // chunks per checkpoint segment
     int64_t n_chunks = 0; // chunks per (sequence, value head)
-    long long o_T = 0, o_QKD = 0, o_gam = 0, o_r = 0, o_W = 0, o_U = 0, o_Mc = 0, o_dM = 0,
-              o_dDel = 0, o_dX = 0;
+    long long o_T = 0, o_QKD = 0, o_QDT = 0, o_gam = 0, o_r = 0, o_W = 0, o_U = 0, o_Mc = 0, o_dM = 0,
+              o_dDel = 0, o_dX = 0, o_Tr = 0, o_Z = 0, o_KK = 0, o_QK = 0, o_Dm = 0;
     size_t fwd_ws_bytes = 0, bwd_ws_bytes = 0;
 };
 
@@ -140,6 +140,7 @@ Plan make_plan(const gdn_params_t* p)
         long long o = 0;
         pl.o_T = o;   o += al(CH * BC * BC);
         pl.o_QKD = o; o += al(CH * BC * BC);
+        pl.o_QDT = o; o += al(CH * BC * BC);
         pl.o_gam = o; o += al(CH * BC);
         pl.o_r = o;   o += al(CH * BC);
         const long long common = o;
@@ -152,6 +153,11 @@ Plan make_plan(const gdn_params_t* p)
         } else {
             o = common;
         }
+        pl.o_Tr = o;   o += al(CH * BC * BC);
+        pl.o_Z = o;    o += al(CH * BC * BC);
+        pl.o_KK = o;   o += al(CH * BC * BC);
+        pl.o_QK = o;   o += al(CH * BC * BC);
+        pl.o_Dm = o;   o += al(CH * BC * BC);
         pl.o_dM = o;   o += al(CH * D * D);
         pl.o_dDel = o; o += al(CH * BC * D);
         pl.o_dX = o;   o += al(CH * BC * D);
@@ -217,8 +223,9 @@ void fill_chunk_common(gdn::ChunkArgs& c, const gdn_params_t* p, const Plan& pl)
     c.N = (int)p->n_seq; c.T = (int)p->T; c.H_k = (int)p->H_k; c.H_v = (int)p->H_v;
     c.C = (int)pl.C; c.n_ck = (int)pl.n_ck; c.cps = pl.cps; c.n_chunks = (int)pl.n_chunks;
     c.scale = p->scale;
-    c.o_T = pl.o_T; c.o_QKD = pl.o_QKD; c.o_gam = pl.o_gam; c.o_r = pl.o_r; c.o_W = pl.o_W;
+    c.o_T = pl.o_T; c.o_QKD = pl.o_QKD; c.o_QDT = pl.o_QDT; c.o_gam = pl.o_gam; c.o_r = pl.o_r; c.o_W = pl.o_W;
     c.o_U = pl.o_U; c.o_Mc = pl.o_Mc; c.o_dM = pl.o_dM; c.o_dDel = pl.o_dDel; c.o_dX = pl.o_dX;
+    c.o_Tr = pl.o_Tr; c.o_Z = pl.o_Z; c.o_KK = pl.o_KK; c.o_QK = pl.o_QK; c.o_Dm = pl.o_Dm;
 }
 
 }  // namespace
@@ -442,6 +449,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
         c.dg = packed + off[3]; c.dbeta = packed + off[4]; c.dstate0 = packed + off[5];
         fill_chunk_common(c, p, pl);
         c.want_wu = pl.cps > 1;
+        c.want_factors = 1;
         c.vec_q = vec_ok(q, p->q_s); c.vec_k = vec_ok(k, p->k_s); c.vec_v = vec_ok(v, p->v_s);
         c.vec_gy = vec_ok(gy, p->gy_s);
         return cuda_status(gdn::launch_chunk_backward(c, pl.D, stream, tap), "backward launch");

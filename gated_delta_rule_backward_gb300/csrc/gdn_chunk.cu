@@ -36,8 +36,13 @@ namespace gdn {
 
 constexpr int CT = 256;        // threads per CTA (all chunk kernels)
 constexpr int LDB = BC + 4;    // leading dimension of BC-wide shared rows
-constexpr int RR = 32;         // rows of M per CTA in the state kernels
-constexpr int LDR = RR + 4;
+// Rows of M per CTA in the state kernels: 24 at head size 128 (6 CTAs per head, the last
+// one 8 rows short; 48 heads then fill two CTAs per SM on 144 SMs), else 32.
+template <int D>
+struct Rows {
+    static constexpr int RR = (D == 128) ? 24 : 32;
+    static constexpr int P = (D + RR - 1) / RR;
+};
 constexpr unsigned kFullMask = 0xffffffffu;
 
 template <int D>
@@ -146,32 +151,74 @@ __device__ void chunk_prep(const float* QKs, const float* gs, const float* bs, f
         Dm[t * LDB + tau] = (tau <= t) ? expf(__fsub_rn(Gs[t], Gs[tau])) : 0.f;
     }
     __syncthreads();
-    if (tid < 32) {  // forward substitution, lane j owns column j of Z
-        const int j = tid;
-        for (int t = 0; t < BC; ++t) {
-            float z;
-            if (t < j) {
-                z = 0.f;
-            } else if (t == j) {
-                z = 1.f;
-            } else {
-                float a0 = 0.f, a1 = 0.f;
-                int tau = j;
-                for (; tau + 1 < t; tau += 2) {
-                    a0 = __fmaf_rn(__fmul_rn(Dm[t * LDB + tau], KKm[t * LDB + tau]),
-                                   Zs[tau * LDB + j], a0);
-                    a1 = __fmaf_rn(__fmul_rn(Dm[t * LDB + tau + 1], KKm[t * LDB + tau + 1]),
-                                   Zs[(tau + 1) * LDB + j], a1);
-                }
-                if (tau < t)
-                    a0 = __fmaf_rn(__fmul_rn(Dm[t * LDB + tau], KKm[t * LDB + tau]),
-                                   Zs[tau * LDB + j], a0);
-                z = -__fmul_rn(bs[t], __fadd_rn(a0, a1));
-            }
-            Zs[t * LDB + j] = z;
+    // Z = (I + A)^-1 with A = diag(beta) (Dm (.) KK) strictly lower, blockwise:
+    // [[I + A11, 0], [A21, I + A22]]^-1 = [[Z11, 0], [-Z22 A21 Z11, Z22]],
+    // from four 8 x 8 diagonal blocks (forward substitution) up to 32 x 32.
+    // Ts holds A meanwhile.
+    for (int idx = tid; idx < BC * BC; idx += CT) {
+        const int t = idx / BC, tau = idx - t * BC;
+        Ts[t * LDB + tau] = (tau < t) ? __fmul_rn(bs[t], __fmul_rn(Dm[t * LDB + tau], KKm[t * LDB + tau]))
+                                      : 0.f;
+        Zs[t * LDB + tau] = 0.f;
+    }
+    __syncthreads();
+    if (tid < 32) {  // diagonal 8 x 8 blocks: lane = 8 block + column
+        const int r0 = (tid >> 3) * 8, j = r0 + (tid & 7);
+        float z[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int row = r0 + t;
+            float acc = 0.f;
+#pragma unroll
+            for (int tau = 0; tau < t; ++tau)
+                if (r0 + tau >= j) acc = __fmaf_rn(Ts[row * LDB + r0 + tau], z[tau], acc);
+            z[t] = (row < j) ? 0.f : (row == j ? 1.f : -acc);
+            Zs[row * LDB + j] = z[t];
         }
     }
     __syncthreads();
+    // level 16: blocks (1,0) and (3,2) of 8 x 8: Z_ij = -Z_ii A_ij Z_jj
+    float* Pw = Dm;  // scratch in Dm's strict upper half (columns > rows), zero otherwise
+    if (tid < 128) {
+        const int b = tid >> 6, e = tid & 63, rr = e >> 3, cc = e & 7;
+        const int i0 = 8 + 16 * b, j0 = 16 * b;  // block rows i0.., cols j0..
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc = __fmaf_rn(Ts[(i0 + rr) * LDB + j0 + k], Zs[(j0 + k) * LDB + j0 + cc], acc);
+        Pw[(j0 + cc) * LDB + i0 + rr] = acc;  // stored transposed in Dm's upper half
+    }
+    __syncthreads();
+    if (tid < 128) {
+        const int b = tid >> 6, e = tid & 63, rr = e >> 3, cc = e & 7;
+        const int i0 = 8 + 16 * b, j0 = 16 * b;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc = __fmaf_rn(Zs[(i0 + rr) * LDB + i0 + k], Pw[(j0 + cc) * LDB + i0 + k], acc);
+        Zs[(i0 + rr) * LDB + j0 + cc] = -acc;
+    }
+    __syncthreads();
+    // level 32: Z21 (rows 16..31, cols 0..15) = -Z22 A21 Z11
+    {
+        const int rr = tid >> 4, cc = tid & 15;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc = __fmaf_rn(Ts[(16 + rr) * LDB + k], Zs[k * LDB + cc], acc);
+        Pw[cc * LDB + 16 + rr] = acc;  // transposed, in Dm's upper half
+    }
+    __syncthreads();
+    {
+        const int rr = tid >> 4, cc = tid & 15;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc = __fmaf_rn(Zs[(16 + rr) * LDB + 16 + k], Pw[cc * LDB + 16 + k], acc);
+        Zs[(16 + rr) * LDB + cc] = -acc;
+    }
+    __syncthreads();
+    // restore Dm's upper half to zero
+    for (int idx = tid; idx < BC * BC; idx += CT) {
+        const int t = idx / BC, tau = idx - t * BC;
+        if (tau > t) Dm[t * LDB + tau] = 0.f;
+    }
     for (int idx = tid; idx < BC * BC; idx += CT) {
         const int t = idx / BC, tau = idx - t * BC;
         Ts[t * LDB + tau] = __fmul_rn(Zs[t * LDB + tau], bs[tau]);
@@ -225,21 +272,40 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
     __syncthreads();
     chunk_prep<D>(QKs, gs, bs, Gs, gam, Dm, KKm, QKm, Zs, Ts, tid);
 
-    float* wsT = A.ws + A.o_T + ch * (BC * BC);
+    // T^T, QD = lower(QK^T) (.) Dm, QD^T, gamma, r
+    float* wsTT = A.ws + A.o_T + ch * (BC * BC);
     float* wsQ = A.ws + A.o_QKD + ch * (BC * BC);
+    float* wsQT = A.ws + A.o_QDT + ch * (BC * BC);
     for (int idx = tid; idx < BC * BC; idx += CT) {
         const int t = idx / BC, tau = idx - t * BC;
-        wsT[idx] = Ts[t * LDB + tau];
-        wsQ[idx] = __fmul_rn(QKm[t * LDB + tau], Dm[t * LDB + tau]);
+        const float qd = __fmul_rn(QKm[t * LDB + tau], Dm[t * LDB + tau]);
+        wsTT[tau * BC + t] = Ts[t * LDB + tau];
+        wsQ[idx] = qd;
+        wsQT[tau * BC + t] = qd;
         TG[t * LDB + tau] = __fmul_rn(Ts[t * LDB + tau], gam[tau]);
     }
     if (tid < BC) {
         A.ws[A.o_gam + ch * BC + tid] = gam[tid];
         A.ws[A.o_r + ch * BC + tid] = Dm[(BC - 1) * LDB + tid];
     }
+    if (A.want_factors) {  // the gradient kernel's chunk factors, row-major BC x BC
+        float* fT = A.ws + A.o_Tr + ch * (BC * BC);
+        float* fZ = A.ws + A.o_Z + ch * (BC * BC);
+        float* fK = A.ws + A.o_KK + ch * (BC * BC);
+        float* fQ = A.ws + A.o_QK + ch * (BC * BC);
+        float* fD = A.ws + A.o_Dm + ch * (BC * BC);
+        for (int idx = tid; idx < BC * BC; idx += CT) {
+            const int t = idx / BC, tau = idx - t * BC;
+            fT[idx] = Ts[t * LDB + tau];
+            fZ[idx] = Zs[t * LDB + tau];
+            fK[idx] = KKm[t * LDB + tau];
+            fQ[idx] = QKm[t * LDB + tau];
+            fD[idx] = Dm[t * LDB + tau];
+        }
+    }
     if (!A.want_wu) return;
     __syncthreads();
-    // W = T diag(gamma) K,  U = T V   (BC x D each)
+    // W = T diag(gamma) K  (BC x D, row-major),  U^T = (T V)^T  (D x BC)
     constexpr int TM = D / 32;
     using Map = GemmMap<BC, D, TM, 4, false>;
     float acc[TM][4];
@@ -256,20 +322,57 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) wsU[Map::row(tid, i) * D + Map::col(tid, j)] = acc[i][j];
+        for (int j = 0; j < 4; ++j) wsU[Map::col(tid, j) * BC + Map::row(tid, i)] = acc[i][j];
 }
 
 // ---------------------------------------------------------------------------------
+// Register prefetch of one chunk's raw rows of a strided input (q or k): BC x D floats,
+// NF = D / 32 float4 per thread, zero beyond the chunk's real rows.
+template <int D>
+__device__ __forceinline__ void pf_rows(float4 (&r)[D / 32], const float* src, long long stride,
+                                        int nb, bool vec, int tid)
+{
+#pragma unroll
+    for (int kk = 0; kk < D / 32; ++kk) {
+        const int f = tid + CT * kk, t = f / (D / 4), i4 = f - t * (D / 4);
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < nb) {
+            const float* p = src + t * stride + 4 * i4;
+            x = vec ? __ldg(reinterpret_cast<const float4*>(p))
+                    : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
+        }
+        r[kk] = x;
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void put_rows(float* dst, int ld, const float4 (&r)[D / 32], int tid)
+{
+#pragma unroll
+    for (int kk = 0; kk < D / 32; ++kk) {
+        const int f = tid + CT * kk, t = f / (D / 4), i4 = f - t * (D / 4);
+        *reinterpret_cast<float4*>(dst + t * ld + 4 * i4) = r[kk];
+    }
+}
+
 // State chain, rows [p RR, p RR + RR) of M for one head.
-//   forward  (blockIdx.y = head, blockIdx.x = p): every chunk in order; writes
-//            ckpt at segment starts, y, and state_T.
-//   recompute(blockIdx.y = segment, blockIdx.x = p, blockIdx.z = head): from ckpt[s]
-//            through the segment's chunks but its last, parking each chunk-entry state.
+//   forward  (grid: p, head, sequence): every chunk in order; writes the checkpoints at
+//            segment starts, y, and state_T.
+//   recompute(grid: p, segment, sequence * H_v + head): from ckpt[s] through the
+//            segment's chunks but its last, parking each chunk-entry state.
+// Per chunk (Delta^T and Y^T are kept transposed, rows j):
+//   [W M^T; Q M^T]^T  ->  Delta^T = U^T - (W M^T)^T,   Y^T = gamma (.) (Q M^T)^T
+//   Y^T += (QD Delta)^T,  y = scale Y
+//   M   <- gamma_last M + (r (.) Delta)^T K
+// The next chunk's operands are loaded into registers while the current one computes.
 template <int D, bool FWD>
 __global__ void __launch_bounds__(CT) gdn_chunk_state_kernel(const ChunkArgs A)
 {
     constexpr int ld = Ld<D>::v;
-    constexpr int TM3 = D / 32;  // M_end tile: RR x D
+    constexpr int NF = D / 32;
+    constexpr int RR = Rows<D>::RR;
+    constexpr int TM1 = RR / 8;          // RR x (BC or 2BC) tiles: 8 x 32 threads
+    constexpr int TM3 = RR * D / 1024;   // RR x D tile, float4 columns
     const int tid = threadIdx.x, p = blockIdx.x;
     int n, h, c_begin, c_end;
     if (FWD) {
@@ -278,9 +381,9 @@ __global__ void __launch_bounds__(CT) gdn_chunk_state_kernel(const ChunkArgs A)
         c_begin = 0;
         c_end = A.n_chunks;
     } else {
-        const int head = blockIdx.z;
-        n = head / A.H_v;
-        h = head - n * A.H_v;
+        const int hd = blockIdx.z;
+        n = hd / A.H_v;
+        h = hd - n * A.H_v;
         const int s = blockIdx.y;
         c_begin = s * A.cps;
         const int seg_len = min(A.T, s * A.C + A.C) - s * A.C;
@@ -290,264 +393,305 @@ __global__ void __launch_bounds__(CT) gdn_chunk_state_kernel(const ChunkArgs A)
     const int hk = h % A.H_k;
     const long long head = (long long)n * A.H_v + h;
     const int row0 = p * RR;
-
+    const int nr = min(RR, D - row0);  // real rows of this CTA
     extern __shared__ __align__(16) float sm[];
-    float* Ms = sm;                   // RR x ld   (rows of M)
-    float* WQ = Ms + RR * ld;         // [W; gamma Q]  2BC x ld
-    float* RK = WQ + 2 * BC * ld;     // r (.) K   BC x ld
-    float* Us = RK + BC * ld;         // BC x LDR
-    float* Dls = Us + BC * LDR;       // Delta  BC x LDR
-    float* Y1 = Dls + BC * LDR;       // BC x LDR
-    float* QD = Y1 + BC * LDR;        // BC x LDB
-    float* vec = QD + BC * LDB;       // gam, r
+    float* Ms = sm;                   // RR x ld
+    float* WQs = Ms + RR * ld;        // [W; Q]  2BC x ld
+    float* Ks = WQs + 2 * BC * ld;    // BC x ld
+    float* UT = Ks + BC * ld;         // RR x LDB each:
+    float* QD = UT + RR * LDB;
+    float* DT = QD + BC * LDB;
+    float* DrT = DT + RR * LDB;
+    float* YT = DrT + RR * LDB;
+    float* vec = YT + RR * LDB;
     float *gam = vec, *rr = vec + BC;
 
-    // entry state
-    {
-        const float* src;
-        if (FWD) {
-            src = A.state0 + (head * D + row0) * D;
-        } else {
-            src = A.ckpt + ((head * A.n_ck + blockIdx.y) * D + row0) * D;
-        }
-        for (int idx = tid; idx < RR * (D / 4); idx += CT) {
-            const int j = idx / (D / 4), i4 = idx - j * (D / 4);
-            *reinterpret_cast<float4*>(Ms + j * ld + 4 * i4) =
-                __ldg(reinterpret_cast<const float4*>(src + (long long)j * D) + i4);
-        }
-    }
-    for (int c = c_begin; c < c_end; ++c) {
+    float4 pw[NF], pq[NF], pk[NF], pu, pqd, pgr;
+    auto issue = [&](int c) {
         const ChunkPos cp = chunk_pos(A, c);
         const long long ch = head * A.n_chunks + c;
-        __syncthreads();
-        if (FWD && cp.loc == 0) {  // checkpoint: the state entering segment cp.seg
-            float* dst = A.ckpt_out + ((head * A.n_ck + cp.seg) * D + row0) * D;
-            for (int idx = tid; idx < RR * (D / 4); idx += CT) {
-                const int j = idx / (D / 4), i4 = idx - j * (D / 4);
-                reinterpret_cast<float4*>(dst + (long long)j * D)[i4] =
-                    *reinterpret_cast<const float4*>(Ms + j * ld + 4 * i4);
-            }
-        }
-        if (tid < BC) {
-            gam[tid] = A.ws[A.o_gam + ch * BC + tid];
-            rr[tid] = A.ws[A.o_r + ch * BC + tid];
-        }
-        load_ws(WQ, ld, A.ws + A.o_W + ch * (BC * D), BC, D, tid);
-        for (int idx = tid; idx < BC * (RR / 4); idx += CT) {  // U[:, own rows]
-            const int t = idx / (RR / 4), j4 = idx - t * (RR / 4);
-            *reinterpret_cast<float4*>(Us + t * LDR + 4 * j4) = __ldg(
-                reinterpret_cast<const float4*>(A.ws + A.o_U + ch * (BC * D) + t * D + row0) + j4);
-        }
-        __syncthreads();
+        const float* w = A.ws + A.o_W + ch * (BC * D);
+#pragma unroll
+        for (int kk = 0; kk < NF; ++kk) pw[kk] = __ldg(reinterpret_cast<const float4*>(w) + tid + CT * kk);
         const long long tk = (long long)n * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
-        load_rows_pad(RK, ld, A.k + tk, A.ks1, cp.nb, D, A.vec_k, tid, rr);
+        pf_rows<D>(pk, A.k + tk, A.ks1, cp.nb, A.vec_k, tid);
         if (FWD) {
-            const long long tq =
-                (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
-            load_rows_pad(WQ + BC * ld, ld, A.q + tq, A.qs1, cp.nb, D, A.vec_q, tid, gam);
-            load_ws(QD, LDB, A.ws + A.o_QKD + ch * (BC * BC), BC, BC, tid);
+            const long long tq = (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
+            pf_rows<D>(pq, A.q + tq, A.qs1, cp.nb, A.vec_q, tid);
+            pqd = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_QKD + ch * (BC * BC)) + tid);
         }
-        __syncthreads();
-        const float gl = gam[BC - 1];
-        // [W M^T ; gamma Q M^T]  (2BC x RR)  -> Delta = U - W M^T,  Y1
-        {
-            constexpr int MR = FWD ? 2 * BC : BC;
-            using Map = GemmMap<MR, RR, MR / 16, 2, true>;
-            float acc[MR / 16][2];
-            zero_acc(acc);
-            block_gemm<MR, RR, MR / 16, 2, false, true>(acc, WQ, ld, Ms, ld, D, tid);
-#pragma unroll
-            for (int i = 0; i < MR / 16; ++i) {
-                const int m = Map::row(tid, i);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int nn = Map::col(tid, j);
-                    if (m < BC)
-                        Dls[m * LDR + nn] = __fsub_rn(Us[m * LDR + nn], acc[i][j]);
-                    else
-                        Y1[(m - BC) * LDR + nn] = acc[i][j];
-                }
-            }
+        pu = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (tid < nr * (BC / 4))
+            pu = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_U + ch * (BC * D) + row0 * BC) + tid);
+        if (tid < 8)
+            pgr = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_gam + ch * BC) + tid);
+        else if (tid < 16)
+            pgr = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_r + ch * BC) + tid - 8);
+    };
+    auto commit = [&]() {
+        put_rows<D>(WQs, ld, pw, tid);
+        put_rows<D>(Ks, ld, pk, tid);
+        if (FWD) {
+            put_rows<D>(WQs + BC * ld, ld, pq, tid);
+            *reinterpret_cast<float4*>(QD + (tid >> 3) * LDB + 4 * (tid & 7)) = pqd;
         }
-        __syncthreads();
-        if (FWD) {  // Y = scale (Y1 + lower(QK^T (.) Dm) Delta)
-            using Map = GemmMap<BC, RR, 1, 4, false>;
-            float acc[1][4];
-            zero_acc(acc);
-            block_gemm<BC, RR, 1, 4, false, false>(acc, QD, LDB, Dls, LDR, BC, tid);
-            const int t = Map::row(tid, 0);
-            if (t < cp.nb) {
-                float* yrow = A.y + (((long long)n * A.T + cp.t0 + t) * A.H_v + h) * D + row0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int nn = Map::col(tid, j);
-                    yrow[nn] = __fmul_rn(A.scale, __fadd_rn(Y1[t * LDR + nn], acc[0][j]));
-                }
-            }
-        }
-        {  // M_end = gamma_last M + Delta^T (r (.) K)   (RR x D)
-            using Map = GemmMap<RR, D, TM3, 4, false>;
-            float acc[TM3][4];
-            zero_acc(acc);
-            block_gemm<RR, D, TM3, 4, true, false>(acc, Dls, LDR, RK, ld, BC, tid);
-#pragma unroll
-            for (int i = 0; i < TM3; ++i) {
-                const int j = Map::row(tid, i);
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int ii = Map::col(tid, jj);
-                    Ms[j * ld + ii] = __fmaf_rn(gl, Ms[j * ld + ii], acc[i][jj]);
-                }
-            }
-        }
-        if (!FWD) {  // park the entry state of chunk c + 1
-            __syncthreads();
-            float* dst = A.ws + A.o_Mc + (ch + 1) * (long long)(D * D) + (long long)row0 * D;
-            for (int idx = tid; idx < RR * (D / 4); idx += CT) {
-                const int j = idx / (D / 4), i4 = idx - j * (D / 4);
-                reinterpret_cast<float4*>(dst + (long long)j * D)[i4] =
-                    *reinterpret_cast<const float4*>(Ms + j * ld + 4 * i4);
-            }
-        }
-    }
-    if (FWD) {
-        __syncthreads();
-        float* dst = A.state_T + (head * D + row0) * D;
-        for (int idx = tid; idx < RR * (D / 4); idx += CT) {
+        if (tid < RR * (BC / 4)) *reinterpret_cast<float4*>(UT + (tid >> 3) * LDB + 4 * (tid & 7)) = pu;
+        if (tid < 8)
+            reinterpret_cast<float4*>(gam)[tid] = pgr;
+        else if (tid < 16)
+            reinterpret_cast<float4*>(rr)[tid - 8] = pgr;
+    };
+    auto copy_state = [&](float* dst) {  // Ms -> global rows [row0, row0 + nr)
+        for (int idx = tid; idx < nr * (D / 4); idx += CT) {
             const int j = idx / (D / 4), i4 = idx - j * (D / 4);
             reinterpret_cast<float4*>(dst + (long long)j * D)[i4] =
                 *reinterpret_cast<const float4*>(Ms + j * ld + 4 * i4);
         }
+    };
+
+    {  // entry state
+        const float* src = FWD ? A.state0 + (head * D + row0) * D
+                               : A.ckpt + ((head * A.n_ck + blockIdx.y) * D + row0) * D;
+        for (int idx = tid; idx < RR * (D / 4); idx += CT) {
+            const int j = idx / (D / 4), i4 = idx - j * (D / 4);
+            *reinterpret_cast<float4*>(Ms + j * ld + 4 * i4) =
+                j < nr ? __ldg(reinterpret_cast<const float4*>(src + (long long)j * D) + i4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    issue(c_begin);
+    int y_t0 = 0, y_nb = 0;  // the chunk whose Y^T is staged in YT
+    auto write_y = [&]() {
+        for (int idx = tid; idx < y_nb * nr; idx += CT) {
+            const int t = idx / nr, j = idx - t * nr;
+            A.y[(((long long)n * A.T + y_t0 + t) * A.H_v + h) * D + row0 + j] = YT[j * LDB + t];
+        }
+    };
+    for (int c = c_begin; c < c_end; ++c) {
+        const ChunkPos cp = chunk_pos(A, c);
+        __syncthreads();
+        if (FWD && y_nb > 0) write_y();
+        if (!FWD && c > c_begin) copy_state(A.ws + A.o_Mc + (head * A.n_chunks + c) * (long long)(D * D) + (long long)row0 * D);
+        commit();
+        if (c + 1 < c_end) issue(c + 1);
+        if (FWD && cp.loc == 0) copy_state(A.ckpt_out + ((head * A.n_ck + cp.seg) * D + row0) * D);
+        __syncthreads();
+        {  // [W M^T; Q M^T]^T  (RR x 2BC, or RR x BC)
+            constexpr int NN = FWD ? 2 * BC : BC;
+            constexpr int TN = NN / 32;
+            using Map = GemmMap<RR, NN, TM1, TN, true>;
+            float acc[TM1][TN];
+            zero_acc(acc);
+            block_gemm<RR, NN, TM1, TN, false, true>(acc, Ms, ld, WQs, ld, D, tid);
+#pragma unroll
+            for (int i = 0; i < TM1; ++i) {
+                const int j = Map::row(tid, i);
+#pragma unroll
+                for (int jj = 0; jj < TN; ++jj) {
+                    const int t = Map::col(tid, jj);
+                    if (t < BC) {
+                        const float d = __fsub_rn(UT[j * LDB + t], acc[i][jj]);
+                        DT[j * LDB + t] = d;
+                        DrT[j * LDB + t] = __fmul_rn(rr[t], d);
+                    } else {
+                        YT[j * LDB + t - BC] = __fmul_rn(gam[t - BC], acc[i][jj]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        if (FWD) {  // Y^T += (QD Delta)^T,  then scale
+            using Map = GemmMap<RR, BC, TM1, 1, true>;
+            float acc[TM1][1];
+            zero_acc(acc);
+            block_gemm<RR, BC, TM1, 1, false, true>(acc, DT, LDB, QD, LDB, BC, tid);
+#pragma unroll
+            for (int i = 0; i < TM1; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 1; ++jj) {
+                    const int j = Map::row(tid, i), t = Map::col(tid, jj);
+                    YT[j * LDB + t] = __fmul_rn(A.scale, __fadd_rn(YT[j * LDB + t], acc[i][jj]));
+                }
+            y_t0 = cp.t0;
+            y_nb = cp.nb;
+        }
+        {  // M <- gamma_last M + (r (.) Delta)^T K
+            const float gl = gam[BC - 1];
+            using Map = GemmMap<RR, D, TM3, 4, false>;
+            float acc[TM3][4];
+            zero_acc(acc);
+            block_gemm<RR, D, TM3, 4, false, false>(acc, DrT, LDB, Ks, ld, BC, tid);
+#pragma unroll
+            for (int i = 0; i < TM3; ++i) {
+                float4* mp = reinterpret_cast<float4*>(Ms + Map::row(tid, i) * ld + Map::col(tid, 0));
+                float4 m = *mp;
+                m.x = __fmaf_rn(gl, m.x, acc[i][0]);
+                m.y = __fmaf_rn(gl, m.y, acc[i][1]);
+                m.z = __fmaf_rn(gl, m.z, acc[i][2]);
+                m.w = __fmaf_rn(gl, m.w, acc[i][3]);
+                *mp = m;
+            }
+        }
+    }
+    __syncthreads();
+    if (FWD) {
+        write_y();
+        copy_state(A.state_T + (head * D + row0) * D);
+    } else {
+        copy_state(A.ws + A.o_Mc + (head * A.n_chunks + c_end) * (long long)(D * D) + (long long)row0 * D);
     }
 }
 
 // ---------------------------------------------------------------------------------
-// The dM chain in reverse, rows [p RR, p RR + RR) of one head.  Per chunk:
-//   dDelta = r (.) (K dM^T) + scale QKD^T dY
-//   dX     = T^T dDelta
-//   dM    <- gamma_last dM + dY^T (scale gamma Q) - dX^T (gamma K)
-// Parks dM (as it enters the chunk from the right), dDelta and dX in the workspace.
+// The dM chain in reverse, rows [p RR, p RR + RR) of one head.  Per chunk (dDelta^T and
+// dX^T kept transposed, rows j):
+//   dDelta^T = (r (.) (K dM^T))^T + scale (QD^T dY)^T
+//   dX^T     = (T^T dDelta)^T
+//   dM      <- gamma_last dM + [scale gamma (.) dY ; -gamma (.) dX]^T [Q; K]
+// Parks dM (as it enters the chunk from the right), dDelta^T and dX^T for the gradient
+// kernel.  The next chunk's operands are loaded into registers while the current one
+// computes.
 template <int D>
 __global__ void __launch_bounds__(CT) gdn_chunk_dstate_kernel(const ChunkArgs A)
 {
     constexpr int ld = Ld<D>::v;
-    constexpr int TM4 = D / 32;
+    constexpr int NF = D / 32;
+    constexpr int RR = Rows<D>::RR;
+    constexpr int TM1 = RR / 8;
+    constexpr int TM4 = RR * D / 1024;
+    constexpr int LDA = 2 * BC + 4;
     const int tid = threadIdx.x, p = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int hk = h % A.H_k;
     const long long head = (long long)n * A.H_v + h;
     const int row0 = p * RR;
-
+    const int nr = min(RR, D - row0);  // real rows of this CTA
     extern __shared__ __align__(16) float sm[];
     float* dMs = sm;                   // RR x ld
-    float* Ks = dMs + RR * ld;         // BC x ld (raw k)
-    float* Bst = Ks + BC * ld;         // [scale gamma Q; gamma K]  2BC x ld
-    float* DYX = Bst + 2 * BC * ld;    // [dY; -dX]  2BC x LDR (own rows)
-    float* dDs = DYX + 2 * BC * LDR;   // BC x LDR
-    float* Ts = dDs + BC * LDR;        // BC x LDB
-    float* QD = Ts + BC * LDB;         // BC x LDB
-    float* vec = QD + BC * LDB;
-    float *gam = vec, *rr = vec + BC, *sgam = vec + 2 * BC;
+    float* QKs = dMs + RR * ld;        // [Q; K]  2BC x ld
+    float* dYT = QKs + 2 * BC * ld;    // RR x LDB each:
+    float* QDT = dYT + RR * LDB;
+    float* TT = QDT + BC * LDB;
+    float* dDT = TT + BC * LDB;
+    float* Ap = dDT + RR * LDB;        // RR x LDA
+    float* vec = Ap + RR * LDA;
+    float *gam = vec, *rr = vec + BC;
+
+    float4 pq[NF], pk[NF], pdy, pqt, ptt, pgr;
+    auto issue = [&](int c) {
+        const ChunkPos cp = chunk_pos(A, c);
+        const long long ch = head * A.n_chunks + c;
+        const long long tk = (long long)n * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
+        const long long tq = (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
+        pf_rows<D>(pk, A.k + tk, A.ks1, cp.nb, A.vec_k, tid);
+        pf_rows<D>(pq, A.q + tq, A.qs1, cp.nb, A.vec_q, tid);
+        {  // dY rows t, own columns: float4 index tid -> (t, j4), RR/4 float4 per row
+            const int t = tid / (RR / 4), j4 = tid - t * (RR / 4);
+            pdy = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (tid < BC * (RR / 4) && t < cp.nb && 4 * j4 < nr) {
+                const float* g = A.gy + (long long)n * A.gys0 + (long long)(cp.t0 + t) * A.gys1 +
+                                 (long long)h * A.gys2 + row0 + 4 * j4;
+                pdy = A.vec_gy ? __ldg(reinterpret_cast<const float4*>(g))
+                               : make_float4(__ldg(g), __ldg(g + 1), __ldg(g + 2), __ldg(g + 3));
+            }
+        }
+        pqt = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_QDT + ch * (BC * BC)) + tid);
+        ptt = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_T + ch * (BC * BC)) + tid);
+        if (tid < 8)
+            pgr = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_gam + ch * BC) + tid);
+        else if (tid < 16)
+            pgr = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_r + ch * BC) + tid - 8);
+    };
+    auto commit = [&]() {
+        put_rows<D>(QKs, ld, pq, tid);
+        put_rows<D>(QKs + BC * ld, ld, pk, tid);
+        if (tid < BC * (RR / 4)) {
+            const int t = tid / (RR / 4), j = 4 * (tid - t * (RR / 4));
+            dYT[(j + 0) * LDB + t] = pdy.x;
+            dYT[(j + 1) * LDB + t] = pdy.y;
+            dYT[(j + 2) * LDB + t] = pdy.z;
+            dYT[(j + 3) * LDB + t] = pdy.w;
+        }
+        *reinterpret_cast<float4*>(QDT + (tid >> 3) * LDB + 4 * (tid & 7)) = pqt;
+        *reinterpret_cast<float4*>(TT + (tid >> 3) * LDB + 4 * (tid & 7)) = ptt;
+        if (tid < 8)
+            reinterpret_cast<float4*>(gam)[tid] = pgr;
+        else if (tid < 16)
+            reinterpret_cast<float4*>(rr)[tid - 8] = pgr;
+    };
 
     for (int idx = tid; idx < RR * (D / 4); idx += CT) {
         const int j = idx / (D / 4), i4 = idx - j * (D / 4);
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (A.dstate_T)
+        if (A.dstate_T && j < nr)
             x = __ldg(reinterpret_cast<const float4*>(A.dstate_T + (head * D + row0 + j) * D) + i4);
         *reinterpret_cast<float4*>(dMs + j * ld + 4 * i4) = x;
     }
+    issue(A.n_chunks - 1);
+    using MapS = GemmMap<RR, BC, TM1, 1, true>;
     for (int c = A.n_chunks - 1; c >= 0; --c) {
-        const ChunkPos cp = chunk_pos(A, c);
         const long long ch = head * A.n_chunks + c;
         __syncthreads();
-        if (tid < BC) {
-            const float gm = A.ws[A.o_gam + ch * BC + tid];
-            gam[tid] = gm;
-            sgam[tid] = __fmul_rn(A.scale, gm);
-            rr[tid] = A.ws[A.o_r + ch * BC + tid];
-        }
+        commit();
+        if (c > 0) issue(c - 1);
         {  // park dM (the gradient of this chunk's end state)
             float* dst = A.ws + A.o_dM + ch * (long long)(D * D) + (long long)row0 * D;
-            for (int idx = tid; idx < RR * (D / 4); idx += CT) {
+            for (int idx = tid; idx < nr * (D / 4); idx += CT) {
                 const int j = idx / (D / 4), i4 = idx - j * (D / 4);
                 reinterpret_cast<float4*>(dst + (long long)j * D)[i4] =
                     *reinterpret_cast<const float4*>(dMs + j * ld + 4 * i4);
             }
         }
-        load_ws(Ts, LDB, A.ws + A.o_T + ch * (BC * BC), BC, BC, tid);
-        load_ws(QD, LDB, A.ws + A.o_QKD + ch * (BC * BC), BC, BC, tid);
-        const long long tgy =
-            (long long)n * A.gys0 + (long long)cp.t0 * A.gys1 + (long long)h * A.gys2 + row0;
-        load_rows_pad(DYX, LDR, A.gy + tgy, A.gys1, cp.nb, RR, A.vec_gy, tid);
         __syncthreads();
-        const long long tk = (long long)n * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
-        const long long tq = (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
-        load_rows_pad(Ks, ld, A.k + tk, A.ks1, cp.nb, D, A.vec_k, tid);
-        load_rows_pad(Bst, ld, A.q + tq, A.qs1, cp.nb, D, A.vec_q, tid, sgam);
-        load_rows_pad(Bst + BC * ld, ld, A.k + tk, A.ks1, cp.nb, D, A.vec_k, tid, gam);
-        __syncthreads();
-        {  // dDelta = r (.) (K dM^T)
-            using Map = GemmMap<BC, RR, 2, 2, true>;
-            float acc[2][2];
+        {  // dDelta^T = r (.) (dM K^T) + scale dY^T QD
+            float acc[TM1][1], acc2[TM1][1];
             zero_acc(acc);
-            block_gemm<BC, RR, 2, 2, false, true>(acc, Ks, ld, dMs, ld, D, tid);
+            zero_acc(acc2);
+            block_gemm<RR, BC, TM1, 1, false, true>(acc, dMs, ld, QKs + BC * ld, ld, D, tid);
+            block_gemm<RR, BC, TM1, 1, false, true>(acc2, dYT, LDB, QDT, LDB, BC, tid);
+            float* dst = A.ws + A.o_dDel + ch * (BC * D) + (long long)row0 * BC;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int t = Map::row(tid, i);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) dDs[t * LDR + Map::col(tid, j)] = __fmul_rn(rr[t], acc[i][j]);
+            for (int i = 0; i < TM1; ++i) {
+                const int j = MapS::row(tid, i), t = MapS::col(tid, 0);
+                const float val = __fmaf_rn(A.scale, acc2[i][0], __fmul_rn(rr[t], acc[i][0]));
+                dDT[j * LDB + t] = val;
+                if (j < nr) dst[j * BC + t] = val;
             }
         }
         __syncthreads();
-        {  // dDelta += scale QKD^T dY
-            using Map = GemmMap<BC, RR, 1, 4, false>;
-            float acc[1][4];
+        {  // dX^T = dDelta^T T;  Ap = [scale gamma (.) dY^T | -gamma (.) dX^T]
+            float acc[TM1][1];
             zero_acc(acc);
-            block_gemm<BC, RR, 1, 4, true, false>(acc, QD, LDB, DYX, LDR, BC, tid);
-            const int t = Map::row(tid, 0);
-            float* dst = A.ws + A.o_dDel + ch * (BC * D) + t * D + row0;
+            block_gemm<RR, BC, TM1, 1, false, true>(acc, dDT, LDB, TT, LDB, BC, tid);
+            float* dst = A.ws + A.o_dX + ch * (BC * D) + (long long)row0 * BC;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int nn = Map::col(tid, j);
-                const float val = __fmaf_rn(A.scale, acc[0][j], dDs[t * LDR + nn]);
-                dDs[t * LDR + nn] = val;
-                dst[nn] = val;
+            for (int i = 0; i < TM1; ++i) {
+                const int j = MapS::row(tid, i), t = MapS::col(tid, 0);
+                if (j < nr) dst[j * BC + t] = acc[i][0];
+                Ap[j * LDA + BC + t] = -__fmul_rn(gam[t], acc[i][0]);
+                Ap[j * LDA + t] = __fmul_rn(__fmul_rn(A.scale, gam[t]), dYT[j * LDB + t]);
             }
         }
         __syncthreads();
-        {  // dX = T^T dDelta
-            using Map = GemmMap<BC, RR, 1, 4, false>;
-            float acc[1][4];
-            zero_acc(acc);
-            block_gemm<BC, RR, 1, 4, true, false>(acc, Ts, LDB, dDs, LDR, BC, tid);
-            const int t = Map::row(tid, 0);
-            float* dst = A.ws + A.o_dX + ch * (BC * D) + t * D + row0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int nn = Map::col(tid, j);
-                DYX[(BC + t) * LDR + nn] = -acc[0][j];
-                dst[nn] = acc[0][j];
-            }
-        }
-        __syncthreads();
-        {  // dM <- gamma_last dM + [dY; -dX]^T [scale gamma Q; gamma K]
+        {  // dM <- gamma_last dM + Ap [Q; K]
             const float gl = gam[BC - 1];
             using Map = GemmMap<RR, D, TM4, 4, false>;
             float acc[TM4][4];
             zero_acc(acc);
-            block_gemm<RR, D, TM4, 4, true, false>(acc, DYX, LDR, Bst, ld, 2 * BC, tid);
+            block_gemm<RR, D, TM4, 4, false, false>(acc, Ap, LDA, QKs, ld, 2 * BC, tid);
 #pragma unroll
             for (int i = 0; i < TM4; ++i) {
-                const int j = Map::row(tid, i);
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int ii = Map::col(tid, jj);
-                    dMs[j * ld + ii] = __fmaf_rn(gl, dMs[j * ld + ii], acc[i][jj]);
-                }
+                float4* mp = reinterpret_cast<float4*>(dMs + Map::row(tid, i) * ld + Map::col(tid, 0));
+                float4 m = *mp;
+                m.x = __fmaf_rn(gl, m.x, acc[i][0]);
+                m.y = __fmaf_rn(gl, m.y, acc[i][1]);
+                m.z = __fmaf_rn(gl, m.z, acc[i][2]);
+                m.w = __fmaf_rn(gl, m.w, acc[i][3]);
+                *mp = m;
             }
         }
     }
     __syncthreads();
-    for (int idx = tid; idx < RR * D; idx += CT) {
+    for (int idx = tid; idx < nr * D; idx += CT) {
         const int j = idx / D, i = idx - j * D;
         A.dstate0[(head * D + row0 + j) * D + i] = dMs[j * ld + i];
     }
@@ -573,9 +717,9 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
     float* Xs = MB + D * ld;          // V, then X
     float* Dls = Xs + BC * ld;        // Delta
     float* dYs = Dls + BC * ld;       // dY
-    float* dXs = dYs + BC * ld;       // dX
-    float* dDs = dXs + BC * ld;       // dDelta
-    float* Dm = dDs + BC * ld;        // BC x LDB each:
+    float* dXT = dYs + BC * ld;       // dX^T   D x LDB
+    float* dDT = dXT + D * LDB;       // dDelta^T  D x LDB
+    float* Dm = dDT + D * LDB;        // BC x LDB each:
     float* KKm = Dm + BC * LDB;
     float* QKm = KKm + BC * LDB;
     float* Zs = QKm + BC * LDB;
@@ -586,7 +730,7 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
     float* W1 = dTs + BC * LDB;       // dZ, then dA
     float* W2 = dTs;                  // P1 = dZ Z^T (dT is dead by then)
     float* vec = W1 + BC * LDB;
-    float *gs = vec, *bs = vec + BC, *Gs = vec + 2 * BC, *gam = vec + 3 * BC;
+    float *gs = vec, *bs = vec + BC, *gam = vec + 3 * BC;
     float *dgam = vec + 4 * BC, *dr = vec + 5 * BC, *dG = vec + 6 * BC, *dbs = vec + 7 * BC;
     float* red = vec + 8 * BC;        // CT/32 partials
 
@@ -611,15 +755,20 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
             load_rows_pad(Xs, ld, A.v + tv, A.vs1, cp.nb, D, A.vec_v, tid);
             const long long tg = (long long)n * A.gys0 + (long long)cp.t0 * A.gys1 + (long long)h * A.gys2;
             load_rows_pad(dYs, ld, A.gy + tg, A.gys1, cp.nb, D, A.vec_gy, tid);
-            load_ws(dXs, ld, A.ws + A.o_dX + ch * (BC * D), BC, D, tid);
-            load_ws(dDs, ld, A.ws + A.o_dDel + ch * (BC * D), BC, D, tid);
+            load_ws(dXT, LDB, A.ws + A.o_dX + ch * (BC * D), D, BC, tid);
+            load_ws(dDT, LDB, A.ws + A.o_dDel + ch * (BC * D), D, BC, tid);
             const float* msrc = (cp.loc == 0)
                                     ? A.ckpt + (head * A.n_ck + cp.seg) * (long long)(D * D)
                                     : A.ws + A.o_Mc + ch * (long long)(D * D);
             load_ws(MB, ld, msrc, D, D, tid);
         }
+        load_ws(Ts, LDB, A.ws + A.o_Tr + ch * (BC * BC), BC, BC, tid);
+        load_ws(Zs, LDB, A.ws + A.o_Z + ch * (BC * BC), BC, BC, tid);
+        load_ws(KKm, LDB, A.ws + A.o_KK + ch * (BC * BC), BC, BC, tid);
+        load_ws(QKm, LDB, A.ws + A.o_QK + ch * (BC * BC), BC, BC, tid);
+        load_ws(Dm, LDB, A.ws + A.o_Dm + ch * (BC * BC), BC, BC, tid);
+        if (tid < BC) gam[tid] = __ldg(A.ws + A.o_gam + ch * BC + tid);
         __syncthreads();
-        chunk_prep<D>(QKs, gs, bs, Gs, gam, Dm, KKm, QKm, Zs, Ts, tid);
 
         float hq[TM][4], hkk[TM][4];
         {  // X = V - gamma (.) K M^T
@@ -641,20 +790,32 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
             float acc[TM][4], acc2[TM][4];
             zero_acc(acc);
             zero_acc(acc2);
-            block_gemm<BC, D, TM, 4, false, false>(acc, dYs, ld, MB, ld, D, tid);
-            block_gemm<BC, D, TM, 4, false, false>(acc2, dXs, ld, MB, ld, D, tid);
+            block_gemm_dual<BC, D, TM, 4, false, true, false>(acc, dYs, ld, acc2, dXT, LDB, MB, ld,
+                                                              D, tid);
 #pragma unroll
             for (int i = 0; i < TM; ++i) {
                 const int t = MapQ::row(tid, i);
+                const int c0 = MapQ::col(tid, 0);
+                const float4 qv = *reinterpret_cast<const float4*>(QKs + t * ld + c0);
+                const float4 kv = *reinterpret_cast<const float4*>(Ks + t * ld + c0);
+                const float sg = __fmul_rn(A.scale, gam[t]);
+                hq[i][0] = __fmul_rn(sg, acc[i][0]);
+                hq[i][1] = __fmul_rn(sg, acc[i][1]);
+                hq[i][2] = __fmul_rn(sg, acc[i][2]);
+                hq[i][3] = __fmul_rn(sg, acc[i][3]);
+                hkk[i][0] = -__fmul_rn(gam[t], acc2[i][0]);
+                hkk[i][1] = -__fmul_rn(gam[t], acc2[i][1]);
+                hkk[i][2] = -__fmul_rn(gam[t], acc2[i][2]);
+                hkk[i][3] = -__fmul_rn(gam[t], acc2[i][3]);
                 float part = 0.f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int ii = MapQ::col(tid, j);
-                    hq[i][j] = __fmul_rn(__fmul_rn(A.scale, gam[t]), acc[i][j]);
-                    hkk[i][j] = -__fmul_rn(gam[t], acc2[i][j]);
-                    part = __fmaf_rn(__fmul_rn(A.scale, QKs[t * ld + ii]), acc[i][j], part);
-                    part = __fmaf_rn(-Ks[t * ld + ii], acc2[i][j], part);
-                }
+                part = __fmaf_rn(__fmul_rn(A.scale, qv.x), acc[i][0], part);
+                part = __fmaf_rn(-kv.x, acc2[i][0], part);
+                part = __fmaf_rn(__fmul_rn(A.scale, qv.y), acc[i][1], part);
+                part = __fmaf_rn(-kv.y, acc2[i][1], part);
+                part = __fmaf_rn(__fmul_rn(A.scale, qv.z), acc[i][2], part);
+                part = __fmaf_rn(-kv.z, acc2[i][2], part);
+                part = __fmaf_rn(__fmul_rn(A.scale, qv.w), acc[i][3], part);
+                part = __fmaf_rn(-kv.w, acc2[i][3], part);
                 // row t is spread over the MapQ::NX lanes of one warp segment
 #pragma unroll
                 for (int o = MapQ::NX / 2; o > 0; o >>= 1)
@@ -670,8 +831,8 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
             block_gemm<BC, D, TM, 4, false, false>(acc, Ts, LDB, Xs, ld, BC, tid);
 #pragma unroll
             for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) Dls[Map::row(tid, i) * ld + Map::col(tid, j)] = acc[i][j];
+                *reinterpret_cast<float4*>(Dls + Map::row(tid, i) * ld + Map::col(tid, 0)) =
+                    make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
         }
         {  // MB <- dM_end, with <dM_end, M_c> on the way
             float part = 0.f;
@@ -700,13 +861,14 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
             for (int i = 0; i < TM; ++i) {
                 const int t = MapQ::row(tid, i);
                 const float rt = Dm[(BC - 1) * LDB + t];
+                const float4 kv = *reinterpret_cast<const float4*>(Ks + t * ld + MapQ::col(tid, 0));
                 float part = 0.f;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int ii = MapQ::col(tid, j);
-                    hkk[i][j] = __fmaf_rn(rt, acc[i][j], hkk[i][j]);
-                    part = __fmaf_rn(Ks[t * ld + ii], acc[i][j], part);
-                }
+                for (int j = 0; j < 4; ++j) hkk[i][j] = __fmaf_rn(rt, acc[i][j], hkk[i][j]);
+                part = __fmaf_rn(kv.x, acc[i][0], part);
+                part = __fmaf_rn(kv.y, acc[i][1], part);
+                part = __fmaf_rn(kv.z, acc[i][2], part);
+                part = __fmaf_rn(kv.w, acc[i][3], part);
 #pragma unroll
                 for (int o = MapQ::NX / 2; o > 0; o >>= 1)
                     part = __fadd_rn(part, __shfl_xor_sync(kFullMask, part, o));
@@ -719,7 +881,7 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
             zero_acc(acc);
             zero_acc(acc2);
             block_gemm<BC, BC, 2, 2, false, true>(acc, dYs, ld, Dls, ld, D, tid);
-            block_gemm<BC, BC, 2, 2, false, true>(acc2, dDs, ld, Xs, ld, D, tid);
+            block_gemm<BC, BC, 2, 2, true, true>(acc2, dDT, LDB, Xs, ld, D, tid);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int t = Map::row(tid, i);
@@ -847,11 +1009,13 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
                 A.dbeta[tok * A.H_v + h] = dbs[t];
             }
         }
-        for (int idx = tid; idx < cp.nb * (D / 4); idx += CT) {
-            const int t = idx / (D / 4), i4 = idx - t * (D / 4);
+        for (int idx = tid; idx < BC * (D / 4); idx += CT) {
+            const int i4 = idx / BC, t = idx - i4 * BC;
+            if (t >= cp.nb) continue;
             float4* dst = reinterpret_cast<float4*>(
                 A.dv + (((long long)n * A.T + cp.t0 + t) * A.H_v + h) * D);
-            dst[i4] = *reinterpret_cast<const float4*>(dXs + t * ld + 4 * i4);
+            dst[i4] = make_float4(dXT[(4 * i4 + 0) * LDB + t], dXT[(4 * i4 + 1) * LDB + t],
+                                  dXT[(4 * i4 + 2) * LDB + t], dXT[(4 * i4 + 3) * LDB + t]);
         }
     }
     // dq, dk of the key head (value heads summed in ascending order)
@@ -860,12 +1024,9 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
         const int t = MapQ::row(tid, i);
         if (t >= cp.nb) continue;
         const long long row = (((long long)n * A.T + cp.t0 + t) * A.H_k + hk) * D;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int ii = MapQ::col(tid, j);
-            A.dq[row + ii] = aq[i][j];
-            A.dk[row + ii] = ak[i][j];
-        }
+        const int c0 = MapQ::col(tid, 0);
+        *reinterpret_cast<float4*>(A.dq + row + c0) = make_float4(aq[i][0], aq[i][1], aq[i][2], aq[i][3]);
+        *reinterpret_cast<float4*>(A.dk + row + c0) = make_float4(ak[i][0], ak[i][1], ak[i][2], ak[i][3]);
     }
 }
 
@@ -879,19 +1040,21 @@ size_t prep_smem()
 template <int D>
 size_t state_smem()
 {
-    return sizeof(float) * (RR * Ld<D>::v + 3 * BC * Ld<D>::v + 3 * BC * LDR + BC * LDB + 2 * BC);
+    constexpr int RR = Rows<D>::RR;
+    return sizeof(float) * (RR * Ld<D>::v + 3 * BC * Ld<D>::v + 5 * BC * LDB + 2 * BC);
 }
 template <int D>
 size_t dstate_smem()
 {
     return sizeof(float) *
-           (RR * Ld<D>::v + 3 * BC * Ld<D>::v + 3 * BC * LDR + 2 * BC * LDB + 3 * BC);
+           (Rows<D>::RR * Ld<D>::v + 2 * BC * Ld<D>::v + 4 * BC * LDB + Rows<D>::RR * (2 * BC + 4) +
+            2 * BC);
 }
 template <int D>
 size_t grad_smem()
 {
-    return sizeof(float) * (2 * BC * Ld<D>::v + D * Ld<D>::v + 5 * BC * Ld<D>::v +
-                            9 * BC * LDB + 8 * BC + CT / 32);
+    return sizeof(float) * (2 * BC * Ld<D>::v + D * Ld<D>::v + 3 * BC * Ld<D>::v +
+                            2 * D * LDB + 9 * BC * LDB + 8 * BC + CT / 32);
 }
 
 template <typename K>
@@ -915,7 +1078,7 @@ static int chunk_forward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
 {
     tap.mark(s);
     GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks, a.H_v, a.N), prep_smem<D>());
-    GDN_LAUNCH((gdn_chunk_state_kernel<D, true>), dim3(D / RR, a.H_v, a.N), state_smem<D>());
+    GDN_LAUNCH((gdn_chunk_state_kernel<D, true>), dim3(Rows<D>::P, a.H_v, a.N), state_smem<D>());
     return 0;
 }
 
@@ -925,9 +1088,9 @@ static int chunk_backward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
     tap.mark(s);
     GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks, a.H_v, a.N), prep_smem<D>());
     if (a.cps > 1)
-        GDN_LAUNCH((gdn_chunk_state_kernel<D, false>), dim3(D / RR, a.n_ck, a.N * a.H_v),
+        GDN_LAUNCH((gdn_chunk_state_kernel<D, false>), dim3(Rows<D>::P, a.n_ck, a.N * a.H_v),
                    state_smem<D>());
-    GDN_LAUNCH(gdn_chunk_dstate_kernel<D>, dim3(D / RR, a.H_v, a.N), dstate_smem<D>());
+    GDN_LAUNCH(gdn_chunk_dstate_kernel<D>, dim3(Rows<D>::P, a.H_v, a.N), dstate_smem<D>());
     GDN_LAUNCH(gdn_chunk_grad_kernel<D>, dim3(a.n_chunks, a.H_k, a.N), grad_smem<D>());
     return 0;
 }

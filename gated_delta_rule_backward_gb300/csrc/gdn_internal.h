@@ -98,8 +98,10 @@ struct ChunkArgs {
     int N, T, H_k, H_v, C, n_ck, cps, n_chunks;
     float scale;
     // workspace sub-arrays (float offsets from ws), per (sequence, value head, chunk)
-    long long o_T, o_QKD, o_gam, o_r, o_W, o_U, o_Mc, o_dM, o_dDel, o_dX;
+    long long o_T, o_QKD, o_QDT, o_gam, o_r, o_W, o_U, o_Mc, o_dM, o_dDel, o_dX;
+    long long o_Tr, o_Z, o_KK, o_QK, o_Dm;  // backward: chunk factors for the gradient kernel
     int want_wu;
+    int want_factors;
     int vec_q, vec_k, vec_v, vec_gy;
 };
 
