@@ -816,11 +816,10 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
                 part = __fmaf_rn(-kv.z, acc2[i][2], part);
                 part = __fmaf_rn(__fmul_rn(A.scale, qv.w), acc[i][3], part);
                 part = __fmaf_rn(-kv.w, acc2[i][3], part);
-                // row t is spread over the MapQ::NX lanes of one warp segment
-#pragma unroll
-                for (int o = MapQ::NX / 2; o > 0; o >>= 1)
-                    part = __fadd_rn(part, __shfl_xor_sync(kFullMask, part, o));
-                if ((tid % MapQ::NX) == 0) dgam[t] = part;
+                // row t: 4 lanes of the warp (lane bits 0-1), then the warp columns
+                part = __fadd_rn(part, __shfl_xor_sync(kFullMask, part, 1));
+                part = __fadd_rn(part, __shfl_xor_sync(kFullMask, part, 2));
+                if ((tid & 3) == 0) Ss[MapQ::wc(tid) * LDB + t] = part;
             }
         }
         __syncthreads();
@@ -869,10 +868,9 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
                 part = __fmaf_rn(kv.y, acc[i][1], part);
                 part = __fmaf_rn(kv.z, acc[i][2], part);
                 part = __fmaf_rn(kv.w, acc[i][3], part);
-#pragma unroll
-                for (int o = MapQ::NX / 2; o > 0; o >>= 1)
-                    part = __fadd_rn(part, __shfl_xor_sync(kFullMask, part, o));
-                if ((tid % MapQ::NX) == 0) dr[t] = part;
+                part = __fadd_rn(part, __shfl_xor_sync(kFullMask, part, 1));
+                part = __fadd_rn(part, __shfl_xor_sync(kFullMask, part, 2));
+                if ((tid & 3) == 0) Ss[(8 + MapQ::wc(tid)) * LDB + t] = part;
             }
         }
         {  // dQKD = lower(scale dY Delta^T);  dT = dDelta X^T
@@ -903,6 +901,14 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
             float s = 0.f;
             for (int t = tid; t < BC; ++t) s = __fmaf_rn(Zs[t * LDB + tid], dTs[t * LDB + tid], s);
             dbs[tid] = s;
+            // gather the per-warp-column partials of dgam and dr
+            float g = 0.f, rsum = 0.f;
+            for (int w = 0; w < MapQ::WGC; ++w) {
+                g = __fadd_rn(g, Ss[w * LDB + tid]);
+                rsum = __fadd_rn(rsum, Ss[(8 + w) * LDB + tid]);
+            }
+            dgam[tid] = g;
+            dr[tid] = rsum;
         }
         __syncthreads();
         {  // P1 = dZ Z^T

@@ -77,8 +77,9 @@ def test_kda_d128_T16384_sampled():
         H.compare_group(gpu, prob, n, hk, prob.C)
 
 
-def test_run_to_run_bit_identical():
-    prob = synth.make_problem(2, 300, 2, 6, 128, kda=True, seed=41, C=17, packed=True,
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+def test_run_to_run_bit_identical(kda):
+    prob = synth.make_problem(2, 300, 2, 6, 128, kda=kda, seed=41, C=17, packed=True,
                               dstate_T=True)
     dev = H.upload(prob)
     a, pa = H.run_gpu(prob, dev=dev)
@@ -118,8 +119,9 @@ def test_strided_views_equal_contiguous_copies():
     assert np.array_equal(a["y"], b["y"])
 
 
-def test_broadcast_equals_explicit_replication():
-    prob = synth.make_problem(1, 120, 2, 6, 64, kda=True, seed=44, C=11, dstate_T=True)
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+def test_broadcast_equals_explicit_replication(kda):
+    prob = synth.make_problem(1, 120, 2, 6, 64, kda=kda, seed=44, C=11, dstate_T=True)
     dev = H.upload(prob)
     a, _ = H.run_gpu(prob, dev=dev)
     hk = torch.arange(6, device="cuda") % 2
@@ -137,8 +139,25 @@ def test_broadcast_equals_explicit_replication():
             assert np.array_equal(acc, a[k][:, :, h]), (k, h)
 
 
-def test_single_token():
-    prob = synth.make_problem(1, 1, 1, 2, 32, kda=True, seed=45, dstate_T=True)
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+def test_single_token(kda):
+    prob = synth.make_problem(1, 1, 1, 2, 32, kda=kda, seed=45, dstate_T=True)
+    full_check(prob)
+
+
+def test_chunk_boundaries_and_long_segments():
+    """Scalar gate: C = 100 (4 chunks per segment, ragged last chunk in every segment),
+    T = 333 (ragged last segment), head size 128, broadcast r = 3."""
+    prob = synth.make_problem(1, 333, 2, 6, 128, kda=False, seed=48, C=100, packed=True,
+                              dstate_T=True)
+    full_check(prob)
+
+
+def test_strong_decay_scalar_gate():
+    """g = -softplus(N(0, 2^2)): gamma underflows inside chunks; the chunked form only
+    ever evaluates exp(G_t - G_tau) <= 1."""
+    prob = synth.make_problem(2, 256, 2, 4, 64, kda=False, seed=49, g_std=2.0, C=64,
+                              dstate_T=True)
     full_check(prob)
 
 
