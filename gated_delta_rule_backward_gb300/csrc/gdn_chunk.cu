@@ -31,6 +31,7 @@
 
 #include "gdn_gemm.cuh"
 #include "gdn_internal.h"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 
@@ -237,6 +238,70 @@ __device__ __forceinline__ void load_gate_beta(const ChunkArgs& A, int n, int h,
     }
 }
 
+// Tensor-core operands of one (chunk, head) for the state chain at head size 128, in the
+// operand layout of gdn_tc.cuh: B1 = [W; Q] (64 x 128) and B23 = [scale QD; (r K)^T]
+// (160 x 32) as tf32 hi then lo, and U^T (rows j, 32 tokens) in fp32.  W = T diag(gamma) K,
+// U = T V.  Vs holds V on entry and stages U afterwards.
+template <int D>
+__device__ void prep_tc_operands(const ChunkArgs& A, long long ch, const float* QKs, float* Vs,
+                                 const float* TG, const float* Ts, const float* QKm,
+                                 const float* Dm, int tid)
+{
+    constexpr int ld = Ld<D>::v;
+    constexpr int TM = D / 32;
+    using Map = GemmMap<BC, D, TM, 4, false>;
+    const float* Ks = QKs + BC * ld;
+    float* b1 = A.ws + A.o_B1 + ch * kTcB1Elems;
+    float* b23 = A.ws + A.o_B23 + ch * kTcB23Elems;
+    float* u = A.ws + A.o_U + ch * (BC * D);
+    auto put = [](float* hi_base, int half, int unit, float4 x) {
+        uint4 hi, lo;
+        tc::split_tf32(x.x, hi.x, lo.x);
+        tc::split_tf32(x.y, hi.y, lo.y);
+        tc::split_tf32(x.z, hi.z, lo.z);
+        tc::split_tf32(x.w, hi.w, lo.w);
+        *reinterpret_cast<uint4*>(hi_base + 4 * unit) = hi;
+        *reinterpret_cast<uint4*>(hi_base + half + 4 * unit) = lo;
+    };
+    float acc[TM][4];
+    zero_acc(acc);
+    block_gemm<BC, D, TM, 4, false, false>(acc, Ts, LDB, Vs, ld, BC, tid);  // U = T V
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+        *reinterpret_cast<float4*>(Vs + Map::row(tid, i) * ld + Map::col(tid, 0)) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    zero_acc(acc);
+    block_gemm<BC, D, TM, 4, false, false>(acc, TG, LDB, Ks, ld, BC, tid);  // W
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {  // rows t of B1, 4 consecutive k per thread
+        const int t = Map::row(tid, i), c0 = Map::col(tid, 0);
+        put(b1, kTcB1Elems / 2, (c0 >> 2) * 64 + t, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+    }
+    for (int idx = tid; idx < BC * (D / 4); idx += CT) {  // rows 32 + t of B1: Q
+        const int t = idx % BC, kc = idx / BC;
+        put(b1, kTcB1Elems / 2, kc * 64 + BC + t, *reinterpret_cast<const float4*>(QKs + t * ld + 4 * kc));
+    }
+    for (int idx = tid; idx < 160 * (BC / 4); idx += CT) {  // B23, unit = kc * 160 + row
+        const int r = idx % 160, kc = idx / 160;
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int tau = 4 * kc + e;
+            x[e] = (r < BC) ? __fmul_rn(A.scale, __fmul_rn(QKm[r * LDB + tau], Dm[r * LDB + tau]))
+                            : __fmul_rn(Dm[(BC - 1) * LDB + tau], Ks[tau * ld + r - BC]);
+        }
+        put(b23, kTcB23Elems / 2, idx, make_float4(x[0], x[1], x[2], x[3]));
+    }
+    __syncthreads();
+    for (int idx = tid; idx < (BC / 4) * D; idx += CT) {  // U^T, unit = b * 128 + j
+        const int j = idx % D, b = idx / D;
+        *reinterpret_cast<float4*>(u + 4 * idx) =
+            make_float4(Vs[(4 * b) * ld + j], Vs[(4 * b + 1) * ld + j], Vs[(4 * b + 2) * ld + j],
+                        Vs[(4 * b + 3) * ld + j]);
+    }
+}
+
 // ---------------------------------------------------------------------------------
 // Prep: one CTA per (chunk, value head, sequence).
 template <int D>
@@ -305,6 +370,12 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
     }
     if (!A.want_wu) return;
     __syncthreads();
+    if constexpr (D == 128) {
+        if (A.want_tc) {
+            prep_tc_operands<D>(A, ch, QKs, Vs, TG, Ts, QKm, Dm, tid);
+            return;
+        }
+    }
     // W = T diag(gamma) K  (BC x D, row-major),  U^T = (T V)^T  (D x BC)
     constexpr int TM = D / 32;
     using Map = GemmMap<BC, D, TM, 4, false>;
@@ -1084,6 +1155,12 @@ static int chunk_forward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
 {
     tap.mark(s);
     GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks, a.H_v, a.N), prep_smem<D>());
+    if (D == 128 && a.want_tc) {
+        const int e = launch_tc_state(a, true, s);
+        if (e) return e;
+        tap.mark(s);
+        return 0;
+    }
     GDN_LAUNCH((gdn_chunk_state_kernel<D, true>), dim3(Rows<D>::P, a.H_v, a.N), state_smem<D>());
     return 0;
 }
@@ -1093,9 +1170,16 @@ static int chunk_backward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
 {
     tap.mark(s);
     GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks, a.H_v, a.N), prep_smem<D>());
-    if (a.cps > 1)
-        GDN_LAUNCH((gdn_chunk_state_kernel<D, false>), dim3(Rows<D>::P, a.n_ck, a.N * a.H_v),
-                   state_smem<D>());
+    if (a.cps > 1) {
+        if (D == 128 && a.want_tc) {
+            const int e = launch_tc_state(a, false, s);
+            if (e) return e;
+            tap.mark(s);
+        } else {
+            GDN_LAUNCH((gdn_chunk_state_kernel<D, false>), dim3(Rows<D>::P, a.n_ck, a.N * a.H_v),
+                       state_smem<D>());
+        }
+    }
     GDN_LAUNCH(gdn_chunk_dstate_kernel<D>, dim3(Rows<D>::P, a.H_v, a.N), dstate_smem<D>());
     GDN_LAUNCH(gdn_chunk_grad_kernel<D>, dim3(a.n_chunks, a.H_k, a.N), grad_smem<D>());
     return 0;

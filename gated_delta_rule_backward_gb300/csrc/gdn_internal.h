@@ -100,8 +100,10 @@ struct ChunkArgs {
     // workspace sub-arrays (float offsets from ws), per (sequence, value head, chunk)
     long long o_T, o_QKD, o_QDT, o_gam, o_r, o_W, o_U, o_Mc, o_dM, o_dDel, o_dX;
     long long o_Tr, o_Z, o_KK, o_QK, o_Dm;  // backward: chunk factors for the gradient kernel
+    long long o_B1, o_B23;                  // tensor-core operands of the state chain
     int want_wu;
     int want_factors;
+    int want_tc;                            // head size 128: state chain on the tensor cores
     int vec_q, vec_k, vec_v, vec_gy;
 };
 
@@ -114,7 +116,18 @@ struct EventTap {
     void mark(void* stream);
 };
 
+// Tensor-core operands of the state chain (head size 128), floats per (chunk, head):
+// [W; Q] as tf32 hi then lo (2 x 64 x 128) and [scale QD; (r K)^T] as hi then lo
+// (2 x 160 x 32), in the operand layout of gdn_tc.cuh.
+constexpr int kTcB1Elems = 2 * 64 * 128;
+constexpr int kTcB23Elems = 2 * 160 * 32;
+
 int launch_chunk_forward(const ChunkArgs& a, int D, void* stream, EventTap& tap);
+// The state chain on the tensor cores (gdn_tc_state.cu): forward or recompute mode.
+int launch_tc_state(const ChunkArgs& a, bool fwd, void* stream);
+// Reads and clears the tensor-core kernels' device status word (0 or GDN_ERR_TIMEOUT),
+// synchronising `stream`.  Returns a cudaError_t as int.
+int tc_take_status(void* stream, int* status);
 int launch_chunk_backward(const ChunkArgs& a, int D, void* stream, EventTap& tap);
 
 // Shared-memory layout of the backward kernel, in floats (every offset a multiple of 4).

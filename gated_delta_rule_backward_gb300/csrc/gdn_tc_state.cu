@@ -1,0 +1,351 @@
+// gdn_tc_state.cu -- the chunked state chain of the scalar gate at head size 128 on the
+// 5th-generation tensor cores (tcgen05, kind::tf32, three-pass split for fp32 accuracy).
+//
+// One CTA owns one head's whole state M (128 x 128, rows j = value index) and walks its
+// chunks in order.  Per chunk (32 tokens; "metal: GATED_DELTA_NET_BACK" row form regrouped
+// by chunks, see gdn_chunk.cu for the derivation):
+//   D1  = M [W; Q]^T                    128 x 64, K = 128    (A = M from TMEM, B = [W; Q])
+//   Delta^T = U^T - D1[:, 0:32]         in registers, split to tf32 hi/lo in shared memory
+//   D23 = Delta^T [scale QD; (r K)^T]^T 128 x 160, K = 32    (A = Delta^T, B from smem)
+//   y^T = scale gamma (.) D1[:, 32:64] + D23[:, 0:32]
+//   M   <- gamma_last M + D23[:, 32:160]
+// M itself stays in registers in fp32 (thread = row j, 64 columns); each chunk it is split
+// into tf32 hi/lo parts written to TMEM as the A operand of the next D1.  The chunk
+// operands ([W; Q], [scale QD; (r K)^T] as tf32 hi/lo, U^T in fp32, gamma) are written by
+// the prep kernel in the tensor-core operand layout and arrive by bulk copies (TMA), the
+// next chunk's as soon as the current one's buffer is free.
+//
+// Modes: forward (grid: head, sequence) writes y, the checkpoints and state_T;
+// recompute (grid: segment, sequence * head) rebuilds the chunk-entry states of one
+// segment from its checkpoint and parks them.  Both run the identical instruction
+// sequence per chunk, so recomputed states equal the forward's bit for bit.
+#include <cuda_runtime.h>
+
+#include "gdn_internal.h"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+// Status word of the tensor-core kernels on this device: 0, or GDN_ERR_TIMEOUT (6) after a
+// bounded wait gave up.  Read and cleared by tc_take_status.
+__device__ int g_tc_status;
+
+namespace {
+
+constexpr int TD = 128;                       // head size
+constexpr int TCT = 288;                      // 8 compute warps (row j, column half) + 1 issuer warp
+constexpr int kIssuer = 256;                  // issues the MMAs and bulk copies
+constexpr uint32_t kColMhi = 0;               // TMEM columns: M hi  (A operand, K = 128)
+constexpr uint32_t kColMlo = 128;             //               M lo
+constexpr uint32_t kColD1 = 256;              //               D1 (64 columns)
+constexpr uint32_t kColD23 = 320;             //               D23 (160 columns)
+constexpr uint32_t kTmemCols = 512;
+constexpr int kStatusTimeout = 6;
+
+// Shared memory, in floats.
+constexpr int kSB1 = 0;                            // [W; Q] hi, lo    2 x 64 x 128
+constexpr int kSB23 = kSB1 + kTcB1Elems;           // [sQD; rK^T] hi, lo  2 x 160 x 32
+constexpr int kSU = kSB23 + kTcB23Elems;           // U^T, operand layout (R = 128), fp32
+constexpr int kSDel = kSU + BC * TD;               // Delta^T hi, lo   2 x 128 x 32
+constexpr int kSGam = kSDel + 2 * BC * TD;         // gamma (32)
+constexpr int kSFloats = kSGam + BC;
+constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 64;   // + barriers
+
+constexpr uint32_t kB1Bytes = sizeof(float) * kTcB1Elems;
+constexpr uint32_t kB23Bytes = sizeof(float) * kTcB23Elems + sizeof(float) * BC * TD + sizeof(float) * BC;
+
+__device__ __forceinline__ void load_b1(const ChunkArgs& A, long long ch, float* sm, uint64_t* bar)
+{
+    tc::mbar_expect_tx(bar, kB1Bytes);
+    tc::bulk_g2s(sm + kSB1, A.ws + A.o_B1 + ch * kTcB1Elems, kB1Bytes, bar);
+}
+
+__device__ __forceinline__ void load_b23(const ChunkArgs& A, long long ch, float* sm, uint64_t* bar)
+{
+    tc::mbar_expect_tx(bar, kB23Bytes);
+    tc::bulk_g2s(sm + kSB23, A.ws + A.o_B23 + ch * kTcB23Elems, sizeof(float) * kTcB23Elems, bar);
+    tc::bulk_g2s(sm + kSU, A.ws + A.o_U + ch * (BC * TD), sizeof(float) * BC * TD, bar);
+    tc::bulk_g2s(sm + kSGam, A.ws + A.o_gam + ch * BC, sizeof(float) * BC, bar);
+}
+
+}  // namespace
+
+template <bool FWD>
+__global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
+{
+    extern __shared__ __align__(1024) float sm[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSFloats);  // b1, b23, mma
+    uint64_t* bar_b1 = bars;
+    uint64_t* bar_b23 = bars + 1;
+    uint64_t* bar_mma = bars + 2;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool compute = warp < 8;          // warps 0-7 hold M; warp 8 issues MMAs and copies
+    const bool issuer = tid == kIssuer;
+    const int j = 32 * (warp & 3) + lane;   // row of M (compute warps)
+    const int hc = (warp >> 2) & 1;         // column half: columns [64 hc, 64 hc + 64)
+
+    int n, h, c_begin, c_end;
+    if (FWD) {
+        h = blockIdx.x;
+        n = blockIdx.y;
+        c_begin = 0;
+        c_end = A.n_chunks;
+    } else {
+        const int hd = blockIdx.y;
+        n = hd / A.H_v;
+        h = hd - n * A.H_v;
+        const int s = blockIdx.x;
+        c_begin = s * A.cps;
+        const int seg_len = min(A.T, s * A.C + A.C) - s * A.C;
+        c_end = c_begin + (seg_len + BC - 1) / BC - 1;  // chunks whose end state is needed
+        if (c_end <= c_begin) return;
+    }
+    const long long head = (long long)n * A.H_v + h;
+
+    if (tid == 0) {
+        tc::mbar_init(bar_b1, 1);
+        tc::mbar_init(bar_b23, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::mbar_fence_init();
+        s_err = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = s_tmem;
+
+    uint32_t ph_b1 = 0, ph_b23 = 0, ph_mma = 0;
+    bool b1_pending = false, b23_pending = false;
+    if (issuer) {
+        load_b1(A, head * A.n_chunks + c_begin, sm, bar_b1);
+        load_b23(A, head * A.n_chunks + c_begin, sm, bar_b23);
+        b1_pending = b23_pending = true;
+    }
+
+    // entry state: this thread's 64 columns of row j
+    float m[64];
+    if (compute) {
+        const float* src = FWD ? A.state0 + (head * TD + j) * TD
+                               : A.ckpt + ((head * A.n_ck + blockIdx.x) * TD + j) * TD;
+        const float4* s4 = reinterpret_cast<const float4*>(src + 64 * hc);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float4 x = __ldg(s4 + q);
+            m[4 * q] = x.x;
+            m[4 * q + 1] = x.y;
+            m[4 * q + 2] = x.z;
+            m[4 * q + 3] = x.w;
+        }
+    }
+    auto store_state = [&](float* dst) {  // row j, this thread's 64 columns
+        float4* d4 = reinterpret_cast<float4*>(dst + (long long)j * TD + 64 * hc);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) d4[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+    };
+    // y^T of the previous chunk (column-half 1 threads), stored while the next chunk's D1 runs
+    float y[32];
+    int y_t0 = 0, y_nb = 0;
+    auto store_y = [&]() {
+        float* yp = A.y + (((long long)n * A.T + y_t0) * A.H_v + h) * TD + j;
+        const long long ys = (long long)A.H_v * TD;
+#pragma unroll
+        for (int t = 0; t < BC; ++t)
+            if (t < y_nb) yp[t * ys] = y[t];
+    };
+
+    const float* sU = sm + kSU;
+    const float* sGam = sm + kSGam;
+    float* sDel = sm + kSDel;
+    const uint32_t id64 = tc::idesc_tf32(64), id160 = tc::idesc_tf32(160);
+
+    int c = c_begin;
+    for (; c < c_end; ++c) {
+        const int seg = c / A.cps;
+        const int loc = c - seg * A.cps;
+        const int t0 = seg * A.C + loc * BC;
+        const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
+        const long long ch = head * A.n_chunks + c;
+        // (1) M -> tf32 hi/lo, the A operand of D1 in TMEM
+        if (compute) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) tc::split_tf32(m[16 * q + e], hi[e], lo[e]);
+                tc::st16(tc::taddr(tmem, warp, kColMhi + 64 * hc + 16 * q), hi);
+                tc::st16(tc::taddr(tmem, warp, kColMlo + 64 * hc + 16 * q), lo);
+            }
+            tc::wait_st();
+        }
+        tc::fence_before();
+        __syncthreads();
+        // (2) D1 = M [W; Q]^T on the tensor cores; meanwhile the pending global stores
+        if (issuer) {
+            tc::fence_after();
+            if (!tc::mbar_wait(bar_b1, ph_b1)) s_err = 1;
+            ph_b1 ^= 1;
+            b1_pending = false;
+            if (!s_err) {
+                const uint64_t bhi = tc::tile_desc(sm + kSB1, 64);
+                const uint64_t blo = tc::tile_desc(sm + kSB1 + kTcB1Elems / 2, 64);
+#pragma unroll
+                for (int s = 0; s < TD / 8; ++s) {
+                    const uint32_t ahi = tmem + kColMhi + 8 * s, alo = tmem + kColMlo + 8 * s;
+                    tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice(bhi, 64, s), id64, s > 0);
+                    tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice(blo, 64, s), id64, 1);
+                    tc::mma_ts(tmem + kColD1, alo, tc::desc_kslice(bhi, 64, s), id64, 1);
+                }
+                tc::commit(bar_mma);
+            }
+        } else if (compute) {
+            if (FWD && hc == 1 && y_nb > 0) store_y();
+            if (FWD && loc == 0) store_state(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
+            if (!FWD && c > c_begin) store_state(A.ws + A.o_Mc + ch * (long long)(TD * TD));
+        }
+        // (3) Delta^T (rows j) and the Q part of y^T
+        bool ok = tc::mbar_wait(bar_mma, ph_mma);
+        ph_mma ^= 1;
+        tc::fence_after();
+        float gl = 0.f;
+        if (issuer) {
+            if (ok && c + 1 < c_end) {
+                load_b1(A, ch + 1, sm, bar_b1);
+                b1_pending = true;
+            }
+        } else if (compute) {
+            ok = tc::mbar_wait(bar_b23, ph_b23) && ok;
+            gl = sGam[BC - 1];
+            float x[32];
+            tc::ld32(tc::taddr(tmem, warp, kColD1 + 32 * hc), x);
+            tc::wait_ld();
+            if (hc == 0) {
+                // Delta^T[j][t] = U^T[j][t] - x[t], split into the operand tile (R = 128, K = 32)
+#pragma unroll
+                for (int b = 0; b < BC / 4; ++b) {
+                    const float4 u = *reinterpret_cast<const float4*>(sU + 4 * (b * TD + j));
+                    const float d0 = __fsub_rn(u.x, x[4 * b]), d1 = __fsub_rn(u.y, x[4 * b + 1]);
+                    const float d2 = __fsub_rn(u.z, x[4 * b + 2]), d3 = __fsub_rn(u.w, x[4 * b + 3]);
+                    uint4 hi, lo;
+                    tc::split_tf32(d0, hi.x, lo.x);
+                    tc::split_tf32(d1, hi.y, lo.y);
+                    tc::split_tf32(d2, hi.z, lo.z);
+                    tc::split_tf32(d3, hi.w, lo.w);
+                    *reinterpret_cast<uint4*>(sDel + 4 * (b * TD + j)) = hi;
+                    *reinterpret_cast<uint4*>(sDel + BC * TD + 4 * (b * TD + j)) = lo;
+                }
+            } else if (FWD) {
+#pragma unroll
+                for (int t = 0; t < BC; ++t) y[t] = __fmul_rn(__fmul_rn(A.scale, sGam[t]), x[t]);
+            }
+        }
+        ph_b23 ^= 1;
+        if (!ok) s_err = 1;
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        if (s_err) break;
+        // (4) D23 = Delta^T [scale QD; (r K)^T]^T
+        if (issuer) {
+            b23_pending = false;
+            tc::fence_after();
+            const uint64_t ahi = tc::tile_desc(sDel, TD), alo = tc::tile_desc(sDel + BC * TD, TD);
+            const uint64_t bhi = tc::tile_desc(sm + kSB23, 160);
+            const uint64_t blo = tc::tile_desc(sm + kSB23 + kTcB23Elems / 2, 160);
+#pragma unroll
+            for (int s = 0; s < BC / 8; ++s) {
+                const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
+                const uint64_t b_h = tc::desc_kslice(bhi, 160, s), b_l = tc::desc_kslice(blo, 160, s);
+                tc::mma_ss(tmem + kColD23, a_h, b_h, id160, s > 0);
+                tc::mma_ss(tmem + kColD23, a_h, b_l, id160, 1);
+                tc::mma_ss(tmem + kColD23, a_l, b_h, id160, 1);
+            }
+            tc::commit(bar_mma);
+        }
+        // (5) y and the state update
+        ok = tc::mbar_wait(bar_mma, ph_mma);
+        ph_mma ^= 1;
+        tc::fence_after();
+        if (!__syncthreads_and(ok)) {
+            s_err = 1;
+            break;
+        }
+        if (issuer) {
+            if (c + 1 < c_end) {
+                tc::fence_async_smem();
+                load_b23(A, ch + 1, sm, bar_b23);
+                b23_pending = true;
+            }
+        } else if (compute) {
+            if (FWD && hc == 1) {
+                float x[32];
+                tc::ld32(tc::taddr(tmem, warp, kColD23), x);
+                tc::wait_ld();
+#pragma unroll
+                for (int t = 0; t < BC; ++t) y[t] = __fadd_rn(y[t], x[t]);
+                y_t0 = t0;
+                y_nb = nb;
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float x[32];
+                tc::ld32(tc::taddr(tmem, warp, kColD23 + BC + 64 * hc + 32 * q), x);
+                tc::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) m[32 * q + e] = __fmaf_rn(gl, m[32 * q + e], x[e]);
+            }
+        }
+    }
+
+    if (s_err) {
+        // give the copies in flight a bounded chance to land before the TMEM is released
+        if (issuer) {
+            atomicExch(&g_tc_status, kStatusTimeout);
+            if (b1_pending) tc::mbar_wait(bar_b1, ph_b1);
+            if (b23_pending) tc::mbar_wait(bar_b23, ph_b23);
+        }
+    } else if (compute) {
+        if (FWD) {
+            if (hc == 1 && y_nb > 0) store_y();
+            store_state(A.state_T + head * (long long)(TD * TD));
+        } else {
+            store_state(A.ws + A.o_Mc + (head * A.n_chunks + c_end) * (long long)(TD * TD));
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) tc::tmem_free(tmem, kTmemCols);
+}
+
+int launch_tc_state(const ChunkArgs& a, bool fwd, void* stream)
+{
+    cudaStream_t s = (cudaStream_t)stream;
+    auto kern = fwd ? gdn_tc_state_kernel<true> : gdn_tc_state_kernel<false>;
+    int e = (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e) return e;
+    const dim3 grid = fwd ? dim3(a.H_v, a.N) : dim3(a.n_ck, a.N * a.H_v);
+    kern<<<grid, TCT, kSmemBytes, s>>>(a);
+    return (int)cudaGetLastError();
+}
+
+int tc_take_status(void* stream, int* status)
+{
+    cudaStream_t s = (cudaStream_t)stream;
+    int v = 0;
+    int e = (int)cudaMemcpyFromSymbolAsync(&v, g_tc_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+    if (!e) e = (int)cudaStreamSynchronize(s);
+    if (e) return e;
+    if (v) {
+        const int zero = 0;
+        e = (int)cudaMemcpyToSymbolAsync(g_tc_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+        if (!e) e = (int)cudaStreamSynchronize(s);
+    }
+    *status = v;
+    return e;
+}
+
+}  // namespace gdn

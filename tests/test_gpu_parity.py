@@ -103,6 +103,19 @@ def test_checkpoint_interval_invariance(kda):
         assert np.array_equal(got["y"], base["y"]) and np.array_equal(got["state_T"], base["state_T"])
 
 
+def test_checkpoint_interval_invariance_head128():
+    """Head size 128 runs the state chain on the tensor cores; the backward's recomputed
+    chunk-entry states must equal the forward's bit for bit, so gradients do not depend on
+    C across chunk-aligned intervals."""
+    prob = synth.make_problem(1, 300, 2, 6, 128, kda=False, seed=50, packed=True, dstate_T=True)
+    dev = H.upload(prob)
+    base, pbase = H.run_gpu(prob, C=32, dev=dev)
+    for C in (64, 96, 160, 1000):
+        got, pk = H.run_gpu(prob, C=C, dev=dev)
+        assert torch.equal(pk, pbase), C
+        assert np.array_equal(got["y"], base["y"]) and np.array_equal(got["state_T"], base["state_T"])
+
+
 def test_strided_views_equal_contiguous_copies():
     prob = synth.make_problem(2, 100, 2, 6, 64, kda=False, seed=43, C=9, packed=True,
                               dstate_T=True)
