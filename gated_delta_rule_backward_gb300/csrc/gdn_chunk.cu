@@ -302,6 +302,83 @@ __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, const float* 
     }
 }
 
+// Tensor-core operands of one (chunk, head) for the dM chain at head size 128: the block
+// at o_DS (layout in gdn_internal.h; tiles in the operand layout of gdn_tc.cuh).  Vs and
+// Zs are free on entry and are used for dY and QD.
+template <int D>
+__device__ void prep_tc_dstate_operands(const ChunkArgs& A, int n, int h, const ChunkPos& cp,
+                                        long long ch, const float* QKs, float* Vs, float* Zs,
+                                        const float* Ts, const float* QKm, const float* Dm,
+                                        const float* gam, int tid)
+{
+    constexpr int ld = Ld<D>::v;
+    constexpr int TM = D / 32;
+    using Map = GemmMap<BC, D, TM, 4, false>;
+    const float* Ks = QKs + BC * ld;
+    float* blk = A.ws + A.o_DS + ch * kTcDsElems;
+    auto put = [](float* hi_base, int half, int unit, float4 x) {
+        uint4 hi, lo;
+        tc::split_tf32(x.x, hi.x, lo.x);
+        tc::split_tf32(x.y, hi.y, lo.y);
+        tc::split_tf32(x.z, hi.z, lo.z);
+        tc::split_tf32(x.w, hi.w, lo.w);
+        *reinterpret_cast<uint4*>(hi_base + 4 * unit) = hi;
+        *reinterpret_cast<uint4*>(hi_base + half + 4 * unit) = lo;
+    };
+    {
+        const long long tg = (long long)n * A.gys0 + (long long)cp.t0 * A.gys1 + (long long)h * A.gys2;
+        load_rows_pad(Vs, ld, A.gy + tg, A.gys1, cp.nb, D, A.vec_gy, tid);
+    }
+    for (int idx = tid; idx < BC * BC; idx += CT) {
+        const int t = idx / BC, tau = idx - t * BC;
+        Zs[t * LDB + tau] = __fmul_rn(QKm[t * LDB + tau], Dm[t * LDB + tau]);
+    }
+    __syncthreads();
+    {  // E^T = scale QD^T dY (rows t), stored as E (rows j), fp32
+        float acc[TM][4];
+        zero_acc(acc);
+        block_gemm<BC, D, TM, 4, true, false>(acc, Zs, LDB, Vs, ld, BC, tid);
+        float* e = blk + kDsE;
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int t = Map::row(tid, i);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = Map::col(tid, jj);
+                e[4 * ((t >> 2) * D + j) + (t & 3)] = __fmul_rn(A.scale, acc[i][jj]);
+            }
+        }
+    }
+    for (int idx = tid; idx < (BC / 4) * D; idx += CT) {  // scale gamma dY^T, unit b * 128 + j
+        const int j = idx % D, b = idx / D;
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            x[e] = __fmul_rn(__fmul_rn(A.scale, gam[4 * b + e]), Vs[(4 * b + e) * ld + j]);
+        put(blk + kDsG, 2 * 128 * 32 / 2, idx, make_float4(x[0], x[1], x[2], x[3]));
+    }
+    for (int idx = tid; idx < (D / 4) * BC; idx += CT) {  // K rows t, unit kc * 32 + t
+        const int t = idx % BC, kc = idx / BC;
+        put(blk + kDsKb, 2 * 32 * 128 / 2, idx, *reinterpret_cast<const float4*>(Ks + t * ld + 4 * kc));
+    }
+    for (int idx = tid; idx < (BC / 4) * BC; idx += CT) {  // T^T rows t: T[t'][t], unit kc * 32 + t
+        const int t = idx % BC, kc = idx / BC;
+        put(blk + kDsTT, 2 * 32 * 32 / 2, idx,
+            make_float4(Ts[(4 * kc) * LDB + t], Ts[(4 * kc + 1) * LDB + t], Ts[(4 * kc + 2) * LDB + t],
+                        Ts[(4 * kc + 3) * LDB + t]));
+    }
+    for (int idx = tid; idx < (2 * BC / 4) * D; idx += CT) {  // [Q^T | K^T] rows i, unit kc * 128 + i
+        const int i = idx % D, kc = idx / D;
+        put(blk + kDsQKT, 2 * 128 * 64 / 2, idx,
+            make_float4(QKs[(4 * kc) * ld + i], QKs[(4 * kc + 1) * ld + i], QKs[(4 * kc + 2) * ld + i],
+                        QKs[(4 * kc + 3) * ld + i]));
+    }
+    if (tid < BC) {
+        blk[kDsR + tid] = Dm[(BC - 1) * LDB + tid];
+        blk[kDsGam + tid] = gam[tid];
+    }
+}
+
 // ---------------------------------------------------------------------------------
 // Prep: one CTA per (chunk, value head, sequence).
 template <int D>
@@ -368,14 +445,21 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
             fD[idx] = Dm[t * LDB + tau];
         }
     }
-    if (!A.want_wu) return;
-    __syncthreads();
     if constexpr (D == 128) {
         if (A.want_tc) {
-            prep_tc_operands<D>(A, ch, QKs, Vs, TG, Ts, QKm, Dm, tid);
+            if (A.want_wu) {
+                __syncthreads();
+                prep_tc_operands<D>(A, ch, QKs, Vs, TG, Ts, QKm, Dm, tid);
+            }
+            if (A.want_factors) {
+                __syncthreads();
+                prep_tc_dstate_operands<D>(A, n, h, cp, ch, QKs, Vs, Zs, Ts, QKm, Dm, gam, tid);
+            }
             return;
         }
     }
+    if (!A.want_wu) return;
+    __syncthreads();
     // W = T diag(gamma) K  (BC x D, row-major),  U^T = (T V)^T  (D x BC)
     constexpr int TM = D / 32;
     using Map = GemmMap<BC, D, TM, 4, false>;
@@ -1180,7 +1264,13 @@ static int chunk_backward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
                        state_smem<D>());
         }
     }
-    GDN_LAUNCH(gdn_chunk_dstate_kernel<D>, dim3(Rows<D>::P, a.H_v, a.N), dstate_smem<D>());
+    if (D == 128 && a.want_tc) {
+        const int e = launch_tc_dstate(a, s);
+        if (e) return e;
+        tap.mark(s);
+    } else {
+        GDN_LAUNCH(gdn_chunk_dstate_kernel<D>, dim3(Rows<D>::P, a.H_v, a.N), dstate_smem<D>());
+    }
     GDN_LAUNCH(gdn_chunk_grad_kernel<D>, dim3(a.n_chunks, a.H_k, a.N), grad_smem<D>());
     return 0;
 }

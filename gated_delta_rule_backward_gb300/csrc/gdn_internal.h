@@ -101,6 +101,7 @@ struct ChunkArgs {
     long long o_T, o_QKD, o_QDT, o_gam, o_r, o_W, o_U, o_Mc, o_dM, o_dDel, o_dX;
     long long o_Tr, o_Z, o_KK, o_QK, o_Dm;  // backward: chunk factors for the gradient kernel
     long long o_B1, o_B23;                  // tensor-core operands of the state chain
+    long long o_DS;                         // tensor-core operands of the dM chain
     int want_wu;
     int want_factors;
     int want_tc;                            // head size 128: state chain on the tensor cores
@@ -121,10 +122,24 @@ struct EventTap {
 // (2 x 160 x 32), in the operand layout of gdn_tc.cuh.
 constexpr int kTcB1Elems = 2 * 64 * 128;
 constexpr int kTcB23Elems = 2 * 160 * 32;
+// Tensor-core operands of the dM chain, one contiguous block per (chunk, head), floats:
+// K (32 x 128, B operand of dM K^T), T^T (32 x 32, B of dDelta^T T), [Q^T | K^T]
+// (128 x 64, B of the dM update), scale gamma dY^T (128 x 32, A of the update), each as
+// tf32 hi then lo; E = scale dY^T QD (128 x 32, fp32, rows j); r and gamma (32 each).
+constexpr int kDsKb = 0;
+constexpr int kDsTT = kDsKb + 2 * 32 * 128;
+constexpr int kDsQKT = kDsTT + 2 * 32 * 32;
+constexpr int kDsG = kDsQKT + 2 * 128 * 64;
+constexpr int kDsE = kDsG + 2 * 128 * 32;
+constexpr int kDsR = kDsE + 128 * 32;
+constexpr int kDsGam = kDsR + 32;
+constexpr int kTcDsElems = kDsGam + 32;
 
 int launch_chunk_forward(const ChunkArgs& a, int D, void* stream, EventTap& tap);
-// The state chain on the tensor cores (gdn_tc_state.cu): forward or recompute mode.
+// The state chain on the tensor cores (gdn_tc_chain.cu): forward or recompute mode.
 int launch_tc_state(const ChunkArgs& a, bool fwd, void* stream);
+// The dM chain on the tensor cores (gdn_tc_chain.cu).
+int launch_tc_dstate(const ChunkArgs& a, void* stream);
 // Reads and clears the tensor-core kernels' device status word (0 or GDN_ERR_TIMEOUT),
 // synchronising `stream`.  Returns a cudaError_t as int.
 int tc_take_status(void* stream, int* status);

@@ -1,7 +1,10 @@
-// gdn_tc_state.cu -- the chunked state chain of the scalar gate at head size 128 on the
-// 5th-generation tensor cores (tcgen05, kind::tf32, three-pass split for fp32 accuracy).
+// gdn_tc_chain.cu -- the two serial chains of the chunked scalar gate at head size 128 on
+// the 5th-generation tensor cores (tcgen05, kind::tf32, three-pass split for fp32
+// accuracy): the state chain (forward and recompute) and the dM chain of the backward.
 //
-// One CTA owns one head's whole state M (128 x 128, rows j = value index) and walks its
+// State chain:
+//
+// one CTA owns one head's whole state M (128 x 128, rows j = value index) and walks its
 // chunks in order.  Per chunk (32 tokens; "metal: GATED_DELTA_NET_BACK" row form regrouped
 // by chunks, see gdn_chunk.cu for the derivation):
 //   D1  = M [W; Q]^T                    128 x 64, K = 128    (A = M from TMEM, B = [W; Q])
@@ -319,6 +322,313 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
     __syncthreads();
     tc::fence_after();
     if (warp == 0) tc::tmem_free(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------------
+// The dM chain in reverse on the tensor cores.  One CTA per head owns dM (128 x 128, rows j;
+// fp32 in registers, tf32 hi/lo in TMEM as an A operand).  Per chunk, last first:
+//   park dM (the gradient of the chunk's end state)
+//   Da = dM K^T                 128 x 32,  K = 128   (B: K rows t)
+//   dDelta^T = r (.) Da + E     E = scale dY^T QD, precomputed by the prep kernel
+//   Db = dDelta^T T             128 x 32,  K = 32    (B: T^T rows t)
+//   dX^T = Db
+//   Dc = [scale gamma dY^T | -gamma dX^T] [Q; K]     128 x 128, K = 64   (B: [Q^T | K^T]);
+//        the dY half does not depend on the chain and is issued right after Da
+//   dM <- gamma_last dM + Dc
+// Parks dDelta^T and dX^T (rows j) for the gradient kernel; writes dstate0 at the end.
+namespace {
+constexpr uint32_t kDsColHi = 0, kDsColLo = 128, kDsColA = 256, kDsColB = 288, kDsColC = 320;
+constexpr int kDsA = kTcDsElems;                   // smem: the operand block, then the A tile
+constexpr int kDsFloats = kDsA + 2 * BC * TD;      //       dDelta^T / -gamma dX^T hi, lo
+constexpr size_t kDsSmemBytes = sizeof(float) * kDsFloats + 64;
+constexpr uint32_t kDsBytesKb = sizeof(float) * (kDsTT - kDsKb);
+constexpr uint32_t kDsBytesRest = sizeof(float) * (kTcDsElems - kDsTT);
+
+__device__ __forceinline__ void ds_load_kb(const ChunkArgs& A, long long ch, float* sm, uint64_t* bar)
+{
+    tc::mbar_expect_tx(bar, kDsBytesKb);
+    tc::bulk_g2s(sm + kDsKb, A.ws + A.o_DS + ch * kTcDsElems + kDsKb, kDsBytesKb, bar);
+}
+__device__ __forceinline__ void ds_load_rest(const ChunkArgs& A, long long ch, float* sm, uint64_t* bar)
+{
+    tc::mbar_expect_tx(bar, kDsBytesRest);
+    tc::bulk_g2s(sm + kDsTT, A.ws + A.o_DS + ch * kTcDsElems + kDsTT, kDsBytesRest, bar);
+}
+}  // namespace
+
+__global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A)
+{
+    extern __shared__ __align__(1024) float sm[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kDsFloats);  // kb, rest, mma
+    uint64_t* bar_kb = bars;
+    uint64_t* bar_rest = bars + 1;
+    uint64_t* bar_mma = bars + 2;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool compute = warp < 8;
+    const bool issuer = tid == kIssuer;
+    const int j = 32 * (warp & 3) + lane;   // row of dM
+    const int hc = (warp >> 2) & 1;         // dM columns [64 hc, 64 hc + 64); chunk columns [16 hc, 16 hc + 16)
+    const int h = blockIdx.x, n = blockIdx.y;
+    const long long head = (long long)n * A.H_v + h;
+
+    if (tid == 0) {
+        tc::mbar_init(bar_kb, 1);
+        tc::mbar_init(bar_rest, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::mbar_fence_init();
+        s_err = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = s_tmem;
+
+    const int c_last = A.n_chunks - 1;
+    uint32_t ph_kb = 0, ph_rest = 0, ph_mma = 0;
+    bool kb_pending = false, rest_pending = false;
+    if (issuer) {
+        ds_load_kb(A, head * A.n_chunks + c_last, sm, bar_kb);
+        ds_load_rest(A, head * A.n_chunks + c_last, sm, bar_rest);
+        kb_pending = rest_pending = true;
+    }
+    float m[64];
+    if (compute) {
+        if (A.dstate_T) {
+            const float4* s4 = reinterpret_cast<const float4*>(A.dstate_T + (head * TD + j) * TD + 64 * hc);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float4 x = __ldg(s4 + q);
+                m[4 * q] = x.x;
+                m[4 * q + 1] = x.y;
+                m[4 * q + 2] = x.z;
+                m[4 * q + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) m[e] = 0.f;
+        }
+    }
+    const float* sE = sm + kDsE;
+    const float* sR = sm + kDsR;
+    const float* sGam = sm + kDsGam;
+    float* sA = sm + kDsA;
+    const uint32_t id32 = tc::idesc_tf32(32), id128 = tc::idesc_tf32(128);
+    // rows j of a 128 x 32 (rows j, K = t) tile: columns t of this thread, [16 hc, 16 hc + 16)
+    auto put_a = [&](const float (&v)[16]) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            uint4 hi, lo;
+            tc::split_tf32(v[4 * b], hi.x, lo.x);
+            tc::split_tf32(v[4 * b + 1], hi.y, lo.y);
+            tc::split_tf32(v[4 * b + 2], hi.z, lo.z);
+            tc::split_tf32(v[4 * b + 3], hi.w, lo.w);
+            const int unit = (4 * hc + b) * TD + j;
+            *reinterpret_cast<uint4*>(sA + 4 * unit) = hi;
+            *reinterpret_cast<uint4*>(sA + BC * TD + 4 * unit) = lo;
+        }
+    };
+    auto park16 = [&](long long off, const float (&v)[16]) {  // rows j, 32 columns per row
+        float4* d = reinterpret_cast<float4*>(A.ws + off + (long long)j * BC + 16 * hc);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) d[b] = make_float4(v[4 * b], v[4 * b + 1], v[4 * b + 2], v[4 * b + 3]);
+    };
+
+    int c = c_last;
+    for (; c >= 0; --c) {
+        const long long ch = head * A.n_chunks + c;
+        // (1) dM -> tf32 hi/lo in TMEM
+        if (compute) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) tc::split_tf32(m[16 * q + e], hi[e], lo[e]);
+                tc::st16(tc::taddr(tmem, warp, kDsColHi + 64 * hc + 16 * q), hi);
+                tc::st16(tc::taddr(tmem, warp, kDsColLo + 64 * hc + 16 * q), lo);
+            }
+            tc::wait_st();
+        }
+        tc::fence_before();
+        __syncthreads();
+        // (2) Da = dM K^T, then the chain-free half of Dc; meanwhile park dM
+        if (issuer) {
+            tc::fence_after();
+            if (!tc::mbar_wait(bar_kb, ph_kb)) s_err = 1;
+            ph_kb ^= 1;
+            kb_pending = false;
+            if (!s_err) {
+                const uint64_t bhi = tc::tile_desc(sm + kDsKb, 32);
+                const uint64_t blo = tc::tile_desc(sm + kDsKb + 32 * TD, 32);
+#pragma unroll
+                for (int s = 0; s < TD / 8; ++s) {
+                    const uint32_t ahi = tmem + kDsColHi + 8 * s, alo = tmem + kDsColLo + 8 * s;
+                    tc::mma_ts(tmem + kDsColA, ahi, tc::desc_kslice(bhi, 32, s), id32, s > 0);
+                    tc::mma_ts(tmem + kDsColA, ahi, tc::desc_kslice(blo, 32, s), id32, 1);
+                    tc::mma_ts(tmem + kDsColA, alo, tc::desc_kslice(bhi, 32, s), id32, 1);
+                }
+                tc::commit(bar_mma);
+                if (!tc::mbar_wait(bar_rest, ph_rest)) s_err = 1;
+                if (!s_err) {
+                    const uint64_t ahi = tc::tile_desc(sm + kDsG, TD), alo = tc::tile_desc(sm + kDsG + BC * TD, TD);
+                    const uint64_t qhi = tc::tile_desc(sm + kDsQKT, TD);
+                    const uint64_t qlo = tc::tile_desc(sm + kDsQKT + 2 * BC * TD, TD);
+#pragma unroll
+                    for (int s = 0; s < BC / 8; ++s) {
+                        const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
+                        const uint64_t b_h = tc::desc_kslice(qhi, TD, s), b_l = tc::desc_kslice(qlo, TD, s);
+                        tc::mma_ss(tmem + kDsColC, a_h, b_h, id128, s > 0);
+                        tc::mma_ss(tmem + kDsColC, a_h, b_l, id128, 1);
+                        tc::mma_ss(tmem + kDsColC, a_l, b_h, id128, 1);
+                    }
+                }
+            }
+        } else if (compute) {
+            float* dst = A.ws + A.o_dM + ch * (long long)(TD * TD) + (long long)j * TD + 64 * hc;
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                reinterpret_cast<float4*>(dst)[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+        }
+        // (3) dDelta^T = r (.) Da + E
+        bool ok = tc::mbar_wait(bar_mma, ph_mma);
+        ph_mma ^= 1;
+        tc::fence_after();
+        if (issuer) {
+            if (ok && c > 0) {
+                ds_load_kb(A, ch - 1, sm, bar_kb);
+                kb_pending = true;
+            }
+        } else if (compute) {
+            ok = tc::mbar_wait(bar_rest, ph_rest) && ok;
+            float x[16];
+            tc::ld16(tc::taddr(tmem, warp, kDsColA + 16 * hc), x);
+            tc::wait_ld();
+            float v[16];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const float4 e = *reinterpret_cast<const float4*>(sE + 4 * ((4 * hc + b) * TD + j));
+                const int t = 16 * hc + 4 * b;
+                v[4 * b] = __fmaf_rn(sR[t], x[4 * b], e.x);
+                v[4 * b + 1] = __fmaf_rn(sR[t + 1], x[4 * b + 1], e.y);
+                v[4 * b + 2] = __fmaf_rn(sR[t + 2], x[4 * b + 2], e.z);
+                v[4 * b + 3] = __fmaf_rn(sR[t + 3], x[4 * b + 3], e.w);
+            }
+            park16(A.o_dDel + ch * (BC * TD), v);
+            put_a(v);
+        }
+        ph_rest ^= 1;
+        if (!ok) s_err = 1;
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        if (s_err) break;
+        // (4) Db = dDelta^T T
+        if (issuer) {
+            rest_pending = false;
+            tc::fence_after();
+            const uint64_t ahi = tc::tile_desc(sA, TD), alo = tc::tile_desc(sA + BC * TD, TD);
+            const uint64_t bhi = tc::tile_desc(sm + kDsTT, 32), blo = tc::tile_desc(sm + kDsTT + 32 * 32, 32);
+#pragma unroll
+            for (int s = 0; s < BC / 8; ++s) {
+                const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
+                const uint64_t b_h = tc::desc_kslice(bhi, 32, s), b_l = tc::desc_kslice(blo, 32, s);
+                tc::mma_ss(tmem + kDsColB, a_h, b_h, id32, s > 0);
+                tc::mma_ss(tmem + kDsColB, a_h, b_l, id32, 1);
+                tc::mma_ss(tmem + kDsColB, a_l, b_h, id32, 1);
+            }
+            tc::commit(bar_mma);
+        }
+        // (5) dX^T = Db;  A tile <- -gamma dX^T
+        ok = tc::mbar_wait(bar_mma, ph_mma);
+        ph_mma ^= 1;
+        tc::fence_after();
+        float gl = 0.f;
+        if (compute) {
+            gl = sGam[BC - 1];
+            float x[16];
+            tc::ld16(tc::taddr(tmem, warp, kDsColB + 16 * hc), x);
+            tc::wait_ld();
+            park16(A.o_dX + ch * (BC * TD), x);
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = -__fmul_rn(sGam[16 * hc + e], x[e]);
+            put_a(v);
+        }
+        if (!ok) s_err = 1;
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        if (s_err) break;
+        // (6) Dc += (-gamma dX^T) K
+        if (issuer) {
+            tc::fence_after();
+            const uint64_t ahi = tc::tile_desc(sA, TD), alo = tc::tile_desc(sA + BC * TD, TD);
+            const uint64_t qhi = tc::tile_desc(sm + kDsQKT, TD);
+            const uint64_t qlo = tc::tile_desc(sm + kDsQKT + 2 * BC * TD, TD);
+#pragma unroll
+            for (int s = 0; s < BC / 8; ++s) {
+                const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
+                const uint64_t b_h = tc::desc_kslice(qhi, TD, s + BC / 8), b_l = tc::desc_kslice(qlo, TD, s + BC / 8);
+                tc::mma_ss(tmem + kDsColC, a_h, b_h, id128, 1);
+                tc::mma_ss(tmem + kDsColC, a_h, b_l, id128, 1);
+                tc::mma_ss(tmem + kDsColC, a_l, b_h, id128, 1);
+            }
+            tc::commit(bar_mma);
+        }
+        // (7) dM <- gamma_last dM + Dc
+        ok = tc::mbar_wait(bar_mma, ph_mma);
+        ph_mma ^= 1;
+        tc::fence_after();
+        if (!__syncthreads_and(ok)) {
+            s_err = 1;
+            break;
+        }
+        if (issuer) {
+            if (c > 0) {
+                tc::fence_async_smem();
+                ds_load_rest(A, ch - 1, sm, bar_rest);
+                rest_pending = true;
+            }
+        } else if (compute) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float x[32];
+                tc::ld32(tc::taddr(tmem, warp, kDsColC + 64 * hc + 32 * q), x);
+                tc::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) m[32 * q + e] = __fmaf_rn(gl, m[32 * q + e], x[e]);
+            }
+        }
+    }
+
+    if (s_err) {
+        if (issuer) {
+            atomicExch(&g_tc_status, kStatusTimeout);
+            if (kb_pending) tc::mbar_wait(bar_kb, ph_kb);
+            if (rest_pending) tc::mbar_wait(bar_rest, ph_rest);
+        }
+    } else if (compute) {
+        float4* d4 = reinterpret_cast<float4*>(A.dstate0 + (head * TD + j) * TD + 64 * hc);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) d4[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) tc::tmem_free(tmem, kTmemCols);
+}
+
+int launch_tc_dstate(const ChunkArgs& a, void* stream)
+{
+    cudaStream_t s = (cudaStream_t)stream;
+    int e = (int)cudaFuncSetAttribute(gdn_tc_dstate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kDsSmemBytes);
+    if (e) return e;
+    gdn_tc_dstate_kernel<<<dim3(a.H_v, a.N), TCT, kDsSmemBytes, s>>>(a);
+    return (int)cudaGetLastError();
 }
 
 int launch_tc_state(const ChunkArgs& a, bool fwd, void* stream)
