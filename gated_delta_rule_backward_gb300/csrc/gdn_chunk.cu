@@ -106,6 +106,17 @@ __device__ __forceinline__ void load_ws(float* dst, int ld, const float* src, in
     }
 }
 
+// A rows x width block stored in the unit layout (float4 unit (c / 4) * rows + row holds
+// row `row`, columns c .. c + 3) into shared memory, row-major with leading dimension ld.
+__device__ __forceinline__ void load_units(float* dst, int ld, const float* src, int rows, int width,
+                                           int tid)
+{
+    for (int idx = tid; idx < rows * (width >> 2); idx += CT) {
+        const int r = idx % rows, c4 = idx / rows;
+        *reinterpret_cast<float4*>(dst + r * ld + 4 * c4) = __ldg(reinterpret_cast<const float4*>(src) + idx);
+    }
+}
+
 // ---------------------------------------------------------------------------------
 // Chunk-local quantities from Q, K (shared, [Q; K] stacked, zero-padded rows), g, beta.
 // Out: G (inclusive cumsum), gam = exp(G), Dm (lower incl), KKm = K K^T (strict lower),
@@ -910,12 +921,21 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
             load_rows_pad(Xs, ld, A.v + tv, A.vs1, cp.nb, D, A.vec_v, tid);
             const long long tg = (long long)n * A.gys0 + (long long)cp.t0 * A.gys1 + (long long)h * A.gys2;
             load_rows_pad(dYs, ld, A.gy + tg, A.gys1, cp.nb, D, A.vec_gy, tid);
-            load_ws(dXT, LDB, A.ws + A.o_dX + ch * (BC * D), D, BC, tid);
-            load_ws(dDT, LDB, A.ws + A.o_dDel + ch * (BC * D), D, BC, tid);
             const float* msrc = (cp.loc == 0)
                                     ? A.ckpt + (head * A.n_ck + cp.seg) * (long long)(D * D)
                                     : A.ws + A.o_Mc + ch * (long long)(D * D);
-            load_ws(MB, ld, msrc, D, D, tid);
+            if (A.want_tc) {  // the tensor-core chains park in the unit layout
+                load_units(dXT, LDB, A.ws + A.o_dX + ch * (BC * D), D, BC, tid);
+                load_units(dDT, LDB, A.ws + A.o_dDel + ch * (BC * D), D, BC, tid);
+                if (cp.loc == 0)
+                    load_ws(MB, ld, msrc, D, D, tid);
+                else
+                    load_units(MB, ld, msrc, D, D, tid);
+            } else {
+                load_ws(dXT, LDB, A.ws + A.o_dX + ch * (BC * D), D, BC, tid);
+                load_ws(dDT, LDB, A.ws + A.o_dDel + ch * (BC * D), D, BC, tid);
+                load_ws(MB, ld, msrc, D, D, tid);
+            }
         }
         load_ws(Ts, LDB, A.ws + A.o_Tr + ch * (BC * BC), BC, BC, tid);
         load_ws(Zs, LDB, A.ws + A.o_Z + ch * (BC * BC), BC, BC, tid);
@@ -992,8 +1012,15 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
             float part = 0.f;
             const float* src = A.ws + A.o_dM + ch * (long long)(D * D);
             for (int idx = tid; idx < D * (D / 4); idx += CT) {
-                const int j = idx / (D / 4), i4 = idx - j * (D / 4);
-                const float4 dm = __ldg(reinterpret_cast<const float4*>(src + (long long)j * D) + i4);
+                int j, i4;
+                if (A.want_tc) {  // unit layout
+                    j = idx % D;
+                    i4 = idx / D;
+                } else {
+                    j = idx / (D / 4);
+                    i4 = idx - j * (D / 4);
+                }
+                const float4 dm = __ldg(reinterpret_cast<const float4*>(src) + (A.want_tc ? idx : j * (D / 4) + i4));
                 float4* mp = reinterpret_cast<float4*>(MB + j * ld + 4 * i4);
                 const float4 m = *mp;
                 part = __fmaf_rn(dm.x, m.x, part);

@@ -20,7 +20,8 @@
 //
 // Modes: forward (grid: head, sequence) writes y, the checkpoints and state_T;
 // recompute (grid: segment, sequence * head) rebuilds the chunk-entry states of one
-// segment from its checkpoint and parks them.  Both run the identical instruction
+// segment from its checkpoint and parks them in the unit layout (float4 unit
+// (i / 4) * 128 + j holds M[j][i .. i + 3]), in which every warp store is one 512-byte run.  Both run the identical instruction
 // sequence per chunk, so recomputed states equal the forward's bit for bit.
 #include <cuda_runtime.h>
 
@@ -144,10 +145,16 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
             m[4 * q + 3] = x.w;
         }
     }
-    auto store_state = [&](float* dst) {  // row j, this thread's 64 columns
+    auto store_state = [&](float* dst) {  // row j, this thread's 64 columns, row-major
         float4* d4 = reinterpret_cast<float4*>(dst + (long long)j * TD + 64 * hc);
 #pragma unroll
         for (int q = 0; q < 16; ++q) d4[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+    };
+    auto park_state = [&](float* dst) {  // the same in the unit layout: a warp writes 512 B runs
+        float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            d4[(16 * hc + q) * TD + j] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
     };
     // y^T of the previous chunk (column-half 1 threads), stored while the next chunk's D1 runs
     float y[32];
@@ -207,7 +214,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
         } else if (compute) {
             if (FWD && hc == 1 && y_nb > 0) store_y();
             if (FWD && loc == 0) store_state(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
-            if (!FWD && c > c_begin) store_state(A.ws + A.o_Mc + ch * (long long)(TD * TD));
+            if (!FWD && c > c_begin) park_state(A.ws + A.o_Mc + ch * (long long)(TD * TD));
         }
         // (3) Delta^T (rows j) and the Q part of y^T
         bool ok = tc::mbar_wait(bar_mma, ph_mma);
@@ -315,7 +322,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
             if (hc == 1 && y_nb > 0) store_y();
             store_state(A.state_T + head * (long long)(TD * TD));
         } else {
-            store_state(A.ws + A.o_Mc + (head * A.n_chunks + c_end) * (long long)(TD * TD));
+            park_state(A.ws + A.o_Mc + (head * A.n_chunks + c_end) * (long long)(TD * TD));
         }
     }
     tc::fence_before();
@@ -335,7 +342,8 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
 //   Dc = [scale gamma dY^T | -gamma dX^T] [Q; K]     128 x 128, K = 64   (B: [Q^T | K^T]);
 //        the dY half does not depend on the chain and is issued right after Da
 //   dM <- gamma_last dM + Dc
-// Parks dDelta^T and dX^T (rows j) for the gradient kernel; writes dstate0 at the end.
+// Parks dM, dDelta^T and dX^T for the gradient kernel in the unit layout (float4 unit
+// (c / 4) * 128 + j holds row j, columns c .. c + 3); writes dstate0 at the end.
 namespace {
 constexpr uint32_t kDsColHi = 0, kDsColLo = 128, kDsColA = 256, kDsColB = 288, kDsColC = 320;
 constexpr int kDsA = kTcDsElems;                   // smem: the operand block, then the A tile
@@ -431,10 +439,11 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
             *reinterpret_cast<uint4*>(sA + BC * TD + 4 * unit) = lo;
         }
     };
-    auto park16 = [&](long long off, const float (&v)[16]) {  // rows j, 32 columns per row
-        float4* d = reinterpret_cast<float4*>(A.ws + off + (long long)j * BC + 16 * hc);
+    auto park16 = [&](long long off, const float (&v)[16]) {  // unit layout, 128 x 32
+        float4* d = reinterpret_cast<float4*>(A.ws + off);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) d[b] = make_float4(v[4 * b], v[4 * b + 1], v[4 * b + 2], v[4 * b + 3]);
+        for (int b = 0; b < 4; ++b)
+            d[(4 * hc + b) * TD + j] = make_float4(v[4 * b], v[4 * b + 1], v[4 * b + 2], v[4 * b + 3]);
     };
 
     int c = c_last;
@@ -487,10 +496,10 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
                 }
             }
         } else if (compute) {
-            float* dst = A.ws + A.o_dM + ch * (long long)(TD * TD) + (long long)j * TD + 64 * hc;
+            float4* dst = reinterpret_cast<float4*>(A.ws + A.o_dM + ch * (long long)(TD * TD));
 #pragma unroll
             for (int q = 0; q < 16; ++q)
-                reinterpret_cast<float4*>(dst)[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+                dst[(16 * hc + q) * TD + j] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
         }
         // (3) dDelta^T = r (.) Da + E
         bool ok = tc::mbar_wait(bar_mma, ph_mma);
