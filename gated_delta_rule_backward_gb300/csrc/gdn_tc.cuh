@@ -4,9 +4,8 @@
 // accumulator in tensor memory (TMEM), issued by one thread of the CTA:
 //   * A is read from TMEM (lane = row, one 32-bit column per K element) or from shared memory;
 //   * B is read from shared memory;
-//   * fp32 accuracy comes from a three-pass split: x = hi + lo with hi = tf32(x) and
-//     lo = tf32(x - hi), and a b ~= hi_a hi_b + hi_a lo_b + lo_a hi_b (the dropped lo lo
-//     term and the truncation of lo are below 2^-21 relative).
+//   * fp32 accuracy comes from a three-pass split: x = hi + lo with hi, lo tf32 values,
+//     and a b ~= hi_a hi_b + hi_a lo_b + lo_a hi_b (split_tf32 below bounds what is lost).
 //
 // Shared-memory operand layout (no swizzle, K-major): an R x K tile of 4-byte elements is
 // stored as core matrices of 8 rows x 4 elements (128 contiguous bytes, row-major inside);
@@ -138,6 +137,15 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16])
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void ld8(uint32_t taddr, float (&v)[8])
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32])
@@ -158,6 +166,11 @@ __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16])
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
 }
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
+}
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // TMEM address of (lane quarter of this warp, column col).
@@ -166,18 +179,25 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, int col)
     return base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)col;
 }
 
-// tf32 split on the integer pipe: hi = x rounded to 10 explicit mantissa bits, to nearest
-// with ties away from zero (add half a unit in bit 12 of the magnitude, clear bits 0-12;
-// exact for every finite x below the largest binade); lo = x - hi, exact in fp32, then
-// truncated to tf32 (|lo| <= 2^-11 |x|, so the truncation is below 2^-21 |x|).
+// tf32 split: hi = x with its 13 low mantissa bits cleared (truncation, one integer op),
+// lo = x - hi (exact in fp32, |lo| < 2^-10 |x|).  The tensor core reads lo as tf32, keeping
+// its 10 leading mantissa bits, so the split represents x to within 2^-21 |x|, and the
+// three-pass product misses only the lo lo term, below 2^-20 |a b|.
 __device__ __forceinline__ uint32_t to_tf32(float x)
 {
-    return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
+    return __float_as_uint(x) & 0xFFFFE000u;
 }
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo)
 {
     hi = to_tf32(x);
-    lo = __float_as_uint(__fsub_rn(x, __uint_as_float(hi))) & 0xFFFFE000u;
+    lo = __float_as_uint(__fsub_rn(x, __uint_as_float(hi)));
+}
+
+// Barrier among the first `threads` threads of the CTA (named barrier 1), leaving the rest
+// of the CTA free to run.
+__device__ __forceinline__ void bar_sync_first(int threads)
+{
+    asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
 }
 
 // ---- mbarriers and bulk copies ----

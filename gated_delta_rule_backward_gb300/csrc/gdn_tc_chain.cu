@@ -53,6 +53,7 @@ constexpr int kSU = kSB23 + kTcB23Elems;           // U^T, operand layout (R = 1
 constexpr int kSDel = kSU + BC * TD;               // Delta^T hi, lo   2 x 128 x 32
 constexpr int kSGam = kSDel + 2 * BC * TD;         // gamma (32)
 constexpr int kSFloats = kSGam + BC;
+constexpr int kStageLd = TD + 4;                   // staging rows for coalesced global writes
 constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 64;   // + barriers
 
 constexpr uint32_t kB1Bytes = sizeof(float) * kTcB1Elems;
@@ -145,11 +146,6 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
             m[4 * q + 3] = x.w;
         }
     }
-    auto store_state = [&](float* dst) {  // row j, this thread's 64 columns, row-major
-        float4* d4 = reinterpret_cast<float4*>(dst + (long long)j * TD + 64 * hc);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) d4[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
-    };
     auto park_state = [&](float* dst) {  // the same in the unit layout: a warp writes 512 B runs
         float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -159,13 +155,54 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
     // y^T of the previous chunk (column-half 1 threads), stored while the next chunk's D1 runs
     float y[32];
     int y_t0 = 0, y_nb = 0;
-    auto store_y = [&]() {
-        float* yp = A.y + (((long long)n * A.T + y_t0) * A.H_v + h) * TD + j;
-        const long long ys = (long long)A.H_v * TD;
+    float* stage = sm + kSDel;   // idle while D1 runs: 32 rows of kStageLd floats
+    const int ctid = tid;        // 0..255 for the compute warps
+    auto store_y = [&]() {       // through `stage`: the global writes are whole 512-byte rows
+        if (hc == 1) {
 #pragma unroll
-        for (int t = 0; t < BC; ++t)
-            if (t < y_nb) yp[t * ys] = y[t];
+            for (int t = 0; t < BC; ++t) stage[t * kStageLd + j] = y[t];
+        }
+        tc::bar_sync_first(256);
+        float* yp = A.y + (((long long)n * A.T + y_t0) * A.H_v + h) * TD;
+        const long long ys = (long long)A.H_v * TD;
+        for (int idx = ctid; idx < y_nb * (TD / 4); idx += 256) {
+            const int t = idx / (TD / 4), q = idx - t * (TD / 4);
+            *reinterpret_cast<float4*>(yp + t * ys + 4 * q) =
+                *reinterpret_cast<const float4*>(stage + t * kStageLd + 4 * q);
+        }
+        tc::bar_sync_first(256);
     };
+    auto store_ckpt = [&](float* dst) {  // row-major M through `stage`, 32 rows at a time
+#pragma unroll 1
+        for (int r = 0; r < 4; ++r) {
+            if ((warp & 3) == r) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    *reinterpret_cast<float4*>(stage + lane * kStageLd + 64 * hc + 4 * q) =
+                        make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+            }
+            tc::bar_sync_first(256);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int idx = ctid + 256 * k, row = idx >> 5, q = idx & 31;
+                *reinterpret_cast<float4*>(dst + (long long)(32 * r + row) * TD + 4 * q) =
+                    *reinterpret_cast<const float4*>(stage + row * kStageLd + 4 * q);
+            }
+            tc::bar_sync_first(256);
+        }
+    };
+    auto split_store = [&](int q) {  // columns [8 q, 8 q + 8) of this thread's half -> TMEM hi/lo
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) tc::split_tf32(m[8 * q + e], hi[e], lo[e]);
+        tc::st8(tc::taddr(tmem, warp, kColMhi + 64 * hc + 8 * q), hi);
+        tc::st8(tc::taddr(tmem, warp, kColMlo + 64 * hc + 8 * q), lo);
+    };
+    if (compute) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) split_store(q);
+        tc::wait_st();
+    }
 
     const float* sU = sm + kSU;
     const float* sGam = sm + kSGam;
@@ -179,18 +216,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
         const int t0 = seg * A.C + loc * BC;
         const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
         const long long ch = head * A.n_chunks + c;
-        // (1) M -> tf32 hi/lo, the A operand of D1 in TMEM
-        if (compute) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t hi[16], lo[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) tc::split_tf32(m[16 * q + e], hi[e], lo[e]);
-                tc::st16(tc::taddr(tmem, warp, kColMhi + 64 * hc + 16 * q), hi);
-                tc::st16(tc::taddr(tmem, warp, kColMlo + 64 * hc + 16 * q), lo);
-            }
-            tc::wait_st();
-        }
+        // (1) M (tf32 hi/lo, the A operand of D1) is in TMEM
         tc::fence_before();
         __syncthreads();
         // (2) D1 = M [W; Q]^T on the tensor cores; meanwhile the pending global stores
@@ -212,8 +238,8 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
                 tc::commit(bar_mma);
             }
         } else if (compute) {
-            if (FWD && hc == 1 && y_nb > 0) store_y();
-            if (FWD && loc == 0) store_state(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
+            if (FWD && y_nb > 0) store_y();
+            if (FWD && loc == 0) store_ckpt(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
             if (!FWD && c > c_begin) park_state(A.ws + A.o_Mc + ch * (long long)(TD * TD));
         }
         // (3) Delta^T (rows j) and the Q part of y^T
@@ -290,23 +316,28 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
                 b23_pending = true;
             }
         } else if (compute) {
-            if (FWD && hc == 1) {
-                float x[32];
-                tc::ld32(tc::taddr(tmem, warp, kColD23), x);
-                tc::wait_ld();
+            if (FWD) {
+                if (hc == 1) {
+                    float x[32];
+                    tc::ld32(tc::taddr(tmem, warp, kColD23), x);
+                    tc::wait_ld();
 #pragma unroll
-                for (int t = 0; t < BC; ++t) y[t] = __fadd_rn(y[t], x[t]);
+                    for (int t = 0; t < BC; ++t) y[t] = __fadd_rn(y[t], x[t]);
+                }
                 y_t0 = t0;
                 y_nb = nb;
             }
+            // M <- gamma_last M + D23[:, 32:160], split at once into the next D1's A operand
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float x[32];
-                tc::ld32(tc::taddr(tmem, warp, kColD23 + BC + 64 * hc + 32 * q), x);
+            for (int q = 0; q < 8; ++q) {
+                float x[8];
+                tc::ld8(tc::taddr(tmem, warp, kColD23 + BC + 64 * hc + 8 * q), x);
                 tc::wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) m[32 * q + e] = __fmaf_rn(gl, m[32 * q + e], x[e]);
+                for (int e = 0; e < 8; ++e) m[8 * q + e] = __fmaf_rn(gl, m[8 * q + e], x[e]);
+                split_store(q);
             }
+            tc::wait_st();
         }
     }
 
@@ -319,8 +350,8 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
         }
     } else if (compute) {
         if (FWD) {
-            if (hc == 1 && y_nb > 0) store_y();
-            store_state(A.state_T + head * (long long)(TD * TD));
+            if (y_nb > 0) store_y();
+            store_ckpt(A.state_T + head * (long long)(TD * TD));
         } else {
             park_state(A.ws + A.o_Mc + (head * A.n_chunks + c_end) * (long long)(TD * TD));
         }
