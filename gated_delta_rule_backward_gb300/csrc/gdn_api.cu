@@ -52,7 +52,7 @@ struct Plan {
     int cps = 1;          // chunks per checkpoint segment
     int64_t n_chunks = 0; // chunks per (sequence, value head)
     long long o_T = 0, o_QKD = 0, o_QDT = 0, o_gam = 0, o_r = 0, o_W = 0, o_U = 0, o_Mc = 0, o_dM = 0,
-              o_dDel = 0, o_dX = 0, o_Tr = 0, o_Z = 0, o_KK = 0, o_QK = 0, o_Dm = 0, o_B1 = 0, o_B23 = 0, o_DS = 0;
+              o_dDel = 0, o_dX = 0, o_Tr = 0, o_Z = 0, o_KK = 0, o_QK = 0, o_Dm = 0, o_W1 = 0, o_Q1 = 0, o_B23 = 0, o_DK = 0, o_DS = 0;
     bool tensor = false;  // head size 128: the state chain runs on the tensor cores
     size_t fwd_ws_bytes = 0, bwd_ws_bytes = 0;
 };
@@ -135,6 +135,7 @@ Plan make_plan(const gdn_params_t* p)
         const int64_t last_len = p->T - (pl.n_ck - 1) * pl.C;
         pl.n_chunks = (pl.n_ck - 1) * pl.cps + (last_len + BC - 1) / BC;
         const int64_t CH = p->n_seq * p->H_v * pl.n_chunks;
+        const int64_t CK = p->n_seq * p->H_k * pl.n_chunks;
         const int64_t D = pl.D;
         // float offsets, each sub-array 256-byte aligned
         auto al = [](int64_t f) { return (long long)((f + 63) & ~int64_t(63)); };
@@ -148,7 +149,8 @@ Plan make_plan(const gdn_params_t* p)
         pl.tensor = (D == 128);
         if (pl.tensor) {  // U^T in fp32 and the tf32 hi/lo operands, tensor-core layout
             pl.o_U = o;   o += al(CH * BC * D);
-            pl.o_B1 = o;  o += al(CH * gdn::kTcB1Elems);
+            pl.o_W1 = o;  o += al(CH * gdn::kTcWElems);
+            pl.o_Q1 = o;  o += al(CK * gdn::kTcQElems);
             pl.o_B23 = o; o += al(CH * gdn::kTcB23Elems);
         } else {
             pl.o_W = o;   o += al(CH * BC * D);
@@ -170,6 +172,7 @@ Plan make_plan(const gdn_params_t* p)
         pl.o_dDel = o; o += al(CH * BC * D);
         pl.o_dX = o;   o += al(CH * BC * D);
         if (pl.tensor) {
+            pl.o_DK = o; o += al(CK * gdn::kTcDkElems);
             pl.o_DS = o; o += al(CH * gdn::kTcDsElems);
         }
         pl.bwd_ws_bytes = (size_t)o * 4;
@@ -237,7 +240,7 @@ void fill_chunk_common(gdn::ChunkArgs& c, const gdn_params_t* p, const Plan& pl)
     c.o_T = pl.o_T; c.o_QKD = pl.o_QKD; c.o_QDT = pl.o_QDT; c.o_gam = pl.o_gam; c.o_r = pl.o_r; c.o_W = pl.o_W;
     c.o_U = pl.o_U; c.o_Mc = pl.o_Mc; c.o_dM = pl.o_dM; c.o_dDel = pl.o_dDel; c.o_dX = pl.o_dX;
     c.o_Tr = pl.o_Tr; c.o_Z = pl.o_Z; c.o_KK = pl.o_KK; c.o_QK = pl.o_QK; c.o_Dm = pl.o_Dm;
-    c.o_B1 = pl.o_B1; c.o_B23 = pl.o_B23; c.o_DS = pl.o_DS;
+    c.o_W1 = pl.o_W1; c.o_Q1 = pl.o_Q1; c.o_B23 = pl.o_B23; c.o_DK = pl.o_DK; c.o_DS = pl.o_DS;
     c.want_tc = pl.tensor;
 }
 

@@ -250,19 +250,20 @@ __device__ __forceinline__ void load_gate_beta(const ChunkArgs& A, int n, int h,
 }
 
 // Tensor-core operands of one (chunk, head) for the state chain at head size 128, in the
-// operand layout of gdn_tc.cuh: B1 = [W; Q] (64 x 128) and B23 = [scale QD; (r K)^T]
-// (160 x 32) as tf32 hi then lo, and U^T (rows j, 32 tokens) in fp32.  W = T diag(gamma) K,
-// U = T V.  Vs holds V on entry and stages U afterwards.
+// operand layouts of gdn_tc.cuh: W = T diag(gamma) K (32 x 128, row-group-major; the key
+// head's Q beside it when `first`), B23 = [scale QD; (r K)^T] (160 x 32) as tf32 hi then lo,
+// and U^T (rows j, 32 tokens) in fp32, U = T V.  Vs holds V on entry and stages U afterwards.
 template <int D>
-__device__ void prep_tc_operands(const ChunkArgs& A, long long ch, const float* QKs, float* Vs,
-                                 const float* TG, const float* Ts, const float* QKm,
-                                 const float* Dm, int tid)
+__device__ void prep_tc_operands(const ChunkArgs& A, long long ch, long long ck, bool first,
+                                 const float* QKs, float* Vs, const float* TG, const float* Ts,
+                                 const float* QKm, const float* Dm, int tid)
 {
     constexpr int ld = Ld<D>::v;
     constexpr int TM = D / 32;
     using Map = GemmMap<BC, D, TM, 4, false>;
     const float* Ks = QKs + BC * ld;
-    float* b1 = A.ws + A.o_B1 + ch * kTcB1Elems;
+    float* w1 = A.ws + A.o_W1 + ch * kTcWElems;
+    float* q1 = A.ws + A.o_Q1 + ck * kTcQElems;
     float* b23 = A.ws + A.o_B23 + ch * kTcB23Elems;
     float* u = A.ws + A.o_U + ch * (BC * D);
     auto put = [](float* hi_base, int half, int unit, float4 x) {
@@ -285,13 +286,15 @@ __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, const float* 
     zero_acc(acc);
     block_gemm<BC, D, TM, 4, false, false>(acc, TG, LDB, Ks, ld, BC, tid);  // W
 #pragma unroll
-    for (int i = 0; i < TM; ++i) {  // rows t of B1, 4 consecutive k per thread
+    for (int i = 0; i < TM; ++i) {  // rows t of W, 4 consecutive k per thread
         const int t = Map::row(tid, i), c0 = Map::col(tid, 0);
-        put(b1, kTcB1Elems / 2, (c0 >> 2) * 64 + t, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+        put(w1, kTcWElems / 2, tc::kmaj_rg(t, c0, D) >> 2, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
     }
-    for (int idx = tid; idx < BC * (D / 4); idx += CT) {  // rows 32 + t of B1: Q
-        const int t = idx % BC, kc = idx / BC;
-        put(b1, kTcB1Elems / 2, kc * 64 + BC + t, *reinterpret_cast<const float4*>(QKs + t * ld + 4 * kc));
+    if (first) {  // Q, unit u = (row group * 32 + k-chunk) * 8 + row % 8
+        for (int u = tid; u < BC * (D / 4); u += CT) {
+            const int t = ((u >> 8) << 3) + (u & 7), kc = (u >> 3) & 31;
+            put(q1, kTcQElems / 2, u, *reinterpret_cast<const float4*>(QKs + t * ld + 4 * kc));
+        }
     }
     for (int idx = tid; idx < 160 * (BC / 4); idx += CT) {  // B23, unit = kc * 160 + row
         const int r = idx % 160, kc = idx / 160;
@@ -313,20 +316,22 @@ __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, const float* 
     }
 }
 
-// Tensor-core operands of one (chunk, head) for the dM chain at head size 128: the block
-// at o_DS (layout in gdn_internal.h; tiles in the operand layout of gdn_tc.cuh).  Vs and
-// Zs are free on entry and are used for dY and QD.
+// Tensor-core operands of one (chunk, head) for the dM chain at head size 128: the value
+// head's block at o_DS and, when `first`, the key head's block at o_DK (layouts in
+// gdn_internal.h; tiles in the operand layout of gdn_tc.cuh).  Vs and Zs are free on entry
+// and are used for dY and QD.
 template <int D>
 __device__ void prep_tc_dstate_operands(const ChunkArgs& A, int n, int h, const ChunkPos& cp,
-                                        long long ch, const float* QKs, float* Vs, float* Zs,
-                                        const float* Ts, const float* QKm, const float* Dm,
-                                        const float* gam, int tid)
+                                        long long ch, long long ck, bool first, const float* QKs,
+                                        float* Vs, float* Zs, const float* Ts, const float* QKm,
+                                        const float* Dm, const float* gam, int tid)
 {
     constexpr int ld = Ld<D>::v;
     constexpr int TM = D / 32;
     using Map = GemmMap<BC, D, TM, 4, false>;
     const float* Ks = QKs + BC * ld;
     float* blk = A.ws + A.o_DS + ch * kTcDsElems;
+    float* kblk = A.ws + A.o_DK + ck * kTcDkElems;
     auto put = [](float* hi_base, int half, int unit, float4 x) {
         uint4 hi, lo;
         tc::split_tf32(x.x, hi.x, lo.x);
@@ -368,21 +373,23 @@ __device__ void prep_tc_dstate_operands(const ChunkArgs& A, int n, int h, const 
             x[e] = __fmul_rn(__fmul_rn(A.scale, gam[4 * b + e]), Vs[(4 * b + e) * ld + j]);
         put(blk + kDsG, 2 * 128 * 32 / 2, idx, make_float4(x[0], x[1], x[2], x[3]));
     }
-    for (int idx = tid; idx < (D / 4) * BC; idx += CT) {  // K rows t, unit kc * 32 + t
-        const int t = idx % BC, kc = idx / BC;
-        put(blk + kDsKb, 2 * 32 * 128 / 2, idx, *reinterpret_cast<const float4*>(Ks + t * ld + 4 * kc));
+    if (first) {
+        for (int idx = tid; idx < (D / 4) * BC; idx += CT) {  // K rows t, unit kc * 32 + t
+            const int t = idx % BC, kc = idx / BC;
+            put(kblk + kDkKb, 2 * 32 * 128 / 2, idx, *reinterpret_cast<const float4*>(Ks + t * ld + 4 * kc));
+        }
+        for (int idx = tid; idx < (2 * BC / 4) * D; idx += CT) {  // [Q^T | K^T] rows i, unit kc * 128 + i
+            const int i = idx % D, kc = idx / D;
+            put(kblk + kDkQKT, 2 * 128 * 64 / 2, idx,
+                make_float4(QKs[(4 * kc) * ld + i], QKs[(4 * kc + 1) * ld + i], QKs[(4 * kc + 2) * ld + i],
+                            QKs[(4 * kc + 3) * ld + i]));
+        }
     }
     for (int idx = tid; idx < (BC / 4) * BC; idx += CT) {  // T^T rows t: T[t'][t], unit kc * 32 + t
         const int t = idx % BC, kc = idx / BC;
         put(blk + kDsTT, 2 * 32 * 32 / 2, idx,
             make_float4(Ts[(4 * kc) * LDB + t], Ts[(4 * kc + 1) * LDB + t], Ts[(4 * kc + 2) * LDB + t],
                         Ts[(4 * kc + 3) * LDB + t]));
-    }
-    for (int idx = tid; idx < (2 * BC / 4) * D; idx += CT) {  // [Q^T | K^T] rows i, unit kc * 128 + i
-        const int i = idx % D, kc = idx / D;
-        put(blk + kDsQKT, 2 * 128 * 64 / 2, idx,
-            make_float4(QKs[(4 * kc) * ld + i], QKs[(4 * kc + 1) * ld + i], QKs[(4 * kc + 2) * ld + i],
-                        QKs[(4 * kc + 3) * ld + i]));
     }
     if (tid < BC) {
         blk[kDsR + tid] = Dm[(BC - 1) * LDB + tid];
@@ -458,13 +465,15 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
     }
     if constexpr (D == 128) {
         if (A.want_tc) {
+            const long long ck = ((long long)n * A.H_k + hk) * A.n_chunks + c;
+            const bool first = h < A.H_k;  // the key head's first value head writes its operands
             if (A.want_wu) {
                 __syncthreads();
-                prep_tc_operands<D>(A, ch, QKs, Vs, TG, Ts, QKm, Dm, tid);
+                prep_tc_operands<D>(A, ch, ck, first, QKs, Vs, TG, Ts, QKm, Dm, tid);
             }
             if (A.want_factors) {
                 __syncthreads();
-                prep_tc_dstate_operands<D>(A, n, h, cp, ch, QKs, Vs, Zs, Ts, QKm, Dm, gam, tid);
+                prep_tc_dstate_operands<D>(A, n, h, cp, ch, ck, first, QKs, Vs, Zs, Ts, QKm, Dm, gam, tid);
             }
             return;
         }

@@ -100,8 +100,8 @@ struct ChunkArgs {
     // workspace sub-arrays (float offsets from ws), per (sequence, value head, chunk)
     long long o_T, o_QKD, o_QDT, o_gam, o_r, o_W, o_U, o_Mc, o_dM, o_dDel, o_dX;
     long long o_Tr, o_Z, o_KK, o_QK, o_Dm;  // backward: chunk factors for the gradient kernel
-    long long o_B1, o_B23;                  // tensor-core operands of the state chain
-    long long o_DS;                         // tensor-core operands of the dM chain
+    long long o_W1, o_Q1, o_B23;            // tensor-core operands of the state chain
+    long long o_DK, o_DS;                   // tensor-core operands of the dM chain
     int want_wu;
     int want_factors;
     int want_tc;                            // head size 128: state chain on the tensor cores
@@ -117,19 +117,23 @@ struct EventTap {
     void mark(void* stream);
 };
 
-// Tensor-core operands of the state chain (head size 128), floats per (chunk, head):
-// [W; Q] as tf32 hi then lo (2 x 64 x 128) and [scale QD; (r K)^T] as hi then lo
-// (2 x 160 x 32), in the operand layout of gdn_tc.cuh.
-constexpr int kTcB1Elems = 2 * 64 * 128;
+// Tensor-core operands of the state chain (head size 128), in the operand layouts of
+// gdn_tc.cuh, floats: W = T diag(gamma) K per (chunk, value head) and Q per (chunk, key head),
+// each 32 x 128 as tf32 hi then lo in the row-group-major layout (the two stack into the
+// 64-row B operand [W; Q]); [scale QD; (r K)^T] per (chunk, value head) as hi then lo
+// (2 x 160 x 32, k-chunk-major).
+constexpr int kTcWElems = 2 * 32 * 128;
+constexpr int kTcQElems = 2 * 32 * 128;
 constexpr int kTcB23Elems = 2 * 160 * 32;
-// Tensor-core operands of the dM chain, one contiguous block per (chunk, head), floats:
-// K (32 x 128, B operand of dM K^T), T^T (32 x 32, B of dDelta^T T), [Q^T | K^T]
-// (128 x 64, B of the dM update), scale gamma dY^T (128 x 32, A of the update), each as
-// tf32 hi then lo; E = scale dY^T QD (128 x 32, fp32, rows j); r and gamma (32 each).
-constexpr int kDsKb = 0;
-constexpr int kDsTT = kDsKb + 2 * 32 * 128;
-constexpr int kDsQKT = kDsTT + 2 * 32 * 32;
-constexpr int kDsG = kDsQKT + 2 * 128 * 64;
+// Tensor-core operands of the dM chain.  Per (chunk, key head): K (32 x 128, B of dM K^T)
+// and [Q^T | K^T] (128 x 64, B of the dM update) as hi then lo.  Per (chunk, value head):
+// T^T (32 x 32, B of dDelta^T T) and scale gamma dY^T (128 x 32, A of the update) as hi
+// then lo, E = scale dY^T QD (128 x 32, fp32, rows j), r and gamma (32 each).
+constexpr int kDkKb = 0;
+constexpr int kDkQKT = kDkKb + 2 * 32 * 128;
+constexpr int kTcDkElems = kDkQKT + 2 * 128 * 64;
+constexpr int kDsTT = 0;
+constexpr int kDsG = kDsTT + 2 * 32 * 32;
 constexpr int kDsE = kDsG + 2 * 128 * 32;
 constexpr int kDsR = kDsE + 128 * 32;
 constexpr int kDsGam = kDsR + 32;

@@ -33,6 +33,14 @@ GDN_HD inline int kmaj(int r, int k, int R)
 {
     return (((k >> 2) * (R >> 3) + (r >> 3)) << 5) + ((r & 7) << 2) + (k & 3);
 }
+// The row-group-major variant of a tile with K elements per row: core matrix (row group g,
+// k-chunk kc) at float offset (g * (K / 4) + kc) * 32, so each group of 8 rows is one
+// contiguous block and tiles of whole row groups stack by concatenation.  LBO = 128 bytes,
+// SBO = K * 32 bytes; the K = 8 slice s starts 256 s bytes in.
+GDN_HD inline int kmaj_rg(int r, int k, int K)
+{
+    return (((r >> 3) * (K >> 2) + (k >> 2)) << 5) + ((r & 7) << 2) + (k & 3);
+}
 
 #if defined(__CUDACC__)
 
@@ -59,6 +67,14 @@ __device__ __forceinline__ uint64_t tile_desc(const float* base, int R)
 __device__ __forceinline__ uint64_t desc_kslice(uint64_t d, int R, int s)
 {
     return d + (uint64_t)((2 * (R / 8) * 128 * s) >> 4);
+}
+__device__ __forceinline__ uint64_t tile_desc_rg(const float* base, int K)
+{
+    return make_desc(smem_addr(base), 128u, (uint32_t)K * 32u);
+}
+__device__ __forceinline__ uint64_t desc_kslice_rg(uint64_t d, int s)
+{
+    return d + (uint64_t)(16 * s);
 }
 
 // Instruction descriptor, kind::tf32: fp32 accumulator, tf32 A and B, both K-major, M = 128.

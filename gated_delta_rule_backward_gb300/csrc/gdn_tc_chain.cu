@@ -47,8 +47,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kStatusTimeout = 6;
 
 // Shared memory, in floats.
-constexpr int kSB1 = 0;                            // [W; Q] hi, lo    2 x 64 x 128
-constexpr int kSB23 = kSB1 + kTcB1Elems;           // [sQD; rK^T] hi, lo  2 x 160 x 32
+constexpr int kSB1 = 0;                            // [W; Q] hi, then lo: 2 x 64 x 128, row-group-major
+constexpr int kSB23 = kSB1 + kTcWElems + kTcQElems;  // [sQD; rK^T] hi, lo  2 x 160 x 32
 constexpr int kSU = kSB23 + kTcB23Elems;           // U^T, operand layout (R = 128), fp32
 constexpr int kSDel = kSU + BC * TD;               // Delta^T hi, lo   2 x 128 x 32
 constexpr int kSGam = kSDel + 2 * BC * TD;         // gamma (32)
@@ -56,13 +56,21 @@ constexpr int kSFloats = kSGam + BC;
 constexpr int kStageLd = TD + 4;                   // staging rows for coalesced global writes
 constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 64;   // + barriers
 
-constexpr uint32_t kB1Bytes = sizeof(float) * kTcB1Elems;
+constexpr uint32_t kB1Bytes = sizeof(float) * (kTcWElems + kTcQElems);
+constexpr int kHalfW = kTcWElems / 2;  // 32 x 128 floats
 constexpr uint32_t kB23Bytes = sizeof(float) * kTcB23Elems + sizeof(float) * BC * TD + sizeof(float) * BC;
 
-__device__ __forceinline__ void load_b1(const ChunkArgs& A, long long ch, float* sm, uint64_t* bar)
+// [W; Q] hi then lo: W of the value head and Q of its key head, stacked by row groups.
+__device__ __forceinline__ void load_b1(const ChunkArgs& A, long long ch, long long ck, float* sm, uint64_t* bar)
 {
+    const float* w = A.ws + A.o_W1 + ch * kTcWElems;
+    const float* q = A.ws + A.o_Q1 + ck * kTcQElems;
+    constexpr uint32_t part = sizeof(float) * kHalfW;
     tc::mbar_expect_tx(bar, kB1Bytes);
-    tc::bulk_g2s(sm + kSB1, A.ws + A.o_B1 + ch * kTcB1Elems, kB1Bytes, bar);
+    tc::bulk_g2s(sm + kSB1, w, part, bar);
+    tc::bulk_g2s(sm + kSB1 + kHalfW, q, part, bar);
+    tc::bulk_g2s(sm + kSB1 + 2 * kHalfW, w + kHalfW, part, bar);
+    tc::bulk_g2s(sm + kSB1 + 3 * kHalfW, q + kHalfW, part, bar);
 }
 
 __device__ __forceinline__ void load_b23(const ChunkArgs& A, long long ch, float* sm, uint64_t* bar)
@@ -109,6 +117,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
         if (c_end <= c_begin) return;
     }
     const long long head = (long long)n * A.H_v + h;
+    const long long khead = (long long)n * A.H_k + h % A.H_k;
 
     if (tid == 0) {
         tc::mbar_init(bar_b1, 1);
@@ -126,7 +135,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
     uint32_t ph_b1 = 0, ph_b23 = 0, ph_mma = 0;
     bool b1_pending = false, b23_pending = false;
     if (issuer) {
-        load_b1(A, head * A.n_chunks + c_begin, sm, bar_b1);
+        load_b1(A, head * A.n_chunks + c_begin, khead * A.n_chunks + c_begin, sm, bar_b1);
         load_b23(A, head * A.n_chunks + c_begin, sm, bar_b23);
         b1_pending = b23_pending = true;
     }
@@ -226,14 +235,14 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
             ph_b1 ^= 1;
             b1_pending = false;
             if (!s_err) {
-                const uint64_t bhi = tc::tile_desc(sm + kSB1, 64);
-                const uint64_t blo = tc::tile_desc(sm + kSB1 + kTcB1Elems / 2, 64);
+                const uint64_t bhi = tc::tile_desc_rg(sm + kSB1, TD);
+                const uint64_t blo = tc::tile_desc_rg(sm + kSB1 + 2 * kHalfW, TD);
 #pragma unroll
                 for (int s = 0; s < TD / 8; ++s) {
                     const uint32_t ahi = tmem + kColMhi + 8 * s, alo = tmem + kColMlo + 8 * s;
-                    tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice(bhi, 64, s), id64, s > 0);
-                    tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice(blo, 64, s), id64, 1);
-                    tc::mma_ts(tmem + kColD1, alo, tc::desc_kslice(bhi, 64, s), id64, 1);
+                    tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice_rg(bhi, s), id64, s > 0);
+                    tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice_rg(blo, s), id64, 1);
+                    tc::mma_ts(tmem + kColD1, alo, tc::desc_kslice_rg(bhi, s), id64, 1);
                 }
                 tc::commit(bar_mma);
             }
@@ -249,7 +258,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
         float gl = 0.f;
         if (issuer) {
             if (ok && c + 1 < c_end) {
-                load_b1(A, ch + 1, sm, bar_b1);
+                load_b1(A, ch + 1, khead * A.n_chunks + c + 1, sm, bar_b1);
                 b1_pending = true;
             }
         } else if (compute) {
@@ -377,21 +386,34 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
 // (c / 4) * 128 + j holds row j, columns c .. c + 3); writes dstate0 at the end.
 namespace {
 constexpr uint32_t kDsColHi = 0, kDsColLo = 128, kDsColA = 256, kDsColB = 288, kDsColC = 320;
-constexpr int kDsA = kTcDsElems;                   // smem: the operand block, then the A tile
-constexpr int kDsFloats = kDsA + 2 * BC * TD;      //       dDelta^T / -gamma dX^T hi, lo
+// shared memory (floats): K | T^T | [Q^T | K^T] | scale gamma dY^T | E | r | gamma | A tile
+constexpr int kSmKb = 0;
+constexpr int kSmTT = kSmKb + kDkQKT - kDkKb;
+constexpr int kSmQKT = kSmTT + kDsG - kDsTT;
+constexpr int kSmG = kSmQKT + kTcDkElems - kDkQKT;
+constexpr int kSmE = kSmG + kDsE - kDsG;
+constexpr int kSmR = kSmE + kDsR - kDsE;
+constexpr int kSmGam = kSmR + kDsGam - kDsR;
+constexpr int kDsA = kSmGam + BC;                  // dDelta^T / -gamma dX^T hi, lo
+constexpr int kDsFloats = kDsA + 2 * BC * TD;
 constexpr size_t kDsSmemBytes = sizeof(float) * kDsFloats + 64;
-constexpr uint32_t kDsBytesKb = sizeof(float) * (kDsTT - kDsKb);
-constexpr uint32_t kDsBytesRest = sizeof(float) * (kTcDsElems - kDsTT);
+constexpr uint32_t kDsBytesKb = sizeof(float) * (kDkQKT - kDkKb);
+constexpr uint32_t kDsBytesTT = sizeof(float) * (kDsG - kDsTT);
+constexpr uint32_t kDsBytesQKT = sizeof(float) * (kTcDkElems - kDkQKT);
+constexpr uint32_t kDsBytesTail = sizeof(float) * (kTcDsElems - kDsG);
 
-__device__ __forceinline__ void ds_load_kb(const ChunkArgs& A, long long ch, float* sm, uint64_t* bar)
+__device__ __forceinline__ void ds_load_kb(const ChunkArgs& A, long long ck, float* sm, uint64_t* bar)
 {
     tc::mbar_expect_tx(bar, kDsBytesKb);
-    tc::bulk_g2s(sm + kDsKb, A.ws + A.o_DS + ch * kTcDsElems + kDsKb, kDsBytesKb, bar);
+    tc::bulk_g2s(sm + kSmKb, A.ws + A.o_DK + ck * kTcDkElems + kDkKb, kDsBytesKb, bar);
 }
-__device__ __forceinline__ void ds_load_rest(const ChunkArgs& A, long long ch, float* sm, uint64_t* bar)
+__device__ __forceinline__ void ds_load_rest(const ChunkArgs& A, long long ch, long long ck, float* sm,
+                                             uint64_t* bar)
 {
-    tc::mbar_expect_tx(bar, kDsBytesRest);
-    tc::bulk_g2s(sm + kDsTT, A.ws + A.o_DS + ch * kTcDsElems + kDsTT, kDsBytesRest, bar);
+    tc::mbar_expect_tx(bar, kDsBytesTT + kDsBytesQKT + kDsBytesTail);
+    tc::bulk_g2s(sm + kSmTT, A.ws + A.o_DS + ch * kTcDsElems + kDsTT, kDsBytesTT, bar);
+    tc::bulk_g2s(sm + kSmQKT, A.ws + A.o_DK + ck * kTcDkElems + kDkQKT, kDsBytesQKT, bar);
+    tc::bulk_g2s(sm + kSmG, A.ws + A.o_DS + ch * kTcDsElems + kDsG, kDsBytesTail, bar);
 }
 }  // namespace
 
@@ -412,6 +434,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
     const int hc = (warp >> 2) & 1;         // dM columns [64 hc, 64 hc + 64); chunk columns [16 hc, 16 hc + 16)
     const int h = blockIdx.x, n = blockIdx.y;
     const long long head = (long long)n * A.H_v + h;
+    const long long khead = (long long)n * A.H_k + h % A.H_k;
 
     if (tid == 0) {
         tc::mbar_init(bar_kb, 1);
@@ -430,8 +453,8 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
     uint32_t ph_kb = 0, ph_rest = 0, ph_mma = 0;
     bool kb_pending = false, rest_pending = false;
     if (issuer) {
-        ds_load_kb(A, head * A.n_chunks + c_last, sm, bar_kb);
-        ds_load_rest(A, head * A.n_chunks + c_last, sm, bar_rest);
+        ds_load_kb(A, khead * A.n_chunks + c_last, sm, bar_kb);
+        ds_load_rest(A, head * A.n_chunks + c_last, khead * A.n_chunks + c_last, sm, bar_rest);
         kb_pending = rest_pending = true;
     }
     float m[64];
@@ -451,9 +474,9 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
             for (int e = 0; e < 64; ++e) m[e] = 0.f;
         }
     }
-    const float* sE = sm + kDsE;
-    const float* sR = sm + kDsR;
-    const float* sGam = sm + kDsGam;
+    const float* sE = sm + kSmE;
+    const float* sR = sm + kSmR;
+    const float* sGam = sm + kSmGam;
     float* sA = sm + kDsA;
     const uint32_t id32 = tc::idesc_tf32(32), id128 = tc::idesc_tf32(128);
     // rows j of a 128 x 32 (rows j, K = t) tile: columns t of this thread, [16 hc, 16 hc + 16)
@@ -501,8 +524,8 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
             ph_kb ^= 1;
             kb_pending = false;
             if (!s_err) {
-                const uint64_t bhi = tc::tile_desc(sm + kDsKb, 32);
-                const uint64_t blo = tc::tile_desc(sm + kDsKb + 32 * TD, 32);
+                const uint64_t bhi = tc::tile_desc(sm + kSmKb, 32);
+                const uint64_t blo = tc::tile_desc(sm + kSmKb + 32 * TD, 32);
 #pragma unroll
                 for (int s = 0; s < TD / 8; ++s) {
                     const uint32_t ahi = tmem + kDsColHi + 8 * s, alo = tmem + kDsColLo + 8 * s;
@@ -513,9 +536,9 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
                 tc::commit(bar_mma);
                 if (!tc::mbar_wait(bar_rest, ph_rest)) s_err = 1;
                 if (!s_err) {
-                    const uint64_t ahi = tc::tile_desc(sm + kDsG, TD), alo = tc::tile_desc(sm + kDsG + BC * TD, TD);
-                    const uint64_t qhi = tc::tile_desc(sm + kDsQKT, TD);
-                    const uint64_t qlo = tc::tile_desc(sm + kDsQKT + 2 * BC * TD, TD);
+                    const uint64_t ahi = tc::tile_desc(sm + kSmG, TD), alo = tc::tile_desc(sm + kSmG + BC * TD, TD);
+                    const uint64_t qhi = tc::tile_desc(sm + kSmQKT, TD);
+                    const uint64_t qlo = tc::tile_desc(sm + kSmQKT + 2 * BC * TD, TD);
 #pragma unroll
                     for (int s = 0; s < BC / 8; ++s) {
                         const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
@@ -538,7 +561,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
         tc::fence_after();
         if (issuer) {
             if (ok && c > 0) {
-                ds_load_kb(A, ch - 1, sm, bar_kb);
+                ds_load_kb(A, khead * A.n_chunks + c - 1, sm, bar_kb);
                 kb_pending = true;
             }
         } else if (compute) {
@@ -570,7 +593,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
             rest_pending = false;
             tc::fence_after();
             const uint64_t ahi = tc::tile_desc(sA, TD), alo = tc::tile_desc(sA + BC * TD, TD);
-            const uint64_t bhi = tc::tile_desc(sm + kDsTT, 32), blo = tc::tile_desc(sm + kDsTT + 32 * 32, 32);
+            const uint64_t bhi = tc::tile_desc(sm + kSmTT, 32), blo = tc::tile_desc(sm + kSmTT + 32 * 32, 32);
 #pragma unroll
             for (int s = 0; s < BC / 8; ++s) {
                 const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
@@ -606,8 +629,8 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
         if (issuer) {
             tc::fence_after();
             const uint64_t ahi = tc::tile_desc(sA, TD), alo = tc::tile_desc(sA + BC * TD, TD);
-            const uint64_t qhi = tc::tile_desc(sm + kDsQKT, TD);
-            const uint64_t qlo = tc::tile_desc(sm + kDsQKT + 2 * BC * TD, TD);
+            const uint64_t qhi = tc::tile_desc(sm + kSmQKT, TD);
+            const uint64_t qlo = tc::tile_desc(sm + kSmQKT + 2 * BC * TD, TD);
 #pragma unroll
             for (int s = 0; s < BC / 8; ++s) {
                 const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
@@ -629,7 +652,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
         if (issuer) {
             if (c > 0) {
                 tc::fence_async_smem();
-                ds_load_rest(A, ch - 1, sm, bar_rest);
+                ds_load_rest(A, ch - 1, khead * A.n_chunks + c - 1, sm, bar_rest);
                 rest_pending = true;
             }
         } else if (compute) {
