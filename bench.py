@@ -55,9 +55,47 @@ def chunk_kernel_flops(N, T, H_v, d, C, which):
         "prep_bwd": ch * (4 if cps > 1 else 2) * b2d,
         "recompute": recomputed * 2 * bd2,
         "dstate": ch * (3 * bd2 + 2 * b2d),
-        "grad": ch * (4 * bd2 + 8 * b2d + 2 * BC ** 3),
+        "grad": ch * (4 * bd2 + 6 * b2d + 2 * BC ** 3),
+        "grad_tc": ch * (4 * bd2 + 6 * b2d + 2 * BC ** 3),
+        "dqdk_sum": 0,
     }[which]
     return 2.0 * fma
+
+
+# The head-size-128 chunked kernels run their products on the tensor cores as three tf32
+# passes; their roofline is the tf32 rate (the measured bf16 rate times the nominal
+# tf32 / bf16 ratio 1.1 / 2.25) divided by the three passes, in fp32 flops.
+TENSOR_KINDS = {"state_fwd", "recompute", "dstate", "grad_tc"}
+
+
+def kernel_plan(chunked, d, n_bwd, cps):
+    """(kernel name, flop kind) per launch of one forward and one backward, in order."""
+    if not chunked:
+        return [("gdn_fwd_kernel", None)], [("gdn_bwd_kernel", None), ("gdn_reduce_kernel", None)]
+    tensor = d == 128
+    st = "gdn_tc_state_kernel" if tensor else "gdn_chunk_state_kernel"
+    fwd = [("gdn_chunk_prep_kernel", "prep_fwd"), (st, "state_fwd")]
+    bwd = [("gdn_chunk_prep_kernel", "prep_bwd")]
+    if cps > 1:
+        bwd.append((st + "(recompute)", "recompute"))
+    bwd.append(("gdn_tc_dstate_kernel" if tensor else "gdn_chunk_dstate_kernel", "dstate"))
+    if tensor:
+        bwd += [("gdn_tc_grad_kernel", "grad_tc"), ("gdn_tc_dqdk_sum_kernel", "dqdk_sum")]
+    else:
+        bwd.append(("gdn_chunk_grad_kernel", "grad"))
+    assert len(bwd) == n_bwd, (len(bwd), n_bwd)
+    return fwd, bwd
+
+
+def tensor_peak_tflops():
+    """3xTF32 fp32-equivalent peak: measured bf16 x (1.1 / 2.25) / 3, and where it came from."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        bf16 = float(json.load(open(path))["bf16_tflops"])
+        src = "measured bf16 burst"
+    except (OSError, KeyError, ValueError):
+        bf16, src = 1900.0, "fallback bf16 1.9 PFLOP/s"
+    return bf16 * (1.1 / 2.25) / 3.0, src + " x nominal tf32/bf16 (1.1/2.25) / 3 passes"
 
 
 def _args():
@@ -139,7 +177,7 @@ class ClockSampler:
 def _kernel_sha():
     h = hashlib.sha256()
     for f in ("gdn_chunk.cu", "gdn_gemm.cuh", "gdn_bwd.cu", "gdn_fwd.cu", "gdn_device.cuh",
-              "gdn_internal.h", "gdn_api.cu"):
+              "gdn_internal.h", "gdn_api.cu", "gdn_tc.cuh", "gdn_tc_chain.cu", "gdn_tc_grad.cu"):
         h.update(open(os.path.join(ROOT, "gated_delta_rule_backward_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -288,14 +326,9 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     n_fwd, n_bwd = gdn.launches(p)
     chunked = not prob.kda
-    fwd_names = ["gdn_chunk_prep_kernel", "gdn_chunk_state_kernel"] if chunked else ["gdn_fwd_kernel"]
-    bwd_names = (["gdn_chunk_prep_kernel", "gdn_chunk_state_kernel(recompute)",
-                  "gdn_chunk_dstate_kernel", "gdn_chunk_grad_kernel"] if n_bwd == 4 else
-                 ["gdn_chunk_prep_kernel", "gdn_chunk_dstate_kernel", "gdn_chunk_grad_kernel"]
-                 if chunked else ["gdn_bwd_kernel", "gdn_reduce_kernel"])
-    kinds = (["prep_fwd", "state_fwd"] + (["prep_bwd", "recompute", "dstate", "grad"]
-                                          if n_bwd == 4 else ["prep_bwd", "dstate", "grad"])
-             if chunked else None)
+    fplan, bplan = kernel_plan(chunked, d, n_bwd, -(-C // BC))
+    fwd_names, bwd_names = [nm for nm, _ in fplan], [nm for nm, _ in bplan]
+    kinds = [k for _, k in fplan + bplan] if chunked else None
 
     def step():
         gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, fws, stream)
@@ -402,10 +435,16 @@ def run_ours(args):
     else:
         top_flops = (FWD_FLOPS(d) if top < n_fwd else BWD_FLOPS(d)) * head_tokens
     achieved = top_flops / (kern_ms[top] * 1e-3) / 1e12
+    if chunked and kinds[top] in TENSOR_KINDS:
+        peak, peak_src = tensor_peak_tflops()
+        bound = "tensor"
+    else:
+        peak, peak_src = FP32_PEAK_TFLOPS, "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.070 GHz"
+        bound = "alu"
     path_tflops = (FWD_FLOPS(d) + BWD_FLOPS(d)) * head_tokens / (step_ms * 1e-3) / 1e12
     kernels = [{"kernel": nm, "ms": kern_ms[j],
                 "tflops": (chunk_kernel_flops(N, T, H_v, d, C, kinds[j]) / (kern_ms[j] * 1e-3) / 1e12)
-                if chunked else None} for j, nm in enumerate(names)]
+                if chunked and kinds[j] != "dqdk_sum" else None} for j, nm in enumerate(names)]
     traffic = _recorded_traffic(names[top])
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -418,11 +457,11 @@ def run_ours(args):
                    "gate": "kda" if prob.kda else "scalar", "C": C, "qkv": "packed row views",
                    "l2": "flushed between timed steps (256 MiB write outside the events)",
                    "per_rank": "each rank runs the whole workload on its own GPU"},
-        "roofline": {"bound": "alu", "kernel": names[top],
-                     "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                     "frac": achieved / FP32_PEAK_TFLOPS, "traffic": traffic,
+        "roofline": {"bound": bound, "kernel": names[top],
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
                      "flops_per_launch": top_flops, "launch_ms": kern_ms[top],
-                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.070 GHz"},
+                     "peak_source": peak_src},
         "roofline_path": {"achieved": path_tflops, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                           "frac": path_tflops / FP32_PEAK_TFLOPS,
                           "flops_per_head_token": FWD_FLOPS(d) + BWD_FLOPS(d),

@@ -52,7 +52,8 @@ struct Plan {
     int cps = 1;          // chunks per checkpoint segment
     int64_t n_chunks = 0; // chunks per (sequence, value head)
     long long o_T = 0, o_QKD = 0, o_QDT = 0, o_gam = 0, o_r = 0, o_W = 0, o_U = 0, o_Mc = 0, o_dM = 0,
-              o_dDel = 0, o_dX = 0, o_Tr = 0, o_Z = 0, o_KK = 0, o_QK = 0, o_Dm = 0, o_W1 = 0, o_Q1 = 0, o_B23 = 0, o_DK = 0, o_DS = 0;
+              o_dDel = 0, o_dX = 0, o_Tr = 0, o_Z = 0, o_KK = 0, o_QK = 0, o_Dm = 0, o_W1 = 0, o_Q1 = 0, o_B23 = 0, o_DK = 0, o_DS = 0,
+              o_dqM = 0, o_dkM = 0;
     bool tensor = false;  // head size 128: the state chain runs on the tensor cores
     size_t fwd_ws_bytes = 0, bwd_ws_bytes = 0;
 };
@@ -172,8 +173,10 @@ Plan make_plan(const gdn_params_t* p)
         pl.o_dDel = o; o += al(CH * BC * D);
         pl.o_dX = o;   o += al(CH * BC * D);
         if (pl.tensor) {
-            pl.o_DK = o; o += al(CK * gdn::kTcDkElems);
-            pl.o_DS = o; o += al(CH * gdn::kTcDsElems);
+            pl.o_DK = o;  o += al(CK * gdn::kTcDkElems);
+            pl.o_DS = o;  o += al(CH * gdn::kTcDsElems);
+            pl.o_dqM = o; o += al(CH * BC * D);
+            pl.o_dkM = o; o += al(CH * BC * D);
         }
         pl.bwd_ws_bytes = (size_t)o * 4;
         pl.ws_bytes = pl.bwd_ws_bytes;
@@ -241,6 +244,7 @@ void fill_chunk_common(gdn::ChunkArgs& c, const gdn_params_t* p, const Plan& pl)
     c.o_U = pl.o_U; c.o_Mc = pl.o_Mc; c.o_dM = pl.o_dM; c.o_dDel = pl.o_dDel; c.o_dX = pl.o_dX;
     c.o_Tr = pl.o_Tr; c.o_Z = pl.o_Z; c.o_KK = pl.o_KK; c.o_QK = pl.o_QK; c.o_Dm = pl.o_Dm;
     c.o_W1 = pl.o_W1; c.o_Q1 = pl.o_Q1; c.o_B23 = pl.o_B23; c.o_DK = pl.o_DK; c.o_DS = pl.o_DS;
+    c.o_dqM = pl.o_dqM; c.o_dkM = pl.o_dkM;
     c.want_tc = pl.tensor;
 }
 
@@ -316,7 +320,8 @@ int gdn_backward_launches(const gdn_params_t* p)
     if (check_sizes(p) != GDN_OK) return 0;
     if (p->n_seq == 0) return 0;
     const Plan pl = make_plan(p);
-    if (pl.chunked) return pl.cps > 1 ? 4 : 3;
+    // chunked: prep, [recompute], dM chain, gradients (two kernels on the tensor-core path)
+    if (pl.chunked) return (pl.cps > 1 ? 4 : 3) + (pl.tensor ? 1 : 0);
     return p->T > 0 ? 2 : 1;
 }
 

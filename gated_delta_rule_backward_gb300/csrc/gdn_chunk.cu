@@ -1307,6 +1307,17 @@ static int chunk_backward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
     } else {
         GDN_LAUNCH(gdn_chunk_dstate_kernel<D>, dim3(Rows<D>::P, a.H_v, a.N), dstate_smem<D>());
     }
+    if constexpr (D == 128) {
+        if (a.want_tc) {
+            int e = launch_tc_grad(a, s);
+            if (e) return e;
+            tap.mark(s);
+            e = launch_tc_dqdk_sum(a, s);
+            if (e) return e;
+            tap.mark(s);
+            return 0;
+        }
+    }
     GDN_LAUNCH(gdn_chunk_grad_kernel<D>, dim3(a.n_chunks, a.H_k, a.N), grad_smem<D>());
     return 0;
 }

@@ -102,6 +102,7 @@ struct ChunkArgs {
     long long o_Tr, o_Z, o_KK, o_QK, o_Dm;  // backward: chunk factors for the gradient kernel
     long long o_W1, o_Q1, o_B23;            // tensor-core operands of the state chain
     long long o_DK, o_DS;                   // tensor-core operands of the dM chain
+    long long o_dqM, o_dkM;                 // tensor-core gradient step: per value head dq, dk
     int want_wu;
     int want_factors;
     int want_tc;                            // head size 128: state chain on the tensor cores
@@ -144,6 +145,12 @@ int launch_chunk_forward(const ChunkArgs& a, int D, void* stream, EventTap& tap)
 int launch_tc_state(const ChunkArgs& a, bool fwd, void* stream);
 // The dM chain on the tensor cores (gdn_tc_chain.cu).
 int launch_tc_dstate(const ChunkArgs& a, void* stream);
+// The gradient step on the tensor cores (gdn_tc_grad.cu): per (chunk, value head) every
+// gradient of the chunk (dv, dg, dbeta written; this value head's dq, dk parked row-major
+// [t][i] at o_dqM, o_dkM), then the sum of the value heads of each key head.
+int launch_tc_grad(const ChunkArgs& a, void* stream);
+int launch_tc_dqdk_sum(const ChunkArgs& a, void* stream);
+int tc_grad_take_status(void* stream, int* status);
 // Reads and clears the tensor-core kernels' device status word (0 or GDN_ERR_TIMEOUT),
 // synchronising `stream`.  Returns a cudaError_t as int.
 int tc_take_status(void* stream, int* status);

@@ -14,8 +14,8 @@
 // k-chunks) and stride byte offset SBO = 128 (the step between row groups); the K = 8
 // slice s of the tile starts 2 s LBO bytes in.
 //
-// Every wait on an mbarrier is bounded: it gives up after kSpinLimit polls and reports
-// the failure, so a kernel can record an error status and return instead of hanging.
+// Every wait on an mbarrier is bounded: it gives up after kWaitLimitNs and reports the
+// failure, so a kernel can record an error status and return instead of hanging.
 #pragma once
 
 #include <cstdint>
@@ -26,7 +26,7 @@
 namespace gdn {
 namespace tc {
 
-constexpr uint32_t kSpinLimit = 1u << 26;
+constexpr uint64_t kWaitLimitNs = 200000000ull;  // 0.2 s
 
 // Float offset of element (r, k) of an R-row operand tile in the layout above.
 GDN_HD inline int kmaj(int r, int k, int R)
@@ -223,11 +223,19 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 }
 __device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
-// Polls the phase with parity `parity` until it completes; false after kSpinLimit polls.
+// Polls the phase with parity `parity` until it completes; false once kWaitLimitNs of
+// wall-clock time (%globaltimer) have passed without it, far beyond any legitimate wait.
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
 {
     const uint32_t a = smem_addr(bar);
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    uint64_t start = 0;
+    for (uint32_t it = 0;; ++it) {
         uint32_t done;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -236,8 +244,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
             : "r"(a), "r"(parity)
             : "memory");
         if (done) return true;
+        if ((it & 255) == 0) {
+            const uint64_t now = global_ns();
+            if (it == 0)
+                start = now;
+            else if (now - start > kWaitLimitNs)
+                return false;
+        }
     }
-    return false;
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)

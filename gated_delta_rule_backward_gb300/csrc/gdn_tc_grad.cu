@@ -1,0 +1,709 @@
+// gdn_tc_grad.cu -- the gradient step of the chunked backward (scalar gate, head size
+// 128) on the 5th-generation tensor cores: one CTA per (chunk, value head) computes every
+// gradient of the chunk for that value head, and a small kernel sums the value heads of
+// each key head.
+//
+// With M = M_c the chunk-entry state, dM = dM_end the gradient of the chunk's end state
+// (128 x 128, rows j = value index, columns i = key index) and the chunk's rows t, the
+// chunked form of the recurrence of "metal: GATED_DELTA_NET_BACK" (derived in
+// gdn_chunk.cu) gives, through the chain rule:
+//   X      = V - diag(gamma) K M^T          D_X = M K^T             (A = M,     rows j)
+//   Delta  = T X                            CUDA cores, rows j in registers
+//   D2     = M^T [s gamma dY ; -gamma dX]^T                           (A = M^T,   rows i)
+//   D3     = dM^T Delta^T                                             (A = dM^T,  rows i)
+//   D4     = [dY ; dDelta ; 0] [Delta ; X]^T   its blocks dY Delta^T and dDelta X^T
+//   the 32 x 32 algebra of T, Z, the decay matrix and the gate (CUDA cores), giving P
+//   (the Dm-weighted lower(s dY Delta^T)) and S (the symmetrised key-key gradient)
+//   D2    += [K^T P^T | Q^T P + K^T S]      (A = [Q^T | K^T] from the prep kernel, rows i)
+//   dq_h = D2[:, 0:32]^T,   dk_h = (D2[:, 32:64] + D3 diag(r))^T,   dv = dX,
+//   dg (reverse scan of the gate gradient), dbeta.
+// Every product is a three-pass tf32 split with an fp32 accumulator in TMEM (gdn_tc.cuh);
+// the A operands built here go to TMEM, the B operands to padded shared-memory tiles.
+#include <cuda_runtime.h>
+
+#include "gdn_gemm.cuh"
+#include "gdn_internal.h"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+// Status word of this file's kernel: 0, or GDN_ERR_TIMEOUT (6) after a bounded wait gave up.
+__device__ int g_tcg_status;
+
+namespace {
+
+constexpr int TD = 128;
+constexpr int GT = 288;           // 8 compute warps + the issuer warp
+constexpr int kIss = 256;
+constexpr uint32_t kCA = 0;       // TMEM: A operand, hi in 0..127, lo in 128..255
+constexpr uint32_t kCX = 256;     //       D_X (32)
+constexpr uint32_t kC2 = 288;     //       D2  (64: dq part, dk part)
+constexpr uint32_t kC3 = 352;     //       D3  (32)
+constexpr uint32_t kC4 = 384;     //       D4  (64)
+constexpr uint32_t kCols = 512;
+constexpr int kStatusTimeout = 6;
+constexpr int LDF = BC + 4;       // leading dimension of the 32 x 32 fp32 tiles
+
+// B tiles built here: k-chunk-major with a 16-byte pad between k-chunks, so that 32
+// threads writing one row (32 consecutive k) hit 32 distinct banks.
+__device__ __forceinline__ int padoff(int r, int k, int lbo_floats)
+{
+    return (k >> 2) * lbo_floats + ((r >> 3) << 5) + ((r & 7) << 2) + (k & 3);
+}
+constexpr int kLbo64 = 8 * 128 + 16;        // bytes between k-chunks, 64-row tile
+constexpr int kT64 = 32 * kLbo64 / 4;       // floats per 64-row, K = 128 tile (hi or lo)
+constexpr int kLbo32 = 4 * 128 + 16;        // 32-row tile
+constexpr int kTP = 8 * kLbo32 / 4;         // 32 rows, K = 32
+constexpr int kTPS = 16 * kLbo32 / 4;       // 32 rows, K = 64
+constexpr int kLdM = TD + 4;                // fp32 staging of M / dM, row-major
+
+// shared memory (floats): three big regions reused phase by phase, then small arrays
+constexpr int kR0 = 0;                      // K tile (prep's layout) | [Delta ; X] tile hi, lo
+constexpr int kR1 = kR0 + 2 * kT64;         // [s gamma dY ; -gamma dX] hi, lo | dDelta rows |
+                                            // 32 x 32 algebra tiles and the P, [P ; S] tiles
+constexpr int kR2 = kR1 + 2 * kT64;         // M, then dM, fp32 staging | [Q^T | K^T] tile
+constexpr int kR3 = kR2 + TD * kLdM;
+constexpr int kSTr = kR3;                   // T, Z, KK^T, QK^T, Dm: row-major 32 x 32 each
+constexpr int kSZ = kSTr + BC * BC;
+constexpr int kSKK = kSZ + BC * BC;
+constexpr int kSQK = kSKK + BC * BC;
+constexpr int kSDm = kSQK + BC * BC;
+constexpr int kSGam = kSDm + BC * BC;       // gamma, r (bulk copied), beta
+constexpr int kSR = kSGam + BC;
+constexpr int kSB = kSR + BC;
+constexpr int kSRed = kSB + BC;             // 4 lane quarters x 96 partial sums
+constexpr int kSVec = kSRed + 4 * 96;       // gdg, dr, dG, dbeta, dot
+constexpr int kGFloats = kSVec + 4 * BC + 4;
+constexpr size_t kGSmemBytes = sizeof(float) * kGFloats + 64;
+static_assert(kGSmemBytes <= 227 * 1024, "shared memory");
+// 32 x 32 tiles in R1 after D2 is done: Ps, Ss, dTs, W1, W2, Zs (LDF), then the B tiles
+constexpr int kAPs = kR1;
+constexpr int kASs = kAPs + BC * LDF;
+constexpr int kAdT = kASs + BC * LDF;
+constexpr int kAW1 = kAdT + BC * LDF;
+constexpr int kAW2 = kAW1 + BC * LDF;
+constexpr int kAZ = kAW2 + BC * LDF;
+constexpr int kABP = kAZ + BC * LDF;        // P (rows t, K = 32) hi, lo
+constexpr int kABPS = kABP + 2 * kTP;       // [P ; S]^T (rows t, K = 64) hi, lo
+static_assert(kABPS + 2 * kTPS <= kR2, "R1 overflow");
+constexpr int kDdStage = kR1 + 6 * BC * LDF;   // dDelta rows t (32 x kLdM), before the algebra
+static_assert(kDdStage + BC * kLdM <= kR2, "R1 overflow");
+
+constexpr uint32_t kBytesKb = sizeof(float) * 2 * 32 * 128;
+constexpr uint32_t kBytesFac = sizeof(float) * 5 * BC * BC;
+constexpr uint32_t kBytesGR = sizeof(float) * 2 * BC;
+constexpr uint32_t kBytesQKT = sizeof(float) * 2 * 128 * 64;
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ void put_split(float* tile, int half, int off, float x)
+{
+    uint32_t hi, lo;
+    tc::split_tf32(x, hi, lo);
+    tile[off] = __uint_as_float(hi);
+    tile[half + off] = __uint_as_float(lo);
+}
+
+// Issues a K-slices [s0, s1) three-pass product D (+)= A B^T, A in TMEM (column base a).
+__device__ __forceinline__ void mma3_t(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t b_hi, uint64_t b_lo,
+                                       uint32_t lbo, int s0, int s1, uint32_t idesc, bool acc)
+{
+    for (int s = s0; s < s1; ++s) {
+        const uint64_t off = (uint64_t)((2 * lbo * s) >> 4);
+        tc::mma_ts(d, a_hi + 8 * s, b_hi + off, idesc, (acc || s > s0) ? 1u : 0u);
+        tc::mma_ts(d, a_hi + 8 * s, b_lo + off, idesc, 1);
+        tc::mma_ts(d, a_lo + 8 * s, b_hi + off, idesc, 1);
+    }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
+{
+    extern __shared__ __align__(1024) float sm[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kGFloats);
+    uint64_t* bar_ld = bars;       // K tile, chunk factors, gamma, r
+    uint64_t* bar_qkt = bars + 1;  // [Q^T | K^T]
+    uint64_t* bar_mma = bars + 2;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_err;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool compute = warp < 8;
+    const bool issuer = tid == kIss;
+    const int row = 32 * (warp & 3) + lane;  // this thread's TMEM lane
+    const int hc = (warp >> 2) & 1;          // half: 64 of the K columns, 16 of the 32 tokens
+    const int tb = 16 * hc;                  // this thread's tokens [tb, tb + 16)
+    const int c = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int hk = h % A.H_k;
+    const long long head = (long long)n * A.H_v + h;
+    const long long ch = head * A.n_chunks + c;
+    const long long ck = ((long long)n * A.H_k + hk) * A.n_chunks + c;
+    const int seg = c / A.cps, loc = c - seg * A.cps;
+    const int t0 = seg * A.C + loc * BC;
+    const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
+    const long long tok0 = (long long)n * A.T + t0;
+
+    if (tid == 0) {
+        tc::mbar_init(bar_ld, 1);
+        tc::mbar_init(bar_qkt, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::mbar_fence_init();
+        s_err = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, kCols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t aHi = tmem + kCA, aLo = tmem + kCA + 128;
+    if (issuer) {
+        tc::mbar_expect_tx(bar_ld, kBytesKb + kBytesFac + kBytesGR);
+        tc::bulk_g2s(sm + kR0, A.ws + A.o_DK + ck * kTcDkElems + kDkKb, kBytesKb, bar_ld);
+        const long long f = ch * (BC * BC);
+        tc::bulk_g2s(sm + kSTr, A.ws + A.o_Tr + f, sizeof(float) * BC * BC, bar_ld);
+        tc::bulk_g2s(sm + kSZ, A.ws + A.o_Z + f, sizeof(float) * BC * BC, bar_ld);
+        tc::bulk_g2s(sm + kSKK, A.ws + A.o_KK + f, sizeof(float) * BC * BC, bar_ld);
+        tc::bulk_g2s(sm + kSQK, A.ws + A.o_QK + f, sizeof(float) * BC * BC, bar_ld);
+        tc::bulk_g2s(sm + kSDm, A.ws + A.o_Dm + f, sizeof(float) * BC * BC, bar_ld);
+        tc::bulk_g2s(sm + kSGam, A.ws + A.o_gam + ch * BC, sizeof(float) * BC, bar_ld);
+        tc::bulk_g2s(sm + kSR, A.ws + A.o_r + ch * BC, sizeof(float) * BC, bar_ld);
+    }
+    float* sM = sm + kR2;
+    const bool m_unit = loc > 0;  // M: a parked state (unit layout) or the row-major checkpoint
+    const float* sGam = sm + kSGam;
+    const float* sR = sm + kSR;
+    float* sB = sm + kSB;
+    float* red = sm + kSRed;
+    float* vec = sm + kSVec;  // gdg, dr, dG, dbeta, dot
+
+    // (0) stage M (row-major fp32) and build A = M (rows j)
+    if (compute) {
+        if (tid < BC) {
+            const bool real = tid < nb;
+            sB[tid] = real ? __ldg(A.beta + (tok0 + tid) * A.H_v + h) : 0.f;
+        }
+        const float4* Mg4 = reinterpret_cast<const float4*>(
+            m_unit ? A.ws + A.o_Mc + ch * (long long)(TD * TD) : A.ckpt + (head * A.n_ck + seg) * (long long)(TD * TD));
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {  // 16 float4 per thread, 8 in flight at a time
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldg(Mg4 + tid + 256 * (8 * half + u));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = tid + 256 * (8 * half + u);
+                const int j = m_unit ? idx % TD : idx >> 5, i4 = m_unit ? idx / TD : idx & 31;
+                *reinterpret_cast<float4*>(sM + j * kLdM + 4 * i4) = v[u];
+            }
+        }
+        tc::bar_sync_first(256);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 a = *reinterpret_cast<const float4*>(sM + row * kLdM + 64 * hc + 8 * q);
+            const float4 b = *reinterpret_cast<const float4*>(sM + row * kLdM + 64 * hc + 8 * q + 4);
+            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tc::split_tf32(v[e], hi[e], lo[e]);
+            tc::st8(tc::taddr(tmem, warp, kCA + 64 * hc + 8 * q), hi);
+            tc::st8(tc::taddr(tmem, warp, kCA + 128 + 64 * hc + 8 * q), lo);
+        }
+        tc::wait_st();
+    }
+    tc::fence_before();
+    __syncthreads();
+
+    // (1) D_X = M K^T.  Meanwhile: the B tile [s gamma dY ; -gamma dX], dv, and V for X.
+    float vx[32];
+    if (issuer) {
+        tc::fence_after();
+        if (!tc::mbar_wait(bar_ld, 0)) s_err = 1;
+        if (!s_err) {
+            mma3_t(tmem + kCX, aHi, aLo, tc::tile_desc(sm + kR0, 32), tc::tile_desc(sm + kR0 + 32 * TD, 32),
+                   (32 / 8) * 128, 0, TD / 8, tc::idesc_tf32(32), false);
+            tc::commit(bar_mma);
+        }
+    } else if (compute) {
+        if (!tc::mbar_wait(bar_ld, 0)) s_err = 1;
+        float* b2 = sm + kR1;
+        const float* gy = A.gy + (long long)n * A.gys0 + (long long)t0 * A.gys1 + (long long)h * A.gys2 + row;
+        const float4* dx4 = reinterpret_cast<const float4*>(A.ws + A.o_dX + ch * (BC * TD));
+        const float* vp = A.v + (long long)n * A.vs0 + (long long)t0 * A.vs1 + (long long)h * A.vs2 + row;
+        float dy[16];
+        float4 dx[4];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dy[e] = (tb + e < nb) ? __ldg(gy + (long long)(tb + e) * A.gys1) : 0.f;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) dx[b] = __ldg(dx4 + (4 * hc + b) * TD + row);
+#pragma unroll
+        for (int t = 0; t < BC; ++t) vx[t] = (t < nb) ? __ldg(vp + (long long)t * A.vs1) : 0.f;
+        float* dvp = A.dv + (tok0 * A.H_v + h) * TD + row;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float dxv[4] = {dx[b].x, dx[b].y, dx[b].z, dx[b].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = tb + 4 * b + e;
+                put_split(b2, kT64, padoff(t, row, kLbo64 / 4), __fmul_rn(__fmul_rn(A.scale, sGam[t]), dy[4 * b + e]));
+                put_split(b2, kT64, padoff(BC + t, row, kLbo64 / 4), -__fmul_rn(sGam[t], dxv[e]));
+                if (t < nb) dvp[(long long)t * A.H_v * TD] = dxv[e];
+            }
+        }
+    }
+    uint32_t ph = 0;
+    bool ok = tc::mbar_wait(bar_mma, ph);
+    ph ^= 1;
+    tc::fence_after();
+    // (2) X^T, Delta^T (rows j) -> the [Delta ; X] tile; A = M^T (rows i)
+    if (compute) {
+        const float* sT = sm + kSTr;
+        float x[32];
+        tc::ld32(tc::taddr(tmem, warp, kCX), x);
+        tc::wait_ld();
+#pragma unroll
+        for (int t = 0; t < BC; ++t) x[t] = __fsub_rn(vx[t], __fmul_rn(sGam[t], x[t]));
+        float* b34 = sm + kR0;  // the K tile is dead: D_X is done
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int t = tb + e;
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < BC; ++k) acc = __fmaf_rn(sT[t * BC + k], x[k], acc);
+            put_split(b34, kT64, padoff(t, row, kLbo64 / 4), acc);
+            put_split(b34, kT64, padoff(BC + t, row, kLbo64 / 4), hc ? x[16 + e] : x[e]);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tc::split_tf32(sM[(64 * hc + 8 * q + e) * kLdM + row], hi[e], lo[e]);
+            tc::st8(tc::taddr(tmem, warp, kCA + 64 * hc + 8 * q), hi);
+            tc::st8(tc::taddr(tmem, warp, kCA + 128 + 64 * hc + 8 * q), lo);
+        }
+        tc::wait_st();
+    }
+    if (!ok) s_err = 1;
+    tc::fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    if (s_err) goto done;
+    // (3) D2 = M^T [s gamma dY ; -gamma dX]^T.  Meanwhile dM replaces M in the staging, with
+    //     <dM, M> on the way, and q_t, k_t (this thread's tokens) for the dgamma and dr sums.
+    float qv[16], kv[16];
+    if (issuer) {
+        tc::fence_after();
+        mma3_t(tmem + kC2, aHi, aLo, tc::make_desc(tc::smem_addr(sm + kR1), kLbo64, 128),
+               tc::make_desc(tc::smem_addr(sm + kR1 + kT64), kLbo64, 128), kLbo64, 0, TD / 8,
+               tc::idesc_tf32(64), false);
+        tc::commit(bar_mma);
+    } else if (compute) {
+        const float* qp = A.q + (long long)n * A.qs0 + (long long)t0 * A.qs1 + (long long)hk * A.qs2 + row;
+        const float* kp = A.k + (long long)n * A.ks0 + (long long)t0 * A.ks1 + (long long)hk * A.ks2 + row;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            qv[e] = (tb + e < nb) ? __ldg(qp + (long long)(tb + e) * A.qs1) : 0.f;
+            kv[e] = (tb + e < nb) ? __ldg(kp + (long long)(tb + e) * A.ks1) : 0.f;
+        }
+        const float4* dM4 = reinterpret_cast<const float4*>(A.ws + A.o_dM + ch * (long long)(TD * TD));
+        float dot = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldg(dM4 + tid + 256 * (8 * half + u));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = tid + 256 * (8 * half + u);
+                const int j = idx % TD, i4 = idx / TD;
+                float4* p = reinterpret_cast<float4*>(sM + j * kLdM + 4 * i4);
+                const float4 m = *p;
+                dot = __fmaf_rn(v[u].x, m.x, dot);
+                dot = __fmaf_rn(v[u].y, m.y, dot);
+                dot = __fmaf_rn(v[u].z, m.z, dot);
+                dot = __fmaf_rn(v[u].w, m.w, dot);
+                *p = v[u];
+            }
+        }
+        dot = warp_sum(dot);
+        if (lane == 0) red[(warp & 3) * 96 + 64 + hc] = dot;
+    }
+    ok = tc::mbar_wait(bar_mma, ph);
+    ph ^= 1;
+    tc::fence_after();
+    // (4) gamma dgamma partials from D2; A = dM^T (rows i)
+    if (compute) {
+        tc::bar_sync_first(256);  // dM fully staged
+        float dq[16], dk[16];
+        tc::ld16(tc::taddr(tmem, warp, kC2 + tb), dq);
+        tc::ld16(tc::taddr(tmem, warp, kC2 + BC + tb), dk);
+        tc::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float g = warp_sum(__fmaf_rn(kv[e], dk[e], __fmul_rn(qv[e], dq[e])));
+            if (lane == 0) red[(warp & 3) * 96 + tb + e] = g;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tc::split_tf32(sM[(64 * hc + 8 * q + e) * kLdM + row], hi[e], lo[e]);
+            tc::st8(tc::taddr(tmem, warp, kCA + 64 * hc + 8 * q), hi);
+            tc::st8(tc::taddr(tmem, warp, kCA + 128 + 64 * hc + 8 * q), lo);
+        }
+        tc::wait_st();
+    }
+    if (!ok) s_err = 1;
+    tc::fence_before();
+    __syncthreads();
+    if (s_err) goto done;
+    // (5) D3 = dM^T Delta^T, then [Q^T | K^T] into the staging region.  Meanwhile dDelta
+    //     (rows t) into R1.
+    if (issuer) {
+        tc::fence_after();
+        mma3_t(tmem + kC3, aHi, aLo, tc::make_desc(tc::smem_addr(sm + kR0), kLbo64, 128),
+               tc::make_desc(tc::smem_addr(sm + kR0 + kT64), kLbo64, 128), kLbo64, 0, TD / 8,
+               tc::idesc_tf32(32), false);
+        tc::commit(bar_mma);
+        tc::fence_async_smem();
+        tc::mbar_expect_tx(bar_qkt, kBytesQKT);
+        tc::bulk_g2s(sm + kR2, A.ws + A.o_DK + ck * kTcDkElems + kDkQKT, kBytesQKT, bar_qkt);
+    } else if (compute) {
+        float* sdd = sm + kDdStage;
+        const float4* dd4 = reinterpret_cast<const float4*>(A.ws + A.o_dDel + ch * (BC * TD));
+        float4 d[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) d[u] = __ldg(dd4 + tid + 256 * u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + 256 * u;
+            const int j = idx % TD, t = 4 * (idx / TD);
+            sdd[t * kLdM + j] = d[u].x;
+            sdd[(t + 1) * kLdM + j] = d[u].y;
+            sdd[(t + 2) * kLdM + j] = d[u].z;
+            sdd[(t + 3) * kLdM + j] = d[u].w;
+        }
+    }
+    ok = tc::mbar_wait(bar_mma, ph);
+    ph ^= 1;
+    tc::fence_after();
+    // (6) dr partials from D3 (kept for dk); A = [dY ; dDelta ; 0] (rows t)
+    float d3[16];
+    if (compute) {
+        tc::bar_sync_first(256);  // dDelta staged
+        tc::ld16(tc::taddr(tmem, warp, kC3 + tb), d3);
+        tc::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float g = warp_sum(__fmul_rn(kv[e], d3[e]));
+            if (lane == 0) red[(warp & 3) * 96 + BC + tb + e] = g;
+        }
+        const int quarter = warp & 3;
+        const float* gyr = A.gy + (long long)n * A.gys0 + (long long)(t0 + lane) * A.gys1 + (long long)h * A.gys2 + 64 * hc;
+        const float* sdd = sm + kDdStage + lane * kLdM + 64 * hc;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {  // 32 of this thread's 64 columns at a time
+            float v[32];
+            if (quarter == 0) {  // rows 0..31: dY row t = lane
+                if (lane < nb && A.vec_gy) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float4 x = __ldg(reinterpret_cast<const float4*>(gyr + 32 * half) + u);
+                        v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = (lane < nb) ? __ldg(gyr + 32 * half + e) : 0.f;
+                }
+            } else if (quarter == 1) {  // rows 32..63: dDelta row t = lane
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = sdd[32 * half + e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) tc::split_tf32(v[8 * q + e], hi[e], lo[e]);
+                const int j0 = 64 * hc + 32 * half + 8 * q;
+                tc::st8(tc::taddr(tmem, warp, kCA + j0), hi);
+                tc::st8(tc::taddr(tmem, warp, kCA + 128 + j0), lo);
+            }
+        }
+        tc::wait_st();
+    }
+    if (!ok) s_err = 1;
+    tc::fence_before();
+    __syncthreads();
+    if (s_err) goto done;
+    // (7) D4 = [dY ; dDelta ; 0] [Delta ; X]^T.  Meanwhile the scalars.
+    if (issuer) {
+        tc::fence_after();
+        mma3_t(tmem + kC4, aHi, aLo, tc::make_desc(tc::smem_addr(sm + kR0), kLbo64, 128),
+               tc::make_desc(tc::smem_addr(sm + kR0 + kT64), kLbo64, 128), kLbo64, 0, TD / 8,
+               tc::idesc_tf32(64), false);
+        tc::commit(bar_mma);
+    } else if (compute) {
+        if (tid < 2 * BC) {
+            vec[tid] = __fadd_rn(__fadd_rn(red[tid], red[96 + tid]), __fadd_rn(red[192 + tid], red[288 + tid]));
+        } else if (tid == 2 * BC) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) v = __fadd_rn(v, __fadd_rn(red[w * 96 + 64], red[w * 96 + 65]));
+            vec[4 * BC] = v;
+        }
+        // Z into an LDF tile (operand of two small products)
+        float* Zs = sm + kAZ;
+        for (int idx = tid; idx < BC * BC; idx += 256) Zs[(idx >> 5) * LDF + (idx & 31)] = sm[kSZ + idx];
+    }
+    ok = tc::mbar_wait(bar_mma, ph);
+    ph ^= 1;
+    tc::fence_after();
+    if (compute) {
+        // (8) the 32 x 32 algebra.  D4 blocks: rows 0..31 cols 0..31 = dY Delta^T,
+        //     rows 32..63 cols 32..63 = dDelta X^T.
+        float* Ps = sm + kAPs;
+        float* Ss = sm + kASs;
+        float* dTs = sm + kAdT;
+        float* W1 = sm + kAW1;
+        float* W2 = sm + kAW2;
+        const float* Zs = sm + kAZ;
+        const float* Dm = sm + kSDm;
+        const float* KKm = sm + kSKK;
+        const float* QKm = sm + kSQK;
+        const float* bs = sB;
+        float* gdg = vec;
+        float* dr = vec + BC;
+        float* dG = vec + 2 * BC;
+        float* dbs = vec + 3 * BC;
+        const float dot = vec[4 * BC];
+        if (warp == 0 || warp == 1) {
+            float v[32];
+            tc::ld32(tc::taddr(tmem, warp, kC4 + BC * warp), v);
+            tc::wait_ld();
+            const int t = lane;
+#pragma unroll
+            for (int tau = 0; tau < BC; ++tau) {
+                if (warp == 0)
+                    Ps[t * LDF + tau] = (tau <= t) ? __fmul_rn(A.scale, v[tau]) : 0.f;
+                else
+                    dTs[t * LDF + tau] = (tau <= t) ? v[tau] : 0.f;
+            }
+        }
+        tc::bar_sync_first(256);
+        // dZ = dT diag(beta); dbeta_a[tau] = sum_t Z[t][tau] dT[t][tau]
+        for (int idx = tid; idx < BC * BC; idx += 256) {
+            const int t = idx >> 5, tau = idx & 31;
+            W1[t * LDF + tau] = __fmul_rn(dTs[t * LDF + tau], bs[tau]);
+        }
+        if (tid < BC) {
+            float s = 0.f;
+            for (int t = tid; t < BC; ++t) s = __fmaf_rn(Zs[t * LDF + tid], dTs[t * LDF + tid], s);
+            dbs[tid] = s;
+        }
+        tc::bar_sync_first(256);
+        {  // P1 = dZ Z^T
+            using Map = GemmMap<BC, BC, 2, 2, true>;
+            float acc[2][2];
+            zero_acc(acc);
+            block_gemm<BC, BC, 2, 2, false, true>(acc, W1, LDF, Zs, LDF, BC, tid);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) W2[Map::row(tid, i) * LDF + Map::col(tid, j)] = acc[i][j];
+        }
+        tc::bar_sync_first(256);
+        {  // dA = strict_lower(-Z^T P1)
+            using Map = GemmMap<BC, BC, 1, 4, false>;
+            float acc[1][4];
+            zero_acc(acc);
+            block_gemm<BC, BC, 1, 4, true, false>(acc, Zs, LDF, W2, LDF, BC, tid);
+            const int t = Map::row(tid, 0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int tau = Map::col(tid, j);
+                W1[t * LDF + tau] = (tau < t) ? -acc[0][j] : 0.f;
+            }
+        }
+        tc::bar_sync_first(256);
+        // dL = beta_t dA; dKK = dL (.) Dm; dD = dQKD (.) QK + dL (.) KK (+ dr on the last row);
+        // the E = dD (.) Dm sums give the gate gradient
+        for (int idx = tid; idx < BC * BC; idx += 256) {
+            const int t = idx >> 5, tau = idx & 31;
+            const float dm = Dm[idx];
+            const float dA = W1[t * LDF + tau];
+            const float dL = __fmul_rn(bs[t], dA);
+            float dD = __fmul_rn(Ps[t * LDF + tau], QKm[idx]);
+            dD = __fmaf_rn(dL, KKm[idx], dD);
+            if (t == BC - 1) dD = __fadd_rn(dD, dr[tau]);
+            Ss[t * LDF + tau] = __fmul_rn(dL, dm);
+            Ps[t * LDF + tau] = __fmul_rn(Ps[t * LDF + tau], dm);
+            dTs[t * LDF + tau] = __fmul_rn(dD, dm);
+        }
+        tc::bar_sync_first(256);
+        if (tid < BC) {
+            const int t = tid;
+            float rs = 0.f, cs = 0.f, bb = 0.f;
+            for (int tau = 0; tau < BC; ++tau) {
+                rs = __fadd_rn(rs, dTs[t * LDF + tau]);
+                cs = __fadd_rn(cs, dTs[tau * LDF + t]);
+                bb = __fmaf_rn(W1[t * LDF + tau], __fmul_rn(Dm[t * BC + tau], KKm[t * BC + tau]), bb);
+            }
+            float g = gdg[t];
+            if (t == BC - 1) g = __fmaf_rn(sGam[t], dot, g);
+            dG[t] = __fadd_rn(__fadd_rn(g, rs), -cs);
+            dbs[t] = __fadd_rn(dbs[t], bb);
+        }
+        tc::bar_sync_first(256);
+        if (warp == 0) {  // dg = reverse cumsum of dG; dbeta
+            float x = dG[BC - 1 - lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x = __fadd_rn(x, y);
+            }
+            const int t = BC - 1 - lane;
+            if (t < nb) {
+                A.dg[(tok0 + t) * A.H_v + h] = x;
+                A.dbeta[(tok0 + t) * A.H_v + h] = dbs[t];
+            }
+        }
+        // B tiles of the last products: P (rows t, K = t'), [P ; S]^T (rows t, K = t' < 64);
+        // S is the symmetric dKK + dKK^T of its strict lower part
+        float* bp = sm + kABP;
+        float* bps = sm + kABPS;
+        for (int idx = tid; idx < BC * BC; idx += 256) {
+            const int t = idx & 31, tau = idx >> 5;  // consecutive threads: consecutive rows t
+            const float s = (tau > t) ? Ss[tau * LDF + t] : (tau < t ? Ss[t * LDF + tau] : 0.f);
+            put_split(bp, kTP, padoff(t, tau, kLbo32 / 4), Ps[t * LDF + tau]);
+            put_split(bps, kTPS, padoff(t, tau, kLbo32 / 4), Ps[tau * LDF + t]);
+            put_split(bps, kTPS, padoff(t, BC + tau, kLbo32 / 4), s);
+        }
+    }
+    tc::fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    // (9) D2 += [K^T P^T | Q^T P + K^T S]
+    if (issuer) {
+        tc::fence_after();
+        if (!tc::mbar_wait(bar_qkt, 0)) s_err = 1;
+        if (!s_err) {
+            const uint64_t qhi = tc::tile_desc(sm + kR2, TD), qlo = tc::tile_desc(sm + kR2 + 2 * BC * TD, TD);
+            const uint32_t id32 = tc::idesc_tf32(32);
+            // dq part: A = K^T (k-slices 4..7 of [Q^T | K^T]), B = P
+            const uint64_t phi = tc::make_desc(tc::smem_addr(sm + kABP), kLbo32, 128);
+            const uint64_t plo = tc::make_desc(tc::smem_addr(sm + kABP + kTP), kLbo32, 128);
+#pragma unroll
+            for (int s = 0; s < BC / 8; ++s) {
+                const uint64_t a_h = tc::desc_kslice(qhi, TD, s + BC / 8), a_l = tc::desc_kslice(qlo, TD, s + BC / 8);
+                const uint64_t off = (uint64_t)((2 * kLbo32 * s) >> 4);
+                tc::mma_ss(tmem + kC2, a_h, phi + off, id32, 1);
+                tc::mma_ss(tmem + kC2, a_h, plo + off, id32, 1);
+                tc::mma_ss(tmem + kC2, a_l, phi + off, id32, 1);
+            }
+            // dk part: A = [Q^T | K^T], B = [P ; S]^T
+            const uint64_t shi = tc::make_desc(tc::smem_addr(sm + kABPS), kLbo32, 128);
+            const uint64_t slo = tc::make_desc(tc::smem_addr(sm + kABPS + kTPS), kLbo32, 128);
+#pragma unroll
+            for (int s = 0; s < 2 * BC / 8; ++s) {
+                const uint64_t a_h = tc::desc_kslice(qhi, TD, s), a_l = tc::desc_kslice(qlo, TD, s);
+                const uint64_t off = (uint64_t)((2 * kLbo32 * s) >> 4);
+                tc::mma_ss(tmem + kC2 + BC, a_h, shi + off, id32, 1);
+                tc::mma_ss(tmem + kC2 + BC, a_h, slo + off, id32, 1);
+                tc::mma_ss(tmem + kC2 + BC, a_l, shi + off, id32, 1);
+            }
+            tc::commit(bar_mma);
+        }
+    }
+    ok = tc::mbar_wait(bar_mma, ph);
+    tc::fence_after();
+    // (10) this value head's dq and dk (rows i = row, tokens [tb, tb + 16)) -> workspace
+    if (compute && ok) {
+        float dq[16], dk[16];
+        tc::ld16(tc::taddr(tmem, warp, kC2 + tb), dq);
+        tc::ld16(tc::taddr(tmem, warp, kC2 + BC + tb), dk);
+        tc::wait_ld();
+        float* dqo = A.ws + A.o_dqM + ch * (BC * TD) + row;
+        float* dko = A.ws + A.o_dkM + ch * (BC * TD) + row;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int t = tb + e;
+            dqo[t * TD] = dq[e];
+            dko[t * TD] = __fmaf_rn(sR[t], d3[e], dk[e]);
+        }
+    }
+    if (!ok) s_err = 1;
+done:
+    __syncthreads();
+    if (s_err && issuer) atomicExch(&g_tcg_status, kStatusTimeout);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) tc::tmem_free(tmem, kCols);
+}
+
+// dq, dk of each key head: the value heads' parts summed in ascending order.
+__global__ void __launch_bounds__(256) gdn_tc_dqdk_sum_kernel(const ChunkArgs A)
+{
+    const int c = blockIdx.x, hk = blockIdx.y, n = blockIdx.z;
+    const int seg = c / A.cps, loc = c - seg * A.cps;
+    const int t0 = seg * A.C + loc * BC;
+    const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
+    const int r = A.H_v / A.H_k;
+    for (int idx = threadIdx.x; idx < nb * (TD / 4); idx += 256) {
+        const int t = idx / (TD / 4), i4 = idx - t * (TD / 4);
+        float4 q = make_float4(0.f, 0.f, 0.f, 0.f), k = q;
+        for (int rho = 0; rho < r; ++rho) {
+            const long long ch = ((long long)n * A.H_v + hk + rho * A.H_k) * A.n_chunks + c;
+            const float4 a = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_dqM + ch * (BC * TD) + t * TD) + i4);
+            const float4 b = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_dkM + ch * (BC * TD) + t * TD) + i4);
+            q = make_float4(__fadd_rn(q.x, a.x), __fadd_rn(q.y, a.y), __fadd_rn(q.z, a.z), __fadd_rn(q.w, a.w));
+            k = make_float4(__fadd_rn(k.x, b.x), __fadd_rn(k.y, b.y), __fadd_rn(k.z, b.z), __fadd_rn(k.w, b.w));
+        }
+        const long long o = (((long long)n * A.T + t0 + t) * A.H_k + hk) * TD;
+        reinterpret_cast<float4*>(A.dq + o)[i4] = q;
+        reinterpret_cast<float4*>(A.dk + o)[i4] = k;
+    }
+}
+
+int launch_tc_grad(const ChunkArgs& a, void* stream)
+{
+    cudaStream_t s = (cudaStream_t)stream;
+    int e = (int)cudaFuncSetAttribute(gdn_tc_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kGSmemBytes);
+    if (e) return e;
+    gdn_tc_grad_kernel<<<dim3(a.n_chunks, a.H_v, a.N), GT, kGSmemBytes, s>>>(a);
+    return (int)cudaGetLastError();
+}
+
+int launch_tc_dqdk_sum(const ChunkArgs& a, void* stream)
+{
+    cudaStream_t s = (cudaStream_t)stream;
+    gdn_tc_dqdk_sum_kernel<<<dim3(a.n_chunks, a.H_k, a.N), 256, 0, s>>>(a);
+    return (int)cudaGetLastError();
+}
+
+int tc_grad_take_status(void* stream, int* status)
+{
+    cudaStream_t s = (cudaStream_t)stream;
+    int v = 0;
+    int e = (int)cudaMemcpyFromSymbolAsync(&v, g_tcg_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+    if (!e) e = (int)cudaStreamSynchronize(s);
+    if (e) return e;
+    if (v) {
+        const int zero = 0;
+        e = (int)cudaMemcpyToSymbolAsync(g_tcg_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+        if (!e) e = (int)cudaStreamSynchronize(s);
+    }
+    *status = v;
+    return e;
+}
+
+}  // namespace gdn
