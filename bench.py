@@ -58,6 +58,7 @@ def chunk_kernel_flops(N, T, H_v, d, C, which):
         "grad": ch * (4 * bd2 + 6 * b2d + 2 * BC ** 3),
         "grad_tc": ch * (4 * bd2 + 6 * b2d + 2 * BC ** 3),
         "dqdk_sum": 0,
+        "chains": recomputed * 2 * bd2 + ch * (3 * bd2 + 2 * b2d),
     }[which]
     return 2.0 * fma
 
@@ -65,7 +66,7 @@ def chunk_kernel_flops(N, T, H_v, d, C, which):
 # The head-size-128 chunked kernels run their products on the tensor cores as three tf32
 # passes; their roofline is the tf32 rate (the measured bf16 rate times the nominal
 # tf32 / bf16 ratio 1.1 / 2.25) divided by the three passes, in fp32 flops.
-TENSOR_KINDS = {"state_fwd", "recompute", "dstate", "grad_tc"}
+TENSOR_KINDS = {"state_fwd", "recompute", "dstate", "grad_tc", "chains"}
 
 
 def kernel_plan(chunked, d, n_bwd, cps):
@@ -76,13 +77,13 @@ def kernel_plan(chunked, d, n_bwd, cps):
     st = "gdn_tc_state_kernel" if tensor else "gdn_chunk_state_kernel"
     fwd = [("gdn_chunk_prep_kernel", "prep_fwd"), (st, "state_fwd")]
     bwd = [("gdn_chunk_prep_kernel", "prep_bwd")]
-    if cps > 1:
-        bwd.append((st + "(recompute)", "recompute"))
-    bwd.append(("gdn_tc_dstate_kernel" if tensor else "gdn_chunk_dstate_kernel", "dstate"))
     if tensor:
-        bwd += [("gdn_tc_grad_kernel", "grad_tc"), ("gdn_tc_dqdk_sum_kernel", "dqdk_sum")]
+        bwd += [("gdn_tc_bwd_chains_kernel", "chains"), ("gdn_tc_grad_kernel", "grad_tc"),
+                ("gdn_tc_dqdk_sum_kernel", "dqdk_sum")]
     else:
-        bwd.append(("gdn_chunk_grad_kernel", "grad"))
+        if cps > 1:
+            bwd.append((st + "(recompute)", "recompute"))
+        bwd += [("gdn_chunk_dstate_kernel", "dstate"), ("gdn_chunk_grad_kernel", "grad")]
     assert len(bwd) == n_bwd, (len(bwd), n_bwd)
     return fwd, bwd
 

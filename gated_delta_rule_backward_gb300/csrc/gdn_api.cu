@@ -320,8 +320,9 @@ int gdn_backward_launches(const gdn_params_t* p)
     if (check_sizes(p) != GDN_OK) return 0;
     if (p->n_seq == 0) return 0;
     const Plan pl = make_plan(p);
-    // chunked: prep, [recompute], dM chain, gradients (two kernels on the tensor-core path)
-    if (pl.chunked) return (pl.cps > 1 ? 4 : 3) + (pl.tensor ? 1 : 0);
+    // chunked: prep, [recompute], dM chain, gradients; on the tensor-core path: prep,
+    // both chains in one launch, the gradient step, the sum over value heads
+    if (pl.chunked) return pl.tensor ? 4 : (pl.cps > 1 ? 4 : 3);
     return p->T > 0 ? 2 : 1;
 }
 

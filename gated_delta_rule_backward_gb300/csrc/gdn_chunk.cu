@@ -1276,7 +1276,7 @@ static int chunk_forward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
     tap.mark(s);
     GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks, a.H_v, a.N), prep_smem<D>());
     if (D == 128 && a.want_tc) {
-        const int e = launch_tc_state(a, true, s);
+        const int e = launch_tc_state(a, s);
         if (e) return e;
         tap.mark(s);
         return 0;
@@ -1290,26 +1290,12 @@ static int chunk_backward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
 {
     tap.mark(s);
     GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks, a.H_v, a.N), prep_smem<D>());
-    if (a.cps > 1) {
-        if (D == 128 && a.want_tc) {
-            const int e = launch_tc_state(a, false, s);
+    if constexpr (D == 128) {
+        if (a.want_tc) {  // dM chain and recompute in one launch, then the gradient step
+            int e = launch_tc_bwd_chains(a, s);
             if (e) return e;
             tap.mark(s);
-        } else {
-            GDN_LAUNCH((gdn_chunk_state_kernel<D, false>), dim3(Rows<D>::P, a.n_ck, a.N * a.H_v),
-                       state_smem<D>());
-        }
-    }
-    if (D == 128 && a.want_tc) {
-        const int e = launch_tc_dstate(a, s);
-        if (e) return e;
-        tap.mark(s);
-    } else {
-        GDN_LAUNCH(gdn_chunk_dstate_kernel<D>, dim3(Rows<D>::P, a.H_v, a.N), dstate_smem<D>());
-    }
-    if constexpr (D == 128) {
-        if (a.want_tc) {
-            int e = launch_tc_grad(a, s);
+            e = launch_tc_grad(a, s);
             if (e) return e;
             tap.mark(s);
             e = launch_tc_dqdk_sum(a, s);
@@ -1318,6 +1304,10 @@ static int chunk_backward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
             return 0;
         }
     }
+    if (a.cps > 1)
+        GDN_LAUNCH((gdn_chunk_state_kernel<D, false>), dim3(Rows<D>::P, a.n_ck, a.N * a.H_v),
+                   state_smem<D>());
+    GDN_LAUNCH(gdn_chunk_dstate_kernel<D>, dim3(Rows<D>::P, a.H_v, a.N), dstate_smem<D>());
     GDN_LAUNCH(gdn_chunk_grad_kernel<D>, dim3(a.n_chunks, a.H_k, a.N), grad_smem<D>());
     return 0;
 }

@@ -141,10 +141,10 @@ constexpr int kDsGam = kDsR + 32;
 constexpr int kTcDsElems = kDsGam + 32;
 
 int launch_chunk_forward(const ChunkArgs& a, int D, void* stream, EventTap& tap);
-// The state chain on the tensor cores (gdn_tc_chain.cu): forward or recompute mode.
-int launch_tc_state(const ChunkArgs& a, bool fwd, void* stream);
-// The dM chain on the tensor cores (gdn_tc_chain.cu).
-int launch_tc_dstate(const ChunkArgs& a, void* stream);
+// The chains on the tensor cores (gdn_tc_chain.cu): the forward's state chain, and the
+// backward's dM chain together with the recompute of the chunk-entry states.
+int launch_tc_state(const ChunkArgs& a, void* stream);
+int launch_tc_bwd_chains(const ChunkArgs& a, void* stream);
 // The gradient step on the tensor cores (gdn_tc_grad.cu): per (chunk, value head) every
 // gradient of the chunk (dv, dg, dbeta written; this value head's dq, dk parked row-major
 // [t][i] at o_dqM, o_dkM), then the sum of the value heads of each key head.

@@ -83,10 +83,11 @@ __device__ __forceinline__ void load_b23(const ChunkArgs& A, long long ch, float
 
 }  // namespace
 
+// The state chain of one head (forward: bx = head, by = sequence) or of one segment
+// (recompute: bx = segment, by = sequence * H_v + head); sm is the dynamic shared memory.
 template <bool FWD>
-__global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
+__device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int bx, int by)
 {
-    extern __shared__ __align__(1024) float sm[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSFloats);  // b1, b23, mma
     uint64_t* bar_b1 = bars;
     uint64_t* bar_b23 = bars + 1;
@@ -102,15 +103,15 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
 
     int n, h, c_begin, c_end;
     if (FWD) {
-        h = blockIdx.x;
-        n = blockIdx.y;
+        h = bx;
+        n = by;
         c_begin = 0;
         c_end = A.n_chunks;
     } else {
-        const int hd = blockIdx.y;
+        const int hd = by;
         n = hd / A.H_v;
         h = hd - n * A.H_v;
-        const int s = blockIdx.x;
+        const int s = bx;
         c_begin = s * A.cps;
         const int seg_len = min(A.T, s * A.C + A.C) - s * A.C;
         c_end = c_begin + (seg_len + BC - 1) / BC - 1;  // chunks whose end state is needed
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
     float m[64];
     if (compute) {
         const float* src = FWD ? A.state0 + (head * TD + j) * TD
-                               : A.ckpt + ((head * A.n_ck + blockIdx.x) * TD + j) * TD;
+                               : A.ckpt + ((head * A.n_ck + bx) * TD + j) * TD;
         const float4* s4 = reinterpret_cast<const float4*>(src + 64 * hc);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -417,9 +418,8 @@ __device__ __forceinline__ void ds_load_rest(const ChunkArgs& A, long long ch, l
 }
 }  // namespace
 
-__global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A)
+__device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int h, int n)
 {
-    extern __shared__ __align__(1024) float sm[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kDsFloats);  // kb, rest, mma
     uint64_t* bar_kb = bars;
     uint64_t* bar_rest = bars + 1;
@@ -432,7 +432,6 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
     const bool issuer = tid == kIssuer;
     const int j = 32 * (warp & 3) + lane;   // row of dM
     const int hc = (warp >> 2) & 1;         // dM columns [64 hc, 64 hc + 64); chunk columns [16 hc, 16 hc + 16)
-    const int h = blockIdx.x, n = blockIdx.y;
     const long long head = (long long)n * A.H_v + h;
     const long long khead = (long long)n * A.H_k + h % A.H_k;
 
@@ -684,24 +683,49 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A
     if (warp == 0) tc::tmem_free(tmem, kTmemCols);
 }
 
-int launch_tc_dstate(const ChunkArgs& a, void* stream)
+// The forward's state chain: one CTA per (head, sequence).
+__global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
+{
+    extern __shared__ __align__(1024) float sm[];
+    state_chain<true>(A, sm, blockIdx.x, blockIdx.y);
+}
+
+// The backward's two chains in one launch, as they are independent: CTAs [0, N H_v) run
+// the dM chain of one head each (long, serial); the rest, when segments hold several
+// chunks, rebuild the chunk-entry states of one (segment, head) each on the other SMs.
+__global__ void __launch_bounds__(TCT, 1) gdn_tc_bwd_chains_kernel(const ChunkArgs A)
+{
+    extern __shared__ __align__(1024) float sm[];
+    const int nds = A.N * A.H_v;
+    const int b = blockIdx.x;
+    if (b < nds) {
+        dstate_chain(A, sm, b % A.H_v, b / A.H_v);
+        return;
+    }
+    const int r = b - nds;
+    state_chain<false>(A, sm, r % A.n_ck, r / A.n_ck);
+}
+
+int launch_tc_state(const ChunkArgs& a, void* stream)
 {
     cudaStream_t s = (cudaStream_t)stream;
-    int e = (int)cudaFuncSetAttribute(gdn_tc_dstate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kDsSmemBytes);
+    int e = (int)cudaFuncSetAttribute(gdn_tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kSmemBytes);
     if (e) return e;
-    gdn_tc_dstate_kernel<<<dim3(a.H_v, a.N), TCT, kDsSmemBytes, s>>>(a);
+    gdn_tc_state_kernel<<<dim3(a.H_v, a.N), TCT, kSmemBytes, s>>>(a);
     return (int)cudaGetLastError();
 }
 
-int launch_tc_state(const ChunkArgs& a, bool fwd, void* stream)
+int launch_tc_bwd_chains(const ChunkArgs& a, void* stream)
 {
     cudaStream_t s = (cudaStream_t)stream;
-    auto kern = fwd ? gdn_tc_state_kernel<true> : gdn_tc_state_kernel<false>;
-    int e = (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    const size_t bytes = kSmemBytes > kDsSmemBytes ? kSmemBytes : kDsSmemBytes;
+    int e = (int)cudaFuncSetAttribute(gdn_tc_bwd_chains_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)bytes);
     if (e) return e;
-    const dim3 grid = fwd ? dim3(a.H_v, a.N) : dim3(a.n_ck, a.N * a.H_v);
-    kern<<<grid, TCT, kSmemBytes, s>>>(a);
+    const long long nds = (long long)a.N * a.H_v;
+    const long long nrc = a.cps > 1 ? (long long)a.n_ck * nds : 0;
+    gdn_tc_bwd_chains_kernel<<<(unsigned)(nds + nrc), TCT, bytes, s>>>(a);
     return (int)cudaGetLastError();
 }
 

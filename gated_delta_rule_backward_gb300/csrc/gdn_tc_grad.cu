@@ -182,8 +182,20 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     float* red = sm + kSRed;
     float* vec = sm + kSVec;  // gdg, dr, dG, dbeta, dot
 
-    // (0) stage M (row-major fp32) and build A = M (rows j)
+    // (0) stage M (row-major fp32) and build A = M (rows j).  The loads of step (1), which do
+    //     not depend on M, go out first so that their latency overlaps the staging.
+    float vx[32], dy[16];
+    float4 dx[4];
     if (compute) {
+        const float* gy = A.gy + (long long)n * A.gys0 + (long long)t0 * A.gys1 + (long long)h * A.gys2 + row;
+        const float4* dx4 = reinterpret_cast<const float4*>(A.ws + A.o_dX + ch * (BC * TD));
+        const float* vp = A.v + (long long)n * A.vs0 + (long long)t0 * A.vs1 + (long long)h * A.vs2 + row;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dy[e] = (tb + e < nb) ? __ldg(gy + (long long)(tb + e) * A.gys1) : 0.f;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) dx[b] = __ldg(dx4 + (4 * hc + b) * TD + row);
+#pragma unroll
+        for (int t = 0; t < BC; ++t) vx[t] = (t < nb) ? __ldg(vp + (long long)t * A.vs1) : 0.f;
         if (tid < BC) {
             const bool real = tid < nb;
             sB[tid] = real ? __ldg(A.beta + (tok0 + tid) * A.H_v + h) : 0.f;
@@ -219,8 +231,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     tc::fence_before();
     __syncthreads();
 
-    // (1) D_X = M K^T.  Meanwhile: the B tile [s gamma dY ; -gamma dX], dv, and V for X.
-    float vx[32];
+    // (1) D_X = M K^T.  Meanwhile: the B tile [s gamma dY ; -gamma dX] and dv.
     if (issuer) {
         tc::fence_after();
         if (!tc::mbar_wait(bar_ld, 0)) s_err = 1;
@@ -232,17 +243,6 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     } else if (compute) {
         if (!tc::mbar_wait(bar_ld, 0)) s_err = 1;
         float* b2 = sm + kR1;
-        const float* gy = A.gy + (long long)n * A.gys0 + (long long)t0 * A.gys1 + (long long)h * A.gys2 + row;
-        const float4* dx4 = reinterpret_cast<const float4*>(A.ws + A.o_dX + ch * (BC * TD));
-        const float* vp = A.v + (long long)n * A.vs0 + (long long)t0 * A.vs1 + (long long)h * A.vs2 + row;
-        float dy[16];
-        float4 dx[4];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) dy[e] = (tb + e < nb) ? __ldg(gy + (long long)(tb + e) * A.gys1) : 0.f;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) dx[b] = __ldg(dx4 + (4 * hc + b) * TD + row);
-#pragma unroll
-        for (int t = 0; t < BC; ++t) vx[t] = (t < nb) ? __ldg(vp + (long long)t * A.vs1) : 0.f;
         float* dvp = A.dv + (tok0 * A.H_v + h) * TD + row;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {

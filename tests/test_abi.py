@@ -74,11 +74,12 @@ def test_empty_batch_launches_nothing():
 
 
 def test_chunked_launch_count_with_several_chunks_per_segment():
-    # C = 64 > 32-token chunks: the backward also rebuilds the chunk-entry states; head
-    # size 128 splits the gradient step into a tensor-core kernel and a chunk-local one
+    # C = 64 > 32-token chunks: the backward also rebuilds the chunk-entry states (head
+    # size 128: in the same launch as the dM chain, then the gradient step and the sum
+    # over value heads)
     p = gdn.make_params(1, 4096, 16, 48, 128, False)
     assert gdn.checkpoint_interval(p) == 64
-    assert gdn.launches(p) == (2, 5)
+    assert gdn.launches(p) == (2, 4)
     p = gdn.make_params(1, 4096, 16, 48, 64, False)
     assert gdn.launches(p) == (2, 4)
 
