@@ -432,16 +432,19 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
     __syncthreads();
     chunk_prep<D>(QKs, gs, bs, Gs, gam, Dm, KKm, QKm, Zs, Ts, tid);
 
-    // T^T, QD = lower(QK^T) (.) Dm, QD^T, gamma, r
+    // T^T, QD = lower(QK^T) (.) Dm, QD^T (the FP32 chain kernels' operands), gamma, r
+    const bool fp32_chains = !(D == 128 && A.want_tc);
     float* wsTT = A.ws + A.o_T + ch * (BC * BC);
     float* wsQ = A.ws + A.o_QKD + ch * (BC * BC);
     float* wsQT = A.ws + A.o_QDT + ch * (BC * BC);
     for (int idx = tid; idx < BC * BC; idx += CT) {
         const int t = idx / BC, tau = idx - t * BC;
-        const float qd = __fmul_rn(QKm[t * LDB + tau], Dm[t * LDB + tau]);
-        wsTT[tau * BC + t] = Ts[t * LDB + tau];
-        wsQ[idx] = qd;
-        wsQT[tau * BC + t] = qd;
+        if (fp32_chains) {
+            const float qd = __fmul_rn(QKm[t * LDB + tau], Dm[t * LDB + tau]);
+            wsTT[tau * BC + t] = Ts[t * LDB + tau];
+            wsQ[idx] = qd;
+            wsQT[tau * BC + t] = qd;
+        }
         TG[t * LDB + tau] = __fmul_rn(Ts[t * LDB + tau], gam[tau]);
     }
     if (tid < BC) {
@@ -467,7 +470,10 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
         if (A.want_tc) {
             const long long ck = ((long long)n * A.H_k + hk) * A.n_chunks + c;
             const bool first = h < A.H_k;  // the key head's first value head writes its operands
-            if (A.want_wu) {
+            // the backward rebuilds only the states entering a segment's later chunks, so the
+            // last chunk of a segment needs no state-chain operands there
+            const bool seg_last = cp.t0 + BC >= min(A.T, cp.seg * A.C + A.C);
+            if (A.want_wu && !(A.want_factors && seg_last)) {
                 __syncthreads();
                 prep_tc_operands<D>(A, ch, ck, first, QKs, Vs, TG, Ts, QKm, Dm, tid);
             }
