@@ -416,8 +416,8 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
     float* QKm = KKm + BC * LDB;
     float* Zs = QKm + BC * LDB;
     float* Ts = Zs + BC * LDB;
-    float* TG = Ts + BC * LDB;
-    float* vec = TG + BC * LDB;       // gs, bs, Gs, gam
+    float* TG = Zs;                   // T diag(gamma), once Z has been written out
+    float* vec = Ts + BC * LDB;       // gs, bs, Gs, gam
     float *gs = vec, *bs = vec + BC, *Gs = vec + 2 * BC, *gam = vec + 3 * BC;
 
     const long long tq = (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
@@ -445,7 +445,6 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
             wsQ[idx] = qd;
             wsQT[tau * BC + t] = qd;
         }
-        TG[t * LDB + tau] = __fmul_rn(Ts[t * LDB + tau], gam[tau]);
     }
     if (tid < BC) {
         A.ws[A.o_gam + ch * BC + tid] = gam[tid];
@@ -465,6 +464,11 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
             fQ[idx] = QKm[t * LDB + tau];
             fD[idx] = Dm[t * LDB + tau];
         }
+    }
+    __syncthreads();  // Z is out: its tile now holds T diag(gamma)
+    for (int idx = tid; idx < BC * BC; idx += CT) {
+        const int t = idx / BC, tau = idx - t * BC;
+        TG[t * LDB + tau] = __fmul_rn(Ts[t * LDB + tau], gam[tau]);
     }
     if constexpr (D == 128) {
         if (A.want_tc) {
@@ -1238,7 +1242,7 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
 template <int D>
 size_t prep_smem()
 {
-    return sizeof(float) * (3 * BC * Ld<D>::v + 6 * BC * LDB + 4 * BC);
+    return sizeof(float) * (3 * BC * Ld<D>::v + 5 * BC * LDB + 4 * BC);
 }
 template <int D>
 size_t state_smem()
