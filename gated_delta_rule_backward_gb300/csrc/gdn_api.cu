@@ -326,6 +326,21 @@ int gdn_backward_launches(const gdn_params_t* p)
     return p->T > 0 ? 2 : 1;
 }
 
+gdn_status_t gdn_device_status(void* stream)
+{
+    int a = 0, b = 0;
+    int e = gdn::tc_take_status(stream, &a);
+    if (!e) e = gdn::tc_grad_take_status(stream, &b);
+    if (e) return cuda_status(e, "device status");
+    return (a || b) ? fail(GDN_ERR_TIMEOUT, "a kernel's bounded wait gave up; that call's outputs are invalid")
+                    : GDN_OK;
+}
+
+gdn_status_t gdn_selftest_wait_timeout(void* stream)
+{
+    return cuda_status(gdn::launch_selftest_wait(stream), "selftest launch");
+}
+
 const char* gdn_status_str(gdn_status_t s)
 {
     switch (s) {

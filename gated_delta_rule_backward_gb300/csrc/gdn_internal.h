@@ -154,6 +154,8 @@ int tc_grad_take_status(void* stream, int* status);
 // Reads and clears the tensor-core kernels' device status word (0 or GDN_ERR_TIMEOUT),
 // synchronising `stream`.  Returns a cudaError_t as int.
 int tc_take_status(void* stream, int* status);
+// One kernel whose bounded wait gives up, recording a timeout (test of that path).
+int launch_selftest_wait(void* stream);
 int launch_chunk_backward(const ChunkArgs& a, int D, void* stream, EventTap& tap);
 
 // Shared-memory layout of the backward kernel, in floats (every offset a multiple of 4).

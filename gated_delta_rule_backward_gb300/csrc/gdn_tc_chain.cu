@@ -729,6 +729,24 @@ int launch_tc_bwd_chains(const ChunkArgs& a, void* stream)
     return (int)cudaGetLastError();
 }
 
+// A bounded wait on a barrier that nothing completes: gives up and records the timeout.
+__global__ void gdn_selftest_wait_kernel()
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !tc::mbar_wait(&bar, 0)) atomicExch(&g_tc_status, kStatusTimeout);
+}
+
+int launch_selftest_wait(void* stream)
+{
+    gdn_selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>();
+    return (int)cudaGetLastError();
+}
+
 int tc_take_status(void* stream, int* status)
 {
     cudaStream_t s = (cudaStream_t)stream;

@@ -31,7 +31,7 @@ EXPORTS = ["gdn_checkpoint_interval", "gdn_num_checkpoints", "gdn_ckpt_elems", "
            "gdn_packed_grad_elems", "gdn_packed_grad_offsets", "gdn_backward_workspace_bytes",
            "gdn_backward", "gdn_status_str", "gdn_last_error", "gdn_forward_launches",
            "gdn_backward_launches", "gdn_set_timing_events", "gdn_backward_noalloc",
-           "gdn_forward_workspace_bytes"]
+           "gdn_forward_workspace_bytes", "gdn_device_status", "gdn_selftest_wait_timeout"]
 
 
 class GdnParams(ctypes.Structure):
@@ -78,6 +78,10 @@ _lib.gdn_set_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c
 _lib.gdn_set_timing_events.restype = None
 _lib.gdn_forward_workspace_bytes.argtypes = [_P]
 _lib.gdn_forward_workspace_bytes.restype = ctypes.c_size_t
+_lib.gdn_device_status.argtypes = [_vp]
+_lib.gdn_device_status.restype = ctypes.c_int
+_lib.gdn_selftest_wait_timeout.argtypes = [_vp]
+_lib.gdn_selftest_wait_timeout.restype = ctypes.c_int
 
 
 class GdnError(RuntimeError):
@@ -214,6 +218,19 @@ def gdn_backward_noalloc(p: GdnParams, q, k, v, g, beta, ckpt, gy, dstate_T, pac
                                    _ptr(packed), _stream_handle(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_backward_noalloc")
+
+
+def device_status(stream=None) -> int:
+    """Synchronise `stream` and return (and clear) the device status: GDN_OK, or
+    6 (GDN_ERR_TIMEOUT) when a tensor-core kernel's bounded wait gave up."""
+    return int(_lib.gdn_device_status(_stream_handle(stream)))
+
+
+def selftest_wait_timeout(stream=None):
+    """Enqueue the kernel whose bounded wait gives up (test of the timeout path)."""
+    st = _lib.gdn_selftest_wait_timeout(_stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_selftest_wait_timeout")
 
 
 def forward(q, k, v, g, beta, state0, C=None, scale=None, stream=None):

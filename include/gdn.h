@@ -168,6 +168,23 @@ void gdn_set_timing_events(void* const* events, int n_events);
 int gdn_forward_launches(const gdn_params_t* p);
 int gdn_backward_launches(const gdn_params_t* p);
 
+/* Device-side status of the work enqueued so far on the current device.  The
+ * tensor-core kernels (head size 128) wait on hardware barriers for their operand copies
+ * and products; every such wait is bounded (0.2 s of wall clock, far beyond any
+ * legitimate wait), and a wait that gives up makes its kernel return early and record
+ * GDN_ERR_TIMEOUT in a device status word, leaving that call's outputs invalid.  This
+ * call synchronises `stream` (a cudaStream_t, NULL = legacy default stream), then reads
+ * and clears the status words: GDN_OK, GDN_ERR_TIMEOUT, or GDN_ERR_CUDA if the stream or
+ * the read failed (text in gdn_last_error()).  No counterpart on the pages; it exists
+ * because a GPU kernel cannot return an error code by itself. */
+gdn_status_t gdn_device_status(void* stream);
+
+/* Test hook for the timeout path: enqueues one single-CTA kernel whose bounded wait on a
+ * barrier that nothing completes gives up, as above, so that the next gdn_device_status
+ * returns GDN_ERR_TIMEOUT.  Touches no caller memory; takes about 0.2 s of GPU time.
+ * Returns GDN_ERR_CUDA if the launch failed. */
+gdn_status_t gdn_selftest_wait_timeout(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

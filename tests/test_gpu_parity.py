@@ -191,3 +191,17 @@ def test_empty_batch_is_a_no_op():
     gdn.gdn_forward(p, e, e, e, e, e, e, e, e, e, None)
     gdn.gdn_backward(p, e, e, e, e, e, e, e, None, e, None)
     torch.cuda.synchronize()
+
+
+def test_device_status_reports_bounded_wait_timeouts():
+    """A kernel whose bounded wait gives up returns early and leaves GDN_ERR_TIMEOUT in the
+    device status word; reading it clears it; normal head-size-128 runs report GDN_OK."""
+    from gated_delta_rule_backward_gb300 import gdn
+    assert gdn.device_status() == gdn.GDN_OK
+    gdn.selftest_wait_timeout()
+    assert gdn.device_status() == 6
+    assert b"bounded wait" in gdn.library().gdn_last_error()
+    assert gdn.device_status() == gdn.GDN_OK
+    prob = synth.make_problem(1, 100, 1, 2, 128, kda=False, seed=51, C=64)
+    H.run_gpu(prob)
+    assert gdn.device_status() == gdn.GDN_OK
