@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "../../include/gdn.h"
@@ -53,7 +54,7 @@ struct Plan {
     int64_t n_chunks = 0; // chunks per (sequence, value head)
     long long o_T = 0, o_QKD = 0, o_QDT = 0, o_gam = 0, o_r = 0, o_W = 0, o_U = 0, o_Mc = 0, o_dM = 0,
               o_dDel = 0, o_dX = 0, o_Tr = 0, o_Z = 0, o_KK = 0, o_QK = 0, o_Dm = 0, o_W1 = 0, o_Q1 = 0, o_B23 = 0, o_DK = 0, o_DS = 0,
-              o_dqM = 0, o_dkM = 0;
+              o_dqM = 0, o_dkM = 0, o_carry = 0, o_carry_b = 0;
     bool tensor = false;  // head size 128: the state chain runs on the tensor cores
     size_t fwd_ws_bytes = 0, bwd_ws_bytes = 0;
 };
@@ -153,6 +154,7 @@ Plan make_plan(const gdn_params_t* p)
             pl.o_W1 = o;  o += al(CH * gdn::kTcWElems);
             pl.o_Q1 = o;  o += al(CK * gdn::kTcQElems);
             pl.o_B23 = o; o += al(CH * gdn::kTcB23Elems);
+            pl.o_carry = o; o += al(p->n_seq * p->H_v * D * D);  // forward: state between ranges
         } else {
             pl.o_W = o;   o += al(CH * BC * D);
             pl.o_U = o;   o += al(CH * BC * D);
@@ -177,6 +179,7 @@ Plan make_plan(const gdn_params_t* p)
             pl.o_DS = o;  o += al(CH * gdn::kTcDsElems);
             pl.o_dqM = o; o += al(CH * BC * D);
             pl.o_dkM = o; o += al(CH * BC * D);
+            pl.o_carry_b = o; o += al(p->n_seq * p->H_v * D * D);  // dM between ranges
         }
         pl.bwd_ws_bytes = (size_t)o * 4;
         pl.ws_bytes = pl.bwd_ws_bytes;
@@ -246,11 +249,84 @@ void fill_chunk_common(gdn::ChunkArgs& c, const gdn_params_t* p, const Plan& pl)
     c.o_W1 = pl.o_W1; c.o_Q1 = pl.o_Q1; c.o_B23 = pl.o_B23; c.o_DK = pl.o_DK; c.o_DS = pl.o_DS;
     c.o_dqM = pl.o_dqM; c.o_dkM = pl.o_dkM;
     c.want_tc = pl.tensor;
+    c.c_lo = 0;
+    c.c_hi = (int)pl.n_chunks;
+}
+
+// Chunk ranges the pipelined tensor-core path launches (non-empty ones).
+int tc_ranges(const Plan& pl, bool backward)
+{
+    const int R = gdn::pipeline_ranges((int)pl.n_ck, backward);
+    const int64_t seg_per = (pl.n_ck + R - 1) / R;
+    int n = 0;
+    for (int r = 0; r < R; ++r)
+        if (r * seg_per * pl.cps < pl.n_chunks) ++n;
+    return n;
 }
 
 }  // namespace
 
 void gdn::set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
+namespace {
+constexpr int kMaxDevices = 64;
+gdn::Pipeline g_pipes[kMaxDevices];
+bool g_pipe_ready[kMaxDevices];
+std::mutex g_pipe_mu[kMaxDevices];
+thread_local int g_pipe_held = -1;
+}  // namespace
+
+int gdn::acquire_pipeline(gdn::Pipeline** out)
+{
+    int dev = 0;
+    int e = (int)cudaGetDevice(&dev);
+    if (e) return e;
+    if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+    g_pipe_mu[dev].lock();
+    g_pipe_held = dev;
+    if (!g_pipe_ready[dev]) {
+        gdn::Pipeline& P = g_pipes[dev];
+        int least = 0, greatest = 0;
+        e = (int)cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        cudaStream_t hi = nullptr, lo = nullptr;
+        if (!e) e = (int)cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest);
+        if (!e) e = (int)cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, least);
+        cudaEvent_t ev[3 + 2 * gdn::kMaxRanges] = {};
+        for (int i = 0; i < 3 + 2 * gdn::kMaxRanges && !e; ++i)
+            e = (int)cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+        if (e) {
+            release_pipeline();
+            return e;
+        }
+        P.hi = hi;
+        P.lo = lo;
+        P.fork = ev[0];
+        P.join_hi = ev[1];
+        P.join_lo = ev[2];
+        for (int i = 0; i < gdn::kMaxRanges; ++i) {
+            P.prep_done[i] = ev[3 + i];
+            P.chain_go[i] = ev[3 + gdn::kMaxRanges + i];
+        }
+        g_pipe_ready[dev] = true;
+    }
+    *out = &g_pipes[dev];
+    return 0;
+}
+
+void gdn::release_pipeline()
+{
+    if (g_pipe_held >= 0) {
+        const int dev = g_pipe_held;
+        g_pipe_held = -1;
+        g_pipe_mu[dev].unlock();
+    }
+}
+
+int gdn::pipeline_ranges(int n_ck, bool backward)
+{
+    if (backward) return 1;
+    return n_ck < gdn::kMaxRanges ? (n_ck < 1 ? 1 : n_ck) : gdn::kMaxRanges;
+}
 
 void gdn::EventTap::mark(void* stream)
 {
@@ -312,7 +388,18 @@ int gdn_forward_launches(const gdn_params_t* p)
 {
     if (check_sizes(p) != GDN_OK) return 0;
     if (p->n_seq == 0) return 0;
-    return make_plan(p).chunked ? 2 : 1;
+    const Plan pl = make_plan(p);
+    if (pl.chunked && pl.tensor) return 2 * tc_ranges(pl, false);  // prep + state chain per range
+    return pl.chunked ? 2 : 1;
+}
+
+int gdn_timing_stages(const gdn_params_t* p, int backward)
+{
+    if (check_sizes(p) != GDN_OK) return 0;
+    if (p->n_seq == 0) return 0;
+    const Plan pl = make_plan(p);
+    if (pl.chunked && pl.tensor) return backward ? 3 : 1;
+    return backward ? gdn_backward_launches(p) : gdn_forward_launches(p);
 }
 
 int gdn_backward_launches(const gdn_params_t* p)
@@ -320,9 +407,10 @@ int gdn_backward_launches(const gdn_params_t* p)
     if (check_sizes(p) != GDN_OK) return 0;
     if (p->n_seq == 0) return 0;
     const Plan pl = make_plan(p);
-    // chunked: prep, [recompute], dM chain, gradients; on the tensor-core path: prep,
-    // both chains in one launch, the gradient step, the sum over value heads
-    if (pl.chunked) return pl.tensor ? 4 : (pl.cps > 1 ? 4 : 3);
+    // chunked: prep, [recompute], dM chain, gradients; on the tensor-core path: per chunk
+    // range a prep and a launch of both chains, then the gradient step and the sum over
+    // value heads
+    if (pl.chunked) return pl.tensor ? 2 * tc_ranges(pl, true) + 2 : (pl.cps > 1 ? 4 : 3);
     return p->T > 0 ? 2 : 1;
 }
 
@@ -414,6 +502,7 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, 
         c.q = q; c.k = k; c.v = v; c.g = g; c.beta = beta; c.state0 = state0;
         c.y = y; c.state_T = state_T; c.ckpt_out = ckpt; c.ws = (float*)workspace;
         fill_chunk_common(c, p, pl);
+        c.carry = pl.tensor ? c.ws + pl.o_carry : nullptr;
         c.want_wu = 1;
         c.vec_q = vec_ok(q, p->q_s); c.vec_k = vec_ok(k, p->k_s); c.vec_v = vec_ok(v, p->v_s);
         return cuda_status(gdn::launch_chunk_forward(c, pl.D, stream, tap), "forward launch");
@@ -485,6 +574,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
         c.dq = packed + off[0]; c.dk = packed + off[1]; c.dv = packed + off[2];
         c.dg = packed + off[3]; c.dbeta = packed + off[4]; c.dstate0 = packed + off[5];
         fill_chunk_common(c, p, pl);
+        c.carry = pl.tensor ? c.ws + pl.o_carry_b : nullptr;
         c.want_wu = pl.cps > 1;
         c.want_factors = 1;
         c.vec_q = vec_ok(q, p->q_s); c.vec_k = vec_ok(k, p->k_s); c.vec_v = vec_ok(v, p->v_s);

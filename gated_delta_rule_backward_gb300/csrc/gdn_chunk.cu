@@ -403,7 +403,7 @@ template <int D>
 __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
 {
     constexpr int ld = Ld<D>::v;
-    const int c = blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
+    const int c = A.c_lo + blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
     const int hk = h % A.H_k;
     const ChunkPos cp = chunk_pos(A, c);
     const long long ch = ((long long)n * A.H_v + h) * A.n_chunks + c;
@@ -1280,17 +1280,87 @@ static int set_smem(K kern, size_t bytes)
         tap.mark(s);                                                                   \
     } while (0)
 
+// The tensor-core path (head size 128): the chunk range r of the prep runs on a
+// low-priority library stream while the serial chain works through range r - 1 on a
+// high-priority one (the chain's 48 CTAs leave most SMs to the prep).  Only events order
+// the two: prep(r) -> chain(r), and the caller's stream forks into both and joins back.
+static void range_of(const ChunkArgs& a, int R, int r, ChunkArgs& out)
+{
+    const int seg_per = (a.n_ck + R - 1) / R;
+    out = a;
+    out.c_lo = min(a.n_chunks, r * seg_per * a.cps);
+    out.c_hi = min(a.n_chunks, (r + 1) * seg_per * a.cps);
+}
+
+static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, EventTap& tap)
+{
+    Pipeline* P = nullptr;
+    int e = acquire_pipeline(&P);
+    if (e) return e;
+    const cudaStream_t hi = (cudaStream_t)P->hi, lo = (cudaStream_t)P->lo;
+    const int R = pipeline_ranges(a.n_ck, backward);
+    tap.mark(user);
+    e = (int)cudaEventRecord((cudaEvent_t)P->fork, user);
+    if (!e) e = (int)cudaStreamWaitEvent(lo, (cudaEvent_t)P->fork, 0);
+    if (!e) e = (int)cudaStreamWaitEvent(hi, (cudaEvent_t)P->fork, 0);
+    // The forward's chain runs ranges first to last, the dM chain last to first.  The prep
+    // of the next range waits until the chain of this range is about to launch, so that
+    // the chain's CTAs (a whole SM each) are placed before the prep's fill the GPU.
+    int order[kMaxRanges], nr = 0;
+    for (int i = 0; i < R; ++i) {
+        const int r = backward ? R - 1 - i : i;
+        ChunkArgs ar;
+        range_of(a, R, r, ar);
+        if (ar.c_hi > ar.c_lo) order[nr++] = r;
+    }
+    auto launch_prep = [&](int r) -> int {
+        ChunkArgs ar;
+        range_of(a, R, r, ar);
+        int err = set_smem(gdn_chunk_prep_kernel<128>, prep_smem<128>());
+        if (err) return err;
+        gdn_chunk_prep_kernel<128><<<dim3(ar.c_hi - ar.c_lo, a.H_v, a.N), CT, prep_smem<128>(), lo>>>(ar);
+        err = (int)cudaGetLastError();
+        if (!err) err = (int)cudaEventRecord((cudaEvent_t)P->prep_done[r], lo);
+        return err;
+    };
+    if (!e && nr > 0) e = launch_prep(order[0]);
+    for (int i = 0; i < nr && !e; ++i) {
+        const int r = order[i];
+        ChunkArgs ar;
+        range_of(a, R, r, ar);
+        e = (int)cudaStreamWaitEvent(hi, (cudaEvent_t)P->prep_done[r], 0);
+        if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->chain_go[r], hi);
+        if (!e) e = backward ? launch_tc_bwd_chains(ar, hi) : launch_tc_state(ar, hi);
+        if (!e && i + 1 < nr) {
+            e = (int)cudaStreamWaitEvent(lo, (cudaEvent_t)P->chain_go[r], 0);
+            if (!e) e = launch_prep(order[i + 1]);
+        }
+    }
+    if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_hi, hi);
+    if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_lo, lo);
+    if (!e) e = (int)cudaStreamWaitEvent(user, (cudaEvent_t)P->join_hi, 0);
+    if (!e) e = (int)cudaStreamWaitEvent(user, (cudaEvent_t)P->join_lo, 0);
+    release_pipeline();
+    if (e) return e;
+    tap.mark(user);
+    if (!backward) return 0;
+    e = launch_tc_grad(a, user);
+    if (e) return e;
+    tap.mark(user);
+    e = launch_tc_dqdk_sum(a, user);
+    if (e) return e;
+    tap.mark(user);
+    return 0;
+}
+
 template <int D>
 static int chunk_forward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
 {
+    if constexpr (D == 128) {
+        if (a.want_tc) return tc_pipelined(a, s, false, tap);
+    }
     tap.mark(s);
     GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks, a.H_v, a.N), prep_smem<D>());
-    if (D == 128 && a.want_tc) {
-        const int e = launch_tc_state(a, s);
-        if (e) return e;
-        tap.mark(s);
-        return 0;
-    }
     GDN_LAUNCH((gdn_chunk_state_kernel<D, true>), dim3(Rows<D>::P, a.H_v, a.N), state_smem<D>());
     return 0;
 }
@@ -1298,22 +1368,11 @@ static int chunk_forward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
 template <int D>
 static int chunk_backward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
 {
+    if constexpr (D == 128) {
+        if (a.want_tc) return tc_pipelined(a, s, true, tap);
+    }
     tap.mark(s);
     GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks, a.H_v, a.N), prep_smem<D>());
-    if constexpr (D == 128) {
-        if (a.want_tc) {  // dM chain and recompute in one launch, then the gradient step
-            int e = launch_tc_bwd_chains(a, s);
-            if (e) return e;
-            tap.mark(s);
-            e = launch_tc_grad(a, s);
-            if (e) return e;
-            tap.mark(s);
-            e = launch_tc_dqdk_sum(a, s);
-            if (e) return e;
-            tap.mark(s);
-            return 0;
-        }
-    }
     if (a.cps > 1)
         GDN_LAUNCH((gdn_chunk_state_kernel<D, false>), dim3(Rows<D>::P, a.n_ck, a.N * a.H_v),
                    state_smem<D>());

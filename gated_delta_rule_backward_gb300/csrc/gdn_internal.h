@@ -106,17 +106,41 @@ struct ChunkArgs {
     int want_wu;
     int want_factors;
     int want_tc;                            // head size 128: state chain on the tensor cores
+    int c_lo, c_hi;                         // chunk range of this launch (prep and chains)
+    float* carry;                           // [N][H_v][D][D] state (or dM) between ranges
     int vec_q, vec_k, vec_v, vec_gy;
 };
 
-// Records caller-provided timing events around the kernels of one call: mark() before
-// the first kernel and after each one, while events remain.
+// Records caller-provided timing events around the stages of one call: mark() before
+// the first stage and after each one, while events remain.
 struct EventTap {
     void* const* ev;
     int n;
     int i;
     void mark(void* stream);
 };
+
+// Library streams of one device for the pipelined tensor-core path: chunk-range preps on
+// a low-priority stream overlap the serial chains on a high-priority one.  Created on
+// first use; `mu` serialises the enqueueing of calls that use them.
+constexpr int kMaxRanges = 4;
+struct Pipeline {
+    void* hi;
+    void* lo;
+    void* fork;
+    void* join_hi;
+    void* join_lo;
+    void* prep_done[kMaxRanges];
+    void* chain_go[kMaxRanges];
+};
+// Returns the current device's pipeline (creating it on first use) with its lock held;
+// release_pipeline() unlocks.  Returns a cudaError_t as int.
+int acquire_pipeline(Pipeline** out);
+void release_pipeline();
+// Chunk ranges of the pipelined path: segment-aligned, at most kMaxRanges (forward).  The
+// backward runs one range: its parallel work (prep and recompute) outweighs the dM chain,
+// so splitting it only adds launches.
+int pipeline_ranges(int n_ck, bool backward);
 
 // Tensor-core operands of the state chain (head size 128), in the operand layouts of
 // gdn_tc.cuh, floats: W = T diag(gamma) K per (chunk, value head) and Q per (chunk, key head),

@@ -105,8 +105,8 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     if (FWD) {
         h = bx;
         n = by;
-        c_begin = 0;
-        c_end = A.n_chunks;
+        c_begin = A.c_lo;
+        c_end = A.c_hi;
     } else {
         const int hd = by;
         n = hd / A.H_v;
@@ -144,8 +144,9 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     // entry state: this thread's 64 columns of row j
     float m[64];
     if (compute) {
-        const float* src = FWD ? A.state0 + (head * TD + j) * TD
-                               : A.ckpt + ((head * A.n_ck + bx) * TD + j) * TD;
+        const float* src = !FWD ? A.ckpt + ((head * A.n_ck + bx) * TD + j) * TD
+                           : c_begin == 0 ? A.state0 + (head * TD + j) * TD
+                                          : A.carry + (head * TD + j) * TD;
         const float4* s4 = reinterpret_cast<const float4*>(src + 64 * hc);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -361,7 +362,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     } else if (compute) {
         if (FWD) {
             if (y_nb > 0) store_y();
-            store_ckpt(A.state_T + head * (long long)(TD * TD));
+            store_ckpt((c_end == A.n_chunks ? A.state_T : A.carry) + head * (long long)(TD * TD));
         } else {
             park_state(A.ws + A.o_Mc + (head * A.n_chunks + c_end) * (long long)(TD * TD));
         }
@@ -448,7 +449,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
     tc::fence_after();
     const uint32_t tmem = s_tmem;
 
-    const int c_last = A.n_chunks - 1;
+    const int c_last = A.c_hi - 1;
     uint32_t ph_kb = 0, ph_rest = 0, ph_mma = 0;
     bool kb_pending = false, rest_pending = false;
     if (issuer) {
@@ -458,8 +459,9 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
     }
     float m[64];
     if (compute) {
-        if (A.dstate_T) {
-            const float4* s4 = reinterpret_cast<const float4*>(A.dstate_T + (head * TD + j) * TD + 64 * hc);
+        const float* seed = A.c_hi == A.n_chunks ? A.dstate_T : A.carry;
+        if (seed) {
+            const float4* s4 = reinterpret_cast<const float4*>(seed + (head * TD + j) * TD + 64 * hc);
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
                 const float4 x = __ldg(s4 + q);
@@ -500,7 +502,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
     };
 
     int c = c_last;
-    for (; c >= 0; --c) {
+    for (; c >= A.c_lo; --c) {
         const long long ch = head * A.n_chunks + c;
         // (1) dM -> tf32 hi/lo in TMEM
         if (compute) {
@@ -559,7 +561,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
         ph_mma ^= 1;
         tc::fence_after();
         if (issuer) {
-            if (ok && c > 0) {
+            if (ok && c > A.c_lo) {
                 ds_load_kb(A, khead * A.n_chunks + c - 1, sm, bar_kb);
                 kb_pending = true;
             }
@@ -649,7 +651,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
             break;
         }
         if (issuer) {
-            if (c > 0) {
+            if (c > A.c_lo) {
                 tc::fence_async_smem();
                 ds_load_rest(A, ch - 1, khead * A.n_chunks + c - 1, sm, bar_rest);
                 rest_pending = true;
@@ -673,7 +675,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
             if (rest_pending) tc::mbar_wait(bar_rest, ph_rest);
         }
     } else if (compute) {
-        float4* d4 = reinterpret_cast<float4*>(A.dstate0 + (head * TD + j) * TD + 64 * hc);
+        float4* d4 = reinterpret_cast<float4*>((A.c_lo == 0 ? A.dstate0 : A.carry) + (head * TD + j) * TD + 64 * hc);
 #pragma unroll
         for (int q = 0; q < 16; ++q) d4[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
     }
@@ -702,8 +704,10 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_bwd_chains_kernel(const ChunkAr
         dstate_chain(A, sm, b % A.H_v, b / A.H_v);
         return;
     }
+    // recompute CTAs: the segments whose chunks lie in [c_lo, c_hi)
+    const int s_lo = A.c_lo / A.cps, s_hi = (A.c_hi + A.cps - 1) / A.cps;
     const int r = b - nds;
-    state_chain<false>(A, sm, r % A.n_ck, r / A.n_ck);
+    state_chain<false>(A, sm, s_lo + r % (s_hi - s_lo), r / (s_hi - s_lo));
 }
 
 int launch_tc_state(const ChunkArgs& a, void* stream)
@@ -724,7 +728,8 @@ int launch_tc_bwd_chains(const ChunkArgs& a, void* stream)
                                       (int)bytes);
     if (e) return e;
     const long long nds = (long long)a.N * a.H_v;
-    const long long nrc = a.cps > 1 ? (long long)a.n_ck * nds : 0;
+    const int s_lo = a.c_lo / a.cps, s_hi = (a.c_hi + a.cps - 1) / a.cps;
+    const long long nrc = a.cps > 1 ? (long long)(s_hi - s_lo) * nds : 0;
     gdn_tc_bwd_chains_kernel<<<(unsigned)(nds + nrc), TCT, bytes, s>>>(a);
     return (int)cudaGetLastError();
 }

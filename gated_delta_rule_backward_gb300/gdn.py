@@ -31,7 +31,8 @@ EXPORTS = ["gdn_checkpoint_interval", "gdn_num_checkpoints", "gdn_ckpt_elems", "
            "gdn_packed_grad_elems", "gdn_packed_grad_offsets", "gdn_backward_workspace_bytes",
            "gdn_backward", "gdn_status_str", "gdn_last_error", "gdn_forward_launches",
            "gdn_backward_launches", "gdn_set_timing_events", "gdn_backward_noalloc",
-           "gdn_forward_workspace_bytes", "gdn_device_status", "gdn_selftest_wait_timeout"]
+           "gdn_forward_workspace_bytes", "gdn_device_status", "gdn_selftest_wait_timeout",
+           "gdn_timing_stages"]
 
 
 class GdnParams(ctypes.Structure):
@@ -78,6 +79,8 @@ _lib.gdn_set_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c
 _lib.gdn_set_timing_events.restype = None
 _lib.gdn_forward_workspace_bytes.argtypes = [_P]
 _lib.gdn_forward_workspace_bytes.restype = ctypes.c_size_t
+_lib.gdn_timing_stages.argtypes = [_P, ctypes.c_int]
+_lib.gdn_timing_stages.restype = ctypes.c_int
 _lib.gdn_device_status.argtypes = [_vp]
 _lib.gdn_device_status.restype = ctypes.c_int
 _lib.gdn_selftest_wait_timeout.argtypes = [_vp]
@@ -168,13 +171,19 @@ def launches(p: GdnParams):
             int(_lib.gdn_backward_launches(ctypes.byref(p))))
 
 
+def timing_stages(p: GdnParams):
+    """(forward stages, backward stages) that set_timing_events brackets."""
+    return (int(_lib.gdn_timing_stages(ctypes.byref(p), 0)),
+            int(_lib.gdn_timing_stages(ctypes.byref(p), 1)))
+
+
 _EVENTS = None
 
 
 def set_timing_events(events):
     """A list of recorded torch.cuda.Event(enable_timing=True) objects, or None.  Each
-    gdn_forward / gdn_backward call then records events[0] before its first kernel and
-    events[i] after its i-th kernel."""
+    gdn_forward / gdn_backward call then records events[0] before its first stage and
+    events[i] after its i-th stage (see timing_stages)."""
     global _EVENTS
     if events is None:
         _EVENTS = None

@@ -46,9 +46,13 @@
  *
  * Ownership and ordering
  * ----------------------
- * The caller owns every buffer and the stream; the library allocates nothing and keeps
- * no pointer after a call returns.  Work is enqueued on `stream` (a cudaStream_t; NULL
- * is the legacy default stream): GDN_OK means "validated and launched".  The inputs and
+ * The caller owns every buffer and the stream; the library allocates no device memory
+ * and keeps no pointer after a call returns.  Work is enqueued on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream): GDN_OK means "validated and
+ * launched".  At head size 128 the scalar-gate path also uses two library streams per
+ * device (created on first use): the call's stream forks into them and joins back with
+ * events, so everything the call enqueues is ordered after earlier work on `stream` and
+ * before later work on it; calls on one device enqueue one at a time.  The inputs and
  * ckpt must stay unchanged between gdn_forward and gdn_backward; the backward never
  * writes its inputs.  Inputs must be finite.
  *
@@ -156,17 +160,26 @@ gdn_status_t gdn_backward_noalloc(const gdn_params_t* p, const float* q, const f
 const char* gdn_status_str(gdn_status_t s);
 const char* gdn_last_error(void);
 
-/* Optional per-kernel timing for the calling thread: while `events` is non-NULL, every
+/* Optional per-stage timing for the calling thread: while `events` is non-NULL, every
  * gdn_forward / gdn_backward call records events[0] on its stream before its first
- * kernel and events[i] after its i-th kernel, for i < n_events.  The events are
- * cudaEvent_t handles the caller created and owns; NULL turns the recording off.  Not
- * part of the operation: it lets a caller time each kernel of a call. */
+ * stage and events[i] after its i-th stage, for i < n_events (stages: see
+ * gdn_timing_stages).  The events are cudaEvent_t handles the caller created and owns;
+ * NULL turns the recording off.  Not part of the operation: it lets a caller time the
+ * kernels of a call. */
 void gdn_set_timing_events(void* const* events, int n_events);
 
 /* Kernels a forward / backward call with these params launches (0 when the call would
  * fail validation).  Lets callers account for the work they enqueue. */
 int gdn_forward_launches(const gdn_params_t* p);
 int gdn_backward_launches(const gdn_params_t* p);
+
+/* Timed stages of a forward (backward = 0) or backward (backward = 1) call with these
+ * params: gdn_set_timing_events records one event before the first stage and one after
+ * each stage.  A stage is one kernel, except on the head-size-128 path, where the chunk
+ * preps and the serial chains run pipelined over chunk ranges on two library streams and
+ * form one stage (forward: 1 stage; backward: 3 stages -- the pipelined preps and chains,
+ * the gradient step, the sum over value heads).  0 when the call would fail validation. */
+int gdn_timing_stages(const gdn_params_t* p, int backward);
 
 /* Device-side status of the work enqueued so far on the current device.  The
  * tensor-core kernels (head size 128) wait on hardware barriers for their operand copies

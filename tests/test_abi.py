@@ -53,6 +53,7 @@ def test_packed_layout_and_sizes():
         # scalar gate: chunked kernels (prep + state chain; prep + dM chain + gradients),
         # KDA gate: token recurrence (forward; backward + reduction)
         assert gdn.launches(p) == ((1, 2) if kda else (2, 3))
+        assert gdn.timing_stages(p) == gdn.launches(p)
         assert (gdn.forward_workspace_bytes(p) == 0) == kda
 
 
@@ -74,12 +75,16 @@ def test_empty_batch_launches_nothing():
 
 
 def test_chunked_launch_count_with_several_chunks_per_segment():
-    # C = 64 > 32-token chunks: the backward also rebuilds the chunk-entry states (head
-    # size 128: in the same launch as the dM chain, then the gradient step and the sum
-    # over value heads)
+    # C = 64 > 32-token chunks: the backward also rebuilds the chunk-entry states.  Head
+    # size 128 pipelines the forward over 4 chunk ranges (a prep and a chain launch each);
+    # the backward runs the prep, the dM chain with the recompute, the gradient step and
+    # the sum over value heads.
     p = gdn.make_params(1, 4096, 16, 48, 128, False)
     assert gdn.checkpoint_interval(p) == 64
-    assert gdn.launches(p) == (2, 4)
+    assert gdn.launches(p) == (8, 4)
+    assert gdn.timing_stages(p) == (1, 3)
+    p = gdn.make_params(1, 100, 1, 2, 128, False, C=64)   # 2 segments -> 2 ranges
+    assert gdn.launches(p) == (4, 4)
     p = gdn.make_params(1, 4096, 16, 48, 64, False)
     assert gdn.launches(p) == (2, 4)
 
