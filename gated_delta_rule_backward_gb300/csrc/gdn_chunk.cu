@@ -94,6 +94,35 @@ __device__ __forceinline__ void load_rows_pad(float* dst, int ld, const float* s
     }
 }
 
+// Register prefetch of one chunk's raw rows of a strided input (q or k): BC x D floats,
+// NF = D / 32 float4 per thread, zero beyond the chunk's real rows.
+template <int D>
+__device__ __forceinline__ void pf_rows(float4 (&r)[D / 32], const float* src, long long stride,
+                                        int nb, bool vec, int tid)
+{
+#pragma unroll
+    for (int kk = 0; kk < D / 32; ++kk) {
+        const int f = tid + CT * kk, t = f / (D / 4), i4 = f - t * (D / 4);
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < nb) {
+            const float* p = src + t * stride + 4 * i4;
+            x = vec ? __ldg(reinterpret_cast<const float4*>(p))
+                    : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
+        }
+        r[kk] = x;
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void put_rows(float* dst, int ld, const float4 (&r)[D / 32], int tid)
+{
+#pragma unroll
+    for (int kk = 0; kk < D / 32; ++kk) {
+        const int f = tid + CT * kk, t = f / (D / 4), i4 = f - t * (D / 4);
+        *reinterpret_cast<float4*>(dst + t * ld + 4 * i4) = r[kk];
+    }
+}
+
 // A dense [rows][width] block of the workspace (row stride = width) into shared memory.
 __device__ __forceinline__ void load_ws(float* dst, int ld, const float* src, int rows, int width,
                                         int tid)
@@ -343,7 +372,9 @@ __device__ void prep_tc_dstate_operands(const ChunkArgs& A, int n, int h, const 
     };
     {
         const long long tg = (long long)n * A.gys0 + (long long)cp.t0 * A.gys1 + (long long)h * A.gys2;
-        load_rows_pad(Vs, ld, A.gy + tg, A.gys1, cp.nb, D, A.vec_gy, tid);
+        float4 r[D / 32];
+        pf_rows<D>(r, A.gy + tg, A.gys1, cp.nb, A.vec_gy, tid);
+        put_rows<D>(Vs, ld, r, tid);
     }
     for (int idx = tid; idx < BC * BC; idx += CT) {
         const int t = idx / BC, tau = idx - t * BC;
@@ -422,13 +453,19 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
 
     const long long tq = (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
     const long long tk = (long long)n * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
-    load_rows_pad(QKs, ld, A.q + tq, A.qs1, cp.nb, D, A.vec_q, tid);
-    load_rows_pad(QKs + BC * ld, ld, A.k + tk, A.ks1, cp.nb, D, A.vec_k, tid);
-    if (A.want_wu) {
-        const long long tv = (long long)n * A.vs0 + (long long)cp.t0 * A.vs1 + (long long)h * A.vs2;
-        load_rows_pad(Vs, ld, A.v + tv, A.vs1, cp.nb, D, A.vec_v, tid);
+    {  // every load in flight before the first store
+        float4 rq[D / 32], rk[D / 32], rv[D / 32];
+        pf_rows<D>(rq, A.q + tq, A.qs1, cp.nb, A.vec_q, tid);
+        pf_rows<D>(rk, A.k + tk, A.ks1, cp.nb, A.vec_k, tid);
+        if (A.want_wu) {
+            const long long tv = (long long)n * A.vs0 + (long long)cp.t0 * A.vs1 + (long long)h * A.vs2;
+            pf_rows<D>(rv, A.v + tv, A.vs1, cp.nb, A.vec_v, tid);
+        }
+        load_gate_beta(A, n, h, cp, gs, bs, tid);
+        put_rows<D>(QKs, ld, rq, tid);
+        put_rows<D>(QKs + BC * ld, ld, rk, tid);
+        if (A.want_wu) put_rows<D>(Vs, ld, rv, tid);
     }
-    load_gate_beta(A, n, h, cp, gs, bs, tid);
     __syncthreads();
     chunk_prep<D>(QKs, gs, bs, Gs, gam, Dm, KKm, QKm, Zs, Ts, tid);
 
@@ -511,35 +548,6 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
 }
 
 // ---------------------------------------------------------------------------------
-// Register prefetch of one chunk's raw rows of a strided input (q or k): BC x D floats,
-// NF = D / 32 float4 per thread, zero beyond the chunk's real rows.
-template <int D>
-__device__ __forceinline__ void pf_rows(float4 (&r)[D / 32], const float* src, long long stride,
-                                        int nb, bool vec, int tid)
-{
-#pragma unroll
-    for (int kk = 0; kk < D / 32; ++kk) {
-        const int f = tid + CT * kk, t = f / (D / 4), i4 = f - t * (D / 4);
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < nb) {
-            const float* p = src + t * stride + 4 * i4;
-            x = vec ? __ldg(reinterpret_cast<const float4*>(p))
-                    : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
-        }
-        r[kk] = x;
-    }
-}
-
-template <int D>
-__device__ __forceinline__ void put_rows(float* dst, int ld, const float4 (&r)[D / 32], int tid)
-{
-#pragma unroll
-    for (int kk = 0; kk < D / 32; ++kk) {
-        const int f = tid + CT * kk, t = f / (D / 4), i4 = f - t * (D / 4);
-        *reinterpret_cast<float4*>(dst + t * ld + 4 * i4) = r[kk];
-    }
-}
-
 // State chain, rows [p RR, p RR + RR) of M for one head.
 //   forward  (grid: p, head, sequence): every chunk in order; writes the checkpoints at
 //            segment starts, y, and state_T.
