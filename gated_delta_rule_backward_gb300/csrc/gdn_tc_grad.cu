@@ -55,13 +55,16 @@ constexpr int kT64 = 32 * kLbo64 / 4;       // floats per 64-row, K = 128 tile (
 constexpr int kLbo32 = 4 * 128 + 16;        // 32-row tile
 constexpr int kTP = 8 * kLbo32 / 4;         // 32 rows, K = 32
 constexpr int kTPS = 16 * kLbo32 / 4;       // 32 rows, K = 64
-constexpr int kLdM = TD + 4;                // fp32 staging of M / dM, row-major
+constexpr int kLdM = TD + 4;                // fp32 staging, row-major rows of TD floats
+constexpr int kLdU = 4 * TD + 4;            // fp32 staging of a unit-layout park: one row of
+                                            // 128 float4 per 4 columns, 16 bytes of pad between
 
 // shared memory (floats): three big regions reused phase by phase, then small arrays
 constexpr int kR0 = 0;                      // K tile (prep's layout) | [Delta ; X] tile hi, lo
-constexpr int kR1 = kR0 + 2 * kT64;         // [s gamma dY ; -gamma dX] hi, lo | dDelta rows |
+constexpr int kR1 = kR0 + 2 * kT64;         // [s gamma dY ; -gamma dX] hi, lo | dDelta, dY |
                                             // 32 x 32 algebra tiles and the P, [P ; S] tiles
 constexpr int kR2 = kR1 + 2 * kT64;         // M, then dM, fp32 staging | [Q^T | K^T] tile
+static_assert(BC * kLdU <= TD * kLdM, "unit-layout staging of M fits the region");
 constexpr int kR3 = kR2 + TD * kLdM;
 constexpr int kSTr = kR3;                   // T, Z, KK^T, QK^T, Dm: row-major 32 x 32 each
 constexpr int kSZ = kSTr + BC * BC;
@@ -86,13 +89,16 @@ constexpr int kAZ = kAW2 + BC * LDF;
 constexpr int kABP = kAZ + BC * LDF;        // P (rows t, K = 32) hi, lo
 constexpr int kABPS = kABP + 2 * kTP;       // [P ; S]^T (rows t, K = 64) hi, lo
 static_assert(kABPS + 2 * kTPS <= kR2, "R1 overflow");
-constexpr int kDdStage = kR1 + 6 * BC * LDF;   // dDelta rows t (32 x kLdM), before the algebra
-static_assert(kDdStage + BC * kLdM <= kR2, "R1 overflow");
+constexpr int kDdStage = kR1 + 6 * BC * LDF;   // dDelta (unit layout, 8 x kLdU), then
+constexpr int kDyStage = kDdStage + BC * kLdM; // dY rows t (32 x kLdM), before the algebra
+static_assert((BC / 4) * kLdU <= BC * kLdM && kDyStage + BC * kLdM <= kR2, "R1 overflow");
 
 constexpr uint32_t kBytesKb = sizeof(float) * 2 * 32 * 128;
 constexpr uint32_t kBytesFac = sizeof(float) * 5 * BC * BC;
 constexpr uint32_t kBytesGR = sizeof(float) * 2 * BC;
 constexpr uint32_t kBytesQKT = sizeof(float) * 2 * 128 * 64;
+constexpr uint32_t kBytesState = sizeof(float) * TD * TD;
+constexpr uint32_t kBytesDd = sizeof(float) * BC * TD;
 
 __device__ __forceinline__ float warp_sum(float v)
 {
@@ -130,8 +136,12 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     uint64_t* bar_ld = bars;       // K tile, chunk factors, gamma, r
     uint64_t* bar_qkt = bars + 1;  // [Q^T | K^T]
     uint64_t* bar_mma = bars + 2;
+    uint64_t* bar_m = bars + 3;    // M
+    uint64_t* bar_dm = bars + 4;   // dM
+    uint64_t* bar_dd = bars + 5;   // dDelta, dY rows
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
+    __shared__ int s_armed;        // bit b: bars[b] waits for bulk copies
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool compute = warp < 8;
@@ -153,8 +163,12 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         tc::mbar_init(bar_ld, 1);
         tc::mbar_init(bar_qkt, 1);
         tc::mbar_init(bar_mma, 1);
+        tc::mbar_init(bar_m, 1);
+        tc::mbar_init(bar_dm, 1);
+        tc::mbar_init(bar_dd, 1);
         tc::mbar_fence_init();
         s_err = 0;
+        s_armed = 0;
     }
     if (warp == 0) tc::tmem_alloc(&s_tmem, kCols);
     tc::fence_before();
@@ -162,6 +176,30 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     tc::fence_after();
     const uint32_t tmem = s_tmem;
     const uint32_t aHi = tmem + kCA, aLo = tmem + kCA + 128;
+    float* sM = sm + kR2;
+    const bool m_unit = loc > 0;  // M: a parked state (unit layout) or the row-major checkpoint
+    // One L2 prefetch (the chunk's first q row, read in step (3)) through the load/store
+    // path before the CTA's first bulk copies.  Measured on GB300: the whole kernel runs
+    // 0.95 ms at the bench size with it and 1.08 ms without it, a difference spread over
+    // every memory-bound step; more prefetches here are slower again.  The cause is not
+    // known; the timing is what keeps it.
+    if (issuer)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(A.q + (long long)n * A.qs0 + (long long)t0 * A.qs1 +
+                                                       (long long)hk * A.qs2));
+    if (warp == 8) {  // M into R2 by the bulk-copy engine: 32 padded runs, or 128 padded rows
+        if (lane == 0) {
+            s_armed = (1 << 0) | (1 << 3);
+            tc::mbar_expect_tx(bar_m, kBytesState);
+        }
+        __syncwarp();
+        if (m_unit) {
+            tc::bulk_g2s(sM + lane * kLdU, A.ws + A.o_Mc + ch * (long long)(TD * TD) + lane * 4 * TD,
+                         sizeof(float) * 4 * TD, bar_m);
+        } else {
+            const float* ck0 = A.ckpt + (head * A.n_ck + seg) * (long long)(TD * TD);
+            for (int r = lane; r < TD; r += 32) tc::bulk_g2s(sM + r * kLdM, ck0 + r * TD, sizeof(float) * TD, bar_m);
+        }
+    }
     if (issuer) {
         tc::mbar_expect_tx(bar_ld, kBytesKb + kBytesFac + kBytesGR);
         tc::bulk_g2s(sm + kR0, A.ws + A.o_DK + ck * kTcDkElems + kDkKb, kBytesKb, bar_ld);
@@ -174,16 +212,16 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         tc::bulk_g2s(sm + kSGam, A.ws + A.o_gam + ch * BC, sizeof(float) * BC, bar_ld);
         tc::bulk_g2s(sm + kSR, A.ws + A.o_r + ch * BC, sizeof(float) * BC, bar_ld);
     }
-    float* sM = sm + kR2;
-    const bool m_unit = loc > 0;  // M: a parked state (unit layout) or the row-major checkpoint
     const float* sGam = sm + kSGam;
     const float* sR = sm + kSR;
     float* sB = sm + kSB;
     float* red = sm + kSRed;
     float* vec = sm + kSVec;  // gdg, dr, dG, dbeta, dot
 
-    // (0) stage M (row-major fp32) and build A = M (rows j).  The loads of step (1), which do
-    //     not depend on M, go out first so that their latency overlaps the staging.
+    // (0) build A = M (rows j) from the staged M.  The loads of step (1), which do not depend
+    //     on M, go out while the copy is in flight.
+    uint32_t ph = 0;
+    bool ok = true;
     float vx[32], dy[16];
     float4 dx[4];
     if (compute) {
@@ -200,25 +238,17 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             const bool real = tid < nb;
             sB[tid] = real ? __ldg(A.beta + (tok0 + tid) * A.H_v + h) : 0.f;
         }
-        const float4* Mg4 = reinterpret_cast<const float4*>(
-            m_unit ? A.ws + A.o_Mc + ch * (long long)(TD * TD) : A.ckpt + (head * A.n_ck + seg) * (long long)(TD * TD));
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {  // 16 float4 per thread, 8 in flight at a time
-            float4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldg(Mg4 + tid + 256 * (8 * half + u));
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int idx = tid + 256 * (8 * half + u);
-                const int j = m_unit ? idx % TD : idx >> 5, i4 = m_unit ? idx / TD : idx & 31;
-                *reinterpret_cast<float4*>(sM + j * kLdM + 4 * i4) = v[u];
-            }
-        }
-        tc::bar_sync_first(256);
+        if (!tc::mbar_wait(bar_m, 0)) s_err = 1;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const float4 a = *reinterpret_cast<const float4*>(sM + row * kLdM + 64 * hc + 8 * q);
-            const float4 b = *reinterpret_cast<const float4*>(sM + row * kLdM + 64 * hc + 8 * q + 4);
+            float4 a, b;
+            if (m_unit) {
+                a = *reinterpret_cast<const float4*>(sM + (16 * hc + 2 * q) * kLdU + 4 * row);
+                b = *reinterpret_cast<const float4*>(sM + (16 * hc + 2 * q + 1) * kLdU + 4 * row);
+            } else {
+                a = *reinterpret_cast<const float4*>(sM + row * kLdM + 64 * hc + 8 * q);
+                b = *reinterpret_cast<const float4*>(sM + row * kLdM + 64 * hc + 8 * q + 4);
+            }
             const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
             uint32_t hi[8], lo[8];
 #pragma unroll
@@ -230,6 +260,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     }
     tc::fence_before();
     __syncthreads();
+    if (s_err) goto done;
 
     // (1) D_X = M K^T.  Meanwhile: the B tile [s gamma dY ; -gamma dX] and dv.
     if (issuer) {
@@ -256,8 +287,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             }
         }
     }
-    uint32_t ph = 0;
-    bool ok = tc::mbar_wait(bar_mma, ph);
+    ok = tc::mbar_wait(bar_mma, ph);
     ph ^= 1;
     tc::fence_after();
     // (2) X^T, Delta^T (rows j) -> the [Delta ; X] tile; A = M^T (rows i)
@@ -278,13 +308,17 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             put_split(b34, kT64, padoff(t, row, kLbo64 / 4), acc);
             put_split(b34, kT64, padoff(BC + t, row, kLbo64 / 4), hc ? x[16 + e] : x[e]);
         }
+        {  // M[j][row] for this thread's 64 j
+            const float* mc = sM + (m_unit ? (row >> 2) * kLdU + (row & 3) : row);
+            const int js = m_unit ? 4 : kLdM;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            uint32_t hi[8], lo[8];
+            for (int q = 0; q < 8; ++q) {
+                uint32_t hi[8], lo[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) tc::split_tf32(sM[(64 * hc + 8 * q + e) * kLdM + row], hi[e], lo[e]);
-            tc::st8(tc::taddr(tmem, warp, kCA + 64 * hc + 8 * q), hi);
-            tc::st8(tc::taddr(tmem, warp, kCA + 128 + 64 * hc + 8 * q), lo);
+                for (int e = 0; e < 8; ++e) tc::split_tf32(mc[(64 * hc + 8 * q + e) * js], hi[e], lo[e]);
+                tc::st8(tc::taddr(tmem, warp, kCA + 64 * hc + 8 * q), hi);
+                tc::st8(tc::taddr(tmem, warp, kCA + 128 + 64 * hc + 8 * q), lo);
+            }
         }
         tc::wait_st();
     }
@@ -293,9 +327,20 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     tc::fence_before();
     __syncthreads();
     if (s_err) goto done;
-    // (3) D2 = M^T [s gamma dY ; -gamma dX]^T.  Meanwhile dM replaces M in the staging, with
-    //     <dM, M> on the way, and q_t, k_t (this thread's tokens) for the dgamma and dr sums.
+    // (3) D2 = M^T [s gamma dY ; -gamma dX]^T.  Meanwhile dM replaces M in R2 (bulk copy), and
+    //     q_t, k_t (this thread's tokens) come in for the dgamma and dr sums.
     float qv[16], kv[16];
+    if (warp == 8) {
+        if (lane == 0) {
+            tc::fence_async_smem();
+            s_armed |= 1 << 4;
+            tc::mbar_expect_tx(bar_dm, kBytesState);
+        }
+        __syncwarp();
+        tc::bulk_g2s(sM + lane * kLdU, A.ws + A.o_dM + ch * (long long)(TD * TD) + lane * 4 * TD,
+                     sizeof(float) * 4 * TD, bar_dm);
+        __syncwarp();
+    }
     if (issuer) {
         tc::fence_after();
         mma3_t(tmem + kC2, aHi, aLo, tc::make_desc(tc::smem_addr(sm + kR1), kLbo64, 128),
@@ -310,35 +355,29 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             qv[e] = (tb + e < nb) ? __ldg(qp + (long long)(tb + e) * A.qs1) : 0.f;
             kv[e] = (tb + e < nb) ? __ldg(kp + (long long)(tb + e) * A.ks1) : 0.f;
         }
-        const float4* dM4 = reinterpret_cast<const float4*>(A.ws + A.o_dM + ch * (long long)(TD * TD));
-        float dot = 0.f;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldg(dM4 + tid + 256 * (8 * half + u));
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int idx = tid + 256 * (8 * half + u);
-                const int j = idx % TD, i4 = idx / TD;
-                float4* p = reinterpret_cast<float4*>(sM + j * kLdM + 4 * i4);
-                const float4 m = *p;
-                dot = __fmaf_rn(v[u].x, m.x, dot);
-                dot = __fmaf_rn(v[u].y, m.y, dot);
-                dot = __fmaf_rn(v[u].z, m.z, dot);
-                dot = __fmaf_rn(v[u].w, m.w, dot);
-                *p = v[u];
-            }
-        }
-        dot = warp_sum(dot);
-        if (lane == 0) red[(warp & 3) * 96 + 64 + hc] = dot;
     }
     ok = tc::mbar_wait(bar_mma, ph);
     ph ^= 1;
     tc::fence_after();
-    // (4) gamma dgamma partials from D2; A = dM^T (rows i)
+    // (4) gamma dgamma partials from D2; A = dM^T (rows i) and <dM, M> (M^T still in TMEM).
+    //     R1's B tile is dead: dDelta and the dY rows come into it.
+    if (warp == 8) {
+        const bool dy_bulk = A.vec_gy != 0;
+        if (lane == 0) {
+            s_armed |= 1 << 5;
+            tc::mbar_expect_tx(bar_dd, kBytesDd + (dy_bulk ? nb * (uint32_t)sizeof(float) * TD : 0u));
+        }
+        __syncwarp();
+        if (lane < BC / 4)
+            tc::bulk_g2s(sm + kDdStage + lane * kLdU, A.ws + A.o_dDel + ch * (BC * TD) + lane * 4 * TD,
+                         sizeof(float) * 4 * TD, bar_dd);
+        if (dy_bulk && lane < nb)
+            tc::bulk_g2s(sm + kDyStage + lane * kLdM,
+                         A.gy + (long long)n * A.gys0 + (long long)(t0 + lane) * A.gys1 + (long long)h * A.gys2,
+                         sizeof(float) * TD, bar_dd);
+    }
     if (compute) {
-        tc::bar_sync_first(256);  // dM fully staged
+        if (!tc::mbar_wait(bar_dm, 0)) s_err = 1;
         float dq[16], dk[16];
         tc::ld16(tc::taddr(tmem, warp, kC2 + tb), dq);
         tc::ld16(tc::taddr(tmem, warp, kC2 + BC + tb), dk);
@@ -348,13 +387,28 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             const float g = warp_sum(__fmaf_rn(kv[e], dk[e], __fmul_rn(qv[e], dq[e])));
             if (lane == 0) red[(warp & 3) * 96 + tb + e] = g;
         }
+        {
+            const float* dmc = sM + (row >> 2) * kLdU + (row & 3);  // dM[j][row] at dmc[4 j]
+            float dot = 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            uint32_t hi[8], lo[8];
+            for (int q = 0; q < 8; ++q) {
+                const int j0 = 64 * hc + 8 * q;
+                float mh[8], ml[8];
+                tc::ld8(tc::taddr(tmem, warp, kCA + j0), mh);
+                tc::ld8(tc::taddr(tmem, warp, kCA + 128 + j0), ml);
+                tc::wait_ld();
+                uint32_t hi[8], lo[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) tc::split_tf32(sM[(64 * hc + 8 * q + e) * kLdM + row], hi[e], lo[e]);
-            tc::st8(tc::taddr(tmem, warp, kCA + 64 * hc + 8 * q), hi);
-            tc::st8(tc::taddr(tmem, warp, kCA + 128 + 64 * hc + 8 * q), lo);
+                for (int e = 0; e < 8; ++e) {
+                    const float d = dmc[4 * (j0 + e)];
+                    dot = __fmaf_rn(d, __fadd_rn(mh[e], ml[e]), dot);  // hi + lo = M exactly
+                    tc::split_tf32(d, hi[e], lo[e]);
+                }
+                tc::st8(tc::taddr(tmem, warp, kCA + j0), hi);
+                tc::st8(tc::taddr(tmem, warp, kCA + 128 + j0), lo);
+            }
+            dot = warp_sum(dot);
+            if (lane == 0) red[(warp & 3) * 96 + 64 + hc] = dot;
         }
         tc::wait_st();
     }
@@ -362,8 +416,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     tc::fence_before();
     __syncthreads();
     if (s_err) goto done;
-    // (5) D3 = dM^T Delta^T, then [Q^T | K^T] into the staging region.  Meanwhile dDelta
-    //     (rows t) into R1.
+    // (5) D3 = dM^T Delta^T, then [Q^T | K^T] into the staging region.
     if (issuer) {
         tc::fence_after();
         mma3_t(tmem + kC3, aHi, aLo, tc::make_desc(tc::smem_addr(sm + kR0), kLbo64, 128),
@@ -371,23 +424,9 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                tc::idesc_tf32(32), false);
         tc::commit(bar_mma);
         tc::fence_async_smem();
+        s_armed |= 1 << 1;
         tc::mbar_expect_tx(bar_qkt, kBytesQKT);
         tc::bulk_g2s(sm + kR2, A.ws + A.o_DK + ck * kTcDkElems + kDkQKT, kBytesQKT, bar_qkt);
-    } else if (compute) {
-        float* sdd = sm + kDdStage;
-        const float4* dd4 = reinterpret_cast<const float4*>(A.ws + A.o_dDel + ch * (BC * TD));
-        float4 d[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) d[u] = __ldg(dd4 + tid + 256 * u);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = tid + 256 * u;
-            const int j = idx % TD, t = 4 * (idx / TD);
-            sdd[t * kLdM + j] = d[u].x;
-            sdd[(t + 1) * kLdM + j] = d[u].y;
-            sdd[(t + 2) * kLdM + j] = d[u].z;
-            sdd[(t + 3) * kLdM + j] = d[u].w;
-        }
     }
     ok = tc::mbar_wait(bar_mma, ph);
     ph ^= 1;
@@ -395,7 +434,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     // (6) dr partials from D3 (kept for dk); A = [dY ; dDelta ; 0] (rows t)
     float d3[16];
     if (compute) {
-        tc::bar_sync_first(256);  // dDelta staged
+        if (!tc::mbar_wait(bar_dd, 0)) s_err = 1;
         tc::ld16(tc::taddr(tmem, warp, kC3 + tb), d3);
         tc::wait_ld();
 #pragma unroll
@@ -405,7 +444,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         }
         const int quarter = warp & 3;
         const float* gyr = A.gy + (long long)n * A.gys0 + (long long)(t0 + lane) * A.gys1 + (long long)h * A.gys2 + 64 * hc;
-        const float* sdd = sm + kDdStage + lane * kLdM + 64 * hc;
+        const float* sdd = sm + kDdStage + (lane >> 2) * kLdU + (lane & 3) + 4 * 64 * hc;  // dDelta[lane][j]
+        const float* sdy = sm + kDyStage + lane * kLdM + 64 * hc;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {  // 32 of this thread's 64 columns at a time
             float v[32];
@@ -413,7 +453,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                 if (lane < nb && A.vec_gy) {
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        const float4 x = __ldg(reinterpret_cast<const float4*>(gyr + 32 * half) + u);
+                        const float4 x = *reinterpret_cast<const float4*>(sdy + 32 * half + 4 * u);
                         v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
                     }
                 } else {
@@ -422,7 +462,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                 }
             } else if (quarter == 1) {  // rows 32..63: dDelta row t = lane
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = sdd[32 * half + e];
+                for (int e = 0; e < 32; ++e) v[e] = sdd[4 * (32 * half + e)];
             } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0.f;
@@ -642,7 +682,11 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     if (!ok) s_err = 1;
 done:
     __syncthreads();
-    if (s_err && issuer) atomicExch(&g_tcg_status, kStatusTimeout);
+    if (s_err && issuer) {
+        atomicExch(&g_tcg_status, kStatusTimeout);
+        for (int b = 0; b < 6; ++b)  // let this CTA's bulk copies land before it exits
+            if (s_armed & (1 << b)) tc::mbar_wait(bars + b, 0);
+    }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
