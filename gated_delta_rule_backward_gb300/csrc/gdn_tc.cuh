@@ -262,6 +262,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
 
 // Bulk copy global -> shared (TMA engine, no tensor map): both addresses 16-byte aligned,
 // bytes a multiple of 16.  Completion is counted on `bar` in bytes.
+// An L2 prefetch hint for one line through the load/store path.  A CTA whose first global
+// access is a bulk copy ran its memory-bound steps measurably slower on GB300 than one that
+// touched global memory through the load/store path first (cause unknown); the kernels issue
+// one of these before their first bulk copies.
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
 {
     asm volatile(

@@ -136,6 +136,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     uint32_t ph_b1 = 0, ph_b23 = 0, ph_mma = 0;
     bool b1_pending = false, b23_pending = false;
     if (issuer) {
+        tc::prefetch_l2(A.ws + A.o_U + (head * A.n_chunks + c_begin) * (BC * TD));  // see prefetch_l2
         load_b1(A, head * A.n_chunks + c_begin, khead * A.n_chunks + c_begin, sm, bar_b1);
         load_b23(A, head * A.n_chunks + c_begin, sm, bar_b23);
         b1_pending = b23_pending = true;
@@ -453,6 +454,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
     uint32_t ph_kb = 0, ph_rest = 0, ph_mma = 0;
     bool kb_pending = false, rest_pending = false;
     if (issuer) {
+        tc::prefetch_l2(A.ws + A.o_DS + (head * A.n_chunks + c_last) * kTcDsElems);  // see prefetch_l2
         ds_load_kb(A, khead * A.n_chunks + c_last, sm, bar_kb);
         ds_load_rest(A, head * A.n_chunks + c_last, khead * A.n_chunks + c_last, sm, bar_rest);
         kb_pending = rest_pending = true;

@@ -178,14 +178,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     const uint32_t aHi = tmem + kCA, aLo = tmem + kCA + 128;
     float* sM = sm + kR2;
     const bool m_unit = loc > 0;  // M: a parked state (unit layout) or the row-major checkpoint
-    // One L2 prefetch (the chunk's first q row, read in step (3)) through the load/store
-    // path before the CTA's first bulk copies.  Measured on GB300: the whole kernel runs
-    // 0.95 ms at the bench size with it and 1.08 ms without it, a difference spread over
-    // every memory-bound step; more prefetches here are slower again.  The cause is not
-    // known; the timing is what keeps it.
-    if (issuer)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(A.q + (long long)n * A.qs0 + (long long)t0 * A.qs1 +
-                                                       (long long)hk * A.qs2));
+    if (issuer)  // see tc::prefetch_l2 (measured 0.95 vs 1.08 ms per launch at the bench size)
+        tc::prefetch_l2(A.q + (long long)n * A.qs0 + (long long)t0 * A.qs1 + (long long)hk * A.qs2);
     if (warp == 8) {  // M into R2 by the bulk-copy engine: 32 padded runs, or 128 padded rows
         if (lane == 0) {
             s_armed = (1 << 0) | (1 << 3);
