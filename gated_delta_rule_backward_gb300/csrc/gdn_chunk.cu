@@ -434,7 +434,10 @@ template <int D>
 __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
 {
     constexpr int ld = Ld<D>::v;
-    const int c = A.c_lo + blockIdx.x, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
+    // blockIdx.x = (chunk - c_lo) * H_v + slot, the r value heads of one key head in adjacent
+    // slots: they run together and read the key head's q and k rows through L2
+    const int slot = blockIdx.x % A.H_v, c = A.c_lo + blockIdx.x / A.H_v, n = blockIdx.y, tid = threadIdx.x;
+    const int h = (slot % (A.H_v / A.H_k)) * A.H_k + slot / (A.H_v / A.H_k);
     const int hk = h % A.H_k;
     const ChunkPos cp = chunk_pos(A, c);
     const long long ch = ((long long)n * A.H_v + h) * A.n_chunks + c;
@@ -1326,7 +1329,7 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
         range_of(a, R, r, ar);
         int err = set_smem(gdn_chunk_prep_kernel<128>, prep_smem<128>());
         if (err) return err;
-        gdn_chunk_prep_kernel<128><<<dim3(ar.c_hi - ar.c_lo, a.H_v, a.N), CT, prep_smem<128>(), lo>>>(ar);
+        gdn_chunk_prep_kernel<128><<<dim3((ar.c_hi - ar.c_lo) * a.H_v, a.N), CT, prep_smem<128>(), lo>>>(ar);
         err = (int)cudaGetLastError();
         if (!err) err = (int)cudaEventRecord((cudaEvent_t)P->prep_done[r], lo);
         return err;
@@ -1368,7 +1371,7 @@ static int chunk_forward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
         if (a.want_tc) return tc_pipelined(a, s, false, tap);
     }
     tap.mark(s);
-    GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks, a.H_v, a.N), prep_smem<D>());
+    GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks * a.H_v, a.N), prep_smem<D>());
     GDN_LAUNCH((gdn_chunk_state_kernel<D, true>), dim3(Rows<D>::P, a.H_v, a.N), state_smem<D>());
     return 0;
 }
@@ -1380,7 +1383,7 @@ static int chunk_backward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
         if (a.want_tc) return tc_pipelined(a, s, true, tap);
     }
     tap.mark(s);
-    GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks, a.H_v, a.N), prep_smem<D>());
+    GDN_LAUNCH(gdn_chunk_prep_kernel<D>, dim3(a.n_chunks * a.H_v, a.N), prep_smem<D>());
     if (a.cps > 1)
         GDN_LAUNCH((gdn_chunk_state_kernel<D, false>), dim3(Rows<D>::P, a.n_ck, a.N * a.H_v),
                    state_smem<D>());
