@@ -108,6 +108,10 @@ WORKLOADS = {
     # the throughput shape: 1 seq, H_k=16/H_v=48, d=128, T=4096, scalar gate, default C
     "bench_d128_T4096": dict(N=1, T=4096, H_k=16, H_v=48, d=128, kda=False, C=None,
                              seed=1004, packed=True),
+    # the throughput shape cut to T=1024 with the same C=64 (two chunks per segment): the
+    # size a many-pass profiler capture of one kernel launch stays small at
+    "profile_d128_T1024": dict(N=1, T=1024, H_k=16, H_v=48, d=128, kda=False, C=64,
+                               seed=1005, packed=True),
 }
 
 
