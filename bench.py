@@ -75,9 +75,10 @@ def kernel_plan(chunked, d, n_bwd, cps):
     """(stage name, flop kind) per timed stage of one forward and one backward, in order."""
     if not chunked:
         return [("gdn_fwd_kernel", None)], [("gdn_bwd_kernel", None), ("gdn_reduce_kernel", None)]
-    if d == 128:  # chunk-range preps pipelined with the chains on two streams
+    if d == 128:  # forward: chunk-range preps pipelined with the state chain; backward, as
+        # timed stage by stage (its calls with timing events run the stages in sequence)
         fwd = [("gdn_chunk_prep_kernel + gdn_tc_state_kernel (pipelined)", "fwd_pipe")]
-        bwd = [("gdn_chunk_prep_kernel + gdn_tc_bwd_chains_kernel (pipelined)", "bwd_pipe"),
+        bwd = [("gdn_chunk_prep_kernel + gdn_tc_bwd_chains_kernel", "bwd_pipe"),
                ("gdn_tc_grad_kernel", "grad_tc"), ("gdn_tc_dqdk_sum_kernel", "dqdk_sum")]
         return fwd, bwd
     fwd = [("gdn_chunk_prep_kernel", "prep_fwd"), ("gdn_chunk_state_kernel", "state_fwd")]
@@ -352,13 +353,21 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
 
-    # per step: forward events (before + after each kernel), backward events likewise
+    # Timed steps: events on the stream around each call only (no per-stage events), so the
+    # calls run exactly as a user's do.
     mk = lambda: torch.cuda.Event(enable_timing=True)
+    sev = [(mk(), mk(), mk()) for _ in range(args.steps)]
+    for trio in sev:
+        for e in trio:
+            e.record(stream)  # materialise the event handles
+    # Per-stage times, from separate steps with the library's stage events (a backward call
+    # with stage events runs its kernels one after another, so each stage is one kernel).
+    n_stage_steps = max(3, min(args.steps, 5))
     ev = [([mk() for _ in range(n_fwd + 1)], [mk() for _ in range(n_bwd + 1)])
-          for _ in range(args.steps)]
+          for _ in range(n_stage_steps)]
     for fe, be in ev:
         for e in fe + be:
-            e.record(stream)  # materialise the event handles
+            e.record(stream)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     if dist:
@@ -368,6 +377,21 @@ def run_ours(args):
     time.sleep(0.3)
     for i in range(args.steps):
         flush.zero_()  # L2 flush between timed steps (not inside the events)
+        e0, e1, e2 = sev[i]
+        e0.record(stream)
+        gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, fws, stream)
+        e1.record(stream)
+        gdn.gdn_backward(p, q, k, v, g, beta, ck, gy, None, packed, ws, stream)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    fwd_ms = [e0.elapsed_time(e1) for e0, e1, _ in sev]
+    bwd_ms = [e1.elapsed_time(e2) for _, e1, e2 in sev]
+    steps_ms = [e0.elapsed_time(e2) for e0, _, e2 in sev]
+    for i in range(n_stage_steps):
+        flush.zero_()
         fe, be = ev[i]
         gdn.set_timing_events(fe)
         gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, fws, stream)
@@ -375,19 +399,12 @@ def run_ours(args):
         gdn.gdn_backward(p, q, k, v, g, beta, ck, gy, None, packed, ws, stream)
     gdn.set_timing_events(None)
     torch.cuda.synchronize()
-    clk = clocks.stop()
-    if dist:
-        dist.barrier()
     kern_ms = [0.0] * (n_fwd + n_bwd)
-    fwd_ms, bwd_ms, steps_ms = [], [], []
     for fe, be in ev:
         for j in range(n_fwd):
-            kern_ms[j] += fe[j].elapsed_time(fe[j + 1]) / args.steps
+            kern_ms[j] += fe[j].elapsed_time(fe[j + 1]) / n_stage_steps
         for j in range(n_bwd):
-            kern_ms[n_fwd + j] += be[j].elapsed_time(be[j + 1]) / args.steps
-        fwd_ms.append(fe[0].elapsed_time(fe[-1]))
-        bwd_ms.append(be[0].elapsed_time(be[-1]))
-        steps_ms.append(fe[0].elapsed_time(be[-1]))
+            kern_ms[n_fwd + j] += be[j].elapsed_time(be[j + 1]) / n_stage_steps
     step_ms = sum(steps_ms) / args.steps
     if dist:
         step_ms = max_over_ranks(step_ms, dist, dev)

@@ -288,11 +288,16 @@ int gdn::acquire_pipeline(gdn::Pipeline** out)
         gdn::Pipeline& P = g_pipes[dev];
         int least = 0, greatest = 0;
         e = (int)cudaDeviceGetStreamPriorityRange(&least, &greatest);
-        cudaStream_t hi = nullptr, lo = nullptr;
+        // numerically lower is more urgent; the middle level falls back to the lowest
+        const int middle = greatest + 1 < least ? greatest + 1 : least;
+        cudaStream_t hi = nullptr, lo = nullptr, bg = nullptr, rc = nullptr;
         if (!e) e = (int)cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest);
-        if (!e) e = (int)cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, least);
-        cudaEvent_t ev[3 + 2 * gdn::kMaxRanges] = {};
-        for (int i = 0; i < 3 + 2 * gdn::kMaxRanges && !e; ++i)
+        if (!e) e = (int)cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, middle);
+        if (!e) e = (int)cudaStreamCreateWithPriority(&bg, cudaStreamNonBlocking, least);
+        if (!e) e = (int)cudaStreamCreateWithPriority(&rc, cudaStreamNonBlocking, middle);
+        constexpr int kEv = 5 + 4 * gdn::kMaxRanges;
+        cudaEvent_t ev[kEv] = {};
+        for (int i = 0; i < kEv && !e; ++i)
             e = (int)cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
         if (e) {
             release_pipeline();
@@ -300,12 +305,18 @@ int gdn::acquire_pipeline(gdn::Pipeline** out)
         }
         P.hi = hi;
         P.lo = lo;
+        P.bg = bg;
+        P.rc = rc;
         P.fork = ev[0];
         P.join_hi = ev[1];
         P.join_lo = ev[2];
+        P.join_bg = ev[3];
+        P.join_rc = ev[4];
         for (int i = 0; i < gdn::kMaxRanges; ++i) {
-            P.prep_done[i] = ev[3 + i];
-            P.chain_go[i] = ev[3 + gdn::kMaxRanges + i];
+            P.prep_done[i] = ev[5 + i];
+            P.chain_go[i] = ev[5 + gdn::kMaxRanges + i];
+            P.ds_done[i] = ev[5 + 2 * gdn::kMaxRanges + i];
+            P.rc_done[i] = ev[5 + 3 * gdn::kMaxRanges + i];
         }
         g_pipe_ready[dev] = true;
     }
@@ -324,8 +335,8 @@ void gdn::release_pipeline()
 
 int gdn::pipeline_ranges(int n_ck, bool backward)
 {
-    if (backward) return 1;
-    return n_ck < gdn::kMaxRanges ? (n_ck < 1 ? 1 : n_ck) : gdn::kMaxRanges;
+    const int m = backward ? 2 : gdn::kMaxRanges;
+    return n_ck < m ? (n_ck < 1 ? 1 : n_ck) : m;
 }
 
 void gdn::EventTap::mark(void* stream)
@@ -407,10 +418,10 @@ int gdn_backward_launches(const gdn_params_t* p)
     if (check_sizes(p) != GDN_OK) return 0;
     if (p->n_seq == 0) return 0;
     const Plan pl = make_plan(p);
-    // chunked: prep, [recompute], dM chain, gradients; on the tensor-core path: per chunk
-    // range a prep and a launch of both chains, then the gradient step and the sum over
-    // value heads
-    if (pl.chunked) return pl.tensor ? 2 * tc_ranges(pl, true) + 2 : (pl.cps > 1 ? 4 : 3);
+    // chunked: prep, [recompute], dM chain, gradients; on the tensor-core path, per chunk
+    // range: prep, dM chain, [recompute,] gradient step and sum over value heads (a call
+    // with timing events: prep, both chains, gradient step, sum, i.e. 4)
+    if (pl.chunked) return pl.tensor ? tc_ranges(pl, true) * (pl.cps > 1 ? 5 : 4) : (pl.cps > 1 ? 4 : 3);
     return p->T > 0 ? 2 : 1;
 }
 

@@ -1291,10 +1291,7 @@ static int set_smem(K kern, size_t bytes)
         tap.mark(s);                                                                   \
     } while (0)
 
-// The tensor-core path (head size 128): the chunk range r of the prep runs on a
-// low-priority library stream while the serial chain works through range r - 1 on a
-// high-priority one (the chain's 48 CTAs leave most SMs to the prep).  Only events order
-// the two: prep(r) -> chain(r), and the caller's stream forks into both and joins back.
+// Chunk range r of R: whole checkpoint segments, [c_lo, c_hi).
 static void range_of(const ChunkArgs& a, int R, int r, ChunkArgs& out)
 {
     const int seg_per = (a.n_ck + R - 1) / R;
@@ -1303,20 +1300,48 @@ static void range_of(const ChunkArgs& a, int R, int r, ChunkArgs& out)
     out.c_hi = min(a.n_chunks, (r + 1) * seg_per * a.cps);
 }
 
+static int launch_prep_range(const ChunkArgs& a, int R, int r, cudaStream_t st)
+{
+    ChunkArgs ar;
+    range_of(a, R, r, ar);
+    int err = set_smem(gdn_chunk_prep_kernel<128>, prep_smem<128>());
+    if (err) return err;
+    gdn_chunk_prep_kernel<128><<<dim3((ar.c_hi - ar.c_lo) * a.H_v, a.N), CT, prep_smem<128>(), st>>>(ar);
+    return (int)cudaGetLastError();
+}
+
+// The pipelined tensor-core path at head size 128.  The chunks are cut into R
+// segment-aligned ranges (range_of); only events order the library streams, and the call
+// forks from and joins back to the caller's stream.
+//
+// Forward, ranges first to last: prep(r) on the middle-priority stream, then the state
+// chain of range r on the high-priority one (the chain's 48 CTAs leave most SMs free);
+// prep(r + 1) is enqueued once chain(r) has been, so that the chain's whole-SM CTAs are
+// placed before the prep fills the GPU.
+//
+// Backward, ranges last to first, three streams:
+//   high:   dM chain of range r (after prep(r)), carrying dM to range r - 1
+//   middle: prep(r), then prep(r - 1) once the dM chain of r has been enqueued
+//   low:    recompute of range r's segments (after prep(r)), then, after the dM chain of r,
+//           the gradient step and the sum over value heads for range r
+// so that the gradient work of one range runs while the chain walks the next.  With timing
+// events set, the backward instead runs its stages one after another as a single range
+// (prep, both chains, gradient step, sum), each between two events.
 static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, EventTap& tap)
 {
     Pipeline* P = nullptr;
     int e = acquire_pipeline(&P);
     if (e) return e;
-    const cudaStream_t hi = (cudaStream_t)P->hi, lo = (cudaStream_t)P->lo;
-    const int R = pipeline_ranges(a.n_ck, backward);
+    const cudaStream_t hi = (cudaStream_t)P->hi, lo = (cudaStream_t)P->lo, bg = (cudaStream_t)P->bg;
+    const cudaStream_t rc = (cudaStream_t)P->rc;
+    const bool staged = backward && tap.ev != nullptr;
+    const int R = staged ? 1 : pipeline_ranges(a.n_ck, backward);
     tap.mark(user);
     e = (int)cudaEventRecord((cudaEvent_t)P->fork, user);
     if (!e) e = (int)cudaStreamWaitEvent(lo, (cudaEvent_t)P->fork, 0);
     if (!e) e = (int)cudaStreamWaitEvent(hi, (cudaEvent_t)P->fork, 0);
-    // The forward's chain runs ranges first to last, the dM chain last to first.  The prep
-    // of the next range waits until the chain of this range is about to launch, so that
-    // the chain's CTAs (a whole SM each) are placed before the prep's fill the GPU.
+    if (!e && backward && !staged) e = (int)cudaStreamWaitEvent(bg, (cudaEvent_t)P->fork, 0);
+    if (!e && backward && !staged) e = (int)cudaStreamWaitEvent(rc, (cudaEvent_t)P->fork, 0);
     int order[kMaxRanges], nr = 0;
     for (int i = 0; i < R; ++i) {
         const int r = backward ? R - 1 - i : i;
@@ -1324,37 +1349,52 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
         range_of(a, R, r, ar);
         if (ar.c_hi > ar.c_lo) order[nr++] = r;
     }
-    auto launch_prep = [&](int r) -> int {
-        ChunkArgs ar;
-        range_of(a, R, r, ar);
-        int err = set_smem(gdn_chunk_prep_kernel<128>, prep_smem<128>());
-        if (err) return err;
-        gdn_chunk_prep_kernel<128><<<dim3((ar.c_hi - ar.c_lo) * a.H_v, a.N), CT, prep_smem<128>(), lo>>>(ar);
-        err = (int)cudaGetLastError();
+    auto prep = [&](int r) -> int {
+        int err = launch_prep_range(a, R, r, lo);
         if (!err) err = (int)cudaEventRecord((cudaEvent_t)P->prep_done[r], lo);
         return err;
     };
-    if (!e && nr > 0) e = launch_prep(order[0]);
+    if (!e && nr > 0) e = prep(order[0]);
     for (int i = 0; i < nr && !e; ++i) {
         const int r = order[i];
         ChunkArgs ar;
         range_of(a, R, r, ar);
         e = (int)cudaStreamWaitEvent(hi, (cudaEvent_t)P->prep_done[r], 0);
         if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->chain_go[r], hi);
-        if (!e) e = backward ? launch_tc_bwd_chains(ar, hi) : launch_tc_state(ar, hi);
+        if (!e) {
+            if (!backward) e = launch_tc_state(ar, hi);
+            else if (staged) e = launch_tc_bwd_chains(ar, hi);
+            else e = launch_tc_dstate(ar, hi);
+        }
+        if (!e && backward && !staged) {
+            e = (int)cudaEventRecord((cudaEvent_t)P->ds_done[r], hi);
+            if (!e) e = (int)cudaStreamWaitEvent(rc, (cudaEvent_t)P->prep_done[r], 0);
+            if (!e) e = launch_tc_recompute(ar, rc);
+            if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->rc_done[r], rc);
+            if (!e) e = (int)cudaStreamWaitEvent(bg, (cudaEvent_t)P->rc_done[r], 0);
+            if (!e) e = (int)cudaStreamWaitEvent(bg, (cudaEvent_t)P->ds_done[r], 0);
+            if (!e) e = launch_tc_grad(ar, bg);
+            if (!e) e = launch_tc_dqdk_sum(ar, bg);
+        }
         if (!e && i + 1 < nr) {
             e = (int)cudaStreamWaitEvent(lo, (cudaEvent_t)P->chain_go[r], 0);
-            if (!e) e = launch_prep(order[i + 1]);
+            if (!e) e = prep(order[i + 1]);
         }
     }
     if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_hi, hi);
     if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_lo, lo);
     if (!e) e = (int)cudaStreamWaitEvent(user, (cudaEvent_t)P->join_hi, 0);
     if (!e) e = (int)cudaStreamWaitEvent(user, (cudaEvent_t)P->join_lo, 0);
+    if (!e && backward && !staged) {
+        e = (int)cudaEventRecord((cudaEvent_t)P->join_bg, bg);
+        if (!e) e = (int)cudaStreamWaitEvent(user, (cudaEvent_t)P->join_bg, 0);
+        if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_rc, rc);
+        if (!e) e = (int)cudaStreamWaitEvent(user, (cudaEvent_t)P->join_rc, 0);
+    }
     release_pipeline();
     if (e) return e;
     tap.mark(user);
-    if (!backward) return 0;
+    if (!staged) return 0;
     e = launch_tc_grad(a, user);
     if (e) return e;
     tap.mark(user);

@@ -120,26 +120,32 @@ struct EventTap {
     void mark(void* stream);
 };
 
-// Library streams of one device for the pipelined tensor-core path: chunk-range preps on
-// a low-priority stream overlap the serial chains on a high-priority one.  Created on
-// first use; `mu` serialises the enqueueing of calls that use them.
+// Library streams of one device for the pipelined tensor-core path: the serial chains on
+// a high-priority stream, the chunk-range preps on a middle one, and (backward) the
+// recompute, gradient and sum kernels on a low one.  Created on first use; the lock
+// serialises the enqueueing of calls that use them.
 constexpr int kMaxRanges = 4;
 struct Pipeline {
     void* hi;
     void* lo;
+    void* bg;
+    void* rc;
     void* fork;
     void* join_hi;
     void* join_lo;
+    void* join_bg;
+    void* join_rc;
     void* prep_done[kMaxRanges];
     void* chain_go[kMaxRanges];
+    void* ds_done[kMaxRanges];
+    void* rc_done[kMaxRanges];
 };
 // Returns the current device's pipeline (creating it on first use) with its lock held;
 // release_pipeline() unlocks.  Returns a cudaError_t as int.
 int acquire_pipeline(Pipeline** out);
 void release_pipeline();
-// Chunk ranges of the pipelined path: segment-aligned, at most kMaxRanges (forward).  The
-// backward runs one range: its parallel work (prep and recompute) outweighs the dM chain,
-// so splitting it only adds launches.
+// Chunk ranges of the pipelined path: segment-aligned, at most kMaxRanges.  (A backward
+// call with timing events runs its stages one after another instead, as one range.)
 int pipeline_ranges(int n_ck, bool backward);
 
 // Tensor-core operands of the state chain (head size 128), in the operand layouts of
@@ -168,7 +174,9 @@ int launch_chunk_forward(const ChunkArgs& a, int D, void* stream, EventTap& tap)
 // The chains on the tensor cores (gdn_tc_chain.cu): the forward's state chain, and the
 // backward's dM chain together with the recompute of the chunk-entry states.
 int launch_tc_state(const ChunkArgs& a, void* stream);
-int launch_tc_bwd_chains(const ChunkArgs& a, void* stream);
+int launch_tc_bwd_chains(const ChunkArgs& a, void* stream);  // dM chain + recompute
+int launch_tc_dstate(const ChunkArgs& a, void* stream);      // dM chain over [c_lo, c_hi)
+int launch_tc_recompute(const ChunkArgs& a, void* stream);   // states of its segments
 // The gradient step on the tensor cores (gdn_tc_grad.cu): per (chunk, value head) every
 // gradient of the chunk (dv, dg, dbeta written; this value head's dq, dk parked row-major
 // [t][i] at o_dqM, o_dkM), then the sum of the value heads of each key head.

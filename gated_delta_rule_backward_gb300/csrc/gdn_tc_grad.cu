@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     const int row = 32 * (warp & 3) + lane;  // this thread's TMEM lane
     const int hc = (warp >> 2) & 1;          // half: 64 of the K columns, 16 of the 32 tokens
     const int tb = 16 * hc;                  // this thread's tokens [tb, tb + 16)
-    const int c = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int c = A.c_lo + blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int hk = h % A.H_k;
     const long long head = (long long)n * A.H_v + h;
     const long long ch = head * A.n_chunks + c;
@@ -690,7 +690,7 @@ done:
 // dq, dk of each key head: the value heads' parts summed in ascending order.
 __global__ void __launch_bounds__(256) gdn_tc_dqdk_sum_kernel(const ChunkArgs A)
 {
-    const int c = blockIdx.x, hk = blockIdx.y, n = blockIdx.z;
+    const int c = A.c_lo + blockIdx.x, hk = blockIdx.y, n = blockIdx.z;
     const int seg = c / A.cps, loc = c - seg * A.cps;
     const int t0 = seg * A.C + loc * BC;
     const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
@@ -717,14 +717,16 @@ int launch_tc_grad(const ChunkArgs& a, void* stream)
     int e = (int)cudaFuncSetAttribute(gdn_tc_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kGSmemBytes);
     if (e) return e;
-    gdn_tc_grad_kernel<<<dim3(a.n_chunks, a.H_v, a.N), GT, kGSmemBytes, s>>>(a);
+    if (a.c_hi <= a.c_lo) return 0;
+    gdn_tc_grad_kernel<<<dim3(a.c_hi - a.c_lo, a.H_v, a.N), GT, kGSmemBytes, s>>>(a);
     return (int)cudaGetLastError();
 }
 
 int launch_tc_dqdk_sum(const ChunkArgs& a, void* stream)
 {
     cudaStream_t s = (cudaStream_t)stream;
-    gdn_tc_dqdk_sum_kernel<<<dim3(a.n_chunks, a.H_k, a.N), 256, 0, s>>>(a);
+    if (a.c_hi <= a.c_lo) return 0;
+    gdn_tc_dqdk_sum_kernel<<<dim3(a.c_hi - a.c_lo, a.H_k, a.N), 256, 0, s>>>(a);
     return (int)cudaGetLastError();
 }
 

@@ -169,16 +169,20 @@ const char* gdn_last_error(void);
 void gdn_set_timing_events(void* const* events, int n_events);
 
 /* Kernels a forward / backward call with these params launches (0 when the call would
- * fail validation).  Lets callers account for the work they enqueue. */
+ * fail validation).  Lets callers account for the work they enqueue.  On the head-size-128
+ * path this is the count without timing events; a backward call with timing events set
+ * runs its stages one after another and launches 4 kernels. */
 int gdn_forward_launches(const gdn_params_t* p);
 int gdn_backward_launches(const gdn_params_t* p);
 
 /* Timed stages of a forward (backward = 0) or backward (backward = 1) call with these
  * params: gdn_set_timing_events records one event before the first stage and one after
- * each stage.  A stage is one kernel, except on the head-size-128 path, where the chunk
- * preps and the serial chains run pipelined over chunk ranges on two library streams and
- * form one stage (forward: 1 stage; backward: 3 stages -- the pipelined preps and chains,
- * the gradient step, the sum over value heads).  0 when the call would fail validation. */
+ * each stage.  A stage is one kernel, except on the head-size-128 path.  There the
+ * forward's chunk preps and state chain run pipelined over chunk ranges on library
+ * streams and form 1 stage.  The backward normally overlaps all of its kernels across
+ * chunk ranges; with timing events set it runs them one after another instead, in 3
+ * stages (prep and both chains, the gradient step, the sum over value heads), so that
+ * each kernel can be timed.  0 when the call would fail validation. */
 int gdn_timing_stages(const gdn_params_t* p, int backward);
 
 /* Device-side status of the work enqueued so far on the current device.  The

@@ -116,6 +116,32 @@ def test_checkpoint_interval_invariance_head128():
         assert np.array_equal(got["y"], base["y"]) and np.array_equal(got["state_T"], base["state_T"])
 
 
+def test_staged_backward_equals_overlapped():
+    """A backward call with timing events runs its stages one after another as one chunk
+    range; without them it overlaps the gradient work of one range with the chains of the
+    next.  Every chunk is computed by the same kernels either way: bit-identical."""
+    from gated_delta_rule_backward_gb300 import gdn
+    prob = synth.make_problem(1, 700, 2, 6, 128, kda=False, seed=51, C=64, packed=True,
+                              dstate_T=True)
+    dev = H.upload(prob)
+    free, pfree = H.run_gpu(prob, dev=dev)
+    p = gdn.params_for(dev["q"], dev["k"], dev["v"], dev["g"], gy=dev["gy"], C=prob.C,
+                       scale=prob.scale)
+    n_f, n_b = gdn.timing_stages(p)
+    assert (n_f, n_b) == (1, 3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_b + 1)]
+    for e in ev:
+        e.record()
+    gdn.set_timing_events(ev)
+    try:
+        staged, pstaged = H.run_gpu(prob, dev=dev)
+    finally:
+        gdn.set_timing_events(None)
+    assert torch.equal(pfree, pstaged)
+    for k in ("y", "state_T", "ckpt"):
+        assert np.array_equal(free[k], staged[k]), k
+
+
 def test_strided_views_equal_contiguous_copies():
     prob = synth.make_problem(2, 100, 2, 6, 64, kda=False, seed=43, C=9, packed=True,
                               dstate_T=True)
