@@ -147,6 +147,61 @@ __device__ __forceinline__ void load_units(float* dst, int ld, const float* src,
 }
 
 // ---------------------------------------------------------------------------------
+// One m16n8k8 tf32 product C += A B on the tensor pipe (warp-level).  Operand registers
+// hold fp32 bit patterns; the tensor pipe reads their top 19 bits (tf32).
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// [Q; K] K^T for one chunk: 64 x 32 outputs over k < D, rows [Q; K] of QKs (row stride
+// ld), B(k, n) = K[n][k].  Each operand is split x = hi + lo (hi: the 13 low mantissa bits
+// cleared; lo = x - hi, exact) and the product accumulated as hi hi + hi lo + lo hi, which
+// is fp32-accurate (the terms dropped are below 2^-20 of |a b|).  Warp w owns rows
+// 16 (w / 2) .. + 16 and the two 8-column tiles 2 (w % 2), 2 (w % 2) + 1; c[nt] is the
+// m16n8 accumulator fragment (rows g, g + 8; columns 2 tq, 2 tq + 1; g = lane / 4,
+// tq = lane % 4).  Row-stride ld = 4 mod 32 keeps the fragment loads free of bank
+// conflicts.
+template <int D>
+__device__ __forceinline__ void qk_products(float (&c)[2][4], const float* QKs, const float* Ks, int ld, int tid)
+{
+    const int warp = tid >> 5, g = (tid & 31) >> 2, tq = tid & 3;
+    const float* a0 = QKs + (16 * (warp >> 1) + g) * ld + tq;
+    const float* a1 = a0 + 8 * ld;
+    const float* b0 = Ks + (8 * (2 * (warp & 1)) + g) * ld + tq;
+    const float* b1 = b0 + 8 * ld;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
+    auto split = [](float x, uint32_t& hi, uint32_t& lo) {
+        hi = __float_as_uint(x) & 0xffffe000u;
+        lo = __float_as_uint(__fsub_rn(x, __uint_as_float(hi)));
+    };
+#pragma unroll 4
+    for (int k0 = 0; k0 < D; k0 += 8) {
+        uint32_t ah[4], al[4], bh[2][2], bl[2][2];
+        split(a0[k0], ah[0], al[0]);
+        split(a1[k0], ah[1], al[1]);
+        split(a0[k0 + 4], ah[2], al[2]);
+        split(a1[k0 + 4], ah[3], al[3]);
+        split(b0[k0], bh[0][0], bl[0][0]);
+        split(b0[k0 + 4], bh[0][1], bl[0][1]);
+        split(b1[k0], bh[1][0], bl[1][0]);
+        split(b1[k0 + 4], bh[1][1], bl[1][1]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            mma_tf32(c[nt], ah, bh[nt]);
+            mma_tf32(c[nt], ah, bl[nt]);
+            mma_tf32(c[nt], al, bh[nt]);
+        }
+    }
+}
+
 // Chunk-local quantities from Q, K (shared, [Q; K] stacked, zero-padded rows), g, beta.
 // Out: G (inclusive cumsum), gam = exp(G), Dm (lower incl), KKm = K K^T (strict lower),
 // QKm = Q K^T (lower incl), Zs = (I + diag(beta) (Dm (.) KK))^-1, Ts = Zs diag(beta).
@@ -168,23 +223,24 @@ __device__ void chunk_prep(const float* QKs, const float* gs, const float* bs, f
         Gs[tid] = x;
         gam[tid] = expf(x);
     }
-    {  // [QK; KK] = [Q; K] K^T
-        using Map = GemmMap<2 * BC, BC, 4, 2, true>;
-        float acc[4][2];
-        zero_acc(acc);
-        block_gemm<2 * BC, BC, 4, 2, false, true>(acc, QKs, ld, Ks, ld, D, tid);
+    {  // [QK; KK] = [Q; K] K^T, 64 x 32 x D, on the tensor pipe (tf32x3, warp-level MMA)
+        float c[2][4];
+        qk_products<D>(c, QKs, Ks, ld, tid);
+        const int warp = tid >> 5, g = (tid & 31) >> 2, tq = tid & 3;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int m = Map::row(tid, i);
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int n = Map::col(tid, j);
-                if (m < BC)
-                    QKm[m * LDB + n] = (n <= m) ? acc[i][j] : 0.f;
-                else
-                    KKm[(m - BC) * LDB + n] = (n < m - BC) ? acc[i][j] : 0.f;
-            }
-        }
+            for (int half = 0; half < 2; ++half)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int m = 16 * (warp >> 1) + g + 8 * half;
+                    const int n = 8 * (2 * (warp & 1) + nt) + 2 * tq + e;
+                    const float v = c[nt][2 * half + e];
+                    if (m < BC)
+                        QKm[m * LDB + n] = (n <= m) ? v : 0.f;
+                    else
+                        KKm[(m - BC) * LDB + n] = (n < m - BC) ? v : 0.f;
+                }
     }
     __syncthreads();
     for (int idx = tid; idx < BC * BC; idx += CT) {
