@@ -202,6 +202,50 @@ __device__ __forceinline__ void qk_products(float (&c)[2][4], const float* QKs, 
     }
 }
 
+// C (32 x 128) = A (32 x 32) B (32 x 128) on the tensor pipe, three-pass tf32 as in
+// qk_products: A(m, k) = A[m * lda + k], or A[k * lda + m] when A_T; B(k, n) = B[k * ldb + n].
+// Warp w owns rows 16 (w % 2) .. + 16 and columns 32 (w / 2) .. + 32 (four 8-column
+// tiles); c[nt] is the m16n8 accumulator fragment of tile nt (rows g, g + 8; columns
+// 2 tq, 2 tq + 1).  rows_cols() gives a thread's first row and column.
+template <bool A_T>
+__device__ __forceinline__ void mma_32x128x32(float (&c)[4][4], const float* A, int lda, const float* B, int ldb,
+                                              int tid)
+{
+    const int warp = tid >> 5, g = (tid & 31) >> 2, tq = tid & 3;
+    const int m0 = 16 * (warp & 1), n0 = 32 * (warp >> 1);
+    auto split = [](float x, uint32_t& hi, uint32_t& lo) {
+        hi = __float_as_uint(x) & 0xffffe000u;
+        lo = __float_as_uint(__fsub_rn(x, __uint_as_float(hi)));
+    };
+    auto a_at = [&](int m, int k) { return A_T ? A[k * lda + m] : A[m * lda + k]; };
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
+#pragma unroll
+    for (int k0 = 0; k0 < 32; k0 += 8) {
+        uint32_t ah[4], al[4];
+        split(a_at(m0 + g, k0 + tq), ah[0], al[0]);
+        split(a_at(m0 + g + 8, k0 + tq), ah[1], al[1]);
+        split(a_at(m0 + g, k0 + tq + 4), ah[2], al[2]);
+        split(a_at(m0 + g + 8, k0 + tq + 4), ah[3], al[3]);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            uint32_t bh[2], bl[2];
+            split(B[(k0 + tq) * ldb + n0 + 8 * nt + g], bh[0], bl[0]);
+            split(B[(k0 + tq + 4) * ldb + n0 + 8 * nt + g], bh[1], bl[1]);
+            mma_tf32(c[nt], ah, bh);
+            mma_tf32(c[nt], ah, bl);
+            mma_tf32(c[nt], al, bh);
+        }
+    }
+}
+__device__ __forceinline__ void mma_32x128_origin(int tid, int& m, int& n)
+{
+    m = 16 * ((tid >> 5) & 1) + ((tid & 31) >> 2);
+    n = 32 * (tid >> 6) + 2 * (tid & 3);
+}
+
 // Chunk-local quantities from Q, K (shared, [Q; K] stacked, zero-padded rows), g, beta.
 // Out: G (inclusive cumsum), gam = exp(G), Dm (lower incl), KKm = K K^T (strict lower),
 // QKm = Q K^T (lower incl), Zs = (I + diag(beta) (Dm (.) KK))^-1, Ts = Zs diag(beta).
@@ -344,8 +388,6 @@ __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, long long ck,
                                  const float* QKm, const float* Dm, int tid)
 {
     constexpr int ld = Ld<D>::v;
-    constexpr int TM = D / 32;
-    using Map = GemmMap<BC, D, TM, 4, false>;
     const float* Ks = QKs + BC * ld;
     float* w1 = A.ws + A.o_W1 + ch * kTcWElems;
     float* q1 = A.ws + A.o_Q1 + ck * kTcQElems;
@@ -360,21 +402,29 @@ __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, long long ck,
         *reinterpret_cast<uint4*>(hi_base + 4 * unit) = hi;
         *reinterpret_cast<uint4*>(hi_base + half + 4 * unit) = lo;
     };
-    float acc[TM][4];
-    zero_acc(acc);
-    block_gemm<BC, D, TM, 4, false, false>(acc, Ts, LDB, Vs, ld, BC, tid);  // U = T V
+    static_assert(D == 128, "tensor-core operands are built at head size 128");
+    int fm, fn;
+    mma_32x128_origin(tid, fm, fn);
+    float c[4][4];
+    mma_32x128x32<false>(c, Ts, LDB, Vs, ld, tid);  // U = T V
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < TM; ++i)
-        *reinterpret_cast<float4*>(Vs + Map::row(tid, i) * ld + Map::col(tid, 0)) =
-            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-    zero_acc(acc);
-    block_gemm<BC, D, TM, 4, false, false>(acc, TG, LDB, Ks, ld, BC, tid);  // W
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-    for (int i = 0; i < TM; ++i) {  // rows t of W, 4 consecutive k per thread
-        const int t = Map::row(tid, i), c0 = Map::col(tid, 0);
-        put(w1, kTcWElems / 2, tc::kmaj_rg(t, c0, D) >> 2, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
-    }
+        for (int hf = 0; hf < 2; ++hf)
+            *reinterpret_cast<float2*>(Vs + (fm + 8 * hf) * ld + fn + 8 * nt) = make_float2(c[nt][2 * hf], c[nt][2 * hf + 1]);
+    mma_32x128x32<false>(c, TG, LDB, Ks, ld, tid);  // W = T diag(gamma) K
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {  // rows t of W, 2 consecutive k per thread
+            const int off = tc::kmaj_rg(fm + 8 * hf, fn + 8 * nt, D);
+            uint2 hi, lo;
+            tc::split_tf32(c[nt][2 * hf], hi.x, lo.x);
+            tc::split_tf32(c[nt][2 * hf + 1], hi.y, lo.y);
+            *reinterpret_cast<uint2*>(w1 + off) = hi;
+            *reinterpret_cast<uint2*>(w1 + kTcWElems / 2 + off) = lo;
+        }
     if (first) {  // Q, unit u = (row group * 32 + k-chunk) * 8 + row % 8
         for (int u = tid; u < BC * (D / 4); u += CT) {
             const int t = ((u >> 8) << 3) + (u & 7), kc = (u >> 3) & 31;
@@ -412,8 +462,6 @@ __device__ void prep_tc_dstate_operands(const ChunkArgs& A, int n, int h, const 
                                         const float* Dm, const float* gam, int tid)
 {
     constexpr int ld = Ld<D>::v;
-    constexpr int TM = D / 32;
-    using Map = GemmMap<BC, D, TM, 4, false>;
     const float* Ks = QKs + BC * ld;
     float* blk = A.ws + A.o_DS + ch * kTcDsElems;
     float* kblk = A.ws + A.o_DK + ck * kTcDkElems;
@@ -438,19 +486,21 @@ __device__ void prep_tc_dstate_operands(const ChunkArgs& A, int n, int h, const 
     }
     __syncthreads();
     {  // E^T = scale QD^T dY (rows t), stored as E (rows j), fp32
-        float acc[TM][4];
-        zero_acc(acc);
-        block_gemm<BC, D, TM, 4, true, false>(acc, Zs, LDB, Vs, ld, BC, tid);
+        static_assert(D == 128, "tensor-core operands are built at head size 128");
+        float c[4][4];
+        mma_32x128x32<true>(c, Zs, LDB, Vs, ld, tid);
+        int fm, fn;
+        mma_32x128_origin(tid, fm, fn);
         float* e = blk + kDsE;
 #pragma unroll
-        for (int i = 0; i < TM; ++i) {
-            const int t = Map::row(tid, i);
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int j = Map::col(tid, jj);
-                e[4 * ((t >> 2) * D + j) + (t & 3)] = __fmul_rn(A.scale, acc[i][jj]);
-            }
-        }
+            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const int t = fm + 8 * hf, j = fn + 8 * nt + x;
+                    e[4 * ((t >> 2) * D + j) + (t & 3)] = __fmul_rn(A.scale, c[nt][2 * hf + x]);
+                }
     }
     for (int idx = tid; idx < (BC / 4) * D; idx += CT) {  // scale gamma dY^T, unit b * 128 + j
         const int j = idx % D, b = idx / D;
