@@ -321,9 +321,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     tc::fence_before();
     __syncthreads();
     if (s_err) goto done;
-    // (3) D2 = M^T [s gamma dY ; -gamma dX]^T.  Meanwhile dM replaces M in R2 (bulk copy), and
-    //     q_t, k_t (this thread's tokens) come in for the dgamma and dr sums.
-    float qv[16], kv[16];
+    // (3) D2 = M^T [s gamma dY ; -gamma dX]^T.  Meanwhile dM replaces M in R2 (bulk copy).
     if (warp == 8) {
         if (lane == 0) {
             tc::fence_async_smem();
@@ -341,20 +339,12 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                tc::make_desc(tc::smem_addr(sm + kR1 + kT64), kLbo64, 128), kLbo64, 0, TD / 8,
                tc::idesc_tf32(64), false);
         tc::commit(bar_mma);
-    } else if (compute) {
-        const float* qp = A.q + (long long)n * A.qs0 + (long long)t0 * A.qs1 + (long long)hk * A.qs2 + row;
-        const float* kp = A.k + (long long)n * A.ks0 + (long long)t0 * A.ks1 + (long long)hk * A.ks2 + row;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            qv[e] = (tb + e < nb) ? __ldg(qp + (long long)(tb + e) * A.qs1) : 0.f;
-            kv[e] = (tb + e < nb) ? __ldg(kp + (long long)(tb + e) * A.ks1) : 0.f;
-        }
     }
     ok = tc::mbar_wait(bar_mma, ph);
     ph ^= 1;
     tc::fence_after();
-    // (4) gamma dgamma partials from D2; A = dM^T (rows i) and <dM, M> (M^T still in TMEM).
-    //     R1's B tile is dead: dDelta and the dY rows come into it.
+    // (4) A = dM^T (rows i) and <dM, M> (M^T still in TMEM).  R1's B tile is dead: dDelta and
+    //     the dY rows come into it.
     if (warp == 8) {
         const bool dy_bulk = A.vec_gy != 0;
         if (lane == 0) {
@@ -372,15 +362,6 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     }
     if (compute) {
         if (!tc::mbar_wait(bar_dm, 0)) s_err = 1;
-        float dq[16], dk[16];
-        tc::ld16(tc::taddr(tmem, warp, kC2 + tb), dq);
-        tc::ld16(tc::taddr(tmem, warp, kC2 + BC + tb), dk);
-        tc::wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const float g = warp_sum(__fmaf_rn(kv[e], dk[e], __fmul_rn(qv[e], dq[e])));
-            if (lane == 0) red[(warp & 3) * 96 + tb + e] = g;
-        }
         {
             const float* dmc = sM + (row >> 2) * kLdU + (row & 3);  // dM[j][row] at dmc[4 j]
             float dot = 0.f;
@@ -410,31 +391,58 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     tc::fence_before();
     __syncthreads();
     if (s_err) goto done;
-    // (5) D3 = dM^T Delta^T, then [Q^T | K^T] into the staging region.
+    // (5) [Q^T | K^T] into the staging region (dM is in TMEM now), then D3 = dM^T Delta^T.
     if (issuer) {
         tc::fence_after();
-        mma3_t(tmem + kC3, aHi, aLo, tc::make_desc(tc::smem_addr(sm + kR0), kLbo64, 128),
-               tc::make_desc(tc::smem_addr(sm + kR0 + kT64), kLbo64, 128), kLbo64, 0, TD / 8,
-               tc::idesc_tf32(32), false);
-        tc::commit(bar_mma);
         tc::fence_async_smem();
         s_armed |= 1 << 1;
         tc::mbar_expect_tx(bar_qkt, kBytesQKT);
         tc::bulk_g2s(sm + kR2, A.ws + A.o_DK + ck * kTcDkElems + kDkQKT, kBytesQKT, bar_qkt);
+        mma3_t(tmem + kC3, aHi, aLo, tc::make_desc(tc::smem_addr(sm + kR0), kLbo64, 128),
+               tc::make_desc(tc::smem_addr(sm + kR0 + kT64), kLbo64, 128), kLbo64, 0, TD / 8,
+               tc::idesc_tf32(32), false);
+        tc::commit(bar_mma);
     }
     ok = tc::mbar_wait(bar_mma, ph);
     ph ^= 1;
     tc::fence_after();
-    // (6) dr partials from D3 (kept for dk); A = [dY ; dDelta ; 0] (rows t)
+    // (6) the gamma dgamma partials (from D2, which holds M^T [s gamma dY ; -gamma dX]^T until
+    //     step (9)) and the dr partials (from D3, kept for dk), with q_t, k_t of this
+    //     thread's tokens read from the [Q^T | K^T] tile (hi + lo is exact); then
+    //     A = [dY ; dDelta ; 0] (rows t)
     float d3[16];
     if (compute) {
-        if (!tc::mbar_wait(bar_dd, 0)) s_err = 1;
-        tc::ld16(tc::taddr(tmem, warp, kC3 + tb), d3);
-        tc::wait_ld();
+        if (!tc::mbar_wait(bar_dd, 0) || !tc::mbar_wait(bar_qkt, 0)) s_err = 1;
+        {
+            float dq[16], dk[16];
+            tc::ld16(tc::taddr(tmem, warp, kC2 + tb), dq);
+            tc::ld16(tc::taddr(tmem, warp, kC2 + BC + tb), dk);
+            tc::ld16(tc::taddr(tmem, warp, kC3 + tb), d3);
+            tc::wait_ld();
+            const float* qkt = sm + kR2 + 4 * row;  // element (row, t) at (t / 4) 512 + t % 4
+            constexpr int kLo = 2 * BC * TD;        // lo half of the tile
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const float g = warp_sum(__fmul_rn(kv[e], d3[e]));
-            if (lane == 0) red[(warp & 3) * 96 + BC + tb + e] = g;
+            for (int b = 0; b < 4; ++b) {
+                const int u = (tb >> 2) + b;
+                const float4 qh = *reinterpret_cast<const float4*>(qkt + u * 4 * TD);
+                const float4 ql = *reinterpret_cast<const float4*>(qkt + kLo + u * 4 * TD);
+                const float4 kh = *reinterpret_cast<const float4*>(qkt + (BC / 4 + u) * 4 * TD);
+                const float4 kl = *reinterpret_cast<const float4*>(qkt + kLo + (BC / 4 + u) * 4 * TD);
+                const float qv[4] = {__fadd_rn(qh.x, ql.x), __fadd_rn(qh.y, ql.y), __fadd_rn(qh.z, ql.z),
+                                     __fadd_rn(qh.w, ql.w)};
+                const float kv[4] = {__fadd_rn(kh.x, kl.x), __fadd_rn(kh.y, kl.y), __fadd_rn(kh.z, kl.z),
+                                     __fadd_rn(kh.w, kl.w)};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int x = 4 * b + e;
+                    const float g1 = warp_sum(__fmaf_rn(kv[e], dk[x], __fmul_rn(qv[e], dq[x])));
+                    const float g2 = warp_sum(__fmul_rn(kv[e], d3[x]));
+                    if (lane == 0) {
+                        red[(warp & 3) * 96 + tb + x] = g1;
+                        red[(warp & 3) * 96 + BC + tb + x] = g2;
+                    }
+                }
+            }
         }
         const int quarter = warp & 3;
         const float* gyr = A.gy + (long long)n * A.gys0 + (long long)(t0 + lane) * A.gys1 + (long long)h * A.gys2 + 64 * hc;
