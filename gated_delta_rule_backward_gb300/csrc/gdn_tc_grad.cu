@@ -545,10 +545,11 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             const int t = idx >> 5, tau = idx & 31;
             W1[t * LDF + tau] = __fmul_rn(dTs[t * LDF + tau], bs[tau]);
         }
-        if (tid < BC) {
-            float s = 0.f;
-            for (int t = tid; t < BC; ++t) s = __fmaf_rn(Zs[t * LDF + tid], dTs[t * LDF + tid], s);
-            dbs[tid] = s;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // warp w: columns 4 w .. 4 w + 3, lanes over t
+            const int tau = 4 * warp + q;
+            const float s = warp_sum(__fmul_rn(Zs[lane * LDF + tau], dTs[lane * LDF + tau]));
+            if (lane == 0) dbs[tau] = s;
         }
         tc::bar_sync_first(256);
         {  // P1 = dZ Z^T
@@ -590,18 +591,18 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             dTs[t * LDF + tau] = __fmul_rn(dD, dm);
         }
         tc::bar_sync_first(256);
-        if (tid < BC) {
-            const int t = tid;
-            float rs = 0.f, cs = 0.f, bb = 0.f;
-            for (int tau = 0; tau < BC; ++tau) {
-                rs = __fadd_rn(rs, dTs[t * LDF + tau]);
-                cs = __fadd_rn(cs, dTs[tau * LDF + t]);
-                bb = __fmaf_rn(W1[t * LDF + tau], __fmul_rn(Dm[t * BC + tau], KKm[t * BC + tau]), bb);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // warp w: rows t = 4 w .. 4 w + 3, lanes over tau
+            const int t = 4 * warp + q, tau = lane;
+            const float rs = warp_sum(dTs[t * LDF + tau]);
+            const float cs = warp_sum(dTs[tau * LDF + t]);
+            const float bb = warp_sum(__fmul_rn(W1[t * LDF + tau], __fmul_rn(Dm[t * BC + tau], KKm[t * BC + tau])));
+            if (lane == 0) {
+                float g = gdg[t];
+                if (t == BC - 1) g = __fmaf_rn(sGam[t], dot, g);
+                dG[t] = __fadd_rn(__fadd_rn(g, rs), -cs);
+                dbs[t] = __fadd_rn(dbs[t], bb);
             }
-            float g = gdg[t];
-            if (t == BC - 1) g = __fmaf_rn(sGam[t], dot, g);
-            dG[t] = __fadd_rn(__fadd_rn(g, rs), -cs);
-            dbs[t] = __fadd_rn(dbs[t], bb);
         }
         tc::bar_sync_first(256);
         if (warp == 0) {  // dg = reverse cumsum of dG; dbeta
