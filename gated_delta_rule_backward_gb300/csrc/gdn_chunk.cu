@@ -147,17 +147,6 @@ __device__ __forceinline__ void load_units(float* dst, int ld, const float* src,
 }
 
 // ---------------------------------------------------------------------------------
-// One m16n8k8 tf32 product C += A B on the tensor pipe (warp-level).  Operand registers
-// hold fp32 bit patterns; the tensor pipe reads their top 19 bits (tf32).
-__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
 // [Q; K] K^T for one chunk: 64 x 32 outputs over k < D, rows [Q; K] of QKs (row stride
 // ld), B(k, n) = K[n][k].  Each operand is split x = hi + lo (hi: the 13 low mantissa bits
 // cleared; lo = x - hi, exact) and the product accumulated as hi hi + hi lo + lo hi, which
@@ -195,9 +184,9 @@ __device__ __forceinline__ void qk_products(float (&c)[2][4], const float* QKs, 
         split(b1[k0 + 4], bh[1][1], bl[1][1]);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            mma_tf32(c[nt], ah, bh[nt]);
-            mma_tf32(c[nt], ah, bl[nt]);
-            mma_tf32(c[nt], al, bh[nt]);
+            tc::mma_warp_tf32(c[nt], ah, bh[nt]);
+            tc::mma_warp_tf32(c[nt], ah, bl[nt]);
+            tc::mma_warp_tf32(c[nt], al, bh[nt]);
         }
     }
 }
@@ -234,9 +223,9 @@ __device__ __forceinline__ void mma_32x128x32(float (&c)[4][4], const float* A, 
             uint32_t bh[2], bl[2];
             split(B[(k0 + tq) * ldb + n0 + 8 * nt + g], bh[0], bl[0]);
             split(B[(k0 + tq + 4) * ldb + n0 + 8 * nt + g], bh[1], bl[1]);
-            mma_tf32(c[nt], ah, bh);
-            mma_tf32(c[nt], ah, bl);
-            mma_tf32(c[nt], al, bh);
+            tc::mma_warp_tf32(c[nt], ah, bh);
+            tc::mma_warp_tf32(c[nt], ah, bl);
+            tc::mma_warp_tf32(c[nt], al, bh);
         }
     }
 }

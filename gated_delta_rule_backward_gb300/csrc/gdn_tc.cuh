@@ -262,6 +262,21 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
 
 // Bulk copy global -> shared (TMA engine, no tensor map): both addresses 16-byte aligned,
 // bytes a multiple of 16.  Completion is counted on `bar` in bytes.
+// One m16n8k8 tf32 product C += A B issued by a whole warp (mma.sync; for the small
+// products of the CUDA-core kernels, where a TMEM accumulator and an issuing thread do not
+// pay).  A: rows g, g + 8 and columns tq, tq + 4 of the 16 x 8 tile (g = lane / 4,
+// tq = lane % 4); B: rows tq, tq + 4 of column g of the 8 x 8 tile; C: rows g, g + 8 and
+// columns 2 tq, 2 tq + 1.  Operand registers hold fp32 bit patterns, of which the tensor
+// pipe reads the top 19 bits (tf32).
+__device__ __forceinline__ void mma_warp_tf32(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // An L2 prefetch hint for one line through the load/store path.  A CTA whose first global
 // access is a bulk copy ran its memory-bound steps measurably slower on GB300 than one that
 // touched global memory through the load/store path first (cause unknown); the kernels issue
