@@ -140,6 +140,8 @@ def _args():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="throughput of every sweep point (d x T x N x gate), one JSON line each")
     return ap.parse_args()
 
 
@@ -547,8 +549,79 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """Throughput of every sweep point: d in {32, 64, 128} x T in {512, 4096, 16384} x
+    N in {1, 4, 8} (H_v = 48 over H_k = 16) x {scalar, KDA}, C = ceil(sqrt(T)).  Inputs follow
+    the recipe's distributions but are drawn on the device (seeded torch generators): the
+    points reach 6.3 M head-tokens, too large to draw in float64 on the host.  Each point:
+    one warm-up step, then timed steps (about 0.5 s of them, at most --steps) with the L2
+    flushed between them; one JSON line each."""
+    import torch
+    from gated_delta_rule_backward_gb300 import gdn, synth
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+    for pt in synth.sweep_points():
+        N, T, H_k, H_v, d, kda = pt["N"], pt["T"], pt["H_k"], pt["H_v"], pt["d"], pt["kda"]
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(pt["seed"])
+        rnd = lambda *shape: torch.randn(*shape, generator=gen, device=dev)
+        qkv = rnd(N, T, (2 * H_k + H_v) * d)
+        q = qkv[:, :, : H_k * d].view(N, T, H_k, d)
+        k = qkv[:, :, H_k * d: 2 * H_k * d].view(N, T, H_k, d)
+        v = qkv[:, :, 2 * H_k * d:].view(N, T, H_v, d)
+        q /= q.norm(dim=-1, keepdim=True)
+        k /= k.norm(dim=-1, keepdim=True)
+        g = -torch.nn.functional.softplus(rnd(N, T, H_v, d) if kda else rnd(N, T, H_v))
+        beta = torch.sigmoid(rnd(N, T, H_v))
+        state0 = 0.1 * rnd(N, H_v, d, d)
+        gy = rnd(N, T, H_v, d)
+        p = gdn.params_for(q, k, v, g, gy=gy, C=None, scale=1.0 / math.sqrt(d))
+        y = torch.empty((N, T, H_v, d), device=dev)
+        sT = torch.empty((N, H_v, d, d), device=dev)
+        ck = torch.empty((N, H_v, gdn.num_checkpoints(p), d, d), device=dev)
+        packed = torch.empty(gdn.packed_grad_elems(p), device=dev)
+        ws = torch.empty(max(gdn.backward_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
+        fws_n = gdn.forward_workspace_bytes(p)
+        fws = torch.empty(fws_n, dtype=torch.uint8, device=dev) if fws_n else None
+
+        def step():
+            gdn.gdn_forward(p, q, k, v, g, beta, state0, y, sT, ck, fws, stream)
+            gdn.gdn_backward(p, q, k, v, g, beta, ck, gy, None, packed, ws, stream)
+
+        step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step()
+        torch.cuda.synchronize()
+        est = time.perf_counter() - t0
+        steps = max(1, min(args.steps, int(0.5 / max(est, 1e-6))))
+        mk = lambda: torch.cuda.Event(enable_timing=True)
+        evs = [(mk(), mk()) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+        head_tokens = N * H_v * T
+        tflops = (FWD_FLOPS(d) + BWD_FLOPS(d)) * head_tokens / (ms * 1e-3) / 1e12
+        print(json.dumps({"point": {"d": d, "T": T, "N": N, "H_k": H_k, "H_v": H_v,
+                                    "gate": "kda" if kda else "scalar", "C": gdn.checkpoint_interval(p)},
+                          "metric": METRIC, "value": head_tokens / (ms * 1e-3), "unit": UNIT,
+                          "ms_per_step": ms, "steps": steps, "dtype": "f32", "data": "synthetic",
+                          "roofline_path": {"achieved": tflops, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                                            "frac": tflops / FP32_PEAK_TFLOPS}}), flush=True)
+        del qkv, q, k, v, g, beta, state0, gy, y, sT, ck, packed, ws, fws
+        torch.cuda.empty_cache()
+
+
 def main():
     args = _args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
