@@ -52,9 +52,10 @@ constexpr int kSB23 = kSB1 + kTcWElems + kTcQElems;  // [sQD; rK^T] hi, lo  2 x 
 constexpr int kSU = kSB23 + kTcB23Elems;           // U^T, operand layout (R = 128), fp32
 constexpr int kSDel = kSU + BC * TD;               // Delta^T hi, lo   2 x 128 x 32
 constexpr int kSGam = kSDel + 2 * BC * TD;         // gamma (32)
-constexpr int kSFloats = kSGam + BC;
 constexpr int kStageLd = TD + 4;                   // staging rows for coalesced global writes
-constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 64;   // + barriers
+constexpr int kSY = kSGam + BC;                    // y of the chunk, rows t (forward)
+constexpr int kSFloats = kSY + BC * kStageLd;
+constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 128;  // + 11 barriers
 
 constexpr uint32_t kB1Bytes = sizeof(float) * (kTcWElems + kTcQElems);
 constexpr int kHalfW = kTcWElems / 2;  // 32 x 128 floats
@@ -88,10 +89,11 @@ __device__ __forceinline__ void load_b23(const ChunkArgs& A, long long ch, float
 template <bool FWD>
 __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int bx, int by)
 {
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSFloats);  // b1, b23, mma
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSFloats);  // b1, b23, mma, a[8]
     uint64_t* bar_b1 = bars;
     uint64_t* bar_b23 = bars + 1;
     uint64_t* bar_mma = bars + 2;
+    uint64_t* bar_a = bars + 3;  // bar_a[g]: columns [32 g, 32 g + 32) of both halves of M are in TMEM
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
@@ -124,6 +126,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         tc::mbar_init(bar_b1, 1);
         tc::mbar_init(bar_b23, 1);
         tc::mbar_init(bar_mma, 1);
+        for (int g = 0; g < 2; ++g) tc::mbar_init(bar_a + g, 8);  // one arrival per compute warp
         tc::mbar_fence_init();
         s_err = 0;
     }
@@ -164,23 +167,21 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         for (int q = 0; q < 16; ++q)
             d4[(16 * hc + q) * TD + j] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
     };
-    // y^T of the previous chunk (column-half 1 threads), stored while the next chunk's D1 runs
-    float y[32];
+    // y of a chunk is assembled in shared memory (rows t) by the column-half 1 threads: the Q
+    // part in (3), the QD Delta part added in (5); it goes to global memory while the next
+    // chunk's D1 runs
     int y_t0 = 0, y_nb = 0;
-    float* stage = sm + kSDel;   // idle while D1 runs: 32 rows of kStageLd floats
+    float* stage = sm + kSDel;   // idle while D1 runs: 32 rows of kStageLd floats (checkpoints)
+    float* sY = sm + kSY;
     const int ctid = tid;        // 0..255 for the compute warps
-    auto store_y = [&]() {       // through `stage`: the global writes are whole 512-byte rows
-        if (hc == 1) {
-#pragma unroll
-            for (int t = 0; t < BC; ++t) stage[t * kStageLd + j] = y[t];
-        }
+    auto store_y = [&]() {       // the global writes are whole 512-byte rows
         tc::bar_sync_first(256);
         float* yp = A.y + (((long long)n * A.T + y_t0) * A.H_v + h) * TD;
         const long long ys = (long long)A.H_v * TD;
         for (int idx = ctid; idx < y_nb * (TD / 4); idx += 256) {
             const int t = idx / (TD / 4), q = idx - t * (TD / 4);
             *reinterpret_cast<float4*>(yp + t * ys + 4 * q) =
-                *reinterpret_cast<const float4*>(stage + t * kStageLd + 4 * q);
+                *reinterpret_cast<const float4*>(sY + t * kStageLd + 4 * q);
         }
         tc::bar_sync_first(256);
     };
@@ -210,10 +211,20 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         tc::st8(tc::taddr(tmem, warp, kColMhi + 64 * hc + 8 * q), hi);
         tc::st8(tc::taddr(tmem, warp, kColMlo + 64 * hc + 8 * q), lo);
     };
+    // Columns [32 g, 32 g + 32) of this thread's half of the next D1's A operand are written:
+    // the issuer may use k-slices 4 g .. 4 g + 3 and 8 + 4 g .. 8 + 4 g + 3 (one arrival per
+    // compute warp, after the warp's stores are complete).
+    auto release_group = [&](int g) {
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bar_a + g);
+    };
     if (compute) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) split_store(q);
-        tc::wait_st();
+        release_group(0);
+        release_group(1);
     }
 
     const float* sU = sm + kSU;
@@ -228,12 +239,11 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         const int t0 = seg * A.C + loc * BC;
         const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
         const long long ch = head * A.n_chunks + c;
-        // (1) M (tf32 hi/lo, the A operand of D1) is in TMEM
-        tc::fence_before();
-        __syncthreads();
-        // (2) D1 = M [W; Q]^T on the tensor cores; meanwhile the pending global stores
+        // (1) M (tf32 hi/lo, the A operand of D1) goes into TMEM slice by slice (release_slice)
+        // (2) D1 = M [W; Q]^T on the tensor cores, each k-slice issued as soon as its columns of
+        //     M are in TMEM; meanwhile the pending global stores
+        const uint32_t ph_a = (uint32_t)(c - c_begin) & 1u;
         if (issuer) {
-            tc::fence_after();
             if (!tc::mbar_wait(bar_b1, ph_b1)) s_err = 1;
             ph_b1 ^= 1;
             b1_pending = false;
@@ -241,13 +251,24 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 const uint64_t bhi = tc::tile_desc_rg(sm + kSB1, TD);
                 const uint64_t blo = tc::tile_desc_rg(sm + kSB1 + 2 * kHalfW, TD);
 #pragma unroll
-                for (int s = 0; s < TD / 8; ++s) {
-                    const uint32_t ahi = tmem + kColMhi + 8 * s, alo = tmem + kColMlo + 8 * s;
-                    tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice_rg(bhi, s), id64, s > 0);
-                    tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice_rg(blo, s), id64, 1);
-                    tc::mma_ts(tmem + kColD1, alo, tc::desc_kslice_rg(bhi, s), id64, 1);
+                for (int q = 0; q < 8; ++q) {
+                    if ((q & 3) == 0) {
+                        if (!tc::mbar_wait(bar_a + (q >> 2), ph_a)) {
+                            s_err = 1;
+                            break;
+                        }
+                        tc::fence_after();
+                    }
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int s = q + 8 * h2;
+                        const uint32_t ahi = tmem + kColMhi + 8 * s, alo = tmem + kColMlo + 8 * s;
+                        tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice_rg(bhi, s), id64, s > 0);
+                        tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice_rg(blo, s), id64, 1);
+                        tc::mma_ts(tmem + kColD1, alo, tc::desc_kslice_rg(bhi, s), id64, 1);
+                    }
                 }
-                tc::commit(bar_mma);
+                if (!s_err) tc::commit(bar_mma);
             }
         } else if (compute) {
             if (FWD && y_nb > 0) store_y();
@@ -285,9 +306,9 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                     *reinterpret_cast<uint4*>(sDel + 4 * (b * TD + j)) = hi;
                     *reinterpret_cast<uint4*>(sDel + BC * TD + 4 * (b * TD + j)) = lo;
                 }
-            } else if (FWD) {
+            } else if (FWD) {  // the Q part of y
 #pragma unroll
-                for (int t = 0; t < BC; ++t) y[t] = __fmul_rn(__fmul_rn(A.scale, sGam[t]), x[t]);
+                for (int t = 0; t < BC; ++t) sY[t * kStageLd + j] = __fmul_rn(__fmul_rn(A.scale, sGam[t]), x[t]);
             }
         }
         ph_b23 ^= 1;
@@ -329,17 +350,18 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             }
         } else if (compute) {
             if (FWD) {
-                if (hc == 1) {
+                if (hc == 1) {  // y += D23[:, 0:32]
                     float x[32];
                     tc::ld32(tc::taddr(tmem, warp, kColD23), x);
                     tc::wait_ld();
 #pragma unroll
-                    for (int t = 0; t < BC; ++t) y[t] = __fadd_rn(y[t], x[t]);
+                    for (int t = 0; t < BC; ++t) sY[t * kStageLd + j] = __fadd_rn(sY[t * kStageLd + j], x[t]);
                 }
                 y_t0 = t0;
                 y_nb = nb;
             }
-            // M <- gamma_last M + D23[:, 32:160], split at once into the next D1's A operand
+            // M <- gamma_last M + D23[:, 32:160], split at once into the next D1's A operand and
+            // released to the issuer slice by slice
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 float x[8];
@@ -348,8 +370,8 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
 #pragma unroll
                 for (int e = 0; e < 8; ++e) m[8 * q + e] = __fmaf_rn(gl, m[8 * q + e], x[e]);
                 split_store(q);
+                if ((q & 3) == 3) release_group(q >> 2);
             }
-            tc::wait_st();
         }
     }
 
