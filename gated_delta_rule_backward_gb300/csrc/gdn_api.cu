@@ -4,6 +4,7 @@
 // any part of the recurrence: every step runs in the kernels of gdn_fwd.cu / gdn_bwd.cu.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
@@ -257,10 +258,13 @@ void fill_chunk_common(gdn::ChunkArgs& c, const gdn_params_t* p, const Plan& pl)
 int tc_ranges(const Plan& pl, bool backward)
 {
     const int R = gdn::pipeline_ranges((int)pl.n_ck, backward);
-    const int64_t seg_per = (pl.n_ck + R - 1) / R;
     int n = 0;
-    for (int r = 0; r < R; ++r)
-        if (r * seg_per * pl.cps < pl.n_chunks) ++n;
+    for (int r = 0; r < R; ++r) {
+        int s_lo = 0, s_hi = 0;
+        gdn::range_segments((int)pl.n_ck, R, backward, r, &s_lo, &s_hi);
+        if (std::min<int64_t>(pl.n_chunks, (int64_t)s_hi * pl.cps) > std::min<int64_t>(pl.n_chunks, (int64_t)s_lo * pl.cps))
+            ++n;
+    }
     return n;
 }
 
@@ -337,6 +341,19 @@ int gdn::pipeline_ranges(int n_ck, bool backward)
 {
     const int m = backward ? 2 : gdn::kMaxRanges;
     return n_ck < m ? (n_ck < 1 ? 1 : n_ck) : m;
+}
+
+void gdn::range_segments(int n_ck, int R, bool backward, int r, int* s_lo, int* s_hi)
+{
+    if (!backward && R == 4 && n_ck >= 40) {  // every range keeps at least 4 segments
+        static const int kCum[5] = {0, 10, 30, 60, 100};  // percent of the segments
+        *s_lo = (int)((long long)n_ck * kCum[r] / 100);
+        *s_hi = (int)((long long)n_ck * kCum[r + 1] / 100);
+        return;
+    }
+    const int per = (n_ck + R - 1) / R;
+    *s_lo = std::min(n_ck, r * per);
+    *s_hi = std::min(n_ck, (r + 1) * per);
 }
 
 void gdn::EventTap::mark(void* stream)

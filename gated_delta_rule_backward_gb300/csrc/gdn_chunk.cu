@@ -1386,19 +1386,20 @@ static int set_smem(K kern, size_t bytes)
         tap.mark(s);                                                                   \
     } while (0)
 
-// Chunk range r of R: whole checkpoint segments, [c_lo, c_hi).
-static void range_of(const ChunkArgs& a, int R, int r, ChunkArgs& out)
+// Chunk range r of R: whole checkpoint segments (range_segments), [c_lo, c_hi).
+static void range_of(const ChunkArgs& a, int R, bool backward, int r, ChunkArgs& out)
 {
-    const int seg_per = (a.n_ck + R - 1) / R;
+    int s_lo = 0, s_hi = 0;
+    range_segments(a.n_ck, R, backward, r, &s_lo, &s_hi);
     out = a;
-    out.c_lo = min(a.n_chunks, r * seg_per * a.cps);
-    out.c_hi = min(a.n_chunks, (r + 1) * seg_per * a.cps);
+    out.c_lo = min(a.n_chunks, s_lo * a.cps);
+    out.c_hi = min(a.n_chunks, s_hi * a.cps);
 }
 
-static int launch_prep_range(const ChunkArgs& a, int R, int r, cudaStream_t st)
+static int launch_prep_range(const ChunkArgs& a, int R, bool backward, int r, cudaStream_t st)
 {
     ChunkArgs ar;
-    range_of(a, R, r, ar);
+    range_of(a, R, backward, r, ar);
     int err = set_smem(gdn_chunk_prep_kernel<128>, prep_smem<128>());
     if (err) return err;
     gdn_chunk_prep_kernel<128><<<dim3((ar.c_hi - ar.c_lo) * a.H_v, a.N), CT, prep_smem<128>(), st>>>(ar);
@@ -1441,11 +1442,11 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
     for (int i = 0; i < R; ++i) {
         const int r = backward ? R - 1 - i : i;
         ChunkArgs ar;
-        range_of(a, R, r, ar);
+        range_of(a, R, backward, r, ar);
         if (ar.c_hi > ar.c_lo) order[nr++] = r;
     }
     auto prep = [&](int r) -> int {
-        int err = launch_prep_range(a, R, r, lo);
+        int err = launch_prep_range(a, R, backward, r, lo);
         if (!err) err = (int)cudaEventRecord((cudaEvent_t)P->prep_done[r], lo);
         return err;
     };
@@ -1453,7 +1454,7 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
     for (int i = 0; i < nr && !e; ++i) {
         const int r = order[i];
         ChunkArgs ar;
-        range_of(a, R, r, ar);
+        range_of(a, R, backward, r, ar);
         e = (int)cudaStreamWaitEvent(hi, (cudaEvent_t)P->prep_done[r], 0);
         if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->chain_go[r], hi);
         if (!e) {

@@ -147,6 +147,11 @@ void release_pipeline();
 // Chunk ranges of the pipelined path: segment-aligned, at most kMaxRanges.  (A backward
 // call with timing events runs its stages one after another instead, as one range.)
 int pipeline_ranges(int n_ck, bool backward);
+// Checkpoint segments [s_lo, s_hi) of range r of R.  The forward's 4 ranges grow (10, 20,
+// 30, 40 % of the segments, from 40 segments up): the state chain cannot start before the
+// first range's prep, and each later prep is shorter than the chain range it runs beside.
+// Otherwise equal.
+void range_segments(int n_ck, int R, bool backward, int r, int* s_lo, int* s_hi);
 
 // Tensor-core operands of the state chain (head size 128), in the operand layouts of
 // gdn_tc.cuh, floats: W = T diag(gamma) K per (chunk, value head) and Q per (chunk, key head),
