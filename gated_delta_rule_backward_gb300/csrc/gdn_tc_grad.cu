@@ -284,24 +284,11 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     ok = tc::mbar_wait(bar_mma, ph);
     ph ^= 1;
     tc::fence_after();
-    // (2) X^T, Delta^T (rows j) -> the [Delta ; X] tile; A = M^T (rows i)
+    // (2) A = M^T (rows i); D_X goes to registers first (A = M is dead: D_X is done)
+    float x[32];
     if (compute) {
-        const float* sT = sm + kSTr;
-        float x[32];
         tc::ld32(tc::taddr(tmem, warp, kCX), x);
         tc::wait_ld();
-#pragma unroll
-        for (int t = 0; t < BC; ++t) x[t] = __fsub_rn(vx[t], __fmul_rn(sGam[t], x[t]));
-        float* b34 = sm + kR0;  // the K tile is dead: D_X is done
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int t = tb + e;
-            float acc = 0.f;
-#pragma unroll
-            for (int k = 0; k < BC; ++k) acc = __fmaf_rn(sT[t * BC + k], x[k], acc);
-            put_split(b34, kT64, padoff(t, row, kLbo64 / 4), acc);
-            put_split(b34, kT64, padoff(BC + t, row, kLbo64 / 4), hc ? x[16 + e] : x[e]);
-        }
         {  // M[j][row] for this thread's 64 j
             const float* mc = sM + (m_unit ? (row >> 2) * kLdU + (row & 3) : row);
             const int js = m_unit ? 4 : kLdM;
@@ -317,11 +304,11 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         tc::wait_st();
     }
     if (!ok) s_err = 1;
-    tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
     if (s_err) goto done;
-    // (3) D2 = M^T [s gamma dY ; -gamma dX]^T.  Meanwhile dM replaces M in R2 (bulk copy).
+    // (3) D2 = M^T [s gamma dY ; -gamma dX]^T on the tensor cores.  Meanwhile dM replaces M
+    //     in R2 (bulk copy) and X^T, Delta^T (rows j) go into the [Delta ; X] tile.
     if (warp == 8) {
         if (lane == 0) {
             tc::fence_async_smem();
@@ -339,6 +326,21 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                tc::make_desc(tc::smem_addr(sm + kR1 + kT64), kLbo64, 128), kLbo64, 0, TD / 8,
                tc::idesc_tf32(64), false);
         tc::commit(bar_mma);
+    } else if (compute) {
+        const float* sT = sm + kSTr;
+#pragma unroll
+        for (int t = 0; t < BC; ++t) x[t] = __fsub_rn(vx[t], __fmul_rn(sGam[t], x[t]));
+        float* b34 = sm + kR0;  // the K tile is dead: D_X is done
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int t = tb + e;
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < BC; ++k) acc = __fmaf_rn(sT[t * BC + k], x[k], acc);
+            put_split(b34, kT64, padoff(t, row, kLbo64 / 4), acc);
+            put_split(b34, kT64, padoff(BC + t, row, kLbo64 / 4), hc ? x[16 + e] : x[e]);
+        }
+        tc::fence_async_smem();  // the tile is read by the tensor cores from (5) on
     }
     ok = tc::mbar_wait(bar_mma, ph);
     ph ^= 1;
