@@ -43,6 +43,8 @@ constexpr uint32_t kColMhi = 0;               // TMEM columns: M hi  (A operand,
 constexpr uint32_t kColMlo = 128;             //               M lo
 constexpr uint32_t kColD1 = 256;              //               D1 (64 columns)
 constexpr uint32_t kColD23 = 320;             //               D23 (160 columns)
+constexpr uint32_t kColDh = 480;              //               Delta^T hi (A of D23, K = 32); its lo
+                                              //               reuses D1's first 32 columns
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStatusTimeout = 6;
 
@@ -50,12 +52,12 @@ constexpr int kStatusTimeout = 6;
 constexpr int kSB1 = 0;                            // [W; Q] hi, then lo: 2 x 64 x 128, row-group-major
 constexpr int kSB23 = kSB1 + kTcWElems + kTcQElems;  // [sQD; rK^T] hi, lo  2 x 160 x 32
 constexpr int kSU = kSB23 + kTcB23Elems;           // U^T, operand layout (R = 128), fp32
-constexpr int kSDel = kSU + BC * TD;               // Delta^T hi, lo   2 x 128 x 32
+constexpr int kSDel = kSU + BC * TD;               // staging of checkpoint rows (32 x kStageLd)
 constexpr int kSGam = kSDel + 2 * BC * TD;         // gamma (32)
 constexpr int kStageLd = TD + 4;                   // staging rows for coalesced global writes
 constexpr int kSY = kSGam + BC;                    // y of the chunk, rows t (forward)
 constexpr int kSFloats = kSY + BC * kStageLd;
-constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 128;  // + 11 barriers
+constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 128;  // + barriers (6 used)
 
 constexpr uint32_t kB1Bytes = sizeof(float) * (kTcWElems + kTcQElems);
 constexpr int kHalfW = kTcWElems / 2;  // 32 x 128 floats
@@ -94,6 +96,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     uint64_t* bar_b23 = bars + 1;
     uint64_t* bar_mma = bars + 2;
     uint64_t* bar_a = bars + 3;  // bar_a[g]: columns [32 g, 32 g + 32) of both halves of M are in TMEM
+    uint64_t* bar_d = bars + 5;  // Delta^T (the A operand of D23) is in TMEM
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
@@ -127,6 +130,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         tc::mbar_init(bar_b23, 1);
         tc::mbar_init(bar_mma, 1);
         for (int g = 0; g < 2; ++g) tc::mbar_init(bar_a + g, 8);  // one arrival per compute warp
+        tc::mbar_init(bar_d, 4);                                  // one per column-half 0 warp
         tc::mbar_fence_init();
         s_err = 0;
     }
@@ -229,7 +233,6 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
 
     const float* sU = sm + kSU;
     const float* sGam = sm + kSGam;
-    float* sDel = sm + kSDel;
     const uint32_t id64 = tc::idesc_tf32(64), id160 = tc::idesc_tf32(160);
 
     int c = c_begin;
@@ -292,20 +295,27 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             tc::ld32(tc::taddr(tmem, warp, kColD1 + 32 * hc), x);
             tc::wait_ld();
             if (hc == 0) {
-                // Delta^T[j][t] = U^T[j][t] - x[t], split into the operand tile (R = 128, K = 32)
+                // Delta^T[j][t] = U^T[j][t] - x[t], split into TMEM: the A operand of D23 (hi at
+                // kColDh, lo over D1's first 32 columns, which this thread has just read)
 #pragma unroll
-                for (int b = 0; b < BC / 4; ++b) {
-                    const float4 u = *reinterpret_cast<const float4*>(sU + 4 * (b * TD + j));
-                    const float d0 = __fsub_rn(u.x, x[4 * b]), d1 = __fsub_rn(u.y, x[4 * b + 1]);
-                    const float d2 = __fsub_rn(u.z, x[4 * b + 2]), d3 = __fsub_rn(u.w, x[4 * b + 3]);
-                    uint4 hi, lo;
-                    tc::split_tf32(d0, hi.x, lo.x);
-                    tc::split_tf32(d1, hi.y, lo.y);
-                    tc::split_tf32(d2, hi.z, lo.z);
-                    tc::split_tf32(d3, hi.w, lo.w);
-                    *reinterpret_cast<uint4*>(sDel + 4 * (b * TD + j)) = hi;
-                    *reinterpret_cast<uint4*>(sDel + BC * TD + 4 * (b * TD + j)) = lo;
+                for (int q = 0; q < BC / 8; ++q) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int b = 2 * q + h2;
+                        const float4 u = *reinterpret_cast<const float4*>(sU + 4 * (b * TD + j));
+                        tc::split_tf32(__fsub_rn(u.x, x[4 * b]), hi[4 * h2], lo[4 * h2]);
+                        tc::split_tf32(__fsub_rn(u.y, x[4 * b + 1]), hi[4 * h2 + 1], lo[4 * h2 + 1]);
+                        tc::split_tf32(__fsub_rn(u.z, x[4 * b + 2]), hi[4 * h2 + 2], lo[4 * h2 + 2]);
+                        tc::split_tf32(__fsub_rn(u.w, x[4 * b + 3]), hi[4 * h2 + 3], lo[4 * h2 + 3]);
+                    }
+                    tc::st8(tc::taddr(tmem, warp, kColDh + 8 * q), hi);
+                    tc::st8(tc::taddr(tmem, warp, kColD1 + 8 * q), lo);
                 }
+                tc::wait_st();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar_d);
             } else if (FWD) {  // the Q part of y
 #pragma unroll
                 for (int t = 0; t < BC; ++t) sY[t * kStageLd + j] = __fmul_rn(__fmul_rn(A.scale, sGam[t]), x[t]);
@@ -313,26 +323,24 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         }
         ph_b23 ^= 1;
         if (!ok) s_err = 1;
-        tc::fence_async_smem();
-        tc::fence_before();
-        __syncthreads();
-        if (s_err) break;
-        // (4) D23 = Delta^T [scale QD; (r K)^T]^T
+        // (4) D23 = Delta^T [scale QD; (r K)^T]^T, issued as soon as Delta^T is in TMEM
         if (issuer) {
             b23_pending = false;
+            if (!tc::mbar_wait(bar_d, (uint32_t)(c - c_begin) & 1u)) s_err = 1;
             tc::fence_after();
-            const uint64_t ahi = tc::tile_desc(sDel, TD), alo = tc::tile_desc(sDel + BC * TD, TD);
-            const uint64_t bhi = tc::tile_desc(sm + kSB23, 160);
-            const uint64_t blo = tc::tile_desc(sm + kSB23 + kTcB23Elems / 2, 160);
+            if (!s_err) {
+                const uint64_t bhi = tc::tile_desc(sm + kSB23, 160);
+                const uint64_t blo = tc::tile_desc(sm + kSB23 + kTcB23Elems / 2, 160);
 #pragma unroll
-            for (int s = 0; s < BC / 8; ++s) {
-                const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
-                const uint64_t b_h = tc::desc_kslice(bhi, 160, s), b_l = tc::desc_kslice(blo, 160, s);
-                tc::mma_ss(tmem + kColD23, a_h, b_h, id160, s > 0);
-                tc::mma_ss(tmem + kColD23, a_h, b_l, id160, 1);
-                tc::mma_ss(tmem + kColD23, a_l, b_h, id160, 1);
+                for (int s = 0; s < BC / 8; ++s) {
+                    const uint32_t a_h = tmem + kColDh + 8 * s, a_l = tmem + kColD1 + 8 * s;
+                    const uint64_t b_h = tc::desc_kslice(bhi, 160, s), b_l = tc::desc_kslice(blo, 160, s);
+                    tc::mma_ts(tmem + kColD23, a_h, b_h, id160, s > 0);
+                    tc::mma_ts(tmem + kColD23, a_h, b_l, id160, 1);
+                    tc::mma_ts(tmem + kColD23, a_l, b_h, id160, 1);
+                }
+                tc::commit(bar_mma);
             }
-            tc::commit(bar_mma);
         }
         // (5) y and the state update
         ok = tc::mbar_wait(bar_mma, ph_mma);
