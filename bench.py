@@ -427,6 +427,7 @@ def run_ours(args):
         gdn.gdn_backward(p, q, k, v, g, beta, ck, gy, None, packed, ws, stream)
     gdn.set_timing_events(None)
     torch.cuda.synchronize()
+    check_device(stream, "the timed steps")
     kern_ms = [0.0] * (n_fwd + n_bwd)
     for fe, be in ev:
         for j in range(n_fwd):
@@ -505,6 +506,7 @@ def run_ours(args):
         run_steps(k_e2e)
         b_.record(stream)
         torch.cuda.synchronize()
+        check_device(stream, "the end-to-end steps")
         e2e_ms = a.elapsed_time(b_) / k_e2e
         e2e = {"value": world * head_tokens / (e2e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -634,6 +636,7 @@ def run_sweep(args):
             step()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
+        check_device(stream, f"the sweep point d={d} T={T} N={N}")
         ms = sum(a.elapsed_time(b) for a, b in evs) / steps
         head_tokens = N * H_v * T
         tflops = (FWD_FLOPS(d) + BWD_FLOPS(d)) * head_tokens / (ms * 1e-3) / 1e12
@@ -645,6 +648,14 @@ def run_sweep(args):
                                             "frac": tflops / FP32_PEAK_TFLOPS}}), flush=True)
         del qkv, q, k, v, g, beta, state0, gy, y, sT, ck, packed, ws, fws
         torch.cuda.empty_cache()
+
+
+def check_device(stream, what):
+    """A run in which a kernel's bounded wait gave up has invalid outputs: no number."""
+    from gated_delta_rule_backward_gb300 import gdn
+    st = gdn.device_status(stream)
+    if st:
+        raise RuntimeError(f"device status {st} after {what}: {gdn.library().gdn_last_error().decode()}")
 
 
 def main():

@@ -448,8 +448,14 @@ gdn_status_t gdn_device_status(void* stream)
     int e = gdn::tc_take_status(stream, &a);
     if (!e) e = gdn::tc_grad_take_status(stream, &b);
     if (e) return cuda_status(e, "device status");
-    return (a || b) ? fail(GDN_ERR_TIMEOUT, "a kernel's bounded wait gave up; that call's outputs are invalid")
-                    : GDN_OK;
+    if (!a && !b) return GDN_OK;
+    // chain status word: 6 | kernel << 4 | wait-site bits << 8 (gdn_tc_chain.cu)
+    static const char* const kernels[] = {"?", "state chain", "recompute", "dM chain", "selftest"};
+    const int ker = (a >> 4) & 15;
+    return fail(GDN_ERR_TIMEOUT,
+                "a kernel's bounded wait gave up; that call's outputs are invalid (chains: %s, "
+                "wait sites 0x%x; gradient kernel: %s)",
+                a ? kernels[ker < 5 ? ker : 0] : "ok", (unsigned)a >> 8, b ? "timed out" : "ok");
 }
 
 gdn_status_t gdn_selftest_wait_timeout(void* stream)

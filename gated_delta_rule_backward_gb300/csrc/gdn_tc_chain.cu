@@ -30,8 +30,9 @@
 
 namespace gdn {
 
-// Status word of the tensor-core kernels on this device: 0, or GDN_ERR_TIMEOUT (6) after a
-// bounded wait gave up.  Read and cleared by tc_take_status.
+// Status word of the tensor-core kernels on this device: 0, or after a bounded wait gave up
+// GDN_ERR_TIMEOUT (6) | kernel << 4 | wait sites << 8 (bits kW* of the CTAs that gave up,
+// OR-ed).  Read and cleared by tc_take_status.
 __device__ int g_tc_status;
 
 namespace {
@@ -47,6 +48,16 @@ constexpr uint32_t kColDh = 480;              //               Delta^T hi (A of 
                                               //               reuses D1's first 32 columns
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStatusTimeout = 6;
+// kernel field of the status word
+constexpr int kKerState = 1, kKerRecompute = 2, kKerDstate = 3, kKerSelftest = 4;
+// wait sites (s_err bits): the issuer's waits on copies and operand handoffs, and the
+// compute warps' waits on MMA completion
+constexpr int kWCopyA = 1 << 0, kWCopyB = 1 << 1, kWHandoff1 = 1 << 2, kWHandoff2 = 1 << 3,
+              kWMma1 = 1 << 4, kWMma2 = 1 << 5, kWMma3 = 1 << 6;
+__device__ __forceinline__ void raise_timeout(int kernel, int sites)
+{
+    atomicOr(&g_tc_status, kStatusTimeout | kernel << 4 | sites << 8);
+}
 
 // Shared memory, in floats.
 constexpr int kSB1 = 0;                            // [W; Q] hi, then lo: 2 x 64 x 128, row-group-major
@@ -96,7 +107,8 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     uint64_t* bar_b23 = bars + 1;
     uint64_t* bar_mma = bars + 2;
     uint64_t* bar_a = bars + 3;  // bar_a[g]: columns [32 g, 32 g + 32) of both halves of M are in TMEM
-    uint64_t* bar_d = bars + 5;  // Delta^T (the A operand of D23) is in TMEM
+    uint64_t* bar_d = bars + 5;  // Delta^T (the A operand of D23) is in TMEM, and every compute
+                                 // warp has seen D1 complete
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
@@ -130,7 +142,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         tc::mbar_init(bar_b23, 1);
         tc::mbar_init(bar_mma, 1);
         for (int g = 0; g < 2; ++g) tc::mbar_init(bar_a + g, 8);  // one arrival per compute warp
-        tc::mbar_init(bar_d, 4);                                  // one per column-half 0 warp
+        tc::mbar_init(bar_d, 8);                                  // one per compute warp
         tc::mbar_fence_init();
         s_err = 0;
     }
@@ -247,7 +259,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         //     M are in TMEM; meanwhile the pending global stores
         const uint32_t ph_a = (uint32_t)(c - c_begin) & 1u;
         if (issuer) {
-            if (!tc::mbar_wait(bar_b1, ph_b1)) s_err = 1;
+            if (!tc::mbar_wait(bar_b1, ph_b1)) atomicOr(&s_err, kWCopyA);
             ph_b1 ^= 1;
             b1_pending = false;
             if (!s_err) {
@@ -257,7 +269,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 for (int q = 0; q < 8; ++q) {
                     if ((q & 3) == 0) {
                         if (!tc::mbar_wait(bar_a + (q >> 2), ph_a)) {
-                            s_err = 1;
+                            atomicOr(&s_err, kWHandoff1);
                             break;
                         }
                         tc::fence_after();
@@ -278,8 +290,11 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             if (FWD && loc == 0) store_ckpt(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
             if (!FWD && c > c_begin) park_state(A.ws + A.o_Mc + ch * (long long)(TD * TD));
         }
-        // (3) Delta^T (rows j) and the Q part of y^T
-        bool ok = tc::mbar_wait(bar_mma, ph_mma);
+        // (3) Delta^T (rows j) and the Q part of y^T.  Only the compute warps and the issuer
+        // wait on bar_mma: every waiter must have seen a phase complete before the next commit
+        // on it can land (else it would wait on the phase after), and only the bar_d arrivals
+        // of the compute warps order that for D23.
+        bool ok = !(compute || issuer) || tc::mbar_wait(bar_mma, ph_mma);
         ph_mma ^= 1;
         tc::fence_after();
         float gl = 0.f;
@@ -289,6 +304,10 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 b1_pending = true;
             }
         } else if (compute) {
+            if (hc == 1) {  // D23 overwrites nothing these warps read: release it at once
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar_d);
+            }
             ok = tc::mbar_wait(bar_b23, ph_b23) && ok;
             gl = sGam[BC - 1];
             float x[32];
@@ -322,11 +341,11 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             }
         }
         ph_b23 ^= 1;
-        if (!ok) s_err = 1;
+        if (!ok) atomicOr(&s_err, kWMma1);
         // (4) D23 = Delta^T [scale QD; (r K)^T]^T, issued as soon as Delta^T is in TMEM
         if (issuer) {
             b23_pending = false;
-            if (!tc::mbar_wait(bar_d, (uint32_t)(c - c_begin) & 1u)) s_err = 1;
+            if (!tc::mbar_wait(bar_d, (uint32_t)(c - c_begin) & 1u)) atomicOr(&s_err, kWHandoff2);
             tc::fence_after();
             if (!s_err) {
                 const uint64_t bhi = tc::tile_desc(sm + kSB23, 160);
@@ -343,11 +362,12 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             }
         }
         // (5) y and the state update
-        ok = tc::mbar_wait(bar_mma, ph_mma);
+        ok = !(compute || issuer) || tc::mbar_wait(bar_mma, ph_mma);
         ph_mma ^= 1;
         tc::fence_after();
         if (!__syncthreads_and(ok)) {
-            s_err = 1;
+            if (!ok) atomicOr(&s_err, kWMma2);
+            __syncthreads();
             break;
         }
         if (issuer) {
@@ -386,7 +406,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     if (s_err) {
         // give the copies in flight a bounded chance to land before the TMEM is released
         if (issuer) {
-            atomicExch(&g_tc_status, kStatusTimeout);
+            raise_timeout(FWD ? kKerState : kKerRecompute, s_err);
             if (b1_pending) tc::mbar_wait(bar_b1, ph_b1);
             if (b23_pending) tc::mbar_wait(bar_b23, ph_b23);
         }
@@ -419,7 +439,8 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
 // (c / 4) * 128 + j holds row j, columns c .. c + 3); writes dstate0 at the end.
 namespace {
 constexpr uint32_t kDsColHi = 0, kDsColLo = 128, kDsColA = 256, kDsColB = 288, kDsColC = 320;
-// shared memory (floats): K | T^T | [Q^T | K^T] | scale gamma dY^T | E | r | gamma | A tile
+constexpr uint32_t kDsColXh = 448, kDsColXl = 480;  // A of Db, then of Dc's second half (K = 32)
+// shared memory (floats): K | T^T | [Q^T | K^T] | scale gamma dY^T | E | r | gamma
 constexpr int kSmKb = 0;
 constexpr int kSmTT = kSmKb + kDkQKT - kDkKb;
 constexpr int kSmQKT = kSmTT + kDsG - kDsTT;
@@ -427,8 +448,7 @@ constexpr int kSmG = kSmQKT + kTcDkElems - kDkQKT;
 constexpr int kSmE = kSmG + kDsE - kDsG;
 constexpr int kSmR = kSmE + kDsR - kDsE;
 constexpr int kSmGam = kSmR + kDsGam - kDsR;
-constexpr int kDsA = kSmGam + BC;                  // dDelta^T / -gamma dX^T hi, lo
-constexpr int kDsFloats = kDsA + 2 * BC * TD;
+constexpr int kDsFloats = kSmGam + BC;
 constexpr size_t kDsSmemBytes = sizeof(float) * kDsFloats + 64;
 constexpr uint32_t kDsBytesKb = sizeof(float) * (kDkQKT - kDkKb);
 constexpr uint32_t kDsBytesTT = sizeof(float) * (kDsG - kDsTT);
@@ -452,10 +472,12 @@ __device__ __forceinline__ void ds_load_rest(const ChunkArgs& A, long long ch, l
 
 __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int h, int n)
 {
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kDsFloats);  // kb, rest, mma
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kDsFloats);  // kb, rest, mma, x, y
     uint64_t* bar_kb = bars;
     uint64_t* bar_rest = bars + 1;
     uint64_t* bar_mma = bars + 2;
+    uint64_t* bar_x = bars + 3;   // dDelta^T, the A operand of Db, is in TMEM
+    uint64_t* bar_y = bars + 4;   // -gamma dX^T, the A operand of Dc's second half, is in TMEM
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
@@ -471,6 +493,8 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
         tc::mbar_init(bar_kb, 1);
         tc::mbar_init(bar_rest, 1);
         tc::mbar_init(bar_mma, 1);
+        tc::mbar_init(bar_x, 8);  // one arrival per compute warp
+        tc::mbar_init(bar_y, 8);
         tc::mbar_fence_init();
         s_err = 0;
     }
@@ -510,21 +534,20 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
     const float* sE = sm + kSmE;
     const float* sR = sm + kSmR;
     const float* sGam = sm + kSmGam;
-    float* sA = sm + kDsA;
     const uint32_t id32 = tc::idesc_tf32(32), id128 = tc::idesc_tf32(128);
-    // rows j of a 128 x 32 (rows j, K = t) tile: columns t of this thread, [16 hc, 16 hc + 16)
-    auto put_a = [&](const float (&v)[16]) {
+    // Row j of a 128 x 32 (rows j, K = t) A operand in TMEM: this thread's columns t in
+    // [16 hc, 16 hc + 16), tf32 hi at kDsColXh and lo at kDsColXl; then one arrival on `bar`
+    // per warp once the warp's stores are complete.
+    auto put_a = [&](const float (&v)[16], uint64_t* bar) {
+        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            uint4 hi, lo;
-            tc::split_tf32(v[4 * b], hi.x, lo.x);
-            tc::split_tf32(v[4 * b + 1], hi.y, lo.y);
-            tc::split_tf32(v[4 * b + 2], hi.z, lo.z);
-            tc::split_tf32(v[4 * b + 3], hi.w, lo.w);
-            const int unit = (4 * hc + b) * TD + j;
-            *reinterpret_cast<uint4*>(sA + 4 * unit) = hi;
-            *reinterpret_cast<uint4*>(sA + BC * TD + 4 * unit) = lo;
-        }
+        for (int e = 0; e < 16; ++e) tc::split_tf32(v[e], hi[e], lo[e]);
+        tc::st16(tc::taddr(tmem, warp, kDsColXh + 16 * hc), hi);
+        tc::st16(tc::taddr(tmem, warp, kDsColXl + 16 * hc), lo);
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bar);
     };
     auto park16 = [&](long long off, const float (&v)[16]) {  // unit layout, 128 x 32
         float4* d = reinterpret_cast<float4*>(A.ws + off);
@@ -553,7 +576,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
         // (2) Da = dM K^T, then the chain-free half of Dc; meanwhile park dM
         if (issuer) {
             tc::fence_after();
-            if (!tc::mbar_wait(bar_kb, ph_kb)) s_err = 1;
+            if (!tc::mbar_wait(bar_kb, ph_kb)) atomicOr(&s_err, kWCopyA);
             ph_kb ^= 1;
             kb_pending = false;
             if (!s_err) {
@@ -567,7 +590,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
                     tc::mma_ts(tmem + kDsColA, alo, tc::desc_kslice(bhi, 32, s), id32, 1);
                 }
                 tc::commit(bar_mma);
-                if (!tc::mbar_wait(bar_rest, ph_rest)) s_err = 1;
+                if (!tc::mbar_wait(bar_rest, ph_rest)) atomicOr(&s_err, kWCopyB);
                 if (!s_err) {
                     const uint64_t ahi = tc::tile_desc(sm + kSmG, TD), alo = tc::tile_desc(sm + kSmG + BC * TD, TD);
                     const uint64_t qhi = tc::tile_desc(sm + kSmQKT, TD);
@@ -588,8 +611,11 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
             for (int q = 0; q < 16; ++q)
                 dst[(16 * hc + q) * TD + j] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
         }
-        // (3) dDelta^T = r (.) Da + E
-        bool ok = tc::mbar_wait(bar_mma, ph_mma);
+        // (3) dDelta^T = r (.) Da + E.  Only the compute warps and the issuer wait on bar_mma,
+        // and each compute warp arrives on bar_x / bar_y after its wait: so every waiter has
+        // seen a phase complete before the issuer commits the next one (a waiter that missed
+        // a phase would wait on the one after it).
+        bool ok = !(compute || issuer) || tc::mbar_wait(bar_mma, ph_mma);
         ph_mma ^= 1;
         tc::fence_after();
         if (issuer) {
@@ -613,32 +639,31 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
                 v[4 * b + 3] = __fmaf_rn(sR[t + 3], x[4 * b + 3], e.w);
             }
             park16(A.o_dDel + ch * (BC * TD), v);
-            put_a(v);
+            put_a(v, bar_x);
         }
         ph_rest ^= 1;
-        if (!ok) s_err = 1;
-        tc::fence_async_smem();
-        tc::fence_before();
-        __syncthreads();
-        if (s_err) break;
-        // (4) Db = dDelta^T T
+        if (!ok) atomicOr(&s_err, kWMma1);
+        const uint32_t ph_xy = (uint32_t)(c_last - c) & 1u;
+        // (4) Db = dDelta^T T, issued as soon as dDelta^T is in TMEM
         if (issuer) {
             rest_pending = false;
+            if (!tc::mbar_wait(bar_x, ph_xy)) atomicOr(&s_err, kWHandoff1);
             tc::fence_after();
-            const uint64_t ahi = tc::tile_desc(sA, TD), alo = tc::tile_desc(sA + BC * TD, TD);
-            const uint64_t bhi = tc::tile_desc(sm + kSmTT, 32), blo = tc::tile_desc(sm + kSmTT + 32 * 32, 32);
+            if (!s_err) {
+                const uint64_t bhi = tc::tile_desc(sm + kSmTT, 32), blo = tc::tile_desc(sm + kSmTT + 32 * 32, 32);
 #pragma unroll
-            for (int s = 0; s < BC / 8; ++s) {
-                const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
-                const uint64_t b_h = tc::desc_kslice(bhi, 32, s), b_l = tc::desc_kslice(blo, 32, s);
-                tc::mma_ss(tmem + kDsColB, a_h, b_h, id32, s > 0);
-                tc::mma_ss(tmem + kDsColB, a_h, b_l, id32, 1);
-                tc::mma_ss(tmem + kDsColB, a_l, b_h, id32, 1);
+                for (int s = 0; s < BC / 8; ++s) {
+                    const uint32_t a_h = tmem + kDsColXh + 8 * s, a_l = tmem + kDsColXl + 8 * s;
+                    const uint64_t b_h = tc::desc_kslice(bhi, 32, s), b_l = tc::desc_kslice(blo, 32, s);
+                    tc::mma_ts(tmem + kDsColB, a_h, b_h, id32, s > 0);
+                    tc::mma_ts(tmem + kDsColB, a_h, b_l, id32, 1);
+                    tc::mma_ts(tmem + kDsColB, a_l, b_h, id32, 1);
+                }
+                tc::commit(bar_mma);
             }
-            tc::commit(bar_mma);
         }
-        // (5) dX^T = Db;  A tile <- -gamma dX^T
-        ok = tc::mbar_wait(bar_mma, ph_mma);
+        // (5) dX^T = Db;  A operand <- -gamma dX^T
+        ok = !(compute || issuer) || tc::mbar_wait(bar_mma, ph_mma);
         ph_mma ^= 1;
         tc::fence_after();
         float gl = 0.f;
@@ -651,35 +676,34 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
             float v[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = -__fmul_rn(sGam[16 * hc + e], x[e]);
-            put_a(v);
+            put_a(v, bar_y);  // Db is done: its A operand's columns are free
         }
-        if (!ok) s_err = 1;
-        tc::fence_async_smem();
-        tc::fence_before();
-        __syncthreads();
-        if (s_err) break;
-        // (6) Dc += (-gamma dX^T) K
+        if (!ok) atomicOr(&s_err, kWMma3);
+        // (6) Dc += (-gamma dX^T) K, issued as soon as -gamma dX^T is in TMEM
         if (issuer) {
+            if (!tc::mbar_wait(bar_y, ph_xy)) atomicOr(&s_err, kWHandoff2);
             tc::fence_after();
-            const uint64_t ahi = tc::tile_desc(sA, TD), alo = tc::tile_desc(sA + BC * TD, TD);
-            const uint64_t qhi = tc::tile_desc(sm + kSmQKT, TD);
-            const uint64_t qlo = tc::tile_desc(sm + kSmQKT + 2 * BC * TD, TD);
+            if (!s_err) {
+                const uint64_t qhi = tc::tile_desc(sm + kSmQKT, TD);
+                const uint64_t qlo = tc::tile_desc(sm + kSmQKT + 2 * BC * TD, TD);
 #pragma unroll
-            for (int s = 0; s < BC / 8; ++s) {
-                const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
-                const uint64_t b_h = tc::desc_kslice(qhi, TD, s + BC / 8), b_l = tc::desc_kslice(qlo, TD, s + BC / 8);
-                tc::mma_ss(tmem + kDsColC, a_h, b_h, id128, 1);
-                tc::mma_ss(tmem + kDsColC, a_h, b_l, id128, 1);
-                tc::mma_ss(tmem + kDsColC, a_l, b_h, id128, 1);
+                for (int s = 0; s < BC / 8; ++s) {
+                    const uint32_t a_h = tmem + kDsColXh + 8 * s, a_l = tmem + kDsColXl + 8 * s;
+                    const uint64_t b_h = tc::desc_kslice(qhi, TD, s + BC / 8), b_l = tc::desc_kslice(qlo, TD, s + BC / 8);
+                    tc::mma_ts(tmem + kDsColC, a_h, b_h, id128, 1);
+                    tc::mma_ts(tmem + kDsColC, a_h, b_l, id128, 1);
+                    tc::mma_ts(tmem + kDsColC, a_l, b_h, id128, 1);
+                }
+                tc::commit(bar_mma);
             }
-            tc::commit(bar_mma);
         }
         // (7) dM <- gamma_last dM + Dc
-        ok = tc::mbar_wait(bar_mma, ph_mma);
+        ok = !(compute || issuer) || tc::mbar_wait(bar_mma, ph_mma);
         ph_mma ^= 1;
         tc::fence_after();
         if (!__syncthreads_and(ok)) {
-            s_err = 1;
+            if (!ok) atomicOr(&s_err, kWMma2);
+            __syncthreads();
             break;
         }
         if (issuer) {
@@ -702,7 +726,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
 
     if (s_err) {
         if (issuer) {
-            atomicExch(&g_tc_status, kStatusTimeout);
+            raise_timeout(kKerDstate, s_err);
             if (kb_pending) tc::mbar_wait(bar_kb, ph_kb);
             if (rest_pending) tc::mbar_wait(bar_rest, ph_rest);
         }
@@ -803,7 +827,7 @@ __global__ void gdn_selftest_wait_kernel()
         tc::mbar_fence_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0 && !tc::mbar_wait(&bar, 0)) atomicExch(&g_tc_status, kStatusTimeout);
+    if (threadIdx.x == 0 && !tc::mbar_wait(&bar, 0)) raise_timeout(kKerSelftest, kWHandoff1);
 }
 
 int launch_selftest_wait(void* stream)

@@ -31,6 +31,13 @@ def upload(prob, device="cuda"):
     return d
 
 
+def assert_device_ok():
+    """No bounded wait of a tensor-core kernel gave up since the last check."""
+    from gated_delta_rule_backward_gb300 import gdn
+    st = gdn.device_status()
+    assert st == 0, f"device status {st}: {gdn.library().gdn_last_error().decode()}"
+
+
 def run_gpu(prob, C=None, dev=None, dstate_T="from_problem"):
     """Forward + backward through the C ABI.  Returns numpy outputs."""
     import torch
@@ -43,6 +50,7 @@ def run_gpu(prob, C=None, dev=None, dstate_T="from_problem"):
     packed, views = gdn.backward(p, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], ck,
                                  dev["gy"], dsT)
     torch.cuda.synchronize()
+    assert_device_ok()
     out = {"y": y, "state_T": sT, "ckpt": ck}
     out.update(views)
     return {k: v.cpu().numpy() for k, v in out.items()}, packed
