@@ -368,8 +368,8 @@ __device__ __forceinline__ void load_gate_beta(const ChunkArgs& A, int n, int h,
 }
 
 // Tensor-core operands of one (chunk, head) for the state chain at head size 128, in the
-// operand layouts of gdn_tc.cuh: W = T diag(gamma) K (32 x 128, row-group-major; the key
-// head's Q beside it when `first`), B23 = [scale QD; (r K)^T] (160 x 32) as tf32 hi then lo,
+// bf16 operand layouts of gdn_tc.cuh: W = T diag(gamma) K (32 x 128, row-group-major; the key
+// head's Q beside it when `first`), B23 = [scale QD; (r K)^T] (160 x 32) as bf16 hi then lo,
 // and U^T (rows j, 32 tokens) in fp32, U = T V.  Vs holds V on entry and stages U afterwards.
 template <int D>
 __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, long long ck, bool first,
@@ -382,12 +382,12 @@ __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, long long ck,
     float* q1 = A.ws + A.o_Q1 + ck * kTcQElems;
     float* b23 = A.ws + A.o_B23 + ch * kTcB23Elems;
     float* u = A.ws + A.o_U + ch * (BC * D);
-    auto put = [](float* hi_base, int half, int unit, float4 x) {
+    auto put8 = [](float* hi_base, int half, int unit, const float (&x)[8]) {  // 8 consecutive k
         uint4 hi, lo;
-        tc::split_tf32(x.x, hi.x, lo.x);
-        tc::split_tf32(x.y, hi.y, lo.y);
-        tc::split_tf32(x.z, hi.z, lo.z);
-        tc::split_tf32(x.w, hi.w, lo.w);
+        tc::split_bf16x2(x[0], x[1], hi.x, lo.x);
+        tc::split_bf16x2(x[2], x[3], hi.y, lo.y);
+        tc::split_bf16x2(x[4], x[5], hi.z, lo.z);
+        tc::split_bf16x2(x[6], x[7], hi.w, lo.w);
         *reinterpret_cast<uint4*>(hi_base + 4 * unit) = hi;
         *reinterpret_cast<uint4*>(hi_base + half + 4 * unit) = lo;
     };
@@ -406,30 +406,32 @@ __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, long long ck,
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {  // rows t of W, 2 consecutive k per thread
-            const int off = tc::kmaj_rg(fm + 8 * hf, fn + 8 * nt, D);
-            uint2 hi, lo;
-            tc::split_tf32(c[nt][2 * hf], hi.x, lo.x);
-            tc::split_tf32(c[nt][2 * hf + 1], hi.y, lo.y);
-            *reinterpret_cast<uint2*>(w1 + off) = hi;
-            *reinterpret_cast<uint2*>(w1 + kTcWElems / 2 + off) = lo;
+        for (int hf = 0; hf < 2; ++hf) {  // rows t of W, 2 consecutive k (the first even) per thread
+            const int off = tc::kmaj16_rg(fm + 8 * hf, fn + 8 * nt, D);
+            uint32_t hi, lo;
+            tc::split_bf16x2(c[nt][2 * hf], c[nt][2 * hf + 1], hi, lo);
+            reinterpret_cast<uint32_t*>(w1)[off] = hi;
+            reinterpret_cast<uint32_t*>(w1 + kTcWElems / 2)[off] = lo;
         }
-    if (first) {  // Q, unit u = (row group * 32 + k-chunk) * 8 + row % 8
-        for (int u = tid; u < BC * (D / 4); u += CT) {
-            const int t = ((u >> 8) << 3) + (u & 7), kc = (u >> 3) & 31;
-            put(q1, kTcQElems / 2, u, *reinterpret_cast<const float4*>(QKs + t * ld + 4 * kc));
+    if (first) {  // Q, 16-byte unit u = (row group * 16 + k-chunk) * 8 + row % 8
+        for (int u = tid; u < BC * (D / 8); u += CT) {
+            const int t = ((u >> 7) << 3) + (u & 7), kc = (u >> 3) & 15;
+            const float4 a = *reinterpret_cast<const float4*>(QKs + t * ld + 8 * kc);
+            const float4 b = *reinterpret_cast<const float4*>(QKs + t * ld + 8 * kc + 4);
+            const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            put8(q1, kTcQElems / 2, u, x);
         }
     }
-    for (int idx = tid; idx < 160 * (BC / 4); idx += CT) {  // B23, unit = kc * 160 + row
+    for (int idx = tid; idx < 160 * (BC / 8); idx += CT) {  // B23, 16-byte unit = kc * 160 + row
         const int r = idx % 160, kc = idx / 160;
-        float x[4];
+        float x[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int tau = 4 * kc + e;
+        for (int e = 0; e < 8; ++e) {
+            const int tau = 8 * kc + e;
             x[e] = (r < BC) ? __fmul_rn(A.scale, __fmul_rn(QKm[r * LDB + tau], Dm[r * LDB + tau]))
                             : __fmul_rn(Dm[(BC - 1) * LDB + tau], Ks[tau * ld + r - BC]);
         }
-        put(b23, kTcB23Elems / 2, idx, make_float4(x[0], x[1], x[2], x[3]));
+        put8(b23, kTcB23Elems / 2, idx, x);
     }
     __syncthreads();
     for (int idx = tid; idx < (BC / 4) * D; idx += CT) {  // U^T, unit = b * 128 + j

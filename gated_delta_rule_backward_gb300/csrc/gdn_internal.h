@@ -153,14 +153,14 @@ int pipeline_ranges(int n_ck, bool backward);
 // Otherwise equal.
 void range_segments(int n_ck, int R, bool backward, int r, int* s_lo, int* s_hi);
 
-// Tensor-core operands of the state chain (head size 128), in the operand layouts of
-// gdn_tc.cuh, floats: W = T diag(gamma) K per (chunk, value head) and Q per (chunk, key head),
-// each 32 x 128 as tf32 hi then lo in the row-group-major layout (the two stack into the
-// 64-row B operand [W; Q]); [scale QD; (r K)^T] per (chunk, value head) as hi then lo
-// (2 x 160 x 32, k-chunk-major).
-constexpr int kTcWElems = 2 * 32 * 128;
-constexpr int kTcQElems = 2 * 32 * 128;
-constexpr int kTcB23Elems = 2 * 160 * 32;
+// Tensor-core operands of the state chain (head size 128), in the bf16 operand layouts of
+// gdn_tc.cuh, sizes in floats: W = T diag(gamma) K per (chunk, value head) and Q per (chunk,
+// key head), each 32 x 128 as bf16 hi then lo in the row-group-major layout (the two stack
+// into the 64-row B operand [W; Q]); [scale QD; (r K)^T] per (chunk, value head) as bf16 hi
+// then lo (2 x 160 x 32, k-chunk-major).
+constexpr int kTcWElems = 32 * 128;
+constexpr int kTcQElems = 32 * 128;
+constexpr int kTcB23Elems = 160 * 32;
 // Tensor-core operands of the dM chain.  Per (chunk, key head): K (32 x 128, B of dM K^T)
 // and [Q^T | K^T] (128 x 64, B of the dM update) as hi then lo.  Per (chunk, value head):
 // T^T (32 x 32, B of dDelta^T T) and scale gamma dY^T (128 x 32, A of the update) as hi

@@ -1,14 +1,20 @@
 // gdn_tc.cuh -- 5th-generation tensor-core (tcgen05) building blocks for sm_103a, in inline PTX.
 //
-// Every product here is D[128][N] (+)= A[128][K] B[N][K]^T in kind::tf32 with an fp32
-// accumulator in tensor memory (TMEM), issued by one thread of the CTA:
-//   * A is read from TMEM (lane = row, one 32-bit column per K element) or from shared memory;
-//   * B is read from shared memory;
-//   * fp32 accuracy comes from a three-pass split: x = hi + lo with hi, lo tf32 values,
-//     and a b ~= hi_a hi_b + hi_a lo_b + lo_a hi_b (split_tf32 below bounds what is lost).
+// Every product here is D[128][N] (+)= A[128][K] B[N][K]^T with an fp32 accumulator in
+// tensor memory (TMEM), issued by one thread of the CTA:
+//   * A is read from TMEM (lane = row) or from shared memory; B is read from shared memory;
+//   * fp32-level accuracy comes from a three-pass split x = hi + lo, a b ~= hi_a hi_b +
+//     hi_a lo_b + lo_a hi_b, in one of two kinds:
+//       - kind::tf32 (K = 8 per instruction): hi, lo tf32 values (split_tf32), one TMEM column
+//         per K element;
+//       - kind::f16 with bf16 operands (K = 16 per instruction, half the instructions): hi, lo
+//         bf16 values rounded to nearest (split_bf16x2), two K elements per TMEM column, the
+//         even one in the low half.  hi + lo carries 16 significant bits and the exponent
+//         range of fp32.
 //
 // Shared-memory operand layout (no swizzle, K-major): an R x K tile of 4-byte elements is
-// stored as core matrices of 8 rows x 4 elements (128 contiguous bytes, row-major inside);
+// stored as core matrices of 8 rows x 4 elements (128 contiguous bytes, row-major inside;
+// for 2-byte elements 8 rows x 8 elements, with the same byte strides below);
 // core matrix (k-chunk kc, row group g) starts at float offset (kc * (R / 8) + g) * 32.
 // Its descriptor has leading-dimension byte offset LBO = R / 8 * 128 (the step between
 // k-chunks) and stride byte offset SBO = 128 (the step between row groups); the K = 8
@@ -40,6 +46,13 @@ GDN_HD inline int kmaj(int r, int k, int R)
 GDN_HD inline int kmaj_rg(int r, int k, int K)
 {
     return (((r >> 3) * (K >> 2) + (k >> 2)) << 5) + ((r & 7) << 2) + (k & 3);
+}
+// The same layout for 2-byte (bf16) elements: the 32-bit word holding elements (r, k) and
+// (r, k + 1) of a row-group-major tile, k even (core matrices of 8 rows x 8 elements; LBO =
+// 128 bytes, SBO = K * 16 bytes; the K = 16 slice s starts 256 s bytes in).
+GDN_HD inline int kmaj16_rg(int r, int k, int K)
+{
+    return (((r >> 3) * (K >> 3) + (k >> 3)) << 5) + ((r & 7) << 2) + ((k & 7) >> 1);
 }
 
 #if defined(__CUDACC__)
@@ -76,11 +89,32 @@ __device__ __forceinline__ uint64_t desc_kslice_rg(uint64_t d, int s)
 {
     return d + (uint64_t)(16 * s);
 }
+// Row-group-major tile of bf16 elements with K per row (kmaj16_rg); its K = 16 slice s is
+// desc_kslice_rg(d, s), and a k-chunk-major bf16 tile takes tile_desc / desc_kslice as they are.
+__device__ __forceinline__ uint64_t tile_desc16_rg(const void* base, int K)
+{
+    return make_desc(smem_addr(base), 128u, (uint32_t)K * 16u);
+}
 
 // Instruction descriptor, kind::tf32: fp32 accumulator, tf32 A and B, both K-major, M = 128.
 __host__ __device__ constexpr uint32_t idesc_tf32(int n)
 {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16 with bf16 A and B: fp32 accumulator, both K-major, M = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+// D (+)= A B^T, kind::f16 (bf16 operands), A in TMEM (two K elements per column).
+__device__ __forceinline__ void mma_ts16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -182,6 +216,11 @@ __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16])
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
 }
+__device__ __forceinline__ void st4(uint32_t taddr, const uint32_t (&r)[4])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]));
+}
 __device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8])
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
@@ -207,6 +246,20 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo)
 {
     hi = to_tf32(x);
     lo = __float_as_uint(__fsub_rn(x, __uint_as_float(hi)));
+}
+// Two fp32 values as one 32-bit word of bf16 values rounded to nearest: x0 in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float x0, float x1)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(x1), "f"(x0));
+    return r;
+}
+// x0, x1 (consecutive K elements, x0 the even one) split into bf16 hi and lo words:
+// x = hi + lo + O(2^-16 |x|).
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo)
+{
+    hi = pack_bf16x2(x0, x1);
+    lo = pack_bf16x2(__fsub_rn(x0, __uint_as_float(hi << 16)), __fsub_rn(x1, __uint_as_float(hi & 0xFFFF0000u)));
 }
 
 // Barrier among the first `threads` threads of the CTA (named barrier 1), leaving the rest

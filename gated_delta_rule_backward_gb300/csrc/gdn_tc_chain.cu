@@ -1,6 +1,7 @@
 // gdn_tc_chain.cu -- the two serial chains of the chunked scalar gate at head size 128 on
-// the 5th-generation tensor cores (tcgen05, kind::tf32, three-pass split for fp32
-// accuracy): the state chain (forward and recompute) and the dM chain of the backward.
+// the 5th-generation tensor cores (tcgen05, three-pass split for fp32-level accuracy): the
+// state chain (forward and recompute; kind::f16 with bf16 hi/lo operands) and the dM chain
+// of the backward (kind::tf32).
 //
 // State chain:
 //
@@ -8,15 +9,17 @@
 // chunks in order.  Per chunk (32 tokens; "metal: GATED_DELTA_NET_BACK" row form regrouped
 // by chunks, see gdn_chunk.cu for the derivation):
 //   D1  = M [W; Q]^T                    128 x 64, K = 128    (A = M from TMEM, B = [W; Q])
-//   Delta^T = U^T - D1[:, 0:32]         in registers, split to tf32 hi/lo in shared memory
+//   Delta^T = U^T - D1[:, 0:32]         in registers, split to bf16 hi/lo in TMEM
 //   D23 = Delta^T [scale QD; (r K)^T]^T 128 x 160, K = 32    (A = Delta^T, B from smem)
 //   y^T = scale gamma (.) D1[:, 32:64] + D23[:, 0:32]
 //   M   <- gamma_last M + D23[:, 32:160]
 // M itself stays in registers in fp32 (thread = row j, 64 columns); each chunk it is split
-// into tf32 hi/lo parts written to TMEM as the A operand of the next D1.  The chunk
-// operands ([W; Q], [scale QD; (r K)^T] as tf32 hi/lo, U^T in fp32, gamma) are written by
+// into bf16 hi/lo parts written to TMEM as the A operand of the next D1.  The chunk
+// operands ([W; Q], [scale QD; (r K)^T] as bf16 hi/lo, U^T in fp32, gamma) are written by
 // the prep kernel in the tensor-core operand layout and arrive by bulk copies (TMA), the
-// next chunk's as soon as the current one's buffer is free.
+// next chunk's as soon as the current one's buffer is free.  In bf16 (K = 16 per
+// instruction) the chunk's two products take 30 MMAs instead of 60 in tf32; M, the
+// accumulators and every sum outside the products stay fp32.
 //
 // Modes: forward (grid: head, sequence) writes y, the checkpoints and state_T;
 // recompute (grid: segment, sequence * head) rebuilds the chunk-entry states of one
@@ -40,12 +43,12 @@ namespace {
 constexpr int TD = 128;                       // head size
 constexpr int TCT = 288;                      // 8 compute warps (row j, column half) + 1 issuer warp
 constexpr int kIssuer = 256;                  // issues the MMAs and bulk copies
-constexpr uint32_t kColMhi = 0;               // TMEM columns: M hi  (A operand, K = 128)
-constexpr uint32_t kColMlo = 128;             //               M lo
+constexpr uint32_t kColMhi = 0;               // TMEM columns: M hi  (bf16 A operand, K = 128)
+constexpr uint32_t kColMlo = 64;              //               M lo
+constexpr uint32_t kColDh = 128;              //               Delta^T hi (bf16 A of D23, K = 32)
+constexpr uint32_t kColDl = 144;              //               Delta^T lo
 constexpr uint32_t kColD1 = 256;              //               D1 (64 columns)
 constexpr uint32_t kColD23 = 320;             //               D23 (160 columns)
-constexpr uint32_t kColDh = 480;              //               Delta^T hi (A of D23, K = 32); its lo
-                                              //               reuses D1's first 32 columns
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStatusTimeout = 6;
 // kernel field of the status word
@@ -60,8 +63,8 @@ __device__ __forceinline__ void raise_timeout(int kernel, int sites)
 }
 
 // Shared memory, in floats.
-constexpr int kSB1 = 0;                            // [W; Q] hi, then lo: 2 x 64 x 128, row-group-major
-constexpr int kSB23 = kSB1 + kTcWElems + kTcQElems;  // [sQD; rK^T] hi, lo  2 x 160 x 32
+constexpr int kSB1 = 0;                            // [W; Q] bf16 hi, then lo: 2 x 64 x 128, row-group-major
+constexpr int kSB23 = kSB1 + kTcWElems + kTcQElems;  // [sQD; rK^T] bf16 hi, lo  2 x 160 x 32
 constexpr int kSU = kSB23 + kTcB23Elems;           // U^T, operand layout (R = 128), fp32
 constexpr int kSDel = kSU + BC * TD;               // staging of checkpoint rows (32 x kStageLd)
 constexpr int kSGam = kSDel + 2 * BC * TD;         // gamma (32)
@@ -71,7 +74,7 @@ constexpr int kSFloats = kSY + BC * kStageLd;
 constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 128;  // + barriers (6 used)
 
 constexpr uint32_t kB1Bytes = sizeof(float) * (kTcWElems + kTcQElems);
-constexpr int kHalfW = kTcWElems / 2;  // 32 x 128 floats
+constexpr int kHalfW = kTcWElems / 2;  // 32 x 128 bf16 values
 constexpr uint32_t kB23Bytes = sizeof(float) * kTcB23Elems + sizeof(float) * BC * TD + sizeof(float) * BC;
 
 // [W; Q] hi then lo: W of the value head and Q of its key head, stacked by row groups.
@@ -220,16 +223,18 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             tc::bar_sync_first(256);
         }
     };
-    auto split_store = [&](int q) {  // columns [8 q, 8 q + 8) of this thread's half -> TMEM hi/lo
-        uint32_t hi[8], lo[8];
+    // Columns [8 q, 8 q + 8) of this thread's half of M -> bf16 hi/lo in TMEM (4 columns
+    // each): half of the K = 16 slice 4 hc + q / 2 of the next D1's A operand.
+    auto split_store = [&](int q) {
+        uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) tc::split_tf32(m[8 * q + e], hi[e], lo[e]);
-        tc::st8(tc::taddr(tmem, warp, kColMhi + 64 * hc + 8 * q), hi);
-        tc::st8(tc::taddr(tmem, warp, kColMlo + 64 * hc + 8 * q), lo);
+        for (int e = 0; e < 4; ++e) tc::split_bf16x2(m[8 * q + 2 * e], m[8 * q + 2 * e + 1], hi[e], lo[e]);
+        tc::st4(tc::taddr(tmem, warp, kColMhi + 32 * hc + 4 * q), hi);
+        tc::st4(tc::taddr(tmem, warp, kColMlo + 32 * hc + 4 * q), lo);
     };
     // Columns [32 g, 32 g + 32) of this thread's half of the next D1's A operand are written:
-    // the issuer may use k-slices 4 g .. 4 g + 3 and 8 + 4 g .. 8 + 4 g + 3 (one arrival per
-    // compute warp, after the warp's stores are complete).
+    // the issuer may use k-slices 2 g, 2 g + 1, 4 + 2 g and 5 + 2 g (one arrival per compute
+    // warp, after the warp's stores are complete).
     auto release_group = [&](int g) {
         tc::wait_st();
         tc::fence_before();
@@ -245,7 +250,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
 
     const float* sU = sm + kSU;
     const float* sGam = sm + kSGam;
-    const uint32_t id64 = tc::idesc_tf32(64), id160 = tc::idesc_tf32(160);
+    const uint32_t id64 = tc::idesc_bf16(64), id160 = tc::idesc_bf16(160);
 
     int c = c_begin;
     for (; c < c_end; ++c) {
@@ -254,7 +259,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         const int t0 = seg * A.C + loc * BC;
         const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
         const long long ch = head * A.n_chunks + c;
-        // (1) M (tf32 hi/lo, the A operand of D1) goes into TMEM slice by slice (release_slice)
+        // (1) M (bf16 hi/lo, the A operand of D1) goes into TMEM slice by slice (release_group)
         // (2) D1 = M [W; Q]^T on the tensor cores, each k-slice issued as soon as its columns of
         //     M are in TMEM; meanwhile the pending global stores
         const uint32_t ph_a = (uint32_t)(c - c_begin) & 1u;
@@ -263,12 +268,12 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             ph_b1 ^= 1;
             b1_pending = false;
             if (!s_err) {
-                const uint64_t bhi = tc::tile_desc_rg(sm + kSB1, TD);
-                const uint64_t blo = tc::tile_desc_rg(sm + kSB1 + 2 * kHalfW, TD);
+                const uint64_t bhi = tc::tile_desc16_rg(sm + kSB1, TD);
+                const uint64_t blo = tc::tile_desc16_rg(sm + kSB1 + 2 * kHalfW, TD);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if ((q & 3) == 0) {
-                        if (!tc::mbar_wait(bar_a + (q >> 2), ph_a)) {
+                for (int q = 0; q < 4; ++q) {
+                    if ((q & 1) == 0) {
+                        if (!tc::mbar_wait(bar_a + (q >> 1), ph_a)) {
                             atomicOr(&s_err, kWHandoff1);
                             break;
                         }
@@ -276,11 +281,11 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                     }
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
-                        const int s = q + 8 * h2;
+                        const int s = q + 4 * h2;
                         const uint32_t ahi = tmem + kColMhi + 8 * s, alo = tmem + kColMlo + 8 * s;
-                        tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice_rg(bhi, s), id64, s > 0);
-                        tc::mma_ts(tmem + kColD1, ahi, tc::desc_kslice_rg(blo, s), id64, 1);
-                        tc::mma_ts(tmem + kColD1, alo, tc::desc_kslice_rg(bhi, s), id64, 1);
+                        tc::mma_ts16(tmem + kColD1, ahi, tc::desc_kslice_rg(bhi, s), id64, s > 0);
+                        tc::mma_ts16(tmem + kColD1, ahi, tc::desc_kslice_rg(blo, s), id64, 1);
+                        tc::mma_ts16(tmem + kColD1, alo, tc::desc_kslice_rg(bhi, s), id64, 1);
                     }
                 }
                 if (!s_err) tc::commit(bar_mma);
@@ -310,32 +315,34 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             }
             ok = tc::mbar_wait(bar_b23, ph_b23) && ok;
             gl = sGam[BC - 1];
-            float x[32];
-            tc::ld32(tc::taddr(tmem, warp, kColD1 + 32 * hc), x);
-            tc::wait_ld();
             if (hc == 0) {
-                // Delta^T[j][t] = U^T[j][t] - x[t], split into TMEM: the A operand of D23 (hi at
-                // kColDh, lo over D1's first 32 columns, which this thread has just read)
+                // Delta^T[j][t] = U^T[j][t] - D1[j][t], split into bf16 hi/lo in TMEM: the A
+                // operand of D23 (K = t, 16 tokens per 8 columns)
 #pragma unroll
-                for (int q = 0; q < BC / 8; ++q) {
+                for (int q = 0; q < BC / 16; ++q) {
+                    float x[16];
+                    tc::ld16(tc::taddr(tmem, warp, kColD1 + 16 * q), x);
+                    tc::wait_ld();
                     uint32_t hi[8], lo[8];
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int b = 2 * q + h2;
+                    for (int h4 = 0; h4 < 4; ++h4) {
+                        const int b = 4 * q + h4;
                         const float4 u = *reinterpret_cast<const float4*>(sU + 4 * (b * TD + j));
-                        tc::split_tf32(__fsub_rn(u.x, x[4 * b]), hi[4 * h2], lo[4 * h2]);
-                        tc::split_tf32(__fsub_rn(u.y, x[4 * b + 1]), hi[4 * h2 + 1], lo[4 * h2 + 1]);
-                        tc::split_tf32(__fsub_rn(u.z, x[4 * b + 2]), hi[4 * h2 + 2], lo[4 * h2 + 2]);
-                        tc::split_tf32(__fsub_rn(u.w, x[4 * b + 3]), hi[4 * h2 + 3], lo[4 * h2 + 3]);
+                        tc::split_bf16x2(__fsub_rn(u.x, x[4 * h4]), __fsub_rn(u.y, x[4 * h4 + 1]), hi[2 * h4], lo[2 * h4]);
+                        tc::split_bf16x2(__fsub_rn(u.z, x[4 * h4 + 2]), __fsub_rn(u.w, x[4 * h4 + 3]), hi[2 * h4 + 1],
+                                         lo[2 * h4 + 1]);
                     }
                     tc::st8(tc::taddr(tmem, warp, kColDh + 8 * q), hi);
-                    tc::st8(tc::taddr(tmem, warp, kColD1 + 8 * q), lo);
+                    tc::st8(tc::taddr(tmem, warp, kColDl + 8 * q), lo);
                 }
                 tc::wait_st();
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar_d);
             } else if (FWD) {  // the Q part of y
+                float x[32];
+                tc::ld32(tc::taddr(tmem, warp, kColD1 + BC), x);
+                tc::wait_ld();
 #pragma unroll
                 for (int t = 0; t < BC; ++t) sY[t * kStageLd + j] = __fmul_rn(__fmul_rn(A.scale, sGam[t]), x[t]);
             }
@@ -351,12 +358,12 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 const uint64_t bhi = tc::tile_desc(sm + kSB23, 160);
                 const uint64_t blo = tc::tile_desc(sm + kSB23 + kTcB23Elems / 2, 160);
 #pragma unroll
-                for (int s = 0; s < BC / 8; ++s) {
-                    const uint32_t a_h = tmem + kColDh + 8 * s, a_l = tmem + kColD1 + 8 * s;
+                for (int s = 0; s < BC / 16; ++s) {
+                    const uint32_t a_h = tmem + kColDh + 8 * s, a_l = tmem + kColDl + 8 * s;
                     const uint64_t b_h = tc::desc_kslice(bhi, 160, s), b_l = tc::desc_kslice(blo, 160, s);
-                    tc::mma_ts(tmem + kColD23, a_h, b_h, id160, s > 0);
-                    tc::mma_ts(tmem + kColD23, a_h, b_l, id160, 1);
-                    tc::mma_ts(tmem + kColD23, a_l, b_h, id160, 1);
+                    tc::mma_ts16(tmem + kColD23, a_h, b_h, id160, s > 0);
+                    tc::mma_ts16(tmem + kColD23, a_h, b_l, id160, 1);
+                    tc::mma_ts16(tmem + kColD23, a_l, b_h, id160, 1);
                 }
                 tc::commit(bar_mma);
             }
@@ -389,7 +396,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 y_nb = nb;
             }
             // M <- gamma_last M + D23[:, 32:160], split at once into the next D1's A operand and
-            // released to the issuer slice by slice
+            // released to the issuer in two column groups
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 float x[8];
