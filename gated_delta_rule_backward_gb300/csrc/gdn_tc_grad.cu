@@ -52,6 +52,13 @@ __device__ __forceinline__ int padoff(int r, int k, int lbo_floats)
 }
 constexpr int kLbo64 = 8 * 128 + 16;        // bytes between k-chunks, 64-row tile
 constexpr int kT64 = 32 * kLbo64 / 4;       // floats per 64-row, K = 128 tile (hi or lo)
+// The bf16 tiles built here ([Delta ; X]) keep the layout with 8 elements (16 bytes) per
+// core-matrix row: a 64-row, K = 128 tile has 16 k-chunks, kLbo64 bytes apart.
+constexpr int kT64h = 16 * kLbo64 / 4;      // floats per 64-row, K = 128 bf16 tile (hi or lo)
+__device__ __forceinline__ int padoff16(int r, int k)  // byte offset of (r, k) in that tile
+{
+    return (k >> 3) * kLbo64 + ((r >> 3) << 7) + ((r & 7) << 4) + ((k & 7) << 1);
+}
 constexpr int kLbo32 = 4 * 128 + 16;        // 32-row tile
 constexpr int kTP = 8 * kLbo32 / 4;         // 32 rows, K = 32
 constexpr int kTPS = 16 * kLbo32 / 4;       // 32 rows, K = 64
@@ -113,6 +120,28 @@ __device__ __forceinline__ void put_split(float* tile, int half, int off, float 
     tc::split_tf32(x, hi, lo);
     tile[off] = __uint_as_float(hi);
     tile[half + off] = __uint_as_float(lo);
+}
+
+// x as bf16 hi (at byte offset off of the tile) and lo (kT64h floats further).
+__device__ __forceinline__ void put_split16(float* tile, int off, float x)
+{
+    const uint32_t h = tc::pack_bf16x2(x, 0.f);
+    const uint32_t l = tc::pack_bf16x2(__fsub_rn(x, __uint_as_float(h << 16)), 0.f);
+    unsigned char* b = reinterpret_cast<unsigned char*>(tile);
+    *reinterpret_cast<uint16_t*>(b + off) = (uint16_t)h;
+    *reinterpret_cast<uint16_t*>(b + 4 * kT64h + off) = (uint16_t)l;
+}
+
+// The same in kind::f16 with bf16 operands: K = 16 slices, A in TMEM two K elements per column.
+__device__ __forceinline__ void mma3_t16(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t b_hi, uint64_t b_lo,
+                                         uint32_t lbo, int s0, int s1, uint32_t idesc, bool acc)
+{
+    for (int s = s0; s < s1; ++s) {
+        const uint64_t off = (uint64_t)((2 * lbo * s) >> 4);
+        tc::mma_ts16(d, a_hi + 8 * s, b_hi + off, idesc, (acc || s > s0) ? 1u : 0u);
+        tc::mma_ts16(d, a_hi + 8 * s, b_lo + off, idesc, 1);
+        tc::mma_ts16(d, a_lo + 8 * s, b_hi + off, idesc, 1);
+    }
 }
 
 // Issues a K-slices [s0, s1) three-pass product D (+)= A B^T, A in TMEM (column base a).
@@ -337,8 +366,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             float acc = 0.f;
 #pragma unroll
             for (int k = 0; k < BC; ++k) acc = __fmaf_rn(sT[t * BC + k], x[k], acc);
-            put_split(b34, kT64, padoff(t, row, kLbo64 / 4), acc);
-            put_split(b34, kT64, padoff(BC + t, row, kLbo64 / 4), hc ? x[16 + e] : x[e]);
+            put_split16(b34, padoff16(t, row), acc);
+            put_split16(b34, padoff16(BC + t, row), hc ? x[16 + e] : x[e]);
         }
         tc::fence_async_smem();  // the tile is read by the tensor cores from (5) on
     }
@@ -364,8 +393,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     }
     if (compute) {
         if (!tc::mbar_wait(bar_dm, 0)) s_err = 1;
+        const float* dmc = sM + (row >> 2) * kLdU + (row & 3);  // dM[j][row] at dmc[4 j]
         {
-            const float* dmc = sM + (row >> 2) * kLdU + (row & 3);  // dM[j][row] at dmc[4 j]
             float dot = 0.f;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -374,18 +403,25 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                 tc::ld8(tc::taddr(tmem, warp, kCA + j0), mh);
                 tc::ld8(tc::taddr(tmem, warp, kCA + 128 + j0), ml);
                 tc::wait_ld();
-                uint32_t hi[8], lo[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float d = dmc[4 * (j0 + e)];
-                    dot = __fmaf_rn(d, __fadd_rn(mh[e], ml[e]), dot);  // hi + lo = M exactly
-                    tc::split_tf32(d, hi[e], lo[e]);
-                }
-                tc::st8(tc::taddr(tmem, warp, kCA + j0), hi);
-                tc::st8(tc::taddr(tmem, warp, kCA + 128 + j0), lo);
+                for (int e = 0; e < 8; ++e)
+                    dot = __fmaf_rn(dmc[4 * (j0 + e)], __fadd_rn(mh[e], ml[e]), dot);  // hi + lo = M exactly
             }
             dot = warp_sum(dot);
             if (lane == 0) red[(warp & 3) * 96 + 64 + hc] = dot;
+        }
+        // every compute thread has read M^T before dM^T (bf16, two j per column) overwrites it
+        tc::fence_before();
+        tc::bar_sync_first(256);
+        tc::fence_after();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int j0 = 64 * hc + 8 * q;
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tc::split_bf16x2(dmc[4 * (j0 + 2 * e)], dmc[4 * (j0 + 2 * e + 1)], hi[e], lo[e]);
+            tc::st4(tc::taddr(tmem, warp, kCA + j0 / 2), hi);
+            tc::st4(tc::taddr(tmem, warp, kCA + 64 + j0 / 2), lo);
         }
         tc::wait_st();
     }
@@ -400,9 +436,9 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         s_armed |= 1 << 1;
         tc::mbar_expect_tx(bar_qkt, kBytesQKT);
         tc::bulk_g2s(sm + kR2, A.ws + A.o_DK + ck * kTcDkElems + kDkQKT, kBytesQKT, bar_qkt);
-        mma3_t(tmem + kC3, aHi, aLo, tc::make_desc(tc::smem_addr(sm + kR0), kLbo64, 128),
-               tc::make_desc(tc::smem_addr(sm + kR0 + kT64), kLbo64, 128), kLbo64, 0, TD / 8,
-               tc::idesc_tf32(32), false);
+        mma3_t16(tmem + kC3, aHi, aHi + 64, tc::make_desc(tc::smem_addr(sm + kR0), kLbo64, 128),
+                 tc::make_desc(tc::smem_addr(sm + kR0 + kT64h), kLbo64, 128), kLbo64, 0, TD / 16,
+                 tc::idesc_bf16(32), false);
         tc::commit(bar_mma);
     }
     ok = tc::mbar_wait(bar_mma, ph);
@@ -472,13 +508,13 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                 for (int e = 0; e < 32; ++e) v[e] = 0.f;
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {  // bf16, two j per column
                 uint32_t hi[8], lo[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) tc::split_tf32(v[8 * q + e], hi[e], lo[e]);
-                const int j0 = 64 * hc + 32 * half + 8 * q;
-                tc::st8(tc::taddr(tmem, warp, kCA + j0), hi);
-                tc::st8(tc::taddr(tmem, warp, kCA + 128 + j0), lo);
+                for (int e = 0; e < 8; ++e) tc::split_bf16x2(v[16 * q + 2 * e], v[16 * q + 2 * e + 1], hi[e], lo[e]);
+                const int c0 = 32 * hc + 16 * half + 8 * q;
+                tc::st8(tc::taddr(tmem, warp, kCA + c0), hi);
+                tc::st8(tc::taddr(tmem, warp, kCA + 64 + c0), lo);
             }
         }
         tc::wait_st();
@@ -490,9 +526,9 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     // (7) D4 = [dY ; dDelta ; 0] [Delta ; X]^T.  Meanwhile the scalars.
     if (issuer) {
         tc::fence_after();
-        mma3_t(tmem + kC4, aHi, aLo, tc::make_desc(tc::smem_addr(sm + kR0), kLbo64, 128),
-               tc::make_desc(tc::smem_addr(sm + kR0 + kT64), kLbo64, 128), kLbo64, 0, TD / 8,
-               tc::idesc_tf32(64), false);
+        mma3_t16(tmem + kC4, aHi, aHi + 64, tc::make_desc(tc::smem_addr(sm + kR0), kLbo64, 128),
+                 tc::make_desc(tc::smem_addr(sm + kR0 + kT64h), kLbo64, 128), kLbo64, 0, TD / 16,
+                 tc::idesc_bf16(64), false);
         tc::commit(bar_mma);
     } else if (compute) {
         if (tid < 2 * BC) {
