@@ -382,15 +382,6 @@ __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, long long ck,
     float* q1 = A.ws + A.o_Q1 + ck * kTcQElems;
     float* b23 = A.ws + A.o_B23 + ch * kTcB23Elems;
     float* u = A.ws + A.o_U + ch * (BC * D);
-    auto put8 = [](float* hi_base, int half, int unit, const float (&x)[8]) {  // 8 consecutive k
-        uint4 hi, lo;
-        tc::split_bf16x2(x[0], x[1], hi.x, lo.x);
-        tc::split_bf16x2(x[2], x[3], hi.y, lo.y);
-        tc::split_bf16x2(x[4], x[5], hi.z, lo.z);
-        tc::split_bf16x2(x[6], x[7], hi.w, lo.w);
-        *reinterpret_cast<uint4*>(hi_base + 4 * unit) = hi;
-        *reinterpret_cast<uint4*>(hi_base + half + 4 * unit) = lo;
-    };
     static_assert(D == 128, "tensor-core operands are built at head size 128");
     int fm, fn;
     mma_32x128_origin(tid, fm, fn);
@@ -419,7 +410,7 @@ __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, long long ck,
             const float4 a = *reinterpret_cast<const float4*>(QKs + t * ld + 8 * kc);
             const float4 b = *reinterpret_cast<const float4*>(QKs + t * ld + 8 * kc + 4);
             const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            put8(q1, kTcQElems / 2, u, x);
+            tc::put_bf16x8(q1, kTcQElems / 2, u, x);
         }
     }
     for (int idx = tid; idx < 160 * (BC / 8); idx += CT) {  // B23, 16-byte unit = kc * 160 + row
@@ -431,7 +422,7 @@ __device__ void prep_tc_operands(const ChunkArgs& A, long long ch, long long ck,
             x[e] = (r < BC) ? __fmul_rn(A.scale, __fmul_rn(QKm[r * LDB + tau], Dm[r * LDB + tau]))
                             : __fmul_rn(Dm[(BC - 1) * LDB + tau], Ks[tau * ld + r - BC]);
         }
-        put8(b23, kTcB23Elems / 2, idx, x);
+        tc::put_bf16x8(b23, kTcB23Elems / 2, idx, x);
     }
     __syncthreads();
     for (int idx = tid; idx < (BC / 4) * D; idx += CT) {  // U^T, unit = b * 128 + j
@@ -456,15 +447,6 @@ __device__ void prep_tc_dstate_operands(const ChunkArgs& A, int n, int h, const 
     const float* Ks = QKs + BC * ld;
     float* blk = A.ws + A.o_DS + ch * kTcDsElems;
     float* kblk = A.ws + A.o_DK + ck * kTcDkElems;
-    auto put = [](float* hi_base, int half, int unit, float4 x) {
-        uint4 hi, lo;
-        tc::split_tf32(x.x, hi.x, lo.x);
-        tc::split_tf32(x.y, hi.y, lo.y);
-        tc::split_tf32(x.z, hi.z, lo.z);
-        tc::split_tf32(x.w, hi.w, lo.w);
-        *reinterpret_cast<uint4*>(hi_base + 4 * unit) = hi;
-        *reinterpret_cast<uint4*>(hi_base + half + 4 * unit) = lo;
-    };
     {
         const long long tg = (long long)n * A.gys0 + (long long)cp.t0 * A.gys1 + (long long)h * A.gys2;
         float4 r[D / 32];
@@ -493,31 +475,37 @@ __device__ void prep_tc_dstate_operands(const ChunkArgs& A, int n, int h, const 
                     e[4 * ((t >> 2) * D + j) + (t & 3)] = __fmul_rn(A.scale, c[nt][2 * hf + x]);
                 }
     }
-    for (int idx = tid; idx < (BC / 4) * D; idx += CT) {  // scale gamma dY^T, unit b * 128 + j
-        const int j = idx % D, b = idx / D;
-        float x[4];
+    // bf16 tiles, k-chunk-major: 16-byte unit kc * R + row holds 8 consecutive K elements
+    for (int idx = tid; idx < (BC / 8) * D; idx += CT) {  // scale gamma dY^T, unit kc * 128 + j
+        const int j = idx % D, kc = idx / D;
+        float x[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            x[e] = __fmul_rn(__fmul_rn(A.scale, gam[4 * b + e]), Vs[(4 * b + e) * ld + j]);
-        put(blk + kDsG, 2 * 128 * 32 / 2, idx, make_float4(x[0], x[1], x[2], x[3]));
+        for (int e = 0; e < 8; ++e)
+            x[e] = __fmul_rn(__fmul_rn(A.scale, gam[8 * kc + e]), Vs[(8 * kc + e) * ld + j]);
+        tc::put_bf16x8(blk + kDsG, 128 * 32 / 2, idx, x);
     }
     if (first) {
-        for (int idx = tid; idx < (D / 4) * BC; idx += CT) {  // K rows t, unit kc * 32 + t
+        for (int idx = tid; idx < (D / 8) * BC; idx += CT) {  // K rows t, unit kc * 32 + t
             const int t = idx % BC, kc = idx / BC;
-            put(kblk + kDkKb, 2 * 32 * 128 / 2, idx, *reinterpret_cast<const float4*>(Ks + t * ld + 4 * kc));
+            const float4 a = *reinterpret_cast<const float4*>(Ks + t * ld + 8 * kc);
+            const float4 b = *reinterpret_cast<const float4*>(Ks + t * ld + 8 * kc + 4);
+            const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            tc::put_bf16x8(kblk + kDkKb, 32 * 128 / 2, idx, x);
         }
-        for (int idx = tid; idx < (2 * BC / 4) * D; idx += CT) {  // [Q^T | K^T] rows i, unit kc * 128 + i
+        for (int idx = tid; idx < (2 * BC / 8) * D; idx += CT) {  // [Q^T | K^T] rows i, unit kc * 128 + i
             const int i = idx % D, kc = idx / D;
-            put(kblk + kDkQKT, 2 * 128 * 64 / 2, idx,
-                make_float4(QKs[(4 * kc) * ld + i], QKs[(4 * kc + 1) * ld + i], QKs[(4 * kc + 2) * ld + i],
-                            QKs[(4 * kc + 3) * ld + i]));
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = QKs[(8 * kc + e) * ld + i];
+            tc::put_bf16x8(kblk + kDkQKT, 128 * 64 / 2, idx, x);
         }
     }
-    for (int idx = tid; idx < (BC / 4) * BC; idx += CT) {  // T^T rows t: T[t'][t], unit kc * 32 + t
+    for (int idx = tid; idx < (BC / 8) * BC; idx += CT) {  // T^T rows t: T[t'][t], unit kc * 32 + t
         const int t = idx % BC, kc = idx / BC;
-        put(blk + kDsTT, 2 * 32 * 32 / 2, idx,
-            make_float4(Ts[(4 * kc) * LDB + t], Ts[(4 * kc + 1) * LDB + t], Ts[(4 * kc + 2) * LDB + t],
-                        Ts[(4 * kc + 3) * LDB + t]));
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = Ts[(8 * kc + e) * LDB + t];
+        tc::put_bf16x8(blk + kDsTT, 32 * 32 / 2, idx, x);
     }
     if (tid < BC) {
         blk[kDsR + tid] = Dm[(BC - 1) * LDB + tid];

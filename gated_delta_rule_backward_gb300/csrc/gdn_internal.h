@@ -161,16 +161,17 @@ void range_segments(int n_ck, int R, bool backward, int r, int* s_lo, int* s_hi)
 constexpr int kTcWElems = 32 * 128;
 constexpr int kTcQElems = 32 * 128;
 constexpr int kTcB23Elems = 160 * 32;
-// Tensor-core operands of the dM chain.  Per (chunk, key head): K (32 x 128, B of dM K^T)
-// and [Q^T | K^T] (128 x 64, B of the dM update) as hi then lo.  Per (chunk, value head):
-// T^T (32 x 32, B of dDelta^T T) and scale gamma dY^T (128 x 32, A of the update) as hi
-// then lo, E = scale dY^T QD (128 x 32, fp32, rows j), r and gamma (32 each).
+// Tensor-core operands of the dM chain and the gradient step, sizes in floats.  Per (chunk,
+// key head): K (32 x 128, B of dM K^T and of M K^T) and [Q^T | K^T] (128 x 64, B of the dM
+// update, A of the gradient's last product) as bf16 hi then lo.  Per (chunk, value head):
+// T^T (32 x 32, B of dDelta^T T) and scale gamma dY^T (128 x 32, A of the update) as bf16
+// hi then lo, E = scale dY^T QD (128 x 32, fp32, rows j), r and gamma (32 each).
 constexpr int kDkKb = 0;
-constexpr int kDkQKT = kDkKb + 2 * 32 * 128;
-constexpr int kTcDkElems = kDkQKT + 2 * 128 * 64;
+constexpr int kDkQKT = kDkKb + 32 * 128;
+constexpr int kTcDkElems = kDkQKT + 128 * 64;
 constexpr int kDsTT = 0;
-constexpr int kDsG = kDsTT + 2 * 32 * 32;
-constexpr int kDsE = kDsG + 2 * 128 * 32;
+constexpr int kDsG = kDsTT + 32 * 32;
+constexpr int kDsE = kDsG + 128 * 32;
 constexpr int kDsR = kDsE + 128 * 32;
 constexpr int kDsGam = kDsR + 32;
 constexpr int kTcDsElems = kDsGam + 32;

@@ -117,6 +117,16 @@ __device__ __forceinline__ void mma_ts16(uint32_t d_tmem, uint32_t a_tmem, uint6
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// D (+)= A B^T, kind::f16 (bf16 operands), A and B in shared memory.
+__device__ __forceinline__ void mma_ss16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate)
 {
@@ -260,6 +270,19 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
 {
     hi = pack_bf16x2(x0, x1);
     lo = pack_bf16x2(__fsub_rn(x0, __uint_as_float(hi << 16)), __fsub_rn(x1, __uint_as_float(hi & 0xFFFF0000u)));
+}
+
+// 8 consecutive K elements of one row (one 16-byte unit of a bf16 tile in the layouts above)
+// as bf16 hi at hi_base + 4 unit and lo `half` floats further.
+__device__ __forceinline__ void put_bf16x8(float* hi_base, int half, int unit, const float (&x)[8])
+{
+    uint4 hi, lo;
+    split_bf16x2(x[0], x[1], hi.x, lo.x);
+    split_bf16x2(x[2], x[3], hi.y, lo.y);
+    split_bf16x2(x[4], x[5], hi.z, lo.z);
+    split_bf16x2(x[6], x[7], hi.w, lo.w);
+    *reinterpret_cast<uint4*>(hi_base + 4 * unit) = hi;
+    *reinterpret_cast<uint4*>(hi_base + half + 4 * unit) = lo;
 }
 
 // Barrier among the first `threads` threads of the CTA (named barrier 1), leaving the rest

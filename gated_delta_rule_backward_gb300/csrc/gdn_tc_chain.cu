@@ -1,7 +1,7 @@
 // gdn_tc_chain.cu -- the two serial chains of the chunked scalar gate at head size 128 on
-// the 5th-generation tensor cores (tcgen05, three-pass split for fp32-level accuracy): the
-// state chain (forward and recompute; kind::f16 with bf16 hi/lo operands) and the dM chain
-// of the backward (kind::tf32).
+// the 5th-generation tensor cores (tcgen05, kind::f16 with bf16 hi/lo operands, three-pass
+// split for fp32-level accuracy): the state chain (forward and recompute) and the dM chain
+// of the backward.
 //
 // State chain:
 //
@@ -433,7 +433,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
 
 // ---------------------------------------------------------------------------------
 // The dM chain in reverse on the tensor cores.  One CTA per head owns dM (128 x 128, rows j;
-// fp32 in registers, tf32 hi/lo in TMEM as an A operand).  Per chunk, last first:
+// fp32 in registers, bf16 hi/lo in TMEM as an A operand).  Per chunk, last first:
 //   park dM (the gradient of the chunk's end state)
 //   Da = dM K^T                 128 x 32,  K = 128   (B: K rows t)
 //   dDelta^T = r (.) Da + E     E = scale dY^T QD, precomputed by the prep kernel
@@ -445,8 +445,10 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
 // Parks dM, dDelta^T and dX^T for the gradient kernel in the unit layout (float4 unit
 // (c / 4) * 128 + j holds row j, columns c .. c + 3); writes dstate0 at the end.
 namespace {
-constexpr uint32_t kDsColHi = 0, kDsColLo = 128, kDsColA = 256, kDsColB = 288, kDsColC = 320;
-constexpr uint32_t kDsColXh = 448, kDsColXl = 480;  // A of Db, then of Dc's second half (K = 32)
+// TMEM columns: dM as bf16 hi/lo pairs (A of Da, K = 128), Da, Db, Dc, and the bf16 A operand
+// of Db, then of Dc's second half (K = 32)
+constexpr uint32_t kDsColHi = 0, kDsColLo = 64, kDsColA = 256, kDsColB = 288, kDsColC = 320;
+constexpr uint32_t kDsColXh = 448, kDsColXl = 480;
 // shared memory (floats): K | T^T | [Q^T | K^T] | scale gamma dY^T | E | r | gamma
 constexpr int kSmKb = 0;
 constexpr int kSmTT = kSmKb + kDkQKT - kDkKb;
@@ -541,16 +543,16 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
     const float* sE = sm + kSmE;
     const float* sR = sm + kSmR;
     const float* sGam = sm + kSmGam;
-    const uint32_t id32 = tc::idesc_tf32(32), id128 = tc::idesc_tf32(128);
+    const uint32_t id32 = tc::idesc_bf16(32), id128 = tc::idesc_bf16(128);
     // Row j of a 128 x 32 (rows j, K = t) A operand in TMEM: this thread's columns t in
-    // [16 hc, 16 hc + 16), tf32 hi at kDsColXh and lo at kDsColXl; then one arrival on `bar`
-    // per warp once the warp's stores are complete.
+    // [16 hc, 16 hc + 16), bf16 hi at kDsColXh and lo at kDsColXl (two t per column); then
+    // one arrival on `bar` per warp once the warp's stores are complete.
     auto put_a = [&](const float (&v)[16], uint64_t* bar) {
-        uint32_t hi[16], lo[16];
+        uint32_t hi[8], lo[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) tc::split_tf32(v[e], hi[e], lo[e]);
-        tc::st16(tc::taddr(tmem, warp, kDsColXh + 16 * hc), hi);
-        tc::st16(tc::taddr(tmem, warp, kDsColXl + 16 * hc), lo);
+        for (int e = 0; e < 8; ++e) tc::split_bf16x2(v[2 * e], v[2 * e + 1], hi[e], lo[e]);
+        tc::st8(tc::taddr(tmem, warp, kDsColXh + 8 * hc), hi);
+        tc::st8(tc::taddr(tmem, warp, kDsColXl + 8 * hc), lo);
         tc::wait_st();
         tc::fence_before();
         __syncwarp();
@@ -566,15 +568,15 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
     int c = c_last;
     for (; c >= A.c_lo; --c) {
         const long long ch = head * A.n_chunks + c;
-        // (1) dM -> tf32 hi/lo in TMEM
+        // (1) dM -> bf16 hi/lo in TMEM (two columns i per TMEM column)
         if (compute) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t hi[16], lo[16];
+            for (int q = 0; q < 8; ++q) {
+                uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) tc::split_tf32(m[16 * q + e], hi[e], lo[e]);
-                tc::st16(tc::taddr(tmem, warp, kDsColHi + 64 * hc + 16 * q), hi);
-                tc::st16(tc::taddr(tmem, warp, kDsColLo + 64 * hc + 16 * q), lo);
+                for (int e = 0; e < 4; ++e) tc::split_bf16x2(m[8 * q + 2 * e], m[8 * q + 2 * e + 1], hi[e], lo[e]);
+                tc::st4(tc::taddr(tmem, warp, kDsColHi + 32 * hc + 4 * q), hi);
+                tc::st4(tc::taddr(tmem, warp, kDsColLo + 32 * hc + 4 * q), lo);
             }
             tc::wait_st();
         }
@@ -588,27 +590,27 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
             kb_pending = false;
             if (!s_err) {
                 const uint64_t bhi = tc::tile_desc(sm + kSmKb, 32);
-                const uint64_t blo = tc::tile_desc(sm + kSmKb + 32 * TD, 32);
+                const uint64_t blo = tc::tile_desc(sm + kSmKb + 32 * TD / 2, 32);
 #pragma unroll
-                for (int s = 0; s < TD / 8; ++s) {
+                for (int s = 0; s < TD / 16; ++s) {
                     const uint32_t ahi = tmem + kDsColHi + 8 * s, alo = tmem + kDsColLo + 8 * s;
-                    tc::mma_ts(tmem + kDsColA, ahi, tc::desc_kslice(bhi, 32, s), id32, s > 0);
-                    tc::mma_ts(tmem + kDsColA, ahi, tc::desc_kslice(blo, 32, s), id32, 1);
-                    tc::mma_ts(tmem + kDsColA, alo, tc::desc_kslice(bhi, 32, s), id32, 1);
+                    tc::mma_ts16(tmem + kDsColA, ahi, tc::desc_kslice(bhi, 32, s), id32, s > 0);
+                    tc::mma_ts16(tmem + kDsColA, ahi, tc::desc_kslice(blo, 32, s), id32, 1);
+                    tc::mma_ts16(tmem + kDsColA, alo, tc::desc_kslice(bhi, 32, s), id32, 1);
                 }
                 tc::commit(bar_mma);
                 if (!tc::mbar_wait(bar_rest, ph_rest)) atomicOr(&s_err, kWCopyB);
                 if (!s_err) {
-                    const uint64_t ahi = tc::tile_desc(sm + kSmG, TD), alo = tc::tile_desc(sm + kSmG + BC * TD, TD);
+                    const uint64_t ahi = tc::tile_desc(sm + kSmG, TD), alo = tc::tile_desc(sm + kSmG + BC * TD / 2, TD);
                     const uint64_t qhi = tc::tile_desc(sm + kSmQKT, TD);
-                    const uint64_t qlo = tc::tile_desc(sm + kSmQKT + 2 * BC * TD, TD);
+                    const uint64_t qlo = tc::tile_desc(sm + kSmQKT + BC * TD, TD);
 #pragma unroll
-                    for (int s = 0; s < BC / 8; ++s) {
+                    for (int s = 0; s < BC / 16; ++s) {
                         const uint64_t a_h = tc::desc_kslice(ahi, TD, s), a_l = tc::desc_kslice(alo, TD, s);
                         const uint64_t b_h = tc::desc_kslice(qhi, TD, s), b_l = tc::desc_kslice(qlo, TD, s);
-                        tc::mma_ss(tmem + kDsColC, a_h, b_h, id128, s > 0);
-                        tc::mma_ss(tmem + kDsColC, a_h, b_l, id128, 1);
-                        tc::mma_ss(tmem + kDsColC, a_l, b_h, id128, 1);
+                        tc::mma_ss16(tmem + kDsColC, a_h, b_h, id128, s > 0);
+                        tc::mma_ss16(tmem + kDsColC, a_h, b_l, id128, 1);
+                        tc::mma_ss16(tmem + kDsColC, a_l, b_h, id128, 1);
                     }
                 }
             }
@@ -657,14 +659,14 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
             if (!tc::mbar_wait(bar_x, ph_xy)) atomicOr(&s_err, kWHandoff1);
             tc::fence_after();
             if (!s_err) {
-                const uint64_t bhi = tc::tile_desc(sm + kSmTT, 32), blo = tc::tile_desc(sm + kSmTT + 32 * 32, 32);
+                const uint64_t bhi = tc::tile_desc(sm + kSmTT, 32), blo = tc::tile_desc(sm + kSmTT + 32 * 32 / 2, 32);
 #pragma unroll
-                for (int s = 0; s < BC / 8; ++s) {
+                for (int s = 0; s < BC / 16; ++s) {
                     const uint32_t a_h = tmem + kDsColXh + 8 * s, a_l = tmem + kDsColXl + 8 * s;
                     const uint64_t b_h = tc::desc_kslice(bhi, 32, s), b_l = tc::desc_kslice(blo, 32, s);
-                    tc::mma_ts(tmem + kDsColB, a_h, b_h, id32, s > 0);
-                    tc::mma_ts(tmem + kDsColB, a_h, b_l, id32, 1);
-                    tc::mma_ts(tmem + kDsColB, a_l, b_h, id32, 1);
+                    tc::mma_ts16(tmem + kDsColB, a_h, b_h, id32, s > 0);
+                    tc::mma_ts16(tmem + kDsColB, a_h, b_l, id32, 1);
+                    tc::mma_ts16(tmem + kDsColB, a_l, b_h, id32, 1);
                 }
                 tc::commit(bar_mma);
             }
@@ -692,14 +694,14 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
             tc::fence_after();
             if (!s_err) {
                 const uint64_t qhi = tc::tile_desc(sm + kSmQKT, TD);
-                const uint64_t qlo = tc::tile_desc(sm + kSmQKT + 2 * BC * TD, TD);
+                const uint64_t qlo = tc::tile_desc(sm + kSmQKT + BC * TD, TD);
 #pragma unroll
-                for (int s = 0; s < BC / 8; ++s) {
+                for (int s = 0; s < BC / 16; ++s) {
                     const uint32_t a_h = tmem + kDsColXh + 8 * s, a_l = tmem + kDsColXl + 8 * s;
-                    const uint64_t b_h = tc::desc_kslice(qhi, TD, s + BC / 8), b_l = tc::desc_kslice(qlo, TD, s + BC / 8);
-                    tc::mma_ts(tmem + kDsColC, a_h, b_h, id128, 1);
-                    tc::mma_ts(tmem + kDsColC, a_h, b_l, id128, 1);
-                    tc::mma_ts(tmem + kDsColC, a_l, b_h, id128, 1);
+                    const uint64_t b_h = tc::desc_kslice(qhi, TD, s + BC / 16), b_l = tc::desc_kslice(qlo, TD, s + BC / 16);
+                    tc::mma_ts16(tmem + kDsColC, a_h, b_h, id128, 1);
+                    tc::mma_ts16(tmem + kDsColC, a_h, b_l, id128, 1);
+                    tc::mma_ts16(tmem + kDsColC, a_l, b_h, id128, 1);
                 }
                 tc::commit(bar_mma);
             }

@@ -17,8 +17,10 @@
 //   D2    += [K^T P^T | Q^T P + K^T S]      (A = [Q^T | K^T] from the prep kernel, rows i)
 //   dq_h = D2[:, 0:32]^T,   dk_h = (D2[:, 32:64] + D3 diag(r))^T,   dv = dX,
 //   dg (reverse scan of the gate gradient), dbeta.
-// Every product is a three-pass tf32 split with an fp32 accumulator in TMEM (gdn_tc.cuh);
-// the A operands built here go to TMEM, the B operands to padded shared-memory tiles.
+// Every product is a three-pass split with an fp32 accumulator in TMEM (gdn_tc.cuh): bf16
+// hi/lo (kind::f16) for all but D2's first part, which keeps tf32 hi/lo because the exact
+// tf32 split of M^T also gives <dM, M>.  The A operands built here go to TMEM, the B
+// operands to padded shared-memory tiles.
 #include <cuda_runtime.h>
 
 #include "gdn_gemm.cuh"
@@ -55,13 +57,13 @@ constexpr int kT64 = 32 * kLbo64 / 4;       // floats per 64-row, K = 128 tile (
 // The bf16 tiles built here ([Delta ; X]) keep the layout with 8 elements (16 bytes) per
 // core-matrix row: a 64-row, K = 128 tile has 16 k-chunks, kLbo64 bytes apart.
 constexpr int kT64h = 16 * kLbo64 / 4;      // floats per 64-row, K = 128 bf16 tile (hi or lo)
-__device__ __forceinline__ int padoff16(int r, int k)  // byte offset of (r, k) in that tile
+__device__ __forceinline__ int padoff16(int r, int k, int lbo = kLbo64)  // byte offset of (r, k)
 {
-    return (k >> 3) * kLbo64 + ((r >> 3) << 7) + ((r & 7) << 4) + ((k & 7) << 1);
+    return (k >> 3) * lbo + ((r >> 3) << 7) + ((r & 7) << 4) + ((k & 7) << 1);
 }
 constexpr int kLbo32 = 4 * 128 + 16;        // 32-row tile
-constexpr int kTP = 8 * kLbo32 / 4;         // 32 rows, K = 32
-constexpr int kTPS = 16 * kLbo32 / 4;       // 32 rows, K = 64
+constexpr int kTP = 4 * kLbo32 / 4;         // 32 rows, K = 32 (bf16: 4 k-chunks of 8)
+constexpr int kTPS = 8 * kLbo32 / 4;        // 32 rows, K = 64 (bf16)
 constexpr int kLdM = TD + 4;                // fp32 staging, row-major rows of TD floats
 constexpr int kLdU = 4 * TD + 4;            // fp32 staging of a unit-layout park: one row of
                                             // 128 float4 per 4 columns, 16 bytes of pad between
@@ -100,10 +102,10 @@ constexpr int kDdStage = kR1 + 6 * BC * LDF;   // dDelta (unit layout, 8 x kLdU)
 constexpr int kDyStage = kDdStage + BC * kLdM; // dY rows t (32 x kLdM), before the algebra
 static_assert((BC / 4) * kLdU <= BC * kLdM && kDyStage + BC * kLdM <= kR2, "R1 overflow");
 
-constexpr uint32_t kBytesKb = sizeof(float) * 2 * 32 * 128;
+constexpr uint32_t kBytesKb = sizeof(float) * (kDkQKT - kDkKb);
 constexpr uint32_t kBytesFac = sizeof(float) * 5 * BC * BC;
 constexpr uint32_t kBytesGR = sizeof(float) * 2 * BC;
-constexpr uint32_t kBytesQKT = sizeof(float) * 2 * 128 * 64;
+constexpr uint32_t kBytesQKT = sizeof(float) * (kTcDkElems - kDkQKT);
 constexpr uint32_t kBytesState = sizeof(float) * TD * TD;
 constexpr uint32_t kBytesDd = sizeof(float) * BC * TD;
 
@@ -122,14 +124,14 @@ __device__ __forceinline__ void put_split(float* tile, int half, int off, float 
     tile[half + off] = __uint_as_float(lo);
 }
 
-// x as bf16 hi (at byte offset off of the tile) and lo (kT64h floats further).
-__device__ __forceinline__ void put_split16(float* tile, int off, float x)
+// x as bf16 hi (at byte offset off of the tile) and lo (`half` floats further).
+__device__ __forceinline__ void put_split16(float* tile, int off, float x, int half = kT64h)
 {
     const uint32_t h = tc::pack_bf16x2(x, 0.f);
     const uint32_t l = tc::pack_bf16x2(__fsub_rn(x, __uint_as_float(h << 16)), 0.f);
     unsigned char* b = reinterpret_cast<unsigned char*>(tile);
     *reinterpret_cast<uint16_t*>(b + off) = (uint16_t)h;
-    *reinterpret_cast<uint16_t*>(b + 4 * kT64h + off) = (uint16_t)l;
+    *reinterpret_cast<uint16_t*>(b + 4 * half + off) = (uint16_t)l;
 }
 
 // The same in kind::f16 with bf16 operands: K = 16 slices, A in TMEM two K elements per column.
@@ -272,12 +274,13 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                 a = *reinterpret_cast<const float4*>(sM + row * kLdM + 64 * hc + 8 * q);
                 b = *reinterpret_cast<const float4*>(sM + row * kLdM + 64 * hc + 8 * q + 4);
             }
-            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            uint32_t hi[8], lo[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) tc::split_tf32(v[e], hi[e], lo[e]);
-            tc::st8(tc::taddr(tmem, warp, kCA + 64 * hc + 8 * q), hi);
-            tc::st8(tc::taddr(tmem, warp, kCA + 128 + 64 * hc + 8 * q), lo);
+            uint32_t hi[4], lo[4];  // bf16, two columns per TMEM column
+            tc::split_bf16x2(a.x, a.y, hi[0], lo[0]);
+            tc::split_bf16x2(a.z, a.w, hi[1], lo[1]);
+            tc::split_bf16x2(b.x, b.y, hi[2], lo[2]);
+            tc::split_bf16x2(b.z, b.w, hi[3], lo[3]);
+            tc::st4(tc::taddr(tmem, warp, kCA + 32 * hc + 4 * q), hi);
+            tc::st4(tc::taddr(tmem, warp, kCA + 64 + 32 * hc + 4 * q), lo);
         }
         tc::wait_st();
     }
@@ -290,8 +293,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         tc::fence_after();
         if (!tc::mbar_wait(bar_ld, 0)) s_err = 1;
         if (!s_err) {
-            mma3_t(tmem + kCX, aHi, aLo, tc::tile_desc(sm + kR0, 32), tc::tile_desc(sm + kR0 + 32 * TD, 32),
-                   (32 / 8) * 128, 0, TD / 8, tc::idesc_tf32(32), false);
+            mma3_t16(tmem + kCX, aHi, aHi + 64, tc::tile_desc(sm + kR0, 32), tc::tile_desc(sm + kR0 + 32 * TD / 2, 32),
+                     (32 / 8) * 128, 0, TD / 16, tc::idesc_bf16(32), false);
             tc::commit(bar_mma);
         }
     } else if (compute) {
@@ -446,7 +449,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     tc::fence_after();
     // (6) the gamma dgamma partials (from D2, which holds M^T [s gamma dY ; -gamma dX]^T until
     //     step (9)) and the dr partials (from D3, kept for dk), with q_t, k_t of this
-    //     thread's tokens read from the [Q^T | K^T] tile (hi + lo is exact); then
+    //     thread's tokens read from the [Q^T | K^T] tile (bf16 hi + lo: 16 significant bits); then
     //     A = [dY ; dDelta ; 0] (rows t)
     float d3[16];
     if (compute) {
@@ -457,22 +460,29 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             tc::ld16(tc::taddr(tmem, warp, kC2 + BC + tb), dk);
             tc::ld16(tc::taddr(tmem, warp, kC3 + tb), d3);
             tc::wait_ld();
-            const float* qkt = sm + kR2 + 4 * row;  // element (row, t) at (t / 4) 512 + t % 4
-            constexpr int kLo = 2 * BC * TD;        // lo half of the tile
+            // the bf16 [Q^T | K^T] tile: 16-byte unit kc * 128 + row holds t' = 8 kc .. 8 kc + 7
+            const uint4* qkt = reinterpret_cast<const uint4*>(sm + kR2) + row;
+            constexpr int kLo = BC * TD / 4;  // lo half of the tile, in 16-byte units
+            auto lo16 = [](uint32_t w) { return __uint_as_float(w << 16); };
+            auto hi16 = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int u = (tb >> 2) + b;
-                const float4 qh = *reinterpret_cast<const float4*>(qkt + u * 4 * TD);
-                const float4 ql = *reinterpret_cast<const float4*>(qkt + kLo + u * 4 * TD);
-                const float4 kh = *reinterpret_cast<const float4*>(qkt + (BC / 4 + u) * 4 * TD);
-                const float4 kl = *reinterpret_cast<const float4*>(qkt + kLo + (BC / 4 + u) * 4 * TD);
-                const float qv[4] = {__fadd_rn(qh.x, ql.x), __fadd_rn(qh.y, ql.y), __fadd_rn(qh.z, ql.z),
-                                     __fadd_rn(qh.w, ql.w)};
-                const float kv[4] = {__fadd_rn(kh.x, kl.x), __fadd_rn(kh.y, kl.y), __fadd_rn(kh.z, kl.z),
-                                     __fadd_rn(kh.w, kl.w)};
+            for (int cq = 0; cq < 2; ++cq) {
+                const int kq = (tb >> 3) + cq, kk = BC / 8 + kq;
+                const uint4 qh = qkt[kq * TD], ql = qkt[kLo + kq * TD];
+                const uint4 kh = qkt[kk * TD], kl = qkt[kLo + kk * TD];
+                const uint32_t qhw[4] = {qh.x, qh.y, qh.z, qh.w}, qlw[4] = {ql.x, ql.y, ql.z, ql.w};
+                const uint32_t khw[4] = {kh.x, kh.y, kh.z, kh.w}, klw[4] = {kl.x, kl.y, kl.z, kl.w};
+                float qv[8], kv[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int x = 4 * b + e;
+                for (int w = 0; w < 4; ++w) {
+                    qv[2 * w] = __fadd_rn(lo16(qhw[w]), lo16(qlw[w]));
+                    qv[2 * w + 1] = __fadd_rn(hi16(qhw[w]), hi16(qlw[w]));
+                    kv[2 * w] = __fadd_rn(lo16(khw[w]), lo16(klw[w]));
+                    kv[2 * w + 1] = __fadd_rn(hi16(khw[w]), hi16(klw[w]));
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int x = 8 * cq + e;
                     const float g1 = warp_sum(__fmaf_rn(kv[e], dk[x], __fmul_rn(qv[e], dq[x])));
                     const float g2 = warp_sum(__fmul_rn(kv[e], d3[x]));
                     if (lane == 0) {
@@ -663,9 +673,9 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         for (int idx = tid; idx < BC * BC; idx += 256) {
             const int t = idx & 31, tau = idx >> 5;  // consecutive threads: consecutive rows t
             const float s = (tau > t) ? Ss[tau * LDF + t] : (tau < t ? Ss[t * LDF + tau] : 0.f);
-            put_split(bp, kTP, padoff(t, tau, kLbo32 / 4), Ps[t * LDF + tau]);
-            put_split(bps, kTPS, padoff(t, tau, kLbo32 / 4), Ps[tau * LDF + t]);
-            put_split(bps, kTPS, padoff(t, BC + tau, kLbo32 / 4), s);
+            put_split16(bp, padoff16(t, tau, kLbo32), Ps[t * LDF + tau], kTP);
+            put_split16(bps, padoff16(t, tau, kLbo32), Ps[tau * LDF + t], kTPS);
+            put_split16(bps, padoff16(t, BC + tau, kLbo32), s, kTPS);
         }
     }
     tc::fence_async_smem();
@@ -676,29 +686,29 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         tc::fence_after();
         if (!tc::mbar_wait(bar_qkt, 0)) s_err = 1;
         if (!s_err) {
-            const uint64_t qhi = tc::tile_desc(sm + kR2, TD), qlo = tc::tile_desc(sm + kR2 + 2 * BC * TD, TD);
-            const uint32_t id32 = tc::idesc_tf32(32);
-            // dq part: A = K^T (k-slices 4..7 of [Q^T | K^T]), B = P
+            const uint64_t qhi = tc::tile_desc(sm + kR2, TD), qlo = tc::tile_desc(sm + kR2 + BC * TD, TD);
+            const uint32_t id32 = tc::idesc_bf16(32);
+            // dq part: A = K^T (k-slices 2, 3 of the bf16 [Q^T | K^T]), B = P
             const uint64_t phi = tc::make_desc(tc::smem_addr(sm + kABP), kLbo32, 128);
             const uint64_t plo = tc::make_desc(tc::smem_addr(sm + kABP + kTP), kLbo32, 128);
 #pragma unroll
-            for (int s = 0; s < BC / 8; ++s) {
-                const uint64_t a_h = tc::desc_kslice(qhi, TD, s + BC / 8), a_l = tc::desc_kslice(qlo, TD, s + BC / 8);
+            for (int s = 0; s < BC / 16; ++s) {
+                const uint64_t a_h = tc::desc_kslice(qhi, TD, s + BC / 16), a_l = tc::desc_kslice(qlo, TD, s + BC / 16);
                 const uint64_t off = (uint64_t)((2 * kLbo32 * s) >> 4);
-                tc::mma_ss(tmem + kC2, a_h, phi + off, id32, 1);
-                tc::mma_ss(tmem + kC2, a_h, plo + off, id32, 1);
-                tc::mma_ss(tmem + kC2, a_l, phi + off, id32, 1);
+                tc::mma_ss16(tmem + kC2, a_h, phi + off, id32, 1);
+                tc::mma_ss16(tmem + kC2, a_h, plo + off, id32, 1);
+                tc::mma_ss16(tmem + kC2, a_l, phi + off, id32, 1);
             }
             // dk part: A = [Q^T | K^T], B = [P ; S]^T
             const uint64_t shi = tc::make_desc(tc::smem_addr(sm + kABPS), kLbo32, 128);
             const uint64_t slo = tc::make_desc(tc::smem_addr(sm + kABPS + kTPS), kLbo32, 128);
 #pragma unroll
-            for (int s = 0; s < 2 * BC / 8; ++s) {
+            for (int s = 0; s < 2 * BC / 16; ++s) {
                 const uint64_t a_h = tc::desc_kslice(qhi, TD, s), a_l = tc::desc_kslice(qlo, TD, s);
                 const uint64_t off = (uint64_t)((2 * kLbo32 * s) >> 4);
-                tc::mma_ss(tmem + kC2 + BC, a_h, shi + off, id32, 1);
-                tc::mma_ss(tmem + kC2 + BC, a_h, slo + off, id32, 1);
-                tc::mma_ss(tmem + kC2 + BC, a_l, shi + off, id32, 1);
+                tc::mma_ss16(tmem + kC2 + BC, a_h, shi + off, id32, 1);
+                tc::mma_ss16(tmem + kC2 + BC, a_h, slo + off, id32, 1);
+                tc::mma_ss16(tmem + kC2 + BC, a_l, shi + off, id32, 1);
             }
             tc::commit(bar_mma);
         }
