@@ -299,7 +299,7 @@ int gdn::acquire_pipeline(gdn::Pipeline** out)
         if (!e) e = (int)cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, middle);
         if (!e) e = (int)cudaStreamCreateWithPriority(&bg, cudaStreamNonBlocking, least);
         if (!e) e = (int)cudaStreamCreateWithPriority(&rc, cudaStreamNonBlocking, middle);
-        constexpr int kEv = 5 + 4 * gdn::kMaxRanges;
+        constexpr int kEv = 5 + 5 * gdn::kMaxRanges;
         cudaEvent_t ev[kEv] = {};
         for (int i = 0; i < kEv && !e; ++i)
             e = (int)cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
@@ -321,6 +321,7 @@ int gdn::acquire_pipeline(gdn::Pipeline** out)
             P.chain_go[i] = ev[5 + gdn::kMaxRanges + i];
             P.ds_done[i] = ev[5 + 2 * gdn::kMaxRanges + i];
             P.rc_done[i] = ev[5 + 3 * gdn::kMaxRanges + i];
+            P.grad_done[i] = ev[5 + 4 * gdn::kMaxRanges + i];
         }
         g_pipe_ready[dev] = true;
     }

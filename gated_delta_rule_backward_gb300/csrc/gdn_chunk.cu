@@ -1460,12 +1460,20 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
             if (!e) e = (int)cudaStreamWaitEvent(bg, (cudaEvent_t)P->rc_done[r], 0);
             if (!e) e = (int)cudaStreamWaitEvent(bg, (cudaEvent_t)P->ds_done[r], 0);
             if (!e) e = launch_tc_grad(ar, bg);
-            if (!e) e = launch_tc_dqdk_sum(ar, bg);
+            if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->grad_done[r], bg);
         }
         if (!e && i + 1 < nr) {
             e = (int)cudaStreamWaitEvent(lo, (cudaEvent_t)P->chain_go[r], 0);
             if (!e) e = prep(order[i + 1]);
         }
+    }
+    // the value-head sums on the prep stream, after its last prep: a range's sum runs beside
+    // the next range's gradient step instead of ahead of it on the gradient stream
+    for (int i = 0; i < nr && !e && backward && !staged; ++i) {
+        ChunkArgs ar;
+        range_of(a, R, backward, order[i], ar);
+        e = (int)cudaStreamWaitEvent(lo, (cudaEvent_t)P->grad_done[order[i]], 0);
+        if (!e) e = launch_tc_dqdk_sum(ar, lo);
     }
     if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_hi, hi);
     if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_lo, lo);

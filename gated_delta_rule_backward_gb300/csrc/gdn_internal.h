@@ -121,8 +121,9 @@ struct EventTap {
 };
 
 // Library streams of one device for the pipelined tensor-core path: the serial chains on
-// a high-priority stream, the chunk-range preps on a middle one, and (backward) the
-// recompute, gradient and sum kernels on a low one.  Created on first use; the lock
+// a high-priority stream, the chunk-range preps (then, backward, the value-head sums) on a
+// middle one, the recompute on another middle one and the gradient steps on a low one.
+// Created on first use; the lock
 // serialises the enqueueing of calls that use them.
 constexpr int kMaxRanges = 4;
 struct Pipeline {
@@ -139,6 +140,7 @@ struct Pipeline {
     void* chain_go[kMaxRanges];
     void* ds_done[kMaxRanges];
     void* rc_done[kMaxRanges];
+    void* grad_done[kMaxRanges];
 };
 // Returns the current device's pipeline (creating it on first use) with its lock held;
 // release_pipeline() unlocks.  Returns a cudaError_t as int.
