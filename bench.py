@@ -120,15 +120,26 @@ def hbm_peak_gbs():
         return 6800.0, "fallback 6.8 TB/s"
 
 
-def tensor_peak_tflops():
-    """3xTF32 fp32-equivalent peak: measured bf16 x (1.1 / 2.25) / 3, and where it came from."""
+# Share of the gradient step's tensor-core multiply-adds done in kind::tf32 (the first part of
+# D2, 128 x 64 x 128 of the 3,538,944 per (chunk, value head)); the rest is bf16 (kind::f16).
+GRAD_TF32_SHARE = 128 * 64 * 128 / 3538944
+
+
+def tensor_peak_tflops(tf32_share=GRAD_TF32_SHARE):
+    """fp32-equivalent peak of three-pass split products, tf32_share of them in tf32 and the
+    rest in bf16: measured bf16 / 3 for the bf16 passes, x nominal tf32/bf16 (1.1 / 2.25) for
+    the tf32 ones, combined by time per flop; and where it came from."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         bf16 = float(json.load(open(path))["bf16_tflops"])
         src = "measured bf16 burst"
     except (OSError, KeyError, ValueError):
         bf16, src = 1900.0, "fallback bf16 1.9 PFLOP/s"
-    return bf16 * (1.1 / 2.25) / 3.0, src + " x nominal tf32/bf16 (1.1/2.25) / 3 passes"
+    p_bf16 = bf16 / 3.0
+    p_tf32 = bf16 * (1.1 / 2.25) / 3.0
+    peak = 1.0 / (tf32_share / p_tf32 + (1.0 - tf32_share) / p_bf16)
+    return peak, (src + " / 3 passes, %.0f %% of the flops at the nominal tf32/bf16 rate (1.1/2.25)"
+                  % (100 * tf32_share))
 
 
 def _args():
