@@ -69,8 +69,8 @@ constexpr int kSU = kSB23 + kTcB23Elems;           // U^T, operand layout (R = 1
 constexpr int kSDel = kSU + BC * TD;               // staging of checkpoint rows (32 x kStageLd)
 constexpr int kSGam = kSDel + 2 * BC * TD;         // gamma (32)
 constexpr int kStageLd = TD + 4;                   // staging rows for coalesced global writes
-constexpr int kSY = kSGam + BC;                    // y of the chunk, rows t (forward)
-constexpr int kSFloats = kSY + BC * kStageLd;
+constexpr int kSY = kSGam + BC;                    // y of two chunks, rows t (forward)
+constexpr int kSFloats = kSY + 2 * BC * kStageLd;
 constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 128;  // + barriers (6 used)
 
 constexpr uint32_t kB1Bytes = sizeof(float) * (kTcWElems + kTcQElems);
@@ -186,23 +186,23 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         for (int q = 0; q < 16; ++q)
             d4[(16 * hc + q) * TD + j] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
     };
-    // y of a chunk is assembled in shared memory (rows t) by the column-half 1 threads: the Q
-    // part in (3), the QD Delta part added in (5); it goes to global memory while the next
-    // chunk's D1 runs
+    // y of a chunk is assembled in shared memory (rows t, one of two buffers by chunk parity)
+    // by the column-half 1 threads: the Q part in (3), the QD Delta part added in (5).  It
+    // goes to global memory during the next chunk's D23, when the compute warps would only
+    // wait (the buffer is next written two chunks later, after the CTA barrier of (5)).
     int y_t0 = 0, y_nb = 0;
+    const float* y_buf = sm + kSY;  // the buffer of the chunk whose y is pending
     float* stage = sm + kSDel;   // idle while D1 runs: 32 rows of kStageLd floats (checkpoints)
-    float* sY = sm + kSY;
     const int ctid = tid;        // 0..255 for the compute warps
     auto store_y = [&]() {       // the global writes are whole 512-byte rows
-        tc::bar_sync_first(256);
+        tc::bar_sync_first(256);  // the column-half 1 threads' adds to y_buf are complete
         float* yp = A.y + (((long long)n * A.T + y_t0) * A.H_v + h) * TD;
         const long long ys = (long long)A.H_v * TD;
         for (int idx = ctid; idx < y_nb * (TD / 4); idx += 256) {
             const int t = idx / (TD / 4), q = idx - t * (TD / 4);
             *reinterpret_cast<float4*>(yp + t * ys + 4 * q) =
-                *reinterpret_cast<const float4*>(sY + t * kStageLd + 4 * q);
+                *reinterpret_cast<const float4*>(y_buf + t * kStageLd + 4 * q);
         }
-        tc::bar_sync_first(256);
     };
     auto store_ckpt = [&](float* dst) {  // row-major M through `stage`, 32 rows at a time
 #pragma unroll 1
@@ -259,9 +259,10 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         const int t0 = seg * A.C + loc * BC;
         const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
         const long long ch = head * A.n_chunks + c;
+        float* sY = sm + kSY + (c & 1) * (BC * kStageLd);  // this chunk's y (forward)
         // (1) M (bf16 hi/lo, the A operand of D1) goes into TMEM slice by slice (release_group)
         // (2) D1 = M [W; Q]^T on the tensor cores, each k-slice issued as soon as its columns of
-        //     M are in TMEM; meanwhile the pending global stores
+        //     M are in TMEM; meanwhile the checkpoint (forward) or the parked state (recompute)
         const uint32_t ph_a = (uint32_t)(c - c_begin) & 1u;
         if (issuer) {
             if (!tc::mbar_wait(bar_b1, ph_b1)) atomicOr(&s_err, kWCopyA);
@@ -291,7 +292,6 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 if (!s_err) tc::commit(bar_mma);
             }
         } else if (compute) {
-            if (FWD && y_nb > 0) store_y();
             if (FWD && loc == 0) store_ckpt(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
             if (!FWD && c > c_begin) park_state(A.ws + A.o_Mc + ch * (long long)(TD * TD));
         }
@@ -346,6 +346,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
 #pragma unroll
                 for (int t = 0; t < BC; ++t) sY[t * kStageLd + j] = __fmul_rn(__fmul_rn(A.scale, sGam[t]), x[t]);
             }
+            if (FWD && y_nb > 0) store_y();  // the previous chunk's y, while D23 runs
         }
         ph_b23 ^= 1;
         if (!ok) atomicOr(&s_err, kWMma1);
@@ -394,6 +395,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 }
                 y_t0 = t0;
                 y_nb = nb;
+                y_buf = sY;
             }
             // M <- gamma_last M + D23[:, 32:160], split at once into the next D1's A operand and
             // released to the issuer in two column groups
