@@ -78,7 +78,7 @@ def kernel_plan(chunked, d, n_bwd, cps):
     if d == 128:  # forward: chunk-range preps pipelined with the state chain; backward, as
         # timed stage by stage (its calls with timing events run the stages in sequence)
         fwd = [("gdn_chunk_prep_kernel + gdn_tc_state_kernel (pipelined)", "fwd_pipe")]
-        bwd = [("gdn_chunk_prep_kernel + gdn_tc_bwd_chains_kernel", "bwd_pipe"),
+        bwd = [("gdn_chunk_prep_kernel + gdn_tc_dstate_kernel", "bwd_pipe"),
                ("gdn_tc_grad_kernel", "grad_tc"), ("gdn_tc_dqdk_sum_kernel", "dqdk_sum")]
         return fwd, bwd
     fwd = [("gdn_chunk_prep_kernel", "prep_fwd"), ("gdn_chunk_state_kernel", "state_fwd")]

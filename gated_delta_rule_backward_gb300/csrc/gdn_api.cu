@@ -252,6 +252,7 @@ void fill_chunk_common(gdn::ChunkArgs& c, const gdn_params_t* p, const Plan& pl)
     c.want_tc = pl.tensor;
     c.c_lo = 0;
     c.c_hi = (int)pl.n_chunks;
+    c.grad_loc = -1;
 }
 
 // Chunk ranges the pipelined tensor-core path launches (non-empty ones).
@@ -264,6 +265,26 @@ int tc_ranges(const Plan& pl, bool backward)
         gdn::range_segments((int)pl.n_ck, R, backward, r, &s_lo, &s_hi);
         if (std::min<int64_t>(pl.n_chunks, (int64_t)s_hi * pl.cps) > std::min<int64_t>(pl.n_chunks, (int64_t)s_lo * pl.cps))
             ++n;
+    }
+    return n;
+}
+
+// Kernels of a tensor-core backward call: per non-empty range the prep, the dM chain, one
+// gradient launch per place in a segment that has chunks there, and the sum.
+int tc_backward_launches(const Plan& pl)
+{
+    const int R = gdn::pipeline_ranges((int)pl.n_ck, true);
+    int n = 0;
+    for (int r = 0; r < R; ++r) {
+        int s_lo = 0, s_hi = 0;
+        gdn::range_segments((int)pl.n_ck, R, true, r, &s_lo, &s_hi);
+        gdn::ChunkArgs a{};
+        a.cps = pl.cps;
+        a.c_lo = (int)std::min<int64_t>(pl.n_chunks, (int64_t)s_lo * pl.cps);
+        a.c_hi = (int)std::min<int64_t>(pl.n_chunks, (int64_t)s_hi * pl.cps);
+        if (a.c_hi <= a.c_lo) continue;
+        n += 3;
+        for (a.grad_loc = 0; a.grad_loc < pl.cps; ++a.grad_loc) n += gdn::tc_grad_units(a) > 0 ? 1 : 0;
     }
     return n;
 }
@@ -294,12 +315,11 @@ int gdn::acquire_pipeline(gdn::Pipeline** out)
         e = (int)cudaDeviceGetStreamPriorityRange(&least, &greatest);
         // numerically lower is more urgent; the middle level falls back to the lowest
         const int middle = greatest + 1 < least ? greatest + 1 : least;
-        cudaStream_t hi = nullptr, lo = nullptr, bg = nullptr, rc = nullptr;
+        cudaStream_t hi = nullptr, lo = nullptr, bg = nullptr;
         if (!e) e = (int)cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest);
         if (!e) e = (int)cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, middle);
         if (!e) e = (int)cudaStreamCreateWithPriority(&bg, cudaStreamNonBlocking, least);
-        if (!e) e = (int)cudaStreamCreateWithPriority(&rc, cudaStreamNonBlocking, middle);
-        constexpr int kEv = 5 + 5 * gdn::kMaxRanges;
+        constexpr int kEv = 4 + 4 * gdn::kMaxRanges;
         cudaEvent_t ev[kEv] = {};
         for (int i = 0; i < kEv && !e; ++i)
             e = (int)cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
@@ -310,18 +330,15 @@ int gdn::acquire_pipeline(gdn::Pipeline** out)
         P.hi = hi;
         P.lo = lo;
         P.bg = bg;
-        P.rc = rc;
         P.fork = ev[0];
         P.join_hi = ev[1];
         P.join_lo = ev[2];
         P.join_bg = ev[3];
-        P.join_rc = ev[4];
         for (int i = 0; i < gdn::kMaxRanges; ++i) {
-            P.prep_done[i] = ev[5 + i];
-            P.chain_go[i] = ev[5 + gdn::kMaxRanges + i];
-            P.ds_done[i] = ev[5 + 2 * gdn::kMaxRanges + i];
-            P.rc_done[i] = ev[5 + 3 * gdn::kMaxRanges + i];
-            P.grad_done[i] = ev[5 + 4 * gdn::kMaxRanges + i];
+            P.prep_done[i] = ev[4 + i];
+            P.chain_go[i] = ev[4 + gdn::kMaxRanges + i];
+            P.ds_done[i] = ev[4 + 2 * gdn::kMaxRanges + i];
+            P.grad_done[i] = ev[4 + 3 * gdn::kMaxRanges + i];
         }
         g_pipe_ready[dev] = true;
     }
@@ -436,10 +453,10 @@ int gdn_backward_launches(const gdn_params_t* p)
     if (check_sizes(p) != GDN_OK) return 0;
     if (p->n_seq == 0) return 0;
     const Plan pl = make_plan(p);
-    // chunked: prep, [recompute], dM chain, gradients; on the tensor-core path, per chunk
-    // range: prep, dM chain, [recompute,] gradient step and sum over value heads (a call
-    // with timing events: prep, both chains, gradient step, sum, i.e. 4)
-    if (pl.chunked) return pl.tensor ? tc_ranges(pl, true) * (pl.cps > 1 ? 5 : 4) : (pl.cps > 1 ? 4 : 3);
+    // chunked: prep, [recompute], dM chain, gradients.  On the tensor-core path, per chunk
+    // range: prep, dM chain, a gradient launch per place in a segment, and the sum over value
+    // heads (a call with timing events runs the same kernels as one range).
+    if (pl.chunked) return pl.tensor ? tc_backward_launches(pl) : (pl.cps > 1 ? 4 : 3);
     return p->T > 0 ? 2 : 1;
 }
 
@@ -610,7 +627,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
         c.dg = packed + off[3]; c.dbeta = packed + off[4]; c.dstate0 = packed + off[5];
         fill_chunk_common(c, p, pl);
         c.carry = pl.tensor ? c.ws + pl.o_carry_b : nullptr;
-        c.want_wu = pl.cps > 1;
+        c.want_wu = pl.cps > 1 && !pl.tensor;  // the tensor-core gradient parks the states itself
         c.want_factors = 1;
         c.vec_q = vec_ok(q, p->q_s); c.vec_k = vec_ok(k, p->k_s); c.vec_v = vec_ok(v, p->v_s);
         c.vec_gy = vec_ok(gy, p->gy_s);

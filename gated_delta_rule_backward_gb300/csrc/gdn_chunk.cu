@@ -1413,13 +1413,25 @@ static int launch_prep_range(const ChunkArgs& a, int R, bool backward, int r, cu
 // so that the gradient work of one range runs while the chain walks the next.  With timing
 // events set, the backward instead runs its stages one after another as a single range
 // (prep, both chains, gradient step, sum), each between two events.
+// The gradient launches of a chunk range: one per place in a segment, in order, each
+// parking the entry states of the next place's chunks (launch_tc_grad).
+static int launch_grads(const ChunkArgs& ar, cudaStream_t st)
+{
+    ChunkArgs g = ar;
+    int e = 0;
+    for (int k = 0; k < ar.cps && !e; ++k) {
+        g.grad_loc = k;
+        e = launch_tc_grad(g, st);
+    }
+    return e;
+}
+
 static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, EventTap& tap)
 {
     Pipeline* P = nullptr;
     int e = acquire_pipeline(&P);
     if (e) return e;
     const cudaStream_t hi = (cudaStream_t)P->hi, lo = (cudaStream_t)P->lo, bg = (cudaStream_t)P->bg;
-    const cudaStream_t rc = (cudaStream_t)P->rc;
     const bool staged = backward && tap.ev != nullptr;
     const int R = staged ? 1 : pipeline_ranges(a.n_ck, backward);
     tap.mark(user);
@@ -1427,7 +1439,6 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
     if (!e) e = (int)cudaStreamWaitEvent(lo, (cudaEvent_t)P->fork, 0);
     if (!e) e = (int)cudaStreamWaitEvent(hi, (cudaEvent_t)P->fork, 0);
     if (!e && backward && !staged) e = (int)cudaStreamWaitEvent(bg, (cudaEvent_t)P->fork, 0);
-    if (!e && backward && !staged) e = (int)cudaStreamWaitEvent(rc, (cudaEvent_t)P->fork, 0);
     int order[kMaxRanges], nr = 0;
     for (int i = 0; i < R; ++i) {
         const int r = backward ? R - 1 - i : i;
@@ -1449,17 +1460,12 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
         if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->chain_go[r], hi);
         if (!e) {
             if (!backward) e = launch_tc_state(ar, hi);
-            else if (staged) e = launch_tc_bwd_chains(ar, hi);
             else e = launch_tc_dstate(ar, hi);
         }
         if (!e && backward && !staged) {
             e = (int)cudaEventRecord((cudaEvent_t)P->ds_done[r], hi);
-            if (!e) e = (int)cudaStreamWaitEvent(rc, (cudaEvent_t)P->prep_done[r], 0);
-            if (!e) e = launch_tc_recompute(ar, rc);
-            if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->rc_done[r], rc);
-            if (!e) e = (int)cudaStreamWaitEvent(bg, (cudaEvent_t)P->rc_done[r], 0);
             if (!e) e = (int)cudaStreamWaitEvent(bg, (cudaEvent_t)P->ds_done[r], 0);
-            if (!e) e = launch_tc_grad(ar, bg);
+            if (!e) e = launch_grads(ar, bg);
             if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->grad_done[r], bg);
         }
         if (!e && i + 1 < nr) {
@@ -1482,14 +1488,12 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
     if (!e && backward && !staged) {
         e = (int)cudaEventRecord((cudaEvent_t)P->join_bg, bg);
         if (!e) e = (int)cudaStreamWaitEvent(user, (cudaEvent_t)P->join_bg, 0);
-        if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_rc, rc);
-        if (!e) e = (int)cudaStreamWaitEvent(user, (cudaEvent_t)P->join_rc, 0);
     }
     release_pipeline();
     if (e) return e;
     tap.mark(user);
     if (!staged) return 0;
-    e = launch_tc_grad(a, user);
+    e = launch_grads(a, user);
     if (e) return e;
     tap.mark(user);
     e = launch_tc_dqdk_sum(a, user);

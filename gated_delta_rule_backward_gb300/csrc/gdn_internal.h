@@ -107,6 +107,8 @@ struct ChunkArgs {
     int want_factors;
     int want_tc;                            // head size 128: state chain on the tensor cores
     int c_lo, c_hi;                         // chunk range of this launch (prep and chains)
+    int grad_loc;                           // gradient launch: -1 for every chunk of [c_lo, c_hi),
+                                            // else only the chunks at this place in their segment
     float* carry;                           // [N][H_v][D][D] state (or dM) between ranges
     int vec_q, vec_k, vec_v, vec_gy;
 };
@@ -122,24 +124,20 @@ struct EventTap {
 
 // Library streams of one device for the pipelined tensor-core path: the serial chains on
 // a high-priority stream, the chunk-range preps (then, backward, the value-head sums) on a
-// middle one, the recompute on another middle one and the gradient steps on a low one.
-// Created on first use; the lock
+// middle one and the gradient steps on a low one.  Created on first use; the lock
 // serialises the enqueueing of calls that use them.
 constexpr int kMaxRanges = 4;
 struct Pipeline {
     void* hi;
     void* lo;
     void* bg;
-    void* rc;
     void* fork;
     void* join_hi;
     void* join_lo;
     void* join_bg;
-    void* join_rc;
     void* prep_done[kMaxRanges];
     void* chain_go[kMaxRanges];
     void* ds_done[kMaxRanges];
-    void* rc_done[kMaxRanges];
     void* grad_done[kMaxRanges];
 };
 // Returns the current device's pipeline (creating it on first use) with its lock held;
@@ -179,16 +177,18 @@ constexpr int kDsGam = kDsR + 32;
 constexpr int kTcDsElems = kDsGam + 32;
 
 int launch_chunk_forward(const ChunkArgs& a, int D, void* stream, EventTap& tap);
-// The chains on the tensor cores (gdn_tc_chain.cu): the forward's state chain, and the
-// backward's dM chain together with the recompute of the chunk-entry states.
+// The chains on the tensor cores (gdn_tc_chain.cu): the forward's state chain and the
+// backward's dM chain over [c_lo, c_hi).
 int launch_tc_state(const ChunkArgs& a, void* stream);
-int launch_tc_bwd_chains(const ChunkArgs& a, void* stream);  // dM chain + recompute
-int launch_tc_dstate(const ChunkArgs& a, void* stream);      // dM chain over [c_lo, c_hi)
-int launch_tc_recompute(const ChunkArgs& a, void* stream);   // states of its segments
+int launch_tc_dstate(const ChunkArgs& a, void* stream);
 // The gradient step on the tensor cores (gdn_tc_grad.cu): per (chunk, value head) every
 // gradient of the chunk (dv, dg, dbeta written; this value head's dq, dk parked row-major
 // [t][i] at o_dqM, o_dkM), then the sum of the value heads of each key head.
+// With grad_loc = k >= 0 a launch covers the chunks at place k of the segments of
+// [c_lo, c_hi) and parks the entry state of each one's successor in its segment (the
+// launch for k + 1 reads it), so the launches for k = 0, 1, .. run in order.
 int launch_tc_grad(const ChunkArgs& a, void* stream);
+int tc_grad_units(const ChunkArgs& a);  // the launch's chunks per (value head, sequence)
 int launch_tc_dqdk_sum(const ChunkArgs& a, void* stream);
 int tc_grad_take_status(void* stream, int* status);
 // Reads and clears the tensor-core kernels' device status word (0 or GDN_ERR_TIMEOUT),

@@ -759,23 +759,11 @@ __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
     state_chain<true>(A, sm, blockIdx.x, blockIdx.y);
 }
 
-// The backward's two chains in one launch, as they are independent: CTAs [0, N H_v) run
-// the dM chain of one head each (long, serial); the rest, when segments hold several
-// chunks, rebuild the chunk-entry states of one (segment, head) each on the other SMs.
-// CTAs [0, nds) run the dM chain of one head each (nds = N H_v, or 0 for a launch of the
-// recompute alone); the rest recompute segments.
-__global__ void __launch_bounds__(TCT, 1) gdn_tc_bwd_chains_kernel(const ChunkArgs A, int nds)
+// The backward's dM chain: one CTA per (value head, sequence), over the chunks [c_lo, c_hi).
+__global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A)
 {
     extern __shared__ __align__(1024) float sm[];
-    const int b = blockIdx.x;
-    if (b < nds) {
-        dstate_chain(A, sm, b % A.H_v, b / A.H_v);
-        return;
-    }
-    // recompute CTAs: the segments whose chunks lie in [c_lo, c_hi)
-    const int s_lo = A.c_lo / A.cps, s_hi = (A.c_hi + A.cps - 1) / A.cps;
-    const int r = b - nds;
-    state_chain<false>(A, sm, s_lo + r % (s_hi - s_lo), r / (s_hi - s_lo));
+    dstate_chain(A, sm, blockIdx.x, blockIdx.y);
 }
 
 int launch_tc_state(const ChunkArgs& a, void* stream)
@@ -788,44 +776,13 @@ int launch_tc_state(const ChunkArgs& a, void* stream)
     return (int)cudaGetLastError();
 }
 
-int launch_tc_bwd_chains(const ChunkArgs& a, void* stream)
-{
-    cudaStream_t s = (cudaStream_t)stream;
-    const size_t bytes = kSmemBytes > kDsSmemBytes ? kSmemBytes : kDsSmemBytes;
-    int e = (int)cudaFuncSetAttribute(gdn_tc_bwd_chains_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)bytes);
-    if (e) return e;
-    const long long nds = (long long)a.N * a.H_v;
-    const int s_lo = a.c_lo / a.cps, s_hi = (a.c_hi + a.cps - 1) / a.cps;
-    const long long nrc = a.cps > 1 ? (long long)(s_hi - s_lo) * nds : 0;
-    gdn_tc_bwd_chains_kernel<<<(unsigned)(nds + nrc), TCT, bytes, s>>>(a, (int)nds);
-    return (int)cudaGetLastError();
-}
-
 int launch_tc_dstate(const ChunkArgs& a, void* stream)
 {
     cudaStream_t s = (cudaStream_t)stream;
-    const size_t bytes = kSmemBytes > kDsSmemBytes ? kSmemBytes : kDsSmemBytes;
-    int e = (int)cudaFuncSetAttribute(gdn_tc_bwd_chains_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)bytes);
+    int e = (int)cudaFuncSetAttribute(gdn_tc_dstate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kDsSmemBytes);
     if (e) return e;
-    const int nds = a.N * a.H_v;
-    gdn_tc_bwd_chains_kernel<<<(unsigned)nds, TCT, bytes, s>>>(a, nds);
-    return (int)cudaGetLastError();
-}
-
-int launch_tc_recompute(const ChunkArgs& a, void* stream)
-{
-    if (a.cps <= 1) return 0;  // every chunk starts a segment: nothing to rebuild
-    cudaStream_t s = (cudaStream_t)stream;
-    const size_t bytes = kSmemBytes > kDsSmemBytes ? kSmemBytes : kDsSmemBytes;
-    int e = (int)cudaFuncSetAttribute(gdn_tc_bwd_chains_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)bytes);
-    if (e) return e;
-    const int s_lo = a.c_lo / a.cps, s_hi = (a.c_hi + a.cps - 1) / a.cps;
-    const long long nrc = (long long)(s_hi - s_lo) * a.N * a.H_v;
-    if (nrc <= 0) return 0;
-    gdn_tc_bwd_chains_kernel<<<(unsigned)nrc, TCT, bytes, s>>>(a, 0);
+    gdn_tc_dstate_kernel<<<dim3(a.H_v, a.N), TCT, kDsSmemBytes, s>>>(a);
     return (int)cudaGetLastError();
 }
 

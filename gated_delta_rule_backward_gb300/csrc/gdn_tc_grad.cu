@@ -42,6 +42,8 @@ constexpr uint32_t kCX = 256;     //       D_X (32)
 constexpr uint32_t kC2 = 288;     //       D2  (64: dq part, dk part)
 constexpr uint32_t kC3 = 352;     //       D3  (32)
 constexpr uint32_t kC4 = 384;     //       D4  (64)
+constexpr uint32_t kCN = 128;     //       D_N = (r Delta)^T K (128, once M^T is dead)
+constexpr uint32_t kCNA = 448;    //       its bf16 A operand (r Delta)^T: hi 448.., lo 464..
 constexpr uint32_t kCols = 512;
 constexpr int kStatusTimeout = 6;
 constexpr int LDF = BC + 4;       // leading dimension of the 32 x 32 fp32 tiles
@@ -180,7 +182,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     const int row = 32 * (warp & 3) + lane;  // this thread's TMEM lane
     const int hc = (warp >> 2) & 1;          // half: 64 of the K columns, 16 of the 32 tokens
     const int tb = 16 * hc;                  // this thread's tokens [tb, tb + 16)
-    const int c = A.c_lo + blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int c = A.grad_loc < 0 ? A.c_lo + blockIdx.x : (A.c_lo / A.cps + blockIdx.x) * A.cps + A.grad_loc;
+    const int h = blockIdx.y, n = blockIdx.z;
     const int hk = h % A.H_k;
     const long long head = (long long)n * A.H_v + h;
     const long long ch = head * A.n_chunks + c;
@@ -189,6 +192,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     const int t0 = seg * A.C + loc * BC;
     const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
     const long long tok0 = (long long)n * A.T + t0;
+    // the next chunk of this segment takes its entry state from this CTA (M_N below)
+    const bool park_next = A.grad_loc >= 0 && t0 + BC < min(A.T, seg * A.C + A.C);
 
     if (tid == 0) {
         tc::mbar_init(bar_ld, 1);
@@ -363,6 +368,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
 #pragma unroll
         for (int t = 0; t < BC; ++t) x[t] = __fsub_rn(vx[t], __fmul_rn(sGam[t], x[t]));
         float* b34 = sm + kR0;  // the K tile is dead: D_X is done
+        float rd[16];           // r (.) Delta, row `row`, this thread's tokens
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int t = tb + e;
@@ -371,8 +377,16 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             for (int k = 0; k < BC; ++k) acc = __fmaf_rn(sT[t * BC + k], x[k], acc);
             put_split16(b34, padoff16(t, row), acc);
             put_split16(b34, padoff16(BC + t, row), hc ? x[16 + e] : x[e]);
+            rd[e] = __fmul_rn(sR[t], acc);
         }
         tc::fence_async_smem();  // the tile is read by the tensor cores from (5) on
+        if (park_next) {  // (r Delta)^T, rows j, K = t: the bf16 A operand of M_N
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tc::split_bf16x2(rd[2 * e], rd[2 * e + 1], hi[e], lo[e]);
+            tc::st8(tc::taddr(tmem, warp, kCNA + 8 * hc), hi);
+            tc::st8(tc::taddr(tmem, warp, kCNA + 16 + 8 * hc), lo);
+        }
     }
     ok = tc::mbar_wait(bar_mma, ph);
     ph ^= 1;
@@ -710,6 +724,16 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                 tc::mma_ss16(tmem + kC2 + BC, a_h, slo + off, id32, 1);
                 tc::mma_ss16(tmem + kC2 + BC, a_l, shi + off, id32, 1);
             }
+            if (park_next) {  // M_N = (r Delta)^T K, K from the k-slices 2, 3 of [Q^T | K^T]
+                const uint32_t id128 = tc::idesc_bf16(128);
+#pragma unroll
+                for (int s = 0; s < BC / 16; ++s) {
+                    const uint64_t b_h = tc::desc_kslice(qhi, TD, s + BC / 16), b_l = tc::desc_kslice(qlo, TD, s + BC / 16);
+                    tc::mma_ts16(tmem + kCN, tmem + kCNA + 8 * s, b_h, id128, s > 0);
+                    tc::mma_ts16(tmem + kCN, tmem + kCNA + 8 * s, b_l, id128, 1);
+                    tc::mma_ts16(tmem + kCN, tmem + kCNA + 16 + 8 * s, b_h, id128, 1);
+                }
+            }
             tc::commit(bar_mma);
         }
     }
@@ -728,6 +752,30 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             const int t = tb + e;
             dqo[t * TD] = dq[e];
             dko[t * TD] = __fmaf_rn(sR[t], d3[e], dk[e]);
+        }
+        if (park_next) {
+            // the next chunk's entry state M_N = gamma_last M + (r Delta)^T K, row `row`, this
+            // thread's 64 columns, parked in the unit layout (a warp writes 512-byte runs).
+            // M is read again from where (0) got it (L2 still holds it).
+            const float gl = sGam[BC - 1];
+            const float4* src = m_unit
+                ? reinterpret_cast<const float4*>(A.ws + A.o_Mc + ch * (long long)(TD * TD)) + 16 * hc * TD + row
+                : reinterpret_cast<const float4*>(A.ckpt + (head * A.n_ck + seg) * (long long)(TD * TD) + row * TD + 64 * hc);
+            const int sstride = m_unit ? TD : 1;
+            float4* dst = reinterpret_cast<float4*>(A.ws + A.o_Mc + (ch + 1) * (long long)(TD * TD)) + 16 * hc * TD + row;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float v[32];
+                tc::ld32(tc::taddr(tmem, warp, kCN + 64 * hc + 32 * h2), v);
+                tc::wait_ld();
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int u = 8 * h2 + q;
+                    const float4 mo = __ldg(src + u * sstride);
+                    dst[u * TD] = make_float4(__fmaf_rn(gl, mo.x, v[4 * q]), __fmaf_rn(gl, mo.y, v[4 * q + 1]),
+                                              __fmaf_rn(gl, mo.z, v[4 * q + 2]), __fmaf_rn(gl, mo.w, v[4 * q + 3]));
+                }
+            }
         }
     }
     if (!ok) s_err = 1;
@@ -774,9 +822,21 @@ int launch_tc_grad(const ChunkArgs& a, void* stream)
     int e = (int)cudaFuncSetAttribute(gdn_tc_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kGSmemBytes);
     if (e) return e;
-    if (a.c_hi <= a.c_lo) return 0;
-    gdn_tc_grad_kernel<<<dim3(a.c_hi - a.c_lo, a.H_v, a.N), GT, kGSmemBytes, s>>>(a);
+    const int units = tc_grad_units(a);
+    if (units <= 0) return 0;
+    gdn_tc_grad_kernel<<<dim3(units, a.H_v, a.N), GT, kGSmemBytes, s>>>(a);
     return (int)cudaGetLastError();
+}
+
+int tc_grad_units(const ChunkArgs& a)
+{
+    if (a.c_hi <= a.c_lo) return 0;
+    if (a.grad_loc < 0) return a.c_hi - a.c_lo;
+    // segments of [c_lo, c_hi) (segment-aligned) with a chunk at place grad_loc: all but
+    // possibly the last, which may be short
+    const int s_lo = a.c_lo / a.cps, s_hi = (a.c_hi + a.cps - 1) / a.cps;
+    const int last = a.c_hi - (s_hi - 1) * a.cps;  // chunks of the range's last segment
+    return (s_hi - s_lo) - (a.grad_loc >= last ? 1 : 0);
 }
 
 int launch_tc_dqdk_sum(const ChunkArgs& a, void* stream)

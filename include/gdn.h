@@ -49,7 +49,7 @@
  * The caller owns every buffer and the stream; the library allocates no device memory
  * and keeps no pointer after a call returns.  Work is enqueued on `stream` (a
  * cudaStream_t; NULL is the legacy default stream): GDN_OK means "validated and
- * launched".  At head size 128 the scalar-gate path also uses two library streams per
+ * launched".  At head size 128 the scalar-gate path also uses three library streams per
  * device (created on first use): the call's stream forks into them and joins back with
  * events, so everything the call enqueues is ordered after earlier work on `stream` and
  * before later work on it; calls on one device enqueue one at a time.  The inputs and
@@ -170,8 +170,9 @@ void gdn_set_timing_events(void* const* events, int n_events);
 
 /* Kernels a forward / backward call with these params launches (0 when the call would
  * fail validation).  Lets callers account for the work they enqueue.  On the head-size-128
- * path this is the count without timing events; a backward call with timing events set
- * runs its stages one after another and launches 4 kernels. */
+ * path this is the count without timing events.  A backward call with timing events set
+ * runs its stages one after another as one chunk range: the prep, the dM chain, one
+ * gradient launch per place of a chunk in its segment, and the sum. */
 int gdn_forward_launches(const gdn_params_t* p);
 int gdn_backward_launches(const gdn_params_t* p);
 

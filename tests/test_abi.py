@@ -75,19 +75,21 @@ def test_empty_batch_launches_nothing():
 
 
 def test_chunked_launch_count_with_several_chunks_per_segment():
-    # C = 64 > 32-token chunks: the backward also rebuilds the chunk-entry states.  Head
-    # size 128 pipelines over chunk ranges: the forward launches a prep and a state chain
-    # for each of 4 ranges, the backward a prep, a dM chain, a recompute, a gradient step
-    # and a sum for each of 2.  With timing events the backward runs 3 stages one after
-    # another.
+    # C = 64 > 32-token chunks.  Head size 128 pipelines over chunk ranges: the forward
+    # launches a prep and a state chain for each of 4 ranges; the backward launches, for
+    # each of 2, a prep, a dM chain, one gradient launch per place of a chunk in its segment
+    # (the first parks the second's entry states) and a sum.  With timing events the
+    # backward runs 3 stages one after another.
     p = gdn.make_params(1, 4096, 16, 48, 128, False)
     assert gdn.checkpoint_interval(p) == 64
     assert gdn.launches(p) == (8, 10)
     assert gdn.timing_stages(p) == (1, 3)
     p = gdn.make_params(1, 100, 1, 2, 128, False, C=64)   # 2 segments -> 2 ranges
     assert gdn.launches(p) == (4, 10)
-    p = gdn.make_params(1, 100, 1, 2, 128, False, C=32)   # one chunk per segment: no recompute
+    p = gdn.make_params(1, 100, 1, 2, 128, False, C=32)   # one chunk per segment
     assert gdn.launches(p) == (8, 8)
+    p = gdn.make_params(1, 100, 1, 2, 128, False, C=96)   # 3 places; the last segment has 1 chunk
+    assert gdn.launches(p) == (4, 6 + 4)
     p = gdn.make_params(1, 4096, 16, 48, 64, False)
     assert gdn.launches(p) == (2, 4)
 
