@@ -56,19 +56,21 @@ def chunk_kernel_flops(N, T, H_v, d, C, which):
         "recompute": recomputed * 2 * bd2,
         "dstate": ch * (3 * bd2 + 2 * b2d),
         "grad": ch * (4 * bd2 + 6 * b2d + 2 * BC ** 3),
-        "grad_tc": ch * (4 * bd2 + 6 * b2d + 2 * BC ** 3),
+        # head size 128: the gradient step also builds the entry state of each chunk's
+        # successor in its segment, M' = gamma M + (r Delta)^T K (B d^2)
+        "grad_tc": ch * (4 * bd2 + 6 * b2d + 2 * BC ** 3) + recomputed * bd2,
         "dqdk_sum": 0,
-        "chains": recomputed * 2 * bd2 + ch * (3 * bd2 + 2 * b2d),
         "fwd_pipe": ch * 4 * b2d + ch * (3 * bd2 + b2d),
-        "bwd_pipe": ch * (4 if cps > 1 else 2) * b2d + recomputed * 2 * bd2 + ch * (3 * bd2 + 2 * b2d),
+        # head size 128: prep ([QK^T; KK^T], E = s dY^T QD) and the dM chain
+        "bwd_pipe": ch * 3 * b2d + ch * (3 * bd2 + 2 * b2d),
     }[which]
     return 2.0 * fma
 
 
-# The head-size-128 chunked kernels run their products on the tensor cores as three tf32
-# passes; their roofline is the tf32 rate (the measured bf16 rate times the nominal
-# tf32 / bf16 ratio 1.1 / 2.25) divided by the three passes, in fp32 flops.
-TENSOR_KINDS = {"state_fwd", "recompute", "dstate", "grad_tc", "chains"}
+# The head-size-128 chunked kernels run their products on the tensor cores as three-pass
+# split products (bf16 hi/lo, part of the gradient step in tf32); their flop peak is
+# tensor_peak_tflops().
+TENSOR_KINDS = {"state_fwd", "dstate", "grad_tc"}
 
 
 def kernel_plan(chunked, d, n_bwd, cps):
@@ -94,13 +96,14 @@ def kernel_plan(chunked, d, n_bwd, cps):
 PIPELINED_KINDS = {"fwd_pipe", "bwd_pipe"}
 
 
-def chunk_kernel_bytes(N, T, H_v, d, C, which):
+def chunk_kernel_bytes(N, T, H_k, H_v, d, C, which):
     """Algorithmic DRAM bytes per launch (fp32): what the kernel has to read and write, with
     no re-reads and its operands stored once, unsplit (None where not counted).  The gradient
     step per (chunk, value head): the chunk-entry state M and dM_end (2 d^2); the dDelta,
     dX, V and dY rows (4 BC d); the chunk factors T, Z, KK^T, QK^T, Dm and gamma, r, beta
     (5 BC^2 + 3 BC); the key head's q and k rows (2 BC d); written: this value head's dq
-    and dk parts and dv (3 BC d), dg and dbeta (2 BC)."""
+    and dk parts and dv (3 BC d), dg and dbeta (2 BC).  The parked successor states are the
+    design's own traffic, not counted."""
     if which != "grad_tc":
         return None
     cps = -(-C // BC)
@@ -543,7 +546,7 @@ def run_ours(args):
     if chunked and kinds[top] in TENSOR_KINDS:
         peak, peak_src = tensor_peak_tflops()
         bound = "tensor"
-        top_bytes = chunk_kernel_bytes(N, T, H_v, d, C, kinds[top])
+        top_bytes = chunk_kernel_bytes(N, T, H_k, H_v, d, C, kinds[top])
         if top_bytes:  # the roofline is whichever floor is higher: bytes / HBM or flops / tensor
             hbm, hbm_src = hbm_peak_gbs()
             if top_bytes / (hbm * 1e9) > top_flops / (peak * 1e12):
@@ -573,7 +576,7 @@ def run_ours(args):
         "roofline": {"bound": bound, "kernel": names[top],
                      "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": chunk_kernel_bytes(N, T, H_v, d, C, kinds[top])
+                     "algorithmic_bytes_per_launch": chunk_kernel_bytes(N, T, H_k, H_v, d, C, kinds[top])
                      if chunked else None,
                      "flops_per_launch": top_flops, "launch_ms": kern_ms[top],
                      "peak_source": peak_src, "tensor": tensor_side},

@@ -355,9 +355,19 @@ void gdn::release_pipeline()
     }
 }
 
+namespace {
+// The backward's ranges and their shares of the segments, in the order the backward walks
+// them (the last segments first).  The first range is the smaller: its prep and dM chain
+// run with nothing beside them, while the second range's run beside the first range's
+// gradient step (at the 4096-token, 64-segment workload, 35/65 took the step from
+// 1.88 to 1.83 ms; 25/75 gave 1.84, and three ranges 1.90-1.94).
+constexpr int kBwdRanges = 2;
+constexpr int kBwdWalkPct[gdn::kMaxRanges] = {35, 65, 0, 0};
+}  // namespace
+
 int gdn::pipeline_ranges(int n_ck, bool backward)
 {
-    const int m = backward ? 2 : gdn::kMaxRanges;
+    const int m = backward ? kBwdRanges : gdn::kMaxRanges;
     return n_ck < m ? (n_ck < 1 ? 1 : n_ck) : m;
 }
 
@@ -367,6 +377,15 @@ void gdn::range_segments(int n_ck, int R, bool backward, int r, int* s_lo, int* 
         static const int kCum[5] = {0, 10, 30, 60, 100};  // percent of the segments
         *s_lo = (int)((long long)n_ck * kCum[r] / 100);
         *s_hi = (int)((long long)n_ck * kCum[r + 1] / 100);
+        return;
+    }
+    if (backward && R == kBwdRanges && R > 1 && n_ck >= 40) {
+        const int w = R - 1 - r;  // walk position of range r
+        int cum_lo = 0;
+        for (int i = 0; i < w; ++i) cum_lo += kBwdWalkPct[i];
+        const int cum_hi = w == R - 1 ? 100 : cum_lo + kBwdWalkPct[w];
+        *s_hi = n_ck - (int)((long long)n_ck * cum_lo / 100);
+        *s_lo = n_ck - (int)((long long)n_ck * cum_hi / 100);
         return;
     }
     const int per = (n_ck + R - 1) / R;

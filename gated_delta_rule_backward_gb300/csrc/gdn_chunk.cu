@@ -1407,12 +1407,12 @@ static int launch_prep_range(const ChunkArgs& a, int R, bool backward, int r, cu
 //
 // Backward, ranges last to first, three streams:
 //   high:   dM chain of range r (after prep(r)), carrying dM to range r - 1
-//   middle: prep(r), then prep(r - 1) once the dM chain of r has been enqueued
-//   low:    recompute of range r's segments (after prep(r)), then, after the dM chain of r,
-//           the gradient step and the sum over value heads for range r
+//   middle: prep(r), then prep(r - 1) once the dM chain of r has been enqueued; after the
+//           last prep, the sum over value heads of each range once its gradients are done
+//   low:    after the dM chain of r, the gradient launches of range r
 // so that the gradient work of one range runs while the chain walks the next.  With timing
 // events set, the backward instead runs its stages one after another as a single range
-// (prep, both chains, gradient step, sum), each between two events.
+// (prep and dM chain, gradient step, sum), each between two events.
 // The gradient launches of a chunk range: one per place in a segment, in order, each
 // parking the entry states of the next place's chunks (launch_tc_grad).
 static int launch_grads(const ChunkArgs& ar, cudaStream_t st)
