@@ -41,7 +41,7 @@ BC = 32  # chunk length of the chunked (scalar-gate) kernels
 
 def chunk_kernel_flops(N, T, H_v, d, C, which):
     """Flops (FMA = 2) each chunked kernel executes per launch: the dense products of the
-    WY form per (sequence, value head, 32-token chunk); see the design doc."""
+    WY form per (sequence, value head, 32-token chunk)."""
     cps = -(-C // BC)
     n_ck = -(-T // C)
     last = T - (n_ck - 1) * C
