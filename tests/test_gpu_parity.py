@@ -77,6 +77,26 @@ def test_kda_d128_T16384_sampled():
         H.compare_group(gpu, prob, n, hk, prob.C)
 
 
+def _sweep_point(d, T, N, kda):
+    for pt in synth.sweep_points():
+        if (pt["d"], pt["T"], pt["N"], pt["kda"]) == (d, T, N, kda):
+            return pt
+    raise KeyError((d, T, N, kda))
+
+
+@pytest.mark.parametrize("d,T,N,kda", [
+    (32, 4096, 1, False), (32, 4096, 1, True), (64, 4096, 1, False), (64, 4096, 1, True),
+    (128, 512, 8, False), (64, 512, 8, True), (128, 16384, 1, False), (32, 16384, 1, True)],
+    ids=lambda x: str(x))
+def test_sweep_point_sampled(d, T, N, kda):
+    """Points of the throughput sweep at their full sizes (default C = ceil(sqrt(T)), the
+    sweep's seeds), checked on one (sequence, key-head group) unit: the last sequence and
+    key head 7."""
+    prob = synth.make_problem(**_sweep_point(d, T, N, kda))
+    gpu, _ = H.run_gpu(prob)
+    H.compare_group(gpu, prob, N - 1, 7, prob.C)
+
+
 @pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
 def test_run_to_run_bit_identical(kda):
     prob = synth.make_problem(2, 300, 2, 6, 128, kda=kda, seed=41, C=17, packed=True,
