@@ -116,18 +116,44 @@ __device__ __forceinline__ void recurrence_step(float4 (&m)[RT][NV], float4 (&sp
     }
 }
 
+// The 16-byte path of load_rows: up to B loads per thread are in flight before the first
+// of their shared-memory stores, so a tile costs one global round trip per batch instead
+// of one per load.  f maps each loaded float4 to the stored one.
+template <int B, typename F>
+__device__ __forceinline__ void load_rows_vec(float* dst, const float* src, long long stride,
+                                              int nt, int width, int tid, int nthr, F f)
+{
+    const int per = width >> 2, total = nt * per;
+    for (int base = tid; base < total; base += B * nthr) {
+        float4 x[B];
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const int idx = base + b * nthr;
+            if (idx < total) {
+                const int tt = idx / per, i4 = idx - tt * per;
+                x[b] = __ldg(reinterpret_cast<const float4*>(src + tt * stride) + i4);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const int idx = base + b * nthr;
+            if (idx < total) {
+                const int tt = idx / per, i4 = idx - tt * per;
+                reinterpret_cast<float4*>(dst + tt * width)[i4] = f(x[b]);
+            }
+        }
+    }
+}
+
 // Cooperative copy of nt rows of `width` floats (row stride `stride` in global memory)
 // into a dense shared tile.  vec: every row start is 16-byte aligned and width % 4 == 0.
+// B: loads per thread in flight at once on the 16-byte path.
+template <int B = 1>
 __device__ __forceinline__ void load_rows(float* dst, const float* src, long long stride,
                                           int nt, int width, bool vec, int tid, int nthr)
 {
     if (vec) {
-        const int per = width >> 2;
-        for (int idx = tid; idx < nt * per; idx += nthr) {
-            const int tt = idx / per, i4 = idx - tt * per;
-            const float4 x = __ldg(reinterpret_cast<const float4*>(src + tt * stride) + i4);
-            reinterpret_cast<float4*>(dst + tt * width)[i4] = x;
-        }
+        load_rows_vec<B>(dst, src, stride, nt, width, tid, nthr, [](float4 x) { return x; });
     } else {
         for (int idx = tid; idx < nt * width; idx += nthr) {
             const int tt = idx / width, i = idx - tt * width;
@@ -137,17 +163,13 @@ __device__ __forceinline__ void load_rows(float* dst, const float* src, long lon
 }
 
 // As load_rows, storing exp(x) (the gate a = exp(g), accurate expf).
+template <int B = 1>
 __device__ __forceinline__ void load_rows_exp(float* dst, const float* src, long long stride,
                                               int nt, int width, bool vec, int tid, int nthr)
 {
     if (vec) {
-        const int per = width >> 2;
-        for (int idx = tid; idx < nt * per; idx += nthr) {
-            const int tt = idx / per, i4 = idx - tt * per;
-            const float4 x = __ldg(reinterpret_cast<const float4*>(src + tt * stride) + i4);
-            reinterpret_cast<float4*>(dst + tt * width)[i4] =
-                make_float4(expf(x.x), expf(x.y), expf(x.z), expf(x.w));
-        }
+        load_rows_vec<B>(dst, src, stride, nt, width, tid, nthr,
+                      [](float4 x) { return make_float4(expf(x.x), expf(x.y), expf(x.z), expf(x.w)); });
     } else {
         for (int idx = tid; idx < nt * width; idx += nthr) {
             const int tt = idx / width, i = idx - tt * width;

@@ -16,7 +16,7 @@
 namespace gdn {
 
 template <int D, int RT, bool KDA>
-__global__ void __launch_bounds__(256) gdn_fwd_kernel(const FwdArgs A)
+__global__ void __launch_bounds__(128, 3) gdn_fwd_kernel(const FwdArgs A)
 {
     constexpr int NV = D / 32;
     const int NT = blockDim.x, W = NT >> 5;
@@ -50,19 +50,19 @@ __global__ void __launch_bounds__(256) gdn_fwd_kernel(const FwdArgs A)
     for (int t0 = 0; t0 < A.T; t0 += tc) {
         const int nt = min(tc, A.T - t0);
         __syncthreads();
-        load_rows(sk, A.k + n * A.ks0 + (long long)t0 * A.ks1 + hk * A.ks2, A.ks1, nt, D,
+        load_rows<4>(sk, A.k + n * A.ks0 + (long long)t0 * A.ks1 + hk * A.ks2, A.ks1, nt, D,
                   A.vec_k, tid, NT);
-        load_rows(sq, A.q + n * A.qs0 + (long long)t0 * A.qs1 + hk * A.qs2, A.qs1, nt, D,
+        load_rows<4>(sq, A.q + n * A.qs0 + (long long)t0 * A.qs1 + hk * A.qs2, A.qs1, nt, D,
                   A.vec_q, tid, NT);
         const long long tok0 = (long long)n * A.T + t0;
         if (KDA) {
-            load_rows_exp(sa, A.g + (tok0 * A.H_v + h) * D, (long long)A.H_v * D, nt, D,
+            load_rows_exp<4>(sa, A.g + (tok0 * A.H_v + h) * D, (long long)A.H_v * D, nt, D,
                           A.vec_g, tid, NT);
         } else {
             for (int tt = tid; tt < nt; tt += NT) sa[tt] = expf(__ldg(A.g + (tok0 + tt) * A.H_v + h));
         }
         for (int tt = tid; tt < nt; tt += NT) sb[tt] = __ldg(A.beta + (tok0 + tt) * A.H_v + h);
-        load_rows(sv, A.v + n * A.vs0 + (long long)t0 * A.vs1 + h * A.vs2 + p * R, A.vs1, nt, R,
+        load_rows<4>(sv, A.v + n * A.vs0 + (long long)t0 * A.vs1 + h * A.vs2 + p * R, A.vs1, nt, R,
                   A.vec_v, tid, NT);
         __syncthreads();
 

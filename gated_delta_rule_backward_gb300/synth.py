@@ -112,6 +112,10 @@ WORKLOADS = {
     # size a many-pass profiler capture of one kernel launch stays small at
     "profile_d128_T1024": dict(N=1, T=1024, H_k=16, H_v=48, d=128, kda=False, C=64,
                                seed=1005, packed=True),
+    # the per-key-column gate at the same heads and C as the 16384-token workload, cut to
+    # 1024 tokens for many-pass profiler captures of the token-recurrence kernels
+    "profile_kda_d128_T1024": dict(N=1, T=1024, H_k=16, H_v=48, d=128, kda=True, C=128,
+                                   seed=1006, packed=True, g_std=2.0),
 }
 
 
