@@ -487,7 +487,7 @@ gdn_status_t gdn_device_status(void* stream)
     if (e) return cuda_status(e, "device status");
     if (!a && !b) return GDN_OK;
     // chain status word: 6 | kernel << 4 | wait-site bits << 8 (gdn_tc_chain.cu)
-    static const char* const kernels[] = {"?", "state chain", "recompute", "dM chain", "selftest"};
+    static const char* const kernels[] = {"?", "state chain", "?", "dM chain", "selftest"};
     const int ker = (a >> 4) & 15;
     return fail(GDN_ERR_TIMEOUT,
                 "a kernel's bounded wait gave up; that call's outputs are invalid (chains: %s, "

@@ -1,7 +1,7 @@
 // gdn_tc_chain.cu -- the two serial chains of the chunked scalar gate at head size 128 on
 // the 5th-generation tensor cores (tcgen05, kind::f16 with bf16 hi/lo operands, three-pass
-// split for fp32-level accuracy): the state chain (forward and recompute) and the dM chain
-// of the backward.
+// split for fp32-level accuracy): the forward's state chain and the dM chain of the
+// backward.
 //
 // State chain:
 //
@@ -21,11 +21,9 @@
 // instruction) the chunk's two products take 30 MMAs instead of 60 in tf32; M, the
 // accumulators and every sum outside the products stay fp32.
 //
-// Modes: forward (grid: head, sequence) writes y, the checkpoints and state_T;
-// recompute (grid: segment, sequence * head) rebuilds the chunk-entry states of one
-// segment from its checkpoint and parks them in the unit layout (float4 unit
-// (i / 4) * 128 + j holds M[j][i .. i + 3]), in which every warp store is one 512-byte run.  Both run the identical instruction
-// sequence per chunk, so recomputed states equal the forward's bit for bit.
+// Grid: (head, sequence); the chain writes y, the checkpoints and state_T (or, between
+// chunk ranges, the carried state).  The backward needs no rerun of it: its gradient step
+// rebuilds the chunk-entry states it needs (gdn_tc_grad.cu).
 #include <cuda_runtime.h>
 
 #include "gdn_internal.h"
@@ -52,7 +50,7 @@ constexpr uint32_t kColD23 = 320;             //               D23 (160 columns)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStatusTimeout = 6;
 // kernel field of the status word
-constexpr int kKerState = 1, kKerRecompute = 2, kKerDstate = 3, kKerSelftest = 4;
+constexpr int kKerState = 1, kKerDstate = 3, kKerSelftest = 4;  // 2: no longer used
 // wait sites (s_err bits): the issuer's waits on copies and operand handoffs, and the
 // compute warps' waits on MMA completion
 constexpr int kWCopyA = 1 << 0, kWCopyB = 1 << 1, kWHandoff1 = 1 << 2, kWHandoff2 = 1 << 3,
@@ -100,9 +98,7 @@ __device__ __forceinline__ void load_b23(const ChunkArgs& A, long long ch, float
 
 }  // namespace
 
-// The state chain of one head (forward: bx = head, by = sequence) or of one segment
-// (recompute: bx = segment, by = sequence * H_v + head); sm is the dynamic shared memory.
-template <bool FWD>
+// The state chain of one head (bx = head, by = sequence); sm is the dynamic shared memory.
 __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int bx, int by)
 {
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSFloats);  // b1, b23, mma, a[8]
@@ -121,22 +117,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     const int j = 32 * (warp & 3) + lane;   // row of M (compute warps)
     const int hc = (warp >> 2) & 1;         // column half: columns [64 hc, 64 hc + 64)
 
-    int n, h, c_begin, c_end;
-    if (FWD) {
-        h = bx;
-        n = by;
-        c_begin = A.c_lo;
-        c_end = A.c_hi;
-    } else {
-        const int hd = by;
-        n = hd / A.H_v;
-        h = hd - n * A.H_v;
-        const int s = bx;
-        c_begin = s * A.cps;
-        const int seg_len = min(A.T, s * A.C + A.C) - s * A.C;
-        c_end = c_begin + (seg_len + BC - 1) / BC - 1;  // chunks whose end state is needed
-        if (c_end <= c_begin) return;
-    }
+    const int h = bx, n = by, c_begin = A.c_lo, c_end = A.c_hi;
     const long long head = (long long)n * A.H_v + h;
     const long long khead = (long long)n * A.H_k + h % A.H_k;
 
@@ -167,9 +148,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     // entry state: this thread's 64 columns of row j
     float m[64];
     if (compute) {
-        const float* src = !FWD ? A.ckpt + ((head * A.n_ck + bx) * TD + j) * TD
-                           : c_begin == 0 ? A.state0 + (head * TD + j) * TD
-                                          : A.carry + (head * TD + j) * TD;
+        const float* src = c_begin == 0 ? A.state0 + (head * TD + j) * TD : A.carry + (head * TD + j) * TD;
         const float4* s4 = reinterpret_cast<const float4*>(src + 64 * hc);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -180,12 +159,6 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             m[4 * q + 3] = x.w;
         }
     }
-    auto park_state = [&](float* dst) {  // the same in the unit layout: a warp writes 512 B runs
-        float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-            d4[(16 * hc + q) * TD + j] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
-    };
     // y of a chunk is assembled in shared memory (rows t, one of two buffers by chunk parity)
     // by the column-half 1 threads: the Q part in (3), the QD Delta part added in (5).  It
     // goes to global memory during the next chunk's D23, when the compute warps would only
@@ -259,10 +232,11 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         const int t0 = seg * A.C + loc * BC;
         const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
         const long long ch = head * A.n_chunks + c;
-        float* sY = sm + kSY + (c & 1) * (BC * kStageLd);  // this chunk's y (forward)
+        float* sY = sm + kSY + (c & 1) * (BC * kStageLd);  // this chunk's y
         // (1) M (bf16 hi/lo, the A operand of D1) goes into TMEM slice by slice (release_group)
         // (2) D1 = M [W; Q]^T on the tensor cores, each k-slice issued as soon as its columns of
-        //     M are in TMEM; meanwhile the checkpoint (forward) or the parked state (recompute)
+        //     M are in TMEM; meanwhile the compute warps store the checkpoint at a segment's
+        //     first chunk
         const uint32_t ph_a = (uint32_t)(c - c_begin) & 1u;
         if (issuer) {
             if (!tc::mbar_wait(bar_b1, ph_b1)) atomicOr(&s_err, kWCopyA);
@@ -292,8 +266,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 if (!s_err) tc::commit(bar_mma);
             }
         } else if (compute) {
-            if (FWD && loc == 0) store_ckpt(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
-            if (!FWD && c > c_begin) park_state(A.ws + A.o_Mc + ch * (long long)(TD * TD));
+            if (loc == 0) store_ckpt(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
         }
         // (3) Delta^T (rows j) and the Q part of y^T.  Only the compute warps and the issuer
         // wait on bar_mma: every waiter must have seen a phase complete before the next commit
@@ -339,14 +312,14 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar_d);
-            } else if (FWD) {  // the Q part of y
+            } else {  // the Q part of y
                 float x[32];
                 tc::ld32(tc::taddr(tmem, warp, kColD1 + BC), x);
                 tc::wait_ld();
 #pragma unroll
                 for (int t = 0; t < BC; ++t) sY[t * kStageLd + j] = __fmul_rn(__fmul_rn(A.scale, sGam[t]), x[t]);
             }
-            if (FWD && y_nb > 0) store_y();  // the previous chunk's y, while D23 runs
+            if (y_nb > 0) store_y();  // the previous chunk's y, while D23 runs
         }
         ph_b23 ^= 1;
         if (!ok) atomicOr(&s_err, kWMma1);
@@ -385,18 +358,16 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 b23_pending = true;
             }
         } else if (compute) {
-            if (FWD) {
-                if (hc == 1) {  // y += D23[:, 0:32]
-                    float x[32];
-                    tc::ld32(tc::taddr(tmem, warp, kColD23), x);
-                    tc::wait_ld();
+            if (hc == 1) {  // y += D23[:, 0:32]
+                float x[32];
+                tc::ld32(tc::taddr(tmem, warp, kColD23), x);
+                tc::wait_ld();
 #pragma unroll
-                    for (int t = 0; t < BC; ++t) sY[t * kStageLd + j] = __fadd_rn(sY[t * kStageLd + j], x[t]);
-                }
-                y_t0 = t0;
-                y_nb = nb;
-                y_buf = sY;
+                for (int t = 0; t < BC; ++t) sY[t * kStageLd + j] = __fadd_rn(sY[t * kStageLd + j], x[t]);
             }
+            y_t0 = t0;
+            y_nb = nb;
+            y_buf = sY;
             // M <- gamma_last M + D23[:, 32:160], split at once into the next D1's A operand and
             // released to the issuer in two column groups
 #pragma unroll
@@ -415,17 +386,13 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     if (s_err) {
         // give the copies in flight a bounded chance to land before the TMEM is released
         if (issuer) {
-            raise_timeout(FWD ? kKerState : kKerRecompute, s_err);
+            raise_timeout(kKerState, s_err);
             if (b1_pending) tc::mbar_wait(bar_b1, ph_b1);
             if (b23_pending) tc::mbar_wait(bar_b23, ph_b23);
         }
     } else if (compute) {
-        if (FWD) {
-            if (y_nb > 0) store_y();
-            store_ckpt((c_end == A.n_chunks ? A.state_T : A.carry) + head * (long long)(TD * TD));
-        } else {
-            park_state(A.ws + A.o_Mc + (head * A.n_chunks + c_end) * (long long)(TD * TD));
-        }
+        if (y_nb > 0) store_y();
+        store_ckpt((c_end == A.n_chunks ? A.state_T : A.carry) + head * (long long)(TD * TD));
     }
     tc::fence_before();
     __syncthreads();
@@ -756,7 +723,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
 __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
 {
     extern __shared__ __align__(1024) float sm[];
-    state_chain<true>(A, sm, blockIdx.x, blockIdx.y);
+    state_chain(A, sm, blockIdx.x, blockIdx.y);
 }
 
 // The backward's dM chain: one CTA per (value head, sequence), over the chunks [c_lo, c_hi).
