@@ -30,8 +30,7 @@ METRIC = "GDN fwd+bwd head-tokens/s at d=128,H_v=48,T=4096; % of FP32/HBM roofli
 UNIT = "head-tokens/s"
 WORKLOAD = "bench_d128_T4096"
 
-# FP32 CUDA-core peak of GB300: 152 SMs x 128 FP32 lanes x 2 flop (FMA) x 2.070 GHz.
-FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 # Algorithmic flops per head-token of the path (FMA = 2): forward 7 d^2; backward = one
 # recompute 5 d^2 + reverse step 15 d^2.
 FWD_FLOPS = lambda d: 7 * d * d
@@ -114,11 +113,44 @@ def chunk_kernel_bytes(N, T, H_k, H_v, d, C, which):
     return N * H_v * n_chunks * per
 
 
+def fp32_peak(dev=None):
+    """FP32 CUDA-core peak of the device: its SM count (device properties) x 128 FP32 lanes
+    x 2 flop (FMA) x the maximum SM clock (MEASURED_PEAKS.json, else 2070 MHz).  Returns
+    (TFLOP/s, SMs, MHz, how it was derived)."""
+    import torch
+    sms = int(torch.cuda.get_device_properties(dev).multi_processor_count)
+    try:
+        mhz, src = float(json.load(open(PEAKS_FILE))["sm_max_mhz"]), "sm_max_mhz of MEASURED_PEAKS.json"
+    except (OSError, KeyError, ValueError):
+        mhz, src = 2070.0, "maximum SM clock 2070 MHz"
+    peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+    return peak, sms, mhz, (f"derived: {sms} SMs (device properties) x 128 FP32 lanes x 2 flop x "
+                            f"{mhz:.0f} MHz ({src})")
+
+
+def compulsory_bytes(d, r, T, kda):
+    """Compulsory DRAM bytes per head-token of a whole step (fp32; every input read once per
+    pass that needs it and every output written once; q, k shared by the r value heads of a
+    key head; checkpoints excluded): q, k read by both passes and dq, dk written (6 d / r);
+    v read twice, y, dv written, dY read (5 d); g, beta read twice, dg, dbeta written (6);
+    state0, state_T, dstate_T, dstate0 (16 d^2 / T); the per-key-column gate reads and writes
+    d values where the scalar gate has one (12 d - 12 more)."""
+    b = 4 * (6 * d / r + 5 * d + 6) + 16 * d * d / T
+    return b + (12 * d - 12 if kda else 0)
+
+
+# Arithmetic of the path, by head size and gate (stated in every bench line).
+ARITH_TC = ("fp32 inputs, outputs, state and accumulators; the state-sized products on the "
+            "tcgen05 tensor cores as three-pass split products (bf16 hi/lo, kind::f16, and tf32 "
+            "hi/lo for one product of the gradient step), the chunk-sized ones as three-pass "
+            "tf32 warp-level MMAs")
+ARITH_FP32 = "fp32 throughout (FP32 pipe), with three-pass tf32 warp-level MMAs for chunk-sized products"
+
+
 def hbm_peak_gbs():
     """Measured copy bandwidth (GB/s) of the GB300s, and where it came from."""
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
-        return float(json.load(open(path))["hbm_gbs"]), "measured copy bandwidth (MEASURED_PEAKS.json)"
+        return float(json.load(open(PEAKS_FILE))["hbm_gbs"]), "measured copy bandwidth (MEASURED_PEAKS.json)"
     except (OSError, KeyError, ValueError):
         return 6800.0, "fallback 6.8 TB/s"
 
@@ -132,9 +164,8 @@ def tensor_peak_tflops(tf32_share=GRAD_TF32_SHARE):
     """fp32-equivalent peak of three-pass split products, tf32_share of them in tf32 and the
     rest in bf16: measured bf16 / 3 for the bf16 passes, x nominal tf32/bf16 (1.1 / 2.25) for
     the tf32 ones, combined by time per flop; and where it came from."""
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
-        bf16 = float(json.load(open(path))["bf16_tflops"])
+        bf16 = float(json.load(open(PEAKS_FILE))["bf16_tflops"])
         src = "measured bf16 burst"
     except (OSError, KeyError, ValueError):
         bf16, src = 1900.0, "fallback bf16 1.9 PFLOP/s"
@@ -259,56 +290,118 @@ def _recorded_traffic(kernel):
         return None
 
 
+def _recorded_step_traffic(workload, chunked):
+    """DRAM bytes of one whole step (every launch of a forward and a backward call) from the
+    committed ncu summary of the workload, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"step_dram_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    h = hashlib.sha256()
+    for f in (CHUNKED_SOURCES if chunked else TOKEN_SOURCES):
+        h.update(open(os.path.join(ROOT, "gated_delta_rule_backward_gb300", "csrc", f), "rb").read())
+    if vals.get("kernel_sources_sha") != h.hexdigest()[:16]:
+        return None
+    try:
+        return float(vals["dram_bytes_per_step"])
+    except (KeyError, ValueError):
+        return None
+
+
 # --------------------------------------------------------------------------- oracle
-def _oracle_sample(prob, groups, lib=None):
-    """Run the oracle forward+backward on `groups` (n, hk) key-head groups of prob.
-    Returns (head_tokens, seconds)."""
+def _unit_sample(prob, units):
+    """The sub-problem of `units` (sequence n, value head h) of prob, one unit per value head:
+    each unit's key-head q, k rows sit beside its own v, g, beta, state0, dY (H_k = H_v)."""
     import numpy as np
+    st = lambda xs: np.ascontiguousarray(np.stack(xs, axis=1)[None], dtype=np.float64)
+    hk = lambda h: h % prob.H_k
+    q = st([prob.q[n, :, hk(h)] for n, h in units])
+    k = st([prob.k[n, :, hk(h)] for n, h in units])
+    v = st([prob.v[n, :, h] for n, h in units])
+    g = st([prob.g[n, :, h] for n, h in units])
+    b = st([prob.beta[n, :, h] for n, h in units])
+    gy = st([prob.gy[n, :, h] for n, h in units])
+    s0 = np.ascontiguousarray(np.stack([prob.state0[n, h] for n, h in units])[None], dtype=np.float64)
+    return q, k, v, g, b, s0, gy
+
+
+def _oracle_sample(prob, units, lib=None):
+    """The oracle's forward + checkpointed backward on `units` (sequence, value head) of
+    prob.  Returns (head_tokens, seconds)."""
     import oracle
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import gpu_helpers as H
-    qs, ks, vs, gs, bs, s0, gys = [], [], [], [], [], [], []
-    for n, hk in groups:
-        sub, heads = H.group_problem(prob, n, hk)
-        qs.append(np.repeat(sub["q"], len(heads), axis=2))  # one unit per value head
-        ks.append(np.repeat(sub["k"], len(heads), axis=2))
-        vs.append(sub["v"]); gs.append(sub["g"]); bs.append(sub["beta"])
-        s0.append(sub["state0"]); gys.append(sub["gy"])
-    cat = lambda xs, ax: np.ascontiguousarray(np.concatenate(xs, axis=ax), dtype=np.float64)
-    q, k, v, g, b = cat(qs, 2), cat(ks, 2), cat(vs, 2), cat(gs, 2), cat(bs, 2)
-    st0, gy = cat(s0, 1), cat(gys, 2)
+    q, k, v, g, b, s0, gy = _unit_sample(prob, units)
     t0 = time.perf_counter()
-    _, _, ck = oracle.forward(q, k, v, g, b, st0, prob.scale, C=prob.C, lib=lib)
-    oracle.backward(q, k, v, g, b, st0, gy, None, prob.scale, C=prob.C, ckpt=ck, lib=lib)
+    _, _, ck = oracle.forward(q, k, v, g, b, s0, prob.scale, C=prob.C, lib=lib)
+    oracle.backward(q, k, v, g, b, s0, gy, None, prob.scale, C=prob.C, ckpt=ck, lib=lib)
     dt = time.perf_counter() - t0
-    return q.shape[2] * prob.T, dt
+    return len(units) * prob.T, dt
 
 
-def _sample_groups(prob, cores):
-    r = prob.H_v // prob.H_k
-    n_groups = max(1, min(prob.H_k, cores // r))
-    return [(0, hk) for hk in range(n_groups)]
+def _first_units(prob, count):
+    """The first `count` (sequence, value head) units in (sequence, head) order."""
+    units = [(n, h) for n in range(prob.N) for h in range(prob.H_v)]
+    return units[:max(1, min(count, len(units)))]
 
 
-def cpu_baseline(prob, reps=2):
-    """The oracle on the host cores: `reps` runs of whole key-head groups over all tokens
-    (one value head per thread), about 10-30 core-seconds at the bench workload."""
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+# The oracle's timed sample: the throughput workload, the 2048-token broadcast workload and
+# the 16384-token strong-decay KDA workload, each on all host cores and on one.
+CPU_WORKLOADS = ("bench_d128_T4096", "bcast_d128_T2048", "kda_d128_T16384")
+
+
+def cpu_baseline(target):
+    """The oracle (float64 C, OpenMP over (sequence, value head)) on the host cores.  On each
+    workload of CPU_WORKLOADS: all cores (one value head per thread, as many value heads as
+    threads) and one core (one value head), every unit over all of the workload's tokens,
+    forward + checkpointed backward.  `value` is the all-core figure on `target`."""
     import oracle
+    from gated_delta_rule_backward_gb300 import synth
     lib = oracle.load()
-    cores = oracle.max_threads(lib)
-    groups = _sample_groups(prob, cores)
-    ht, dt = 0, 0.0
-    for _ in range(reps):
-        h, d = _oracle_sample(prob, groups, lib)
-        ht, dt = ht + h, dt + d
-    r = prob.H_v // prob.H_k
-    used = min(cores, len(groups) * r)
-    return {"value": ht / dt, "unit": UNIT, "cores": used,
+    threads = oracle.max_threads(lib)
+    runs = []
+    head = None
+    for wl in (target,) + tuple(w for w in CPU_WORKLOADS if w != target):
+        prob = synth.workload(wl)
+        for nt in (threads, 1):
+            oracle.set_threads(nt, lib)
+            units = _first_units(prob, nt)
+            ht, dt = _oracle_sample(prob, units, lib)
+            run = {"workload": wl, "threads": nt, "value_heads": len(units), "tokens": prob.T,
+                   "seconds": round(dt, 3), "head_tokens_per_s": ht / dt}
+            runs.append(run)
+            if wl == target and nt == threads:
+                head = run
+        del prob
+    oracle.set_threads(threads, lib)
+    return {"value": head["head_tokens_per_s"], "unit": UNIT, "cores": threads,
             "kind": "oracle",
-            "sample": f"{reps} x {len(groups) * r} of {prob.N * prob.H_v} value heads (sequence 0, "
-                      f"key heads 0..{len(groups) - 1}) over all {prob.T} tokens, forward + "
-                      f"checkpointed backward, float64: {dt:.1f} s wall on {used} threads "
-                      f"({dt * used:.0f} core-seconds)"}
+            "sample": f"{head['value_heads']} of the value heads of {target} (sequence 0, heads "
+                      f"0..{head['value_heads'] - 1}) over all {head['tokens']} tokens, forward + "
+                      f"checkpointed backward, float64, one value head per thread: "
+                      f"{head['seconds']:.2f} s wall on {threads} threads",
+            "nproc": os.cpu_count(), "omp_threads": threads, "cpu_model": _cpu_model(),
+            "runs": runs}
 
 
 def run_reference(args):
@@ -320,18 +413,18 @@ def run_reference(args):
     prob = synth.workload(args.workload)
     lib = oracle.load()
     cores = oracle.max_threads(lib)
-    groups = _sample_groups(prob, cores)
+    units = _first_units(prob, cores)
     for _ in range(args.warmup):
-        _oracle_sample(prob, groups[:1], lib)
+        _oracle_sample(prob, units[:1], lib)
     tot_ht, tot_s = 0, 0.0
     for _ in range(args.steps):
-        ht, dt = _oracle_sample(prob, groups, lib)
+        ht, dt = _oracle_sample(prob, units, lib)
         tot_ht += ht
         tot_s += dt
     value = tot_ht / tot_s
-    r = prob.H_v // prob.H_k
-    sample = (f"per step {len(groups) * r} of {prob.N * prob.H_v} value heads (sequence 0) over "
-              f"all {prob.T} tokens, forward + checkpointed backward, float64 C oracle")
+    sample = (f"per step {len(units)} of {prob.N * prob.H_v} value heads (sequence 0) over "
+              f"all {prob.T} tokens, forward + checkpointed backward, float64 C oracle, one "
+              f"value head per thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -340,8 +433,9 @@ def run_reference(args):
         "config": {"workload": args.workload, "N": prob.N, "T": prob.T, "H_k": prob.H_k,
                    "H_v": prob.H_v, "d": prob.d, "gate": "kda" if prob.kda else "scalar",
                    "C": prob.C or math.isqrt(prob.T - 1) + 1, "sample": sample},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, len(groups) * r),
-                         "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, len(units)),
+                         "kind": "oracle", "sample": sample, "nproc": os.cpu_count(),
+                         "cpu_model": _cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -545,54 +639,59 @@ def run_ours(args):
     names = fwd_names + bwd_names
     single = [j for j in range(len(kern_ms)) if not (chunked and kinds[j] in PIPELINED_KINDS)]
     top = max(single, key=lambda j: kern_ms[j])
+    # The roofline of the method (the survey's measurement plan): its algorithmic flops, 27 d^2
+    # per head-token (forward 7, one recompute 5, backward 15), against the FP32 pipe of this
+    # device; the compulsory bytes at the measured HBM bandwidth are the other floor, far lower.
+    peak32, sms, mhz, peak32_src = fp32_peak(dev)
+    hbm, hbm_src = hbm_peak_gbs()
+    path_flops = (FWD_FLOPS(d) + BWD_FLOPS(d)) * head_tokens
+    path_tflops = path_flops / (step_ms * 1e-3) / 1e12
+    comp = compulsory_bytes(d, H_v // H_k, T, prob.kda) * head_tokens
+    fp32_floor_ms = path_flops / (peak32 * 1e12) * 1e3
+    hbm_floor_ms = comp / (hbm * 1e9) * 1e3
+    step_traffic = _recorded_step_traffic(args.workload, chunked)
+    # the dominant kernel (largest staged stage time): what it executes and moves
+    top_ms = kern_ms[top]
+    top_traffic = _recorded_traffic(names[top])
+    dom = {"kernel": names[top], "ms": top_ms, "share_of_staged_stages": top_ms / sum(kern_ms),
+           "dram_bytes_per_launch": top_traffic,
+           "dram_over_step_compulsory": (top_traffic / comp) if top_traffic else None,
+           "dram_gbs": (top_traffic / (top_ms * 1e-3) / 1e9) if top_traffic else None,
+           "hbm_peak_gbs": hbm}
     if chunked:
-        top_flops = chunk_kernel_flops(N, T, H_v, d, C, kinds[top])
-    else:
-        top_flops = (FWD_FLOPS(d) if top < n_fwd else BWD_FLOPS(d)) * head_tokens
-    achieved = top_flops / (kern_ms[top] * 1e-3) / 1e12
-    unit = "TFLOP/s"
-    tensor_side = None
-    if chunked and kinds[top] in TENSOR_KINDS:
-        peak, peak_src = tensor_peak_tflops()
-        bound = "tensor"
-        top_bytes = chunk_kernel_bytes(N, T, H_k, H_v, d, C, kinds[top])
-        if top_bytes:  # the roofline is whichever floor is higher: bytes / HBM or flops / tensor
-            hbm, hbm_src = hbm_peak_gbs()
-            if top_bytes / (hbm * 1e9) > top_flops / (peak * 1e12):
-                tensor_side = {"achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                               "frac": achieved / peak, "peak_source": peak_src}
-                achieved = top_bytes / (kern_ms[top] * 1e-3) / 1e9
-                peak, peak_src, unit, bound = hbm, hbm_src, "GB/s", "hbm"
-    else:
-        peak, peak_src = FP32_PEAK_TFLOPS, "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.070 GHz"
-        bound = "alu"
-    path_tflops = (FWD_FLOPS(d) + BWD_FLOPS(d)) * head_tokens / (step_ms * 1e-3) / 1e12
+        ex = chunk_kernel_flops(N, T, H_v, d, C, kinds[top])
+        dom["executed_flops_per_launch"] = ex
+        if kinds[top] in TENSOR_KINDS:
+            tpk, tsrc = tensor_peak_tflops()
+            dom["tensor"] = {"achieved": ex / (top_ms * 1e-3) / 1e12, "peak": tpk, "unit": "TFLOP/s",
+                             "frac": ex / (top_ms * 1e-3) / 1e12 / tpk, "peak_source": tsrc}
     kernels = [{"kernel": nm, "ms": kern_ms[j],
                 "tflops": (chunk_kernel_flops(N, T, H_v, d, C, kinds[j]) / (kern_ms[j] * 1e-3) / 1e12)
                 if chunked and kinds[j] != "dqdk_sum" else None} for j, nm in enumerate(names)]
-    traffic = _recorded_traffic(names[top])
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(prob)
+        cpu = cpu_baseline(args.workload)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "N": N, "T": T, "H_k": H_k, "H_v": H_v, "d": d,
                    "gate": "kda" if prob.kda else "scalar", "C": C, "qkv": "packed row views",
+                   "arithmetic": ARITH_TC if (chunked and d == 128) else ARITH_FP32,
                    "l2": "flushed between timed steps (256 MiB write outside the events)",
                    "per_rank": "each rank runs the whole workload on its own GPU"},
-        "roofline": {"bound": bound, "kernel": names[top],
-                     "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": chunk_kernel_bytes(N, T, H_k, H_v, d, C, kinds[top])
-                     if chunked else None,
-                     "flops_per_launch": top_flops, "launch_ms": kern_ms[top],
-                     "peak_source": peak_src, "tensor": tensor_side},
-        "roofline_path": {"achieved": path_tflops, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                          "frac": path_tflops / FP32_PEAK_TFLOPS,
-                          "flops_per_head_token": FWD_FLOPS(d) + BWD_FLOPS(d),
-                          "fwd_ms": fwd_avg, "bwd_ms": bwd_avg},
+        "roofline": {"bound": "alu", "kernel": "whole step: gdn_forward + gdn_backward",
+                     "achieved": path_tflops, "peak": peak32, "unit": "TFLOP/s",
+                     "frac": path_tflops / peak32, "traffic": step_traffic,
+                     "flops_per_launch": path_flops, "launch_ms": step_ms,
+                     "flops_per_head_token": FWD_FLOPS(d) + BWD_FLOPS(d),
+                     "frac_without_recompute": 22 * d * d * head_tokens / (step_ms * 1e-3) / 1e12 / peak32,
+                     "compulsory_bytes_per_launch": comp,
+                     "traffic_over_compulsory": (step_traffic / comp) if step_traffic else None,
+                     "fp32_floor_ms": fp32_floor_ms, "hbm_floor_ms": hbm_floor_ms,
+                     "sm_count": sms, "peak_source": peak32_src, "hbm_peak_gbs": hbm,
+                     "hbm_peak_source": hbm_src, "fwd_ms": fwd_avg, "bwd_ms": bwd_avg,
+                     "dominant_kernel": dom},
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -663,12 +762,13 @@ def run_sweep(args):
         ms = sum(a.elapsed_time(b) for a, b in evs) / steps
         head_tokens = N * H_v * T
         tflops = (FWD_FLOPS(d) + BWD_FLOPS(d)) * head_tokens / (ms * 1e-3) / 1e12
+        peak32 = fp32_peak(dev)[0]
         print(json.dumps({"point": {"d": d, "T": T, "N": N, "H_k": H_k, "H_v": H_v,
                                     "gate": "kda" if kda else "scalar", "C": gdn.checkpoint_interval(p)},
                           "metric": METRIC, "value": head_tokens / (ms * 1e-3), "unit": UNIT,
                           "ms_per_step": ms, "steps": steps, "dtype": "f32", "data": "synthetic",
-                          "roofline_path": {"achieved": tflops, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                                            "frac": tflops / FP32_PEAK_TFLOPS}}), flush=True)
+                          "roofline": {"bound": "alu", "achieved": tflops, "peak": peak32, "unit": "TFLOP/s",
+                                       "frac": tflops / peak32}}), flush=True)
         del qkv, q, k, v, g, beta, state0, gy, y, sT, ck, packed, ws, fws
         torch.cuda.empty_cache()
 

@@ -489,10 +489,13 @@ gdn_status_t gdn_device_status(void* stream)
     // chain status word: 6 | kernel << 4 | wait-site bits << 8 (gdn_tc_chain.cu)
     static const char* const kernels[] = {"?", "state chain", "?", "dM chain", "selftest"};
     const int ker = (a >> 4) & 15;
+    // wait-site bit 0x80 (chains) and gradient-kernel bit 8: a product was still running when
+    // its kernel gave up and released the tensor memory
+    const char* grad = !b ? "ok" : ((b >> 8) & 1) ? "timed out, a product still in flight at exit" : "timed out";
     return fail(GDN_ERR_TIMEOUT,
                 "a kernel's bounded wait gave up; that call's outputs are invalid (chains: %s, "
                 "wait sites 0x%x; gradient kernel: %s)",
-                a ? kernels[ker < 5 ? ker : 0] : "ok", (unsigned)a >> 8, b ? "timed out" : "ok");
+                a ? kernels[ker < 5 ? ker : 0] : "ok", (unsigned)a >> 8, grad);
 }
 
 gdn_status_t gdn_selftest_wait_timeout(void* stream)

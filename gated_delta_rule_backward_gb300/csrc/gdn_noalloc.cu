@@ -17,6 +17,9 @@
 //     streams, no ordering between them) race on the array and give wrong results.
 //   * Problems whose workspace exceeds kNoAllocScratchBytes are rejected with
 //     GDN_ERR_WORKSPACE before anything is launched.
+//   * The looked-up address is kept for the life of the process.  A cudaDeviceReset
+//     unloads the module that holds the array, so after one the address is stale: the
+//     entry point is not for processes that reset a device they use it on.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -60,10 +63,17 @@ gdn_status_t gdn_backward_noalloc(const gdn_params_t* p, const float* q, const f
     }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    if (e != cudaSuccess) {
         snprintf(msg, sizeof msg, "cudaGetDevice failed: %s", cudaGetErrorString(e));
         gdn::set_last_error(msg);
         return GDN_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        snprintf(msg, sizeof msg,
+                 "device %d is beyond the %d devices the no-allocation entry point keeps a "
+                 "scratch address for", dev, kMaxDevices);
+        gdn::set_last_error(msg);
+        return GDN_ERR_UNSUPPORTED;
     }
     void* scratch = nullptr;
     {

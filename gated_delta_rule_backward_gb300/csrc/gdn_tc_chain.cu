@@ -54,7 +54,9 @@ constexpr int kKerState = 1, kKerDstate = 3, kKerSelftest = 4;  // 2: no longer 
 // wait sites (s_err bits): the issuer's waits on copies and operand handoffs, and the
 // compute warps' waits on MMA completion
 constexpr int kWCopyA = 1 << 0, kWCopyB = 1 << 1, kWHandoff1 = 1 << 2, kWHandoff2 = 1 << 3,
-              kWMma1 = 1 << 4, kWMma2 = 1 << 5, kWMma3 = 1 << 6;
+              kWMma1 = 1 << 4, kWMma2 = 1 << 5, kWMma3 = 1 << 6,
+              kWTmem = 1 << 7;  // an MMA committed before a give-up did not complete either:
+                                // the tensor memory may still be written after its release
 __device__ __forceinline__ void raise_timeout(int kernel, int sites)
 {
     atomicOr(&g_tc_status, kStatusTimeout | kernel << 4 | sites << 8);
@@ -137,6 +139,8 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     const uint32_t tmem = s_tmem;
 
     uint32_t ph_b1 = 0, ph_b23 = 0, ph_mma = 0;
+    bool mma_out = false;  // issuer: a committed MMA group not yet seen complete, phase ph_out
+    uint32_t ph_out = 0;
     bool b1_pending = false, b23_pending = false;
     if (issuer) {
         tc::prefetch_l2(A.ws + A.o_U + (head * A.n_chunks + c_begin) * (BC * TD));  // see prefetch_l2
@@ -263,7 +267,11 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                         tc::mma_ts16(tmem + kColD1, alo, tc::desc_kslice_rg(bhi, s), id64, 1);
                     }
                 }
-                if (!s_err) tc::commit(bar_mma);
+                if (!s_err) {
+                    tc::commit(bar_mma);
+                    mma_out = true;
+                    ph_out = ph_mma;
+                }
             }
         } else if (compute) {
             if (loc == 0) store_ckpt(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
@@ -273,6 +281,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         // on it can land (else it would wait on the phase after), and only the bar_d arrivals
         // of the compute warps order that for D23.
         bool ok = !(compute || issuer) || tc::mbar_wait(bar_mma, ph_mma);
+        if (issuer && ok) mma_out = false;
         ph_mma ^= 1;
         tc::fence_after();
         float gl = 0.f;
@@ -340,10 +349,13 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                     tc::mma_ts16(tmem + kColD23, a_l, b_h, id160, 1);
                 }
                 tc::commit(bar_mma);
+                mma_out = true;
+                ph_out = ph_mma;
             }
         }
         // (5) y and the state update
         ok = !(compute || issuer) || tc::mbar_wait(bar_mma, ph_mma);
+        if (issuer && ok) mma_out = false;
         ph_mma ^= 1;
         tc::fence_after();
         if (!__syncthreads_and(ok)) {
@@ -387,6 +399,8 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         // give the copies in flight a bounded chance to land before the TMEM is released
         if (issuer) {
             raise_timeout(kKerState, s_err);
+            // the products in flight must be done before the tensor memory is released
+            if (mma_out && !tc::mbar_wait(bar_mma, ph_out)) raise_timeout(kKerState, kWTmem);
             if (b1_pending) tc::mbar_wait(bar_b1, ph_b1);
             if (b23_pending) tc::mbar_wait(bar_b23, ph_b23);
         }
@@ -484,6 +498,8 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
 
     const int c_last = A.c_hi - 1;
     uint32_t ph_kb = 0, ph_rest = 0, ph_mma = 0;
+    bool mma_out = false;  // issuer: a committed MMA group not yet seen complete, phase ph_out
+    uint32_t ph_out = 0;
     bool kb_pending = false, rest_pending = false;
     if (issuer) {
         tc::prefetch_l2(A.ws + A.o_DS + (head * A.n_chunks + c_last) * kTcDsElems);  // see prefetch_l2
@@ -568,6 +584,8 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
                     tc::mma_ts16(tmem + kDsColA, alo, tc::desc_kslice(bhi, 32, s), id32, 1);
                 }
                 tc::commit(bar_mma);
+                mma_out = true;
+                ph_out = ph_mma;
                 if (!tc::mbar_wait(bar_rest, ph_rest)) atomicOr(&s_err, kWCopyB);
                 if (!s_err) {
                     const uint64_t ahi = tc::tile_desc(sm + kSmG, TD), alo = tc::tile_desc(sm + kSmG + BC * TD / 2, TD);
@@ -594,6 +612,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
         // seen a phase complete before the issuer commits the next one (a waiter that missed
         // a phase would wait on the one after it).
         bool ok = !(compute || issuer) || tc::mbar_wait(bar_mma, ph_mma);
+        if (issuer && ok) mma_out = false;
         ph_mma ^= 1;
         tc::fence_after();
         if (issuer) {
@@ -638,10 +657,13 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
                     tc::mma_ts16(tmem + kDsColB, a_l, b_h, id32, 1);
                 }
                 tc::commit(bar_mma);
+                mma_out = true;
+                ph_out = ph_mma;
             }
         }
         // (5) dX^T = Db;  A operand <- -gamma dX^T
         ok = !(compute || issuer) || tc::mbar_wait(bar_mma, ph_mma);
+        if (issuer && ok) mma_out = false;
         ph_mma ^= 1;
         tc::fence_after();
         float gl = 0.f;
@@ -673,10 +695,13 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
                     tc::mma_ts16(tmem + kDsColC, a_l, b_h, id128, 1);
                 }
                 tc::commit(bar_mma);
+                mma_out = true;
+                ph_out = ph_mma;
             }
         }
         // (7) dM <- gamma_last dM + Dc
         ok = !(compute || issuer) || tc::mbar_wait(bar_mma, ph_mma);
+        if (issuer && ok) mma_out = false;
         ph_mma ^= 1;
         tc::fence_after();
         if (!__syncthreads_and(ok)) {
@@ -705,6 +730,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
     if (s_err) {
         if (issuer) {
             raise_timeout(kKerDstate, s_err);
+            if (mma_out && !tc::mbar_wait(bar_mma, ph_out)) raise_timeout(kKerDstate, kWTmem);
             if (kb_pending) tc::mbar_wait(bar_kb, ph_kb);
             if (rest_pending) tc::mbar_wait(bar_rest, ph_rest);
         }

@@ -251,6 +251,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     // (0) build A = M (rows j) from the staged M.  The loads of step (1), which do not depend
     //     on M, go out while the copy is in flight.
     uint32_t ph = 0;
+    bool mma_out = false;  // issuer: a committed MMA group not yet seen complete, phase ph_out
+    uint32_t ph_out = 0;
     bool ok = true;
     float vx[32], dy[16];
     float4 dx[4];
@@ -301,6 +303,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             mma3_t16(tmem + kCX, aHi, aHi + 64, tc::tile_desc(sm + kR0, 32), tc::tile_desc(sm + kR0 + 32 * TD / 2, 32),
                      (32 / 8) * 128, 0, TD / 16, tc::idesc_bf16(32), false);
             tc::commit(bar_mma);
+            mma_out = true;
+            ph_out = ph;
         }
     } else if (compute) {
         if (!tc::mbar_wait(bar_ld, 0)) s_err = 1;
@@ -319,6 +323,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         }
     }
     ok = tc::mbar_wait(bar_mma, ph);
+    if (issuer && ok) mma_out = false;
     ph ^= 1;
     tc::fence_after();
     // (2) A = M^T (rows i); D_X goes to registers first (A = M is dead: D_X is done)
@@ -363,6 +368,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                tc::make_desc(tc::smem_addr(sm + kR1 + kT64), kLbo64, 128), kLbo64, 0, TD / 8,
                tc::idesc_tf32(64), false);
         tc::commit(bar_mma);
+            mma_out = true;
+            ph_out = ph;
     } else if (compute) {
         const float* sT = sm + kSTr;
 #pragma unroll
@@ -389,6 +396,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         }
     }
     ok = tc::mbar_wait(bar_mma, ph);
+    if (issuer && ok) mma_out = false;
     ph ^= 1;
     tc::fence_after();
     // (4) A = dM^T (rows i) and <dM, M> (M^T still in TMEM).  R1's B tile is dead: dDelta and
@@ -457,8 +465,11 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                  tc::make_desc(tc::smem_addr(sm + kR0 + kT64h), kLbo64, 128), kLbo64, 0, TD / 16,
                  tc::idesc_bf16(32), false);
         tc::commit(bar_mma);
+            mma_out = true;
+            ph_out = ph;
     }
     ok = tc::mbar_wait(bar_mma, ph);
+    if (issuer && ok) mma_out = false;
     ph ^= 1;
     tc::fence_after();
     // (6) the gamma dgamma partials (from D2, which holds M^T [s gamma dY ; -gamma dX]^T until
@@ -554,6 +565,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                  tc::make_desc(tc::smem_addr(sm + kR0 + kT64h), kLbo64, 128), kLbo64, 0, TD / 16,
                  tc::idesc_bf16(64), false);
         tc::commit(bar_mma);
+            mma_out = true;
+            ph_out = ph;
     } else if (compute) {
         if (tid < 2 * BC) {
             vec[tid] = __fadd_rn(__fadd_rn(red[tid], red[96 + tid]), __fadd_rn(red[192 + tid], red[288 + tid]));
@@ -568,6 +581,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         for (int idx = tid; idx < BC * BC; idx += 256) Zs[(idx >> 5) * LDF + (idx & 31)] = sm[kSZ + idx];
     }
     ok = tc::mbar_wait(bar_mma, ph);
+    if (issuer && ok) mma_out = false;
     ph ^= 1;
     tc::fence_after();
     if (compute) {
@@ -735,9 +749,12 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                 }
             }
             tc::commit(bar_mma);
+            mma_out = true;
+            ph_out = ph;
         }
     }
     ok = tc::mbar_wait(bar_mma, ph);
+    if (issuer && ok) mma_out = false;
     tc::fence_after();
     // (10) this value head's dq and dk (rows i = row, tokens [tb, tb + 16)) -> workspace
     if (compute && ok) {
@@ -783,6 +800,9 @@ done:
     __syncthreads();
     if (s_err && issuer) {
         atomicExch(&g_tcg_status, kStatusTimeout);
+        // the products in flight must be done before the tensor memory is released; if they
+        // are not, say so (bit 8: the tensor memory may be written after its release)
+        if (mma_out && !tc::mbar_wait(bar_mma, ph_out)) atomicOr(&g_tcg_status, 1 << 8);
         for (int b = 0; b < 6; ++b)  // let this CTA's bulk copies land before it exits
             if (s_armed & (1 << b)) tc::mbar_wait(bars + b, 0);
     }

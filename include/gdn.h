@@ -44,6 +44,17 @@
  *             dg (like g) | dbeta [N][T][H_v] | dstate [N][H_v][S_v][S_k], back to back
  *             (element offsets from gdn_packed_grad_offsets)
  *
+ * Arithmetic
+ * ----------
+ * Inputs, outputs, the state and every accumulator are fp32.  The products are computed
+ * as follows: at head size 128 (scalar gate) the state-sized products run on the tcgen05
+ * tensor cores as three-pass split products -- each operand split x = hi + lo into bf16
+ * (kind::f16) or, for one product of the gradient step, tf32 parts, and a b taken as
+ * hi hi + hi lo + lo hi with an fp32 accumulator, about 2^-16 (bf16) or 2^-20 (tf32) of
+ * |a b| -- and the chunk-sized products as three-pass tf32 warp-level MMAs; elsewhere
+ * every product is fp32 on the FP32 pipe (and three-pass tf32 warp-level MMAs for the
+ * chunk-sized ones).  Gates use the accurate expf; nothing is built with fast-math.
+ *
  * Ownership and ordering
  * ----------------------
  * The caller owns every buffer and the stream; the library allocates no device memory
@@ -52,7 +63,9 @@
  * launched".  At head size 128 the scalar-gate path also uses three library streams per
  * device (created on first use): the call's stream forks into them and joins back with
  * events, so everything the call enqueues is ordered after earlier work on `stream` and
- * before later work on it; calls on one device enqueue one at a time.  The inputs and
+ * before later work on it.  Those streams are shared by every caller on the device, so
+ * such calls are serialised on the GPU even when their own streams are independent (and
+ * their host-side enqueueing takes a per-device lock).  The inputs and
  * ckpt must stay unchanged between gdn_forward and gdn_backward; the backward never
  * writes its inputs.  Inputs must be finite.
  *
@@ -150,7 +163,9 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
  * device current, looks up the array's address; make it before any stream capture.  All
  * calls on a device share the array (no call needs it zeroed: every scratch element a
  * call reads, it wrote first), so calls whose work overlaps on the GPU race on it:
- * order them on one stream or with events. */
+ * order them on one stream or with events.  The address is looked up once per device and
+ * kept: a process that calls cudaDeviceReset on a device must not use this entry point on
+ * it afterwards.  A device index of 64 or more returns GDN_ERR_UNSUPPORTED. */
 gdn_status_t gdn_backward_noalloc(const gdn_params_t* p, const float* q, const float* k,
                                   const float* v, const float* g, const float* beta,
                                   const float* ckpt, const float* gy, const float* dstate_T,

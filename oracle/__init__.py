@@ -67,6 +67,8 @@ def _bind(lib):
     lib.gdn_oracle_num_checkpoints.argtypes = [ctypes.c_int64, ctypes.c_int64]
     lib.gdn_oracle_num_checkpoints.restype = ctypes.c_int64
     lib.gdn_oracle_max_threads.restype = ctypes.c_int
+    lib.gdn_oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.gdn_oracle_set_threads.restype = None
     lib.gdn_oracle_mutation.restype = ctypes.c_int
     return lib
 
@@ -103,6 +105,11 @@ def num_checkpoints(T: int, C: int) -> int:
 
 def max_threads(lib=None) -> int:
     return int((lib or load()).gdn_oracle_max_threads())
+
+
+def set_threads(n: int, lib=None) -> None:
+    """Threads of the oracle's loop over (sequence, value head) units from now on."""
+    (lib or load()).gdn_oracle_set_threads(int(n))
 
 
 def _f64(x):

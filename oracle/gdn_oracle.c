@@ -78,6 +78,18 @@ int gdn_oracle_max_threads(void)
 #endif
 }
 
+/* Host-side thread count of the OpenMP loops over (sequence, value head); n < 1 leaves it
+ * unchanged.  Lets a timing run use all host cores or one.  No arithmetic depends on it:
+ * every unit is computed by one thread in the same order whatever the count. */
+void gdn_oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int gdn_oracle_mutation(void) { return GDN_ORACLE_MUTATION; }
 
 /* The key head that serves value head hv. */

@@ -2,10 +2,10 @@
 
 Tolerance (fp32 kernels vs float64 oracle): max |err| <= 2e-4 (1 + |ref|) for T <= 2048
 and <= 1e-3 (1 + |ref|) beyond, on every output: y, state_T, the checkpoints and every
-region of the packed gradient.  Small and mid-size problems are checked in full (they
-span several tiles, several sub-segments and a ragged last segment); the full-size
-workloads are checked on sampled (sequence, key-head group) units, each a complete
-independent problem the oracle solves on its own.
+region of the packed gradient.  The problems here are small and mid-size and are checked
+in full: they span several tiles, several sub-segments and a ragged last segment, and
+cover the degenerate cases (one token, empty sequences, an empty batch).  The full-size
+workloads and the throughput sweep are in test_gpu_fullsize.py.
 """
 import numpy as np
 import pytest
@@ -47,54 +47,6 @@ def test_mid_size_full(kda, d):
     prob = synth.make_problem(2, 300, 2, 6, d, kda=kda, seed=31 + d, C=17, packed=True,
                               dstate_T=True)
     full_check(prob)
-
-
-@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
-@pytest.mark.parametrize("d", [32, 64])
-def test_sweep_T512(kda, d):
-    prob = synth.make_problem(1, 512, 16, 48, d, kda=kda, seed=2100 + d + kda, packed=True)
-    full_check(prob)
-
-
-def test_bcast_d128_T2048_sampled():
-    prob = synth.workload("bcast_d128_T2048")
-    gpu, _ = H.run_gpu(prob)
-    for n, hk in ((0, 0), (3, 15), (1, 7)):
-        H.compare_group(gpu, prob, n, hk, prob.C)
-
-
-def test_bench_d128_T4096_sampled():
-    prob = synth.workload("bench_d128_T4096")
-    gpu, _ = H.run_gpu(prob)
-    for n, hk in ((0, 0), (0, 11)):
-        H.compare_group(gpu, prob, n, hk, prob.C)
-
-
-def test_kda_d128_T16384_sampled():
-    prob = synth.workload("kda_d128_T16384")
-    gpu, _ = H.run_gpu(prob)
-    for n, hk in ((0, 5),):
-        H.compare_group(gpu, prob, n, hk, prob.C)
-
-
-def _sweep_point(d, T, N, kda):
-    for pt in synth.sweep_points():
-        if (pt["d"], pt["T"], pt["N"], pt["kda"]) == (d, T, N, kda):
-            return pt
-    raise KeyError((d, T, N, kda))
-
-
-@pytest.mark.parametrize("d,T,N,kda", [
-    (32, 4096, 1, False), (32, 4096, 1, True), (64, 4096, 1, False), (64, 4096, 1, True),
-    (128, 512, 8, False), (64, 512, 8, True), (128, 16384, 1, False), (32, 16384, 1, True)],
-    ids=lambda x: str(x))
-def test_sweep_point_sampled(d, T, N, kda):
-    """Points of the throughput sweep at their full sizes (default C = ceil(sqrt(T)), the
-    sweep's seeds), checked on one (sequence, key-head group) unit: the last sequence and
-    key head 7."""
-    prob = synth.make_problem(**_sweep_point(d, T, N, kda))
-    gpu, _ = H.run_gpu(prob)
-    H.compare_group(gpu, prob, N - 1, 7, prob.C)
 
 
 @pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
