@@ -35,7 +35,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 # recompute 5 d^2 + reverse step 15 d^2.
 FWD_FLOPS = lambda d: 7 * d * d
 BWD_FLOPS = lambda d: 20 * d * d
-BC = 32  # chunk length of the chunked (scalar-gate) kernels
+BC = 32  # chunk length of the chunked kernels
 
 
 def chunk_kernel_flops(N, T, H_v, d, C, which):
@@ -257,7 +257,7 @@ class ClockSampler:
 # The sources each family of kernels is built from, launch code included: the chunked
 # (tensor-core and FP32) path and the token recurrence.
 CHUNKED_SOURCES = ("gdn_api.cu", "gdn_chunk.cu", "gdn_gemm.cuh", "gdn_internal.h", "gdn_tc.cuh",
-                   "gdn_tc_chain.cu", "gdn_tc_grad.cu")
+                   "gdn_tc_chain.cu", "gdn_tc_grad.cu", "gdn_kda_prep.cuh")
 TOKEN_SOURCES = ("gdn_api.cu", "gdn_internal.h", "gdn_device.cuh", "gdn_fwd.cu", "gdn_bwd.cu")
 
 
@@ -265,16 +265,21 @@ def _kernel_sha(kernel):
     """Hash of the sources `kernel` is built from: a recorded ncu figure stays valid while
     they do not change."""
     token = kernel.split("(")[0] in ("gdn_fwd_kernel", "gdn_bwd_kernel", "gdn_reduce_kernel")
+    return _sources_sha(not token)
+
+
+def _sources_sha(chunked):
+    """Hash of the chunked path's or the token recurrence's sources."""
     h = hashlib.sha256()
-    for f in TOKEN_SOURCES if token else CHUNKED_SOURCES:
+    for f in CHUNKED_SOURCES if chunked else TOKEN_SOURCES:
         h.update(open(os.path.join(ROOT, "gated_delta_rule_backward_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def _recorded_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"{kernel.split('(')[0]}_bench_d128_T4096.md")
+def _recorded_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel.split('(')[0]}_{workload}.md")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -301,10 +306,7 @@ def _recorded_step_traffic(workload, chunked):
         if line.startswith("- ") and ":" in line:
             k, v = line[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    h = hashlib.sha256()
-    for f in (CHUNKED_SOURCES if chunked else TOKEN_SOURCES):
-        h.update(open(os.path.join(ROOT, "gated_delta_rule_backward_gb300", "csrc", f), "rb").read())
-    if vals.get("kernel_sources_sha") != h.hexdigest()[:16]:
+    if vals.get("kernel_sources_sha") != _sources_sha(chunked):
         return None
     try:
         return float(vals["dram_bytes_per_step"])
@@ -485,7 +487,8 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     n_launch_fwd, n_launch_bwd = gdn.launches(p)
     n_fwd, n_bwd = gdn.timing_stages(p)
-    chunked = not prob.kda
+    # the chunked (WY) kernels: the scalar gate at every head size, the KDA gate at 128
+    chunked = (not prob.kda) or d == 128
     fplan, bplan = kernel_plan(chunked, d, n_bwd, -(-C // BC))
     fwd_names, bwd_names = [nm for nm, _ in fplan], [nm for nm, _ in bplan]
     kinds = [k for _, k in fplan + bplan] if chunked else None
@@ -652,7 +655,7 @@ def run_ours(args):
     step_traffic = _recorded_step_traffic(args.workload, chunked)
     # the dominant kernel (largest staged stage time): what it executes and moves
     top_ms = kern_ms[top]
-    top_traffic = _recorded_traffic(names[top])
+    top_traffic = _recorded_traffic(names[top], args.workload)
     dom = {"kernel": names[top], "ms": top_ms, "share_of_staged_stages": top_ms / sum(kern_ms),
            "dram_bytes_per_launch": top_traffic,
            "dram_over_step_compulsory": (top_traffic / comp) if top_traffic else None,

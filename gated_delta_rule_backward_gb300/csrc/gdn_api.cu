@@ -41,9 +41,9 @@ int64_t ceil_sqrt(int64_t T)
     return r;
 }
 
-// Launch plan: everything the kernels and the workspace sizes depend on.  The scalar
-// gate runs the chunked (WY) kernels; the per-key-column (KDA) gate and the degenerate
-// T = 0 case run the token recurrence kernels.
+// Launch plan: everything the kernels and the workspace sizes depend on.  The scalar gate,
+// and the per-key-column (KDA) gate at head size 128, run the chunked (WY) kernels; the KDA
+// gate at head sizes 32 and 64 and the degenerate T = 0 case run the token recurrence.
 struct Plan {
     int D = 0, RT = 1, W = 4, R = 16, P = 1, tc = 32, c2 = 1, nsub_max = 1;
     bool kda = false;
@@ -55,7 +55,8 @@ struct Plan {
     int64_t n_chunks = 0; // chunks per (sequence, value head)
     long long o_T = 0, o_QKD = 0, o_QDT = 0, o_gam = 0, o_r = 0, o_W = 0, o_U = 0, o_Mc = 0, o_dM = 0,
               o_dDel = 0, o_dX = 0, o_Tr = 0, o_Z = 0, o_KK = 0, o_QK = 0, o_Dm = 0, o_W1 = 0, o_Q1 = 0, o_B23 = 0, o_DK = 0, o_DS = 0,
-              o_dqM = 0, o_dkM = 0, o_carry = 0, o_carry_b = 0;
+              o_dqM = 0, o_dkM = 0, o_carry = 0, o_carry_b = 0, o_gL = 0, o_KG = 0, o_KRT = 0, o_kGam = 0,
+              o_kR = 0;
     bool tensor = false;  // head size 128: the state chain runs on the tensor cores
     size_t fwd_ws_bytes = 0, bwd_ws_bytes = 0;
 };
@@ -131,7 +132,7 @@ Plan make_plan(const gdn_params_t* p)
     pl.off_sc = pl.off_col + align256(col_f * 4);
     pl.ws_bytes = pl.off_sc + align256(sc_f * 4);
 
-    pl.chunked = !pl.kda && p->T > 0;
+    pl.chunked = p->T > 0 && (!pl.kda || pl.D == 128);
     if (pl.chunked) {
         const int64_t BC = gdn::BC;
         pl.cps = (int)((pl.C + BC - 1) / BC);
@@ -140,20 +141,28 @@ Plan make_plan(const gdn_params_t* p)
         const int64_t CH = p->n_seq * p->H_v * pl.n_chunks;
         const int64_t CK = p->n_seq * p->H_k * pl.n_chunks;
         const int64_t D = pl.D;
+        pl.tensor = (D == 128);
+        // the blocks the scalar gate keeps once per key head (Q, K, [Q^T | K^T]) carry the
+        // per-value-head decay with the KDA gate: one per value head
+        const int64_t CKq = pl.kda ? CH : CK;
         // float offsets, each sub-array 256-byte aligned
         auto al = [](int64_t f) { return (long long)((f + 63) & ~int64_t(63)); };
         long long o = 0;
-        pl.o_T = o;   o += al(CH * BC * BC);
-        pl.o_QKD = o; o += al(CH * BC * BC);
-        pl.o_QDT = o; o += al(CH * BC * BC);
+        if (!pl.tensor) {  // the FP32 chains' operands T^T, QD, QD^T
+            pl.o_T = o;   o += al(CH * BC * BC);
+            pl.o_QKD = o; o += al(CH * BC * BC);
+            pl.o_QDT = o; o += al(CH * BC * BC);
+        }
         pl.o_gam = o; o += al(CH * BC);
         pl.o_r = o;   o += al(CH * BC);
+        if (pl.kda) {  // gamma_last per column, written by both preps
+            pl.o_gL = o; o += al(CH * D);
+        }
         const long long common = o;
-        pl.tensor = (D == 128);
         if (pl.tensor) {  // U^T in fp32 and the tf32 hi/lo operands, tensor-core layout
             pl.o_U = o;   o += al(CH * BC * D);
             pl.o_W1 = o;  o += al(CH * gdn::kTcWElems);
-            pl.o_Q1 = o;  o += al(CK * gdn::kTcQElems);
+            pl.o_Q1 = o;  o += al(CKq * gdn::kTcQElems);
             pl.o_B23 = o; o += al(CH * gdn::kTcB23Elems);
             pl.o_carry = o; o += al(p->n_seq * p->H_v * D * D);  // forward: state between ranges
         } else {
@@ -171,16 +180,24 @@ Plan make_plan(const gdn_params_t* p)
         pl.o_Z = o;    o += al(CH * BC * BC);
         pl.o_KK = o;   o += al(CH * BC * BC);
         pl.o_QK = o;   o += al(CH * BC * BC);
-        pl.o_Dm = o;   o += al(CH * BC * BC);
+        if (!pl.kda) {
+            pl.o_Dm = o; o += al(CH * BC * BC);
+        }
         pl.o_dM = o;   o += al(CH * D * D);
         pl.o_dDel = o; o += al(CH * BC * D);
         pl.o_dX = o;   o += al(CH * BC * D);
         if (pl.tensor) {
-            pl.o_DK = o;  o += al(CK * gdn::kTcDkElems);
+            pl.o_DK = o;  o += al(CKq * gdn::kTcDkElems);
             pl.o_DS = o;  o += al(CH * gdn::kTcDsElems);
             pl.o_dqM = o; o += al(CH * BC * D);
             pl.o_dkM = o; o += al(CH * BC * D);
             pl.o_carry_b = o; o += al(p->n_seq * p->H_v * D * D);  // dM between ranges
+            if (pl.kda) {  // the gradient step's K (.) gamma, (K (.) R)^T tiles, gamma and R
+                pl.o_KG = o;   o += al(CH * gdn::kTcKdaTile);
+                pl.o_KRT = o;  o += al(CH * gdn::kTcKdaTile);
+                pl.o_kGam = o; o += al(CH * BC * D);
+                pl.o_kR = o;   o += al(CH * BC * D);
+            }
         }
         pl.bwd_ws_bytes = (size_t)o * 4;
         pl.ws_bytes = pl.bwd_ws_bytes;
@@ -249,6 +266,8 @@ void fill_chunk_common(gdn::ChunkArgs& c, const gdn_params_t* p, const Plan& pl)
     c.o_Tr = pl.o_Tr; c.o_Z = pl.o_Z; c.o_KK = pl.o_KK; c.o_QK = pl.o_QK; c.o_Dm = pl.o_Dm;
     c.o_W1 = pl.o_W1; c.o_Q1 = pl.o_Q1; c.o_B23 = pl.o_B23; c.o_DK = pl.o_DK; c.o_DS = pl.o_DS;
     c.o_dqM = pl.o_dqM; c.o_dkM = pl.o_dkM;
+    c.o_gL = pl.o_gL; c.o_KG = pl.o_KG; c.o_KRT = pl.o_KRT; c.o_kGam = pl.o_kGam; c.o_kR = pl.o_kR;
+    c.kda = pl.kda;
     c.want_tc = pl.tensor;
     c.c_lo = 0;
     c.c_hi = (int)pl.n_chunks;
@@ -579,6 +598,7 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, 
         c.carry = pl.tensor ? c.ws + pl.o_carry : nullptr;
         c.want_wu = 1;
         c.vec_q = vec_ok(q, p->q_s); c.vec_k = vec_ok(k, p->k_s); c.vec_v = vec_ok(v, p->v_s);
+        c.vec_g = aligned(g, 16);
         return cuda_status(gdn::launch_chunk_forward(c, pl.D, stream, tap), "forward launch");
     }
 
@@ -653,6 +673,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
         c.want_factors = 1;
         c.vec_q = vec_ok(q, p->q_s); c.vec_k = vec_ok(k, p->k_s); c.vec_v = vec_ok(v, p->v_s);
         c.vec_gy = vec_ok(gy, p->gy_s);
+        c.vec_g = aligned(g, 16);
         return cuda_status(gdn::launch_chunk_backward(c, pl.D, stream, tap), "backward launch");
     }
 

@@ -235,6 +235,77 @@ __device__ __forceinline__ void mma_32x128_origin(int tid, int& m, int& n)
     n = 32 * (tid >> 6) + 2 * (tid & 3);
 }
 
+// Z = (I + A)^-1 for a strictly lower 32 x 32 A, and T = Z diag(beta).  On entry Ts holds
+// A (row stride LDB), Zs is zero and the CTA is synchronised; Pw is a 32 x LDB tile whose
+// strict upper half (columns > rows) is zero: it serves as scratch and is zero again on
+// return.  Blockwise: [[I + A11, 0], [A21, I + A22]]^-1 = [[Z11, 0], [-Z22 A21 Z11, Z22]],
+// from four 8 x 8 diagonal blocks (forward substitution) up to 32 x 32.  Leaves Z in Zs and
+// T in Ts; ends with a __syncthreads.
+__device__ void unit_lower_inverse(float* Ts, float* Zs, float* Pw, const float* bs, int tid)
+{
+    if (tid < 32) {  // diagonal 8 x 8 blocks: lane = 8 block + column
+        const int r0 = (tid >> 3) * 8, j = r0 + (tid & 7);
+        float z[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int row = r0 + t;
+            float acc = 0.f;
+#pragma unroll
+            for (int tau = 0; tau < t; ++tau)
+                if (r0 + tau >= j) acc = __fmaf_rn(Ts[row * LDB + r0 + tau], z[tau], acc);
+            z[t] = (row < j) ? 0.f : (row == j ? 1.f : -acc);
+            Zs[row * LDB + j] = z[t];
+        }
+    }
+    __syncthreads();
+    // level 16: blocks (1,0) and (3,2) of 8 x 8: Z_ij = -Z_ii A_ij Z_jj
+    if (tid < 128) {
+        const int b = tid >> 6, e = tid & 63, rr = e >> 3, cc = e & 7;
+        const int i0 = 8 + 16 * b, j0 = 16 * b;  // block rows i0.., cols j0..
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc = __fmaf_rn(Ts[(i0 + rr) * LDB + j0 + k], Zs[(j0 + k) * LDB + j0 + cc], acc);
+        Pw[(j0 + cc) * LDB + i0 + rr] = acc;  // stored transposed in Pw's upper half
+    }
+    __syncthreads();
+    if (tid < 128) {
+        const int b = tid >> 6, e = tid & 63, rr = e >> 3, cc = e & 7;
+        const int i0 = 8 + 16 * b, j0 = 16 * b;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc = __fmaf_rn(Zs[(i0 + rr) * LDB + i0 + k], Pw[(j0 + cc) * LDB + i0 + k], acc);
+        Zs[(i0 + rr) * LDB + j0 + cc] = -acc;
+    }
+    __syncthreads();
+    // level 32: Z21 (rows 16..31, cols 0..15) = -Z22 A21 Z11
+    {
+        const int rr = tid >> 4, cc = tid & 15;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc = __fmaf_rn(Ts[(16 + rr) * LDB + k], Zs[k * LDB + cc], acc);
+        Pw[cc * LDB + 16 + rr] = acc;  // transposed, in Pw's upper half
+    }
+    __syncthreads();
+    {
+        const int rr = tid >> 4, cc = tid & 15;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc = __fmaf_rn(Zs[(16 + rr) * LDB + 16 + k], Pw[cc * LDB + 16 + k], acc);
+        Zs[(16 + rr) * LDB + cc] = -acc;
+    }
+    __syncthreads();
+    // restore Pw's strict upper half to zero
+    for (int idx = tid; idx < BC * BC; idx += CT) {
+        const int t = idx / BC, tau = idx - t * BC;
+        if (tau > t) Pw[t * LDB + tau] = 0.f;
+    }
+    for (int idx = tid; idx < BC * BC; idx += CT) {
+        const int t = idx / BC, tau = idx - t * BC;
+        Ts[t * LDB + tau] = __fmul_rn(Zs[t * LDB + tau], bs[tau]);
+    }
+    __syncthreads();
+}
+
 // Chunk-local quantities from Q, K (shared, [Q; K] stacked, zero-padded rows), g, beta.
 // Out: G (inclusive cumsum), gam = exp(G), Dm (lower incl), KKm = K K^T (strict lower),
 // QKm = Q K^T (lower incl), Zs = (I + diag(beta) (Dm (.) KK))^-1, Ts = Zs diag(beta).
@@ -281,10 +352,7 @@ __device__ void chunk_prep(const float* QKs, const float* gs, const float* bs, f
         Dm[t * LDB + tau] = (tau <= t) ? expf(__fsub_rn(Gs[t], Gs[tau])) : 0.f;
     }
     __syncthreads();
-    // Z = (I + A)^-1 with A = diag(beta) (Dm (.) KK) strictly lower, blockwise:
-    // [[I + A11, 0], [A21, I + A22]]^-1 = [[Z11, 0], [-Z22 A21 Z11, Z22]],
-    // from four 8 x 8 diagonal blocks (forward substitution) up to 32 x 32.
-    // Ts holds A meanwhile.
+    // Z = (I + A)^-1 with A = diag(beta) (Dm (.) KK) strictly lower; Ts holds A meanwhile
     for (int idx = tid; idx < BC * BC; idx += CT) {
         const int t = idx / BC, tau = idx - t * BC;
         Ts[t * LDB + tau] = (tau < t) ? __fmul_rn(bs[t], __fmul_rn(Dm[t * LDB + tau], KKm[t * LDB + tau]))
@@ -292,68 +360,7 @@ __device__ void chunk_prep(const float* QKs, const float* gs, const float* bs, f
         Zs[t * LDB + tau] = 0.f;
     }
     __syncthreads();
-    if (tid < 32) {  // diagonal 8 x 8 blocks: lane = 8 block + column
-        const int r0 = (tid >> 3) * 8, j = r0 + (tid & 7);
-        float z[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const int row = r0 + t;
-            float acc = 0.f;
-#pragma unroll
-            for (int tau = 0; tau < t; ++tau)
-                if (r0 + tau >= j) acc = __fmaf_rn(Ts[row * LDB + r0 + tau], z[tau], acc);
-            z[t] = (row < j) ? 0.f : (row == j ? 1.f : -acc);
-            Zs[row * LDB + j] = z[t];
-        }
-    }
-    __syncthreads();
-    // level 16: blocks (1,0) and (3,2) of 8 x 8: Z_ij = -Z_ii A_ij Z_jj
-    float* Pw = Dm;  // scratch in Dm's strict upper half (columns > rows), zero otherwise
-    if (tid < 128) {
-        const int b = tid >> 6, e = tid & 63, rr = e >> 3, cc = e & 7;
-        const int i0 = 8 + 16 * b, j0 = 16 * b;  // block rows i0.., cols j0..
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc = __fmaf_rn(Ts[(i0 + rr) * LDB + j0 + k], Zs[(j0 + k) * LDB + j0 + cc], acc);
-        Pw[(j0 + cc) * LDB + i0 + rr] = acc;  // stored transposed in Dm's upper half
-    }
-    __syncthreads();
-    if (tid < 128) {
-        const int b = tid >> 6, e = tid & 63, rr = e >> 3, cc = e & 7;
-        const int i0 = 8 + 16 * b, j0 = 16 * b;
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc = __fmaf_rn(Zs[(i0 + rr) * LDB + i0 + k], Pw[(j0 + cc) * LDB + i0 + k], acc);
-        Zs[(i0 + rr) * LDB + j0 + cc] = -acc;
-    }
-    __syncthreads();
-    // level 32: Z21 (rows 16..31, cols 0..15) = -Z22 A21 Z11
-    {
-        const int rr = tid >> 4, cc = tid & 15;
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) acc = __fmaf_rn(Ts[(16 + rr) * LDB + k], Zs[k * LDB + cc], acc);
-        Pw[cc * LDB + 16 + rr] = acc;  // transposed, in Dm's upper half
-    }
-    __syncthreads();
-    {
-        const int rr = tid >> 4, cc = tid & 15;
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) acc = __fmaf_rn(Zs[(16 + rr) * LDB + 16 + k], Pw[cc * LDB + 16 + k], acc);
-        Zs[(16 + rr) * LDB + cc] = -acc;
-    }
-    __syncthreads();
-    // restore Dm's upper half to zero
-    for (int idx = tid; idx < BC * BC; idx += CT) {
-        const int t = idx / BC, tau = idx - t * BC;
-        if (tau > t) Dm[t * LDB + tau] = 0.f;
-    }
-    for (int idx = tid; idx < BC * BC; idx += CT) {
-        const int t = idx / BC, tau = idx - t * BC;
-        Ts[t * LDB + tau] = __fmul_rn(Zs[t * LDB + tau], bs[tau]);
-    }
-    __syncthreads();
+    unit_lower_inverse(Ts, Zs, Dm, bs, tid);  // Dm's strict upper half is zero
 }
 
 __device__ __forceinline__ void load_gate_beta(const ChunkArgs& A, int n, int h, const ChunkPos& cp,
@@ -634,6 +641,12 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
 #pragma unroll
         for (int j = 0; j < 4; ++j) wsU[Map::col(tid, j) * BC + Map::row(tid, i)] = acc[i][j];
 }
+
+}  // namespace gdn
+
+#include "gdn_kda_prep.cuh"
+
+namespace gdn {
 
 // ---------------------------------------------------------------------------------
 // State chain, rows [p RR, p RR + RR) of M for one head.
@@ -1340,6 +1353,10 @@ size_t prep_smem()
 {
     return sizeof(float) * (3 * BC * Ld<D>::v + 5 * BC * LDB + 4 * BC);
 }
+size_t kda_prep_smem()
+{
+    return sizeof(float) * (5 * BC * Ld<128>::v + 4 * BC * LDB + BC);
+}
 template <int D>
 size_t state_smem()
 {
@@ -1390,6 +1407,12 @@ static int launch_prep_range(const ChunkArgs& a, int R, bool backward, int r, cu
 {
     ChunkArgs ar;
     range_of(a, R, backward, r, ar);
+    if (a.kda) {
+        int err = set_smem(gdn_kda_prep_kernel, kda_prep_smem());
+        if (err) return err;
+        gdn_kda_prep_kernel<<<dim3((ar.c_hi - ar.c_lo) * a.H_v, a.N), CT, kda_prep_smem(), st>>>(ar);
+        return (int)cudaGetLastError();
+    }
     int err = set_smem(gdn_chunk_prep_kernel<128>, prep_smem<128>());
     if (err) return err;
     gdn_chunk_prep_kernel<128><<<dim3((ar.c_hi - ar.c_lo) * a.H_v, a.N), CT, prep_smem<128>(), st>>>(ar);

@@ -103,6 +103,11 @@ struct ChunkArgs {
     long long o_W1, o_Q1, o_B23;            // tensor-core operands of the state chain
     long long o_DK, o_DS;                   // tensor-core operands of the dM chain
     long long o_dqM, o_dkM;                 // tensor-core gradient step: per value head dq, dk
+    // per-key-column (KDA) gate, head size 128, per (sequence, value head, chunk): gamma_last
+    // (128 floats), the bf16 hi/lo tiles K (.) gamma (rows t) and (K (.) R)^T (rows i), and
+    // gamma, R in fp32 (rows t)
+    long long o_gL, o_KG, o_KRT, o_kGam, o_kR;
+    int kda;
     int want_wu;
     int want_factors;
     int want_tc;                            // head size 128: state chain on the tensor cores
@@ -110,7 +115,7 @@ struct ChunkArgs {
     int grad_loc;                           // gradient launch: -1 for every chunk of [c_lo, c_hi),
                                             // else only the chunks at this place in their segment
     float* carry;                           // [N][H_v][D][D] state (or dM) between ranges
-    int vec_q, vec_k, vec_v, vec_gy;
+    int vec_q, vec_k, vec_v, vec_gy, vec_g;
 };
 
 // Records caller-provided timing events around the stages of one call: mark() before
@@ -176,6 +181,8 @@ constexpr int kDsE = kDsG + 128 * 32;
 constexpr int kDsR = kDsE + 128 * 32;
 constexpr int kDsGam = kDsR + 32;
 constexpr int kTcDsElems = kDsGam + 32;
+// KDA gate: floats of one 32 x 128 bf16 hi/lo tile (K (.) gamma, or (K (.) R)^T).
+constexpr int kTcKdaTile = 32 * 128;
 
 int launch_chunk_forward(const ChunkArgs& a, int D, void* stream, EventTap& tap);
 // The chains on the tensor cores (gdn_tc_chain.cu): the forward's state chain and the

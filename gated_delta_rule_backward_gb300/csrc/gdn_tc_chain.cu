@@ -70,14 +70,18 @@ constexpr int kSDel = kSU + BC * TD;               // staging of checkpoint rows
 constexpr int kSGam = kSDel + 2 * BC * TD;         // gamma (32)
 constexpr int kStageLd = TD + 4;                   // staging rows for coalesced global writes
 constexpr int kSY = kSGam + BC;                    // y of two chunks, rows t (forward)
-constexpr int kSFloats = kSY + 2 * BC * kStageLd;
+constexpr int kSGl = kSY + 2 * BC * kStageLd;      // KDA: gamma_last per column, two buffers by
+                                                   // chunk parity (the next chunk's lands while
+                                                   // this one's update reads)
+constexpr int kSFloats = kSGl + 2 * TD;
 constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 128;  // + barriers (6 used)
 
 constexpr uint32_t kB1Bytes = sizeof(float) * (kTcWElems + kTcQElems);
 constexpr int kHalfW = kTcWElems / 2;  // 32 x 128 bf16 values
 constexpr uint32_t kB23Bytes = sizeof(float) * kTcB23Elems + sizeof(float) * BC * TD + sizeof(float) * BC;
 
-// [W; Q] hi then lo: W of the value head and Q of its key head, stacked by row groups.
+// [W; Q] hi then lo: W of the value head and Q of its key head (KDA: Q (.) gamma of the value
+// head; the caller passes that block's index as ck), stacked by row groups.
 __device__ __forceinline__ void load_b1(const ChunkArgs& A, long long ch, long long ck, float* sm, uint64_t* bar)
 {
     const float* w = A.ws + A.o_W1 + ch * kTcWElems;
@@ -90,17 +94,23 @@ __device__ __forceinline__ void load_b1(const ChunkArgs& A, long long ch, long l
     tc::bulk_g2s(sm + kSB1 + 3 * kHalfW, q + kHalfW, part, bar);
 }
 
-__device__ __forceinline__ void load_b23(const ChunkArgs& A, long long ch, float* sm, uint64_t* bar)
+// [scale QD; (r K)^T], U^T and gamma of chunk c; KDA: also gamma_last (per column) into the
+// buffer of c's parity.
+template <bool KDA>
+__device__ __forceinline__ void load_b23(const ChunkArgs& A, long long ch, int c, float* sm, uint64_t* bar)
 {
-    tc::mbar_expect_tx(bar, kB23Bytes);
+    tc::mbar_expect_tx(bar, kB23Bytes + (KDA ? (uint32_t)sizeof(float) * TD : 0u));
     tc::bulk_g2s(sm + kSB23, A.ws + A.o_B23 + ch * kTcB23Elems, sizeof(float) * kTcB23Elems, bar);
     tc::bulk_g2s(sm + kSU, A.ws + A.o_U + ch * (BC * TD), sizeof(float) * BC * TD, bar);
     tc::bulk_g2s(sm + kSGam, A.ws + A.o_gam + ch * BC, sizeof(float) * BC, bar);
+    if (KDA) tc::bulk_g2s(sm + kSGl + (c & 1) * TD, A.ws + A.o_gL + ch * TD, sizeof(float) * TD, bar);
 }
 
 }  // namespace
 
 // The state chain of one head (bx = head, by = sequence); sm is the dynamic shared memory.
+// KDA: the per-key-column gate (operands per value head, M decayed column by column).
+template <bool KDA>
 __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int bx, int by)
 {
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSFloats);  // b1, b23, mma, a[8]
@@ -121,7 +131,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
 
     const int h = bx, n = by, c_begin = A.c_lo, c_end = A.c_hi;
     const long long head = (long long)n * A.H_v + h;
-    const long long khead = (long long)n * A.H_k + h % A.H_k;
+    const long long khead = KDA ? head : (long long)n * A.H_k + h % A.H_k;
 
     if (tid == 0) {
         tc::mbar_init(bar_b1, 1);
@@ -145,7 +155,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     if (issuer) {
         tc::prefetch_l2(A.ws + A.o_U + (head * A.n_chunks + c_begin) * (BC * TD));  // see prefetch_l2
         load_b1(A, head * A.n_chunks + c_begin, khead * A.n_chunks + c_begin, sm, bar_b1);
-        load_b23(A, head * A.n_chunks + c_begin, sm, bar_b23);
+        load_b23<KDA>(A, head * A.n_chunks + c_begin, c_begin, sm, bar_b23);
         b1_pending = b23_pending = true;
     }
 
@@ -366,7 +376,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         if (issuer) {
             if (c + 1 < c_end) {
                 tc::fence_async_smem();
-                load_b23(A, ch + 1, sm, bar_b23);
+                load_b23<KDA>(A, ch + 1, c + 1, sm, bar_b23);
                 b23_pending = true;
             }
         } else if (compute) {
@@ -387,8 +397,14 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 float x[8];
                 tc::ld8(tc::taddr(tmem, warp, kColD23 + BC + 64 * hc + 8 * q), x);
                 tc::wait_ld();
+                if (KDA) {  // column 64 hc + 8 q + e decays by its own gamma_last
+                    const float* sgl = sm + kSGl + (c & 1) * TD + 64 * hc + 8 * q;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m[8 * q + e] = __fmaf_rn(gl, m[8 * q + e], x[e]);
+                    for (int e = 0; e < 8; ++e) m[8 * q + e] = __fmaf_rn(sgl[e], m[8 * q + e], x[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) m[8 * q + e] = __fmaf_rn(gl, m[8 * q + e], x[e]);
+                }
                 split_store(q);
                 if ((q & 3) == 3) release_group(q >> 2);
             }
@@ -440,7 +456,8 @@ constexpr int kSmG = kSmQKT + kTcDkElems - kDkQKT;
 constexpr int kSmE = kSmG + kDsE - kDsG;
 constexpr int kSmR = kSmE + kDsR - kDsE;
 constexpr int kSmGam = kSmR + kDsGam - kDsR;
-constexpr int kDsFloats = kSmGam + BC;
+constexpr int kSmGl = kSmGam + BC;  // KDA: gamma_last per column, two buffers by chunk parity
+constexpr int kDsFloats = kSmGl + 2 * TD;
 constexpr size_t kDsSmemBytes = sizeof(float) * kDsFloats + 64;
 constexpr uint32_t kDsBytesKb = sizeof(float) * (kDkQKT - kDkKb);
 constexpr uint32_t kDsBytesTT = sizeof(float) * (kDsG - kDsTT);
@@ -452,16 +469,21 @@ __device__ __forceinline__ void ds_load_kb(const ChunkArgs& A, long long ck, flo
     tc::mbar_expect_tx(bar, kDsBytesKb);
     tc::bulk_g2s(sm + kSmKb, A.ws + A.o_DK + ck * kTcDkElems + kDkKb, kDsBytesKb, bar);
 }
-__device__ __forceinline__ void ds_load_rest(const ChunkArgs& A, long long ch, long long ck, float* sm,
+template <bool KDA>
+__device__ __forceinline__ void ds_load_rest(const ChunkArgs& A, long long ch, long long ck, int c, float* sm,
                                              uint64_t* bar)
 {
-    tc::mbar_expect_tx(bar, kDsBytesTT + kDsBytesQKT + kDsBytesTail);
+    tc::mbar_expect_tx(bar, kDsBytesTT + kDsBytesQKT + kDsBytesTail + (KDA ? (uint32_t)sizeof(float) * TD : 0u));
     tc::bulk_g2s(sm + kSmTT, A.ws + A.o_DS + ch * kTcDsElems + kDsTT, kDsBytesTT, bar);
     tc::bulk_g2s(sm + kSmQKT, A.ws + A.o_DK + ck * kTcDkElems + kDkQKT, kDsBytesQKT, bar);
     tc::bulk_g2s(sm + kSmG, A.ws + A.o_DS + ch * kTcDsElems + kDsG, kDsBytesTail, bar);
+    if (KDA) tc::bulk_g2s(sm + kSmGl + (c & 1) * TD, A.ws + A.o_gL + ch * TD, sizeof(float) * TD, bar);
 }
 }  // namespace
 
+// KDA: the per-key-column gate (K (.) R and [Q (.) gamma; K (.) gamma] per value head, r = gamma = 1,
+// dM decayed column by column).
+template <bool KDA>
 __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int h, int n)
 {
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kDsFloats);  // kb, rest, mma, x, y
@@ -479,7 +501,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
     const int j = 32 * (warp & 3) + lane;   // row of dM
     const int hc = (warp >> 2) & 1;         // dM columns [64 hc, 64 hc + 64); chunk columns [16 hc, 16 hc + 16)
     const long long head = (long long)n * A.H_v + h;
-    const long long khead = (long long)n * A.H_k + h % A.H_k;
+    const long long khead = KDA ? head : (long long)n * A.H_k + h % A.H_k;
 
     if (tid == 0) {
         tc::mbar_init(bar_kb, 1);
@@ -504,7 +526,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
     if (issuer) {
         tc::prefetch_l2(A.ws + A.o_DS + (head * A.n_chunks + c_last) * kTcDsElems);  // see prefetch_l2
         ds_load_kb(A, khead * A.n_chunks + c_last, sm, bar_kb);
-        ds_load_rest(A, head * A.n_chunks + c_last, khead * A.n_chunks + c_last, sm, bar_rest);
+        ds_load_rest<KDA>(A, head * A.n_chunks + c_last, khead * A.n_chunks + c_last, c_last, sm, bar_rest);
         kb_pending = rest_pending = true;
     }
     float m[64];
@@ -712,7 +734,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
         if (issuer) {
             if (c > A.c_lo) {
                 tc::fence_async_smem();
-                ds_load_rest(A, ch - 1, khead * A.n_chunks + c - 1, sm, bar_rest);
+                ds_load_rest<KDA>(A, ch - 1, khead * A.n_chunks + c - 1, c - 1, sm, bar_rest);
                 rest_pending = true;
             }
         } else if (compute) {
@@ -721,8 +743,14 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
                 float x[32];
                 tc::ld32(tc::taddr(tmem, warp, kDsColC + 64 * hc + 32 * q), x);
                 tc::wait_ld();
+                if (KDA) {  // column 64 hc + 32 q + e decays by its own gamma_last
+                    const float* sgl = sm + kSmGl + (c & 1) * TD + 64 * hc + 32 * q;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) m[32 * q + e] = __fmaf_rn(gl, m[32 * q + e], x[e]);
+                    for (int e = 0; e < 32; ++e) m[32 * q + e] = __fmaf_rn(sgl[e], m[32 * q + e], x[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) m[32 * q + e] = __fmaf_rn(gl, m[32 * q + e], x[e]);
+                }
             }
         }
     }
@@ -746,37 +774,49 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
 }
 
 // The forward's state chain: one CTA per (head, sequence).
+template <bool KDA>
 __global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
 {
     extern __shared__ __align__(1024) float sm[];
-    state_chain(A, sm, blockIdx.x, blockIdx.y);
+    state_chain<KDA>(A, sm, blockIdx.x, blockIdx.y);
 }
 
 // The backward's dM chain: one CTA per (value head, sequence), over the chunks [c_lo, c_hi).
+template <bool KDA>
 __global__ void __launch_bounds__(TCT, 1) gdn_tc_dstate_kernel(const ChunkArgs A)
 {
     extern __shared__ __align__(1024) float sm[];
-    dstate_chain(A, sm, blockIdx.x, blockIdx.y);
+    dstate_chain<KDA>(A, sm, blockIdx.x, blockIdx.y);
+}
+
+template <bool KDA>
+static int launch_tc_state_t(const ChunkArgs& a, cudaStream_t s)
+{
+    int e = (int)cudaFuncSetAttribute(gdn_tc_state_kernel<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kSmemBytes);
+    if (e) return e;
+    gdn_tc_state_kernel<KDA><<<dim3(a.H_v, a.N), TCT, kSmemBytes, s>>>(a);
+    return (int)cudaGetLastError();
+}
+
+template <bool KDA>
+static int launch_tc_dstate_t(const ChunkArgs& a, cudaStream_t s)
+{
+    int e = (int)cudaFuncSetAttribute(gdn_tc_dstate_kernel<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kDsSmemBytes);
+    if (e) return e;
+    gdn_tc_dstate_kernel<KDA><<<dim3(a.H_v, a.N), TCT, kDsSmemBytes, s>>>(a);
+    return (int)cudaGetLastError();
 }
 
 int launch_tc_state(const ChunkArgs& a, void* stream)
 {
-    cudaStream_t s = (cudaStream_t)stream;
-    int e = (int)cudaFuncSetAttribute(gdn_tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kSmemBytes);
-    if (e) return e;
-    gdn_tc_state_kernel<<<dim3(a.H_v, a.N), TCT, kSmemBytes, s>>>(a);
-    return (int)cudaGetLastError();
+    return a.kda ? launch_tc_state_t<true>(a, (cudaStream_t)stream) : launch_tc_state_t<false>(a, (cudaStream_t)stream);
 }
 
 int launch_tc_dstate(const ChunkArgs& a, void* stream)
 {
-    cudaStream_t s = (cudaStream_t)stream;
-    int e = (int)cudaFuncSetAttribute(gdn_tc_dstate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kDsSmemBytes);
-    if (e) return e;
-    gdn_tc_dstate_kernel<<<dim3(a.H_v, a.N), TCT, kDsSmemBytes, s>>>(a);
-    return (int)cudaGetLastError();
+    return a.kda ? launch_tc_dstate_t<true>(a, (cudaStream_t)stream) : launch_tc_dstate_t<false>(a, (cudaStream_t)stream);
 }
 
 // A bounded wait on a barrier that nothing completes: gives up and records the timeout.

@@ -87,7 +87,12 @@ constexpr int kSR = kSGam + BC;
 constexpr int kSB = kSR + BC;
 constexpr int kSRed = kSB + BC;             // 4 lane quarters x 96 partial sums
 constexpr int kSVec = kSRed + 4 * 96;       // gdg, dr, dG, dbeta, dot
-constexpr int kGFloats = kSVec + 4 * BC + 4;
+// KDA gate: gamma_last (128), <dM, M> per column from the two column halves (2 x 128), and
+// the chunk-end gate partials of the two token halves (2 x 128)
+constexpr int kSGl = kSVec + 4 * BC + 4;
+constexpr int kSColS = kSGl + TD;
+constexpr int kSLast = kSColS + 2 * TD;
+constexpr int kGFloats = kSLast + 2 * TD;
 constexpr size_t kGSmemBytes = sizeof(float) * kGFloats + 64;
 static_assert(kGSmemBytes <= 227 * 1024, "shared memory");
 // 32 x 32 tiles in R1 after D2 is done: Ps, Ss, dTs, W1, W2, Zs (LDF), then the B tiles
@@ -99,6 +104,9 @@ constexpr int kAW2 = kAW1 + BC * LDF;
 constexpr int kAZ = kAW2 + BC * LDF;
 constexpr int kABP = kAZ + BC * LDF;        // P (rows t, K = 32) hi, lo
 constexpr int kABPS = kABP + 2 * kTP;       // [P ; S]^T (rows t, K = 64) hi, lo
+constexpr int kKcol = kR1 + 6 * BC * LDF;   // KDA, step (9): the column-side exchange and dG
+constexpr int kKdg = kKcol + BC * TD;
+static_assert(kKdg + BC * TD <= kR2, "KDA tiles overflow R1");
 static_assert(kABPS + 2 * kTPS <= kR2, "R1 overflow");
 constexpr int kDdStage = kR1 + 6 * BC * LDF;   // dDelta (unit layout, 8 x kLdU), then
 constexpr int kDyStage = kDdStage + BC * kLdM; // dY rows t (32 x kLdM), before the algebra
@@ -106,6 +114,14 @@ static_assert((BC / 4) * kLdU <= BC * kLdM && kDyStage + BC * kLdM <= kR2, "R1 o
 
 constexpr uint32_t kBytesKb = sizeof(float) * (kDkQKT - kDkKb);
 constexpr uint32_t kBytesFac = sizeof(float) * 5 * BC * BC;
+constexpr uint32_t kBytesFacKda = sizeof(float) * 4 * BC * BC;  // no decay matrix
+constexpr uint32_t kBytesKrt = sizeof(float) * kTcKdaTile;      // (K (.) R)^T, bf16 hi/lo
+// KDA tiles of step (9), dense rows of TD floats: q, k, a = exp(g), gamma in R0; the
+// (K (.) R)^T tile, R and the row-side exchange in R2; the column-side exchange and the gate
+// gradient in R1 after the 32 x 32 algebra tiles.
+constexpr int kKq = kR0, kKk = kR0 + BC * TD, kKa = kR0 + 2 * BC * TD, kKg = kR0 + 3 * BC * TD;
+constexpr int kKrt = kR2, kKr = kR2 + kTcKdaTile, kKrowQ = kKr + BC * TD, kKrowK = kKrowQ + BC * TD;
+static_assert(kKg + BC * TD <= kR1 && kKrowK + BC * TD <= kR3, "KDA tiles overflow R0 / R2");
 constexpr uint32_t kBytesGR = sizeof(float) * 2 * BC;
 constexpr uint32_t kBytesQKT = sizeof(float) * (kTcDkElems - kDkQKT);
 constexpr uint32_t kBytesState = sizeof(float) * TD * TD;
@@ -160,8 +176,139 @@ __device__ __forceinline__ void mma3_t(uint32_t d, uint32_t a_hi, uint32_t a_lo,
     }
 }
 
+// Step (9) of the KDA gradient on the CUDA cores (compute warps; thread = key column i = row,
+// half hc).  With P = dAqk (lower, diagonal included), S = dAkk (strictly lower) from the 32 x 32
+// algebra and E[t][tau] = a[tau + 1] ... a[t] per column (running products of a = exp(g), in
+// the prep's order):
+//   row side (hc = 0): dqA[t] = sum_tau P[t][tau] k[tau] E,   dkA+[t] = sum_tau S[t][tau] k[tau] E
+//   column side (hc = 1): dkA-[tau] = sum_t (P[t][tau] q[t] + S[t][tau] k[t]) E
+// Then, for this thread's tokens, with D2 = [d(Q (.) gamma) | d(K (.) gamma)] and
+// d3 = d(K (.) R) from the tensor cores:
+//   dq = gamma d(Q (.) gamma) + dqA,  dk+ = gamma d(K (.) gamma) + dkA+,
+//   dk- = R d(K (.) R) + dkA-,        dk = dk+ + dk-
+// and the gradient of the cumulative gate G (every factor exp(+G_t) or exp(-G_tau) of a
+// product gives q dq, k dk+ or -k dk-):
+//   dG[t] = q dq + k (dk+ - dk-),  dG[last] += sum_tau k R d(K (.) R) + gamma_last <dM, M>_i
+// dg is the reverse running sum of dG over the chunk.  Writes this value head's dq, dk parts
+// and dg; returns false if the wait for the tiles gave up.
+__device__ __forceinline__ bool kda_tail(const ChunkArgs& A, float* sm, uint32_t tmem, uint64_t* bar_kda, int tid,
+                                         int warp, int row, int hc, int tb, int nb, int t0, int n, int hk, int h,
+                                         long long ch, long long tok0, const float (&d3)[16])
+{
+    float* sQ = sm + kKq;
+    float* sK = sm + kKk;
+    float* sA = sm + kKa;
+    const float* sG = sm + kKg;
+    const float* sR = sm + kKr;
+    float* rowQ = sm + kKrowQ;
+    float* rowK = sm + kKrowK;
+    float* col = sm + kKcol;
+    float* dGs = sm + kKdg;
+    const float* Ps = sm + kAPs;
+    const float* Ss = sm + kASs;
+    const int i = row;
+    const bool rows_bulk = A.vec_q && A.vec_k && A.vec_g;
+    // the rows the copies leave out: the padding (q = k = 0, g = 0), and every row without them
+    for (int idx = tid; idx < BC * TD; idx += 256) {
+        const int t = idx / TD, c = idx - t * TD;
+        if (t >= nb) {
+            sQ[idx] = 0.f;
+            sK[idx] = 0.f;
+            sA[idx] = 0.f;
+        } else if (!rows_bulk) {
+            sQ[idx] = __ldg(A.q + (long long)n * A.qs0 + (long long)(t0 + t) * A.qs1 + (long long)hk * A.qs2 + c);
+            sK[idx] = __ldg(A.k + (long long)n * A.ks0 + (long long)(t0 + t) * A.ks1 + (long long)hk * A.ks2 + c);
+            sA[idx] = __ldg(A.g + ((tok0 + t) * A.H_v + h) * TD + c);
+        }
+    }
+    const bool ok = tc::mbar_wait(bar_kda, 0);
+    tc::bar_sync_first(256);
+    for (int idx = tid; idx < BC * TD; idx += 256) sA[idx] = expf(sA[idx]);
+    tc::bar_sync_first(256);
+    if (hc == 0) {
+        float kc[BC], E[BC];
+#pragma unroll
+        for (int tau = 0; tau < BC; ++tau) kc[tau] = sK[tau * TD + i];
+#pragma unroll
+        for (int t = 0; t < BC; ++t) {
+            const float at = sA[t * TD + i];
+#pragma unroll
+            for (int tau = 0; tau < t; ++tau) E[tau] = __fmul_rn(E[tau], at);
+            E[t] = 1.f;
+            float dq = 0.f, dk = 0.f;
+#pragma unroll
+            for (int tau = 0; tau <= t; ++tau) {
+                const float w = __fmul_rn(kc[tau], E[tau]);
+                dq = __fmaf_rn(Ps[t * LDF + tau], w, dq);
+                dk = __fmaf_rn(Ss[t * LDF + tau], w, dk);
+            }
+            rowQ[t * TD + i] = dq;
+            rowK[t * TD + i] = dk;
+        }
+    } else {
+        float E[BC], acc[BC];
+#pragma unroll
+        for (int t = 0; t < BC; ++t) {
+            const float at = sA[t * TD + i], qt = sQ[t * TD + i], kt = sK[t * TD + i];
+#pragma unroll
+            for (int tau = 0; tau < t; ++tau) E[tau] = __fmul_rn(E[tau], at);
+            E[t] = 1.f;
+            acc[t] = 0.f;
+#pragma unroll
+            for (int tau = 0; tau <= t; ++tau) {
+                const float pe = __fmaf_rn(Ss[t * LDF + tau], kt, __fmul_rn(Ps[t * LDF + tau], qt));
+                acc[tau] = __fmaf_rn(pe, E[tau], acc[tau]);
+            }
+        }
+#pragma unroll
+        for (int tau = 0; tau < BC; ++tau) col[tau * TD + i] = acc[tau];
+    }
+    tc::bar_sync_first(256);
+    {
+        float dQG[16], dKG[16];
+        tc::ld16(tc::taddr(tmem, warp, kC2 + tb), dQG);
+        tc::ld16(tc::taddr(tmem, warp, kC2 + BC + tb), dKG);
+        tc::wait_ld();
+        float* dqo = A.ws + A.o_dqM + ch * (BC * TD) + i;
+        float* dko = A.ws + A.o_dkM + ch * (BC * TD) + i;
+        float last = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int t = tb + e, o = t * TD + i;
+            const float gt = sG[o], qt = sQ[o], kt = sK[o];
+            const float dq = __fmaf_rn(gt, dQG[e], rowQ[o]);
+            const float dkp = __fmaf_rn(gt, dKG[e], rowK[o]);
+            const float dkr = __fmul_rn(sR[o], d3[e]);
+            const float dkm = __fadd_rn(dkr, col[o]);
+            dqo[t * TD] = dq;
+            dko[t * TD] = __fadd_rn(dkp, dkm);
+            dGs[o] = __fmaf_rn(qt, dq, __fmul_rn(kt, __fsub_rn(dkp, dkm)));
+            last = __fmaf_rn(kt, dkr, last);
+        }
+        sm[kSLast + hc * TD + i] = last;
+    }
+    tc::bar_sync_first(256);
+    if (hc == 0) {  // dg: reverse running sum of dG down column i, the chunk-end terms on the last row
+        const float colsum = __fadd_rn(sm[kSColS + i], sm[kSColS + TD + i]);
+        const float extra = __fmaf_rn(sm[kSGl + i], colsum, __fadd_rn(sm[kSLast + i], sm[kSLast + TD + i]));
+        float x = 0.f;
+        for (int t = BC - 1; t >= 0; --t) {
+            float v = dGs[t * TD + i];
+            if (t == BC - 1) v = __fadd_rn(v, extra);
+            x = __fadd_rn(x, v);
+            if (t < nb) A.dg[((tok0 + t) * A.H_v + h) * TD + i] = x;
+        }
+    }
+    return ok;
+}
+
 }  // namespace
 
+// KDA: the per-key-column gate.  Every tensor-core product keeps its form (the decay is
+// inside the operands the prep built: K (.) gamma for D_X, (K (.) R)^T for the successor
+// state, gamma = r = 1); the decay-weighted 32 x 32 products of step (9) and the per-column
+// gate gradient run on the CUDA cores.
+template <bool KDA>
 __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
 {
     extern __shared__ __align__(1024) float sm[];
@@ -172,6 +319,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     uint64_t* bar_m = bars + 3;    // M
     uint64_t* bar_dm = bars + 4;   // dM
     uint64_t* bar_dd = bars + 5;   // dDelta, dY rows
+    uint64_t* bar_kda = bars + 6;  // KDA: q, k, g rows, gamma and R tiles for step (9)
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
     __shared__ int s_armed;        // bit b: bars[b] waits for bulk copies
@@ -187,7 +335,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     const int hk = h % A.H_k;
     const long long head = (long long)n * A.H_v + h;
     const long long ch = head * A.n_chunks + c;
-    const long long ck = ((long long)n * A.H_k + hk) * A.n_chunks + c;
+    const long long ck = ((long long)n * A.H_k + hk) * A.n_chunks + c;  // key head's blocks
     const int seg = c / A.cps, loc = c - seg * A.cps;
     const int t0 = seg * A.C + loc * BC;
     const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
@@ -202,6 +350,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         tc::mbar_init(bar_m, 1);
         tc::mbar_init(bar_dm, 1);
         tc::mbar_init(bar_dd, 1);
+        tc::mbar_init(bar_kda, 1);
         tc::mbar_fence_init();
         s_err = 0;
         s_armed = 0;
@@ -231,14 +380,20 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         }
     }
     if (issuer) {
-        tc::mbar_expect_tx(bar_ld, kBytesKb + kBytesFac + kBytesGR);
-        tc::bulk_g2s(sm + kR0, A.ws + A.o_DK + ck * kTcDkElems + kDkKb, kBytesKb, bar_ld);
+        tc::mbar_expect_tx(bar_ld, kBytesKb + (KDA ? kBytesFacKda + (uint32_t)sizeof(float) * TD : kBytesFac) + kBytesGR);
+        if (KDA)  // D_X = M (K (.) gamma)^T
+            tc::bulk_g2s(sm + kR0, A.ws + A.o_KG + ch * kTcKdaTile, kBytesKb, bar_ld);
+        else
+            tc::bulk_g2s(sm + kR0, A.ws + A.o_DK + ck * kTcDkElems + kDkKb, kBytesKb, bar_ld);
         const long long f = ch * (BC * BC);
         tc::bulk_g2s(sm + kSTr, A.ws + A.o_Tr + f, sizeof(float) * BC * BC, bar_ld);
         tc::bulk_g2s(sm + kSZ, A.ws + A.o_Z + f, sizeof(float) * BC * BC, bar_ld);
         tc::bulk_g2s(sm + kSKK, A.ws + A.o_KK + f, sizeof(float) * BC * BC, bar_ld);
         tc::bulk_g2s(sm + kSQK, A.ws + A.o_QK + f, sizeof(float) * BC * BC, bar_ld);
-        tc::bulk_g2s(sm + kSDm, A.ws + A.o_Dm + f, sizeof(float) * BC * BC, bar_ld);
+        if (KDA)
+            tc::bulk_g2s(sm + kSGl, A.ws + A.o_gL + ch * TD, sizeof(float) * TD, bar_ld);
+        else
+            tc::bulk_g2s(sm + kSDm, A.ws + A.o_Dm + f, sizeof(float) * BC * BC, bar_ld);
         tc::bulk_g2s(sm + kSGam, A.ws + A.o_gam + ch * BC, sizeof(float) * BC, bar_ld);
         tc::bulk_g2s(sm + kSR, A.ws + A.o_r + ch * BC, sizeof(float) * BC, bar_ld);
     }
@@ -432,8 +587,12 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                 for (int e = 0; e < 8; ++e)
                     dot = __fmaf_rn(dmc[4 * (j0 + e)], __fadd_rn(mh[e], ml[e]), dot);  // hi + lo = M exactly
             }
-            dot = warp_sum(dot);
-            if (lane == 0) red[(warp & 3) * 96 + 64 + hc] = dot;
+            if (KDA) {  // per key column i = row: this half's 64 j
+                sm[kSColS + hc * TD + row] = dot;
+            } else {
+                dot = warp_sum(dot);
+                if (lane == 0) red[(warp & 3) * 96 + 64 + hc] = dot;
+            }
         }
         // every compute thread has read M^T before dM^T (bf16, two j per column) overwrites it
         tc::fence_before();
@@ -459,8 +618,13 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         tc::fence_after();
         tc::fence_async_smem();
         s_armed |= 1 << 1;
-        tc::mbar_expect_tx(bar_qkt, kBytesQKT);
-        tc::bulk_g2s(sm + kR2, A.ws + A.o_DK + ck * kTcDkElems + kDkQKT, kBytesQKT, bar_qkt);
+        if (KDA) {  // (K (.) R)^T, the B operand of the successor state
+            tc::mbar_expect_tx(bar_qkt, kBytesKrt);
+            tc::bulk_g2s(sm + kKrt, A.ws + A.o_KRT + ch * kTcKdaTile, kBytesKrt, bar_qkt);
+        } else {
+            tc::mbar_expect_tx(bar_qkt, kBytesQKT);
+            tc::bulk_g2s(sm + kR2, A.ws + A.o_DK + ck * kTcDkElems + kDkQKT, kBytesQKT, bar_qkt);
+        }
         mma3_t16(tmem + kC3, aHi, aHi + 64, tc::make_desc(tc::smem_addr(sm + kR0), kLbo64, 128),
                  tc::make_desc(tc::smem_addr(sm + kR0 + kT64h), kLbo64, 128), kLbo64, 0, TD / 16,
                  tc::idesc_bf16(32), false);
@@ -479,7 +643,10 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     float d3[16];
     if (compute) {
         if (!tc::mbar_wait(bar_dd, 0) || !tc::mbar_wait(bar_qkt, 0)) s_err = 1;
-        {
+        if (KDA) {  // d3 = (K (.) R)'s gradient, kept for step (9); the gate sums come there
+            tc::ld16(tc::taddr(tmem, warp, kC3 + tb), d3);
+            tc::wait_ld();
+        } else {
             float dq[16], dk[16];
             tc::ld16(tc::taddr(tmem, warp, kC2 + tb), dq);
             tc::ld16(tc::taddr(tmem, warp, kC2 + BC + tb), dk);
@@ -568,7 +735,8 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             mma_out = true;
             ph_out = ph;
     } else if (compute) {
-        if (tid < 2 * BC) {
+        if (KDA) {
+        } else if (tid < 2 * BC) {
             vec[tid] = __fadd_rn(__fadd_rn(red[tid], red[96 + tid]), __fadd_rn(red[192 + tid], red[288 + tid]));
         } else if (tid == 2 * BC) {
             float v = 0.f;
@@ -584,6 +752,27 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     if (issuer && ok) mma_out = false;
     ph ^= 1;
     tc::fence_after();
+    if (KDA && warp == 8) {
+        // step (9)'s tiles: gamma, R from the prep; q, k, g rows from the inputs (R0 is free: D4
+        // is done; R2 past the (K (.) R)^T tile has been free since (5))
+        const bool rows_bulk = A.vec_q && A.vec_k && A.vec_g;
+        if (lane == 0) {
+            s_armed |= 1 << 6;
+            tc::mbar_expect_tx(bar_kda, 2u * (uint32_t)sizeof(float) * BC * TD +
+                                            (rows_bulk ? 3u * (uint32_t)nb * (uint32_t)sizeof(float) * TD : 0u));
+            tc::bulk_g2s(sm + kKg, A.ws + A.o_kGam + ch * (BC * TD), sizeof(float) * BC * TD, bar_kda);
+            tc::bulk_g2s(sm + kKr, A.ws + A.o_kR + ch * (BC * TD), sizeof(float) * BC * TD, bar_kda);
+        }
+        __syncwarp();
+        if (rows_bulk && lane < nb) {
+            const long long t = t0 + lane;
+            tc::bulk_g2s(sm + kKq + lane * TD, A.q + (long long)n * A.qs0 + t * A.qs1 + (long long)hk * A.qs2,
+                         sizeof(float) * TD, bar_kda);
+            tc::bulk_g2s(sm + kKk + lane * TD, A.k + (long long)n * A.ks0 + t * A.ks1 + (long long)hk * A.ks2,
+                         sizeof(float) * TD, bar_kda);
+            tc::bulk_g2s(sm + kKa + lane * TD, A.g + ((tok0 + lane) * A.H_v + h) * TD, sizeof(float) * TD, bar_kda);
+        }
+    }
     if (compute) {
         // (8) the 32 x 32 algebra.  D4 blocks: rows 0..31 cols 0..31 = dY Delta^T,
         //     rows 32..63 cols 32..63 = dDelta X^T.
@@ -656,9 +845,13 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         // the E = dD (.) Dm sums give the gate gradient
         for (int idx = tid; idx < BC * BC; idx += 256) {
             const int t = idx >> 5, tau = idx & 31;
-            const float dm = Dm[idx];
             const float dA = W1[t * LDF + tau];
             const float dL = __fmul_rn(bs[t], dA);
+            if (KDA) {  // the decay is inside Akk, Aqk: their gradients are dL and P themselves
+                Ss[t * LDF + tau] = dL;
+                continue;
+            }
+            const float dm = Dm[idx];
             float dD = __fmul_rn(Ps[t * LDF + tau], QKm[idx]);
             dD = __fmaf_rn(dL, KKm[idx], dD);
             if (t == BC - 1) dD = __fadd_rn(dD, dr[tau]);
@@ -668,7 +861,13 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         }
         tc::bar_sync_first(256);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // warp w: rows t = 4 w .. 4 w + 3, lanes over tau
+        for (int q = 0; q < 4 && KDA; ++q) {  // dbeta_b[t] = sum_tau dA Akk
+            const int t = 4 * warp + q, tau = lane;
+            const float bb = warp_sum(__fmul_rn(W1[t * LDF + tau], KKm[t * BC + tau]));
+            if (lane == 0) dbs[t] = __fadd_rn(dbs[t], bb);
+        }
+#pragma unroll
+        for (int q = 0; q < 4 && !KDA; ++q) {  // warp w: rows t = 4 w .. 4 w + 3, lanes over tau
             const int t = 4 * warp + q, tau = lane;
             const float rs = warp_sum(dTs[t * LDF + tau]);
             const float cs = warp_sum(dTs[tau * LDF + t]);
@@ -681,7 +880,9 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             }
         }
         tc::bar_sync_first(256);
-        if (warp == 0) {  // dg = reverse cumsum of dG; dbeta
+        if (KDA && warp == 0) {  // dbeta (dg comes in step (9))
+            if (lane < nb) A.dbeta[(tok0 + lane) * A.H_v + h] = dbs[lane];
+        } else if (warp == 0) {  // dg = reverse cumsum of dG; dbeta
             float x = dG[BC - 1 - lane];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -698,7 +899,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         // S is the symmetric dKK + dKK^T of its strict lower part
         float* bp = sm + kABP;
         float* bps = sm + kABPS;
-        for (int idx = tid; idx < BC * BC; idx += 256) {
+        for (int idx = tid; idx < BC * BC && !KDA; idx += 256) {
             const int t = idx & 31, tau = idx >> 5;  // consecutive threads: consecutive rows t
             const float s = (tau > t) ? Ss[tau * LDF + t] : (tau < t ? Ss[t * LDF + tau] : 0.f);
             put_split16(bp, padoff16(t, tau, kLbo32), Ps[t * LDF + tau], kTP);
@@ -709,8 +910,30 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
-    // (9) D2 += [K^T P^T | Q^T P + K^T S]
-    if (issuer) {
+    // (9) D2 += [K^T P^T | Q^T P + K^T S]  (KDA: the successor state only; the decay-weighted
+    //     products run on the CUDA cores meanwhile)
+    if (issuer && KDA) {
+        tc::fence_after();
+        if (!tc::mbar_wait(bar_qkt, 0)) s_err = 1;
+        if (!s_err) {
+            if (park_next) {  // M_N = Delta^T (K (.) R): B = (K (.) R)^T, rows i, K = t
+                const uint64_t khi = tc::tile_desc(sm + kKrt, TD), klo = tc::tile_desc(sm + kKrt + kTcKdaTile / 2, TD);
+                const uint32_t id128 = tc::idesc_bf16(128);
+#pragma unroll
+                for (int s = 0; s < BC / 16; ++s) {
+                    const uint64_t b_h = tc::desc_kslice(khi, TD, s), b_l = tc::desc_kslice(klo, TD, s);
+                    tc::mma_ts16(tmem + kCN, tmem + kCNA + 8 * s, b_h, id128, s > 0);
+                    tc::mma_ts16(tmem + kCN, tmem + kCNA + 8 * s, b_l, id128, 1);
+                    tc::mma_ts16(tmem + kCN, tmem + kCNA + 16 + 8 * s, b_h, id128, 1);
+                }
+            }
+            tc::commit(bar_mma);
+            mma_out = true;
+            ph_out = ph;
+        }
+    } else if (KDA && compute) {
+        if (!kda_tail(A, sm, tmem, bar_kda, tid, warp, row, hc, tb, nb, t0, n, hk, h, ch, tok0, d3)) s_err = 1;
+    } else if (issuer) {
         tc::fence_after();
         if (!tc::mbar_wait(bar_qkt, 0)) s_err = 1;
         if (!s_err) {
@@ -758,17 +981,19 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     tc::fence_after();
     // (10) this value head's dq and dk (rows i = row, tokens [tb, tb + 16)) -> workspace
     if (compute && ok) {
-        float dq[16], dk[16];
-        tc::ld16(tc::taddr(tmem, warp, kC2 + tb), dq);
-        tc::ld16(tc::taddr(tmem, warp, kC2 + BC + tb), dk);
-        tc::wait_ld();
-        float* dqo = A.ws + A.o_dqM + ch * (BC * TD) + row;
-        float* dko = A.ws + A.o_dkM + ch * (BC * TD) + row;
+        if (!KDA) {  // (KDA: written in step (9))
+            float dq[16], dk[16];
+            tc::ld16(tc::taddr(tmem, warp, kC2 + tb), dq);
+            tc::ld16(tc::taddr(tmem, warp, kC2 + BC + tb), dk);
+            tc::wait_ld();
+            float* dqo = A.ws + A.o_dqM + ch * (BC * TD) + row;
+            float* dko = A.ws + A.o_dkM + ch * (BC * TD) + row;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int t = tb + e;
-            dqo[t * TD] = dq[e];
-            dko[t * TD] = __fmaf_rn(sR[t], d3[e], dk[e]);
+            for (int e = 0; e < 16; ++e) {
+                const int t = tb + e;
+                dqo[t * TD] = dq[e];
+                dko[t * TD] = __fmaf_rn(sR[t], d3[e], dk[e]);
+            }
         }
         if (park_next) {
             // the next chunk's entry state M_N = gamma_last M + (r Delta)^T K, row `row`, this
@@ -789,8 +1014,11 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                 for (int q = 0; q < 8; ++q) {
                     const int u = 8 * h2 + q;
                     const float4 mo = __ldg(src + u * sstride);
-                    dst[u * TD] = make_float4(__fmaf_rn(gl, mo.x, v[4 * q]), __fmaf_rn(gl, mo.y, v[4 * q + 1]),
-                                              __fmaf_rn(gl, mo.z, v[4 * q + 2]), __fmaf_rn(gl, mo.w, v[4 * q + 3]));
+                    float4 gq = make_float4(gl, gl, gl, gl);
+                    if (KDA)  // columns 4 u .. 4 u + 3 of this half decay by their own gamma_last
+                        gq = *reinterpret_cast<const float4*>(sm + kSGl + 64 * hc + 4 * u);
+                    dst[u * TD] = make_float4(__fmaf_rn(gq.x, mo.x, v[4 * q]), __fmaf_rn(gq.y, mo.y, v[4 * q + 1]),
+                                              __fmaf_rn(gq.z, mo.z, v[4 * q + 2]), __fmaf_rn(gq.w, mo.w, v[4 * q + 3]));
                 }
             }
         }
@@ -803,7 +1031,7 @@ done:
         // the products in flight must be done before the tensor memory is released; if they
         // are not, say so (bit 8: the tensor memory may be written after its release)
         if (mma_out && !tc::mbar_wait(bar_mma, ph_out)) atomicOr(&g_tcg_status, 1 << 8);
-        for (int b = 0; b < 6; ++b)  // let this CTA's bulk copies land before it exits
+        for (int b = 0; b < 7; ++b)  // let this CTA's bulk copies land before it exits
             if (s_armed & (1 << b)) tc::mbar_wait(bars + b, 0);
     }
     tc::fence_before();
@@ -836,16 +1064,21 @@ __global__ void __launch_bounds__(256) gdn_tc_dqdk_sum_kernel(const ChunkArgs A)
     }
 }
 
-int launch_tc_grad(const ChunkArgs& a, void* stream)
+template <bool KDA>
+static int launch_tc_grad_t(const ChunkArgs& a, cudaStream_t s)
 {
-    cudaStream_t s = (cudaStream_t)stream;
-    int e = (int)cudaFuncSetAttribute(gdn_tc_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    int e = (int)cudaFuncSetAttribute(gdn_tc_grad_kernel<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kGSmemBytes);
     if (e) return e;
     const int units = tc_grad_units(a);
     if (units <= 0) return 0;
-    gdn_tc_grad_kernel<<<dim3(units, a.H_v, a.N), GT, kGSmemBytes, s>>>(a);
+    gdn_tc_grad_kernel<KDA><<<dim3(units, a.H_v, a.N), GT, kGSmemBytes, s>>>(a);
     return (int)cudaGetLastError();
+}
+
+int launch_tc_grad(const ChunkArgs& a, void* stream)
+{
+    return a.kda ? launch_tc_grad_t<true>(a, (cudaStream_t)stream) : launch_tc_grad_t<false>(a, (cudaStream_t)stream);
 }
 
 int tc_grad_units(const ChunkArgs& a)

@@ -75,12 +75,14 @@ def test_checkpoint_interval_invariance(kda):
         assert np.array_equal(got["y"], base["y"]) and np.array_equal(got["state_T"], base["state_T"])
 
 
-def test_checkpoint_interval_invariance_head128():
-    """Head size 128: the forward is the same state chain for every chunk-aligned C, so y and
-    state_T are bit-identical.  The backward takes a segment's later entry states from its
-    own gradient step (not from the forward's chain), so its gradients agree across C to
-    rounding: within 5e-5 (1 + |ref|), some 40 times inside the parity tolerance."""
-    prob = synth.make_problem(1, 300, 2, 6, 128, kda=False, seed=50, packed=True, dstate_T=True)
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+def test_checkpoint_interval_invariance_head128(kda):
+    """Head size 128 (both gates run the chunked form): the forward is the same state chain
+    for every chunk-aligned C, so y and state_T are bit-identical.  The backward takes a
+    segment's later entry states from its own gradient step (not from the forward's chain),
+    so its gradients agree across C to rounding: within 5e-5 (1 + |ref|), some 40 times
+    inside the parity tolerance."""
+    prob = synth.make_problem(1, 300, 2, 6, 128, kda=kda, seed=50, packed=True, dstate_T=True)
     dev = H.upload(prob)
     base, pbase = H.run_gpu(prob, C=32, dev=dev)
     ref = pbase.double().cpu().numpy()
@@ -159,11 +161,24 @@ def test_single_token(kda):
     full_check(prob)
 
 
-def test_chunk_boundaries_and_long_segments():
-    """Scalar gate: C = 100 (4 chunks per segment, ragged last chunk in every segment),
-    T = 333 (ragged last segment), head size 128, broadcast r = 3."""
-    prob = synth.make_problem(1, 333, 2, 6, 128, kda=False, seed=48, C=100, packed=True,
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+def test_chunk_boundaries_and_long_segments(kda):
+    """Chunked form at head size 128: C = 100 (4 chunks per segment, ragged last chunk in
+    every segment), T = 333 (ragged last segment), broadcast r = 3."""
+    prob = synth.make_problem(1, 333, 2, 6, 128, kda=kda, seed=48, C=100, packed=True,
                               dstate_T=True)
+    full_check(prob)
+
+
+def test_kda_head128_extreme_decay():
+    """Per-key-column gate at head size 128 with state resets: every 17th token has
+    g = -100 in every column (a = exp(-100), below fp32's normal range), column 5 has
+    g = -60 throughout, on top of g = -softplus(N(0, 2^2)).  The chunked form carries the
+    decay between tokens as running products of a, so nothing overflows: parity as usual."""
+    prob = synth.make_problem(1, 200, 2, 6, 128, kda=True, seed=52, g_std=2.0, C=64,
+                              packed=True, dstate_T=True)
+    prob.g[:, ::17] = -100.0
+    prob.g[..., 5] = -60.0
     full_check(prob)
 
 
