@@ -599,6 +599,7 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, 
         c.want_wu = 1;
         c.vec_q = vec_ok(q, p->q_s); c.vec_k = vec_ok(k, p->k_s); c.vec_v = vec_ok(v, p->v_s);
         c.vec_g = aligned(g, 16);
+        c.vec_y = aligned(y, 16);
         return cuda_status(gdn::launch_chunk_forward(c, pl.D, stream, tap), "forward launch");
     }
 
@@ -674,6 +675,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
         c.vec_q = vec_ok(q, p->q_s); c.vec_k = vec_ok(k, p->k_s); c.vec_v = vec_ok(v, p->v_s);
         c.vec_gy = vec_ok(gy, p->gy_s);
         c.vec_g = aligned(g, 16);
+        c.vec_ds0 = aligned(c.dstate0, 16);
         return cuda_status(gdn::launch_chunk_backward(c, pl.D, stream, tap), "backward launch");
     }
 

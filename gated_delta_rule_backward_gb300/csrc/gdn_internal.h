@@ -116,6 +116,8 @@ struct ChunkArgs {
                                             // else only the chunks at this place in their segment
     float* carry;                           // [N][H_v][D][D] state (or dM) between ranges
     int vec_q, vec_k, vec_v, vec_gy, vec_g;
+    int vec_ds0;                            // the packed dstate region is 16-byte aligned
+    int vec_y;                              // y is 16-byte aligned
 };
 
 // Records caller-provided timing events around the stages of one call: mark() before

@@ -187,8 +187,13 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         const long long ys = (long long)A.H_v * TD;
         for (int idx = ctid; idx < y_nb * (TD / 4); idx += 256) {
             const int t = idx / (TD / 4), q = idx - t * (TD / 4);
-            *reinterpret_cast<float4*>(yp + t * ys + 4 * q) =
-                *reinterpret_cast<const float4*>(y_buf + t * kStageLd + 4 * q);
+            const float4 v = *reinterpret_cast<const float4*>(y_buf + t * kStageLd + 4 * q);
+            float* yq = yp + t * ys + 4 * q;
+            if (A.vec_y) {  // y is only required to be 4-byte aligned
+                *reinterpret_cast<float4*>(yq) = v;
+            } else {
+                yq[0] = v.x; yq[1] = v.y; yq[2] = v.z; yq[3] = v.w;
+            }
         }
     };
     auto store_ckpt = [&](float* dst) {  // row-major M through `stage`, 32 rows at a time
@@ -763,9 +768,17 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
             if (rest_pending) tc::mbar_wait(bar_rest, ph_rest);
         }
     } else if (compute) {
-        float4* d4 = reinterpret_cast<float4*>((A.c_lo == 0 ? A.dstate0 : A.carry) + (head * TD + j) * TD + 64 * hc);
+        // dstate0 lies in the caller's packed buffer after the dbeta region, so it is 16-byte
+        // aligned only when the regions before it hold a multiple of 4 floats
+        float* out = (A.c_lo == 0 ? A.dstate0 : A.carry) + (head * TD + j) * TD + 64 * hc;
+        if (A.c_lo != 0 || A.vec_ds0) {
+            float4* d4 = reinterpret_cast<float4*>(out);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) d4[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+            for (int q = 0; q < 16; ++q) d4[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) out[e] = m[e];
+        }
     }
     tc::fence_before();
     __syncthreads();

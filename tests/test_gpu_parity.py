@@ -221,3 +221,33 @@ def test_device_status_reports_bounded_wait_timeouts():
     prob = synth.make_problem(1, 100, 1, 2, 128, kda=False, seed=51, C=64)
     H.run_gpu(prob)
     assert gdn.device_status() == gdn.GDN_OK
+
+
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+def test_head128_outputs_only_4_byte_aligned(kda):
+    """The packed buffer's dstate region starts after dg and dbeta, so it is 16-byte aligned
+    only when N T H_v (scalar gate: 2 N T H_v) is a multiple of 4; here N T H_v = 999 leaves it
+    12 bytes off (KDA) or 8 (scalar).  y is a view starting one float into its buffer (the
+    API asks only 4-byte alignment of y).  Both paths store those with 4-byte writes: parity
+    as usual and the same bits as an aligned y."""
+    from gated_delta_rule_backward_gb300 import gdn
+    prob = synth.make_problem(1, 333, 1, 3, 128, kda=kda, seed=53, C=64, packed=True,
+                              dstate_T=True)
+    dev = H.upload(prob)
+    gpu, _ = H.run_gpu(prob, dev=dev)
+    ref = H.run_oracle(H.problem_dict(prob), prob.scale, prob.C)
+    H.compare_all(gpu, ref, H.tolerance(prob.T))
+    p = gdn.params_for(dev["q"], dev["k"], dev["v"], dev["g"], gy=dev["gy"], C=prob.C,
+                       scale=prob.scale)
+    ybuf = torch.empty(1 + 333 * 3 * 128, device="cuda")
+    y = ybuf[1:].view(1, 333, 3, 128)
+    sT = torch.empty((1, 3, 128, 128), device="cuda")
+    ck = torch.empty((1, 3, gdn.num_checkpoints(p), 128, 128), device="cuda")
+    nws = gdn.forward_workspace_bytes(p)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda") if nws else None
+    gdn.gdn_forward(p, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["state0"], y,
+                    sT, ck, ws)
+    torch.cuda.synchronize()
+    H.assert_device_ok()
+    assert np.array_equal(y.cpu().numpy(), gpu["y"])
+    assert np.array_equal(sT.cpu().numpy(), gpu["state_T"])
