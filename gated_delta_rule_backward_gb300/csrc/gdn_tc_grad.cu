@@ -225,22 +225,39 @@ __device__ __forceinline__ bool kda_tail(const ChunkArgs& A, float* sm, uint32_t
     tc::bar_sync_first(256);
     for (int idx = tid; idx < BC * TD; idx += 256) sA[idx] = expf(sA[idx]);
     tc::bar_sync_first(256);
+    // E[tau] = E[t][tau] is carried in registers and multiplied by a_t for tau < t (by 1
+    // otherwise: exact).  The token loop stays rolled and tau runs in blocks of 8, skipped
+    // above the diagonal: the whole triangle unrolled would be tens of KB of straight-line
+    // code, which each warp runs once.  P[t][tau] = 0 for tau > t and S[t][tau] = 0 for
+    // tau >= t, so the diagonal block's extra slots add zeros.
     if (hc == 0) {
         float kc[BC], E[BC];
 #pragma unroll
-        for (int tau = 0; tau < BC; ++tau) kc[tau] = sK[tau * TD + i];
-#pragma unroll
+        for (int tau = 0; tau < BC; ++tau) {
+            kc[tau] = sK[tau * TD + i];
+            E[tau] = 1.f;
+        }
+#pragma unroll 1
         for (int t = 0; t < BC; ++t) {
             const float at = sA[t * TD + i];
-#pragma unroll
-            for (int tau = 0; tau < t; ++tau) E[tau] = __fmul_rn(E[tau], at);
-            E[t] = 1.f;
             float dq = 0.f, dk = 0.f;
 #pragma unroll
-            for (int tau = 0; tau <= t; ++tau) {
-                const float w = __fmul_rn(kc[tau], E[tau]);
-                dq = __fmaf_rn(Ps[t * LDF + tau], w, dq);
-                dk = __fmaf_rn(Ss[t * LDF + tau], w, dk);
+            for (int b = 0; b < BC / 8; ++b) {
+                if (8 * b <= t) {
+                    float pr[8], sr[8];
+                    *reinterpret_cast<float4*>(pr) = *reinterpret_cast<const float4*>(Ps + t * LDF + 8 * b);
+                    *reinterpret_cast<float4*>(pr + 4) = *reinterpret_cast<const float4*>(Ps + t * LDF + 8 * b + 4);
+                    *reinterpret_cast<float4*>(sr) = *reinterpret_cast<const float4*>(Ss + t * LDF + 8 * b);
+                    *reinterpret_cast<float4*>(sr + 4) = *reinterpret_cast<const float4*>(Ss + t * LDF + 8 * b + 4);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int tau = 8 * b + u;
+                        E[tau] = __fmul_rn(E[tau], tau < t ? at : 1.f);
+                        const float w = __fmul_rn(kc[tau], E[tau]);
+                        dq = __fmaf_rn(pr[u], w, dq);
+                        dk = __fmaf_rn(sr[u], w, dk);
+                    }
+                }
             }
             rowQ[t * TD + i] = dq;
             rowK[t * TD + i] = dk;
@@ -248,16 +265,29 @@ __device__ __forceinline__ bool kda_tail(const ChunkArgs& A, float* sm, uint32_t
     } else {
         float E[BC], acc[BC];
 #pragma unroll
+        for (int tau = 0; tau < BC; ++tau) {
+            E[tau] = 1.f;
+            acc[tau] = 0.f;
+        }
+#pragma unroll 1
         for (int t = 0; t < BC; ++t) {
             const float at = sA[t * TD + i], qt = sQ[t * TD + i], kt = sK[t * TD + i];
 #pragma unroll
-            for (int tau = 0; tau < t; ++tau) E[tau] = __fmul_rn(E[tau], at);
-            E[t] = 1.f;
-            acc[t] = 0.f;
+            for (int b = 0; b < BC / 8; ++b) {
+                if (8 * b <= t) {
+                    float pr[8], sr[8];
+                    *reinterpret_cast<float4*>(pr) = *reinterpret_cast<const float4*>(Ps + t * LDF + 8 * b);
+                    *reinterpret_cast<float4*>(pr + 4) = *reinterpret_cast<const float4*>(Ps + t * LDF + 8 * b + 4);
+                    *reinterpret_cast<float4*>(sr) = *reinterpret_cast<const float4*>(Ss + t * LDF + 8 * b);
+                    *reinterpret_cast<float4*>(sr + 4) = *reinterpret_cast<const float4*>(Ss + t * LDF + 8 * b + 4);
 #pragma unroll
-            for (int tau = 0; tau <= t; ++tau) {
-                const float pe = __fmaf_rn(Ss[t * LDF + tau], kt, __fmul_rn(Ps[t * LDF + tau], qt));
-                acc[tau] = __fmaf_rn(pe, E[tau], acc[tau]);
+                    for (int u = 0; u < 8; ++u) {
+                        const int tau = 8 * b + u;
+                        E[tau] = __fmul_rn(E[tau], tau < t ? at : 1.f);
+                        const float pe = __fmaf_rn(sr[u], kt, __fmul_rn(pr[u], qt));
+                        acc[tau] = __fmaf_rn(pe, E[tau], acc[tau]);
+                    }
+                }
             }
         }
 #pragma unroll

@@ -251,3 +251,36 @@ def test_head128_outputs_only_4_byte_aligned(kda):
     H.assert_device_ok()
     assert np.array_equal(y.cpu().numpy(), gpu["y"])
     assert np.array_equal(sT.cpu().numpy(), gpu["state_T"])
+
+
+@pytest.mark.parametrize("kda,d", [(False, 64), (True, 64), (False, 128), (True, 128)],
+                         ids=["scalar-64", "kda-64", "scalar-128", "kda-128"])
+def test_state_chaining_across_calls(kda, d):
+    """A sequence cut in two calls, chained through the states: the second forward starts
+    from the first's state_T, and the first backward is seeded with the second's dstate0
+    (meTile "Recurrent delta attention": state edges between calls take part in the
+    reverse pass).  The pieces, put together, match the oracle's single call."""
+    from gated_delta_rule_backward_gb300 import gdn
+    prob = synth.make_problem(1, 300, 2, 6, d, kda=kda, seed=62, C=64, dstate_T=True)
+    T1 = 128
+    cut = lambda x, s: torch.from_numpy(np.ascontiguousarray(x[:, s])).cuda()
+    a, b = slice(0, T1), slice(T1, None)
+    ins = lambda s: [cut(getattr(prob, nm), s) for nm in ("q", "k", "v", "g", "beta")]
+    s0 = torch.from_numpy(prob.state0).cuda()
+    dsT = torch.from_numpy(prob.dstate_T).cuda()
+    qa, ka, va, ga, ba = ins(a)
+    qb, kb, vb, gb, bb = ins(b)
+    y1, s1, ck1, p1 = gdn.forward(qa, ka, va, ga, ba, s0, C=prob.C, scale=prob.scale)
+    y2, s2, ck2, p2 = gdn.forward(qb, kb, vb, gb, bb, s1, C=prob.C, scale=prob.scale)
+    _, g2 = gdn.backward(p2, qb, kb, vb, gb, bb, ck2, cut(prob.gy, b), dsT)
+    _, g1 = gdn.backward(p1, qa, ka, va, ga, ba, ck1, cut(prob.gy, a), g2["dstate0"].contiguous())
+    torch.cuda.synchronize()
+    H.assert_device_ok()
+    ref = H.run_oracle(H.problem_dict(prob), prob.scale, prob.C)
+    tol = H.tolerance(prob.T)
+    cat = lambda u, w: np.concatenate([u.cpu().numpy(), w.cpu().numpy()], axis=1)
+    H.compare("y", cat(y1, y2), ref["y"], tol)
+    H.compare("state_T", s2.cpu().numpy(), ref["state_T"], tol)
+    for k in ("dq", "dk", "dv", "dg", "dbeta"):
+        H.compare(k, cat(g1[k], g2[k]), ref[k], tol)
+    H.compare("dstate0", g1["dstate0"].cpu().numpy(), ref["dstate0"], tol)

@@ -108,3 +108,33 @@ def test_planted_defect_is_caught(mutation, expect):
     res = P.battery(mlib)
     failed = [k for k, (ok, _) in res.items() if not ok]
     assert failed, f"defect '{expect}' passed every pin"
+
+
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+def test_state_chaining_across_calls(lib, kda):
+    """meTile "Recurrent delta attention": the final state is an output with its own
+    cotangent and the initial state an input with its own gradient, so a sequence cut in
+    two calls chains through them.  The forward of tokens [T1, T) from the state_T of
+    tokens [0, T1), and the backward of [0, T1) seeded with the dstate0 of [T1, T), equal
+    the single call on [0, T) bit for bit (every state is recomputed exactly)."""
+    p = synth.make_problem(2, 37, 1, 2, 8, kda=kda, seed=61, dstate_T=True)
+    f = lambda x: np.asarray(x, dtype=np.float64)
+    T1 = 15
+    y, sT, _ = oracle.forward(p.q, p.k, p.v, p.g, p.beta, p.state0, p.scale, C=4, lib=lib)
+    gr = oracle.backward(p.q, p.k, p.v, p.g, p.beta, p.state0, p.gy, p.dstate_T, p.scale, C=4,
+                         lib=lib)
+    a, b = slice(0, T1), slice(T1, None)
+    part = lambda x, s: np.ascontiguousarray(f(x)[:, s])
+    y1, s1, _ = oracle.forward(part(p.q, a), part(p.k, a), part(p.v, a), part(p.g, a),
+                               part(p.beta, a), p.state0, p.scale, C=4, lib=lib)
+    y2, s2, _ = oracle.forward(part(p.q, b), part(p.k, b), part(p.v, b), part(p.g, b),
+                               part(p.beta, b), s1, p.scale, C=4, lib=lib)
+    g2 = oracle.backward(part(p.q, b), part(p.k, b), part(p.v, b), part(p.g, b), part(p.beta, b),
+                         s1, part(p.gy, b), p.dstate_T, p.scale, C=4, lib=lib)
+    g1 = oracle.backward(part(p.q, a), part(p.k, a), part(p.v, a), part(p.g, a), part(p.beta, a),
+                         p.state0, part(p.gy, a), g2["dstate0"], p.scale, C=4, lib=lib)
+    assert np.array_equal(np.concatenate([y1, y2], axis=1), y)
+    assert np.array_equal(s2, sT)
+    for k in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert np.array_equal(np.concatenate([g1[k], g2[k]], axis=1), gr[k]), k
+    assert np.array_equal(g1["dstate0"], gr["dstate0"])
