@@ -66,8 +66,9 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 gdn_status_t check_sizes(const gdn_params_t* p)
 {
     if (!p) return fail(GDN_ERR_INVALID_ARG, "params is NULL");
-    if (p->reserved0 != 0 || p->reserved1 != 0.0f)
-        return fail(GDN_ERR_INVALID_ARG, "reserved fields must be zero");
+    if (p->reserved1 != 0.0f) return fail(GDN_ERR_INVALID_ARG, "reserved fields must be zero");
+    if (p->in_dtype != GDN_F32 && p->in_dtype != GDN_BF16 && p->in_dtype != GDN_F16)
+        return fail(GDN_ERR_INVALID_ARG, "unknown input dtype %d", (int)p->in_dtype);
     if (p->n_seq < 0 || p->T < 0) return fail(GDN_ERR_INVALID_ARG, "negative n_seq or T");
     if (p->H_k < 1 || p->H_v < 1) return fail(GDN_ERR_INVALID_ARG, "H_k and H_v must be >= 1");
     if (p->H_v % p->H_k != 0)
@@ -209,19 +210,59 @@ struct Range {
     uintptr_t lo, hi;  // [lo, hi)
 };
 
-// Byte extent of a [N][T][H][D] tensor with element strides {s0, s1, s2, 1}.
-Range extent4(const void* ptr, int64_t N, int64_t T, int64_t H, int64_t D, const int64_t s[3])
+// Byte extent of a [N][T][H][D] tensor with element strides {s0, s1, s2, 1} and elements of
+// `es` bytes.
+Range extent4(const void* ptr, int64_t N, int64_t T, int64_t H, int64_t D, const int64_t s[3], size_t es = 4)
 {
     const uintptr_t lo = (uintptr_t)ptr;
     if (!ptr || N == 0 || T == 0 || H == 0 || D == 0) return {lo, lo};
     const uint64_t last = (uint64_t)(s[0] * (N - 1) + s[1] * (T - 1) + s[2] * (H - 1) + D);
-    return {lo, lo + last * 4};
+    return {lo, lo + last * es};
 }
 
-Range extent_dense(const void* ptr, size_t elems)
+Range extent_dense(const void* ptr, size_t elems, size_t es = 4)
 {
     const uintptr_t lo = (uintptr_t)ptr;
-    return {lo, ptr ? lo + elems * 4 : lo};
+    return {lo, ptr ? lo + elems * es : lo};
+}
+
+// 16-bit input storage: the dense fp32 copies of q, k, v, g, beta (and, backward, gy) the
+// call widens its inputs into, at the start of its workspace (byte offsets).
+struct Wide {
+    size_t q = 0, k = 0, v = 0, g = 0, b = 0, gy = 0, total = 0;
+};
+
+Wide wide_layout(const gdn_params_t* p, bool backward)
+{
+    Wide w;
+    if (p->in_dtype == GDN_F32) return w;
+    const size_t N = (size_t)p->n_seq, T = (size_t)p->T, Hk = (size_t)p->H_k, Hv = (size_t)p->H_v;
+    const size_t Sk = (size_t)p->S_k, Sv = (size_t)p->S_v, gw = p->gate == GDN_GATE_KDA ? Sk : 1;
+    size_t o = 0;
+    w.q = o; o += align256(N * T * Hk * Sk * 4);
+    w.k = o; o += align256(N * T * Hk * Sk * 4);
+    w.v = o; o += align256(N * T * Hv * Sv * 4);
+    w.g = o; o += align256(N * T * Hv * gw * 4);
+    w.b = o; o += align256(N * T * Hv * 4);
+    if (backward) {
+        w.gy = o; o += align256(N * T * Hv * Sv * 4);
+    }
+    w.total = o;
+    return w;
+}
+
+// The fp32 parameters of the widened copies: dense strides, in_dtype fp32.
+gdn_params_t dense_f32(const gdn_params_t* p)
+{
+    gdn_params_t q = *p;
+    q.in_dtype = GDN_F32;
+    const int64_t T = p->T, Hk = p->H_k, Hv = p->H_v, Sk = p->S_k, Sv = p->S_v;
+    const int64_t qs[3] = {T * Hk * Sk, Hk * Sk, Sk}, vs[3] = {T * Hv * Sv, Hv * Sv, Sv};
+    for (int i = 0; i < 3; ++i) {
+        q.q_s[i] = q.k_s[i] = qs[i];
+        q.v_s[i] = q.gy_s[i] = vs[i];
+    }
+    return q;
 }
 
 bool overlap(Range a, Range b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
@@ -420,6 +461,11 @@ void gdn::EventTap::mark(void* stream)
 
 extern "C" {
 
+gdn_status_t gdn_forward(const gdn_params_t* p, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* state0, float* y,
+                         float* state_T, float* ckpt, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
 int64_t gdn_checkpoint_interval(const gdn_params_t* p)
 {
     if (!p) return 0;
@@ -458,20 +504,24 @@ void gdn_packed_grad_offsets(const gdn_params_t* p, size_t off[6])
 size_t gdn_backward_workspace_bytes(const gdn_params_t* p)
 {
     if (check_sizes(p) != GDN_OK) return 0;
-    return make_plan(p).ws_bytes;
+    return wide_layout(p, true).total + make_plan(p).ws_bytes;
 }
 
 size_t gdn_forward_workspace_bytes(const gdn_params_t* p)
 {
     if (check_sizes(p) != GDN_OK) return 0;
     const Plan pl = make_plan(p);
-    return pl.chunked ? pl.fwd_ws_bytes : 0;
+    return wide_layout(p, false).total + (pl.chunked ? pl.fwd_ws_bytes : 0);
 }
 
 int gdn_forward_launches(const gdn_params_t* p)
 {
     if (check_sizes(p) != GDN_OK) return 0;
     if (p->n_seq == 0) return 0;
+    if (p->in_dtype != GDN_F32) {  // the widening kernels, then the fp32 path
+        const gdn_params_t q = dense_f32(p);
+        return (p->T > 0 ? 5 : 0) + gdn_forward_launches(&q);
+    }
     const Plan pl = make_plan(p);
     if (pl.chunked && pl.tensor) return 2 * tc_ranges(pl, false);  // prep + state chain per range
     return pl.chunked ? 2 : 1;
@@ -490,6 +540,10 @@ int gdn_backward_launches(const gdn_params_t* p)
 {
     if (check_sizes(p) != GDN_OK) return 0;
     if (p->n_seq == 0) return 0;
+    if (p->in_dtype != GDN_F32) {
+        const gdn_params_t q = dense_f32(p);
+        return (p->T > 0 ? 6 : 0) + gdn_backward_launches(&q);
+    }
     const Plan pl = make_plan(p);
     // chunked: prep, [recompute], dM chain, gradients.  On the tensor-core path, per chunk
     // range: prep, dM chain, a gradient launch per place in a segment, and the sum over value
@@ -544,14 +598,82 @@ void gdn_set_timing_events(void* const* events, int n_events)
     g_n_events = events ? n_events : 0;
 }
 
-gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, const float* v,
-                         const float* g, const float* beta, const float* state0, float* y,
+}  // extern "C"
+
+namespace {
+
+// Widens one 16-bit input [N][T][H][D] (element strides s, last dim contiguous) into its
+// dense fp32 copy.
+gdn_status_t widen_one(const gdn_params_t* p, const void* src, const int64_t s[3], int64_t H, int64_t D, float* dst,
+                       void* stream)
+{
+    const long long ss[3] = {(long long)s[0], (long long)s[1], (long long)s[2]};
+    return cuda_status(gdn::launch_widen(src, p->in_dtype, ss, (int)p->n_seq, (int)p->T, (int)H, (int)D, dst, stream),
+                       "widening launch");
+}
+
+// The caller's 16-bit inputs against the buffers the call writes: no overlap.
+gdn_status_t check_16bit_inputs(const gdn_params_t* p, const void* const* in, int n_in, const Range* out, int n_out)
+{
+    const int64_t N = p->n_seq, T = p->T, Hk = p->H_k, Hv = p->H_v, Sk = p->S_k, Sv = p->S_v;
+    const int64_t gw = p->gate == GDN_GATE_KDA ? Sk : 1;
+    for (int i = 0; i < n_in; ++i)
+        if (!aligned(in[i], 2)) return fail(GDN_ERR_INVALID_ARG, "16-bit input not 2-byte aligned");
+    const Range r[6] = {extent4(in[0], N, T, Hk, Sk, p->q_s, 2), extent4(in[1], N, T, Hk, Sk, p->k_s, 2),
+                        extent4(in[2], N, T, Hv, Sv, p->v_s, 2), extent_dense(in[3], (size_t)(N * T * Hv * gw), 2),
+                        extent_dense(in[4], (size_t)(N * T * Hv), 2),
+                        n_in > 5 ? extent4(in[5], N, T, Hv, Sv, p->gy_s, 2) : Range{0, 0}};
+    for (int i = 0; i < n_in; ++i)
+        for (int j = 0; j < n_out; ++j)
+            if (overlap(r[i], out[j])) return fail(GDN_ERR_ALIAS, "an output or the workspace overlaps an input");
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status_t gdn_forward(const gdn_params_t* p, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* state0, float* y,
                          float* state_T, float* ckpt, void* workspace, size_t workspace_bytes,
                          void* stream)
 {
     gdn_status_t st = check_sizes(p);
     if (st != GDN_OK) return st;
     g_last_error.clear();
+    if (p->in_dtype != GDN_F32 && p->n_seq > 0) {
+        // 16-bit inputs: widen them into the workspace, then run the fp32 path on the copies
+        const int64_t N = p->n_seq, T = p->T, Hv = p->H_v, Sk = p->S_k, Sv = p->S_v;
+        if (T > 0 && (!q || !k || !v || !g || !beta))
+            return fail(GDN_ERR_INVALID_ARG, "q, k, v, g and beta must be non-NULL");
+        const Wide w = wide_layout(p, false);
+        const gdn_params_t p32 = dense_f32(p);
+        const size_t need = w.total + gdn_forward_workspace_bytes(&p32);
+        if (workspace_bytes < need)
+            return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+        if (!workspace || !aligned(workspace, 256))
+            return fail(GDN_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+        const void* in[5] = {q, k, v, g, beta};
+        const Range out[4] = {extent_dense(y, (size_t)(N * T * Hv * Sv)), extent_dense(state_T, (size_t)(N * Hv * Sv * Sk)),
+                              extent_dense(ckpt, gdn_ckpt_elems(p)), {(uintptr_t)workspace, (uintptr_t)workspace + need}};
+        st = check_16bit_inputs(p, in, 5, out, 4);
+        if (st != GDN_OK) return st;
+        char* ws = (char*)workspace;
+        float *wq = (float*)(ws + w.q), *wk = (float*)(ws + w.k), *wv = (float*)(ws + w.v);
+        float *wg = (float*)(ws + w.g), *wb = (float*)(ws + w.b);
+        if (T > 0) {
+            const int64_t gs[3] = {T * Hv * (p->gate == GDN_GATE_KDA ? Sk : 1), Hv * (p->gate == GDN_GATE_KDA ? Sk : 1),
+                                   p->gate == GDN_GATE_KDA ? Sk : 1};
+            const int64_t bs[3] = {T * Hv, Hv, 1};
+            if ((st = widen_one(p, q, p->q_s, p->H_k, Sk, wq, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, k, p->k_s, p->H_k, Sk, wk, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, v, p->v_s, Hv, Sv, wv, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, g, gs, Hv, gs[2], wg, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, beta, bs, Hv, 1, wb, stream)) != GDN_OK) return st;
+        }
+        return gdn_forward(&p32, wq, wk, wv, wg, wb, state0, y, state_T, ckpt, ws + w.total, workspace_bytes - w.total,
+                           stream);
+    }
     const Plan pl = make_plan(p);
     const int64_t N = p->n_seq, T = p->T, Hk = p->H_k, Hv = p->H_v, D = p->S_k;
     if (N == 0) return GDN_OK;
@@ -592,7 +714,8 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, 
     gdn::EventTap tap{g_events, g_n_events, 0};
     if (pl.chunked) {
         gdn::ChunkArgs c{};
-        c.q = q; c.k = k; c.v = v; c.g = g; c.beta = beta; c.state0 = state0;
+        c.q = (const float*)q; c.k = (const float*)k; c.v = (const float*)v; c.g = (const float*)g;
+        c.beta = (const float*)beta; c.state0 = state0;
         c.y = y; c.state_T = state_T; c.ckpt_out = ckpt; c.ws = (float*)workspace;
         fill_chunk_common(c, p, pl);
         c.carry = pl.tensor ? c.ws + pl.o_carry : nullptr;
@@ -604,7 +727,8 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, 
     }
 
     gdn::FwdArgs a{};
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state0 = state0;
+    a.q = (const float*)q; a.k = (const float*)k; a.v = (const float*)v; a.g = (const float*)g;
+    a.beta = (const float*)beta; a.state0 = state0;
     a.y = y; a.state_T = state_T; a.ckpt = ckpt;
     a.qs0 = p->q_s[0]; a.qs1 = p->q_s[1]; a.qs2 = p->q_s[2];
     a.ks0 = p->k_s[0]; a.ks1 = p->k_s[1]; a.ks2 = p->k_s[2];
@@ -619,14 +743,48 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k, 
     return st;
 }
 
-gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k, const float* v,
-                          const float* g, const float* beta, const float* ckpt, const float* gy,
+gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k, const void* v,
+                          const void* g, const void* beta, const float* ckpt, const void* gy,
                           const float* dstate_T, float* packed, void* workspace,
                           size_t workspace_bytes, void* stream)
 {
     gdn_status_t st = check_sizes(p);
     if (st != GDN_OK) return st;
     g_last_error.clear();
+    if (p->in_dtype != GDN_F32 && p->n_seq > 0) {
+        // 16-bit inputs: widen them into the workspace, then run the fp32 path on the copies
+        const int64_t N = p->n_seq, T = p->T, Hv = p->H_v, Sk = p->S_k, Sv = p->S_v;
+        if (T > 0 && (!q || !k || !v || !g || !beta || !gy))
+            return fail(GDN_ERR_INVALID_ARG, "q, k, v, g, beta and gy must be non-NULL");
+        const Wide w = wide_layout(p, true);
+        const gdn_params_t p32 = dense_f32(p);
+        const size_t need = w.total + gdn_backward_workspace_bytes(&p32);
+        if (workspace_bytes < need)
+            return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+        if (!workspace || !aligned(workspace, 256))
+            return fail(GDN_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+        const void* in[6] = {q, k, v, g, beta, gy};
+        const Range out[2] = {extent_dense(packed, gdn_packed_grad_elems(p)),
+                              {(uintptr_t)workspace, (uintptr_t)workspace + need}};
+        st = check_16bit_inputs(p, in, 6, out, 2);
+        if (st != GDN_OK) return st;
+        char* ws = (char*)workspace;
+        float *wq = (float*)(ws + w.q), *wk = (float*)(ws + w.k), *wv = (float*)(ws + w.v);
+        float *wg = (float*)(ws + w.g), *wb = (float*)(ws + w.b), *wgy = (float*)(ws + w.gy);
+        if (T > 0) {
+            const int64_t gw = p->gate == GDN_GATE_KDA ? Sk : 1;
+            const int64_t gs[3] = {T * Hv * gw, Hv * gw, gw};
+            const int64_t bs[3] = {T * Hv, Hv, 1};
+            if ((st = widen_one(p, q, p->q_s, p->H_k, Sk, wq, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, k, p->k_s, p->H_k, Sk, wk, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, v, p->v_s, Hv, Sv, wv, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, g, gs, Hv, gw, wg, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, beta, bs, Hv, 1, wb, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, gy, p->gy_s, Hv, Sv, wgy, stream)) != GDN_OK) return st;
+        }
+        return gdn_backward(&p32, wq, wk, wv, wg, wb, ckpt, wgy, dstate_T, packed, ws + w.total,
+                            workspace_bytes - w.total, stream);
+    }
     const Plan pl = make_plan(p);
     const int64_t N = p->n_seq, T = p->T, Hk = p->H_k, Hv = p->H_v, D = p->S_k;
     if (N == 0) return GDN_OK;
@@ -664,7 +822,8 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
     gdn::EventTap tap{g_events, g_n_events, 0};
     if (pl.chunked) {
         gdn::ChunkArgs c{};
-        c.q = q; c.k = k; c.v = v; c.g = g; c.beta = beta; c.ckpt = ckpt; c.gy = gy;
+        c.q = (const float*)q; c.k = (const float*)k; c.v = (const float*)v; c.g = (const float*)g;
+        c.beta = (const float*)beta; c.ckpt = ckpt; c.gy = (const float*)gy;
         c.dstate_T = dstate_T; c.ws = (float*)workspace;
         c.dq = packed + off[0]; c.dk = packed + off[1]; c.dv = packed + off[2];
         c.dg = packed + off[3]; c.dbeta = packed + off[4]; c.dstate0 = packed + off[5];
@@ -681,7 +840,8 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
 
     char* ws = (char*)workspace;
     gdn::BwdArgs a{};
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.ckpt = ckpt; a.gy = gy;
+    a.q = (const float*)q; a.k = (const float*)k; a.v = (const float*)v; a.g = (const float*)g;
+    a.beta = (const float*)beta; a.ckpt = ckpt; a.gy = (const float*)gy;
     a.dstate_T = dstate_T;
     a.dv = packed + off[2];
     a.dstate0 = packed + off[5];

@@ -260,6 +260,11 @@ int launch_forward(const FwdArgs& a, int D, int RT, int W, bool kda, void* strea
 int launch_backward(const BwdArgs& a, int D, int RT, int W, bool kda, void* stream);
 int launch_reduce(const ReduceArgs& a, void* stream);
 
+// Widens a bf16 (in_dtype 1) or fp16 (2) tensor [N][T][H][D] with element strides s (last
+// dim contiguous) into dense fp32 at dst (gdn_widen.cu).  Returns a cudaError_t as int.
+int launch_widen(const void* src, int in_dtype, const long long s[3], int N, int T, int H, int D, float* dst,
+                 void* stream);
+
 // Sets the text gdn_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
 

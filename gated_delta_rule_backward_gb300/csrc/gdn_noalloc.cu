@@ -42,9 +42,9 @@ void* g_scratch_addr[kMaxDevices] = {};
 
 extern "C" {
 
-gdn_status_t gdn_backward_noalloc(const gdn_params_t* p, const float* q, const float* k,
-                                  const float* v, const float* g, const float* beta,
-                                  const float* ckpt, const float* gy, const float* dstate_T,
+gdn_status_t gdn_backward_noalloc(const gdn_params_t* p, const void* q, const void* k,
+                                  const void* v, const void* g, const void* beta,
+                                  const float* ckpt, const void* gy, const float* dstate_T,
                                   float* packed_grads, void* stream)
 {
     char msg[256];

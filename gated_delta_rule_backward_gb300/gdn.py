@@ -25,6 +25,7 @@ GDN_OK = 0
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIAS",
           4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT"}
 GATE_SCALAR, GATE_KDA = 0, 1
+DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ["gdn_checkpoint_interval", "gdn_num_checkpoints", "gdn_ckpt_elems", "gdn_forward",
@@ -39,7 +40,7 @@ class GdnParams(ctypes.Structure):
     _fields_ = [
         ("n_seq", ctypes.c_int64), ("T", ctypes.c_int64), ("H_k", ctypes.c_int64),
         ("H_v", ctypes.c_int64), ("S_k", ctypes.c_int64), ("S_v", ctypes.c_int64),
-        ("gate", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("gate", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
         ("C", ctypes.c_int64),
         ("scale", ctypes.c_float), ("reserved1", ctypes.c_float),
         ("q_s", ctypes.c_int64 * 3), ("k_s", ctypes.c_int64 * 3),
@@ -99,12 +100,12 @@ def library():
 
 
 def make_params(N, T, H_k, H_v, S, kda, C=None, scale=None, q_s=None, k_s=None, v_s=None,
-                gy_s=None) -> GdnParams:
+                gy_s=None, in_dtype=DTYPE_F32) -> GdnParams:
     """Parameter struct; strides default to the contiguous [N,T,H,S] layout."""
     p = GdnParams()
     p.n_seq, p.T, p.H_k, p.H_v, p.S_k, p.S_v = N, T, H_k, H_v, S, S
     p.gate = GATE_KDA if kda else GATE_SCALAR
-    p.reserved0, p.reserved1 = 0, 0.0
+    p.in_dtype, p.reserved1 = int(in_dtype), 0.0
     p.C = 0 if C is None else int(C)
     p.scale = (1.0 / math.sqrt(S)) if scale is None else float(scale)
     p.q_s[:] = q_s or (T * H_k * S, H_k * S, S)
@@ -124,13 +125,28 @@ def strides3(t):
     return tuple(int(s) for s in t.stride()[:3])
 
 
+def input_dtype(t) -> int:
+    """gdn_dtype_t of an input tensor: fp32, bf16 or fp16."""
+    import torch
+    code = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16}.get(t.dtype)
+    if code is None:
+        raise TypeError(f"inputs must be float32, bfloat16 or float16, not {t.dtype}")
+    return code
+
+
 def params_for(q, k, v, g, gy=None, C=None, scale=None) -> GdnParams:
+    """Parameters for these input tensors: sizes, strides and their storage type (q, k, v,
+    g and gy must all have that type)."""
     N, T, H_k, S = q.shape
     H_v = v.shape[2]
     kda = g.dim() == 4
+    dt = input_dtype(q)
+    for t in (k, v, g) + ((gy,) if gy is not None else ()):
+        if input_dtype(t) != dt:
+            raise TypeError("q, k, v, g (and gy) must share one storage type")
     return make_params(N, T, H_k, H_v, S, kda, C=C, scale=scale, q_s=strides3(q),
                        k_s=strides3(k), v_s=strides3(v),
-                       gy_s=strides3(gy) if gy is not None else None)
+                       gy_s=strides3(gy) if gy is not None else None, in_dtype=dt)
 
 
 def _ptr(t):

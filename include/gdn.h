@@ -28,8 +28,8 @@
  * n_ck = ceil(T/C); the backward recomputes every segment from its checkpoint.  The
  * backward returns one packed buffer [dq|dk|dv|dg|dbeta|dstate] (PR #16 body).
  *
- * Layouts (fp32, M = S^T)
- * -----------------------
+ * Layouts (M = S^T; fp32 unless gdn_params_t.in_dtype makes q, k, v, g, beta, gy 16-bit)
+ * ----------------------------------------------------------------------------------
  *   q, k      [N][T][H_k][S_k]  element strides q_s/k_s = {seq, token, head}; the
  *                               S_k elements of one (seq, token, head) are contiguous
  *                               (so q, k may be row views of a packed qkv buffer)
@@ -72,8 +72,9 @@
  * Errors (no call ever writes an output when it returns an error)
  * ------
  *   GDN_ERR_INVALID_ARG  NULL pointer, negative size, H_v % H_k != 0, a stride that is
- *                        negative, a pointer that is not 4-byte aligned, a state or
- *                        output buffer that is not 16-byte aligned, bad gate kind
+ *                        negative, an input that is not aligned to its element (4 bytes,
+ *                        2 for 16-bit inputs), a state or output buffer that is not
+ *                        16-byte aligned, bad gate kind or input dtype
  *   GDN_ERR_UNSUPPORTED  S_k != S_v, or a head size other than 32, 64, 128
  *   GDN_ERR_ALIAS        an output overlaps an input (state_T over state0 included)
  *   GDN_ERR_WORKSPACE    workspace smaller than gdn_backward_workspace_bytes()
@@ -102,10 +103,18 @@ typedef enum {
 
 typedef enum { GDN_GATE_SCALAR = 0, GDN_GATE_KDA = 1 } gdn_gate_t;
 
+/* Storage type of the inputs q, k, v, g, beta and gy (meTile "Training kernels and
+ * gradients": 16-bit inputs beside fp32 state and fp32 gradients).  States (state0,
+ * dstate_T, state_T, ckpt) and every output are fp32 whatever the input type.  A call with
+ * 16-bit inputs widens them (exactly: every bf16 and fp16 value is an fp32 value) into
+ * dense fp32 copies at the start of its workspace, then runs the fp32 path on them; the
+ * workspace queries include those copies. */
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype_t;
+
 typedef struct {
     int64_t n_seq, T, H_k, H_v, S_k, S_v; /* sizes; H_v = r H_k, key head = h_v mod H_k */
     int32_t gate;                         /* gdn_gate_t */
-    int32_t reserved0;                    /* must be 0 */
+    int32_t in_dtype;                     /* gdn_dtype_t of q, k, v, g, beta, gy (0: fp32) */
     int64_t C;                            /* checkpoint interval; <= 0: ceil(sqrt(T)) */
     float scale;                          /* output scale, usually 1/sqrt(S_k) */
     float reserved1;                      /* must be 0 */
@@ -128,8 +137,8 @@ size_t gdn_forward_workspace_bytes(const gdn_params_t* p);
  * destroyed the initial state the backward needed).  The scalar gate runs the chunked
  * (WY) regrouping of the recurrence (exact, chunks of 32 tokens aligned to the
  * checkpoint segments); the per-key-column gate runs the token recurrence. */
-gdn_status_t gdn_forward(const gdn_params_t* p, const float* q, const float* k,
-                         const float* v, const float* g, const float* beta,
+gdn_status_t gdn_forward(const gdn_params_t* p, const void* q, const void* k,
+                         const void* v, const void* g, const void* beta,
                          const float* state0, float* y, float* state_T, float* ckpt,
                          void* workspace, size_t workspace_bytes, void* stream);
 
@@ -145,9 +154,9 @@ size_t gdn_backward_workspace_bytes(const gdn_params_t* p);
  * gdn_forward with the same params), gy and dstate_T (NULL = zero cotangent for the
  * final state); writes every element of packed_grads.  The workspace is scratch owned
  * by the caller for the duration of the enqueued work. */
-gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
-                          const float* v, const float* g, const float* beta,
-                          const float* ckpt, const float* gy, const float* dstate_T,
+gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k,
+                          const void* v, const void* g, const void* beta,
+                          const float* ckpt, const void* gy, const float* dstate_T,
                           float* packed_grads, void* workspace, size_t workspace_bytes,
                           void* stream);
 
@@ -166,9 +175,9 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const float* q, const float* k,
  * order them on one stream or with events.  The address is looked up once per device and
  * kept: a process that calls cudaDeviceReset on a device must not use this entry point on
  * it afterwards.  A device index of 64 or more returns GDN_ERR_UNSUPPORTED. */
-gdn_status_t gdn_backward_noalloc(const gdn_params_t* p, const float* q, const float* k,
-                                  const float* v, const float* g, const float* beta,
-                                  const float* ckpt, const float* gy, const float* dstate_T,
+gdn_status_t gdn_backward_noalloc(const gdn_params_t* p, const void* q, const void* k,
+                                  const void* v, const void* g, const void* beta,
+                                  const float* ckpt, const void* gy, const float* dstate_T,
                                   float* packed_grads, void* stream);
 
 /* Static text of a status code, and the detail of the calling thread's last error. */

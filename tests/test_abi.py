@@ -141,7 +141,10 @@ def test_invalid_arguments():
     p.gate = 7
     assert call_forward(p) == INVALID
     p = gdn.make_params(1, 8, 1, 1, 32, False)
-    p.reserved0 = 1
+    p.in_dtype = 3                                                          # unknown input dtype
+    assert call_forward(p) == INVALID
+    p = gdn.make_params(1, 8, 1, 1, 32, False)
+    p.reserved1 = 1.0
     assert call_forward(p) == INVALID
     p = gdn.make_params(-1, 8, 1, 1, 32, False)
     assert call_forward(p) == INVALID
@@ -180,3 +183,22 @@ def test_workspace_too_small():
     ptrs = [fake(i) for i in range(10)]
     ptrs[9] = ctypes.c_void_p(BASE + 9 * (1 << 32) + 16)                    # not 256-aligned
     assert call_backward(p, ws, ptrs) == WORKSPACE
+
+
+def test_16bit_inputs_add_their_widened_copies_to_the_workspace():
+    """bf16 / fp16 inputs are widened into dense fp32 copies at the start of the workspace:
+    q, k, v, g, beta (and gy in the backward), each 256-byte aligned; then the fp32 path's
+    own workspace.  The widening adds one kernel per input."""
+    al = lambda b: (b + 255) // 256 * 256
+    for kda, S in ((False, 64), (True, 64), (False, 128), (True, 128)):
+        N, T, Hk, Hv = 2, 61, 2, 6
+        p32 = gdn.make_params(N, T, Hk, Hv, S, kda, C=8)
+        for dt in (gdn.DTYPE_BF16, gdn.DTYPE_F16):
+            p16 = gdn.make_params(N, T, Hk, Hv, S, kda, C=8, in_dtype=dt)
+            gw = S if kda else 1
+            wide_f = 2 * al(N * T * Hk * S * 4) + al(N * T * Hv * S * 4) + al(N * T * Hv * gw * 4) + al(N * T * Hv * 4)
+            wide_b = wide_f + al(N * T * Hv * S * 4)
+            assert gdn.forward_workspace_bytes(p16) == wide_f + gdn.forward_workspace_bytes(p32)
+            assert gdn.backward_workspace_bytes(p16) == wide_b + gdn.backward_workspace_bytes(p32)
+            f32, b32 = gdn.launches(p32)
+            assert gdn.launches(p16) == (f32 + 5, b32 + 6)
