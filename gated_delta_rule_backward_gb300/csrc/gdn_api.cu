@@ -46,6 +46,7 @@ int64_t ceil_sqrt(int64_t T)
 // gate at head sizes 32 and 64 and the degenerate T = 0 case run the token recurrence.
 struct Plan {
     int D = 0, RT = 1, W = 4, R = 16, P = 1, tc = 32, c2 = 1, nsub_max = 1;
+    int SK = 0, DV = 0;  // the state's columns (key head size) and rows (value head size)
     bool kda = false;
     bool chunked = false;
     int64_t C = 1, n_ck = 0;
@@ -77,12 +78,12 @@ gdn_status_t check_sizes(const gdn_params_t* p)
     if (p->gate != GDN_GATE_SCALAR && p->gate != GDN_GATE_KDA)
         return fail(GDN_ERR_INVALID_ARG, "unknown gate kind %d", (int)p->gate);
     if (p->S_k < 1 || p->S_v < 1) return fail(GDN_ERR_INVALID_ARG, "head sizes must be >= 1");
-    if (p->S_k != p->S_v)
-        return fail(GDN_ERR_UNSUPPORTED, "S_k (%lld) != S_v (%lld) is not supported",
-                    (long long)p->S_k, (long long)p->S_v);
-    if (p->S_k != 32 && p->S_k != 64 && p->S_k != 128)
-        return fail(GDN_ERR_UNSUPPORTED, "head size %lld is not supported (32, 64, 128)",
+    if (p->S_k != 16 && p->S_k != 32 && p->S_k != 64 && p->S_k != 128 && p->S_k != 256)
+        return fail(GDN_ERR_UNSUPPORTED, "key head size S_k = %lld is not supported (16, 32, 64, 128, 256)",
                     (long long)p->S_k);
+    if (p->S_v % 16 != 0 || p->S_v > 256)
+        return fail(GDN_ERR_UNSUPPORTED, "value head size S_v = %lld is not supported (a multiple of 16 up to 256)",
+                    (long long)p->S_v);
     if (p->T > INT_MAX / 2 || p->H_v > 65535 || p->n_seq > 65535)
         return fail(GDN_ERR_UNSUPPORTED, "sizes beyond the kernels' index range");
     for (int i = 0; i < 3; ++i)
@@ -94,7 +95,10 @@ gdn_status_t check_sizes(const gdn_params_t* p)
 Plan make_plan(const gdn_params_t* p)
 {
     Plan pl;
-    pl.D = (int)p->S_k;
+    // the token recurrence computes at column width D: S_k, or 32 for S_k = 16 (zero padding)
+    pl.SK = (int)p->S_k;
+    pl.DV = (int)p->S_v;
+    pl.D = pl.SK < 32 ? 32 : pl.SK;
     pl.kda = p->gate == GDN_GATE_KDA;
     pl.C = p->C > 0 ? p->C : ceil_sqrt(p->T);
     if (pl.C > INT_MAX / 2) pl.C = INT_MAX / 2;
@@ -102,7 +106,7 @@ Plan make_plan(const gdn_params_t* p)
     pl.RT = 1;
     pl.W = 4;
     pl.R = 4 * pl.RT * pl.W;
-    pl.P = pl.D / pl.R;
+    pl.P = pl.DV / pl.R;
     pl.tc = 32;
     // Sub-segment length c2: as many ring slots as fit the shared memory of the number
     // of CTAs each SM must hold for the whole grid to be resident (at most 4 per SM).
@@ -133,7 +137,10 @@ Plan make_plan(const gdn_params_t* p)
     pl.off_sc = pl.off_col + align256(col_f * 4);
     pl.ws_bytes = pl.off_sc + align256(sc_f * 4);
 
-    pl.chunked = p->T > 0 && (!pl.kda || pl.D == 128);
+    // chunked (WY) kernels: square heads of size 32, 64 or 128 (the per-key-column gate at
+    // 128 only); every other shape runs the token recurrence
+    pl.chunked = p->T > 0 && pl.SK == pl.DV && (pl.SK == 32 || pl.SK == 64 || pl.SK == 128) &&
+                 (!pl.kda || pl.SK == 128);
     if (pl.chunked) {
         const int64_t BC = gdn::BC;
         pl.cps = (int)((pl.C + BC - 1) / BC);
@@ -675,7 +682,7 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const void* q, const void* k, co
                            stream);
     }
     const Plan pl = make_plan(p);
-    const int64_t N = p->n_seq, T = p->T, Hk = p->H_k, Hv = p->H_v, D = p->S_k;
+    const int64_t N = p->n_seq, T = p->T, Hk = p->H_k, Hv = p->H_v, D = p->S_k, DV = p->S_v;
     if (N == 0) return GDN_OK;
     const bool tok = T > 0;
     if (tok && (!q || !k || !v || !g || !beta))
@@ -690,13 +697,13 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const void* q, const void* k, co
 
     const int64_t gw = pl.kda ? D : 1;
     const Range rq = extent4(q, N, T, Hk, D, p->q_s), rk = extent4(k, N, T, Hk, D, p->k_s);
-    const Range rv = extent4(v, N, T, Hv, D, p->v_s);
+    const Range rv = extent4(v, N, T, Hv, DV, p->v_s);
     const Range rg = extent_dense(g, (size_t)(N * T * Hv * gw));
     const Range rb = extent_dense(beta, (size_t)(N * T * Hv));
-    const Range rs0 = extent_dense(state0, (size_t)(N * Hv * D * D));
-    const Range ry = extent_dense(y, (size_t)(N * T * Hv * D));
-    const Range rsT = extent_dense(state_T, (size_t)(N * Hv * D * D));
-    const Range rck = extent_dense(ckpt, (size_t)(N * Hv * pl.n_ck * D * D));
+    const Range rs0 = extent_dense(state0, (size_t)(N * Hv * DV * D));
+    const Range ry = extent_dense(y, (size_t)(N * T * Hv * DV));
+    const Range rsT = extent_dense(state_T, (size_t)(N * Hv * DV * D));
+    const Range rck = extent_dense(ckpt, (size_t)(N * Hv * pl.n_ck * DV * D));
     for (Range out : {ry, rsT, rck})
         for (Range in : {rq, rk, rv, rg, rb, rs0})
             if (overlap(out, in)) return fail(GDN_ERR_ALIAS, "a forward output overlaps an input");
@@ -735,6 +742,7 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const void* q, const void* k, co
     a.vs0 = p->v_s[0]; a.vs1 = p->v_s[1]; a.vs2 = p->v_s[2];
     a.N = (int)N; a.T = (int)T; a.H_k = (int)Hk; a.H_v = (int)Hv;
     a.C = (int)pl.C; a.n_ck = (int)pl.n_ck; a.scale = p->scale; a.tc = pl.tc;
+    a.SK = pl.SK; a.DV = pl.DV;
     a.vec_q = vec_ok(q, p->q_s); a.vec_k = vec_ok(k, p->k_s); a.vec_v = vec_ok(v, p->v_s);
     a.vec_g = aligned(g, 16);
     tap.mark(stream);
@@ -753,7 +761,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k, c
     g_last_error.clear();
     if (p->in_dtype != GDN_F32 && p->n_seq > 0) {
         // 16-bit inputs: widen them into the workspace, then run the fp32 path on the copies
-        const int64_t N = p->n_seq, T = p->T, Hv = p->H_v, Sk = p->S_k, Sv = p->S_v;
+        const int64_t T = p->T, Hv = p->H_v, Sk = p->S_k, Sv = p->S_v;
         if (T > 0 && (!q || !k || !v || !g || !beta || !gy))
             return fail(GDN_ERR_INVALID_ARG, "q, k, v, g, beta and gy must be non-NULL");
         const Wide w = wide_layout(p, true);
@@ -786,7 +794,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k, c
                             workspace_bytes - w.total, stream);
     }
     const Plan pl = make_plan(p);
-    const int64_t N = p->n_seq, T = p->T, Hk = p->H_k, Hv = p->H_v, D = p->S_k;
+    const int64_t N = p->n_seq, T = p->T, Hk = p->H_k, Hv = p->H_v, D = p->S_k, DV = p->S_v;
     if (N == 0) return GDN_OK;
     const bool tok = T > 0;
     if (tok && (!q || !k || !v || !g || !beta || !ckpt || !gy))
@@ -807,11 +815,11 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k, c
     packed_offsets(p, off);
     const int64_t gw = pl.kda ? D : 1;
     const Range rq = extent4(q, N, T, Hk, D, p->q_s), rk = extent4(k, N, T, Hk, D, p->k_s);
-    const Range rv = extent4(v, N, T, Hv, D, p->v_s), rgy = extent4(gy, N, T, Hv, D, p->gy_s);
+    const Range rv = extent4(v, N, T, Hv, DV, p->v_s), rgy = extent4(gy, N, T, Hv, DV, p->gy_s);
     const Range rg = extent_dense(g, (size_t)(N * T * Hv * gw));
     const Range rb = extent_dense(beta, (size_t)(N * T * Hv));
-    const Range rck = extent_dense(ckpt, (size_t)(N * Hv * pl.n_ck * D * D));
-    const Range rdsT = extent_dense(dstate_T, (size_t)(N * Hv * D * D));
+    const Range rck = extent_dense(ckpt, (size_t)(N * Hv * pl.n_ck * DV * D));
+    const Range rdsT = extent_dense(dstate_T, (size_t)(N * Hv * DV * D));
     const Range rpk = extent_dense(packed, off[6]);
     const Range rws = {(uintptr_t)workspace, (uintptr_t)workspace + (workspace ? pl.ws_bytes : 0)};
     for (Range out : {rpk, rws})
@@ -854,6 +862,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k, c
     a.gys0 = p->gy_s[0]; a.gys1 = p->gy_s[1]; a.gys2 = p->gy_s[2];
     a.N = (int)N; a.T = (int)T; a.H_k = (int)Hk; a.H_v = (int)Hv;
     a.C = (int)pl.C; a.n_ck = (int)pl.n_ck; a.c2 = pl.c2; a.nsub_max = pl.nsub_max;
+    a.SK = pl.SK; a.DV = pl.DV;
     a.scale = p->scale;
     a.vec_q = vec_ok(q, p->q_s); a.vec_k = vec_ok(k, p->k_s); a.vec_v = vec_ok(v, p->v_s);
     a.vec_gy = vec_ok(gy, p->gy_s); a.vec_g = aligned(g, 16);
@@ -866,7 +875,8 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k, c
     gdn::ReduceArgs r{};
     r.ws_col = a.ws_col; r.ws_sc = a.ws_sc;
     r.dq = packed + off[0]; r.dk = packed + off[1]; r.dg = packed + off[3]; r.dbeta = packed + off[4];
-    r.N = (int)N; r.T = (int)T; r.H_k = (int)Hk; r.H_v = (int)Hv; r.D = (int)D; r.P = pl.P;
+    r.N = (int)N; r.T = (int)T; r.H_k = (int)Hk; r.H_v = (int)Hv; r.D = pl.D; r.P = pl.P;
+    r.SK = pl.SK;
     r.NQ = pl.kda ? 3 : 2; r.kda = pl.kda;
     st = cuda_status(gdn::launch_reduce(r, stream), "reduce launch");
     tap.mark(stream);

@@ -25,6 +25,9 @@
 //   dS'     = dM + k du^T                  dg   += dS' (.) S'
 //   dM      = a (.) dS'
 //   dv_j = beta dd_j, dbeta += dd_j (v_j - u_j)
+//
+// D is the column width the kernel computes in (S_k, or 32 for S_k = 16 with zero padding
+// columns); the S_v rows are the grid's row blocks, independent of S_k.
 #include <cuda_runtime.h>
 
 #include "gdn_device.cuh"
@@ -38,7 +41,7 @@ __device__ __forceinline__ float4 fmav4(float4 a, float4 b, float4 acc)
 }
 
 template <int D, int RT, bool KDA>
-__global__ void __launch_bounds__(256) gdn_bwd_kernel(const BwdArgs A)
+__global__ void __launch_bounds__(256, 1) gdn_bwd_kernel(const BwdArgs A)
 {
     constexpr int NV = D / 32;
     constexpr int NQ = KDA ? 3 : 2;  // column quantities: dq, dk (, dg)
@@ -73,6 +76,7 @@ __global__ void __launch_bounds__(256) gdn_bwd_kernel(const BwdArgs A)
 
     const long long head = (long long)n * A.H_v + h;
     const long long cta = head * P + p;
+    const int SK = A.SK, DV = A.DV;
     float4* sub = reinterpret_cast<float4*>(A.sub) +
                   cta * (long long)(A.nsub_max > 1 ? A.nsub_max - 1 : 0) * (RT * NV * NT);
 
@@ -81,19 +85,20 @@ __global__ void __launch_bounds__(256) gdn_bwd_kernel(const BwdArgs A)
     for (int r = 0; r < RT; ++r)
 #pragma unroll
         for (int v = 0; v < NV; ++v)
-            dm[r][v] = A.dstate_T
-                           ? __ldg(reinterpret_cast<const float4*>(A.dstate_T + (head * D + row0 + r) * D) +
-                                   8 * v + cl)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            dm[r][v] = A.dstate_T ? ld_state4(A.dstate_T + (head * DV + row0 + r) * SK, v, cl, SK)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    zero_pad_cols(sk, c2, SK, D, tid, NT);
+    zero_pad_cols(sq, c2, SK, D, tid, NT);
+    if (KDA) zero_pad_cols(sa, c2, SK, D, tid, NT);
 
     // Stage the inputs of tokens [ta, ta + nt) in shared memory.
     auto load_tile = [&](int ta, int nt, bool for_walk) {
         const long long tok0 = (long long)n * A.T + ta;
-        load_rows(sk, A.k + n * A.ks0 + (long long)ta * A.ks1 + hk * A.ks2, A.ks1, nt, D,
-                  A.vec_k, tid, NT);
+        load_rows(sk, A.k + n * A.ks0 + (long long)ta * A.ks1 + hk * A.ks2, A.ks1, nt, SK,
+                  A.vec_k, tid, NT, D);
         if (KDA) {
-            load_rows_exp(sa, A.g + (tok0 * A.H_v + h) * D, (long long)A.H_v * D, nt, D,
-                          A.vec_g, tid, NT);
+            load_rows_exp(sa, A.g + (tok0 * A.H_v + h) * SK, (long long)A.H_v * SK, nt, SK,
+                          A.vec_g, tid, NT, D);
         } else {
             for (int tt = tid; tt < nt; tt += NT) sa[tt] = expf(__ldg(A.g + (tok0 + tt) * A.H_v + h));
         }
@@ -101,31 +106,30 @@ __global__ void __launch_bounds__(256) gdn_bwd_kernel(const BwdArgs A)
         load_rows(sv, A.v + n * A.vs0 + (long long)ta * A.vs1 + h * A.vs2 + p * R, A.vs1, nt, R,
                   A.vec_v, tid, NT);
         if (for_walk) {
-            load_rows(sq, A.q + n * A.qs0 + (long long)ta * A.qs1 + hk * A.qs2, A.qs1, nt, D,
-                      A.vec_q, tid, NT);
+            load_rows(sq, A.q + n * A.qs0 + (long long)ta * A.qs1 + hk * A.qs2, A.qs1, nt, SK,
+                      A.vec_q, tid, NT, D);
             load_rows(sgy, A.gy + n * A.gys0 + (long long)ta * A.gys1 + h * A.gys2 + p * R,
                       A.gys1, nt, R, A.vec_gy, tid, NT);
         }
     };
 
-    auto load_state = [&](float4 (&m)[RT][NV], const float4* src, long long row_stride4) {
+    auto load_state = [&](float4 (&m)[RT][NV], const float* src) {  // rows of SK floats
 #pragma unroll
         for (int r = 0; r < RT; ++r)
 #pragma unroll
-            for (int v = 0; v < NV; ++v) m[r][v] = src[(lrow0 + r) * row_stride4 + 8 * v + cl];
+            for (int v = 0; v < NV; ++v) m[r][v] = ld_state4(src + (lrow0 + r) * SK, v, cl, SK);
     };
 
     for (int s = A.n_ck - 1; s >= 0; --s) {
         const int t0 = s * A.C, t1 = min(A.T, t0 + A.C);
         const int nsub = (t1 - t0 + c2 - 1) / c2;
         // ckpt[n][h][s], this CTA's rows
-        const float4* cks =
-            reinterpret_cast<const float4*>(A.ckpt + ((head * A.n_ck + s) * D + p * R) * D);
+        const float* cks = A.ckpt + ((head * A.n_ck + s) * DV + p * R) * SK;
 
         // ---- level 1: sub-checkpoints at tokens t0 + b c2, b = 1 .. nsub-1 ----
         if (nsub > 1) {
             float4 m[RT][NV];
-            load_state(m, cks, D / 4);
+            load_state(m, cks);
             for (int b = 0; b < nsub - 1; ++b) {
                 const int ta = t0 + b * c2;
                 __syncthreads();
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(256) gdn_bwd_kernel(const BwdArgs A)
             {  // recompute the sub-segment's states into the ring
                 float4 m[RT][NV];
                 if (b == 0) {
-                    load_state(m, cks, D / 4);
+                    load_state(m, cks);
                 } else {
                     const float4* src = sub + (long long)(b - 1) * (RT * NV * NT);
 #pragma unroll
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(256) gdn_bwd_kernel(const BwdArgs A)
             }
             for (int idx = tid; idx < nt * R; idx += NT) {
                 const int tt = idx / R, j = idx - tt * R;
-                A.dv[((tok0 + tt) * A.H_v + h) * D + p * R + j] = __fmul_rn(sb[tt], sdd[idx]);
+                A.dv[((tok0 + tt) * A.H_v + h) * DV + p * R + j] = __fmul_rn(sb[tt], sdd[idx]);
             }
         }
     }
@@ -333,9 +337,10 @@ __global__ void __launch_bounds__(256) gdn_bwd_kernel(const BwdArgs A)
     // dstate0 = dM after the last reverse step (the gradient of the initial state)
 #pragma unroll
     for (int r = 0; r < RT; ++r) {
-        float* dst = A.dstate0 + (head * D + row0 + r) * D;
+        float* dst = A.dstate0 + (head * DV + row0 + r) * SK;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
+            if (32 * v + 4 * cl >= SK) continue;  // padding columns (S_k = 16)
             if (A.vec_ds0) {
                 reinterpret_cast<float4*>(dst)[8 * v + cl] = dm[r][v];
             } else {
@@ -349,11 +354,12 @@ __global__ void __launch_bounds__(256) gdn_bwd_kernel(const BwdArgs A)
 // Fixed-order sums of the per-CTA partials: dq/dk over the value heads h_k, h_k + H_k,
 // ... (ascending) and, inside each, over the P row blocks; dg (KDA), dbeta and dg
 // (scalar gate) over the row blocks.
+// The partials are D wide (the kernels' column width); the outputs SK wide (S_k).
 __global__ void __launch_bounds__(256) gdn_reduce_kernel(const ReduceArgs A)
 {
-    const long long nqk = (long long)A.N * A.T * A.H_k * A.D;
+    const long long nqk = (long long)A.N * A.T * A.H_k * A.SK;
     const long long nhv = (long long)A.N * A.T * A.H_v;
-    const long long ndg = A.kda ? nhv * A.D : 0;
+    const long long ndg = A.kda ? nhv * A.SK : 0;
     const long long total = 2 * nqk + ndg + nhv;
     const int ncol = A.NQ * A.D;
     const int r = A.H_v / A.H_k;
@@ -362,8 +368,8 @@ __global__ void __launch_bounds__(256) gdn_reduce_kernel(const ReduceArgs A)
         if (idx < 2 * nqk) {
             const int which = idx >= nqk;  // 0: dq, 1: dk
             const long long e = idx - which * nqk;
-            const int i = (int)(e % A.D);
-            const long long tokhk = e / A.D;  // (n*T + t)*H_k + hk
+            const int i = (int)(e % A.SK);
+            const long long tokhk = e / A.SK;  // (n*T + t)*H_k + hk
             const int hkk = (int)(tokhk % A.H_k);
             const long long tok = tokhk / A.H_k;
             // per value head: the sum over its P row blocks; then the value heads in
@@ -379,8 +385,8 @@ __global__ void __launch_bounds__(256) gdn_reduce_kernel(const ReduceArgs A)
             (which ? A.dk : A.dq)[e] = acc;
         } else if (idx < 2 * nqk + ndg) {
             const long long e = idx - 2 * nqk;
-            const int i = (int)(e % A.D);
-            const long long tokh = e / A.D;
+            const int i = (int)(e % A.SK);
+            const long long tokh = e / A.SK;
             const float* src = A.ws_col + tokh * A.P * ncol + 2 * A.D + i;
             float acc = 0.f;
             for (int pp = 0; pp < A.P; ++pp) acc = __fadd_rn(acc, src[(long long)pp * ncol]);
@@ -409,7 +415,7 @@ static int launch_bwd_t(const BwdArgs& a, int W, void* stream)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid(D / R, a.H_v, a.N);
+    dim3 grid(a.DV / R, a.H_v, a.N);
     kern<<<grid, 32 * W, smem, (cudaStream_t)stream>>>(a);
     return (int)cudaGetLastError();
 }
@@ -426,15 +432,16 @@ int launch_backward(const BwdArgs& a, int D, int RT, int W, bool kda, void* stre
     GDN_BWD_CASE(32, 2)
     GDN_BWD_CASE(64, 2)
     GDN_BWD_CASE(128, 2)
+    GDN_BWD_CASE(256, 1)
 #undef GDN_BWD_CASE
     return (int)cudaErrorInvalidValue;
 }
 
 int launch_reduce(const ReduceArgs& a, void* stream)
 {
-    const long long nqk = (long long)a.N * a.T * a.H_k * a.D;
+    const long long nqk = (long long)a.N * a.T * a.H_k * a.SK;
     const long long nhv = (long long)a.N * a.T * a.H_v;
-    const long long total = 2 * nqk + (a.kda ? nhv * a.D : 0) + nhv;
+    const long long total = 2 * nqk + (a.kda ? nhv * a.SK : 0) + nhv;
     if (total == 0) return 0;
     long long blocks = (total + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;

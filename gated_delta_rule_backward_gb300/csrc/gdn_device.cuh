@@ -118,10 +118,11 @@ __device__ __forceinline__ void recurrence_step(float4 (&m)[RT][NV], float4 (&sp
 
 // The 16-byte path of load_rows: up to B loads per thread are in flight before the first
 // of their shared-memory stores, so a tile costs one global round trip per batch instead
-// of one per load.  f maps each loaded float4 to the stored one.
+// of one per load.  f maps each loaded float4 to the stored one.  Shared rows are ld
+// floats apart (ld >= width).
 template <int B, typename F>
 __device__ __forceinline__ void load_rows_vec(float* dst, const float* src, long long stride,
-                                              int nt, int width, int tid, int nthr, F f)
+                                              int nt, int width, int tid, int nthr, F f, int ld)
 {
     const int per = width >> 2, total = nt * per;
     for (int base = tid; base < total; base += B * nthr) {
@@ -139,25 +140,27 @@ __device__ __forceinline__ void load_rows_vec(float* dst, const float* src, long
             const int idx = base + b * nthr;
             if (idx < total) {
                 const int tt = idx / per, i4 = idx - tt * per;
-                reinterpret_cast<float4*>(dst + tt * width)[i4] = f(x[b]);
+                reinterpret_cast<float4*>(dst + tt * ld)[i4] = f(x[b]);
             }
         }
     }
 }
 
 // Cooperative copy of nt rows of `width` floats (row stride `stride` in global memory)
-// into a dense shared tile.  vec: every row start is 16-byte aligned and width % 4 == 0.
-// B: loads per thread in flight at once on the 16-byte path.
+// into a shared tile whose rows are ld floats apart (ld = width unless given; the columns
+// [width, ld) are left as they are).  vec: every row start is 16-byte aligned and
+// width % 4 == 0.  B: loads per thread in flight at once on the 16-byte path.
 template <int B = 1>
 __device__ __forceinline__ void load_rows(float* dst, const float* src, long long stride,
-                                          int nt, int width, bool vec, int tid, int nthr)
+                                          int nt, int width, bool vec, int tid, int nthr, int ld = 0)
 {
+    if (ld == 0) ld = width;
     if (vec) {
-        load_rows_vec<B>(dst, src, stride, nt, width, tid, nthr, [](float4 x) { return x; });
+        load_rows_vec<B>(dst, src, stride, nt, width, tid, nthr, [](float4 x) { return x; }, ld);
     } else {
         for (int idx = tid; idx < nt * width; idx += nthr) {
             const int tt = idx / width, i = idx - tt * width;
-            dst[tt * width + i] = __ldg(src + tt * stride + i);
+            dst[tt * ld + i] = __ldg(src + tt * stride + i);
         }
     }
 }
@@ -165,16 +168,40 @@ __device__ __forceinline__ void load_rows(float* dst, const float* src, long lon
 // As load_rows, storing exp(x) (the gate a = exp(g), accurate expf).
 template <int B = 1>
 __device__ __forceinline__ void load_rows_exp(float* dst, const float* src, long long stride,
-                                              int nt, int width, bool vec, int tid, int nthr)
+                                              int nt, int width, bool vec, int tid, int nthr, int ld = 0)
 {
+    if (ld == 0) ld = width;
     if (vec) {
         load_rows_vec<B>(dst, src, stride, nt, width, tid, nthr,
-                      [](float4 x) { return make_float4(expf(x.x), expf(x.y), expf(x.z), expf(x.w)); });
+                      [](float4 x) { return make_float4(expf(x.x), expf(x.y), expf(x.z), expf(x.w)); }, ld);
     } else {
         for (int idx = tid; idx < nt * width; idx += nthr) {
             const int tt = idx / width, i = idx - tt * width;
-            dst[tt * width + i] = expf(__ldg(src + tt * stride + i));
+            dst[tt * ld + i] = expf(__ldg(src + tt * stride + i));
         }
+    }
+}
+
+// One lane's float4 block v of a state row of SK floats in global memory (SK may be below
+// the kernel's column width: the blocks past SK read as zero and are never written).
+__device__ __forceinline__ float4 ld_state4(const float* row, int v, int cl, int SK)
+{
+    return (32 * v + 4 * cl < SK) ? __ldg(reinterpret_cast<const float4*>(row) + 8 * v + cl)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+__device__ __forceinline__ void st_state4(float* row, int v, int cl, int SK, float4 x)
+{
+    if (32 * v + 4 * cl < SK) reinterpret_cast<float4*>(row)[8 * v + cl] = x;
+}
+
+// Zero the columns [sk, ld) of the first `rows` rows of a shared tile (head size 16 runs
+// at column width 32: its padding columns stay zero, so k = q = 0 and M = 0 there).
+__device__ __forceinline__ void zero_pad_cols(float* dst, int rows, int sk, int ld, int tid, int nthr)
+{
+    if (sk >= ld) return;
+    for (int idx = tid; idx < rows * (ld - sk); idx += nthr) {
+        const int t = idx / (ld - sk), i = sk + idx - t * (ld - sk);
+        dst[t * ld + i] = 0.f;
     }
 }
 

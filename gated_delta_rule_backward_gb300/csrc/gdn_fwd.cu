@@ -7,8 +7,12 @@
 // a tile: each warp runs its own chain of tokens over its rows.
 //
 // Per tile of tc tokens the CTA stages k, q, a = exp(g), beta and its own rows of v in
-// shared memory; the state lives in registers (RT rows x S/8 columns per lane).  The
+// shared memory; the state lives in registers (RT rows x D/8 columns per lane).  The
 // state entering token c*C is written to ckpt[c] (PR #16 body: checkpointed recompute).
+//
+// D is the column width the kernel computes in (the key head size S_k, or 32 for S_k = 16,
+// whose padding columns hold zeros throughout); the S_v rows of M are the grid's
+// S_v / R row blocks, so S_k and S_v are independent.
 #include <cuda_runtime.h>
 
 #include "gdn_device.cuh"
@@ -16,7 +20,7 @@
 namespace gdn {
 
 template <int D, int RT, bool KDA>
-__global__ void __launch_bounds__(128, 3) gdn_fwd_kernel(const FwdArgs A)
+__global__ void __launch_bounds__(128, D <= 128 ? 3 : 1) gdn_fwd_kernel(const FwdArgs A)
 {
     constexpr int NV = D / 32;
     const int NT = blockDim.x, W = NT >> 5;
@@ -39,25 +43,27 @@ __global__ void __launch_bounds__(128, 3) gdn_fwd_kernel(const FwdArgs A)
     float* sy = sm + L.sy;
 
     const long long head = (long long)n * A.H_v + h;
+    const int SK = A.SK, DV = A.DV;
     float4 m[RT][NV];
 #pragma unroll
     for (int r = 0; r < RT; ++r)
 #pragma unroll
-        for (int v = 0; v < NV; ++v)
-            m[r][v] = __ldg(reinterpret_cast<const float4*>(A.state0 + (head * D + row0 + r) * D) +
-                            8 * v + cl);
+        for (int v = 0; v < NV; ++v) m[r][v] = ld_state4(A.state0 + (head * DV + row0 + r) * SK, v, cl, SK);
+    zero_pad_cols(sk, A.tc, SK, D, tid, NT);
+    zero_pad_cols(sq, A.tc, SK, D, tid, NT);
+    if (KDA) zero_pad_cols(sa, A.tc, SK, D, tid, NT);
 
     for (int t0 = 0; t0 < A.T; t0 += tc) {
         const int nt = min(tc, A.T - t0);
         __syncthreads();
-        load_rows<4>(sk, A.k + n * A.ks0 + (long long)t0 * A.ks1 + hk * A.ks2, A.ks1, nt, D,
-                  A.vec_k, tid, NT);
-        load_rows<4>(sq, A.q + n * A.qs0 + (long long)t0 * A.qs1 + hk * A.qs2, A.qs1, nt, D,
-                  A.vec_q, tid, NT);
+        load_rows<4>(sk, A.k + n * A.ks0 + (long long)t0 * A.ks1 + hk * A.ks2, A.ks1, nt, SK,
+                  A.vec_k, tid, NT, D);
+        load_rows<4>(sq, A.q + n * A.qs0 + (long long)t0 * A.qs1 + hk * A.qs2, A.qs1, nt, SK,
+                  A.vec_q, tid, NT, D);
         const long long tok0 = (long long)n * A.T + t0;
         if (KDA) {
-            load_rows_exp<4>(sa, A.g + (tok0 * A.H_v + h) * D, (long long)A.H_v * D, nt, D,
-                          A.vec_g, tid, NT);
+            load_rows_exp<4>(sa, A.g + (tok0 * A.H_v + h) * SK, (long long)A.H_v * SK, nt, SK,
+                          A.vec_g, tid, NT, D);
         } else {
             for (int tt = tid; tt < nt; tt += NT) sa[tt] = expf(__ldg(A.g + (tok0 + tt) * A.H_v + h));
         }
@@ -69,12 +75,11 @@ __global__ void __launch_bounds__(128, 3) gdn_fwd_kernel(const FwdArgs A)
         for (int tt = 0; tt < nt; ++tt) {
             const int t = t0 + tt;
             if (t % A.C == 0) {
-                float* ck = A.ckpt + ((head * A.n_ck + t / A.C) * D + row0) * D;
+                float* ck = A.ckpt + ((head * A.n_ck + t / A.C) * DV + row0) * SK;
 #pragma unroll
                 for (int r = 0; r < RT; ++r)
 #pragma unroll
-                    for (int v = 0; v < NV; ++v)
-                        reinterpret_cast<float4*>(ck + r * D)[8 * v + cl] = m[r][v];
+                    for (int v = 0; v < NV; ++v) st_state4(ck + r * SK, v, cl, SK, m[r][v]);
             }
             float4 kv[NV], qv[NV], av[NV];
 #pragma unroll
@@ -102,8 +107,8 @@ __global__ void __launch_bounds__(128, 3) gdn_fwd_kernel(const FwdArgs A)
         }
         __syncthreads();
         // y rows of this CTA for the tile: R contiguous floats per token
-        float* ydst = A.y + (tok0 * A.H_v + h) * D + p * R;
-        const long long ystride = (long long)A.H_v * D;
+        float* ydst = A.y + (tok0 * A.H_v + h) * DV + p * R;
+        const long long ystride = (long long)A.H_v * DV;
         for (int idx = tid; idx < nt * R; idx += NT) {
             const int tt = idx / R, j = idx - tt * R;
             ydst[tt * ystride + j] = sy[tt * R + j];
@@ -113,8 +118,7 @@ __global__ void __launch_bounds__(128, 3) gdn_fwd_kernel(const FwdArgs A)
 #pragma unroll
     for (int r = 0; r < RT; ++r)
 #pragma unroll
-        for (int v = 0; v < NV; ++v)
-            reinterpret_cast<float4*>(A.state_T + (head * D + row0 + r) * D)[8 * v + cl] = m[r][v];
+        for (int v = 0; v < NV; ++v) st_state4(A.state_T + (head * DV + row0 + r) * SK, v, cl, SK, m[r][v]);
 }
 
 template <int D, int RT, bool KDA>
@@ -127,7 +131,7 @@ static int launch_fwd_t(const FwdArgs& a, int W, void* stream)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid(D / R, a.H_v, a.N);
+    dim3 grid(a.DV / R, a.H_v, a.N);
     kern<<<grid, 32 * W, smem, (cudaStream_t)stream>>>(a);
     return (int)cudaGetLastError();
 }
@@ -144,6 +148,7 @@ int launch_forward(const FwdArgs& a, int D, int RT, int W, bool kda, void* strea
     GDN_FWD_CASE(32, 2)
     GDN_FWD_CASE(64, 2)
     GDN_FWD_CASE(128, 2)
+    GDN_FWD_CASE(256, 1)
 #undef GDN_FWD_CASE
     return (int)cudaErrorInvalidValue;
 }

@@ -36,6 +36,7 @@ struct FwdArgs {
     float* ckpt;
     long long qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2;
     int N, T, H_k, H_v, C, n_ck;
+    int SK, DV;  // key head size (the state's columns) and value head size (its rows)
     float scale;
     int tc;  // tokens per shared-memory tile
     int vec_q, vec_k, vec_v, vec_g;
@@ -57,6 +58,7 @@ struct BwdArgs {
     float* ws_sc;           // workspace: per-CTA scalar partials [N*T*H_v][P][2]
     long long qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2, gys0, gys1, gys2;
     int N, T, H_k, H_v, C, n_ck, c2, nsub_max;
+    int SK, DV;  // key head size (the state's columns) and value head size (its rows)
     float scale;
     int vec_q, vec_k, vec_v, vec_gy, vec_g, vec_ds0;
 };
@@ -69,6 +71,7 @@ struct ReduceArgs {
     float* dg;
     float* dbeta;
     int N, T, H_k, H_v, D, P, NQ, kda;
+    int SK;  // output column width (S_k); the partials are D wide
 };
 
 // Chunked (WY) form, scalar gate: chunk length and the arguments of its kernels.

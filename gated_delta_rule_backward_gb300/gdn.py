@@ -100,18 +100,20 @@ def library():
 
 
 def make_params(N, T, H_k, H_v, S, kda, C=None, scale=None, q_s=None, k_s=None, v_s=None,
-                gy_s=None, in_dtype=DTYPE_F32) -> GdnParams:
-    """Parameter struct; strides default to the contiguous [N,T,H,S] layout."""
+                gy_s=None, in_dtype=DTYPE_F32, S_v=None) -> GdnParams:
+    """Parameter struct; S is the key head size S_k, S_v the value head size (default S);
+    strides default to the contiguous [N,T,H,S] layouts."""
+    SV = S if S_v is None else int(S_v)
     p = GdnParams()
-    p.n_seq, p.T, p.H_k, p.H_v, p.S_k, p.S_v = N, T, H_k, H_v, S, S
+    p.n_seq, p.T, p.H_k, p.H_v, p.S_k, p.S_v = N, T, H_k, H_v, S, SV
     p.gate = GATE_KDA if kda else GATE_SCALAR
     p.in_dtype, p.reserved1 = int(in_dtype), 0.0
     p.C = 0 if C is None else int(C)
     p.scale = (1.0 / math.sqrt(S)) if scale is None else float(scale)
     p.q_s[:] = q_s or (T * H_k * S, H_k * S, S)
     p.k_s[:] = k_s or (T * H_k * S, H_k * S, S)
-    p.v_s[:] = v_s or (T * H_v * S, H_v * S, S)
-    p.gy_s[:] = gy_s or (T * H_v * S, H_v * S, S)
+    p.v_s[:] = v_s or (T * H_v * SV, H_v * SV, SV)
+    p.gy_s[:] = gy_s or (T * H_v * SV, H_v * SV, SV)
     return p
 
 
@@ -146,7 +148,8 @@ def params_for(q, k, v, g, gy=None, C=None, scale=None) -> GdnParams:
             raise TypeError("q, k, v, g (and gy) must share one storage type")
     return make_params(N, T, H_k, H_v, S, kda, C=C, scale=scale, q_s=strides3(q),
                        k_s=strides3(k), v_s=strides3(v),
-                       gy_s=strides3(gy) if gy is not None else None, in_dtype=dt)
+                       gy_s=strides3(gy) if gy is not None else None, in_dtype=dt,
+                       S_v=v.shape[3])
 
 
 def _ptr(t):
@@ -263,11 +266,11 @@ def forward(q, k, v, g, beta, state0, C=None, scale=None, stream=None):
     import torch
     p = params_for(q, k, v, g, C=C, scale=scale)
     N, T, H_k, S = q.shape
-    H_v = v.shape[2]
+    H_v, SV = v.shape[2], v.shape[3]
     dev = q.device
-    y = torch.empty((N, T, H_v, S), dtype=torch.float32, device=dev)
-    state_T = torch.empty((N, H_v, S, S), dtype=torch.float32, device=dev)
-    ckpt = torch.empty((N, H_v, num_checkpoints(p), S, S), dtype=torch.float32, device=dev)
+    y = torch.empty((N, T, H_v, SV), dtype=torch.float32, device=dev)
+    state_T = torch.empty((N, H_v, SV, S), dtype=torch.float32, device=dev)
+    ckpt = torch.empty((N, H_v, num_checkpoints(p), SV, S), dtype=torch.float32, device=dev)
     nws = forward_workspace_bytes(p)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
     gdn_forward(p, q, k, v, g, beta, state0, y, state_T, ckpt, ws, stream)
@@ -276,11 +279,11 @@ def forward(q, k, v, g, beta, state0, C=None, scale=None, stream=None):
 
 def split_packed(p: GdnParams, packed):
     """Views of the six regions of a packed gradient buffer."""
-    N, T, H_k, H_v, S = p.n_seq, p.T, p.H_k, p.H_v, p.S_k
+    N, T, H_k, H_v, S, SV = p.n_seq, p.T, p.H_k, p.H_v, p.S_k, p.S_v
     off = packed_grad_offsets(p) + [packed_grad_elems(p)]
-    shapes = [(N, T, H_k, S), (N, T, H_k, S), (N, T, H_v, S),
+    shapes = [(N, T, H_k, S), (N, T, H_k, S), (N, T, H_v, SV),
               (N, T, H_v, S) if p.gate == GATE_KDA else (N, T, H_v), (N, T, H_v),
-              (N, H_v, S, S)]
+              (N, H_v, SV, S)]
     names = ["dq", "dk", "dv", "dg", "dbeta", "dstate0"]
     return {nm: packed[off[i]:off[i + 1]].view(shapes[i]) for i, nm in enumerate(names)}
 

@@ -43,6 +43,7 @@ class Problem:
     gy: np.ndarray      # [N,T,H_v,d]
     dstate_T: np.ndarray | None
     qkv: np.ndarray | None  # the packed buffer when packed=True
+    d_v: int | None = None  # value head size (S_v); d is the key head size (S_k)
 
 
 def _normal(rng, shape, std=1.0):
@@ -63,33 +64,35 @@ def _sigmoid(x):
 
 
 def make_problem(N, T, H_k, H_v, d, kda=False, seed=0, g_std=1.0, C=None,
-                 packed=False, dstate_T=False):
-    """Draw one seeded problem.  Draw order is fixed: q, k, v, g, beta, state0, gy, dstate_T."""
+                 packed=False, dstate_T=False, d_v=None):
+    """Draw one seeded problem.  Draw order is fixed: q, k, v, g, beta, state0, gy, dstate_T.
+    d is the key head size S_k; d_v the value head size S_v (default d)."""
     if H_v % H_k:
         raise ValueError("H_v must be a multiple of H_k")
+    dv = d if d_v is None else d_v
     rng = np.random.default_rng(seed)
     f32 = np.float32
     q = _l2norm(_normal(rng, (N, T, H_k, d))).astype(f32)
     k = _l2norm(_normal(rng, (N, T, H_k, d))).astype(f32)
-    v = _normal(rng, (N, T, H_v, d)).astype(f32)
+    v = _normal(rng, (N, T, H_v, dv)).astype(f32)
     gshape = (N, T, H_v, d) if kda else (N, T, H_v)
     g = (-_softplus(_normal(rng, gshape, g_std))).astype(f32)
     beta = _sigmoid(_normal(rng, (N, T, H_v))).astype(f32)
-    state0 = _normal(rng, (N, H_v, d, d), 0.1).astype(f32)
-    gy = _normal(rng, (N, T, H_v, d)).astype(f32)
-    dsT = _normal(rng, (N, H_v, d, d), 0.1).astype(f32) if dstate_T else None
+    state0 = _normal(rng, (N, H_v, dv, d), 0.1).astype(f32)
+    gy = _normal(rng, (N, T, H_v, dv)).astype(f32)
+    dsT = _normal(rng, (N, H_v, dv, d), 0.1).astype(f32) if dstate_T else None
     qkv = None
     if packed:
-        width = (2 * H_k + H_v) * d
+        width = 2 * H_k * d + H_v * dv
         qkv = np.empty((N, T, width), dtype=f32)
         qkv[:, :, : H_k * d] = q.reshape(N, T, H_k * d)
         qkv[:, :, H_k * d: 2 * H_k * d] = k.reshape(N, T, H_k * d)
-        qkv[:, :, 2 * H_k * d:] = v.reshape(N, T, H_v * d)
+        qkv[:, :, 2 * H_k * d:] = v.reshape(N, T, H_v * dv)
         q = qkv[:, :, : H_k * d].reshape(N, T, H_k, d)
         k = qkv[:, :, H_k * d: 2 * H_k * d].reshape(N, T, H_k, d)
-        v = qkv[:, :, 2 * H_k * d:].reshape(N, T, H_v, d)
+        v = qkv[:, :, 2 * H_k * d:].reshape(N, T, H_v, dv)
     return Problem(N, T, H_k, H_v, d, kda, C, 1.0 / float(np.sqrt(d)), q, k, v, g, beta,
-                   state0, gy, dsT, qkv)
+                   state0, gy, dsT, qkv, dv)
 
 
 # The named workloads (shapes and distributions of the gated delta rule configurations).

@@ -19,11 +19,12 @@ def upload(prob, device="cuda"):
     d = {}
     if prob.qkv is not None:
         N, T, H_k, H_v, S = prob.N, prob.T, prob.H_k, prob.H_v, prob.d
+        SV = prob.d_v or S
         qkv = t(prob.qkv)
         d["qkv"] = qkv
         d["q"] = qkv[:, :, : H_k * S].view(N, T, H_k, S)
         d["k"] = qkv[:, :, H_k * S: 2 * H_k * S].view(N, T, H_k, S)
-        d["v"] = qkv[:, :, 2 * H_k * S:].view(N, T, H_v, S)
+        d["v"] = qkv[:, :, 2 * H_k * S:].view(N, T, H_v, SV)
     else:
         d["q"], d["k"], d["v"] = t(prob.q), t(prob.k), t(prob.v)
     for name in ("g", "beta", "state0", "gy", "dstate_T"):

@@ -124,12 +124,33 @@ def call_backward(p, ws_bytes, ptrs=None):
 
 
 def test_unsupported_head_sizes():
-    assert call_forward(gdn.make_params(1, 8, 1, 1, 48, False)) == UNSUPPORTED
-    assert call_forward(gdn.make_params(1, 8, 1, 1, 16, False)) == UNSUPPORTED
-    p = gdn.make_params(1, 8, 1, 1, 64, False)
-    p.S_v = 32
-    assert call_forward(p) == UNSUPPORTED
-    assert b"S_k" in gdn.library().gdn_last_error()
+    """Key head sizes 16, 32, 64, 128, 256; value head sizes multiples of 16 up to 256, in
+    any combination (S_k != S_v included)."""
+    for sk in (8, 48, 512):
+        assert call_forward(gdn.make_params(1, 8, 1, 1, sk, False)) == UNSUPPORTED
+        assert b"S_k" in gdn.library().gdn_last_error()
+    for sv in (8, 24, 272):
+        assert call_forward(gdn.make_params(1, 8, 1, 1, 64, False, S_v=sv)) == UNSUPPORTED
+        assert b"S_v" in gdn.library().gdn_last_error()
+
+
+def test_head_shapes_beyond_the_chunked_form_run_the_token_recurrence():
+    """Square heads of 32, 64, 128 run the chunked kernels (the per-key-column gate at 128
+    only); head sizes 16 and 256 and S_k != S_v run the token recurrence (forward; backward +
+    reduction), with its work-proportional backward workspace."""
+    for sk, sv, kda in ((64, 32, False), (32, 128, True), (16, 16, False), (16, 64, True),
+                        (256, 256, False), (256, 64, True), (128, 256, False)):
+        p = gdn.make_params(2, 61, 2, 4, sk, kda, C=8, S_v=sv)
+        assert gdn.launches(p) == (1, 2), (sk, sv, kda)
+        assert gdn.forward_workspace_bytes(p) == 0
+        assert gdn.backward_workspace_bytes(p) > 0
+        off = gdn.packed_grad_offsets(p)
+        N, T, Hk, Hv = 2, 61, 2, 4
+        assert off[2] - off[1] == N * T * Hk * sk                 # dk
+        assert off[3] - off[2] == N * T * Hv * sv                 # dv
+        assert gdn.packed_grad_elems(p) - off[5] == N * Hv * sv * sk  # dstate
+    for sk in (32, 64):  # the FP32-pipe chunked kernels (head size 128: the pipelined ones)
+        assert gdn.launches(gdn.make_params(2, 61, 2, 4, sk, False, C=8)) == (2, 3)
 
 
 def test_invalid_arguments():
