@@ -64,16 +64,21 @@ def _sigmoid(x):
 
 
 def make_problem(N, T, H_k, H_v, d, kda=False, seed=0, g_std=1.0, C=None,
-                 packed=False, dstate_T=False, d_v=None):
+                 packed=False, dstate_T=False, d_v=None, seq_rep=1):
     """Draw one seeded problem.  Draw order is fixed: q, k, v, g, beta, state0, gy, dstate_T.
-    d is the key head size S_k; d_v the value head size S_v (default d)."""
+    d is the key head size S_k; d_v the value head size S_v (default d).  With seq_rep > 1
+    q and k hold N / seq_rep sequences, value sequence n reading q/k sequence n / seq_rep
+    (not with packed=True)."""
     if H_v % H_k:
         raise ValueError("H_v must be a multiple of H_k")
+    if N % seq_rep or (packed and seq_rep != 1):
+        raise ValueError("seq_rep must divide N (and the packed layout has one q/k per sequence)")
     dv = d if d_v is None else d_v
+    Nq = N // seq_rep
     rng = np.random.default_rng(seed)
     f32 = np.float32
-    q = _l2norm(_normal(rng, (N, T, H_k, d))).astype(f32)
-    k = _l2norm(_normal(rng, (N, T, H_k, d))).astype(f32)
+    q = _l2norm(_normal(rng, (Nq, T, H_k, d))).astype(f32)
+    k = _l2norm(_normal(rng, (Nq, T, H_k, d))).astype(f32)
     v = _normal(rng, (N, T, H_v, dv)).astype(f32)
     gshape = (N, T, H_v, d) if kda else (N, T, H_v)
     g = (-_softplus(_normal(rng, gshape, g_std))).astype(f32)

@@ -39,6 +39,7 @@ class Dims(ctypes.Structure):
         ("kda", ctypes.c_int64),
         ("C", ctypes.c_int64),
         ("scale", ctypes.c_double),
+        ("rep", ctypes.c_int64),
     ]
 
 
@@ -121,21 +122,25 @@ def _ptr(a):
 
 
 def _dims(q, v, g, C, scale):
-    N, T, H_k, S_k = q.shape
-    H_v, S_v = v.shape[2], v.shape[3]
+    """Sizes from the arrays: v holds the N value sequences, q the N / rep q/k sequences."""
+    N, T, H_v, S_v = v.shape
+    H_k, S_k = q.shape[2], q.shape[3]
+    if q.shape[0] == 0 or N % q.shape[0]:
+        raise ValueError("v's sequences must be a multiple of q's")
     kda = 1 if g.ndim == 4 else 0
-    return Dims(N, T, H_k, H_v, S_k, S_v, kda, int(C), float(scale))
+    return Dims(N, T, H_k, H_v, S_k, S_v, kda, int(C), float(scale), N // q.shape[0])
 
 
 def forward(q, k, v, g, beta, state0, scale, C=None, lib=None):
-    """Oracle forward.  Arrays are promoted to float64 (contiguous semantic layouts).
+    """Oracle forward.  Arrays are promoted to float64 (contiguous semantic layouts); q, k
+    may hold fewer sequences than v (a divisor of its count: the sequence broadcast).
 
     Returns (y [N,T,H_v,S_v], state_T [N,H_v,S_v,S_k], ckpt [N,H_v,n_ck,S_v,S_k]).
     """
     lib = lib or load()
     q, k, v, g, beta, state0 = map(_f64, (q, k, v, g, beta, state0))
-    N, T, H_k, S_k = q.shape
-    H_v, S_v = v.shape[2], v.shape[3]
+    N, T, H_v, S_v = v.shape
+    H_k, S_k = q.shape[2], q.shape[3]
     C = default_C(T) if C is None else int(C)
     d = _dims(q, v, g, C, scale)
     n_ck = num_checkpoints(T, C)
@@ -159,8 +164,8 @@ def backward(q, k, v, g, beta, state0, gy, dstate_T, scale, C=None, mode="checkp
     lib = lib or load()
     q, k, v, g, beta, state0, gy = map(_f64, (q, k, v, g, beta, state0, gy))
     dsT = None if dstate_T is None else _f64(dstate_T)
-    N, T, H_k, S_k = q.shape
-    H_v, S_v = v.shape[2], v.shape[3]
+    N, T, H_v, S_v = v.shape
+    Nq, H_k, S_k = q.shape[0], q.shape[2], q.shape[3]
     C = default_C(T) if C is None else int(C)
     d = _dims(q, v, g, C, scale)
     m = {"store_all": 0, "checkpointed": 1}[mode]
@@ -168,8 +173,8 @@ def backward(q, k, v, g, beta, state0, gy, dstate_T, scale, C=None, mode="checkp
         _, _, ckpt = forward(q, k, v, g, beta, state0, scale, C=C, lib=lib)
     ck = None if m == 0 else _f64(ckpt)
     out = {
-        "dq": np.zeros((N, T, H_k, S_k)),
-        "dk": np.zeros((N, T, H_k, S_k)),
+        "dq": np.zeros((Nq, T, H_k, S_k)),
+        "dk": np.zeros((Nq, T, H_k, S_k)),
         "dv": np.zeros((N, T, H_v, S_v)),
         "dg": np.zeros(g.shape),
         "dbeta": np.zeros((N, T, H_v)),

@@ -26,7 +26,9 @@
  * Readings taken where the pages leave a step open:
  *   - S' is the decayed previous state a (.) M_{t-1} (the matrix u is computed from);
  *     it is the S' of the dk and dg terms.
- *   - The q/k head of value head h_v is h_v mod H_k (PR #16: "iv1 % neq1").
+ *   - The q/k head of value head h_v is h_v mod H_k (PR #16: "iv1 % neq1"), and the q/k
+ *     sequence of value sequence n is n / rep when q, k hold N / rep sequences (PR #16:
+ *     "iv3/rq3"); dq/dk then sum over the rep value sequences that share one.
  *   - g and beta are per value head; the KDA gate indexes the key column i.
  *   - ckpt[c] is the state entering token c*C, c = 0..ceil(T/C)-1; the last segment
  *     may be partial.
@@ -34,14 +36,14 @@
  *     term adds scale * gy_j q_i to dM.
  *   - The only cotangents are gy (per token output) and dstate_T (final state).
  *
- * Layouts (contiguous float64; M = S^T has S_v rows j and S_k columns i):
- *   q, k    [N][T][H_k][S_k]        v, y     [N][T][H_v][S_v]
+ * Layouts (contiguous float64; M = S^T has S_v rows j and S_k columns i; N_q = N / rep):
+ *   q, k    [N_q][T][H_k][S_k]      v, y     [N][T][H_v][S_v]
  *   g       [N][T][H_v]  (scalar)  or [N][T][H_v][S_k] (KDA)
  *   beta    [N][T][H_v]             state    [N][H_v][S_v][S_k]
  *   ckpt    [N][H_v][n_ck][S_v][S_k]
  *   dq, dk  as q, k;  dv as v;  dg as g;  dbeta as beta;  dstate0 as state
  *
- * Mutations: building with -DGDN_ORACLE_MUTATION=m (m = 1..6) plants one known defect.
+ * Mutations: building with -DGDN_ORACLE_MUTATION=m (m = 1..7) plants one known defect.
  * Only the tests build such copies, to prove that the pins catch each defect.
  */
 #include <math.h>
@@ -61,6 +63,7 @@ typedef struct {
     int64_t kda; /* 0: scalar gate g[N][T][H_v]; 1: per-key-column gate g[N][T][H_v][S_k] */
     int64_t C;   /* checkpoint interval, >= 1 */
     double scale;
+    int64_t rep; /* value sequences per q/k sequence (>= 1); q, k hold N / rep sequences */
 } gdn_oracle_dims;
 
 int64_t gdn_oracle_num_checkpoints(int64_t T, int64_t C)
@@ -102,6 +105,16 @@ static int64_t key_head(const gdn_oracle_dims* d, int64_t hv)
 #endif
 }
 
+/* The q/k sequence that serves value sequence n. */
+static int64_t key_seq(const gdn_oracle_dims* d, int64_t n)
+{
+#if GDN_ORACLE_MUTATION == 7
+    return n % (d->N / d->rep); /* planted defect: interleaved grouping */
+#else
+    return n / d->rep;
+#endif
+}
+
 /* Per-token inputs of one (sequence, value head) unit, gathered as plain vectors. */
 typedef struct {
     const double* q;  /* [S_k] */
@@ -115,10 +128,10 @@ static void gather_token(const gdn_oracle_dims* d, const double* q, const double
                          const double* v, const double* g, const double* beta, int64_t n,
                          int64_t t, int64_t hv, token_in* tk)
 {
-    const int64_t hk = key_head(d, hv);
+    const int64_t hk = key_head(d, hv), nq = key_seq(d, n);
     const int64_t S_k = d->S_k, S_v = d->S_v;
-    tk->q = q + ((n * d->T + t) * d->H_k + hk) * S_k;
-    tk->k = k + ((n * d->T + t) * d->H_k + hk) * S_k;
+    tk->q = q + ((nq * d->T + t) * d->H_k + hk) * S_k;
+    tk->k = k + ((nq * d->T + t) * d->H_k + hk) * S_k;
     tk->v = v + ((n * d->T + t) * d->H_v + hv) * S_v;
     tk->beta = beta[(n * d->T + t) * d->H_v + hv];
     if (d->kda) {
@@ -196,7 +209,8 @@ int gdn_oracle_forward(const gdn_oracle_dims* d, const double* q, const double* 
                        const double* v, const double* g, const double* beta,
                        const double* state0, double* y, double* state_T, double* ckpt)
 {
-    if (!d || d->H_k <= 0 || d->H_v % d->H_k != 0 || d->C <= 0 || d->T < 0 || d->N < 0)
+    if (!d || d->H_k <= 0 || d->H_v % d->H_k != 0 || d->C <= 0 || d->T < 0 || d->N < 0 ||
+        d->rep < 1 || d->N % d->rep != 0)
         return 1;
     const int64_t units = d->N * d->H_v;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -385,7 +399,8 @@ static void backward_unit(const gdn_oracle_dims* d, int mode, int64_t n, int64_t
 
 /* Backward.  mode 0 needs state0, mode 1 needs ckpt (written by gdn_oracle_forward
  * with the same C).  dstate_T may be NULL (zero cotangent).  dq/dk are the sums over
- * the H_v/H_k value heads that share a key head, taken in ascending h_v order.
+ * the units that share a key head and a q/k sequence: the rep value sequences in
+ * ascending order, and within each the H_v/H_k value heads in ascending h_v order.
  * Returns 0 on success. */
 int gdn_oracle_backward(const gdn_oracle_dims* d, int mode, const double* q, const double* k,
                         const double* v, const double* g, const double* beta,
@@ -393,7 +408,8 @@ int gdn_oracle_backward(const gdn_oracle_dims* d, int mode, const double* q, con
                         const double* dstate_T, double* dq, double* dk, double* dv,
                         double* dg, double* dbeta, double* dstate0)
 {
-    if (!d || d->H_k <= 0 || d->H_v % d->H_k != 0 || d->C <= 0 || d->T < 0 || d->N < 0)
+    if (!d || d->H_k <= 0 || d->H_v % d->H_k != 0 || d->C <= 0 || d->T < 0 || d->N < 0 ||
+        d->rep < 1 || d->N % d->rep != 0)
         return 1;
     if ((mode == 0 && !state0) || (mode == 1 && !ckpt) || (mode != 0 && mode != 1)) return 2;
     const int64_t N = d->N, T = d->T, H_k = d->H_k, H_v = d->H_v, S_k = d->S_k;
@@ -405,19 +421,23 @@ int gdn_oracle_backward(const gdn_oracle_dims* d, int mode, const double* q, con
     for (int64_t uidx = 0; uidx < units; ++uidx)
         backward_unit(d, mode, uidx / H_v, uidx % H_v, q, k, v, g, beta, state0, ckpt, gy,
                       dstate_T, dqh, dkh, dv, dg, dbeta, dstate0);
-    /* Fold the value heads onto their key head, ascending h_v. */
-    for (int64_t n = 0; n < N; ++n)
+    /* Fold the units onto their q/k sequence and key head: ascending value sequence, then
+     * ascending h_v. */
+    for (int64_t nq = 0; nq < N / d->rep; ++nq)
         for (int64_t t = 0; t < T; ++t)
             for (int64_t hk = 0; hk < H_k; ++hk)
                 for (int64_t i = 0; i < S_k; ++i) {
                     double sq = 0.0, sk = 0.0;
-                    for (int64_t hv = 0; hv < H_v; ++hv) {
-                        if (key_head(d, hv) != hk) continue;
-                        sq += dqh[((n * T + t) * H_v + hv) * S_k + i];
-                        sk += dkh[((n * T + t) * H_v + hv) * S_k + i];
+                    for (int64_t n = 0; n < N; ++n) {
+                        if (key_seq(d, n) != nq) continue;
+                        for (int64_t hv = 0; hv < H_v; ++hv) {
+                            if (key_head(d, hv) != hk) continue;
+                            sq += dqh[((n * T + t) * H_v + hv) * S_k + i];
+                            sk += dkh[((n * T + t) * H_v + hv) * S_k + i];
+                        }
                     }
-                    dq[((n * T + t) * H_k + hk) * S_k + i] = sq;
-                    dk[((n * T + t) * H_k + hk) * S_k + i] = sk;
+                    dq[((nq * T + t) * H_k + hk) * S_k + i] = sq;
+                    dk[((nq * T + t) * H_k + hk) * S_k + i] = sk;
                 }
     free(dkh);
     free(dqh);

@@ -257,6 +257,28 @@ def pin_broadcast(lib, kda, seed=10):
     return dev < 1e-12, f"max dev {dev:.2e}"
 
 
+def pin_seq_broadcast(lib, kda, seed=13):
+    """Sequence broadcast (PR #16 "iv3/rq3"): value sequence n reads q/k sequence n / rep.
+    It must equal the same problem with q, k repeated per value sequence (np.repeat: rows
+    0, 0, 1, 1, ...), with dq/dk summed over each group of rep sequences."""
+    rep_, N = 2, 4
+    x = _as64(synth.make_problem(N, 7, 1, 2, 8, kda=kda, seed=seed, dstate_T=True, seq_rep=rep_))
+    r = dict(x)
+    r["q"] = np.repeat(x["q"], rep_, axis=0)
+    r["k"] = np.repeat(x["k"], rep_, axis=0)
+    yb, sb, _ = _fwd(lib, x, C=3)
+    yr, sr, _ = _fwd(lib, r, C=3)
+    gb = _bwd(lib, x, C=3)
+    gr = _bwd(lib, r, C=3)
+    dev = max(float(np.max(np.abs(yb - yr))), float(np.max(np.abs(sb - sr))))
+    for n in ("dq", "dk"):
+        acc = gr[n][0::rep_] + gr[n][1::rep_]  # ascending value sequence within each group
+        dev = max(dev, float(np.max(np.abs(acc - gb[n]))))
+    for n in ("dv", "dg", "dbeta", "dstate0"):
+        dev = max(dev, float(np.max(np.abs(gb[n] - gr[n]))))
+    return dev < 1e-12, f"max dev {dev:.2e}"
+
+
 def pin_ckpt_exact(lib, kda, seed=12, T=13):
     x = _as64(synth.make_problem(2, T, 1, 2, 8, kda=kda, seed=seed, dstate_T=True))
     ref = _bwd(lib, x, mode="store_all", C=1)
@@ -280,6 +302,7 @@ def battery(lib, quick=False):
         res[f"homogeneity_{tag}"] = pin_homogeneity(lib, kda)
         res[f"euler_{tag}"] = pin_euler(lib, kda)
         res[f"broadcast_{tag}"] = pin_broadcast(lib, kda)
+        res[f"seq_broadcast_{tag}"] = pin_seq_broadcast(lib, kda)
         res[f"ckpt_exact_{tag}"] = pin_ckpt_exact(lib, kda)
     res["kda_equal"] = pin_kda_equal(lib)
     return res

@@ -31,7 +31,7 @@ def test_symbolic_exact_gradients(lib, kda):
 
 @pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
 @pytest.mark.parametrize("pin", ["beta0", "reset", "exact_write", "homogeneity", "euler",
-                                 "broadcast", "ckpt_exact"])
+                                 "broadcast", "seq_broadcast", "ckpt_exact"])
 def test_invariant(lib, pin, kda):
     ok, detail = getattr(P, "pin_" + pin)(lib, kda)
     assert ok, detail
@@ -101,6 +101,7 @@ def test_default_checkpoint_interval():
     (4, "scale dropped from dq"),
     (5, "h_v / r head mapping"),
     (6, "gy ignored"),
+    (7, "interleaved q/k sequence mapping"),
 ])
 def test_planted_defect_is_caught(mutation, expect):
     mlib = oracle.load(mutation=mutation)
