@@ -47,6 +47,7 @@ int64_t ceil_sqrt(int64_t T)
 struct Plan {
     int D = 0, RT = 1, W = 4, R = 16, P = 1, tc = 32, c2 = 1, nsub_max = 1;
     int SK = 0, DV = 0;  // the state's columns (key head size) and rows (value head size)
+    int rep = 1;         // value sequences per q/k sequence
     bool kda = false;
     bool chunked = false;
     int64_t C = 1, n_ck = 0;
@@ -57,7 +58,7 @@ struct Plan {
     long long o_T = 0, o_QKD = 0, o_QDT = 0, o_gam = 0, o_r = 0, o_W = 0, o_U = 0, o_Mc = 0, o_dM = 0,
               o_dDel = 0, o_dX = 0, o_Tr = 0, o_Z = 0, o_KK = 0, o_QK = 0, o_Dm = 0, o_W1 = 0, o_Q1 = 0, o_B23 = 0, o_DK = 0, o_DS = 0,
               o_dqM = 0, o_dkM = 0, o_carry = 0, o_carry_b = 0, o_gL = 0, o_KG = 0, o_KRT = 0, o_kGam = 0,
-              o_kR = 0;
+              o_kR = 0, o_dqS = 0, o_dkS = 0;
     bool tensor = false;  // head size 128: the state chain runs on the tensor cores
     size_t fwd_ws_bytes = 0, bwd_ws_bytes = 0;
 };
@@ -67,7 +68,10 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 gdn_status_t check_sizes(const gdn_params_t* p)
 {
     if (!p) return fail(GDN_ERR_INVALID_ARG, "params is NULL");
-    if (p->reserved1 != 0.0f) return fail(GDN_ERR_INVALID_ARG, "reserved fields must be zero");
+    if (p->seq_rep < 0) return fail(GDN_ERR_INVALID_ARG, "negative seq_rep");
+    if (p->n_seq % (p->seq_rep > 1 ? p->seq_rep : 1) != 0)
+        return fail(GDN_ERR_INVALID_ARG, "n_seq (%lld) is not a multiple of seq_rep (%d)", (long long)p->n_seq,
+                    (int)p->seq_rep);
     if (p->in_dtype != GDN_F32 && p->in_dtype != GDN_BF16 && p->in_dtype != GDN_F16)
         return fail(GDN_ERR_INVALID_ARG, "unknown input dtype %d", (int)p->in_dtype);
     if (p->n_seq < 0 || p->T < 0) return fail(GDN_ERR_INVALID_ARG, "negative n_seq or T");
@@ -99,6 +103,7 @@ Plan make_plan(const gdn_params_t* p)
     pl.SK = (int)p->S_k;
     pl.DV = (int)p->S_v;
     pl.D = pl.SK < 32 ? 32 : pl.SK;
+    pl.rep = p->seq_rep > 1 ? p->seq_rep : 1;
     pl.kda = p->gate == GDN_GATE_KDA;
     pl.C = p->C > 0 ? p->C : ceil_sqrt(p->T);
     if (pl.C > INT_MAX / 2) pl.C = INT_MAX / 2;
@@ -206,6 +211,9 @@ Plan make_plan(const gdn_params_t* p)
                 pl.o_kGam = o; o += al(CH * BC * D);
                 pl.o_kR = o;   o += al(CH * BC * D);
             }
+        } else if (pl.rep > 1) {  // each value sequence's dq, dk before the sequence sums
+            pl.o_dqS = o; o += al(p->n_seq * p->T * p->H_k * D);
+            pl.o_dkS = o; o += al(p->n_seq * p->T * p->H_k * D);
         }
         pl.bwd_ws_bytes = (size_t)o * 4;
         pl.ws_bytes = pl.bwd_ws_bytes;
@@ -245,9 +253,10 @@ Wide wide_layout(const gdn_params_t* p, bool backward)
     if (p->in_dtype == GDN_F32) return w;
     const size_t N = (size_t)p->n_seq, T = (size_t)p->T, Hk = (size_t)p->H_k, Hv = (size_t)p->H_v;
     const size_t Sk = (size_t)p->S_k, Sv = (size_t)p->S_v, gw = p->gate == GDN_GATE_KDA ? Sk : 1;
+    const size_t Nq = (size_t)p->n_seq / (size_t)(p->seq_rep > 1 ? p->seq_rep : 1);
     size_t o = 0;
-    w.q = o; o += align256(N * T * Hk * Sk * 4);
-    w.k = o; o += align256(N * T * Hk * Sk * 4);
+    w.q = o; o += align256(Nq * T * Hk * Sk * 4);
+    w.k = o; o += align256(Nq * T * Hk * Sk * 4);
     w.v = o; o += align256(N * T * Hv * Sv * 4);
     w.g = o; o += align256(N * T * Hv * gw * 4);
     w.b = o; o += align256(N * T * Hv * 4);
@@ -281,13 +290,16 @@ bool vec_ok(const void* ptr, const int64_t s[3])
     return aligned(ptr, 16) && s[0] % 4 == 0 && s[1] % 4 == 0 && s[2] % 4 == 0;
 }
 
+// The q/k sequences: n_seq / seq_rep (the sequence broadcast), else n_seq.
+int64_t qk_seqs(const gdn_params_t* p) { return p->n_seq / (p->seq_rep > 1 ? p->seq_rep : 1); }
+
 void packed_offsets(const gdn_params_t* p, size_t off[7])
 {
     const size_t N = (size_t)p->n_seq, T = (size_t)p->T, Hk = (size_t)p->H_k, Hv = (size_t)p->H_v;
-    const size_t Sk = (size_t)p->S_k, Sv = (size_t)p->S_v;
+    const size_t Sk = (size_t)p->S_k, Sv = (size_t)p->S_v, Nq = (size_t)qk_seqs(p);
     off[0] = 0;
-    off[1] = off[0] + N * T * Hk * Sk;
-    off[2] = off[1] + N * T * Hk * Sk;
+    off[1] = off[0] + Nq * T * Hk * Sk;
+    off[2] = off[1] + Nq * T * Hk * Sk;
     off[3] = off[2] + N * T * Hv * Sv;
     off[4] = off[3] + N * T * Hv * (p->gate == GDN_GATE_KDA ? Sk : 1);
     off[5] = off[4] + N * T * Hv;
@@ -315,7 +327,9 @@ void fill_chunk_common(gdn::ChunkArgs& c, const gdn_params_t* p, const Plan& pl)
     c.o_W1 = pl.o_W1; c.o_Q1 = pl.o_Q1; c.o_B23 = pl.o_B23; c.o_DK = pl.o_DK; c.o_DS = pl.o_DS;
     c.o_dqM = pl.o_dqM; c.o_dkM = pl.o_dkM;
     c.o_gL = pl.o_gL; c.o_KG = pl.o_KG; c.o_KRT = pl.o_KRT; c.o_kGam = pl.o_kGam; c.o_kR = pl.o_kR;
+    c.o_dqS = pl.o_dqS; c.o_dkS = pl.o_dkS;
     c.kda = pl.kda;
+    c.rep = pl.rep;
     c.want_tc = pl.tensor;
     c.c_lo = 0;
     c.c_hi = (int)pl.n_chunks;
@@ -555,7 +569,7 @@ int gdn_backward_launches(const gdn_params_t* p)
     // chunked: prep, [recompute], dM chain, gradients.  On the tensor-core path, per chunk
     // range: prep, dM chain, a gradient launch per place in a segment, and the sum over value
     // heads (a call with timing events runs the same kernels as one range).
-    if (pl.chunked) return pl.tensor ? tc_backward_launches(pl) : (pl.cps > 1 ? 4 : 3);
+    if (pl.chunked) return pl.tensor ? tc_backward_launches(pl) : (pl.cps > 1 ? 4 : 3) + (pl.rep > 1 ? 1 : 0);
     return p->T > 0 ? 2 : 1;
 }
 
@@ -611,11 +625,11 @@ namespace {
 
 // Widens one 16-bit input [N][T][H][D] (element strides s, last dim contiguous) into its
 // dense fp32 copy.
-gdn_status_t widen_one(const gdn_params_t* p, const void* src, const int64_t s[3], int64_t H, int64_t D, float* dst,
-                       void* stream)
+gdn_status_t widen_one(const gdn_params_t* p, const void* src, const int64_t s[3], int64_t N, int64_t H, int64_t D,
+                       float* dst, void* stream)
 {
     const long long ss[3] = {(long long)s[0], (long long)s[1], (long long)s[2]};
-    return cuda_status(gdn::launch_widen(src, p->in_dtype, ss, (int)p->n_seq, (int)p->T, (int)H, (int)D, dst, stream),
+    return cuda_status(gdn::launch_widen(src, p->in_dtype, ss, (int)N, (int)p->T, (int)H, (int)D, dst, stream),
                        "widening launch");
 }
 
@@ -626,7 +640,7 @@ gdn_status_t check_16bit_inputs(const gdn_params_t* p, const void* const* in, in
     const int64_t gw = p->gate == GDN_GATE_KDA ? Sk : 1;
     for (int i = 0; i < n_in; ++i)
         if (!aligned(in[i], 2)) return fail(GDN_ERR_INVALID_ARG, "16-bit input not 2-byte aligned");
-    const Range r[6] = {extent4(in[0], N, T, Hk, Sk, p->q_s, 2), extent4(in[1], N, T, Hk, Sk, p->k_s, 2),
+    const Range r[6] = {extent4(in[0], qk_seqs(p), T, Hk, Sk, p->q_s, 2), extent4(in[1], qk_seqs(p), T, Hk, Sk, p->k_s, 2),
                         extent4(in[2], N, T, Hv, Sv, p->v_s, 2), extent_dense(in[3], (size_t)(N * T * Hv * gw), 2),
                         extent_dense(in[4], (size_t)(N * T * Hv), 2),
                         n_in > 5 ? extent4(in[5], N, T, Hv, Sv, p->gy_s, 2) : Range{0, 0}};
@@ -672,11 +686,11 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const void* q, const void* k, co
             const int64_t gs[3] = {T * Hv * (p->gate == GDN_GATE_KDA ? Sk : 1), Hv * (p->gate == GDN_GATE_KDA ? Sk : 1),
                                    p->gate == GDN_GATE_KDA ? Sk : 1};
             const int64_t bs[3] = {T * Hv, Hv, 1};
-            if ((st = widen_one(p, q, p->q_s, p->H_k, Sk, wq, stream)) != GDN_OK) return st;
-            if ((st = widen_one(p, k, p->k_s, p->H_k, Sk, wk, stream)) != GDN_OK) return st;
-            if ((st = widen_one(p, v, p->v_s, Hv, Sv, wv, stream)) != GDN_OK) return st;
-            if ((st = widen_one(p, g, gs, Hv, gs[2], wg, stream)) != GDN_OK) return st;
-            if ((st = widen_one(p, beta, bs, Hv, 1, wb, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, q, p->q_s, qk_seqs(p), p->H_k, Sk, wq, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, k, p->k_s, qk_seqs(p), p->H_k, Sk, wk, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, v, p->v_s, p->n_seq, Hv, Sv, wv, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, g, gs, p->n_seq, Hv, gs[2], wg, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, beta, bs, p->n_seq, Hv, 1, wb, stream)) != GDN_OK) return st;
         }
         return gdn_forward(&p32, wq, wk, wv, wg, wb, state0, y, state_T, ckpt, ws + w.total, workspace_bytes - w.total,
                            stream);
@@ -696,7 +710,7 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const void* q, const void* k, co
         return fail(GDN_ERR_INVALID_ARG, "state0, state_T and ckpt must be 16-byte aligned");
 
     const int64_t gw = pl.kda ? D : 1;
-    const Range rq = extent4(q, N, T, Hk, D, p->q_s), rk = extent4(k, N, T, Hk, D, p->k_s);
+    const Range rq = extent4(q, qk_seqs(p), T, Hk, D, p->q_s), rk = extent4(k, qk_seqs(p), T, Hk, D, p->k_s);
     const Range rv = extent4(v, N, T, Hv, DV, p->v_s);
     const Range rg = extent_dense(g, (size_t)(N * T * Hv * gw));
     const Range rb = extent_dense(beta, (size_t)(N * T * Hv));
@@ -742,7 +756,7 @@ gdn_status_t gdn_forward(const gdn_params_t* p, const void* q, const void* k, co
     a.vs0 = p->v_s[0]; a.vs1 = p->v_s[1]; a.vs2 = p->v_s[2];
     a.N = (int)N; a.T = (int)T; a.H_k = (int)Hk; a.H_v = (int)Hv;
     a.C = (int)pl.C; a.n_ck = (int)pl.n_ck; a.scale = p->scale; a.tc = pl.tc;
-    a.SK = pl.SK; a.DV = pl.DV;
+    a.SK = pl.SK; a.DV = pl.DV; a.rep = pl.rep;
     a.vec_q = vec_ok(q, p->q_s); a.vec_k = vec_ok(k, p->k_s); a.vec_v = vec_ok(v, p->v_s);
     a.vec_g = aligned(g, 16);
     tap.mark(stream);
@@ -783,12 +797,12 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k, c
             const int64_t gw = p->gate == GDN_GATE_KDA ? Sk : 1;
             const int64_t gs[3] = {T * Hv * gw, Hv * gw, gw};
             const int64_t bs[3] = {T * Hv, Hv, 1};
-            if ((st = widen_one(p, q, p->q_s, p->H_k, Sk, wq, stream)) != GDN_OK) return st;
-            if ((st = widen_one(p, k, p->k_s, p->H_k, Sk, wk, stream)) != GDN_OK) return st;
-            if ((st = widen_one(p, v, p->v_s, Hv, Sv, wv, stream)) != GDN_OK) return st;
-            if ((st = widen_one(p, g, gs, Hv, gw, wg, stream)) != GDN_OK) return st;
-            if ((st = widen_one(p, beta, bs, Hv, 1, wb, stream)) != GDN_OK) return st;
-            if ((st = widen_one(p, gy, p->gy_s, Hv, Sv, wgy, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, q, p->q_s, qk_seqs(p), p->H_k, Sk, wq, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, k, p->k_s, qk_seqs(p), p->H_k, Sk, wk, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, v, p->v_s, p->n_seq, Hv, Sv, wv, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, g, gs, p->n_seq, Hv, gw, wg, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, beta, bs, p->n_seq, Hv, 1, wb, stream)) != GDN_OK) return st;
+            if ((st = widen_one(p, gy, p->gy_s, p->n_seq, Hv, Sv, wgy, stream)) != GDN_OK) return st;
         }
         return gdn_backward(&p32, wq, wk, wv, wg, wb, ckpt, wgy, dstate_T, packed, ws + w.total,
                             workspace_bytes - w.total, stream);
@@ -814,7 +828,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k, c
     size_t off[7];
     packed_offsets(p, off);
     const int64_t gw = pl.kda ? D : 1;
-    const Range rq = extent4(q, N, T, Hk, D, p->q_s), rk = extent4(k, N, T, Hk, D, p->k_s);
+    const Range rq = extent4(q, qk_seqs(p), T, Hk, D, p->q_s), rk = extent4(k, qk_seqs(p), T, Hk, D, p->k_s);
     const Range rv = extent4(v, N, T, Hv, DV, p->v_s), rgy = extent4(gy, N, T, Hv, DV, p->gy_s);
     const Range rg = extent_dense(g, (size_t)(N * T * Hv * gw));
     const Range rb = extent_dense(beta, (size_t)(N * T * Hv));
@@ -862,7 +876,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k, c
     a.gys0 = p->gy_s[0]; a.gys1 = p->gy_s[1]; a.gys2 = p->gy_s[2];
     a.N = (int)N; a.T = (int)T; a.H_k = (int)Hk; a.H_v = (int)Hv;
     a.C = (int)pl.C; a.n_ck = (int)pl.n_ck; a.c2 = pl.c2; a.nsub_max = pl.nsub_max;
-    a.SK = pl.SK; a.DV = pl.DV;
+    a.SK = pl.SK; a.DV = pl.DV; a.rep = pl.rep;
     a.scale = p->scale;
     a.vec_q = vec_ok(q, p->q_s); a.vec_k = vec_ok(k, p->k_s); a.vec_v = vec_ok(v, p->v_s);
     a.vec_gy = vec_ok(gy, p->gy_s); a.vec_g = aligned(g, 16);
@@ -877,6 +891,7 @@ gdn_status_t gdn_backward(const gdn_params_t* p, const void* q, const void* k, c
     r.dq = packed + off[0]; r.dk = packed + off[1]; r.dg = packed + off[3]; r.dbeta = packed + off[4];
     r.N = (int)N; r.T = (int)T; r.H_k = (int)Hk; r.H_v = (int)Hv; r.D = pl.D; r.P = pl.P;
     r.SK = pl.SK;
+    r.rep = pl.rep;
     r.NQ = pl.kda ? 3 : 2; r.kda = pl.kda;
     st = cuda_status(gdn::launch_reduce(r, stream), "reduce launch");
     tap.mark(stream);

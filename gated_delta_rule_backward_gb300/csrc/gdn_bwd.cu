@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(256, 1) gdn_bwd_kernel(const BwdArgs A)
     // Stage the inputs of tokens [ta, ta + nt) in shared memory.
     auto load_tile = [&](int ta, int nt, bool for_walk) {
         const long long tok0 = (long long)n * A.T + ta;
-        load_rows(sk, A.k + n * A.ks0 + (long long)ta * A.ks1 + hk * A.ks2, A.ks1, nt, SK,
+        load_rows(sk, A.k + (long long)(n / A.rep) * A.ks0 + (long long)ta * A.ks1 + hk * A.ks2, A.ks1, nt, SK,
                   A.vec_k, tid, NT, D);
         if (KDA) {
             load_rows_exp(sa, A.g + (tok0 * A.H_v + h) * SK, (long long)A.H_v * SK, nt, SK,
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(256, 1) gdn_bwd_kernel(const BwdArgs A)
         load_rows(sv, A.v + n * A.vs0 + (long long)ta * A.vs1 + h * A.vs2 + p * R, A.vs1, nt, R,
                   A.vec_v, tid, NT);
         if (for_walk) {
-            load_rows(sq, A.q + n * A.qs0 + (long long)ta * A.qs1 + hk * A.qs2, A.qs1, nt, SK,
+            load_rows(sq, A.q + (long long)(n / A.rep) * A.qs0 + (long long)ta * A.qs1 + hk * A.qs2, A.qs1, nt, SK,
                       A.vec_q, tid, NT, D);
             load_rows(sgy, A.gy + n * A.gys0 + (long long)ta * A.gys1 + h * A.gys2 + p * R,
                       A.gys1, nt, R, A.vec_gy, tid, NT);
@@ -354,10 +354,12 @@ __global__ void __launch_bounds__(256, 1) gdn_bwd_kernel(const BwdArgs A)
 // Fixed-order sums of the per-CTA partials: dq/dk over the value heads h_k, h_k + H_k,
 // ... (ascending) and, inside each, over the P row blocks; dg (KDA), dbeta and dg
 // (scalar gate) over the row blocks.
-// The partials are D wide (the kernels' column width); the outputs SK wide (S_k).
+// The partials are D wide (the kernels' column width); the outputs SK wide (S_k).  With the
+// sequence broadcast, dq/dk of q/k sequence nq sum the value sequences nq rep .. nq rep +
+// rep - 1 in ascending order, each as above.
 __global__ void __launch_bounds__(256) gdn_reduce_kernel(const ReduceArgs A)
 {
-    const long long nqk = (long long)A.N * A.T * A.H_k * A.SK;
+    const long long nqk = (long long)(A.N / A.rep) * A.T * A.H_k * A.SK;
     const long long nhv = (long long)A.N * A.T * A.H_v;
     const long long ndg = A.kda ? nhv * A.SK : 0;
     const long long total = 2 * nqk + ndg + nhv;
@@ -371,16 +373,21 @@ __global__ void __launch_bounds__(256) gdn_reduce_kernel(const ReduceArgs A)
             const int i = (int)(e % A.SK);
             const long long tokhk = e / A.SK;  // (n*T + t)*H_k + hk
             const int hkk = (int)(tokhk % A.H_k);
-            const long long tok = tokhk / A.H_k;
+            const long long tokq = tokhk / A.H_k;  // nq*T + t
+            const long long nq = tokq / A.T, t = tokq - nq * A.T;
             // per value head: the sum over its P row blocks; then the value heads in
-            // ascending order (equal, bit for bit, to summing explicitly replicated heads)
+            // ascending order (equal, bit for bit, to summing explicitly replicated heads),
+            // and the value sequences of the q/k sequence in ascending order
             float acc = 0.f;
-            for (int rho = 0; rho < r; ++rho) {
-                const float* src = A.ws_col + ((tok * A.H_v + hkk + rho * A.H_k) * A.P) * ncol +
-                                   which * A.D + i;
-                float part = 0.f;
-                for (int pp = 0; pp < A.P; ++pp) part = __fadd_rn(part, src[(long long)pp * ncol]);
-                acc = __fadd_rn(acc, part);
+            for (int j = 0; j < A.rep; ++j) {
+                const long long tok = (nq * A.rep + j) * A.T + t;
+                for (int rho = 0; rho < r; ++rho) {
+                    const float* src = A.ws_col + ((tok * A.H_v + hkk + rho * A.H_k) * A.P) * ncol +
+                                       which * A.D + i;
+                    float part = 0.f;
+                    for (int pp = 0; pp < A.P; ++pp) part = __fadd_rn(part, src[(long long)pp * ncol]);
+                    acc = __fadd_rn(acc, part);
+                }
             }
             (which ? A.dk : A.dq)[e] = acc;
         } else if (idx < 2 * nqk + ndg) {
@@ -439,7 +446,7 @@ int launch_backward(const BwdArgs& a, int D, int RT, int W, bool kda, void* stre
 
 int launch_reduce(const ReduceArgs& a, void* stream)
 {
-    const long long nqk = (long long)a.N * a.T * a.H_k * a.SK;
+    const long long nqk = (long long)(a.N / a.rep) * a.T * a.H_k * a.SK;
     const long long nhv = (long long)a.N * a.T * a.H_v;
     const long long total = 2 * nqk + (a.kda ? nhv * a.SK : 0) + nhv;
     if (total == 0) return 0;

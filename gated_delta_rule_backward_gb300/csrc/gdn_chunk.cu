@@ -546,8 +546,8 @@ __global__ void __launch_bounds__(CT) gdn_chunk_prep_kernel(const ChunkArgs A)
     float* vec = Ts + BC * LDB;       // gs, bs, Gs, gam
     float *gs = vec, *bs = vec + BC, *Gs = vec + 2 * BC, *gam = vec + 3 * BC;
 
-    const long long tq = (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
-    const long long tk = (long long)n * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
+    const long long tq = (long long)(n / A.rep) * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
+    const long long tk = (long long)(n / A.rep) * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
     {  // every load in flight before the first store
         float4 rq[D / 32], rk[D / 32], rv[D / 32];
         pf_rows<D>(rq, A.q + tq, A.qs1, cp.nb, A.vec_q, tid);
@@ -707,10 +707,10 @@ __global__ void __launch_bounds__(CT) gdn_chunk_state_kernel(const ChunkArgs A)
         const float* w = A.ws + A.o_W + ch * (BC * D);
 #pragma unroll
         for (int kk = 0; kk < NF; ++kk) pw[kk] = __ldg(reinterpret_cast<const float4*>(w) + tid + CT * kk);
-        const long long tk = (long long)n * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
+        const long long tk = (long long)(n / A.rep) * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
         pf_rows<D>(pk, A.k + tk, A.ks1, cp.nb, A.vec_k, tid);
         if (FWD) {
-            const long long tq = (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
+            const long long tq = (long long)(n / A.rep) * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
             pf_rows<D>(pq, A.q + tq, A.qs1, cp.nb, A.vec_q, tid);
             pqd = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_QKD + ch * (BC * BC)) + tid);
         }
@@ -874,8 +874,8 @@ __global__ void __launch_bounds__(CT) gdn_chunk_dstate_kernel(const ChunkArgs A)
     auto issue = [&](int c) {
         const ChunkPos cp = chunk_pos(A, c);
         const long long ch = head * A.n_chunks + c;
-        const long long tk = (long long)n * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
-        const long long tq = (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
+        const long long tk = (long long)(n / A.rep) * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
+        const long long tq = (long long)(n / A.rep) * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
         pf_rows<D>(pk, A.k + tk, A.ks1, cp.nb, A.vec_k, tid);
         pf_rows<D>(pq, A.q + tq, A.qs1, cp.nb, A.vec_q, tid);
         {  // dY rows t, own columns: float4 index tid -> (t, j4), RR/4 float4 per row
@@ -1029,8 +1029,8 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
     float* red = vec + 8 * BC;        // CT/32 partials
 
     {
-        const long long tq = (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
-        const long long tk = (long long)n * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
+        const long long tq = (long long)(n / A.rep) * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
+        const long long tk = (long long)(n / A.rep) * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
         load_rows_pad(QKs, ld, A.q + tq, A.qs1, cp.nb, D, A.vec_q, tid);
         load_rows_pad(Ks, ld, A.k + tk, A.ks1, cp.nb, D, A.vec_k, tid);
     }
@@ -1537,6 +1537,25 @@ static int chunk_forward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
     return 0;
 }
 
+// The sequence broadcast at head sizes 32, 64: dq, dk of q/k sequence nq are the sums of the
+// gradient kernel's per-value-sequence parts over sequences nq rep .. nq rep + rep - 1, in
+// ascending order.  per = T H_k D floats per sequence.
+__global__ void __launch_bounds__(256) gdn_seq_sum_kernel(const float* dqS, const float* dkS, float* dq, float* dk,
+                                                          long long per, int nq_count, int rep)
+{
+    const long long total = 2LL * nq_count * per;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int which = idx >= total / 2;
+        const long long e = idx - which * (total / 2);
+        const long long nq = e / per, o = e - nq * per;
+        const float* src = (which ? dkS : dqS) + nq * rep * per + o;
+        float acc = 0.f;
+        for (int j = 0; j < rep; ++j) acc = __fadd_rn(acc, src[(long long)j * per]);
+        (which ? dk : dq)[e] = acc;
+    }
+}
+
 template <int D>
 static int chunk_backward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
 {
@@ -1549,7 +1568,30 @@ static int chunk_backward_t(const ChunkArgs& a, cudaStream_t s, EventTap& tap)
         GDN_LAUNCH((gdn_chunk_state_kernel<D, false>), dim3(Rows<D>::P, a.n_ck, a.N * a.H_v),
                    state_smem<D>());
     GDN_LAUNCH(gdn_chunk_dstate_kernel<D>, dim3(Rows<D>::P, a.H_v, a.N), dstate_smem<D>());
-    GDN_LAUNCH(gdn_chunk_grad_kernel<D>, dim3(a.n_chunks, a.H_k, a.N), grad_smem<D>());
+    if (a.rep <= 1) {
+        GDN_LAUNCH(gdn_chunk_grad_kernel<D>, dim3(a.n_chunks, a.H_k, a.N), grad_smem<D>());
+        return 0;
+    }
+    {  // sequence broadcast: each value sequence's dq, dk into the workspace, then their sums
+        ChunkArgs g = a;
+        g.dq = a.ws + a.o_dqS;
+        g.dk = a.ws + a.o_dkS;
+        int e = set_smem(gdn_chunk_grad_kernel<D>, grad_smem<D>());
+        if (e) return e;
+        gdn_chunk_grad_kernel<D><<<dim3(a.n_chunks, a.H_k, a.N), CT, grad_smem<D>(), s>>>(g);
+        e = (int)cudaGetLastError();
+        if (e) return e;
+        tap.mark(s);
+        const long long per = (long long)a.T * a.H_k * D;
+        const int nq = a.N / a.rep;
+        long long blocks = (2LL * nq * per + 255) / 256;
+        if (blocks > 152LL * 16) blocks = 152LL * 16;
+        if (blocks > 0)
+            gdn_seq_sum_kernel<<<(unsigned)blocks, 256, 0, s>>>(g.dq, g.dk, a.dq, a.dk, per, nq, a.rep);
+        e = (int)cudaGetLastError();
+        if (e) return e;
+        tap.mark(s);
+    }
     return 0;
 }
 #undef GDN_LAUNCH

@@ -56,9 +56,9 @@ __global__ void __launch_bounds__(128, D <= 128 ? 3 : 1) gdn_fwd_kernel(const Fw
     for (int t0 = 0; t0 < A.T; t0 += tc) {
         const int nt = min(tc, A.T - t0);
         __syncthreads();
-        load_rows<4>(sk, A.k + n * A.ks0 + (long long)t0 * A.ks1 + hk * A.ks2, A.ks1, nt, SK,
+        load_rows<4>(sk, A.k + (long long)(n / A.rep) * A.ks0 + (long long)t0 * A.ks1 + hk * A.ks2, A.ks1, nt, SK,
                   A.vec_k, tid, NT, D);
-        load_rows<4>(sq, A.q + n * A.qs0 + (long long)t0 * A.qs1 + hk * A.qs2, A.qs1, nt, SK,
+        load_rows<4>(sq, A.q + (long long)(n / A.rep) * A.qs0 + (long long)t0 * A.qs1 + hk * A.qs2, A.qs1, nt, SK,
                   A.vec_q, tid, NT, D);
         const long long tok0 = (long long)n * A.T + t0;
         if (KDA) {

@@ -37,6 +37,7 @@ struct FwdArgs {
     long long qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2;
     int N, T, H_k, H_v, C, n_ck;
     int SK, DV;  // key head size (the state's columns) and value head size (its rows)
+    int rep;     // value sequences per q/k sequence: q, k of sequence n are those of n / rep
     float scale;
     int tc;  // tokens per shared-memory tile
     int vec_q, vec_k, vec_v, vec_g;
@@ -59,6 +60,7 @@ struct BwdArgs {
     long long qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2, gys0, gys1, gys2;
     int N, T, H_k, H_v, C, n_ck, c2, nsub_max;
     int SK, DV;  // key head size (the state's columns) and value head size (its rows)
+    int rep;     // value sequences per q/k sequence: q, k of sequence n are those of n / rep
     float scale;
     int vec_q, vec_k, vec_v, vec_gy, vec_g, vec_ds0;
 };
@@ -72,6 +74,7 @@ struct ReduceArgs {
     float* dbeta;
     int N, T, H_k, H_v, D, P, NQ, kda;
     int SK;  // output column width (S_k); the partials are D wide
+    int rep; // value sequences per q/k sequence: dq, dk sum over each group of rep
 };
 
 // Chunked (WY) form, scalar gate: chunk length and the arguments of its kernels.
@@ -99,6 +102,7 @@ struct ChunkArgs {
     float* ws;              // workspace base
     long long qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2, gys0, gys1, gys2;
     int N, T, H_k, H_v, C, n_ck, cps, n_chunks;
+    int rep;                // value sequences per q/k sequence (q, k of n are those of n / rep)
     float scale;
     // workspace sub-arrays (float offsets from ws), per (sequence, value head, chunk)
     long long o_T, o_QKD, o_QDT, o_gam, o_r, o_W, o_U, o_Mc, o_dM, o_dDel, o_dX;
@@ -110,6 +114,9 @@ struct ChunkArgs {
     // (128 floats), the bf16 hi/lo tiles K (.) gamma (rows t) and (K (.) R)^T (rows i), and
     // gamma, R in fp32 (rows t)
     long long o_gL, o_KG, o_KRT, o_kGam, o_kR;
+    // sequence broadcast at head sizes 32, 64: each value sequence's dq, dk [N][T][H_k][D]
+    // before the sum over the sequences that share q, k
+    long long o_dqS, o_dkS;
     int kda;
     int want_wu;
     int want_factors;

@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(CT, 2) gdn_kda_prep_kernel(const ChunkArgs A)
     float* Ts = Zs + BC * LDB;
     float* bs = Ts + BC * LDB;      // beta (BC)
 
-    const long long tq = (long long)n * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
-    const long long tk = (long long)n * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
+    const long long tq = (long long)(n / A.rep) * A.qs0 + (long long)cp.t0 * A.qs1 + (long long)hk * A.qs2;
+    const long long tk = (long long)(n / A.rep) * A.ks0 + (long long)cp.t0 * A.ks1 + (long long)hk * A.ks2;
     const long long tok0 = (long long)n * A.T + cp.t0;
     {  // every load in flight before the first store; g rows are [token][value head][d]
         float4 rq[D / 32], rk[D / 32], rv[D / 32], rg[D / 32];

@@ -216,8 +216,8 @@ __device__ __forceinline__ bool kda_tail(const ChunkArgs& A, float* sm, uint32_t
             sK[idx] = 0.f;
             sA[idx] = 0.f;
         } else if (!rows_bulk) {
-            sQ[idx] = __ldg(A.q + (long long)n * A.qs0 + (long long)(t0 + t) * A.qs1 + (long long)hk * A.qs2 + c);
-            sK[idx] = __ldg(A.k + (long long)n * A.ks0 + (long long)(t0 + t) * A.ks1 + (long long)hk * A.ks2 + c);
+            sQ[idx] = __ldg(A.q + (long long)(n / A.rep) * A.qs0 + (long long)(t0 + t) * A.qs1 + (long long)hk * A.qs2 + c);
+            sK[idx] = __ldg(A.k + (long long)(n / A.rep) * A.ks0 + (long long)(t0 + t) * A.ks1 + (long long)hk * A.ks2 + c);
             sA[idx] = __ldg(A.g + ((tok0 + t) * A.H_v + h) * TD + c);
         }
     }
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     float* sM = sm + kR2;
     const bool m_unit = loc > 0;  // M: a parked state (unit layout) or the row-major checkpoint
     if (issuer)  // see tc::prefetch_l2 (measured 0.95 vs 1.08 ms per launch at the bench size)
-        tc::prefetch_l2(A.q + (long long)n * A.qs0 + (long long)t0 * A.qs1 + (long long)hk * A.qs2);
+        tc::prefetch_l2(A.q + (long long)(n / A.rep) * A.qs0 + (long long)t0 * A.qs1 + (long long)hk * A.qs2);
     if (warp == 8) {  // M into R2 by the bulk-copy engine: 32 padded runs, or 128 padded rows
         if (lane == 0) {
             s_armed = (1 << 0) | (1 << 3);
@@ -796,9 +796,9 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         __syncwarp();
         if (rows_bulk && lane < nb) {
             const long long t = t0 + lane;
-            tc::bulk_g2s(sm + kKq + lane * TD, A.q + (long long)n * A.qs0 + t * A.qs1 + (long long)hk * A.qs2,
+            tc::bulk_g2s(sm + kKq + lane * TD, A.q + (long long)(n / A.rep) * A.qs0 + t * A.qs1 + (long long)hk * A.qs2,
                          sizeof(float) * TD, bar_kda);
-            tc::bulk_g2s(sm + kKk + lane * TD, A.k + (long long)n * A.ks0 + t * A.ks1 + (long long)hk * A.ks2,
+            tc::bulk_g2s(sm + kKk + lane * TD, A.k + (long long)(n / A.rep) * A.ks0 + t * A.ks1 + (long long)hk * A.ks2,
                          sizeof(float) * TD, bar_kda);
             tc::bulk_g2s(sm + kKa + lane * TD, A.g + ((tok0 + lane) * A.H_v + h) * TD, sizeof(float) * TD, bar_kda);
         }
@@ -1070,10 +1070,11 @@ done:
     if (warp == 0) tc::tmem_free(tmem, kCols);
 }
 
-// dq, dk of each key head: the value heads' parts summed in ascending order.
+// dq, dk of each key head: the value heads' parts summed in ascending order (and, with the
+// sequence broadcast, the value sequences of each q/k sequence nq, ascending).
 __global__ void __launch_bounds__(256) gdn_tc_dqdk_sum_kernel(const ChunkArgs A)
 {
-    const int c = A.c_lo + blockIdx.x, hk = blockIdx.y, n = blockIdx.z;
+    const int c = A.c_lo + blockIdx.x, hk = blockIdx.y, nq = blockIdx.z;
     const int seg = c / A.cps, loc = c - seg * A.cps;
     const int t0 = seg * A.C + loc * BC;
     const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
@@ -1081,14 +1082,17 @@ __global__ void __launch_bounds__(256) gdn_tc_dqdk_sum_kernel(const ChunkArgs A)
     for (int idx = threadIdx.x; idx < nb * (TD / 4); idx += 256) {
         const int t = idx / (TD / 4), i4 = idx - t * (TD / 4);
         float4 q = make_float4(0.f, 0.f, 0.f, 0.f), k = q;
-        for (int rho = 0; rho < r; ++rho) {
-            const long long ch = ((long long)n * A.H_v + hk + rho * A.H_k) * A.n_chunks + c;
-            const float4 a = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_dqM + ch * (BC * TD) + t * TD) + i4);
-            const float4 b = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_dkM + ch * (BC * TD) + t * TD) + i4);
-            q = make_float4(__fadd_rn(q.x, a.x), __fadd_rn(q.y, a.y), __fadd_rn(q.z, a.z), __fadd_rn(q.w, a.w));
-            k = make_float4(__fadd_rn(k.x, b.x), __fadd_rn(k.y, b.y), __fadd_rn(k.z, b.z), __fadd_rn(k.w, b.w));
+        for (int j = 0; j < A.rep; ++j) {
+            const int n = nq * A.rep + j;
+            for (int rho = 0; rho < r; ++rho) {
+                const long long ch = ((long long)n * A.H_v + hk + rho * A.H_k) * A.n_chunks + c;
+                const float4 a = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_dqM + ch * (BC * TD) + t * TD) + i4);
+                const float4 b = __ldg(reinterpret_cast<const float4*>(A.ws + A.o_dkM + ch * (BC * TD) + t * TD) + i4);
+                q = make_float4(__fadd_rn(q.x, a.x), __fadd_rn(q.y, a.y), __fadd_rn(q.z, a.z), __fadd_rn(q.w, a.w));
+                k = make_float4(__fadd_rn(k.x, b.x), __fadd_rn(k.y, b.y), __fadd_rn(k.z, b.z), __fadd_rn(k.w, b.w));
+            }
         }
-        const long long o = (((long long)n * A.T + t0 + t) * A.H_k + hk) * TD;
+        const long long o = (((long long)nq * A.T + t0 + t) * A.H_k + hk) * TD;
         reinterpret_cast<float4*>(A.dq + o)[i4] = q;
         reinterpret_cast<float4*>(A.dk + o)[i4] = k;
     }
@@ -1126,7 +1130,7 @@ int launch_tc_dqdk_sum(const ChunkArgs& a, void* stream)
 {
     cudaStream_t s = (cudaStream_t)stream;
     if (a.c_hi <= a.c_lo) return 0;
-    gdn_tc_dqdk_sum_kernel<<<dim3(a.c_hi - a.c_lo, a.H_k, a.N), 256, 0, s>>>(a);
+    gdn_tc_dqdk_sum_kernel<<<dim3(a.c_hi - a.c_lo, a.H_k, a.N / a.rep), 256, 0, s>>>(a);
     return (int)cudaGetLastError();
 }
 

@@ -42,7 +42,7 @@ class GdnParams(ctypes.Structure):
         ("H_v", ctypes.c_int64), ("S_k", ctypes.c_int64), ("S_v", ctypes.c_int64),
         ("gate", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
         ("C", ctypes.c_int64),
-        ("scale", ctypes.c_float), ("reserved1", ctypes.c_float),
+        ("scale", ctypes.c_float), ("seq_rep", ctypes.c_int32),
         ("q_s", ctypes.c_int64 * 3), ("k_s", ctypes.c_int64 * 3),
         ("v_s", ctypes.c_int64 * 3), ("gy_s", ctypes.c_int64 * 3),
     ]
@@ -100,17 +100,18 @@ def library():
 
 
 def make_params(N, T, H_k, H_v, S, kda, C=None, scale=None, q_s=None, k_s=None, v_s=None,
-                gy_s=None, in_dtype=DTYPE_F32, S_v=None) -> GdnParams:
+                gy_s=None, in_dtype=DTYPE_F32, S_v=None, seq_rep=1) -> GdnParams:
     """Parameter struct; S is the key head size S_k, S_v the value head size (default S);
-    strides default to the contiguous [N,T,H,S] layouts."""
+    N counts the value sequences and q, k hold N / seq_rep; strides default to the
+    contiguous [N,T,H,S] layouts."""
     SV = S if S_v is None else int(S_v)
     p = GdnParams()
     p.n_seq, p.T, p.H_k, p.H_v, p.S_k, p.S_v = N, T, H_k, H_v, S, SV
     p.gate = GATE_KDA if kda else GATE_SCALAR
-    p.in_dtype, p.reserved1 = int(in_dtype), 0.0
+    p.in_dtype, p.seq_rep = int(in_dtype), int(seq_rep)
     p.C = 0 if C is None else int(C)
     p.scale = (1.0 / math.sqrt(S)) if scale is None else float(scale)
-    p.q_s[:] = q_s or (T * H_k * S, H_k * S, S)
+    p.q_s[:] = q_s or (T * H_k * S, H_k * S, S)  # per q/k sequence
     p.k_s[:] = k_s or (T * H_k * S, H_k * S, S)
     p.v_s[:] = v_s or (T * H_v * SV, H_v * SV, SV)
     p.gy_s[:] = gy_s or (T * H_v * SV, H_v * SV, SV)
@@ -138,9 +139,12 @@ def input_dtype(t) -> int:
 
 def params_for(q, k, v, g, gy=None, C=None, scale=None) -> GdnParams:
     """Parameters for these input tensors: sizes, strides and their storage type (q, k, v,
-    g and gy must all have that type)."""
-    N, T, H_k, S = q.shape
-    H_v = v.shape[2]
+    g and gy must all have that type).  q, k may hold fewer sequences than v (a divisor of
+    its count): the sequence broadcast."""
+    Nq, T, H_k, S = q.shape
+    N, H_v = v.shape[0], v.shape[2]
+    if Nq == 0 or N % Nq:
+        raise ValueError("v's sequences must be a multiple of q's")
     kda = g.dim() == 4
     dt = input_dtype(q)
     for t in (k, v, g) + ((gy,) if gy is not None else ()):
@@ -149,7 +153,7 @@ def params_for(q, k, v, g, gy=None, C=None, scale=None) -> GdnParams:
     return make_params(N, T, H_k, H_v, S, kda, C=C, scale=scale, q_s=strides3(q),
                        k_s=strides3(k), v_s=strides3(v),
                        gy_s=strides3(gy) if gy is not None else None, in_dtype=dt,
-                       S_v=v.shape[3])
+                       S_v=v.shape[3], seq_rep=N // Nq)
 
 
 def _ptr(t):
@@ -265,8 +269,8 @@ def forward(q, k, v, g, beta, state0, C=None, scale=None, stream=None):
     """Allocate y, state_T, ckpt and run gdn_forward.  Returns (y, state_T, ckpt, params)."""
     import torch
     p = params_for(q, k, v, g, C=C, scale=scale)
-    N, T, H_k, S = q.shape
-    H_v, SV = v.shape[2], v.shape[3]
+    _, T, H_k, S = q.shape
+    N, H_v, SV = v.shape[0], v.shape[2], v.shape[3]
     dev = q.device
     y = torch.empty((N, T, H_v, SV), dtype=torch.float32, device=dev)
     state_T = torch.empty((N, H_v, SV, S), dtype=torch.float32, device=dev)
@@ -280,8 +284,9 @@ def forward(q, k, v, g, beta, state0, C=None, scale=None, stream=None):
 def split_packed(p: GdnParams, packed):
     """Views of the six regions of a packed gradient buffer."""
     N, T, H_k, H_v, S, SV = p.n_seq, p.T, p.H_k, p.H_v, p.S_k, p.S_v
+    Nq = N // max(1, p.seq_rep)
     off = packed_grad_offsets(p) + [packed_grad_elems(p)]
-    shapes = [(N, T, H_k, S), (N, T, H_k, S), (N, T, H_v, SV),
+    shapes = [(Nq, T, H_k, S), (Nq, T, H_k, S), (N, T, H_v, SV),
               (N, T, H_v, S) if p.gate == GATE_KDA else (N, T, H_v), (N, T, H_v),
               (N, H_v, SV, S)]
     names = ["dq", "dk", "dv", "dg", "dbeta", "dstate0"]

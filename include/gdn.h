@@ -21,7 +21,8 @@
  * dk = dM^T delta + S'^T du (dM read before the du update); dM += k du^T (= dS');
  * dg = sum_j dS' (.) S' per key column (KDA) or summed (scalar gate); dM = a (.) dS'.
  * dq/dk are summed over the H_v/H_k value heads that share a key head, in ascending
- * value-head order, without atomics.
+ * value-head order (and, with the sequence broadcast, over the value sequences that share
+ * a q/k sequence, ascending), without atomics.
  *
  * Checkpointed recompute (PR #16 body: "checkpointed recompute (C ~ sqrt(T))"): the
  * forward stores ckpt[c] = the state entering token c*C for c = 0..n_ck-1,
@@ -30,9 +31,10 @@
  *
  * Layouts (M = S^T; fp32 unless gdn_params_t.in_dtype makes q, k, v, g, beta, gy 16-bit)
  * ----------------------------------------------------------------------------------
- *   q, k      [N][T][H_k][S_k]  element strides q_s/k_s = {seq, token, head}; the
+ *   q, k      [N_q][T][H_k][S_k] element strides q_s/k_s = {seq, token, head}; the
  *                               S_k elements of one (seq, token, head) are contiguous
- *                               (so q, k may be row views of a packed qkv buffer)
+ *                               (so q, k may be row views of a packed qkv buffer);
+ *                               N_q = N / seq_rep (N without the sequence broadcast)
  *   v         [N][T][H_v][S_v]  strides v_s, last dim contiguous
  *   gy        [N][T][H_v][S_v]  strides gy_s, last dim contiguous
  *   g         [N][T][H_v] (scalar gate) or [N][T][H_v][S_k] (KDA), contiguous
@@ -40,7 +42,7 @@
  *   state0, state_T, dstate_T    [N][H_v][S_v][S_k] contiguous
  *   y         [N][T][H_v][S_v] contiguous
  *   ckpt      [N][H_v][n_ck][S_v][S_k] contiguous
- *   packed    dq [N][T][H_k][S_k] | dk [N][T][H_k][S_k] | dv [N][T][H_v][S_v] |
+ *   packed    dq [N_q][T][H_k][S_k] | dk [N_q][T][H_k][S_k] | dv [N][T][H_v][S_v] |
  *             dg (like g) | dbeta [N][T][H_v] | dstate [N][H_v][S_v][S_k], back to back
  *             (element offsets from gdn_packed_grad_offsets)
  *
@@ -71,7 +73,8 @@
  *
  * Errors (no call ever writes an output when it returns an error)
  * ------
- *   GDN_ERR_INVALID_ARG  NULL pointer, negative size, H_v % H_k != 0, a stride that is
+ *   GDN_ERR_INVALID_ARG  NULL pointer, negative size, H_v % H_k != 0, n_seq % seq_rep != 0,
+ *                        a stride that is
  *                        negative, an input that is not aligned to its element (4 bytes,
  *                        2 for 16-bit inputs), a state or output buffer that is not
  *                        16-byte aligned, bad gate kind or input dtype
@@ -117,7 +120,10 @@ typedef struct {
     int32_t in_dtype;                     /* gdn_dtype_t of q, k, v, g, beta, gy (0: fp32) */
     int64_t C;                            /* checkpoint interval; <= 0: ceil(sqrt(T)) */
     float scale;                          /* output scale, usually 1/sqrt(S_k) */
-    float reserved1;                      /* must be 0 */
+    int32_t seq_rep;                      /* 0 or 1: q, k have n_seq sequences.  r > 1: the
+                                             sequence broadcast (PR #16 "iv3/rq3"): q, k
+                                             (and dq, dk) hold n_seq / r sequences and value
+                                             sequence n reads q/k sequence n / r */
     int64_t q_s[3], k_s[3], v_s[3], gy_s[3]; /* element strides of {seq, token, head} */
 } gdn_params_t;
 

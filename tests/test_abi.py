@@ -164,8 +164,11 @@ def test_invalid_arguments():
     p = gdn.make_params(1, 8, 1, 1, 32, False)
     p.in_dtype = 3                                                          # unknown input dtype
     assert call_forward(p) == INVALID
-    p = gdn.make_params(1, 8, 1, 1, 32, False)
-    p.reserved1 = 1.0
+    p = gdn.make_params(3, 8, 1, 1, 32, False)
+    p.seq_rep = 2                                                           # 3 % 2 != 0
+    assert call_forward(p) == INVALID
+    p = gdn.make_params(2, 8, 1, 1, 32, False)
+    p.seq_rep = -1
     assert call_forward(p) == INVALID
     p = gdn.make_params(-1, 8, 1, 1, 32, False)
     assert call_forward(p) == INVALID

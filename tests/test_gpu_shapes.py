@@ -43,3 +43,24 @@ def test_head_size_16_checkpoint_interval_invariance(kda):
         got, pk = H.run_gpu(prob, C=C, dev=dev)
         assert torch.equal(pk, pbase), C
         assert np.array_equal(got["y"], base["y"])
+
+
+BCAST = [(128, 128, 2, 64), (128, 128, 2, 9), (64, 64, 2, 9), (32, 32, 3, 40), (64, 32, 2, 9),
+         (16, 16, 2, 9)]
+
+
+@pytest.mark.parametrize("kda", [False, True], ids=["scalar", "kda"])
+@pytest.mark.parametrize("sk,sv,rep,C", BCAST, ids=[f"Sk{a}-Sv{b}-rep{r}-C{c}" for a, b, r, c in BCAST])
+def test_sequence_broadcast(sk, sv, rep, C, kda):
+    """The sequence broadcast ("metal: GATED_DELTA_NET_BACK", PR #16: head mapping iv3/rq3):
+    q, k hold N / rep sequences and value sequence n reads q/k sequence n / rep; dq, dk sum
+    over the rep value sequences of each.  Every path: the tensor-core chunked form (both
+    gates, one and two chunks per segment), the FP32-pipe chunked form and the token
+    recurrence."""
+    N = 2 * rep
+    prob = synth.make_problem(N, 150 if C == 64 else 70, 2, 4, sk, kda=kda, seed=95 + sk + rep, C=C,
+                              dstate_T=True, d_v=sv, seq_rep=rep)
+    gpu, _ = H.run_gpu(prob)
+    assert gpu["dq"].shape[0] == N // rep
+    ref = H.run_oracle(H.problem_dict(prob), prob.scale, prob.C)
+    H.compare_all(gpu, ref, H.tolerance(prob.T))
