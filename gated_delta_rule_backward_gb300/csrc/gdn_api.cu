@@ -440,10 +440,11 @@ namespace {
 // The backward's ranges and their shares of the segments, in the order the backward walks
 // them (the last segments first).  The first range is the smaller: its prep and dM chain
 // run with nothing beside them, while the second range's run beside the first range's
-// gradient step (at the 4096-token, 64-segment workload, 35/65 took the step from
-// 1.88 to 1.83 ms; 25/75 gave 1.84, and three ranges 1.90-1.94).
+// gradient step.  At the 4096-token, 64-segment workload, on one GB300, three runs each:
+// 40/60 1.833 ms per step, 45/55 1.840, 35/65 1.870, 30/70 1.880, 50/50 1.881 (three
+// ranges were 1.90-1.94 when last tried).
 constexpr int kBwdRanges = 2;
-constexpr int kBwdWalkPct[gdn::kMaxRanges] = {35, 65, 0, 0};
+constexpr int kBwdWalkPct[gdn::kMaxRanges] = {40, 60, 0, 0};
 }  // namespace
 
 int gdn::pipeline_ranges(int n_ck, bool backward)
