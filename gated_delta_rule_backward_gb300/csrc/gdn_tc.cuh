@@ -374,21 +374,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Bulk copy shared -> global (TMA engine), tracked by the issuing thread's bulk groups: both
-// addresses 16-byte aligned, bytes a multiple of 16.  commit closes the group of the copies
-// issued since the last commit; wait_read0 returns once every committed copy has finished
-// reading shared memory (the source may then be rewritten); wait_all0 once their writes to
-// global memory are done.
-__device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 #endif  // __CUDACC__
 
 }  // namespace tc

@@ -41,8 +41,6 @@ namespace {
 constexpr int TD = 128;                       // head size
 constexpr int TCT = 288;                      // 8 compute warps (row j, column half) + 1 issuer warp
 constexpr int kIssuer = 256;                  // issues the MMAs and bulk copies
-constexpr int kStateCT = 320;                 // the state chain adds a storer warp (warp 9)
-constexpr int kStorer = 288;                  // its lane 0 stores y and states by bulk copies
 constexpr uint32_t kColMhi = 0;               // TMEM columns: M hi  (bf16 A operand, K = 128)
 constexpr uint32_t kColMlo = 64;              //               M lo
 constexpr uint32_t kColDh = 128;              //               Delta^T hi (bf16 A of D23, K = 32)
@@ -68,16 +66,15 @@ __device__ __forceinline__ void raise_timeout(int kernel, int sites)
 constexpr int kSB1 = 0;                            // [W; Q] bf16 hi, then lo: 2 x 64 x 128, row-group-major
 constexpr int kSB23 = kSB1 + kTcWElems + kTcQElems;  // [sQD; rK^T] bf16 hi, lo  2 x 160 x 32
 constexpr int kSU = kSB23 + kTcB23Elems;           // U^T, operand layout (R = 128), fp32
-constexpr int kSGam = kSU + BC * TD;               // gamma (32)
-constexpr int kStageLd = TD + 4;                   // staging rows (16-byte pad: conflict-free)
-constexpr int kSY = kSGam + BC;                    // y of three chunks, rows t (forward)
-constexpr int kSCk = kSY + 3 * BC * kStageLd;      // a whole state, 128 rows (checkpoints, the end)
-constexpr int kSGl = kSCk + TD * kStageLd;         // KDA: gamma_last per column, two buffers by
+constexpr int kSDel = kSU + BC * TD;               // staging of checkpoint rows (32 x kStageLd)
+constexpr int kSGam = kSDel + 2 * BC * TD;         // gamma (32)
+constexpr int kStageLd = TD + 4;                   // staging rows for coalesced global writes
+constexpr int kSY = kSGam + BC;                    // y of two chunks, rows t (forward)
+constexpr int kSGl = kSY + 2 * BC * kStageLd;      // KDA: gamma_last per column, two buffers by
                                                    // chunk parity (the next chunk's lands while
                                                    // this one's update reads)
 constexpr int kSFloats = kSGl + 2 * TD;
-constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 128;  // + barriers (7 used)
-static_assert(kSmemBytes <= 227 * 1024, "state chain shared memory");
+constexpr size_t kSmemBytes = sizeof(float) * kSFloats + 128;  // + barriers (6 used)
 
 constexpr uint32_t kB1Bytes = sizeof(float) * (kTcWElems + kTcQElems);
 constexpr int kHalfW = kTcWElems / 2;  // 32 x 128 bf16 values
@@ -123,14 +120,12 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     uint64_t* bar_a = bars + 3;  // bar_a[g]: columns [32 g, 32 g + 32) of both halves of M are in TMEM
     uint64_t* bar_d = bars + 5;  // Delta^T (the A operand of D23) is in TMEM, and every compute
                                  // warp has seen D1 complete
-    uint64_t* bar_ck = bars + 6; // a whole state is staged at kSCk (one arrival per compute warp)
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool compute = warp < 8;          // warps 0-7 hold M; warp 8 issues MMAs and copies
     const bool issuer = tid == kIssuer;
-    const bool storer = tid == kStorer;     // warp 9: y and states out by bulk copies
     const int j = 32 * (warp & 3) + lane;   // row of M (compute warps)
     const int hc = (warp >> 2) & 1;         // column half: columns [64 hc, 64 hc + 64)
 
@@ -144,7 +139,6 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         tc::mbar_init(bar_mma, 1);
         for (int g = 0; g < 2; ++g) tc::mbar_init(bar_a + g, 8);  // one arrival per compute warp
         tc::mbar_init(bar_d, 8);                                  // one per compute warp
-        tc::mbar_init(bar_ck, 8);                                 // one per compute warp
         tc::mbar_fence_init();
         s_err = 0;
     }
@@ -154,7 +148,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
     tc::fence_after();
     const uint32_t tmem = s_tmem;
 
-    uint32_t ph_b1 = 0, ph_b23 = 0, ph_mma = 0, ph_ck = 0;
+    uint32_t ph_b1 = 0, ph_b23 = 0, ph_mma = 0;
     bool mma_out = false;  // issuer: a committed MMA group not yet seen complete, phase ph_out
     uint32_t ph_out = 0;
     bool b1_pending = false, b23_pending = false;
@@ -179,41 +173,14 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             m[4 * q + 3] = x.w;
         }
     }
-    // y of a chunk is assembled in shared memory (rows t, one of three buffers, chunk c in
-    // buffer c % 3) by the column-half 1 threads: the Q part in (3), the QD Delta part added
-    // in (5).  The storer copies it out with bulk copies after the next chunk's CTA barrier of
-    // (5) and has the copies read before the barrier after that, one chunk before the buffer is
-    // written again; the compute warps never wait on global stores.  (A y that is only 4-byte
-    // aligned goes out from the compute warps instead, during the next chunk's D23.)
-    // Checkpoints and the final state: the compute warps stage M (all 128 rows) at kSCk and
-    // arrive on bar_ck; the storer copies the rows out and has them read before the CTA
-    // barrier of (5), ahead of the next staging.
+    // y of a chunk is assembled in shared memory (rows t, one of two buffers by chunk parity)
+    // by the column-half 1 threads: the Q part in (3), the QD Delta part added in (5).  It
+    // goes to global memory during the next chunk's D23, when the compute warps would only
+    // wait (the buffer is next written two chunks later, after the CTA barrier of (5)).
     int y_t0 = 0, y_nb = 0;
     const float* y_buf = sm + kSY;  // the buffer of the chunk whose y is pending
+    float* stage = sm + kSDel;   // idle while D1 runs: 32 rows of kStageLd floats (checkpoints)
     const int ctid = tid;        // 0..255 for the compute warps
-    auto stage_state = [&]() {   // this thread's 64 columns of row j, then the warp's arrival
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-            *reinterpret_cast<float4*>(sm + kSCk + j * kStageLd + 64 * hc + 4 * q) =
-                make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
-        tc::fence_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(bar_ck);
-    };
-    auto put_state = [&](float* dst) {  // storer: the staged state to dst (128 rows of 512 bytes)
-        if (!tc::mbar_wait(bar_ck, ph_ck)) atomicOr(&s_err, kWCopyB);
-        ph_ck ^= 1;
-        for (int r = 0; r < TD; ++r) tc::bulk_s2g(dst + (long long)r * TD, sm + kSCk + r * kStageLd, sizeof(float) * TD);
-        tc::bulk_commit();
-    };
-    auto put_y = [&](int t0y, int nby, const float* buf) {  // storer: one chunk's y rows
-        float* yp = A.y + (((long long)n * A.T + t0y) * A.H_v + h) * TD;
-        for (int t = 0; t < nby; ++t)
-            tc::bulk_s2g(yp + (long long)t * A.H_v * TD, buf + t * kStageLd, sizeof(float) * TD);
-        tc::bulk_commit();
-    };
-    int py_t0 = 0, py_nb = 0;       // storer: the chunk whose y goes out after the next barrier
-    const float* py_buf = sm + kSY;
     auto store_y = [&]() {       // the global writes are whole 512-byte rows
         tc::bar_sync_first(256);  // the column-half 1 threads' adds to y_buf are complete
         float* yp = A.y + (((long long)n * A.T + y_t0) * A.H_v + h) * TD;
@@ -222,7 +189,30 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             const int t = idx / (TD / 4), q = idx - t * (TD / 4);
             const float4 v = *reinterpret_cast<const float4*>(y_buf + t * kStageLd + 4 * q);
             float* yq = yp + t * ys + 4 * q;
-            yq[0] = v.x; yq[1] = v.y; yq[2] = v.z; yq[3] = v.w;
+            if (A.vec_y) {  // y is only required to be 4-byte aligned
+                *reinterpret_cast<float4*>(yq) = v;
+            } else {
+                yq[0] = v.x; yq[1] = v.y; yq[2] = v.z; yq[3] = v.w;
+            }
+        }
+    };
+    auto store_ckpt = [&](float* dst) {  // row-major M through `stage`, 32 rows at a time
+#pragma unroll 1
+        for (int r = 0; r < 4; ++r) {
+            if ((warp & 3) == r) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    *reinterpret_cast<float4*>(stage + lane * kStageLd + 64 * hc + 4 * q) =
+                        make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+            }
+            tc::bar_sync_first(256);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int idx = ctid + 256 * k, row = idx >> 5, q = idx & 31;
+                *reinterpret_cast<float4*>(dst + (long long)(32 * r + row) * TD + 4 * q) =
+                    *reinterpret_cast<const float4*>(stage + row * kStageLd + 4 * q);
+            }
+            tc::bar_sync_first(256);
         }
     };
     // Columns [8 q, 8 q + 8) of this thread's half of M -> bf16 hi/lo in TMEM (4 columns
@@ -261,7 +251,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
         const int t0 = seg * A.C + loc * BC;
         const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
         const long long ch = head * A.n_chunks + c;
-        float* sY = sm + kSY + (c % 3) * (BC * kStageLd);  // this chunk's y
+        float* sY = sm + kSY + (c & 1) * (BC * kStageLd);  // this chunk's y
         // (1) M (bf16 hi/lo, the A operand of D1) goes into TMEM slice by slice (release_group)
         // (2) D1 = M [W; Q]^T on the tensor cores, each k-slice issued as soon as its columns of
         //     M are in TMEM; meanwhile the compute warps store the checkpoint at a segment's
@@ -299,10 +289,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 }
             }
         } else if (compute) {
-            if (loc == 0) stage_state();
-        } else if (storer) {
-            if (loc == 0) put_state(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
-            tc::bulk_wait_read0();  // the checkpoint and the y copied out since the last barrier
+            if (loc == 0) store_ckpt(A.ckpt_out + (head * A.n_ck + seg) * (long long)(TD * TD));
         }
         // (3) Delta^T (rows j) and the Q part of y^T.  Only the compute warps and the issuer
         // wait on bar_mma: every waiter must have seen a phase complete before the next commit
@@ -356,7 +343,7 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
 #pragma unroll
                 for (int t = 0; t < BC; ++t) sY[t * kStageLd + j] = __fmul_rn(__fmul_rn(A.scale, sGam[t]), x[t]);
             }
-            if (!A.vec_y && y_nb > 0) store_y();  // the previous chunk's y, while D23 runs
+            if (y_nb > 0) store_y();  // the previous chunk's y, while D23 runs
         }
         ph_b23 ^= 1;
         if (!ok) atomicOr(&s_err, kWMma1);
@@ -397,11 +384,6 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 load_b23<KDA>(A, ch + 1, c + 1, sm, bar_b23);
                 b23_pending = true;
             }
-        } else if (storer) {
-            if (A.vec_y && py_nb > 0) put_y(py_t0, py_nb, py_buf);  // the previous chunk's y is complete
-            py_t0 = t0;
-            py_nb = nb;
-            py_buf = sY;
         } else if (compute) {
             if (hc == 1) {  // y += D23[:, 0:32]
                 float x[32];
@@ -409,7 +391,6 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
                 tc::wait_ld();
 #pragma unroll
                 for (int t = 0; t < BC; ++t) sY[t * kStageLd + j] = __fadd_rn(sY[t * kStageLd + j], x[t]);
-                tc::fence_async_smem();  // the storer's bulk copies read these rows after the next barrier
             }
             y_t0 = t0;
             y_nb = nb;
@@ -445,15 +426,8 @@ __device__ __forceinline__ void state_chain(const ChunkArgs& A, float* sm, int b
             if (b23_pending) tc::mbar_wait(bar_b23, ph_b23);
         }
     } else if (compute) {
-        if (!A.vec_y && y_nb > 0) store_y();
-        stage_state();  // after this warp's last y adds: the storer's wait orders both
-    } else if (storer) {
-        put_state((c_end == A.n_chunks ? A.state_T : A.carry) + head * (long long)(TD * TD));
-        if (A.vec_y && py_nb > 0) put_y(py_t0, py_nb, py_buf);
-    }
-    if (storer) {
-        tc::bulk_wait_all0();  // every bulk store of this CTA has been written
-        if (s_err) raise_timeout(kKerState, s_err);
+        if (y_nb > 0) store_y();
+        store_ckpt((c_end == A.n_chunks ? A.state_T : A.carry) + head * (long long)(TD * TD));
     }
     tc::fence_before();
     __syncthreads();
@@ -814,7 +788,7 @@ __device__ __forceinline__ void dstate_chain(const ChunkArgs& A, float* sm, int 
 
 // The forward's state chain: one CTA per (head, sequence).
 template <bool KDA>
-__global__ void __launch_bounds__(kStateCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
+__global__ void __launch_bounds__(TCT, 1) gdn_tc_state_kernel(const ChunkArgs A)
 {
     extern __shared__ __align__(1024) float sm[];
     state_chain<KDA>(A, sm, blockIdx.x, blockIdx.y);
@@ -834,7 +808,7 @@ static int launch_tc_state_t(const ChunkArgs& a, cudaStream_t s)
     int e = (int)cudaFuncSetAttribute(gdn_tc_state_kernel<KDA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kSmemBytes);
     if (e) return e;
-    gdn_tc_state_kernel<KDA><<<dim3(a.H_v, a.N), kStateCT, kSmemBytes, s>>>(a);
+    gdn_tc_state_kernel<KDA><<<dim3(a.H_v, a.N), TCT, kSmemBytes, s>>>(a);
     return (int)cudaGetLastError();
 }
 
