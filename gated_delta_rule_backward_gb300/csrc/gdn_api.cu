@@ -351,7 +351,8 @@ int tc_ranges(const Plan& pl, bool backward)
 }
 
 // Kernels of a tensor-core backward call: per non-empty range the prep, the dM chain, one
-// gradient launch per place in a segment that has chunks there, and the sum.
+// gradient launch per place in a segment that has chunks there, and the sums over value heads
+// (one per gradient launch, or one per range).
 int tc_backward_launches(const Plan& pl)
 {
     const int R = gdn::pipeline_ranges((int)pl.n_ck, true);
@@ -364,8 +365,11 @@ int tc_backward_launches(const Plan& pl)
         a.c_lo = (int)std::min<int64_t>(pl.n_chunks, (int64_t)s_lo * pl.cps);
         a.c_hi = (int)std::min<int64_t>(pl.n_chunks, (int64_t)s_hi * pl.cps);
         if (a.c_hi <= a.c_lo) continue;
-        n += 3;
-        for (a.grad_loc = 0; a.grad_loc < pl.cps; ++a.grad_loc) n += gdn::tc_grad_units(a) > 0 ? 1 : 0;
+        n += 2;  // prep, dM chain
+        int places = 0;  // gradient launches, one per place with chunks
+        for (a.grad_loc = 0; a.grad_loc < pl.cps; ++a.grad_loc) places += gdn::tc_grad_units(a) > 0 ? 1 : 0;
+        const bool by_place = gdn::kSumByPlace && pl.cps <= gdn::kMaxPlaces;
+        n += places + (by_place ? places : 1);  // and the sums over value heads
     }
     return n;
 }
@@ -394,13 +398,18 @@ int gdn::acquire_pipeline(gdn::Pipeline** out)
         gdn::Pipeline& P = g_pipes[dev];
         int least = 0, greatest = 0;
         e = (int)cudaDeviceGetStreamPriorityRange(&least, &greatest);
-        // numerically lower is more urgent; the middle level falls back to the lowest
-        const int middle = greatest + 1 < least ? greatest + 1 : least;
-        cudaStream_t hi = nullptr, lo = nullptr, bg = nullptr;
+        // numerically lower is more urgent: chains first, then preps; the gradient steps and
+        // the sums in the order kSumBelowGrads sets (levels the device lacks fall back to the
+        // least urgent one)
+        auto level = [&](int k) { return greatest + k < least ? greatest + k : least; };
+        const int grads = gdn::kSumBelowGrads ? level(2) : least;
+        const int sums = gdn::kSumBelowGrads ? least : level(1);
+        cudaStream_t hi = nullptr, lo = nullptr, bg = nullptr, sm = nullptr;
         if (!e) e = (int)cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest);
-        if (!e) e = (int)cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, middle);
-        if (!e) e = (int)cudaStreamCreateWithPriority(&bg, cudaStreamNonBlocking, least);
-        constexpr int kEv = 4 + 4 * gdn::kMaxRanges;
+        if (!e) e = (int)cudaStreamCreateWithPriority(&lo, cudaStreamNonBlocking, level(1));
+        if (!e) e = (int)cudaStreamCreateWithPriority(&bg, cudaStreamNonBlocking, grads);
+        if (!e) e = (int)cudaStreamCreateWithPriority(&sm, cudaStreamNonBlocking, sums);
+        constexpr int kEv = 5 + 4 * gdn::kMaxRanges + gdn::kMaxRanges * gdn::kMaxPlaces;
         cudaEvent_t ev[kEv] = {};
         for (int i = 0; i < kEv && !e; ++i)
             e = (int)cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
@@ -411,15 +420,19 @@ int gdn::acquire_pipeline(gdn::Pipeline** out)
         P.hi = hi;
         P.lo = lo;
         P.bg = bg;
+        P.sum = sm;
         P.fork = ev[0];
         P.join_hi = ev[1];
         P.join_lo = ev[2];
         P.join_bg = ev[3];
+        P.join_sum = ev[4];
         for (int i = 0; i < gdn::kMaxRanges; ++i) {
-            P.prep_done[i] = ev[4 + i];
-            P.chain_go[i] = ev[4 + gdn::kMaxRanges + i];
-            P.ds_done[i] = ev[4 + 2 * gdn::kMaxRanges + i];
-            P.grad_done[i] = ev[4 + 3 * gdn::kMaxRanges + i];
+            P.prep_done[i] = ev[5 + i];
+            P.chain_go[i] = ev[5 + gdn::kMaxRanges + i];
+            P.ds_done[i] = ev[5 + 2 * gdn::kMaxRanges + i];
+            P.grad_done[i] = ev[5 + 3 * gdn::kMaxRanges + i];
+            for (int k = 0; k < gdn::kMaxPlaces; ++k)
+                P.place_done[i][k] = ev[5 + 4 * gdn::kMaxRanges + i * gdn::kMaxPlaces + k];
         }
         g_pipe_ready[dev] = true;
     }
@@ -568,8 +581,8 @@ int gdn_backward_launches(const gdn_params_t* p)
     }
     const Plan pl = make_plan(p);
     // chunked: prep, [recompute], dM chain, gradients.  On the tensor-core path, per chunk
-    // range: prep, dM chain, a gradient launch per place in a segment, and the sum over value
-    // heads (a call with timing events runs the same kernels as one range).
+    // range: prep, dM chain, a gradient launch per place in a segment, and the sums over value
+    // heads.  (A call with timing events runs its stages as one range, with one sum.)
     if (pl.chunked) return pl.tensor ? tc_backward_launches(pl) : (pl.cps > 1 ? 4 : 3) + (pl.rep > 1 ? 1 : 0);
     return p->T > 0 ? 2 : 1;
 }

@@ -1428,11 +1428,13 @@ static int launch_prep_range(const ChunkArgs& a, int R, bool backward, int r, cu
 // prep(r + 1) is enqueued once chain(r) has been, so that the chain's whole-SM CTAs are
 // placed before the prep fills the GPU.
 //
-// Backward, ranges last to first, three streams:
-//   high:   dM chain of range r (after prep(r)), carrying dM to range r - 1
-//   middle: prep(r), then prep(r - 1) once the dM chain of r has been enqueued; after the
-//           last prep, the sum over value heads of each range once its gradients are done
-//   low:    after the dM chain of r, the gradient launches of range r
+// Backward, ranges last to first, four streams (most urgent first):
+//   chains:    dM chain of range r (after prep(r)), carrying dM to range r - 1
+//   preps:     prep(r), then prep(r - 1) once the dM chain of r has been enqueued
+//   gradients: after the dM chain of r, the gradient launches of range r, one per place (a
+//              launch for place k > 0 may start in the tail of the one for place k - 1)
+//   sums:      the sum over value heads of the range's chunks once its gradient launches are
+//              done (or of each place's, kSumByPlace), ahead of the next gradient launch
 // so that the gradient work of one range runs while the chain walks the next.  With timing
 // events set, the backward instead runs its stages one after another as a single range
 // (prep and dM chain, gradient step, sum), each between two events.
@@ -1449,12 +1451,40 @@ static int launch_grads(const ChunkArgs& ar, cudaStream_t st)
     return e;
 }
 
+// The gradient launches of range r on the gradient stream and the sums over value heads on
+// the sum stream: one sum per place once that place's launch is done, or one for the range
+// after its last launch (kSumByPlace).
+static int grads_and_sums(const ChunkArgs& ar, int r, Pipeline* P)
+{
+    const cudaStream_t bg = (cudaStream_t)P->bg, su = (cudaStream_t)P->sum;
+    const bool by_place = kSumByPlace && ar.cps <= kMaxPlaces;
+    ChunkArgs g = ar;
+    int e = 0;
+    for (int k = 0; k < ar.cps && !e; ++k) {
+        g.grad_loc = k;
+        if (tc_grad_units(g) <= 0) continue;
+        e = launch_tc_grad(g, bg);
+        if (!e && by_place) {
+            e = (int)cudaEventRecord((cudaEvent_t)P->place_done[r][k], bg);
+            if (!e) e = (int)cudaStreamWaitEvent(su, (cudaEvent_t)P->place_done[r][k], 0);
+            if (!e) e = launch_tc_dqdk_sum(g, su);
+        }
+    }
+    if (!e && !by_place) {
+        e = (int)cudaEventRecord((cudaEvent_t)P->grad_done[r], bg);
+        if (!e) e = (int)cudaStreamWaitEvent(su, (cudaEvent_t)P->grad_done[r], 0);
+        if (!e) e = launch_tc_dqdk_sum(ar, su);
+    }
+    return e;
+}
+
 static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, EventTap& tap)
 {
     Pipeline* P = nullptr;
     int e = acquire_pipeline(&P);
     if (e) return e;
     const cudaStream_t hi = (cudaStream_t)P->hi, lo = (cudaStream_t)P->lo, bg = (cudaStream_t)P->bg;
+    const cudaStream_t su = (cudaStream_t)P->sum;
     const bool staged = backward && tap.ev != nullptr;
     const int R = staged ? 1 : pipeline_ranges(a.n_ck, backward);
     tap.mark(user);
@@ -1462,6 +1492,7 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
     if (!e) e = (int)cudaStreamWaitEvent(lo, (cudaEvent_t)P->fork, 0);
     if (!e) e = (int)cudaStreamWaitEvent(hi, (cudaEvent_t)P->fork, 0);
     if (!e && backward && !staged) e = (int)cudaStreamWaitEvent(bg, (cudaEvent_t)P->fork, 0);
+    if (!e && backward && !staged) e = (int)cudaStreamWaitEvent(su, (cudaEvent_t)P->fork, 0);
     int order[kMaxRanges], nr = 0;
     for (int i = 0; i < R; ++i) {
         const int r = backward ? R - 1 - i : i;
@@ -1488,21 +1519,12 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
         if (!e && backward && !staged) {
             e = (int)cudaEventRecord((cudaEvent_t)P->ds_done[r], hi);
             if (!e) e = (int)cudaStreamWaitEvent(bg, (cudaEvent_t)P->ds_done[r], 0);
-            if (!e) e = launch_grads(ar, bg);
-            if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->grad_done[r], bg);
+            if (!e) e = grads_and_sums(ar, r, P);
         }
         if (!e && i + 1 < nr) {
             e = (int)cudaStreamWaitEvent(lo, (cudaEvent_t)P->chain_go[r], 0);
             if (!e) e = prep(order[i + 1]);
         }
-    }
-    // the value-head sums on the prep stream, after its last prep: a range's sum runs beside
-    // the next range's gradient step instead of ahead of it on the gradient stream
-    for (int i = 0; i < nr && !e && backward && !staged; ++i) {
-        ChunkArgs ar;
-        range_of(a, R, backward, order[i], ar);
-        e = (int)cudaStreamWaitEvent(lo, (cudaEvent_t)P->grad_done[order[i]], 0);
-        if (!e) e = launch_tc_dqdk_sum(ar, lo);
     }
     if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_hi, hi);
     if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_lo, lo);
@@ -1511,6 +1533,8 @@ static int tc_pipelined(const ChunkArgs& a, cudaStream_t user, bool backward, Ev
     if (!e && backward && !staged) {
         e = (int)cudaEventRecord((cudaEvent_t)P->join_bg, bg);
         if (!e) e = (int)cudaStreamWaitEvent(user, (cudaEvent_t)P->join_bg, 0);
+        if (!e) e = (int)cudaEventRecord((cudaEvent_t)P->join_sum, su);
+        if (!e) e = (int)cudaStreamWaitEvent(user, (cudaEvent_t)P->join_sum, 0);
     }
     release_pipeline();
     if (e) return e;

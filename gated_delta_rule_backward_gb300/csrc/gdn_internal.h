@@ -144,18 +144,31 @@ struct EventTap {
 // middle one and the gradient steps on a low one.  Created on first use; the lock
 // serialises the enqueueing of calls that use them.
 constexpr int kMaxRanges = 4;
+// The backward's value-head sums run on their own stream.  Above the gradient steps'
+// priority (kSumBelowGrads false) a sum's CTAs go first once its gradient launch is done, then
+// the next gradient launch; below it, they take what the gradient CTAs leave free on an SM
+// (measured slower: 1.47 against 1.36 ms per backward at 4096 tokens, 48 heads of 128: beside a
+// gradient CTA a sum CTA slows it more than its own work is worth).  With kSumByPlace, and at
+// most kMaxPlaces places of a chunk in its segment, each gradient launch's chunks are summed as
+// soon as it is done; otherwise each chunk range's once all its gradient launches are.
+constexpr int kMaxPlaces = 4;
+constexpr bool kSumBelowGrads = false;
+constexpr bool kSumByPlace = false;
 struct Pipeline {
-    void* hi;
-    void* lo;
-    void* bg;
+    void* hi;   // chains
+    void* lo;   // preps
+    void* bg;   // gradient steps
+    void* sum;  // value-head sums, the least urgent
     void* fork;
     void* join_hi;
     void* join_lo;
     void* join_bg;
+    void* join_sum;
     void* prep_done[kMaxRanges];
     void* chain_go[kMaxRanges];
     void* ds_done[kMaxRanges];
     void* grad_done[kMaxRanges];
+    void* place_done[kMaxRanges][kMaxPlaces];
 };
 // Returns the current device's pipeline (creating it on first use) with its lock held;
 // release_pipeline() unlocks.  Returns a cudaError_t as int.

@@ -157,6 +157,13 @@ __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::aft
 // Generic-proxy shared-memory writes made visible to the async proxy (MMA, bulk copies).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on the stream (when it
+// is launched with programmatic stream serialisation) start its CTAs once every CTA of this grid
+// has issued it or exited; wait blocks the calling thread until the preceding grid has completed
+// and its writes are visible (at once when no such grid is in flight).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // TMEM allocation by one whole warp; the base address lands in *holder.
 __device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t cols)
 {

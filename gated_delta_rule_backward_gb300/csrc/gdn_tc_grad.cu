@@ -104,6 +104,8 @@ constexpr int kAW2 = kAW1 + BC * LDF;
 constexpr int kAZ = kAW2 + BC * LDF;
 constexpr int kABP = kAZ + BC * LDF;        // P (rows t, K = 32) hi, lo
 constexpr int kABPS = kABP + 2 * kTP;       // [P ; S]^T (rows t, K = 64) hi, lo
+constexpr int kAZb = kABP;                 // Z diag(beta) (LDF): dead before the B tiles are built
+static_assert(kAZb + BC * LDF <= kR2, "R1 overflow");
 constexpr int kKcol = kR1 + 6 * BC * LDF;   // KDA, step (9): the column-side exchange and dG
 constexpr int kKdg = kKcol + BC * TD;
 static_assert(kKdg + BC * TD <= kR2, "KDA tiles overflow R1");
@@ -134,6 +136,27 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// The warp sums of N values per lane (N = 32 or 16) by recursive halving: lane l ends with
+// the sum of value l (N = 32) or l / 2 (N = 16) in v[0].  Each partial sum pairs the same
+// lanes in the same order as warp_sum, so the sums are warp_sum's bit for bit, in
+// N - 1 + (32 / N - 1) shuffles instead of 5 N.
+template <int N>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane)
+{
+    static_assert(N == 32 || N == 16, "32 or 16 values");
+#pragma unroll
+    for (int m = N / 2, o = 16; m >= 1; m >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;  // keeps the upper half of the live values
+#pragma unroll
+        for (int i = 0; i < m; ++i) {
+            const float send = up ? v[i] : v[i + m];
+            const float keep = up ? v[i + m] : v[i];
+            v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+        }
+    }
+    if (N == 16) v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+}
+
 __device__ __forceinline__ void put_split(float* tile, int half, int off, float x)
 {
     uint32_t hi, lo;
@@ -150,6 +173,16 @@ __device__ __forceinline__ void put_split16(float* tile, int off, float x, int h
     unsigned char* b = reinterpret_cast<unsigned char*>(tile);
     *reinterpret_cast<uint16_t*>(b + off) = (uint16_t)h;
     *reinterpret_cast<uint16_t*>(b + 4 * half + off) = (uint16_t)l;
+}
+
+// x0, x1 at consecutive K (x0 even) as one 4-byte word of bf16 hi at byte offset off and one of lo.
+__device__ __forceinline__ void put_split16x2(float* tile, int off, float x0, float x1, int half)
+{
+    uint32_t h, l;
+    tc::split_bf16x2(x0, x1, h, l);
+    unsigned char* b = reinterpret_cast<unsigned char*>(tile);
+    *reinterpret_cast<uint32_t*>(b + off) = h;
+    *reinterpret_cast<uint32_t*>(b + 4 * half + off) = l;
 }
 
 // The same in kind::f16 with bf16 operands: K = 16 slices, A in TMEM two K elements per column.
@@ -350,6 +383,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     uint64_t* bar_dm = bars + 4;   // dM
     uint64_t* bar_dd = bars + 5;   // dDelta, dY rows
     uint64_t* bar_kda = bars + 6;  // KDA: q, k, g rows, gamma and R tiles for step (9)
+    uint64_t* bar_park = bars + 7; // the successor state's product (scalar gate)
     __shared__ uint32_t s_tmem;
     __shared__ int s_err;
     __shared__ int s_armed;        // bit b: bars[b] waits for bulk copies
@@ -372,6 +406,9 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     const long long tok0 = (long long)n * A.T + t0;
     // the next chunk of this segment takes its entry state from this CTA (M_N below)
     const bool park_next = A.grad_loc >= 0 && t0 + BC < min(A.T, seg * A.C + A.C);
+    // the next place's launch may place its CTAs as soon as every CTA of this one has started:
+    // they run their independent loads in this launch's tail and wait for its parks
+    tc::grid_dep_launch();
 
     if (tid == 0) {
         tc::mbar_init(bar_ld, 1);
@@ -381,6 +418,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         tc::mbar_init(bar_dm, 1);
         tc::mbar_init(bar_dd, 1);
         tc::mbar_init(bar_kda, 1);
+        tc::mbar_init(bar_park, 1);
         tc::mbar_fence_init();
         s_err = 0;
         s_armed = 0;
@@ -395,20 +433,6 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     const bool m_unit = loc > 0;  // M: a parked state (unit layout) or the row-major checkpoint
     if (issuer)  // see tc::prefetch_l2 (measured 0.95 vs 1.08 ms per launch at the bench size)
         tc::prefetch_l2(A.q + (long long)(n / A.rep) * A.qs0 + (long long)t0 * A.qs1 + (long long)hk * A.qs2);
-    if (warp == 8) {  // M into R2 by the bulk-copy engine: 32 padded runs, or 128 padded rows
-        if (lane == 0) {
-            s_armed = (1 << 0) | (1 << 3);
-            tc::mbar_expect_tx(bar_m, kBytesState);
-        }
-        __syncwarp();
-        if (m_unit) {
-            tc::bulk_g2s(sM + lane * kLdU, A.ws + A.o_Mc + ch * (long long)(TD * TD) + lane * 4 * TD,
-                         sizeof(float) * 4 * TD, bar_m);
-        } else {
-            const float* ck0 = A.ckpt + (head * A.n_ck + seg) * (long long)(TD * TD);
-            for (int r = lane; r < TD; r += 32) tc::bulk_g2s(sM + r * kLdM, ck0 + r * TD, sizeof(float) * TD, bar_m);
-        }
-    }
     if (issuer) {
         tc::mbar_expect_tx(bar_ld, kBytesKb + (KDA ? kBytesFacKda + (uint32_t)sizeof(float) * TD : kBytesFac) + kBytesGR);
         if (KDA)  // D_X = M (K (.) gamma)^T
@@ -427,6 +451,21 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         tc::bulk_g2s(sm + kSGam, A.ws + A.o_gam + ch * BC, sizeof(float) * BC, bar_ld);
         tc::bulk_g2s(sm + kSR, A.ws + A.o_r + ch * BC, sizeof(float) * BC, bar_ld);
     }
+    if (warp == 8) {  // M into R2 by the bulk-copy engine: 32 padded runs, or 128 padded rows
+        if (lane == 0) {
+            s_armed = (1 << 0) | (1 << 3);
+            tc::mbar_expect_tx(bar_m, kBytesState);
+        }
+        __syncwarp();
+        if (m_unit) {
+            tc::grid_dep_wait();  // the park is written by the preceding launch
+            tc::bulk_g2s(sM + lane * kLdU, A.ws + A.o_Mc + ch * (long long)(TD * TD) + lane * 4 * TD,
+                         sizeof(float) * 4 * TD, bar_m);
+        } else {
+            const float* ck0 = A.ckpt + (head * A.n_ck + seg) * (long long)(TD * TD);
+            for (int r = lane; r < TD; r += 32) tc::bulk_g2s(sM + r * kLdM, ck0 + r * TD, sizeof(float) * TD, bar_m);
+        }
+    }
     const float* sGam = sm + kSGam;
     const float* sR = sm + kSR;
     float* sB = sm + kSB;
@@ -437,6 +476,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     //     on M, go out while the copy is in flight.
     uint32_t ph = 0;
     bool mma_out = false;  // issuer: a committed MMA group not yet seen complete, phase ph_out
+    bool park_out = false; // issuer: the successor state's product committed to bar_park
     uint32_t ph_out = 0;
     bool ok = true;
     float vx[32], dy[16];
@@ -455,6 +495,9 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             const bool real = tid < nb;
             sB[tid] = real ? __ldg(A.beta + (tok0 + tid) * A.H_v + h) : 0.f;
         }
+        // a park is written by the preceding launch: this thread reads it (here through shared
+        // memory, in (10) from global memory) only after that launch has completed
+        if (m_unit) tc::grid_dep_wait();
         if (!tc::mbar_wait(bar_m, 0)) s_err = 1;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -565,8 +608,15 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         for (int e = 0; e < 16; ++e) {
             const int t = tb + e;
             float acc = 0.f;
+            const float4* tr = reinterpret_cast<const float4*>(sT + t * BC);  // T row t, broadcast
 #pragma unroll
-            for (int k = 0; k < BC; ++k) acc = __fmaf_rn(sT[t * BC + k], x[k], acc);
+            for (int k4 = 0; k4 < BC / 4; ++k4) {
+                const float4 w = tr[k4];
+                acc = __fmaf_rn(w.x, x[4 * k4], acc);
+                acc = __fmaf_rn(w.y, x[4 * k4 + 1], acc);
+                acc = __fmaf_rn(w.z, x[4 * k4 + 2], acc);
+                acc = __fmaf_rn(w.w, x[4 * k4 + 3], acc);
+            }
             put_split16(b34, padoff16(t, row), acc);
             put_split16(b34, padoff16(BC + t, row), hc ? x[16 + e] : x[e]);
             rd[e] = __fmul_rn(sR[t], acc);
@@ -671,6 +721,26 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
     //     thread's tokens read from the [Q^T | K^T] tile (bf16 hi + lo: 16 significant bits); then
     //     A = [dY ; dDelta ; 0] (rows t)
     float d3[16];
+    if (!KDA && issuer && park_next) {
+        // the next chunk's entry state: D_N = (r Delta)^T K (A = (r Delta)^T from (3), K from the
+        // k-slices 2, 3 of [Q^T | K^T]), beside the sums below and the 32 x 32 algebra (columns
+        // 128.. have been free since (4))
+        if (!tc::mbar_wait(bar_qkt, 0)) {
+            s_err = 1;
+        } else {
+            const uint64_t qhi = tc::tile_desc(sm + kR2, TD), qlo = tc::tile_desc(sm + kR2 + BC * TD, TD);
+            const uint32_t id128 = tc::idesc_bf16(128);
+#pragma unroll
+            for (int s = 0; s < BC / 16; ++s) {
+                const uint64_t b_h = tc::desc_kslice(qhi, TD, s + BC / 16), b_l = tc::desc_kslice(qlo, TD, s + BC / 16);
+                tc::mma_ts16(tmem + kCN, tmem + kCNA + 8 * s, b_h, id128, s > 0);
+                tc::mma_ts16(tmem + kCN, tmem + kCNA + 8 * s, b_l, id128, 1);
+                tc::mma_ts16(tmem + kCN, tmem + kCNA + 16 + 8 * s, b_h, id128, 1);
+            }
+            tc::commit(bar_park);
+            park_out = true;
+        }
+    }
     if (compute) {
         if (!tc::mbar_wait(bar_dd, 0) || !tc::mbar_wait(bar_qkt, 0)) s_err = 1;
         if (KDA) {  // d3 = (K (.) R)'s gradient, kept for step (9); the gate sums come there
@@ -687,6 +757,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             constexpr int kLo = BC * TD / 4;  // lo half of the tile, in 16-byte units
             auto lo16 = [](uint32_t w) { return __uint_as_float(w << 16); };
             auto hi16 = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
+            float gs[32];  // this thread's terms of the 16 + 16 sums over rows i
 #pragma unroll
             for (int cq = 0; cq < 2; ++cq) {
                 const int kq = (tb >> 3) + cq, kk = BC / 8 + kq;
@@ -705,14 +776,12 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int x = 8 * cq + e;
-                    const float g1 = warp_sum(__fmaf_rn(kv[e], dk[x], __fmul_rn(qv[e], dq[x])));
-                    const float g2 = warp_sum(__fmul_rn(kv[e], d3[x]));
-                    if (lane == 0) {
-                        red[(warp & 3) * 96 + tb + x] = g1;
-                        red[(warp & 3) * 96 + BC + tb + x] = g2;
-                    }
+                    gs[x] = __fmaf_rn(kv[e], dk[x], __fmul_rn(qv[e], dq[x]));
+                    gs[16 + x] = __fmul_rn(kv[e], d3[x]);
                 }
             }
+            warp_reduce_scatter<32>(gs, lane);  // lane l: sum l (l < 16: g1 of token tb + l, else g2)
+            red[(warp & 3) * 96 + (lane < 16 ? tb + lane : BC + tb + lane - 16)] = gs[0];
         }
         const int quarter = warp & 3;
         const float* gyr = A.gy + (long long)n * A.gys0 + (long long)(t0 + lane) * A.gys1 + (long long)h * A.gys2 + 64 * hc;
@@ -774,9 +843,14 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             for (int w = 0; w < 4; ++w) v = __fadd_rn(v, __fadd_rn(red[w * 96 + 64], red[w * 96 + 65]));
             vec[4 * BC] = v;
         }
-        // Z into an LDF tile (operand of two small products)
+        // Z and Z diag(beta) into LDF tiles (operands of the two small products)
         float* Zs = sm + kAZ;
-        for (int idx = tid; idx < BC * BC; idx += 256) Zs[(idx >> 5) * LDF + (idx & 31)] = sm[kSZ + idx];
+        float* Zb = sm + kAZb;
+        for (int idx = tid; idx < BC * BC; idx += 256) {
+            const float z = sm[kSZ + idx];
+            Zs[(idx >> 5) * LDF + (idx & 31)] = z;
+            Zb[(idx >> 5) * LDF + (idx & 31)] = __fmul_rn(z, sB[idx & 31]);
+        }
     }
     ok = tc::mbar_wait(bar_mma, ph);
     if (issuer && ok) mma_out = false;
@@ -821,37 +895,28 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         float* dG = vec + 2 * BC;
         float* dbs = vec + 3 * BC;
         const float dot = vec[4 * BC];
-        if (warp == 0 || warp == 1) {
-            float v[32];
-            tc::ld32(tc::taddr(tmem, warp, kC4 + BC * warp), v);
+        const float* Zb = sm + kAZb;
+        if ((warp & 3) < 2) {  // warps 0, 1, 4, 5: TMEM lanes 0..63, 16 of the 32 columns each
+            const int blk = warp & 1, c0 = 16 * (warp >> 2);
+            float v[16];
+            tc::ld16(tc::taddr(tmem, warp, kC4 + BC * blk + c0), v);
             tc::wait_ld();
             const int t = lane;
 #pragma unroll
-            for (int tau = 0; tau < BC; ++tau) {
-                if (warp == 0)
-                    Ps[t * LDF + tau] = (tau <= t) ? __fmul_rn(A.scale, v[tau]) : 0.f;
+            for (int e = 0; e < 16; ++e) {
+                const int tau = c0 + e;
+                if (blk == 0)
+                    Ps[t * LDF + tau] = (tau <= t) ? __fmul_rn(A.scale, v[e]) : 0.f;
                 else
-                    dTs[t * LDF + tau] = (tau <= t) ? v[tau] : 0.f;
+                    dTs[t * LDF + tau] = (tau <= t) ? v[e] : 0.f;
             }
         }
         tc::bar_sync_first(256);
-        // dZ = dT diag(beta); dbeta_a[tau] = sum_t Z[t][tau] dT[t][tau]
-        for (int idx = tid; idx < BC * BC; idx += 256) {
-            const int t = idx >> 5, tau = idx & 31;
-            W1[t * LDF + tau] = __fmul_rn(dTs[t * LDF + tau], bs[tau]);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {  // warp w: columns 4 w .. 4 w + 3, lanes over t
-            const int tau = 4 * warp + q;
-            const float s = warp_sum(__fmul_rn(Zs[lane * LDF + tau], dTs[lane * LDF + tau]));
-            if (lane == 0) dbs[tau] = s;
-        }
-        tc::bar_sync_first(256);
-        {  // P1 = dZ Z^T
+        {  // P1 = dZ Z^T with dZ = dT diag(beta): the rows of dT against those of Z diag(beta)
             using Map = GemmMap<BC, BC, 2, 2, true>;
             float acc[2][2];
             zero_acc(acc);
-            block_gemm<BC, BC, 2, 2, false, true>(acc, W1, LDF, Zs, LDF, BC, tid);
+            block_gemm<BC, BC, 2, 2, false, true>(acc, dTs, LDF, Zb, LDF, BC, tid);
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -872,7 +937,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         }
         tc::bar_sync_first(256);
         // dL = beta_t dA; dKK = dL (.) Dm; dD = dQKD (.) QK + dL (.) KK (+ dr on the last row);
-        // the E = dD (.) Dm sums give the gate gradient
+        // the E = dD (.) Dm sums give the gate gradient (E into W2: P1 is dead)
         for (int idx = tid; idx < BC * BC; idx += 256) {
             const int t = idx >> 5, tau = idx & 31;
             const float dA = W1[t * LDF + tau];
@@ -887,26 +952,34 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
             if (t == BC - 1) dD = __fadd_rn(dD, dr[tau]);
             Ss[t * LDF + tau] = __fmul_rn(dL, dm);
             Ps[t * LDF + tau] = __fmul_rn(Ps[t * LDF + tau], dm);
-            dTs[t * LDF + tau] = __fmul_rn(dD, dm);
+            W2[t * LDF + tau] = __fmul_rn(dD, dm);
         }
         tc::bar_sync_first(256);
+        {  // warp w, t = 4 w + q: dbeta_a[t] = sum_t' Z[t'][t] dT[t'][t] and dbeta_b[t] = sum_tau
+           // dA (KK, or Dm (.) KK); the scalar gate also the row and column sums of E
+            float sv[16];
 #pragma unroll
-        for (int q = 0; q < 4 && KDA; ++q) {  // dbeta_b[t] = sum_tau dA Akk
-            const int t = 4 * warp + q, tau = lane;
-            const float bb = warp_sum(__fmul_rn(W1[t * LDF + tau], KKm[t * BC + tau]));
-            if (lane == 0) dbs[t] = __fadd_rn(dbs[t], bb);
-        }
-#pragma unroll
-        for (int q = 0; q < 4 && !KDA; ++q) {  // warp w: rows t = 4 w .. 4 w + 3, lanes over tau
-            const int t = 4 * warp + q, tau = lane;
-            const float rs = warp_sum(dTs[t * LDF + tau]);
-            const float cs = warp_sum(dTs[tau * LDF + t]);
-            const float bb = warp_sum(__fmul_rn(W1[t * LDF + tau], __fmul_rn(Dm[t * BC + tau], KKm[t * BC + tau])));
-            if (lane == 0) {
-                float g = gdg[t];
-                if (t == BC - 1) g = __fmaf_rn(sGam[t], dot, g);
-                dG[t] = __fadd_rn(__fadd_rn(g, rs), -cs);
-                dbs[t] = __fadd_rn(dbs[t], bb);
+            for (int q = 0; q < 4; ++q) {
+                const int t = 4 * warp + q, tau = lane;
+                const float dA = W1[t * LDF + tau];
+                sv[4 * q] = __fmul_rn(Zs[tau * LDF + t], dTs[tau * LDF + t]);
+                sv[4 * q + 1] = KDA ? __fmul_rn(dA, KKm[t * BC + tau])
+                                    : __fmul_rn(dA, __fmul_rn(Dm[t * BC + tau], KKm[t * BC + tau]));
+                sv[4 * q + 2] = KDA ? 0.f : W2[t * LDF + tau];
+                sv[4 * q + 3] = KDA ? 0.f : W2[tau * LDF + t];
+            }
+            warp_reduce_scatter<16>(sv, lane);  // lane l: sum l / 2, i.e. lane 8 q + 2 k: sum k of t = 4 w + q
+            const float bb = __shfl_down_sync(0xffffffffu, sv[0], 2);
+            const float rs = __shfl_down_sync(0xffffffffu, sv[0], 4);
+            const float cs = __shfl_down_sync(0xffffffffu, sv[0], 6);
+            if ((lane & 7) == 0) {
+                const int t = 4 * warp + (lane >> 3);
+                dbs[t] = __fadd_rn(sv[0], bb);
+                if (!KDA) {
+                    float g = gdg[t];
+                    if (t == BC - 1) g = __fmaf_rn(sGam[t], dot, g);
+                    dG[t] = __fadd_rn(__fadd_rn(g, rs), -cs);
+                }
             }
         }
         tc::bar_sync_first(256);
@@ -929,12 +1002,15 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         // S is the symmetric dKK + dKK^T of its strict lower part
         float* bp = sm + kABP;
         float* bps = sm + kABPS;
-        for (int idx = tid; idx < BC * BC && !KDA; idx += 256) {
-            const int t = idx & 31, tau = idx >> 5;  // consecutive threads: consecutive rows t
-            const float s = (tau > t) ? Ss[tau * LDF + t] : (tau < t ? Ss[t * LDF + tau] : 0.f);
-            put_split16(bp, padoff16(t, tau, kLbo32), Ps[t * LDF + tau], kTP);
-            put_split16(bps, padoff16(t, tau, kLbo32), Ps[tau * LDF + t], kTPS);
-            put_split16(bps, padoff16(t, BC + tau, kLbo32), s, kTPS);
+        auto S_at = [&](int a, int b) {  // S[a][b] from the strict lower part
+            return (b > a) ? Ss[b * LDF + a] : (b < a ? Ss[a * LDF + b] : 0.f);
+        };
+        for (int idx = tid; idx < BC * BC / 2 && !KDA; idx += 256) {
+            const int t = idx & 31, tau = 2 * (idx >> 5);  // consecutive threads: consecutive rows t
+            const float2 p = *reinterpret_cast<const float2*>(Ps + t * LDF + tau);
+            put_split16x2(bp, padoff16(t, tau, kLbo32), p.x, p.y, kTP);
+            put_split16x2(bps, padoff16(t, tau, kLbo32), Ps[tau * LDF + t], Ps[(tau + 1) * LDF + t], kTPS);
+            put_split16x2(bps, padoff16(t, BC + tau, kLbo32), S_at(t, tau), S_at(t, tau + 1), kTPS);
         }
     }
     tc::fence_async_smem();
@@ -991,20 +1067,23 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
                 tc::mma_ss16(tmem + kC2 + BC, a_h, slo + off, id32, 1);
                 tc::mma_ss16(tmem + kC2 + BC, a_l, shi + off, id32, 1);
             }
-            if (park_next) {  // M_N = (r Delta)^T K, K from the k-slices 2, 3 of [Q^T | K^T]
-                const uint32_t id128 = tc::idesc_bf16(128);
-#pragma unroll
-                for (int s = 0; s < BC / 16; ++s) {
-                    const uint64_t b_h = tc::desc_kslice(qhi, TD, s + BC / 16), b_l = tc::desc_kslice(qlo, TD, s + BC / 16);
-                    tc::mma_ts16(tmem + kCN, tmem + kCNA + 8 * s, b_h, id128, s > 0);
-                    tc::mma_ts16(tmem + kCN, tmem + kCNA + 8 * s, b_l, id128, 1);
-                    tc::mma_ts16(tmem + kCN, tmem + kCNA + 16 + 8 * s, b_h, id128, 1);
-                }
-            }
-            tc::commit(bar_mma);
+            tc::commit(bar_mma);  // (and the successor state's product, issued in (6))
             mma_out = true;
             ph_out = ph;
         }
+    }
+    // the park's gamma_last M term: M is read again from where (0) got it (L2 still holds it),
+    // into registers while the products of (9) run
+    const float4* msrc;  // (no initialisers here: the error exits jump past this point)
+    int sstride;
+    float4 mpre[KDA ? 1 : 16];
+    msrc = m_unit
+        ? reinterpret_cast<const float4*>(A.ws + A.o_Mc + ch * (long long)(TD * TD)) + 16 * hc * TD + row
+        : reinterpret_cast<const float4*>(A.ckpt + (head * A.n_ck + seg) * (long long)(TD * TD) + row * TD + 64 * hc);
+    sstride = m_unit ? TD : 1;
+    if (!KDA && compute && park_next) {
+#pragma unroll
+        for (int u = 0; u < (KDA ? 1 : 16); ++u) mpre[u] = __ldg(msrc + u * sstride);
     }
     ok = tc::mbar_wait(bar_mma, ph);
     if (issuer && ok) mma_out = false;
@@ -1028,12 +1107,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         if (park_next) {
             // the next chunk's entry state M_N = gamma_last M + (r Delta)^T K, row `row`, this
             // thread's 64 columns, parked in the unit layout (a warp writes 512-byte runs).
-            // M is read again from where (0) got it (L2 still holds it).
             const float gl = sGam[BC - 1];
-            const float4* src = m_unit
-                ? reinterpret_cast<const float4*>(A.ws + A.o_Mc + ch * (long long)(TD * TD)) + 16 * hc * TD + row
-                : reinterpret_cast<const float4*>(A.ckpt + (head * A.n_ck + seg) * (long long)(TD * TD) + row * TD + 64 * hc);
-            const int sstride = m_unit ? TD : 1;
             float4* dst = reinterpret_cast<float4*>(A.ws + A.o_Mc + (ch + 1) * (long long)(TD * TD)) + 16 * hc * TD + row;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -1043,7 +1117,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const int u = 8 * h2 + q;
-                    const float4 mo = __ldg(src + u * sstride);
+                    const float4 mo = KDA ? __ldg(msrc + u * sstride) : mpre[KDA ? 0 : u];
                     float4 gq = make_float4(gl, gl, gl, gl);
                     if (KDA)  // columns 4 u .. 4 u + 3 of this half decay by their own gamma_last
                         gq = *reinterpret_cast<const float4*>(sm + kSGl + 64 * hc + 4 * u);
@@ -1061,6 +1135,7 @@ done:
         // the products in flight must be done before the tensor memory is released; if they
         // are not, say so (bit 8: the tensor memory may be written after its release)
         if (mma_out && !tc::mbar_wait(bar_mma, ph_out)) atomicOr(&g_tcg_status, 1 << 8);
+        if (park_out && !tc::mbar_wait(bar_park, 0)) atomicOr(&g_tcg_status, 1 << 8);
         for (int b = 0; b < 7; ++b)  // let this CTA's bulk copies land before it exits
             if (s_armed & (1 << b)) tc::mbar_wait(bars + b, 0);
     }
@@ -1071,10 +1146,12 @@ done:
 }
 
 // dq, dk of each key head: the value heads' parts summed in ascending order (and, with the
-// sequence broadcast, the value sequences of each q/k sequence nq, ascending).
+// sequence broadcast, the value sequences of each q/k sequence nq, ascending); the chunks of
+// [c_lo, c_hi), or with grad_loc = k >= 0 those at place k of their segment.
 __global__ void __launch_bounds__(256) gdn_tc_dqdk_sum_kernel(const ChunkArgs A)
 {
-    const int c = A.c_lo + blockIdx.x, hk = blockIdx.y, nq = blockIdx.z;
+    const int c = A.grad_loc < 0 ? A.c_lo + blockIdx.x : (A.c_lo / A.cps + blockIdx.x) * A.cps + A.grad_loc;
+    const int hk = blockIdx.y, nq = blockIdx.z;
     const int seg = c / A.cps, loc = c - seg * A.cps;
     const int t0 = seg * A.C + loc * BC;
     const int nb = min(BC, min(A.T, seg * A.C + A.C) - t0);
@@ -1106,7 +1183,20 @@ static int launch_tc_grad_t(const ChunkArgs& a, cudaStream_t s)
     if (e) return e;
     const int units = tc_grad_units(a);
     if (units <= 0) return 0;
-    gdn_tc_grad_kernel<KDA><<<dim3(units, a.H_v, a.N), GT, kGSmemBytes, s>>>(a);
+    // A launch for place k > 0 follows the one for place k - 1 on the same stream and reads
+    // its parks only after griddepcontrol.wait: it may start in that launch's tail.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units, a.H_v, a.N);
+    cfg.blockDim = dim3(GT);
+    cfg.dynamicSmemBytes = kGSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = a.grad_loc > 0 ? 1 : 0;
+    e = (int)cudaLaunchKernelEx(&cfg, gdn_tc_grad_kernel<KDA>, a);
+    if (e) return e;
     return (int)cudaGetLastError();
 }
 
@@ -1129,8 +1219,9 @@ int tc_grad_units(const ChunkArgs& a)
 int launch_tc_dqdk_sum(const ChunkArgs& a, void* stream)
 {
     cudaStream_t s = (cudaStream_t)stream;
-    if (a.c_hi <= a.c_lo) return 0;
-    gdn_tc_dqdk_sum_kernel<<<dim3(a.c_hi - a.c_lo, a.H_k, a.N / a.rep), 256, 0, s>>>(a);
+    const int units = tc_grad_units(a);  // every chunk of [c_lo, c_hi), or those at place grad_loc
+    if (units <= 0) return 0;
+    gdn_tc_dqdk_sum_kernel<<<dim3(units, a.H_k, a.N / a.rep), 256, 0, s>>>(a);
     return (int)cudaGetLastError();
 }
 

@@ -78,8 +78,8 @@ def test_chunked_launch_count_with_several_chunks_per_segment():
     # C = 64 > 32-token chunks.  Head size 128 pipelines over chunk ranges: the forward
     # launches a prep and a state chain for each of 4 ranges; the backward launches, for
     # each of 2, a prep, a dM chain, one gradient launch per place of a chunk in its segment
-    # (the first parks the second's entry states) and a sum.  With timing events the
-    # backward runs 3 stages one after another.
+    # (the first parks the second's entry states) and a sum over value heads.  With timing
+    # events the backward runs 3 stages one after another.
     p = gdn.make_params(1, 4096, 16, 48, 128, False)
     assert gdn.checkpoint_interval(p) == 64
     assert gdn.launches(p) == (8, 10)
