@@ -187,6 +187,8 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="throughput of every sweep point (d x T x N x gate), one JSON line each")
+    ap.add_argument("--op", choices=["gdn", "ssm"], default="gdn",
+                    help="gdn: the gated delta rule (default); ssm: the selective scan (SSM_SCAN_BACK)")
     return ap.parse_args()
 
 
@@ -784,8 +786,195 @@ def check_device(stream, what):
         raise RuntimeError(f"device status {st} after {what}: {gdn.library().gdn_last_error().decode()}")
 
 
+# --------------------------------------------------------------------------- selective scan
+SSM_METRIC = "SSM scan fwd+bwd channel-tokens/s; % of FP32 roofline"
+SSM_UNIT = "channel-tokens/s"
+SSM_WORKLOAD = "mamba2_h80_T4096"
+# Algorithmic flops per state element and token (FMA = 2): forward 5 (s = a s + B (x dt): a
+# multiply and an FMA; y: an FMA); backward 13 (ds += dy C: 2; the dC and dB terms and their
+# sums over rows: 2 + 2; dx: 2; d(dt): B x, A a, an FMA with s_{t-1} and an FMA into the sum:
+# 4; ds = a ds: 1).  The walk's recompute of the states and the exps are not counted.
+SSM_FWD_FLOPS, SSM_BWD_FLOPS = 5, 13
+
+
+def ssm_compulsory_bytes(prob):
+    """Bytes a fwd+bwd step must move at least: x, dt, B, C read twice (forward, backward),
+    y written, dy, ds_T read, every gradient written, s0 read, s_T written, the checkpoints
+    written and read back."""
+    N, T, H, P, S, G = prob.N, prob.T, prob.H, prob.P, prob.S, prob.G
+    n_ck = max(1, -(-T // prob.K))
+    per_tok = 4 * (2 * H * P + 2 * H + 4 * G * S)          # x, dt, B, C twice
+    per_tok += 4 * (H * P + H * P + H * P + H + 2 * G * S)  # y; dy; dx, ddt, dB, dC
+    state = 4 * H * P * S
+    return N * (T * per_tok + state * (4 + 2 * n_ck))
+
+
+def ssm_cpu_baseline(prob, workload):
+    """The selective-scan oracle on the host cores: a sample of the workload's heads over all
+    of its tokens (forward + checkpointed walk), all cores (the forward runs a head per
+    thread; the walk a group per thread) and one core."""
+    import numpy as np
+    from oracle import ssm as oss
+    lib = oss.load()
+    threads = oss.max_threads(lib)
+    heads = list(range(min(prob.H, 4 if prob.P > 1 else 64)))
+    sub = {f: np.ascontiguousarray(getattr(prob, f)[:, :, heads]) for f in ("x", "dt", "dy")}
+    sub.update({f: np.ascontiguousarray(getattr(prob, f)[:, heads]) for f in ("s0", "ds_T")})
+    A = np.ascontiguousarray(prob.A[heads])
+    # the sample keeps one group, with every group's B and C rows (heads of one group)
+    B, C = np.ascontiguousarray(prob.B[:, :, :1]), np.ascontiguousarray(prob.C[:, :, :1])
+    runs = []
+    for nt in (threads, 1):
+        oss.set_threads(nt, lib)
+        t0 = time.perf_counter()
+        y, sT, ck = oss.forward(sub["s0"], sub["x"], sub["dt"], A, B, C, K=prob.K, lib=lib)
+        oss.backward(sub["s0"], sub["x"], sub["dt"], A, B, C, sub["dy"], sub["ds_T"], K=prob.K, ckpt=ck, lib=lib)
+        dt = time.perf_counter() - t0
+        runs.append({"threads": nt, "seconds": round(dt, 3),
+                     "channel_tokens_per_s": prob.N * prob.T * len(heads) * prob.P / dt})
+    oss.set_threads(threads, lib)
+    return {"value": runs[0]["channel_tokens_per_s"], "unit": SSM_UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"heads 0..{len(heads) - 1} of {workload} ({len(heads) * prob.P} of its {prob.H * prob.P} "
+                      f"channels) over all {prob.T} tokens, forward + checkpointed walk, float64: "
+                      f"{runs[0]['seconds']:.2f} s wall on {threads} threads, {runs[1]['seconds']:.2f} s on 1",
+            "nproc": os.cpu_count(), "omp_threads": threads, "cpu_model": _cpu_model(), "runs": runs}
+
+
+def run_ssm(args):
+    """The selective scan: ssm_forward + ssm_backward per step on one synthetic batch."""
+    import numpy as np
+    import torch
+    from gated_delta_rule_backward_gb300 import ssm
+    from gated_delta_rule_backward_gb300.ssm_synth import ssm_workload
+
+    rank, world, local = _dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = args.workload if args.workload != WORKLOAD else SSM_WORKLOAD
+    prob = ssm_workload(wl)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    s0, x, dt, A, B, C, dy, dsT = map(t, (prob.s0, prob.x, prob.dt, prob.A, prob.B, prob.C, prob.dy, prob.ds_T))
+    p = ssm.params_for(x, A, B, K=prob.K)
+    out = torch.empty(ssm.packed_out_elems(p), device=dev)
+    ck = torch.empty((p.N, p.H, ssm.num_checkpoints(p), p.P, p.S), device=dev)
+    gin = ssm.pack_grad_in(p, dy, dsT)
+    gout = torch.empty(ssm.packed_grad_elems(p), device=dev)
+    ws = torch.empty(max(ssm.backward_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(xx=x, dtt=dt, BB=B, CC=C, s00=s0, gi=gin, o=out, go=gout):
+        ssm.ssm_forward(p, s00, xx, dtt, A, BB, CC, o, ck, stream)
+        ssm.ssm_backward(p, xx, dtt, A, BB, CC, ck, gi, go, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    sev = [(mk(), mk(), mk()) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()
+        e0, e1, e2 = sev[i]
+        e0.record(stream)
+        ssm.ssm_forward(p, s0, x, dt, A, B, C, out, ck, stream)
+        e1.record(stream)
+        ssm.ssm_backward(p, x, dt, A, B, C, ck, gin, gout, ws, stream)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    check_device(stream, "the timed steps")
+    fwd_ms = sum(a.elapsed_time(b) for a, b, _ in sev) / args.steps
+    bwd_ms = sum(b.elapsed_time(c) for _, b, c in sev) / args.steps
+    step_ms = sum(a.elapsed_time(c) for a, _, c in sev) / args.steps
+    if dist:
+        step_ms = max_over_ranks(step_ms, dist, dev)
+    ch_tok = prob.N * prob.T * prob.H * prob.P
+    value = world * ch_tok / (step_ms * 1e-3)
+
+    e2e = None
+    if not args.no_e2e:
+        # through the same calls with every step's inputs uploaded from pinned host memory and
+        # its outputs (the packed forward output and the packed gradients) downloaded
+        names_in = ("s0", "x", "dt", "B", "C")
+        host = {nm: torch.from_numpy(np.ascontiguousarray(getattr(prob, nm))).pin_memory() for nm in names_in}
+        host["gin"] = gin.cpu().pin_memory()
+        d_in = {nm: torch.empty(h.shape, device=dev) for nm, h in host.items()}
+        out_h, gout_h = torch.empty(out.shape).pin_memory(), torch.empty(gout.shape).pin_memory()
+        h2d = sum(h.numel() * 4 for h in host.values())
+        d2h = (out.numel() + gout.numel()) * 4
+        a, b = mk(), mk()
+        k_e2e = max(3, args.steps)
+        a.record(stream)
+        for _ in range(k_e2e):
+            for nm, h in host.items():
+                d_in[nm].copy_(h, non_blocking=True)
+            step(d_in["x"], d_in["dt"], d_in["B"], d_in["C"], d_in["s0"], d_in["gin"])
+            out_h.copy_(out, non_blocking=True)
+            gout_h.copy_(gout, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / k_e2e
+        e2e = {"value": world * ch_tok / (e2e_ms * 1e-3), "unit": SSM_UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "overlap": "none (copies in stream order)"}
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peak32, sms, mhz, peak32_src = fp32_peak(dev)
+    hbm, hbm_src = hbm_peak_gbs()
+    flops = (SSM_FWD_FLOPS + SSM_BWD_FLOPS) * ch_tok * prob.S
+    tflops = flops / (step_ms * 1e-3) / 1e12
+    comp = ssm_compulsory_bytes(prob)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = ssm_cpu_baseline(prob, wl)
+    line = {
+        "metric": SSM_METRIC, "value": value, "unit": SSM_UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl, "N": prob.N, "T": prob.T, "H": prob.H, "P": prob.P, "S": prob.S,
+                   "G": prob.G, "decay": "per state (Mamba-1)" if prob.mamba1 else "per head (Mamba-2)",
+                   "K": prob.K, "arithmetic": "fp32 FP32-pipe, expf",
+                   "l2": "flushed between timed steps (256 MiB write outside the events)"},
+        "roofline": {"bound": "alu", "kernel": "whole step: ssm_forward + ssm_backward",
+                     "achieved": tflops, "peak": peak32, "unit": "TFLOP/s", "frac": tflops / peak32,
+                     "traffic": None, "flops_per_launch": flops, "launch_ms": step_ms,
+                     "flops_per_state_token": SSM_FWD_FLOPS + SSM_BWD_FLOPS,
+                     "compulsory_bytes_per_launch": comp, "hbm_floor_ms": comp / (hbm * 1e9) * 1e3,
+                     "fp32_floor_ms": flops / (peak32 * 1e12) * 1e3, "sm_count": sms, "peak_source": peak32_src,
+                     "hbm_peak_gbs": hbm, "hbm_peak_source": hbm_src, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                     "workspace_bytes": ws.numel()},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def main():
     args = _args()
+    if args.op == "ssm":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the selective scan's reference arm is "
+                              "the oracle timed by this line's cpu_baseline"}), flush=True)
+            return
+        run_ssm(args)
+        return
     if args.sweep:
         run_sweep(args)
         return
