@@ -10,7 +10,9 @@
 // row-local except the outputs dB, dC (sums over the rows of a group) and ddt (a sum over
 // the rows of a head), so a thread owns 16 columns of one row, the NSL = S / 16 threads of a
 // row sit in adjacent lanes, a warp holds RPW = 32 / NSL rows and a CTA of W warps RPC = W RPW
-// rows, all in one group.  Row sums run over lanes with shuffles, over warps in shared
+// rows, all in one group.  The columns of lane ns are four runs of four, j = 4 (ns + NSL q) + r
+// (q, r < 4): the lanes of a row read a token's B and C, and a state row, as consecutive
+// 16-byte units (no shared-memory bank conflicts, coalesced global accesses).  Row sums run over lanes with shuffles, over warps in shared
 // memory (fixed order), and over a group's CTAs in ssm_reduce_kernel (fixed order); nothing
 // uses atomics.
 //
@@ -50,6 +52,33 @@ struct Args {
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
+// Column of a thread's value e (e < 16) for lane slot ns: four runs of four.
+template <int NSL>
+__device__ __forceinline__ int col_of(int ns, int e) { return 4 * (ns + NSL * (e >> 2)) + (e & 3); }
+
+// A thread's 16 values of a state row (row base `r`, 16-byte aligned) as four float4 loads.
+template <int NSL>
+__device__ __forceinline__ void load_row16(float (&v)[SL], const float* r, int ns)
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 x = ld4(r + 4 * (ns + NSL * q));
+        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+    }
+}
+template <int NSL>
+__device__ __forceinline__ void store_row16(float* r, const float (&v)[SL], int ns)
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) st4(r + 4 * (ns + NSL * q), make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+}
+// A token's 16 values of a row vector in shared memory (B or C), the same columns.
+template <int NSL>
+__device__ __forceinline__ void load_vec16(float (&v)[SL], const float* r, int ns)
+{
+    load_row16<NSL>(v, r, ns);
+}
+
 // Sum of v over the NSL lanes of a row (lanes differ in their low bits).
 template <int NSL>
 __device__ __forceinline__ float row_sum(float v)
@@ -61,8 +90,8 @@ __device__ __forceinline__ float row_sum(float v)
 
 // One token of the scan on a thread's 16 columns: s = a s + B (x dt).
 template <bool PS>
-__device__ __forceinline__ void scan_step(float (&s)[SL], const float* Bt, float xdt, float dtv, const float (&Av)[SL],
-                                          float a_head)
+__device__ __forceinline__ void scan_step(float (&s)[SL], const float (&Bt)[SL], float xdt, float dtv,
+                                          const float (&Av)[SL], float a_head)
 {
 #pragma unroll
     for (int e = 0; e < SL; ++e) {
@@ -88,8 +117,6 @@ __global__ void __launch_bounds__(256) ssm_fwd_kernel(const Args a)
     const long long h_lo = row0 / P;
     const int nh = (int)((row0 + RPC - 1) / P - h_lo + 1);
     const long long g = h_lo / (H / G);
-    const int j0 = ns * SL;
-
     extern __shared__ __align__(16) float sm[];
     float* sB = sm;                          // [kTT][S]
     float* sC = sB + kTT * S;                // [kTT][S]
@@ -100,19 +127,13 @@ __global__ void __launch_bounds__(256) ssm_fwd_kernel(const Args a)
 
     float Av[SL];
 #pragma unroll
-    for (int e = 0; e < SL; ++e) Av[e] = PS ? a.A[h * S + j0 + e] : a.A[h];
+    for (int e = 0; e < SL; ++e) Av[e] = PS ? a.A[h * S + col_of<NSL>(ns, e)] : a.A[h];
     float s[SL];
-    const float* s0r = a.s0 + ((n * H + h) * P + p) * S + j0;
-#pragma unroll
-    for (int q = 0; q < SL / 4; ++q) {
-        const float4 v = ld4(s0r + 4 * q);
-        s[4 * q] = v.x; s[4 * q + 1] = v.y; s[4 * q + 2] = v.z; s[4 * q + 3] = v.w;
-    }
-    float* ckr = a.ckpt + (((n * H + h) * a.n_ck) * P + p) * S + j0;  // + k P S per checkpoint
-    if (T == 0) {
-#pragma unroll
-        for (int q = 0; q < SL / 4; ++q) st4(ckr + 4 * q, make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]));
-    }
+    load_row16<NSL>(s, a.s0 + ((n * H + h) * P + p) * S, ns);
+    float* ckr = a.ckpt + (((n * H + h) * a.n_ck) * P + p) * S;  // + k P S per checkpoint
+    if (T == 0) store_row16<NSL>(ckr, s, ns);
+    int ck_next = 0;   // tokens to the next checkpoint
+    int ck_i = 0;      // its index
 
     for (long long t0 = 0; t0 < T; t0 += kTT) {
         const int nt = (int)std::min<long long>(kTT, T - t0);
@@ -135,20 +156,24 @@ __global__ void __launch_bounds__(256) ssm_fwd_kernel(const Args a)
         }
         __syncthreads();
         const int hk = (int)(h - h_lo);
+        const int Si = (int)S;
         for (int tt = 0; tt < nt; ++tt) {
-            const long long t = t0 + tt;
-            if (t % a.K == 0) {
-                float* ck = ckr + (t / a.K) * P * S;
-#pragma unroll
-                for (int q = 0; q < SL / 4; ++q) st4(ck + 4 * q, make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]));
+            if (ck_next == 0) {
+                store_row16<NSL>(ckr + (long long)ck_i * P * S, s, ns);
+                ck_next = a.K;
+                ++ck_i;
             }
+            --ck_next;
             const float dtv = sdt[tt * nh + hk];
             const float xdt = __fmul_rn(sx[tt * RPC + lrow], dtv);
-            scan_step<PS>(s, sB + tt * S + j0, xdt, dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
-            const float* Ct = sC + tt * S + j0;
-            float yp = 0.f;
+            float Bt[SL], Ct[SL];
+            load_vec16<NSL>(Bt, sB + tt * Si, ns);
+            load_vec16<NSL>(Ct, sC + tt * Si, ns);
+            scan_step<PS>(s, Bt, xdt, dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
+            float y4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < SL; ++e) yp = __fmaf_rn(s[e], Ct[e], yp);
+            for (int e = 0; e < SL; ++e) y4[e & 3] = __fmaf_rn(s[e], Ct[e], y4[e & 3]);
+            float yp = __fadd_rn(__fadd_rn(y4[0], y4[1]), __fadd_rn(y4[2], y4[3]));
             yp = row_sum<NSL>(yp);
             if (ns == 0) sy[tt * RPC + lrow] = yp;
         }
@@ -158,9 +183,9 @@ __global__ void __launch_bounds__(256) ssm_fwd_kernel(const Args a)
             a.y[(n * T + t0 + tt) * H * P + row0 + r] = sy[i];
         }
     }
-    float* sTr = a.sT + ((n * H + h) * P + p) * S + j0;  // (packed: 4-byte alignment only)
+    float* sTr = a.sT + ((n * H + h) * P + p) * S;  // (packed: 4-byte alignment only)
 #pragma unroll
-    for (int e = 0; e < SL; ++e) sTr[e] = s[e];
+    for (int e = 0; e < SL; ++e) sTr[col_of<NSL>(ns, e)] = s[e];
 }
 
 // ---------------------------------------------------------------------------------
@@ -181,13 +206,12 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
     const int nh = (int)((row0 + RPC - 1) / P - h_lo + 1);
     const long long g = h_lo / (H / G);
     const int hk = (int)(h - h_lo);
-    const int j0 = ns * SL;
     const long long rows_g = (H / G) * P;
     const int bg = (int)((row0 % rows_g) / RPC);              // this CTA among its group's
     const int bh = P >= RPC ? (int)((row0 % P) / RPC) : 0;    // this CTA among its head's
 
     extern __shared__ __align__(16) float sm[];
-    float* ring = sm;                                  // [kC2][NT][SL]
+    float* ring = sm;                                  // [kC2][4][NT] float4
     float* sB = ring + kC2 * NT * SL;                  // [kC2][S]
     float* sC = sB + kC2 * S;                          // [kC2][S]
     float* sx = sC + kC2 * S;                          // [kC2][RPC]
@@ -200,14 +224,28 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
 
     float Av[SL];
 #pragma unroll
-    for (int e = 0; e < SL; ++e) Av[e] = PS ? a.A[h * S + j0 + e] : a.A[h];
+    for (int e = 0; e < SL; ++e) Av[e] = PS ? a.A[h * S + col_of<NSL>(ns, e)] : a.A[h];
     float ds[SL];
     {
-        const float* d = a.dsT + ((n * H + h) * P + p) * S + j0;  // (packed: scalar loads)
+        const float* d = a.dsT + ((n * H + h) * P + p) * S;  // (packed: scalar loads)
 #pragma unroll
-        for (int e = 0; e < SL; ++e) ds[e] = d[e];
+        for (int e = 0; e < SL; ++e) ds[e] = d[col_of<NSL>(ns, e)];
     }
-    float* subr = a.sub + (((long long)blockIdx.y * gridDim.x + blockIdx.x) * a.nsub * NT + tid) * SL;
+    // sub-checkpoint k of this thread: float4 q at subr + 4 ((4 k + q) NT)
+    float* subr = a.sub + ((long long)blockIdx.y * gridDim.x + blockIdx.x) * a.nsub * NT * SL + 4 * tid;
+    auto put4 = [&](float* base, int k, const float (&v)[SL]) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            st4(base + 4 * ((4 * k + q) * NT), make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+    };
+    auto get4 = [&](float (&v)[SL], const float* base, int k) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 x = ld4(base + 4 * ((4 * k + q) * NT));
+            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+        }
+    };
+    float* ringr = ring + 4 * tid;
 
     // stage tokens [ts, te) of B (and C, x, dy when `all`), dt and (Mamba-2) a
     auto stage = [&](long long ts, int nt, bool all) {
@@ -238,63 +276,45 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
         if (t1 <= t0) continue;
         // level 1: the segment forward from its checkpoint; a sub-checkpoint every kC2 tokens
         float s[SL];
-        {
-            const float* ck = a.ckpt_in + (((n * H + h) * a.n_ck + seg) * P + p) * S + j0;
-#pragma unroll
-            for (int q = 0; q < SL / 4; ++q) {
-                const float4 v = ld4(ck + 4 * q);
-                s[4 * q] = v.x; s[4 * q + 1] = v.y; s[4 * q + 2] = v.z; s[4 * q + 3] = v.w;
-            }
-        }
+        load_row16<NSL>(s, a.ckpt_in + (((n * H + h) * a.n_ck + seg) * P + p) * S, ns);
         const int nsub = (int)((t1 - t0 + kC2 - 1) / kC2);
         for (int k = 0; k < nsub; ++k) {
             const long long ts = t0 + (long long)k * kC2;
             const int nt = (int)std::min<long long>(kC2, t1 - ts);
-            float* sb = subr + (long long)k * NT * SL;
-#pragma unroll
-            for (int q = 0; q < SL / 4; ++q) st4(sb + 4 * q, make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]));
+            put4(subr, k, s);
             if (k == nsub - 1) break;  // the last sub-segment's states come in level 2
             stage(ts, nt, false);
             for (int tt = 0; tt < nt; ++tt) {
                 const float dtv = sdt[tt * nh + hk];
-                scan_step<PS>(s, sB + tt * S + j0, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av,
-                              PS ? 0.f : sa[tt * nh + hk]);
+                float Bt[SL];
+                load_vec16<NSL>(Bt, sB + tt * (int)S, ns);
+                scan_step<PS>(s, Bt, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
             }
         }
         // level 2: sub-segments last first
         for (int k = nsub - 1; k >= 0; --k) {
             const long long ts = t0 + (long long)k * kC2;
             const int nt = (int)std::min<long long>(kC2, t1 - ts);
-            const float* sb = subr + (long long)k * NT * SL;
-#pragma unroll
-            for (int q = 0; q < SL / 4; ++q) {
-                const float4 v = ld4(sb + 4 * q);
-                s[4 * q] = v.x; s[4 * q + 1] = v.y; s[4 * q + 2] = v.z; s[4 * q + 3] = v.w;
-            }
+            get4(s, subr, k);
             stage(ts, nt, true);
-            for (int tt = 0; tt < nt; ++tt) {  // ring[tt]: the state entering token ts + tt
-                float* rg = ring + ((long long)tt * NT + tid) * SL;
-#pragma unroll
-                for (int q = 0; q < SL / 4; ++q) st4(rg + 4 * q, make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]));
+            for (int tt = 0; tt < nt; ++tt) {  // ring slot tt: the state entering token ts + tt
+                put4(ringr, tt, s);
                 const float dtv = sdt[tt * nh + hk];
-                scan_step<PS>(s, sB + tt * S + j0, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av,
-                              PS ? 0.f : sa[tt * nh + hk]);
+                float Bt[SL];
+                load_vec16<NSL>(Bt, sB + tt * (int)S, ns);
+                scan_step<PS>(s, Bt, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
             }
             // s is now the state after the sub-segment's last token
             for (int tt = nt - 1; tt >= 0; --tt) {
                 float sp[SL];  // the state entering the token
-                const float* rg = ring + ((long long)tt * NT + tid) * SL;
-#pragma unroll
-                for (int q = 0; q < SL / 4; ++q) {
-                    const float4 v = ld4(rg + 4 * q);
-                    sp[4 * q] = v.x; sp[4 * q + 1] = v.y; sp[4 * q + 2] = v.z; sp[4 * q + 3] = v.w;
-                }
+                get4(sp, ringr, tt);
                 const float dtv = sdt[tt * nh + hk];
                 const float a_head = PS ? 0.f : sa[tt * nh + hk];
                 const float xv = sx[tt * RPC + lrow], dyv = sdy[tt * RPC + lrow];
                 const float xdt = __fmul_rn(xv, dtv);
-                const float* Bt = sB + tt * S + j0;
-                const float* Ct = sC + tt * S + j0;
+                float Bt[SL], Ct[SL];
+                load_vec16<NSL>(Bt, sB + tt * (int)S, ns);
+                load_vec16<NSL>(Ct, sC + tt * (int)S, ns);
                 float v[NV];
                 float dxp = 0.f, ddtp = 0.f;
 #pragma unroll
@@ -333,7 +353,7 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
 #pragma unroll
                 for (int i = 0; i < NH; ++i) {
                     const int idx = base + i;
-                    wp[idx < SL ? j0 + idx : S + j0 + idx - SL] = v[i];
+                    wp[idx < SL ? col_of<NSL>(ns, idx) : (int)S + col_of<NSL>(ns, idx - SL)] = v[i];
                 }
             }
             __syncthreads();
@@ -364,9 +384,7 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
             }
         }
     }
-    float* d0 = a.ds0 + ((n * H + h) * P + p) * S + j0;
-#pragma unroll
-    for (int q = 0; q < SL / 4; ++q) st4(d0 + 4 * q, make_float4(ds[4 * q], ds[4 * q + 1], ds[4 * q + 2], ds[4 * q + 3]));
+    store_row16<NSL>(a.ds0 + ((n * H + h) * P + p) * S, ds, ns);
 }
 
 // dB, dC: each group's CTA partials summed in ascending order; ddt: each head's.
