@@ -8,11 +8,12 @@
 // Rows and columns.  The state of one sequence is a matrix with a row per (head, channel)
 // pair, row = h P + p, and a column per state index j.  Every term of the recurrence is
 // row-local except the outputs dB, dC (sums over the rows of a group) and ddt (a sum over
-// the rows of a head), so a thread owns 16 columns of one row, the NSL = S / 16 threads of a
-// row sit in adjacent lanes, a warp holds RPW = 32 / NSL rows and a CTA of W warps RPC = W RPW
-// rows, all in one group.  The columns of lane ns are four runs of four, j = 4 (ns + NSL q) + r
-// (q, r < 4): the lanes of a row read a token's B and C, and a state row, as consecutive
-// 16-byte units (no shared-memory bank conflicts, coalesced global accesses).  Row sums run over lanes with shuffles, over warps in shared
+// the rows of a head), so a thread owns SL columns of one row (SL = 4 for up to 32 states,
+// else 16), the NSL = S / SL threads of a row sit in adjacent lanes, a warp holds
+// RPW = 32 / NSL rows and a CTA of W warps RPC = W RPW rows, all in one group.  The columns of
+// lane ns are runs of four, j = 4 (ns + NSL q) + r (q < SL / 4, r < 4): the lanes of a row read
+// a token's B and C, and a state row, as consecutive 16-byte units (no shared-memory bank
+// conflicts, coalesced global accesses).  Row sums run over lanes with shuffles, over warps in shared
 // memory (fixed order), and over a group's CTAs in ssm_reduce_kernel (fixed order); nothing
 // uses atomics.
 //
@@ -37,7 +38,6 @@ void set_last_error(const char* msg);
 
 namespace ssm {
 
-constexpr int SL = 16;    // columns (states) per thread
 constexpr int kC2 = 4;    // tokens per level-2 sub-segment (the ring)
 constexpr int kTT = 32;   // tokens per tile of the forward
 
@@ -52,31 +52,31 @@ struct Args {
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
-// Column of a thread's value e (e < 16) for lane slot ns: four runs of four.
+// Column of a thread's value e (e < SL) for lane slot ns: runs of four.
 template <int NSL>
 __device__ __forceinline__ int col_of(int ns, int e) { return 4 * (ns + NSL * (e >> 2)) + (e & 3); }
 
-// A thread's 16 values of a state row (row base `r`, 16-byte aligned) as four float4 loads.
-template <int NSL>
+// A thread's SL values of a state row (row base `r`, 16-byte aligned) as float4 loads.
+template <int NSL, int SL>
 __device__ __forceinline__ void load_row16(float (&v)[SL], const float* r, int ns)
 {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < SL / 4; ++q) {
         const float4 x = ld4(r + 4 * (ns + NSL * q));
         v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
     }
 }
-template <int NSL>
+template <int NSL, int SL>
 __device__ __forceinline__ void store_row16(float* r, const float (&v)[SL], int ns)
 {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) st4(r + 4 * (ns + NSL * q), make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+    for (int q = 0; q < SL / 4; ++q) st4(r + 4 * (ns + NSL * q), make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
 }
-// A token's 16 values of a row vector in shared memory (B or C), the same columns.
-template <int NSL>
+// A token's SL values of a row vector in shared memory (B or C), the same columns.
+template <int NSL, int SL>
 __device__ __forceinline__ void load_vec16(float (&v)[SL], const float* r, int ns)
 {
-    load_row16<NSL>(v, r, ns);
+    load_row16<NSL, SL>(v, r, ns);
 }
 
 // Sum of v over the NSL lanes of a row (lanes differ in their low bits).
@@ -88,8 +88,8 @@ __device__ __forceinline__ float row_sum(float v)
     return v;
 }
 
-// One token of the scan on a thread's 16 columns: s = a s + B (x dt).
-template <bool PS>
+// One token of the scan on a thread's SL columns: s = a s + B (x dt).
+template <bool PS, int SL>
 __device__ __forceinline__ void scan_step(float (&s)[SL], const float (&Bt)[SL], float xdt, float dtv,
                                           const float (&Av)[SL], float a_head)
 {
@@ -104,7 +104,7 @@ __device__ __forceinline__ void scan_step(float (&s)[SL], const float (&Bt)[SL],
 // Forward: grid (row blocks, N), W warps.  Tiles of kTT tokens of B, C (the CTA's group), x
 // (its rows), dt and (Mamba-2) a = exp(dt A) per head go to shared memory; y is staged and
 // stored row-contiguously.
-template <int NSL, bool PS>
+template <int NSL, int SL, bool PS>
 __global__ void __launch_bounds__(256) ssm_fwd_kernel(const Args a)
 {
     constexpr int RPW = 32 / NSL;
@@ -129,9 +129,9 @@ __global__ void __launch_bounds__(256) ssm_fwd_kernel(const Args a)
 #pragma unroll
     for (int e = 0; e < SL; ++e) Av[e] = PS ? a.A[h * S + col_of<NSL>(ns, e)] : a.A[h];
     float s[SL];
-    load_row16<NSL>(s, a.s0 + ((n * H + h) * P + p) * S, ns);
+    load_row16<NSL, SL>(s, a.s0 + ((n * H + h) * P + p) * S, ns);
     float* ckr = a.ckpt + (((n * H + h) * a.n_ck) * P + p) * S;  // + k P S per checkpoint
-    if (T == 0) store_row16<NSL>(ckr, s, ns);
+    if (T == 0) store_row16<NSL, SL>(ckr, s, ns);
     int ck_next = 0;   // tokens to the next checkpoint
     int ck_i = 0;      // its index
 
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(256) ssm_fwd_kernel(const Args a)
         const int Si = (int)S;
         for (int tt = 0; tt < nt; ++tt) {
             if (ck_next == 0) {
-                store_row16<NSL>(ckr + (long long)ck_i * P * S, s, ns);
+                store_row16<NSL, SL>(ckr + (long long)ck_i * P * S, s, ns);
                 ck_next = a.K;
                 ++ck_i;
             }
@@ -167,9 +167,9 @@ __global__ void __launch_bounds__(256) ssm_fwd_kernel(const Args a)
             const float dtv = sdt[tt * nh + hk];
             const float xdt = __fmul_rn(sx[tt * RPC + lrow], dtv);
             float Bt[SL], Ct[SL];
-            load_vec16<NSL>(Bt, sB + tt * Si, ns);
-            load_vec16<NSL>(Ct, sC + tt * Si, ns);
-            scan_step<PS>(s, Bt, xdt, dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
+            load_vec16<NSL, SL>(Bt, sB + tt * Si, ns);
+            load_vec16<NSL, SL>(Ct, sC + tt * Si, ns);
+            scan_step<PS, SL>(s, Bt, xdt, dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
             float y4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int e = 0; e < SL; ++e) y4[e & 3] = __fmaf_rn(s[e], Ct[e], y4[e & 3]);
@@ -190,12 +190,13 @@ __global__ void __launch_bounds__(256) ssm_fwd_kernel(const Args a)
 
 // ---------------------------------------------------------------------------------
 // The reverse walk: grid (row blocks, N), W warps.
-template <int NSL, bool PS>
+template <int NSL, int SL, bool PS>
 __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
 {
     constexpr int RPW = 32 / NSL;
     constexpr int NV = 2 * SL;            // dB and dC terms of a thread per token
     constexpr int NH = NV / RPW;          // of them, held per lane after the row reduce-scatter
+    static_assert(NV >= RPW, "one term per lane at least");
     const int W = blockDim.x >> 5, NT = blockDim.x, RPC = W * RPW;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ns = lane % NSL, lrow = warp * RPW + lane / NSL;
@@ -231,17 +232,18 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
 #pragma unroll
         for (int e = 0; e < SL; ++e) ds[e] = d[col_of<NSL>(ns, e)];
     }
-    // sub-checkpoint k of this thread: float4 q at subr + 4 ((4 k + q) NT)
+    // sub-checkpoint k of this thread: float4 q at subr + 4 ((SL / 4 k + q) NT)
+    constexpr int Q = SL / 4;
     float* subr = a.sub + ((long long)blockIdx.y * gridDim.x + blockIdx.x) * a.nsub * NT * SL + 4 * tid;
     auto put4 = [&](float* base, int k, const float (&v)[SL]) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            st4(base + 4 * ((4 * k + q) * NT), make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        for (int q = 0; q < Q; ++q)
+            st4(base + 4 * ((Q * k + q) * NT), make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
     };
     auto get4 = [&](float (&v)[SL], const float* base, int k) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 x = ld4(base + 4 * ((4 * k + q) * NT));
+        for (int q = 0; q < Q; ++q) {
+            const float4 x = ld4(base + 4 * ((Q * k + q) * NT));
             v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
         }
     };
@@ -276,7 +278,7 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
         if (t1 <= t0) continue;
         // level 1: the segment forward from its checkpoint; a sub-checkpoint every kC2 tokens
         float s[SL];
-        load_row16<NSL>(s, a.ckpt_in + (((n * H + h) * a.n_ck + seg) * P + p) * S, ns);
+        load_row16<NSL, SL>(s, a.ckpt_in + (((n * H + h) * a.n_ck + seg) * P + p) * S, ns);
         const int nsub = (int)((t1 - t0 + kC2 - 1) / kC2);
         for (int k = 0; k < nsub; ++k) {
             const long long ts = t0 + (long long)k * kC2;
@@ -287,8 +289,8 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
             for (int tt = 0; tt < nt; ++tt) {
                 const float dtv = sdt[tt * nh + hk];
                 float Bt[SL];
-                load_vec16<NSL>(Bt, sB + tt * (int)S, ns);
-                scan_step<PS>(s, Bt, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
+                load_vec16<NSL, SL>(Bt, sB + tt * (int)S, ns);
+                scan_step<PS, SL>(s, Bt, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
             }
         }
         // level 2: sub-segments last first
@@ -301,8 +303,8 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
                 put4(ringr, tt, s);
                 const float dtv = sdt[tt * nh + hk];
                 float Bt[SL];
-                load_vec16<NSL>(Bt, sB + tt * (int)S, ns);
-                scan_step<PS>(s, Bt, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
+                load_vec16<NSL, SL>(Bt, sB + tt * (int)S, ns);
+                scan_step<PS, SL>(s, Bt, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
             }
             // s is now the state after the sub-segment's last token
             for (int tt = nt - 1; tt >= 0; --tt) {
@@ -313,8 +315,8 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
                 const float xv = sx[tt * RPC + lrow], dyv = sdy[tt * RPC + lrow];
                 const float xdt = __fmul_rn(xv, dtv);
                 float Bt[SL], Ct[SL];
-                load_vec16<NSL>(Bt, sB + tt * (int)S, ns);
-                load_vec16<NSL>(Ct, sC + tt * (int)S, ns);
+                load_vec16<NSL, SL>(Bt, sB + tt * (int)S, ns);
+                load_vec16<NSL, SL>(Ct, sC + tt * (int)S, ns);
                 float v[NV];
                 float dxp = 0.f, ddtp = 0.f;
 #pragma unroll
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
             }
         }
     }
-    store_row16<NSL>(a.ds0 + ((n * H + h) * P + p) * S, ds, ns);
+    store_row16<NSL, SL>(a.ds0 + ((n * H + h) * P + p) * S, ds, ns);
 }
 
 // dB, dC: each group's CTA partials summed in ascending order; ddt: each head's.
@@ -414,8 +416,12 @@ __global__ void __launch_bounds__(256) ssm_reduce_kernel(const Args a)
 
 struct Plan {
     long long N, T, H, P, S, G, K, n_ck;
-    int per_state, NSL, RPW, W, RPC, nb_g, nb_h, nsub, ctas;
+    int per_state, SL, NSL, RPW, W, RPC, nb_g, nb_h, nsub, ctas;
 };
+
+// States per thread: 4 up to 32 states (a Mamba-1 layer has 16: four times the threads, the
+// rows being few), else 16.
+static int states_per_thread(long long S) { return S <= 32 ? 4 : 16; }
 
 static int plan_of(const ssm_params_t* p, Plan& pl, std::string& why)
 {
@@ -440,7 +446,8 @@ static int plan_of(const ssm_params_t* p, Plan& pl, std::string& why)
         why = "S (d_state) must be 16, 32, 64, 128 or 256";
         return GDN_ERR_UNSUPPORTED;
     }
-    pl.NSL = (int)(pl.S / SL);
+    pl.SL = states_per_thread(pl.S);
+    pl.NSL = (int)(pl.S / pl.SL);
     pl.RPW = 32 / pl.NSL;
     const long long rows = pl.H * pl.P, rows_g = (pl.H / pl.G) * pl.P;
     // the largest CTA (up to 8 warps) whose rows lie in one group and cover whole heads or
@@ -476,7 +483,7 @@ static WsLayout ws_layout(const Plan& pl)
     WsLayout w{};
     size_t o = 0;
     w.sub = o;
-    o += align256(sizeof(float) * (size_t)pl.N * pl.ctas * pl.nsub * (32 * pl.W) * SL);
+    o += align256(sizeof(float) * (size_t)pl.N * pl.ctas * pl.nsub * (32 * pl.W) * pl.SL);
     w.partBC = o;
     o += align256(sizeof(float) * (size_t)pl.N * pl.T * pl.G * pl.nb_g * 2 * pl.S);
     w.partDt = o;
@@ -495,7 +502,7 @@ static size_t bwd_smem(const Plan& pl)
 {
     const long long nh = pl.P >= pl.RPC ? 1 : pl.RPC / pl.P;
     const long long NT = 32LL * pl.W;
-    return sizeof(float) * (size_t)(kC2 * NT * SL + 2 * kC2 * pl.S + 4 * kC2 * pl.RPC + 2 * kC2 * nh +
+    return sizeof(float) * (size_t)(kC2 * NT * pl.SL + 2 * kC2 * pl.S + 4 * kC2 * pl.RPC + 2 * kC2 * nh +
                                     (long long)kC2 * pl.W * 2 * pl.S);
 }
 
@@ -507,11 +514,11 @@ static bool overlap(const void* a, size_t an, const void* b, size_t bn)
     return an && bn && x < y + bn && y < x + an;
 }
 
-template <bool FWD, int NSL, bool PS>
+template <bool FWD, int NSL, int SL, bool PS>
 static int launch_t(const Args& a, const Plan& pl, cudaStream_t st)
 {
     const size_t smem = FWD ? fwd_smem(pl) : bwd_smem(pl);
-    auto kern = FWD ? ssm_fwd_kernel<NSL, PS> : ssm_bwd_kernel<NSL, PS>;
+    auto kern = FWD ? ssm_fwd_kernel<NSL, SL, PS> : ssm_bwd_kernel<NSL, SL, PS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     kern<<<dim3(pl.ctas, (unsigned)pl.N), 32 * pl.W, smem, st>>>(a);
@@ -521,13 +528,16 @@ static int launch_t(const Args& a, const Plan& pl, cudaStream_t st)
 template <bool FWD>
 static int launch(const Args& a, const Plan& pl, cudaStream_t st)
 {
-#define SSM_CASE(NN)                                                                          \
-    if (pl.NSL == NN) return pl.per_state ? launch_t<FWD, NN, true>(a, pl, st) : launch_t<FWD, NN, false>(a, pl, st);
-    SSM_CASE(1)
-    SSM_CASE(2)
-    SSM_CASE(4)
-    SSM_CASE(8)
-    SSM_CASE(16)
+#define SSM_CASE(NN, LL)                                                                      \
+    if (pl.NSL == NN && pl.SL == LL)                                                          \
+        return pl.per_state ? launch_t<FWD, NN, LL, true>(a, pl, st) : launch_t<FWD, NN, LL, false>(a, pl, st);
+    SSM_CASE(4, 4)    // 16 states
+    SSM_CASE(8, 4)    // 32
+    SSM_CASE(4, 16)   // 64
+    SSM_CASE(8, 16)   // 128
+    SSM_CASE(16, 16)  // 256
+    SSM_CASE(8, 8)    // 64 at 8 states a thread
+    SSM_CASE(16, 8)   // 128 at 8 states a thread
 #undef SSM_CASE
     return (int)cudaErrorInvalidValue;
 }
