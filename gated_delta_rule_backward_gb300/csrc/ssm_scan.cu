@@ -190,6 +190,29 @@ __global__ void __launch_bounds__(256) ssm_fwd_kernel(const Args a)
 
 // ---------------------------------------------------------------------------------
 // The reverse walk: grid (row blocks, N), W warps.
+//
+// Its stages (a sub-segment's tokens of B, x, dt, and for level 2 also C and dy) run in a
+// fixed order: for each segment, last first, level 1's sub-segments 0 .. nsub - 2, then level
+// 2's nsub - 1 .. 0.  Each stage's inputs are copied into one of two shared-memory buffers by
+// cp.async while the previous stage computes from the other.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+{
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem)
+{
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Position in the walk's stage sequence.
+struct Cursor {
+    int seg, lvl, k;  // lvl 1: level 1 (k ascending); lvl 2: level 2 (k descending); seg < 0: done
+};
+
 template <int NSL, int SL, bool PS>
 __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
 {
@@ -210,22 +233,21 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
     const long long rows_g = (H / G) * P;
     const int bg = (int)((row0 % rows_g) / RPC);              // this CTA among its group's
     const int bh = P >= RPC ? (int)((row0 % P) / RPC) : 0;    // this CTA among its head's
+    const int Si = (int)S;
 
     extern __shared__ __align__(16) float sm[];
-    float* ring = sm;                                  // [kC2][4][NT] float4
-    float* sB = ring + kC2 * NT * SL;                  // [kC2][S]
-    float* sC = sB + kC2 * S;                          // [kC2][S]
-    float* sx = sC + kC2 * S;                          // [kC2][RPC]
-    float* sdy = sx + kC2 * RPC;                       // [kC2][RPC]
-    float* sdx = sdy + kC2 * RPC;                      // [kC2][RPC]
+    float* ring = sm;                                  // [kC2][SL / 4][NT] float4
+    float* sbc = ring + kC2 * NT * SL;                 // [kC2][W][2S] warp partials of dB, dC
+    float* sdx = sbc + kC2 * W * 2 * Si;               // [kC2][RPC]
     float* sdr = sdx + kC2 * RPC;                      // [kC2][RPC]  ddt row partials
-    float* sdt = sdr + kC2 * RPC;                      // [kC2][nh]
-    float* sa = sdt + kC2 * nh;                        // [kC2][nh]
-    float* sbc = sa + kC2 * nh;                        // [kC2][W][2S] warp partials of dB, dC
+    float* stg = sdr + kC2 * RPC;                      // two stage buffers, each:
+    const int stage_floats = 2 * kC2 * Si + 2 * kC2 * RPC + ((kC2 * nh + 3) & ~3);
+    //   [kC2][S] B, [kC2][S] C, [kC2][RPC] x, [kC2][RPC] dy, [kC2][nh] dt
 
     float Av[SL];
 #pragma unroll
     for (int e = 0; e < SL; ++e) Av[e] = PS ? a.A[h * S + col_of<NSL>(ns, e)] : a.A[h];
+    const float A_head = PS ? 0.f : a.A[h];
     float ds[SL];
     {
         const float* d = a.dsT + ((n * H + h) * P + p) * S;  // (packed: scalar loads)
@@ -249,74 +271,111 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
     };
     float* ringr = ring + 4 * tid;
 
-    // stage tokens [ts, te) of B (and C, x, dy when `all`), dt and (Mamba-2) a
-    auto stage = [&](long long ts, int nt, bool all) {
-        __syncthreads();
-        for (int i = tid; i < nt * (int)S / 4; i += NT) {
-            const int tt = i / ((int)S / 4), c4 = i % ((int)S / 4);
-            const long long base = ((n * T + ts + tt) * G + g) * S + 4 * c4;
-            st4(sB + tt * S + 4 * c4, ld4(a.B + base));
-            if (all) st4(sC + tt * S + 4 * c4, ld4(a.C + base));
+    auto seg_t0 = [&](int seg) { return (long long)seg * K; };
+    auto seg_t1 = [&](int seg) { return std::min<long long>(T, (long long)seg * K + K); };
+    auto seg_nsub = [&](int seg) { return (int)((seg_t1(seg) - seg_t0(seg) + kC2 - 1) / kC2); };
+    auto seg_start = [&](int seg) {  // the first stage of segment seg (or of an earlier one)
+        for (; seg >= 0; --seg) {
+            if (seg_t1(seg) <= seg_t0(seg)) continue;
+            const int ns_ = seg_nsub(seg);
+            return ns_ > 1 ? Cursor{seg, 1, 0} : Cursor{seg, 2, 0};
         }
+        return Cursor{-1, 0, 0};
+    };
+    auto advance = [&](Cursor c) {
+        const int ns_ = seg_nsub(c.seg);
+        if (c.lvl == 1) return c.k + 1 < ns_ - 1 ? Cursor{c.seg, 1, c.k + 1} : Cursor{c.seg, 2, ns_ - 1};
+        if (c.k > 0) return Cursor{c.seg, 2, c.k - 1};
+        return seg_start(c.seg - 1);
+    };
+    // copies of stage c's inputs into buffer `buf`
+    auto issue = [&](Cursor c, int buf) {
+        float* b = stg + buf * stage_floats;
+        const long long ts = seg_t0(c.seg) + (long long)c.k * kC2;
+        const int nt = (int)std::min<long long>(kC2, seg_t1(c.seg) - ts);
+        const bool all = c.lvl == 2;
+        const float* Bb = a.B + ((n * T + ts) * G + g) * S;
+        const float* Cb = a.C + ((n * T + ts) * G + g) * S;
+        const int S4 = Si / 4, GS = (int)(G * S);
+        for (int i = tid; i < nt * S4; i += NT) {
+            const int tt = i / S4, c4 = i - tt * S4;
+            cp_async16(b + tt * Si + 4 * c4, Bb + tt * GS + 4 * c4);
+            if (all) cp_async16(b + kC2 * Si + tt * Si + 4 * c4, Cb + tt * GS + 4 * c4);
+        }
+        const float* xb = a.x + (n * T + ts) * H * P + row0;
+        const float* yb = a.dy + (n * T + ts) * H * P + row0;
+        const int HP = (int)(H * P);
+        float* bx = b + 2 * kC2 * Si;
         for (int i = tid; i < nt * RPC; i += NT) {
-            const int tt = i / RPC, r = i % RPC;
-            const long long o = (n * T + ts + tt) * H * P + row0 + r;
-            sx[i] = a.x[o];
-            if (all) sdy[i] = a.dy[o];
+            const int tt = i / RPC, r = i - tt * RPC;
+            cp_async4(bx + i, xb + tt * HP + r);
+            if (all) cp_async4(bx + kC2 * RPC + i, yb + tt * HP + r);
         }
+        const float* db = a.dt + (n * T + ts) * H + h_lo;
+        float* bd = bx + 2 * kC2 * RPC;
         for (int i = tid; i < nt * nh; i += NT) {
-            const int tt = i / nh, k = i % nh;
-            const float dv = a.dt[(n * T + ts + tt) * H + h_lo + k];
-            sdt[i] = dv;
-            if (!PS) sa[i] = expf(__fmul_rn(dv, a.A[h_lo + k]));
+            const int tt = i / nh, k = i - tt * nh;
+            cp_async4(bd + i, db + tt * (int)H + k);
         }
-        __syncthreads();
+        cp_async_commit();
     };
 
-    for (int seg = a.n_ck - 1; seg >= 0; --seg) {
-        const long long t0 = seg * K, t1 = std::min<long long>(T, t0 + K);
-        if (t1 <= t0) continue;
-        // level 1: the segment forward from its checkpoint; a sub-checkpoint every kC2 tokens
-        float s[SL];
-        load_row16<NSL, SL>(s, a.ckpt_in + (((n * H + h) * a.n_ck + seg) * P + p) * S, ns);
-        const int nsub = (int)((t1 - t0 + kC2 - 1) / kC2);
-        for (int k = 0; k < nsub; ++k) {
-            const long long ts = t0 + (long long)k * kC2;
-            const int nt = (int)std::min<long long>(kC2, t1 - ts);
-            put4(subr, k, s);
-            if (k == nsub - 1) break;  // the last sub-segment's states come in level 2
-            stage(ts, nt, false);
+    Cursor c = seg_start(a.n_ck - 1);
+    if (c.seg >= 0) issue(c, 0);
+    int buf = 0;
+    float s[SL];
+    while (c.seg >= 0) {
+        const Cursor nx = advance(c);
+        cp_async_wait_all();
+        __syncthreads();                   // stage c has landed; every thread is done with buf ^ 1
+        if (nx.seg >= 0) issue(nx, buf ^ 1);
+        const float* b = stg + buf * stage_floats;
+        const float* sB = b;
+        const float* sC = b + kC2 * Si;
+        const float* sx = b + 2 * kC2 * Si;
+        const float* sdy = sx + kC2 * RPC;
+        const float* sdt = sdy + kC2 * RPC;
+        const long long t0 = seg_t0(c.seg), t1 = seg_t1(c.seg);
+        const int nsub = seg_nsub(c.seg);
+        const long long ts = t0 + (long long)c.k * kC2;
+        const int nt = (int)std::min<long long>(kC2, t1 - ts);
+        if (c.lvl == 1) {
+            // level 1: the segment forward from its checkpoint; a sub-checkpoint every kC2 tokens
+            if (c.k == 0) load_row16<NSL, SL>(s, a.ckpt_in + (((n * H + h) * a.n_ck + c.seg) * P + p) * S, ns);
+            put4(subr, c.k, s);
             for (int tt = 0; tt < nt; ++tt) {
                 const float dtv = sdt[tt * nh + hk];
                 float Bt[SL];
-                load_vec16<NSL, SL>(Bt, sB + tt * (int)S, ns);
-                scan_step<PS, SL>(s, Bt, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
+                load_vec16<NSL, SL>(Bt, sB + tt * Si, ns);
+                scan_step<PS, SL>(s, Bt, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av,
+                                  PS ? 0.f : expf(__fmul_rn(dtv, A_head)));
             }
-        }
-        // level 2: sub-segments last first
-        for (int k = nsub - 1; k >= 0; --k) {
-            const long long ts = t0 + (long long)k * kC2;
-            const int nt = (int)std::min<long long>(kC2, t1 - ts);
-            get4(s, subr, k);
-            stage(ts, nt, true);
+            if (c.k + 1 == nsub - 1) put4(subr, c.k + 1, s);
+        } else {
+            // level 2: the sub-segment's states into the ring, then its tokens in reverse
+            if (nsub == 1)
+                load_row16<NSL, SL>(s, a.ckpt_in + (((n * H + h) * a.n_ck + c.seg) * P + p) * S, ns);
+            else
+                get4(s, subr, c.k);
             for (int tt = 0; tt < nt; ++tt) {  // ring slot tt: the state entering token ts + tt
                 put4(ringr, tt, s);
                 const float dtv = sdt[tt * nh + hk];
                 float Bt[SL];
-                load_vec16<NSL, SL>(Bt, sB + tt * (int)S, ns);
-                scan_step<PS, SL>(s, Bt, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av, PS ? 0.f : sa[tt * nh + hk]);
+                load_vec16<NSL, SL>(Bt, sB + tt * Si, ns);
+                scan_step<PS, SL>(s, Bt, __fmul_rn(sx[tt * RPC + lrow], dtv), dtv, Av,
+                                  PS ? 0.f : expf(__fmul_rn(dtv, A_head)));
             }
             // s is now the state after the sub-segment's last token
             for (int tt = nt - 1; tt >= 0; --tt) {
                 float sp[SL];  // the state entering the token
                 get4(sp, ringr, tt);
                 const float dtv = sdt[tt * nh + hk];
-                const float a_head = PS ? 0.f : sa[tt * nh + hk];
+                const float a_head = PS ? 0.f : expf(__fmul_rn(dtv, A_head));
                 const float xv = sx[tt * RPC + lrow], dyv = sdy[tt * RPC + lrow];
                 const float xdt = __fmul_rn(xv, dtv);
                 float Bt[SL], Ct[SL];
-                load_vec16<NSL, SL>(Bt, sB + tt * (int)S, ns);
-                load_vec16<NSL, SL>(Ct, sC + tt * (int)S, ns);
+                load_vec16<NSL, SL>(Bt, sB + tt * Si, ns);
+                load_vec16<NSL, SL>(Ct, sC + tt * Si, ns);
                 float v[NV];
                 float dxp = 0.f, ddtp = 0.f;
 #pragma unroll
@@ -351,20 +410,22 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
                     }
                     base += up ? m : 0;
                 }
-                float* wp = sbc + ((long long)tt * W + warp) * 2 * S;
+                float* wp = sbc + (tt * W + warp) * 2 * Si;
 #pragma unroll
                 for (int i = 0; i < NH; ++i) {
                     const int idx = base + i;
-                    wp[idx < SL ? col_of<NSL>(ns, idx) : (int)S + col_of<NSL>(ns, idx - SL)] = v[i];
+                    wp[idx < SL ? col_of<NSL>(ns, idx) : Si + col_of<NSL>(ns, idx - SL)] = v[i];
                 }
             }
             __syncthreads();
             // this sub-segment's per-token sums: dB, dC over the warps, ddt over rows, dx
-            for (int i = tid; i < nt * 2 * (int)S; i += NT) {
-                const int tt = i / (2 * (int)S), c = i % (2 * (int)S);
+            float* pbc = a.partBC + (((n * T + ts) * G + g) * a.nb_g + bg) * 2 * S;
+            const long long pstride = G * a.nb_g * 2 * S;  // one token further
+            for (int i = tid; i < nt * 2 * Si; i += NT) {
+                const int tt = i / (2 * Si), cc = i - tt * 2 * Si;
                 float acc = 0.f;
-                for (int w = 0; w < W; ++w) acc = __fadd_rn(acc, sbc[((long long)tt * W + w) * 2 * S + c]);
-                a.partBC[(((n * T + ts + tt) * G + g) * a.nb_g + bg) * 2 * S + c] = acc;
+                for (int w = 0; w < W; ++w) acc = __fadd_rn(acc, sbc[(tt * W + w) * 2 * Si + cc]);
+                pbc[tt * pstride + cc] = acc;
             }
             if (P >= RPC) {
                 for (int tt = tid; tt < nt; tt += NT) {
@@ -380,12 +441,16 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
                     a.partDt[((n * T + ts + tt) * H + h_lo + k2) * a.nb_h] = acc;
                 }
             }
+            const long long dxo = (n * T + ts) * H * P + row0;
             for (int i = tid; i < nt * RPC; i += NT) {
                 const int tt = i / RPC, r = i % RPC;
-                a.dx[(n * T + ts + tt) * H * P + row0 + r] = sdx[i];
+                a.dx[dxo + (long long)tt * H * P + r] = sdx[i];
             }
         }
+        c = nx;
+        buf ^= 1;
     }
+    cp_async_wait_all();
     store_row16<NSL, SL>(a.ds0 + ((n * H + h) * P + p) * S, ds, ns);
 }
 
@@ -502,8 +567,8 @@ static size_t bwd_smem(const Plan& pl)
 {
     const long long nh = pl.P >= pl.RPC ? 1 : pl.RPC / pl.P;
     const long long NT = 32LL * pl.W;
-    return sizeof(float) * (size_t)(kC2 * NT * pl.SL + 2 * kC2 * pl.S + 4 * kC2 * pl.RPC + 2 * kC2 * nh +
-                                    (long long)kC2 * pl.W * 2 * pl.S);
+    const long long stage = 2 * kC2 * pl.S + 2 * kC2 * pl.RPC + ((kC2 * nh + 3) & ~3LL);
+    return sizeof(float) * (size_t)(kC2 * NT * pl.SL + (long long)kC2 * pl.W * 2 * pl.S + 2 * kC2 * pl.RPC + 2 * stage);
 }
 
 static bool aligned16(const void* q) { return ((uintptr_t)q & 15) == 0; }
