@@ -817,7 +817,7 @@ def ssm_cpu_baseline(prob, workload):
     from oracle import ssm as oss
     lib = oss.load()
     threads = oss.max_threads(lib)
-    heads = list(range(min(prob.H, 4 if prob.P > 1 else 64)))
+    heads = list(range(min(prob.H, 4 if prob.P > 1 else prob.H)))  # Mamba-2: 4 heads; Mamba-1: every channel
     sub = {f: np.ascontiguousarray(getattr(prob, f)[:, :, heads]) for f in ("x", "dt", "dy")}
     sub.update({f: np.ascontiguousarray(getattr(prob, f)[:, heads]) for f in ("s0", "ds_T")})
     A = np.ascontiguousarray(prob.A[heads])

@@ -62,7 +62,7 @@
  * The caller owns every buffer and the stream; the library allocates no device memory
  * and keeps no pointer after a call returns.  Work is enqueued on `stream` (a
  * cudaStream_t; NULL is the legacy default stream): GDN_OK means "validated and
- * launched".  At head size 128 the scalar-gate path also uses three library streams per
+ * launched".  At head size 128 the chunked path also uses four library streams per
  * device (created on first use): the call's stream forks into them and joins back with
  * events, so everything the call enqueues is ordered after earlier work on `stream` and
  * before later work on it.  Those streams are shared by every caller on the device, so
