@@ -237,8 +237,12 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
 
     extern __shared__ __align__(16) float sm[];
     float* ring = sm;                                  // [kC2][SL / 4][NT] float4
-    float* sbc = ring + kC2 * NT * SL;                 // [kC2][W][2S] warp partials of dB, dC
-    float* sdx = sbc + kC2 * W * 2 * Si;               // [kC2][RPC]
+    // warp partials of dB, dC: [kC2][W][2S + 2S / 64], column c at c + c / 64, so that the row
+    // groups of a warp (whose terms sit 64 columns apart after the reduce-scatter) store to
+    // distinct banks
+    const int LB = 2 * Si + 2 * Si / 64;
+    float* sbc = ring + kC2 * NT * SL;
+    float* sdx = sbc + kC2 * W * LB;                   // [kC2][RPC]
     float* sdr = sdx + kC2 * RPC;                      // [kC2][RPC]  ddt row partials
     float* stg = sdr + kC2 * RPC;                      // two stage buffers, each:
     const int stage_floats = 2 * kC2 * Si + 2 * kC2 * RPC + ((kC2 * nh + 3) & ~3);
@@ -410,11 +414,12 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
                     }
                     base += up ? m : 0;
                 }
-                float* wp = sbc + (tt * W + warp) * 2 * Si;
+                float* wp = sbc + (tt * W + warp) * LB;
 #pragma unroll
                 for (int i = 0; i < NH; ++i) {
                     const int idx = base + i;
-                    wp[idx < SL ? col_of<NSL>(ns, idx) : Si + col_of<NSL>(ns, idx - SL)] = v[i];
+                    const int cc = idx < SL ? col_of<NSL>(ns, idx) : Si + col_of<NSL>(ns, idx - SL);
+                    wp[cc + (cc >> 6)] = v[i];
                 }
             }
             __syncthreads();
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(256) ssm_bwd_kernel(const Args a)
             for (int i = tid; i < nt * 2 * Si; i += NT) {
                 const int tt = i / (2 * Si), cc = i - tt * 2 * Si;
                 float acc = 0.f;
-                for (int w = 0; w < W; ++w) acc = __fadd_rn(acc, sbc[(tt * W + w) * 2 * Si + cc]);
+                for (int w = 0; w < W; ++w) acc = __fadd_rn(acc, sbc[(tt * W + w) * LB + cc + (cc >> 6)]);
                 pbc[tt * pstride + cc] = acc;
             }
             if (P >= RPC) {
@@ -568,7 +573,8 @@ static size_t bwd_smem(const Plan& pl)
     const long long nh = pl.P >= pl.RPC ? 1 : pl.RPC / pl.P;
     const long long NT = 32LL * pl.W;
     const long long stage = 2 * kC2 * pl.S + 2 * kC2 * pl.RPC + ((kC2 * nh + 3) & ~3LL);
-    return sizeof(float) * (size_t)(kC2 * NT * pl.SL + (long long)kC2 * pl.W * 2 * pl.S + 2 * kC2 * pl.RPC + 2 * stage);
+    const long long LB = 2 * pl.S + 2 * pl.S / 64;
+    return sizeof(float) * (size_t)(kC2 * NT * pl.SL + (long long)kC2 * pl.W * LB + 2 * kC2 * pl.RPC + 2 * stage);
 }
 
 static bool aligned16(const void* q) { return ((uintptr_t)q & 15) == 0; }
