@@ -72,6 +72,9 @@ SSM_WORKLOADS = {
     "mamba1_d1536_T4096": dict(N=1, T=4096, H=1536, P=1, S=16, G=1, mamba1=True, K=64, seed=12),
     "mamba2_small": dict(N=2, T=100, H=8, P=64, S=128, G=2, mamba1=False, K=16, seed=13),
     "mamba1_small": dict(N=2, T=100, H=96, P=1, S=16, G=1, mamba1=True, K=16, seed=14),
+    # the two layers cut to 512 tokens, for kernel captures of a few hundred MB
+    "profile_mamba2_h80_T512": dict(N=1, T=512, H=80, P=64, S=128, G=1, mamba1=False, K=16, seed=11),
+    "profile_mamba1_d1536_T512": dict(N=1, T=512, H=1536, P=1, S=16, G=1, mamba1=True, K=16, seed=12),
 }
 
 
