@@ -1434,7 +1434,8 @@ static int launch_prep_range(const ChunkArgs& a, int R, bool backward, int r, cu
 //   gradients: after the dM chain of r, the gradient launches of range r, one per place (a
 //              launch for place k > 0 may start in the tail of the one for place k - 1)
 //   sums:      the sum over value heads of the range's chunks once its gradient launches are
-//              done (or of each place's, kSumByPlace), ahead of the next gradient launch
+//              done (or of each place's, kSumByPlace), at the least urgent level: its CTAs
+//              take what the gradient CTAs leave free
 // so that the gradient work of one range runs while the chain walks the next.  With timing
 // events set, the backward instead runs its stages one after another as a single range
 // (prep and dM chain, gradient step, sum), each between two events.
