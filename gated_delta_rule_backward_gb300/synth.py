@@ -124,6 +124,10 @@ WORKLOADS = {
     # 1024 tokens for many-pass profiler captures of the token-recurrence kernels
     "profile_kda_d128_T1024": dict(N=1, T=1024, H_k=16, H_v=48, d=128, kda=True, C=128,
                                    seed=1006, packed=True, g_std=2.0),
+    # sweep shapes at head sizes 64 and 32 (4 sequences, 16 key heads over 48 value heads,
+    # 4096 tokens, scalar gate): the FP32-pipe chunked path, for stage times and captures
+    "d64_T4096_N4": dict(N=4, T=4096, H_k=16, H_v=48, d=64, kda=False, C=None, seed=1007, packed=True),
+    "d32_T4096_N4": dict(N=4, T=4096, H_k=16, H_v=48, d=32, kda=False, C=None, seed=1008, packed=True),
 }
 
 
