@@ -31,6 +31,7 @@
 #include <string>
 
 #include "../../include/ssm.h"
+#include "ssm_chunk.h"
 
 namespace gdn {
 void set_last_error(const char* msg);
@@ -487,7 +488,16 @@ __global__ void __launch_bounds__(256) ssm_reduce_kernel(const Args a)
 struct Plan {
     long long N, T, H, P, S, G, K, n_ck;
     int per_state, SL, NSL, RPW, W, RPC, nb_g, nb_h, nsub, ctas;
+    bool chunked;  // the chunked form (ssm_chunk.cu) runs
+    int HB, nch;   // its heads per gradient CTA and chunks per sequence
 };
+
+// The chunked form takes one decay per head, 64 channels and 128 states (the Mamba-2 layer's
+// head), at least one token and checkpoints on chunk boundaries.
+static bool chunked_shape(const ssm_params_t* p)
+{
+    return p->a_per_state == 0 && p->P == ssd::kP && p->S == ssd::kS && p->T >= 1;
+}
 
 // States per thread: 4 up to 32 states (a Mamba-1 layer has 16: four times the threads, the
 // rows being few), else 16.
@@ -511,6 +521,10 @@ static int plan_of(const ssm_params_t* p, Plan& pl, std::string& why)
     pl.N = p->N; pl.T = p->T; pl.H = p->H; pl.P = p->P; pl.S = p->S; pl.G = p->G;
     pl.per_state = p->a_per_state;
     pl.K = p->K > 0 ? p->K : (p->T > 1 ? (long long)std::ceil(std::sqrt((double)p->T)) : 1);
+    if (p->K == 0 && chunked_shape(p)) pl.K = (pl.K + ssd::kChunk - 1) / ssd::kChunk * ssd::kChunk;
+    pl.chunked = chunked_shape(p) && pl.K % ssd::kChunk == 0;
+    pl.nch = (int)((pl.T + ssd::kChunk - 1) / ssd::kChunk);
+    pl.HB = pl.chunked ? ssd::heads_per_block(pl.N, pl.nch, pl.H, pl.G) : 1;
     pl.n_ck = p->T <= 0 ? 1 : (p->T + pl.K - 1) / pl.K;
     if (pl.S != 16 && pl.S != 32 && pl.S != 64 && pl.S != 128 && pl.S != 256) {
         why = "S (d_state) must be 16, 32, 64, 128 or 256";
@@ -553,6 +567,10 @@ struct WsLayout {
 static WsLayout ws_layout(const Plan& pl)
 {
     WsLayout w{};
+    if (pl.chunked) {
+        w.total = ssd::workspace_layout(pl.N, pl.T, pl.H, pl.G, (int)pl.K, pl.HB).total;
+        return w;
+    }
     size_t o = 0;
     w.sub = o;
     o += align256(sizeof(float) * (size_t)pl.N * pl.ctas * pl.nsub * (32 * pl.W) * pl.SL);
@@ -615,6 +633,15 @@ static int launch(const Args& a, const Plan& pl, cudaStream_t st)
     return (int)cudaErrorInvalidValue;
 }
 
+static ssd::Args chunk_args(const Plan& pl)
+{
+    ssd::Args c{};
+    c.N = pl.N; c.T = pl.T; c.H = pl.H; c.G = pl.G;
+    c.K = (int)pl.K; c.n_ck = (int)pl.n_ck; c.nch = pl.nch; c.m = (int)(pl.K / ssd::kChunk);
+    c.HB = pl.HB; c.nhb = (int)(pl.H / pl.G / pl.HB);
+    return c;
+}
+
 static int fail(int code, const std::string& msg)
 {
     gdn::set_last_error(msg.c_str());
@@ -670,6 +697,29 @@ extern "C" int ssm_supported(const ssm_params_t* p)
     return e;
 }
 
+extern "C" int ssm_chunked(const ssm_params_t* p)
+{
+    Plan pl{};
+    std::string why;
+    return plan_of(p, pl, why) == GDN_OK && pl.chunked ? 1 : 0;
+}
+
+extern "C" int ssm_forward_launches(const ssm_params_t* p)
+{
+    Plan pl{};
+    std::string why;
+    if (plan_of(p, pl, why) != GDN_OK || pl.N == 0) return 0;
+    return pl.chunked ? 3 : 1;
+}
+
+extern "C" int ssm_backward_launches(const ssm_params_t* p)
+{
+    Plan pl{};
+    std::string why;
+    if (plan_of(p, pl, why) != GDN_OK || pl.N == 0 || pl.T == 0) return 0;
+    return pl.chunked ? 4 : 2;
+}
+
 extern "C" int ssm_forward(const ssm_params_t* p, const float* s0, const float* x, const float* dt, const float* A,
                            const float* B, const float* C, float* out_packed, float* ckpt, void* stream)
 {
@@ -703,7 +753,14 @@ extern "C" int ssm_forward(const ssm_params_t* p, const float* s0, const float* 
     a.ckpt = ckpt;
     a.N = pl.N; a.T = pl.T; a.H = pl.H; a.P = pl.P; a.S = pl.S; a.G = pl.G;
     a.K = (int)pl.K; a.n_ck = (int)pl.n_ck; a.per_state = pl.per_state; a.RPC = pl.RPC;
-    e = launch<true>(a, pl, (cudaStream_t)stream);
+    if (pl.chunked) {
+        ssd::Args c = chunk_args(pl);
+        c.x = x; c.dt = dt; c.A = A; c.B = B; c.C = C; c.s0 = s0;
+        c.y = a.y; c.sT = a.sT; c.ckpt = ckpt;
+        e = ssd::forward(c, (cudaStream_t)stream);
+    } else {
+        e = launch<true>(a, pl, (cudaStream_t)stream);
+    }
     if (e) return fail(GDN_ERR_CUDA, std::string("ssm_forward: ") + cudaGetErrorString((cudaError_t)e));
     return GDN_OK;
 }
@@ -761,6 +818,19 @@ extern "C" int ssm_backward(const ssm_params_t* p, const float* x, const float* 
         return GDN_OK;
     }
     char* ws = (char*)workspace;
+    if (pl.chunked) {
+        const ssd::Workspace cw = ssd::workspace_layout(pl.N, pl.T, pl.H, pl.G, (int)pl.K, pl.HB);
+        ssd::Args c = chunk_args(pl);
+        c.x = x; c.dt = dt; c.A = A; c.B = B; c.C = C; c.ckpt_in = ckpt; c.dy = a.dy; c.dsT = a.dsT;
+        c.ds0 = a.ds0; c.dx = a.dx; c.ddt = a.ddt; c.dB = a.dB; c.dC = a.dC;
+        c.dd = (float*)(ws + cw.dd);
+        c.sin_all = (float*)(ws + cw.sin_all);
+        c.gvec = (float*)(ws + cw.gvec);
+        c.partBC = (float*)(ws + cw.partBC);
+        e = ssd::backward(c, st);
+        if (e) return fail(GDN_ERR_CUDA, std::string("ssm_backward: ") + cudaGetErrorString((cudaError_t)e));
+        return GDN_OK;
+    }
     a.sub = (float*)(ws + w.sub);
     a.partBC = (float*)(ws + w.partBC);
     a.partDt = (float*)(ws + w.partDt);

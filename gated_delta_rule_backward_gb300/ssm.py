@@ -16,7 +16,8 @@ _lib = gdn._lib
 
 # Every symbol include/ssm.h declares.
 EXPORTS = ["ssm_checkpoint_interval", "ssm_num_checkpoints", "ssm_packed_out_elems", "ssm_packed_grad_elems",
-           "ssm_backward_workspace_bytes", "ssm_supported", "ssm_forward", "ssm_backward"]
+           "ssm_backward_workspace_bytes", "ssm_supported", "ssm_chunked", "ssm_forward_launches",
+           "ssm_backward_launches", "ssm_forward", "ssm_backward"]
 
 
 class SsmParams(ctypes.Structure):
@@ -48,6 +49,12 @@ _lib.ssm_backward_workspace_bytes.argtypes = [_PP]
 _lib.ssm_backward_workspace_bytes.restype = ctypes.c_size_t
 _lib.ssm_supported.argtypes = [_PP]
 _lib.ssm_supported.restype = ctypes.c_int
+_lib.ssm_chunked.argtypes = [_PP]
+_lib.ssm_chunked.restype = ctypes.c_int
+_lib.ssm_forward_launches.argtypes = [_PP]
+_lib.ssm_forward_launches.restype = ctypes.c_int
+_lib.ssm_backward_launches.argtypes = [_PP]
+_lib.ssm_backward_launches.restype = ctypes.c_int
 _lib.ssm_forward.argtypes = [_PP] + [_V] * 9
 _lib.ssm_forward.restype = ctypes.c_int
 _lib.ssm_backward.argtypes = [_PP] + [_V] * 9 + [ctypes.c_size_t, _V]
@@ -87,6 +94,16 @@ def backward_workspace_bytes(p) -> int:
 
 def supported(p) -> int:
     return int(_lib.ssm_supported(ctypes.byref(p)))
+
+
+def chunked(p) -> bool:
+    """True when these sizes run the chunked form."""
+    return bool(_lib.ssm_chunked(ctypes.byref(p)))
+
+
+def launches(p):
+    """(kernels a forward call launches, kernels a backward call launches)."""
+    return int(_lib.ssm_forward_launches(ctypes.byref(p))), int(_lib.ssm_backward_launches(ctypes.byref(p)))
 
 
 def _ptr(t):

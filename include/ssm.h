@@ -22,6 +22,14 @@
  * Arithmetic: fp32 throughout (FP32 pipe, expf); every sum over channels, heads and states
  * runs in a fixed order (no atomics), so a call's results do not change from run to run.
  *
+ * Two forms compute this.  The token-serial walk follows the recurrences above token by token
+ * (its results do not depend on K).  The chunked form (one decay per head, P = 64, S = 128,
+ * K a multiple of 64; ssm_chunked() says which runs) groups 64 tokens into a chunk and writes
+ * each chunk's part of the recurrence as dense products, with l_t = dt_t A, the running sum
+ * c_t of l over the chunk, Q = C B^T and the mask exp(c_t - c_tau) for tau <= t: the chunk's
+ * outputs and state change are those products, and only the state passes from chunk to chunk
+ * (the same sums in another order; its results depend on K through the checkpoint segments).
+ *
  * Layouts: dense, row-major, fp32, device memory, no strides:
  *     s0 [N][H][P][S]   x [N][T][H][P]   dt [N][T][H]   A [H] or [H][S]   B, C [N][T][G][S]
  *     checkpoints [N][H][n_ck][P][S]: checkpoint k is the state entering token k * K
@@ -65,12 +73,14 @@ typedef struct {
     int64_t S;            /* states per channel (d_state) */
     int64_t G;            /* groups of B and C (H % G == 0) */
     int32_t a_per_state;  /* 1: A is [H][S] (Mamba-1); 0: A is [H] (Mamba-2) */
-    int32_t K;            /* checkpoint interval in tokens; 0 = ceil(sqrt(T)) */
+    int32_t K;            /* checkpoint interval in tokens; 0 = ceil(sqrt(T)), rounded up
+                             to a multiple of 64 for the chunked form's sizes */
     int32_t reserved0;    /* 0 */
     int32_t reserved1;    /* 0 */
 } ssm_params_t;
 
-/* The checkpoint interval in use (K, or ceil(sqrt(T)) for K = 0; at least 1). */
+/* The checkpoint interval in use (K; for K = 0, ceil(sqrt(T)), rounded up to a multiple of
+ * 64 where the chunked form runs; at least 1). */
 int64_t ssm_checkpoint_interval(const ssm_params_t* p);
 /* Checkpoints per (sequence, head): ceil(T / K), and 1 when T = 0. */
 int64_t ssm_num_checkpoints(const ssm_params_t* p);
@@ -81,6 +91,13 @@ size_t ssm_packed_grad_elems(const ssm_params_t* p);
 size_t ssm_backward_workspace_bytes(const ssm_params_t* p);
 /* GDN_OK when the sizes are supported, else the code ssm_forward / ssm_backward would return. */
 int ssm_supported(const ssm_params_t* p);
+/* 1 when these sizes run the chunked form (one decay per head, P = 64, S = 128, T >= 1, K a
+ * multiple of 64), 0 when they run the token-serial walk or are unsupported. */
+int ssm_chunked(const ssm_params_t* p);
+/* Kernels a forward / backward call with these params launches (0 when the call would
+ * launch none: unsupported sizes, N = 0, or the backward at T = 0). */
+int ssm_forward_launches(const ssm_params_t* p);
+int ssm_backward_launches(const ssm_params_t* p);
 
 /* Forward: y and s_T into out_packed, the checkpoints into ckpt (n_ck states per head). */
 int ssm_forward(const ssm_params_t* p, const float* s0, const float* x, const float* dt, const float* A,

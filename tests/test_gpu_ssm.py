@@ -4,8 +4,13 @@ element, through the C ABI.
 Tolerance: every output's largest absolute difference over its largest magnitude, at most
 2e-5 up to 512 tokens and 1e-4 at 4096 (fp32 states: the rounding of a step is ~6e-8 of
 the state, and a decayed sum over T steps collects ~sqrt(T) of them; the oracle is
-float64).  Results at different checkpoint intervals, and of repeated calls, must agree
-bit for bit (the walk recomputes the forward's own states and sums in a fixed order).
+float64).  The token-serial walk's results at different checkpoint intervals, and every
+path's results over repeated calls, must agree bit for bit (the walk recomputes the
+forward's own states; every sum runs in a fixed order).
+
+Both forms run here: sizes with one decay per head, P = 64, S = 128 and K a multiple of 64
+take the chunked form (64-token chunks), every other the token-serial walk; each case
+asserts which one it exercises.
 """
 import numpy as np
 import pytest
@@ -67,7 +72,12 @@ def compare(gpu, ref, tol, names=NAMES):
 
 
 CASES = [
-    dict(N=2, T=100, H=8, P=64, S=128, G=2, mamba1=False, K=16),
+    dict(N=2, T=100, H=8, P=64, S=128, G=2, mamba1=False, K=16),     # token-serial at Mamba-2 sizes
+    dict(N=2, T=100, H=8, P=64, S=128, G=2, mamba1=False, K=64),     # chunked: a ragged 2nd chunk
+    dict(N=1, T=300, H=4, P=64, S=128, G=1, mamba1=False, K=128),    # chunked: 2 chunks a segment
+    dict(N=1, T=200, H=6, P=64, S=128, G=3, mamba1=False, K=192),    # chunked: 3 a segment, 1 used
+    dict(N=3, T=64, H=2, P=64, S=128, G=1, mamba1=False, K=64),      # chunked: one full chunk
+    dict(N=1, T=1, H=2, P=64, S=128, G=2, mamba1=False, K=64),       # chunked: one token
     dict(N=2, T=100, H=96, P=1, S=16, G=1, mamba1=True, K=16),
     dict(N=1, T=37, H=4, P=32, S=64, G=4, mamba1=False, K=5),     # ragged last segment
     dict(N=3, T=1, H=2, P=16, S=32, G=1, mamba1=True, K=1),
@@ -81,6 +91,8 @@ CASES = [
                                                f"{'m1' if c['mamba1'] else 'm2'}K{c['K']}")
 def test_parity(case):
     prob = make_ssm_problem(seed=7, **case)
+    p = ssm.make_params(prob.N, prob.T, prob.H, prob.P, prob.S, prob.G, prob.mamba1, prob.K)
+    assert ssm.chunked(p) == (not prob.mamba1 and prob.P == 64 and prob.S == 128 and prob.K % 64 == 0)
     gpu = run_gpu(prob)
     ref = run_oracle(prob)
     compare(gpu, ref, _tol(prob.T))
@@ -110,11 +122,30 @@ def test_checkpoint_interval_invariance_bitwise(mamba1):
             assert np.array_equal(ck[:, :, c], base["ckpt"][:, :, c * K]), f"K={K}: checkpoint {c}"
 
 
-def test_run_to_run_bitwise():
-    prob = ssm_workload("mamba2_small")
+@pytest.mark.parametrize("K", [16, 64], ids=["serial", "chunked"])
+def test_run_to_run_bitwise(K):
+    prob = ssm_workload("mamba2_small", K=K)
     a, b = run_gpu(prob), run_gpu(prob)
     for k in NAMES:
         assert np.array_equal(a[k], b[k]), k
+
+
+def test_chunked_strong_decay():
+    """dt up to 3 (a chunk's decay exp(64 dt A) far below fp32's range): the masks and the
+    carried state underflow to zero, as the token-serial products do."""
+    prob = make_ssm_problem(N=1, T=130, H=4, P=64, S=128, G=1, K=64, seed=5)
+    prob.dt = np.ascontiguousarray(prob.dt * 30, dtype=np.float32)
+    assert ssm.chunked(ssm.make_params(1, 130, 4, 64, 128, 1, False, 64))
+    compare(run_gpu(prob), run_oracle(prob), _tol(prob.T))
+
+
+def test_mamba2_all_heads_chunked():
+    """Every head of the Mamba-2 workload at 1024 tokens in chunked form: the gradient kernel
+    takes two heads a block here, so dB and dC fold 40 block partials of 2 heads each."""
+    prob = ssm_workload("mamba2_h80_T4096", T=1024, K=64)
+    assert ssm.chunked(ssm.params_for(torch.from_numpy(prob.x), torch.from_numpy(prob.A),
+                                      torch.from_numpy(prob.B), K=64))
+    compare(run_gpu(prob), run_oracle(prob), _tol(prob.T))
 
 
 def test_mamba1_full_size():

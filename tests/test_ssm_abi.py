@@ -33,6 +33,31 @@ def test_sizes():
     assert ssm.backward_workspace_bytes(ssm.make_params(1, 4096, 80, 64, 128, K=64)) > 0
 
 
+def test_chunked_dispatch():
+    """Which form runs, its default checkpoint interval and its launch counts."""
+    p = ssm.make_params(1, 100, 8, 64, 128)            # K = 0: ceil(sqrt(100)) = 10, rounded up to 64
+    assert ssm.chunked(p) and ssm.checkpoint_interval(p) == 64 and ssm.num_checkpoints(p) == 2
+    assert ssm.launches(p) == (3, 4)
+    p = ssm.make_params(1, 5000, 8, 64, 128)           # ceil(sqrt(5000)) = 71 -> 128
+    assert ssm.chunked(p) and ssm.checkpoint_interval(p) == 128
+    for p in (ssm.make_params(1, 100, 8, 64, 128, K=16),          # K off the chunk grid
+              ssm.make_params(1, 100, 8, 64, 64, K=64),           # other state counts
+              ssm.make_params(1, 100, 8, 32, 128, K=64),          # other head sizes
+              ssm.make_params(1, 100, 8, 64, 128, mamba1=True, K=64),
+              ssm.make_params(1, 0, 8, 64, 128, K=64)):           # no tokens
+        assert not ssm.chunked(p)
+    assert ssm.launches(ssm.make_params(1, 100, 8, 64, 128, K=16)) == (1, 2)
+    assert ssm.launches(ssm.make_params(1, 0, 8, 64, 128, K=64)) == (1, 0)
+    assert ssm.launches(ssm.make_params(0, 10, 8, 64, 128, K=64)) == (0, 0)
+    assert ssm.launches(ssm.make_params(1, 10, 8, 64, 24)) == (0, 0)
+    # the chunked workspace: the per-chunk state slabs (one, or two with inner chunks to
+    # replay), the chunk decays and the dB/dC block partials
+    st = 4 * 64 * 8 * 64 * 128
+    w1 = ssm.backward_workspace_bytes(ssm.make_params(1, 4096, 8, 64, 128, K=64))
+    w2 = ssm.backward_workspace_bytes(ssm.make_params(1, 4096, 8, 64, 128, K=128))
+    assert w1 > st and w2 - w1 == st
+
+
 @pytest.mark.parametrize("args,code", [
     (dict(S=24), UNSUPPORTED), (dict(S=512), UNSUPPORTED), (dict(H=6, G=4), INVALID),
     (dict(P=3), UNSUPPORTED), (dict(K=-1), INVALID), (dict(T=-1), INVALID), (dict(S=0), INVALID),
