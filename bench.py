@@ -946,7 +946,8 @@ def run_ssm(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl, "N": prob.N, "T": prob.T, "H": prob.H, "P": prob.P, "S": prob.S,
                    "G": prob.G, "decay": "per state (Mamba-1)" if prob.mamba1 else "per head (Mamba-2)",
-                   "K": prob.K, "arithmetic": "fp32 FP32-pipe, expf",
+                   "K": prob.K, "form": "chunked (64-token chunks)" if ssm.chunked(p) else "token-serial",
+                   "arithmetic": "fp32 FP32-pipe, expf",
                    "l2": "flushed between timed steps (256 MiB write outside the events)"},
         "roofline": {"bound": "alu", "kernel": "whole step: ssm_forward + ssm_backward",
                      "achieved": tflops, "peak": peak32, "unit": "TFLOP/s", "frac": tflops / peak32,
@@ -958,7 +959,7 @@ def run_ssm(args):
                      "workspace_bytes": ws.numel()},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": sum(ssm.launches(p)) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

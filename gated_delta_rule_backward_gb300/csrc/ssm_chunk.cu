@@ -1,6 +1,7 @@
 // ssm_chunk.cu -- the selective scan with one decay per head (Mamba-2) in chunked form: the
-// products of a chunk as CTA-level FP32-pipe GEMMs (gdn_gemm.cuh) that run for every chunk at
-// once, and only an elementwise chain over chunk states left serial.
+// products of a chunk as CTA-level tensor-pipe products (warp-level tf32 MMAs, three-pass
+// split for fp32 accuracy; gdn_mma.cuh) that run for every chunk at once, and only an
+// elementwise chain over chunk states left serial.
 //
 // Source: "dillon-blake llama.cpp PR #26", the SSM_SCAN_BACK section (the reverse walk, the
 // final-state seed, the group fold; the token-serial form is in ssm_scan.cu).  The chunked form
@@ -42,30 +43,32 @@
 #include <algorithm>
 #include <cmath>
 
-#include "gdn_gemm.cuh"
+#include "gdn_mma.cuh"
 
 namespace ssm {
 namespace ssd {
 
-using gdn::block_gemm;
-using gdn::GemmMap;
-using gdn::zero_acc;
+using gdn::block_mma;
+using gdn::MmaAcc;
+using gdn::zero_mma;
 
 constexpr int L = kChunk;
 constexpr int P = kP;
 constexpr int S = kS;
 constexpr int PS = P * S;
 constexpr int CT = 256;     // threads of every kernel but the reduction
-constexpr int LD64 = 68;    // leading dimension of 64-wide tiles (4 mod 32: conflict-free GEMM loads)
+constexpr int LD64 = 68;    // leading dimension of 64-wide tiles (4 mod 32)
 constexpr int LD128 = 132;  // of 128-wide tiles
 constexpr int T64 = L * LD64;
 constexpr int T128 = L * LD128;
 constexpr int NSCAL = 4 * L + 4;  // dt, c, e, w, then g and a spare
 constexpr int SLICES = PS / (4 * CT);  // state slices of the chain kernels (a float4 a thread)
 
-using Map64 = GemmMap<64, 64, 4, 4, false>;    // 64 x 64 outputs, row-major B
-using Map64K = GemmMap<64, 64, 4, 4, true>;    // 64 x 64 outputs, transposed B
-using Map128 = GemmMap<64, 128, 4, 8, false>;  // 64 x 128 outputs, row-major B
+// Output maps of the 64 x 64 and 64 x 128 products (the same for every operand layout).
+using Map64 = gdn::MmaMap<64, 64>;
+using Map128 = gdn::MmaMap<64, 128>;
+using Acc64 = MmaAcc<64, 64>;
+using Acc128 = MmaAcc<64, 128>;
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
@@ -81,10 +84,10 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc)
 {
     return __fmaf_rn(a.w, b.w, __fmaf_rn(a.z, b.z, __fmaf_rn(a.y, b.y, __fmaf_rn(a.x, b.x, acc))));
 }
+__device__ __forceinline__ void st2(float* p, float a, float b) { *reinterpret_cast<float2*>(p) = make_float2(a, b); }
 
-// Sum over the 4 lanes sharing a row of a 64 x 64 product (lane bits 0, 1), and over the 8
-// lanes sharing a column of one with transposed B (lane bits 2 .. 4).  Butterflies: every
-// lane ends with the same bits.
+// Sum over the 4 lanes sharing a row of a product (lane bits 0, 1), and over the 8 lanes
+// sharing a column (lane bits 2 .. 4).  Butterflies: every lane ends with the same bits.
 __device__ __forceinline__ float row_lanes(float v)
 {
     v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 1));
@@ -191,16 +194,17 @@ __device__ __forceinline__ void store_state(float* dst, const float* tile, int t
     }
 }
 
-// A 64 x 128 accumulator (Map128 layout: rows p, columns j) to a dense [P][S] state.
-__device__ __forceinline__ void store_acc128(float* dst, const float (&acc)[4][8], int tid)
+// A 64 x 128 accumulator (rows p, columns j) to a dense [P][S] state.
+__device__ __forceinline__ void store_acc128(float* dst, const Acc128& acc, int tid)
 {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < Map128::MT; ++i)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int r = Map128::row(tid, i), j = Map128::col(tid, 4 * c);
-            st4(dst + r * S + j, make_float4(acc[i][4 * c], acc[i][4 * c + 1], acc[i][4 * c + 2], acc[i][4 * c + 3]));
-        }
+        for (int j = 0; j < Map128::NT; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                st2(dst + Map128::row(tid, i, 2 * h) * S + Map128::col(tid, j, 0), acc[i][j][2 * h],
+                    acc[i][j][2 * h + 1]);
 }
 
 // s <- g s + (diag(w) Xd)^T B across one chunk (sXw: diag(w) Xd, rows tau; sB: the chunk's B
@@ -208,17 +212,19 @@ __device__ __forceinline__ void store_acc128(float* dst, const float (&acc)[4][8
 // the replayed entry states are the forward's bit for bit.  Barriers on both sides.
 __device__ __forceinline__ void state_step(float* sS, const float* sXw, const float* sB, float g, int tid)
 {
-    float acc[4][8];
-    zero_acc(acc);
-    block_gemm<64, 128, 4, 8, true, false>(acc, sXw, LD64, sB, LD128, L, tid);
+    Acc128 acc;
+    zero_mma<64, 128>(acc);
+    block_mma<64, 128, true, false>(acc, sXw, LD64, sB, LD128, L, tid);
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < Map128::MT; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float* x = sS + Map128::row(tid, i) * LD128 + Map128::col(tid, j);
-            *x = __fmaf_rn(g, *x, acc[i][j]);
-        }
+        for (int j = 0; j < Map128::NT; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float* x = sS + Map128::row(tid, i, r) * LD128 + Map128::col(tid, j, r);
+                *x = __fmaf_rn(g, *x, acc[i][j][r]);
+            }
     __syncthreads();
 }
 
@@ -250,8 +256,8 @@ __global__ void __launch_bounds__(CT, 2) ssd_seg_state_kernel(const Args a)
     const Scal sc{sXw + T64};
     const int tid = threadIdx.x;
     const Seg z = seg_of(a);
-    float acc[4][8];
-    zero_acc(acc);
+    Acc128 acc;
+    zero_mma<64, 128>(acc);
     for (int ch = z.ch0; ch < z.ch1; ++ch) {
         const long long t0 = (long long)ch * L;
         const int nt = (int)min((long long)L, a.T - t0);
@@ -261,14 +267,16 @@ __global__ void __launch_bounds__(CT, 2) ssd_seg_state_kernel(const Args a)
         load_bc(sB, a.B, a, z.n, z.g, t0, nt, tid);
         load_xd(nullptr, sXw, a, z.n, z.h, t0, nt, sc, tid);
         __syncthreads();
-        float tmp[4][8];
-        zero_acc(tmp);
-        block_gemm<64, 128, 4, 8, true, false>(tmp, sXw, LD64, sB, LD128, L, tid);
+        Acc128 tmp;
+        zero_mma<64, 128>(tmp);
+        block_mma<64, 128, true, false>(tmp, sXw, LD64, sB, LD128, L, tid);
         const float g = sc.g();
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < Map128::MT; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(g, acc[i][j], tmp[i][j]);
+            for (int j = 0; j < Map128::NT; ++j)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[i][j][r] = __fmaf_rn(g, acc[i][j][r], tmp[i][j][r]);
     }
     float* dst = z.seg + 1 < a.n_ck ? a.ckpt + (z.head * a.n_ck + z.seg + 1) * PS : a.sT + z.head * PS;
     store_acc128(dst, acc, tid);
@@ -326,8 +334,7 @@ __global__ void __launch_bounds__(CT, 1) ssd_output_kernel(const Args a)
     float* sS = sC + T128;   // the state entering the chunk, rows p
     float* sXd = sS + T128;
     float* sM = sXd + T64;   // Lm (.) Q, then diag(w) Xd
-    float* sY = sM + T64;    // diag(e) C s_in^T
-    const Scal sc{sY + T64};
+    const Scal sc{sM + T64};
     const int tid = threadIdx.x;
     const Seg z = seg_of(a);
     load_state(sS, a.ckpt + (z.head * a.n_ck + z.seg) * PS, tid);
@@ -341,40 +348,43 @@ __global__ void __launch_bounds__(CT, 1) ssd_output_kernel(const Args a)
         load_bc(sC, a.C, a, z.n, z.g, t0, nt, tid);
         load_xd(sXd, nullptr, a, z.n, z.h, t0, nt, sc, tid);
         __syncthreads();
-        {  // M = Lm (.) C B^T;  sY = diag(e) C s_in^T
-            float q[4][4], yi[4][4];
-            zero_acc(q);
-            zero_acc(yi);
-            block_gemm<64, 64, 4, 4, false, true>(q, sC, LD128, sB, LD128, S, tid);
-            block_gemm<64, 64, 4, 4, false, true>(yi, sC, LD128, sS, LD128, S, tid);
+        Acc64 yi;  // C s_in^T, rows t, columns p
+        {  // M = Lm (.) C B^T
+            Acc64 q;
+            zero_mma<64, 64>(q);
+            zero_mma<64, 64>(yi);
+            block_mma<64, 64, false, true>(q, sC, LD128, sB, LD128, S, tid);
+            block_mma<64, 64, false, true>(yi, sC, LD128, sS, LD128, S, tid);
             const float* c = sc.c();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = Map64K::row(tid, i);
-                const float e = sc.e()[t];
+            for (int i = 0; i < Map64::MT; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int tau = Map64K::col(tid, j);
-                    sM[t * LD64 + tau] = tau <= t ? __fmul_rn(expf(__fsub_rn(c[t], c[tau])), q[i][j]) : 0.f;
-                    sY[t * LD64 + tau] = __fmul_rn(e, yi[i][j]);
-                }
-            }
+                for (int j = 0; j < Map64::NT; ++j)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int t = Map64::row(tid, i, r), tau = Map64::col(tid, j, r);
+                        sM[t * LD64 + tau] =
+                            tau <= t ? __fmul_rn(expf(__fsub_rn(c[t], c[tau])), q[i][j][r]) : 0.f;
+                    }
         }
         __syncthreads();
-        {  // y = M Xd + sY
-            float yy[4][4];
-            zero_acc(yy);
-            block_gemm<64, 64, 4, 4, false, false>(yy, sM, LD64, sXd, LD64, L, tid);
+        {  // y = M Xd + diag(e) C s_in^T
+            Acc64 yy;
+            zero_mma<64, 64>(yy);
+            block_mma<64, 64, false, false>(yy, sM, LD64, sXd, LD64, L, tid);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = Map64::row(tid, i), p = Map64::col(tid, 0);
-                if (t < nt) {
-                    const float4 yi = ld4(sY + t * LD64 + p);
-                    st4(a.y + ((z.n * a.T + t0 + t) * a.H + z.h) * P + p,
-                        make_float4(__fadd_rn(yy[i][0], yi.x), __fadd_rn(yy[i][1], yi.y), __fadd_rn(yy[i][2], yi.z),
-                                    __fadd_rn(yy[i][3], yi.w)));
+            for (int i = 0; i < Map64::MT; ++i)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = Map64::row(tid, i, 2 * h);
+                    if (t >= nt) continue;
+                    const float e = sc.e()[t];
+                    float* yrow = a.y + ((z.n * a.T + t0 + t) * a.H + z.h) * P;
+#pragma unroll
+                    for (int j = 0; j < Map64::NT; ++j)
+                        st2(yrow + Map64::col(tid, j, 0), __fmaf_rn(e, yi[i][j][2 * h], yy[i][j][2 * h]),
+                            __fmaf_rn(e, yi[i][j][2 * h + 1], yy[i][j][2 * h + 1]));
                 }
-            }
         }
         if (ch + 1 < z.ch1) {  // carry the state to the next chunk of the segment
             __syncthreads();
@@ -419,9 +429,9 @@ __global__ void __launch_bounds__(CT, 2) ssd_dprep_kernel(const Args a)
             st4(sYe + t * LD64 + 4 * q, mul4(head_row4(a.dy, a, z.n, z.h, t0, t, q, nt), sc.e()[t]));
         }
         __syncthreads();
-        float acc[4][8];
-        zero_acc(acc);
-        block_gemm<64, 128, 4, 8, true, false>(acc, sYe, LD64, sC, LD128, L, tid);
+        Acc128 acc;
+        zero_mma<64, 128>(acc);
+        block_mma<64, 128, true, false>(acc, sYe, LD64, sC, LD128, L, tid);
         store_acc128(a.dd + slot, acc, tid);
         if (replay && ch + 1 < z.ch1) {
             __syncthreads();
@@ -485,8 +495,8 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
     float* sdY = sXw + T64;
     float* sM = sdY + T64;   // Lm (.) Q
     float* sdQ = sM + T64;   // Lm (.) dM
-    float* sU = sdQ + T64;   // diag(e) dY, then u = B dS_out^T
-    float* pRow = sU + T64;       // [L][4] row sums of M (.) dM
+    float* sYe = sdQ + T64;  // diag(e) dY
+    float* pRow = sYe + T64;      // [L][4] row sums of M (.) dM
     float* pCol = pRow + 4 * L;   // [L][2] column sums of M (.) dM
     float* pInt = pCol + 2 * L;   // [L][4] sum_p diag(e) dY (C s_in^T)
     float* pV = pInt + 4 * L;     // [L][4] sum_p Xd u
@@ -503,8 +513,8 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
     const long long h0 = g * hpg + (long long)hb * a.HB;
     const long long t0 = (long long)ch * L;
     const int nt = (int)min((long long)L, a.T - t0);
-    const int lr = lane >> 2, lc = lane & 3;
-    const int wr = Map64::wr(tid), wc = Map64::wc(tid);  // the same for the three layouts
+    const int gq = lane >> 2, tq = lane & 3;
+    const int wr = Map64::wr(tid), wc = Map64::wc(tid);  // the same for both output shapes
     const int seg = ch / a.m;
     const bool at_ck = ch == seg * a.m;
 
@@ -512,17 +522,19 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
     load_bc(sC, a.C, a, n, g, t0, nt, tid);
     __syncthreads();
     {  // Q = C B^T, shared by the block's heads
-        float q[4][4];
-        zero_acc(q);
-        block_gemm<64, 64, 4, 4, false, true>(q, sC, LD128, sB, LD128, S, tid);
+        Acc64 q;
+        zero_mma<64, 64>(q);
+        block_mma<64, 64, false, true>(q, sC, LD128, sB, LD128, S, tid);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < Map64::MT; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sQ[Map64K::row(tid, i) * LD64 + Map64K::col(tid, j)] = q[i][j];
+            for (int j = 0; j < Map64::NT; ++j)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sQ[Map64::row(tid, i, r) * LD64 + Map64::col(tid, j, r)] = q[i][j][r];
     }
-    float accB[4][8], accC[4][8];
-    zero_acc(accB);
-    zero_acc(accC);
+    Acc128 accB, accC;
+    zero_mma<64, 128>(accB);
+    zero_mma<64, 128>(accC);
 
     for (int hh = 0; hh < a.HB; ++hh) {
         const long long h = h0 + hh;
@@ -538,24 +550,29 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
             st4(sXd + t * LD64 + 4 * q, xd);
             st4(sXw + t * LD64 + 4 * q, mul4(xd, sc.w()[t]));
             st4(sdY + t * LD64 + 4 * q, dy);
-            st4(sU + t * LD64 + 4 * q, mul4(dy, sc.e()[t]));
+            st4(sYe + t * LD64 + 4 * q, mul4(dy, sc.e()[t]));
         }
         load_state(sSt, at_ck ? a.ckpt_in + (head * a.n_ck + seg) * PS : a.sin_all + slot, tid);
         __syncthreads();
         {  // with s_in: sum_p diag(e) dY (C s_in^T) per row; dC += diag(e) dY s_in
-            float yi[4][4];
-            zero_acc(yi);
-            block_gemm<64, 64, 4, 4, false, true>(yi, sC, LD128, sSt, LD128, S, tid);
+            Acc64 yi;
+            zero_mma<64, 64>(yi);
+            block_mma<64, 64, false, true>(yi, sC, LD128, sSt, LD128, S, tid);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = Map64K::row(tid, i);
-                float v = 0.f;
+            for (int i = 0; i < Map64::MT; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) v = __fmaf_rn(sU[t * LD64 + Map64K::col(tid, j)], yi[i][j], v);
-                v = row_lanes(v);
-                if (lc == 0) pInt[t * 4 + wc] = v;
-            }
-            block_gemm<64, 128, 4, 8, false, false>(accC, sU, LD64, sSt, LD128, P, tid);
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int t = Map64::row(tid, i, 2 * hr);
+                    float v = 0.f;
+#pragma unroll
+                    for (int j = 0; j < Map64::NT; ++j)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            v = __fmaf_rn(sYe[t * LD64 + Map64::col(tid, j, e)], yi[i][j][2 * hr + e], v);
+                    v = row_lanes(v);
+                    if (tq == 0) pInt[t * 4 + wc] = v;
+                }
+            block_mma<64, 128, false, false>(accC, sYe, LD64, sSt, LD128, P, tid);
         }
         __syncthreads();
         {  // dS_out over s_in, and <dS_out, s_in>
@@ -573,71 +590,86 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
             if (lane == 0) red[warp] = v;
         }
         __syncthreads();
-        {  // dM = dY Xd^T; M, dQ; the rows and columns of M (.) dM; u = B dS_out^T; sum_p Xd u
-            float dm[4][4], u[4][4];
-            zero_acc(dm);
-            zero_acc(u);
-            block_gemm<64, 64, 4, 4, false, true>(dm, sdY, LD64, sXd, LD64, P, tid);
-            block_gemm<64, 64, 4, 4, false, true>(u, sB, LD128, sSt, LD128, S, tid);
+        Acc64 u;  // B dS_out^T: rows tokens, columns channels
+        {  // dM = dY Xd^T; M, dQ; the rows and columns of M (.) dM; u; sum_p Xd u
+            Acc64 dm;
+            zero_mma<64, 64>(dm);
+            zero_mma<64, 64>(u);
+            block_mma<64, 64, false, true>(dm, sdY, LD64, sXd, LD64, P, tid);
+            block_mma<64, 64, false, true>(u, sB, LD128, sSt, LD128, S, tid);
             const float* c = sc.c();
-            float cs[4] = {0.f, 0.f, 0.f, 0.f};
+            float cs[Map64::NT][2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = Map64K::row(tid, i);
-                float rs = 0.f, vs = 0.f;
+            for (int j = 0; j < Map64::NT; ++j) cs[j][0] = cs[j][1] = 0.f;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int tau = Map64K::col(tid, j);
-                    const float lm = tau <= t ? expf(__fsub_rn(c[t], c[tau])) : 0.f;
-                    const float m = __fmul_rn(lm, sQ[t * LD64 + tau]);
-                    sM[t * LD64 + tau] = m;
-                    sdQ[t * LD64 + tau] = __fmul_rn(lm, dm[i][j]);
-                    const float r = __fmul_rn(m, dm[i][j]);
-                    rs = __fadd_rn(rs, r);
-                    cs[j] = __fadd_rn(cs[j], r);
-                    // u's row is token t here (B's rows), its column channel tau
-                    vs = __fmaf_rn(sXd[t * LD64 + tau], u[i][j], vs);
-                    sU[t * LD64 + tau] = u[i][j];
+            for (int i = 0; i < Map64::MT; ++i)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int t = Map64::row(tid, i, 2 * hr);
+                    float rs = 0.f, vs = 0.f;
+#pragma unroll
+                    for (int j = 0; j < Map64::NT; ++j)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int r = 2 * hr + e;
+                            const int tau = Map64::col(tid, j, r);
+                            const float lm = tau <= t ? expf(__fsub_rn(c[t], c[tau])) : 0.f;
+                            const float m = __fmul_rn(lm, sQ[t * LD64 + tau]);
+                            sM[t * LD64 + tau] = m;
+                            sdQ[t * LD64 + tau] = __fmul_rn(lm, dm[i][j][r]);
+                            const float R = __fmul_rn(m, dm[i][j][r]);
+                            rs = __fadd_rn(rs, R);
+                            cs[j][e] = __fadd_rn(cs[j][e], R);
+                            // u's row is token t here, its column channel tau
+                            vs = __fmaf_rn(sXd[t * LD64 + tau], u[i][j][r], vs);
+                        }
+                    rs = row_lanes(rs);
+                    vs = row_lanes(vs);
+                    if (tq == 0) {
+                        pRow[t * 4 + wc] = rs;
+                        pV[t * 4 + wc] = vs;
+                    }
                 }
-                rs = row_lanes(rs);
-                vs = row_lanes(vs);
-                if (lc == 0) {
-                    pRow[t * 4 + wc] = rs;
-                    pV[t * 4 + wc] = vs;
-                }
-            }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float v = col_lanes(cs[j]);
-                if (lr == 0) pCol[Map64K::col(tid, j) * 2 + wr] = v;
-            }
+            for (int j = 0; j < Map64::NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float v = col_lanes(cs[j][e]);
+                    if (gq == 0) pCol[Map64::col(tid, j, e) * 2 + wr] = v;
+                }
         }
         __syncthreads();
         {  // dXd = M^T dY + diag(w) u; dx; sum_p x dXd
-            float dxd[4][4];
-            zero_acc(dxd);
-            block_gemm<64, 64, 4, 4, true, false>(dxd, sM, LD64, sdY, LD64, L, tid);
+            Acc64 dxd;
+            zero_mma<64, 64>(dxd);
+            block_mma<64, 64, true, false>(dxd, sM, LD64, sdY, LD64, L, tid);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tau = Map64::row(tid, i), p = Map64::col(tid, 0);
-                const float w = sc.w()[tau], d = sc.dt()[tau];
-                const float4 uu = ld4(sU + tau * LD64 + p);
-                const float g0 = __fmaf_rn(w, uu.x, dxd[i][0]), g1 = __fmaf_rn(w, uu.y, dxd[i][1]);
-                const float g2 = __fmaf_rn(w, uu.z, dxd[i][2]), g3 = __fmaf_rn(w, uu.w, dxd[i][3]);
-                float xs = 0.f;
-                if (tau < nt) {
-                    const long long o = ((n * a.T + t0 + tau) * a.H + h) * P + p;
-                    xs = dot4(ld4(a.x + o), make_float4(g0, g1, g2, g3), 0.f);
-                    st4(a.dx + o, make_float4(__fmul_rn(d, g0), __fmul_rn(d, g1), __fmul_rn(d, g2), __fmul_rn(d, g3)));
+            for (int i = 0; i < Map64::MT; ++i)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int tau = Map64::row(tid, i, 2 * hr);
+                    const float w = sc.w()[tau], d = sc.dt()[tau];
+                    float xs = 0.f;
+                    const long long o = ((n * a.T + t0 + tau) * a.H + h) * P;
+#pragma unroll
+                    for (int j = 0; j < Map64::NT; ++j) {
+                        const int p = Map64::col(tid, j, 0);
+                        const float g0 = __fmaf_rn(w, u[i][j][2 * hr], dxd[i][j][2 * hr]);
+                        const float g1 = __fmaf_rn(w, u[i][j][2 * hr + 1], dxd[i][j][2 * hr + 1]);
+                        if (tau < nt) {
+                            const float2 xv = *reinterpret_cast<const float2*>(a.x + o + p);
+                            xs = __fmaf_rn(xv.y, g1, __fmaf_rn(xv.x, g0, xs));
+                            st2(a.dx + o + p, __fmul_rn(d, g0), __fmul_rn(d, g1));
+                        }
+                    }
+                    xs = row_lanes(xs);
+                    if (tq == 0) pX[tau * 4 + wc] = xs;
                 }
-                xs = row_lanes(xs);
-                if (lc == 0) pX[tau * 4 + wc] = xs;
-            }
         }
         // dC += dQ B;  dB += dQ^T C + diag(w) Xd dS_out
-        block_gemm<64, 128, 4, 8, false, false>(accC, sdQ, LD64, sB, LD128, L, tid);
-        block_gemm<64, 128, 4, 8, true, false>(accB, sdQ, LD64, sC, LD128, L, tid);
-        block_gemm<64, 128, 4, 8, false, false>(accB, sXw, LD64, sSt, LD128, P, tid);
+        block_mma<64, 128, false, false>(accC, sdQ, LD64, sB, LD128, L, tid);
+        block_mma<64, 128, true, false>(accB, sdQ, LD64, sC, LD128, L, tid);
+        block_mma<64, 128, false, false>(accB, sXw, LD64, sSt, LD128, P, tid);
         __syncthreads();
         if (warp == 0) {  // dc, its reverse running sum, ddt
 #pragma unroll
@@ -680,17 +712,19 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
     // this block's dB, dC partial: rows t < nt
     float* part = a.partBC + (long long)hb * 2 * S;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = Map128::row(tid, i);
-        if (t >= nt) continue;
-        float* row = part + ((n * a.T + t0 + t) * a.G + g) * (long long)a.nhb * 2 * S;
+    for (int i = 0; i < Map128::MT; ++i)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int j = Map128::col(tid, 4 * c);
-            st4(row + j, make_float4(accB[i][4 * c], accB[i][4 * c + 1], accB[i][4 * c + 2], accB[i][4 * c + 3]));
-            st4(row + S + j, make_float4(accC[i][4 * c], accC[i][4 * c + 1], accC[i][4 * c + 2], accC[i][4 * c + 3]));
+        for (int hr = 0; hr < 2; ++hr) {
+            const int t = Map128::row(tid, i, 2 * hr);
+            if (t >= nt) continue;
+            float* row = part + ((n * a.T + t0 + t) * a.G + g) * (long long)a.nhb * 2 * S;
+#pragma unroll
+            for (int j = 0; j < Map128::NT; ++j) {
+                const int c = Map128::col(tid, j, 0);
+                st2(row + c, accB[i][j][2 * hr], accB[i][j][2 * hr + 1]);
+                st2(row + S + c, accC[i][j][2 * hr], accC[i][j][2 * hr + 1]);
+            }
         }
-    }
 }
 
 // Backward 4: dB, dC of each token: its group's block partials summed in ascending order.
@@ -713,7 +747,7 @@ __global__ void __launch_bounds__(256) ssd_reduce_kernel(const Args a)
 // Host side.
 
 constexpr size_t kSmemSegState = sizeof(float) * (T128 + T64 + NSCAL);
-constexpr size_t kSmemOutput = sizeof(float) * (3 * T128 + 3 * T64 + NSCAL);
+constexpr size_t kSmemOutput = sizeof(float) * (3 * T128 + 2 * T64 + NSCAL);
 constexpr size_t kSmemDprep1 = sizeof(float) * (T128 + T64 + NSCAL);
 constexpr size_t kSmemDprepR = sizeof(float) * (3 * T128 + T64 + NSCAL);
 constexpr size_t kSmemGrad = sizeof(float) * (3 * T128 + 7 * T64 + 18 * L + L + 8 + NSCAL);

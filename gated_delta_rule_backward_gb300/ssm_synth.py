@@ -75,6 +75,8 @@ SSM_WORKLOADS = {
     # the two layers cut to 512 tokens, for kernel captures of a few hundred MB
     "profile_mamba2_h80_T512": dict(N=1, T=512, H=80, P=64, S=128, G=1, mamba1=False, K=16, seed=11),
     "profile_mamba1_d1536_T512": dict(N=1, T=512, H=1536, P=1, S=16, G=1, mamba1=True, K=16, seed=12),
+    # the Mamba-2 layer in chunked form at 2048 tokens (about 0.5 GB on the device)
+    "profile_mamba2_h80_T2048": dict(N=1, T=2048, H=80, P=64, S=128, G=1, mamba1=False, K=64, seed=11),
 }
 
 
