@@ -25,14 +25,19 @@
 // the end of the sequence enter as dt = 0 and x = B = C = dy = 0, which changes nothing.
 //
 // Kernels (L = 64 tokens, P = 64 channels, S = 128 states; a segment is the m = K / L chunks
-// between two checkpoints):
-//   forward   ssd_seg_state_kernel  (segment, head): dS of the segment from a zero state
+// between two checkpoints).  With one chunk a segment (m = 1) the chunk kernels take a block of
+// HB heads of one group, whose B, C and Q they load or compute once; with several, one head
+// and walk the segment's chunks:
+//   forward   ssd_state_hb_kernel / ssd_seg_state_kernel
+//                                   dS of the segment from a zero state, and its decay G
 //             ssd_chain_kernel      (state slice, head): s_{k+1} = G_k s_k + dS_k over the
-//                                   segments (G_k the segment's decay): the checkpoints, s_T
-//             ssd_output_kernel     (segment, head): y of each chunk from its entry state,
-//                                   the state carried across the segment's chunks
-//   backward  ssd_dprep_kernel      (segment, head): (diag(e) dY)^T C of each chunk, g, and the
-//                                   entry states of the segment's inner chunks (m > 1)
+//                                   segments: the checkpoints, s_T
+//             ssd_output_hb_kernel / ssd_output_kernel
+//                                   y of each chunk from its entry state (m > 1: the state
+//                                   carried across the segment's chunks)
+//   backward  ssd_dprep_hb_kernel / ssd_dprep_kernel
+//                                   (diag(e) dY)^T C of each chunk, g, and the entry states of
+//                                   the segment's inner chunks (m > 1)
 //             ssd_dchain_kernel     (state slice, head): dS_out of every chunk, last first; d_s
 //             ssd_grad_kernel       (chunk, block of HB heads of a group): every gradient of
 //                                   the chunk; dB, dC summed over the block's heads in registers
@@ -109,20 +114,6 @@ struct Scal {
     __device__ float* w() const { return p + 3 * L; }
     __device__ float& g() const { return p[4 * L]; }
 };
-
-// The decay sum of a chunk's tokens, in token order (dt = 0 past the end).  The chain kernels
-// recompute a chunk's c_{L-1} with the same loop, so every kernel has the same g.
-__device__ __forceinline__ float chunk_logdecay(const float* dt, long long T, long long H, long long n, long long h,
-                                                long long t0, float A)
-{
-    float c = 0.f;
-#pragma unroll 8
-    for (int t = 0; t < L; ++t) {
-        const float d = t0 + t < T ? dt[(n * T + t0 + t) * H + h] : 0.f;
-        c = __fadd_rn(c, __fmul_rn(d, A));
-    }
-    return c;
-}
 
 // dt, c, e, w, g of chunk [t0, t0 + L) of head h.  Ends without a barrier.
 __device__ __forceinline__ void load_scalars(const Args& a, long long n, long long h, long long t0, int nt,
@@ -245,8 +236,61 @@ __device__ __forceinline__ Seg seg_of(const Args& a)
     return s;
 }
 
+// A block of HB heads of one group at one chunk: grid (nch, G nhb, N).
+struct Blk {
+    long long n, g, h0, t0;
+    int ch, hb, nt;
+};
+__device__ __forceinline__ Blk blk_of(const Args& a)
+{
+    Blk b;
+    b.ch = blockIdx.x;
+    b.n = blockIdx.z;
+    b.g = blockIdx.y / a.nhb;
+    b.hb = (int)(blockIdx.y - b.g * a.nhb);
+    b.h0 = b.g * (a.H / a.G) + (long long)b.hb * a.HB;
+    b.t0 = (long long)b.ch * L;
+    b.nt = (int)min((long long)L, a.T - b.t0);
+    return b;
+}
+
+// The forward's segment decays G_k wait for the chain in the y region of the output, which the
+// output kernels overwrite afterwards: float (n n_ck + k) H + h (n_ck <= T, so it fits).
+__device__ __forceinline__ float* decay_slot(const Args& a, long long n, long long k, long long h)
+{
+    return a.y + (n * a.n_ck + k) * a.H + h;
+}
+
 // ---------------------------------------------------------------------------------
-// Forward 1: dS of each segment (its state change from a zero entry state), into the slot
+// Forward 1, one chunk a segment: dS of chunk ch for HB heads into the slot the chain turns
+// into checkpoint ch + 1 (the last chunk's into s_T), and g.  Grid (nch, G nhb, N).
+__global__ void __launch_bounds__(CT, 2) ssd_state_hb_kernel(const Args a)
+{
+    extern __shared__ __align__(16) float sm[];
+    float* sB = sm;
+    float* sXw = sB + T128;
+    const Scal sc{sXw + T64};
+    const int tid = threadIdx.x;
+    const Blk b = blk_of(a);
+    load_bc(sB, a.B, a, b.n, b.g, b.t0, b.nt, tid);
+    for (int hh = 0; hh < a.HB; ++hh) {
+        const long long h = b.h0 + hh, head = b.n * a.H + h;
+        __syncthreads();
+        load_scalars(a, b.n, h, b.t0, b.nt, sc, tid);
+        __syncthreads();
+        load_xd(nullptr, sXw, a, b.n, h, b.t0, b.nt, sc, tid);
+        __syncthreads();
+        Acc128 acc;
+        zero_mma<64, 128>(acc);
+        block_mma<64, 128, true, false>(acc, sXw, LD64, sB, LD128, L, tid);
+        float* dst = b.ch + 1 < a.n_ck ? a.ckpt + (head * a.n_ck + b.ch + 1) * PS : a.sT + head * PS;
+        store_acc128(dst, acc, tid);
+        if (tid == 0) *decay_slot(a, b.n, b.ch, h) = sc.g();
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// Forward 1, several chunks a segment: dS of each segment (its state change from a zero entry state), into the slot
 // the chain turns into the next checkpoint (the last segment's into s_T).  Grid (n_ck, H, N).
 __global__ void __launch_bounds__(CT, 2) ssd_seg_state_kernel(const Args a)
 {
@@ -258,6 +302,7 @@ __global__ void __launch_bounds__(CT, 2) ssd_seg_state_kernel(const Args a)
     const Seg z = seg_of(a);
     Acc128 acc;
     zero_mma<64, 128>(acc);
+    float G = 1.f;  // the segment's decay, the product of its chunks' g in order
     for (int ch = z.ch0; ch < z.ch1; ++ch) {
         const long long t0 = (long long)ch * L;
         const int nt = (int)min((long long)L, a.T - t0);
@@ -271,6 +316,7 @@ __global__ void __launch_bounds__(CT, 2) ssd_seg_state_kernel(const Args a)
         zero_mma<64, 128>(tmp);
         block_mma<64, 128, true, false>(tmp, sXw, LD64, sB, LD128, L, tid);
         const float g = sc.g();
+        G = __fmul_rn(G, g);
 #pragma unroll
         for (int i = 0; i < Map128::MT; ++i)
 #pragma unroll
@@ -280,6 +326,7 @@ __global__ void __launch_bounds__(CT, 2) ssd_seg_state_kernel(const Args a)
     }
     float* dst = z.seg + 1 < a.n_ck ? a.ckpt + (z.head * a.n_ck + z.seg + 1) * PS : a.sT + z.head * PS;
     store_acc128(dst, acc, tid);
+    if (tid == 0) *decay_slot(a, z.n, z.seg, z.h) = G;
 }
 
 // Forward 2: the chain over segments, one float4 of one head's state a thread.  Grid
@@ -290,7 +337,6 @@ __global__ void __launch_bounds__(CT) ssd_chain_kernel(const Args a)
     const int tid = threadIdx.x;
     const long long h = blockIdx.y, n = blockIdx.z, head = n * a.H + h;
     const long long off = 4LL * (blockIdx.x * CT + tid);
-    const float A = a.A[h];
     float* ck = a.ckpt + head * a.n_ck * PS + off;
     float* sTp = a.sT + head * PS + off;
     auto slot = [&](int k) { return k + 1 < a.n_ck ? ck + (long long)(k + 1) * PS : sTp; };
@@ -301,14 +347,7 @@ __global__ void __launch_bounds__(CT) ssd_chain_kernel(const Args a)
     for (int k = 0; k < 4; ++k) buf[k] = k < a.n_ck ? ld4(slot(k)) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int base = 0; base < a.n_ck; base += CT) {
         __syncthreads();
-        const int k = base + tid;
-        if (k < a.n_ck) {  // the segment's decay: the product of its chunks' g, in order
-            float G = 1.f;
-            const int c1 = min(a.nch, (k + 1) * a.m);
-            for (int ch = k * a.m; ch < c1; ++ch)
-                G = __fmul_rn(G, expf(chunk_logdecay(a.dt, a.T, a.H, n, h, (long long)ch * L, A)));
-            gs[tid] = G;
-        }
+        if (base + tid < a.n_ck) gs[tid] = *decay_slot(a, n, base + tid, h);
         __syncthreads();
         const int nb = min(CT, a.n_ck - base);
         for (int k0 = 0; k0 < nb; k0 += 4) {
@@ -325,7 +364,80 @@ __global__ void __launch_bounds__(CT) ssd_chain_kernel(const Args a)
     }
 }
 
-// Forward 3: y of every chunk of a segment from the segment's checkpoint.  Grid (n_ck, H, N).
+// Forward 3, one chunk a segment: y of chunk ch for HB heads from checkpoint ch, Q = C B^T
+// computed once.  Grid (nch, G nhb, N).
+__global__ void __launch_bounds__(CT, 1) ssd_output_hb_kernel(const Args a)
+{
+    extern __shared__ __align__(16) float sm[];
+    float* sB = sm;
+    float* sC = sB + T128;
+    float* sS = sC + T128;   // the state entering the chunk, rows p
+    float* sQ = sS + T128;   // C B^T
+    float* sXd = sQ + T64;
+    float* sM = sXd + T64;   // Lm (.) Q
+    const Scal sc{sM + T64};
+    const int tid = threadIdx.x;
+    const Blk b = blk_of(a);
+    load_bc(sB, a.B, a, b.n, b.g, b.t0, b.nt, tid);
+    load_bc(sC, a.C, a, b.n, b.g, b.t0, b.nt, tid);
+    __syncthreads();
+    {
+        Acc64 q;
+        zero_mma<64, 64>(q);
+        block_mma<64, 64, false, true>(q, sC, LD128, sB, LD128, S, tid);
+#pragma unroll
+        for (int i = 0; i < Map64::MT; ++i)
+#pragma unroll
+            for (int j = 0; j < Map64::NT; ++j)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sQ[Map64::row(tid, i, r) * LD64 + Map64::col(tid, j, r)] = q[i][j][r];
+    }
+    for (int hh = 0; hh < a.HB; ++hh) {
+        const long long h = b.h0 + hh, head = b.n * a.H + h;
+        __syncthreads();
+        load_scalars(a, b.n, h, b.t0, b.nt, sc, tid);
+        __syncthreads();
+        load_xd(sXd, nullptr, a, b.n, h, b.t0, b.nt, sc, tid);
+        load_state(sS, a.ckpt + (head * a.n_ck + b.ch) * PS, tid);
+        __syncthreads();
+        Acc64 yi;  // C s_in^T, rows t, columns p
+        zero_mma<64, 64>(yi);
+        block_mma<64, 64, false, true>(yi, sC, LD128, sS, LD128, S, tid);
+        {
+            const float* c = sc.c();
+#pragma unroll
+            for (int i = 0; i < Map64::MT; ++i)
+#pragma unroll
+                for (int j = 0; j < Map64::NT; ++j)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int t = Map64::row(tid, i, r), tau = Map64::col(tid, j, r);
+                        sM[t * LD64 + tau] =
+                            tau <= t ? __fmul_rn(expf(__fsub_rn(c[t], c[tau])), sQ[t * LD64 + tau]) : 0.f;
+                    }
+        }
+        __syncthreads();
+        Acc64 yy;
+        zero_mma<64, 64>(yy);
+        block_mma<64, 64, false, false>(yy, sM, LD64, sXd, LD64, L, tid);
+#pragma unroll
+        for (int i = 0; i < Map64::MT; ++i)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int t = Map64::row(tid, i, 2 * hr);
+                if (t >= b.nt) continue;
+                const float e = sc.e()[t];
+                float* yrow = a.y + ((b.n * a.T + b.t0 + t) * a.H + h) * P;
+#pragma unroll
+                for (int j = 0; j < Map64::NT; ++j)
+                    st2(yrow + Map64::col(tid, j, 0), __fmaf_rn(e, yi[i][j][2 * hr], yy[i][j][2 * hr]),
+                        __fmaf_rn(e, yi[i][j][2 * hr + 1], yy[i][j][2 * hr + 1]));
+            }
+    }
+}
+
+// Forward 3, several chunks a segment: y of every chunk of a segment from the segment's
+// checkpoint.  Grid (n_ck, H, N).
 __global__ void __launch_bounds__(CT, 1) ssd_output_kernel(const Args a)
 {
     extern __shared__ __align__(16) float sm[];
@@ -399,9 +511,39 @@ __global__ void __launch_bounds__(CT, 1) ssd_output_kernel(const Args a)
 }
 
 // ---------------------------------------------------------------------------------
-// Backward 1: per chunk of a segment, (diag(e) dY)^T C into its dd slot and g into gvec; for
-// m > 1 also the entry states of the segment's inner chunks (sin_all), replayed from the
-// checkpoint by the forward's own step.  Grid (n_ck, H, N).
+// Backward 1, one chunk a segment: (diag(e) dY)^T C of chunk ch for HB heads into their dd
+// slots, g into gvec.  Grid (nch, G nhb, N).
+__global__ void __launch_bounds__(CT, 2) ssd_dprep_hb_kernel(const Args a)
+{
+    extern __shared__ __align__(16) float sm[];
+    float* sC = sm;
+    float* sYe = sC + T128;  // diag(e) dY
+    const Scal sc{sYe + T64};
+    const int tid = threadIdx.x;
+    const Blk b = blk_of(a);
+    load_bc(sC, a.C, a, b.n, b.g, b.t0, b.nt, tid);
+    for (int hh = 0; hh < a.HB; ++hh) {
+        const long long h = b.h0 + hh;
+        const long long slot = ((b.n * a.nch + b.ch) * a.H + h) * PS;
+        __syncthreads();
+        load_scalars(a, b.n, h, b.t0, b.nt, sc, tid);
+        __syncthreads();
+        if (tid == 0) a.gvec[(b.n * a.nch + b.ch) * a.H + h] = sc.g();
+        for (int i = tid; i < L * P / 4; i += CT) {
+            const int t = i / (P / 4), q = i - t * (P / 4);
+            st4(sYe + t * LD64 + 4 * q, mul4(head_row4(a.dy, a, b.n, h, b.t0, t, q, b.nt), sc.e()[t]));
+        }
+        __syncthreads();
+        Acc128 acc;
+        zero_mma<64, 128>(acc);
+        block_mma<64, 128, true, false>(acc, sYe, LD64, sC, LD128, L, tid);
+        store_acc128(a.dd + slot, acc, tid);
+    }
+}
+
+// Backward 1, several chunks a segment: per chunk of a segment, (diag(e) dY)^T C into its dd
+// slot and g into gvec, and the entry states of the segment's inner chunks (sin_all),
+// replayed from the checkpoint by the forward's own step.  Grid (n_ck, H, N).
 __global__ void __launch_bounds__(CT, 2) ssd_dprep_kernel(const Args a)
 {
     extern __shared__ __align__(16) float sm[];
@@ -554,25 +696,28 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
         }
         load_state(sSt, at_ck ? a.ckpt_in + (head * a.n_ck + seg) * PS : a.sin_all + slot, tid);
         __syncthreads();
-        {  // with s_in: sum_p diag(e) dY (C s_in^T) per row; dC += diag(e) dY s_in
-            Acc64 yi;
-            zero_mma<64, 64>(yi);
-            block_mma<64, 64, false, true>(yi, sC, LD128, sSt, LD128, S, tid);
+        {  // with s_in: E = diag(e) dY s_in; dC += E, and sum_p diag(e) dY (C s_in^T) per row,
+           // which is sum_j C (.) E
+            Acc128 E;
+            zero_mma<64, 128>(E);
+            block_mma<64, 128, false, false>(E, sYe, LD64, sSt, LD128, P, tid);
 #pragma unroll
-            for (int i = 0; i < Map64::MT; ++i)
+            for (int i = 0; i < Map128::MT; ++i)
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
-                    const int t = Map64::row(tid, i, 2 * hr);
+                    const int t = Map128::row(tid, i, 2 * hr);
                     float v = 0.f;
 #pragma unroll
-                    for (int j = 0; j < Map64::NT; ++j)
+                    for (int j = 0; j < Map128::NT; ++j)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e)
-                            v = __fmaf_rn(sYe[t * LD64 + Map64::col(tid, j, e)], yi[i][j][2 * hr + e], v);
+                        for (int e = 0; e < 2; ++e) {
+                            const int r = 2 * hr + e;
+                            v = __fmaf_rn(sC[t * LD128 + Map128::col(tid, j, r)], E[i][j][r], v);
+                            accC[i][j][r] = __fadd_rn(accC[i][j][r], E[i][j][r]);
+                        }
                     v = row_lanes(v);
                     if (tq == 0) pInt[t * 4 + wc] = v;
                 }
-            block_mma<64, 128, false, false>(accC, sYe, LD64, sSt, LD128, P, tid);
         }
         __syncthreads();
         {  // dS_out over s_in, and <dS_out, s_in>
@@ -748,6 +893,7 @@ __global__ void __launch_bounds__(256) ssd_reduce_kernel(const Args a)
 
 constexpr size_t kSmemSegState = sizeof(float) * (T128 + T64 + NSCAL);
 constexpr size_t kSmemOutput = sizeof(float) * (3 * T128 + 2 * T64 + NSCAL);
+constexpr size_t kSmemOutputHb = sizeof(float) * (3 * T128 + 3 * T64 + NSCAL);
 constexpr size_t kSmemDprep1 = sizeof(float) * (T128 + T64 + NSCAL);
 constexpr size_t kSmemDprepR = sizeof(float) * (3 * T128 + T64 + NSCAL);
 constexpr size_t kSmemGrad = sizeof(float) * (3 * T128 + 7 * T64 + 18 * L + L + 8 + NSCAL);
@@ -797,18 +943,24 @@ static int launch(Kern kern, dim3 grid, size_t smem, const Args& a, cudaStream_t
 int forward(const Args& a, cudaStream_t st)
 {
     const unsigned H = (unsigned)a.H, N = (unsigned)a.N, nck = (unsigned)a.n_ck;
-    int e = launch(ssd_seg_state_kernel, dim3(nck, H, N), kSmemSegState, a, st);
+    const dim3 blk((unsigned)a.nch, (unsigned)(a.G * a.nhb), N);
+    int e = a.m == 1 ? launch(ssd_state_hb_kernel, blk, kSmemSegState, a, st)
+                     : launch(ssd_seg_state_kernel, dim3(nck, H, N), kSmemSegState, a, st);
     if (!e) e = launch(ssd_chain_kernel, dim3(SLICES, H, N), 0, a, st);
-    if (!e) e = launch(ssd_output_kernel, dim3(nck, H, N), kSmemOutput, a, st);
+    if (!e)
+        e = a.m == 1 ? launch(ssd_output_hb_kernel, blk, kSmemOutputHb, a, st)
+                     : launch(ssd_output_kernel, dim3(nck, H, N), kSmemOutput, a, st);
     return e;
 }
 
 int backward(const Args& a, cudaStream_t st)
 {
     const unsigned H = (unsigned)a.H, N = (unsigned)a.N, nck = (unsigned)a.n_ck;
-    int e = launch(ssd_dprep_kernel, dim3(nck, H, N), a.m > 1 ? kSmemDprepR : kSmemDprep1, a, st);
+    const dim3 blk((unsigned)a.nch, (unsigned)(a.G * a.nhb), N);
+    int e = a.m == 1 ? launch(ssd_dprep_hb_kernel, blk, kSmemDprep1, a, st)
+                     : launch(ssd_dprep_kernel, dim3(nck, H, N), kSmemDprepR, a, st);
     if (!e) e = launch(ssd_dchain_kernel, dim3(SLICES, H, N), 0, a, st);
-    if (!e) e = launch(ssd_grad_kernel, dim3((unsigned)a.nch, (unsigned)(a.G * a.nhb), N), kSmemGrad, a, st);
+    if (!e) e = launch(ssd_grad_kernel, blk, kSmemGrad, a, st);
     if (!e) {
         ssd_reduce_kernel<<<(unsigned)(a.N * a.T), 256, 0, st>>>(a);
         e = (int)cudaGetLastError();
