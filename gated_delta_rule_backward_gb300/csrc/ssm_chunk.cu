@@ -659,6 +659,20 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
     const int wr = Map64::wr(tid), wc = Map64::wc(tid);  // the same for both output shapes
     const int seg = ch / a.m;
     const bool at_ck = ch == seg * a.m;
+    // A head's x, dy rows, s_in and dS_out into L2 ahead of their loads (the first head's now,
+    // each next one's while the current one computes): 3 lines of 128 bytes a thread.
+    auto prefetch_head = [&](long long h) {
+        const long long slot = ((n * a.nch + ch) * a.H + h) * PS;
+        const float* si = at_ck ? a.ckpt_in + ((n * a.H + h) * a.n_ck + seg) * PS : a.sin_all + slot;
+        gdn::tc::prefetch_l2(si + 32 * tid);
+        gdn::tc::prefetch_l2(a.dd + slot + 32 * tid);
+        if (tid < 2 * nt) {
+            const long long o = ((n * a.T + t0 + (tid >> 1)) * a.H + h) * P + 32 * (tid & 1);
+            gdn::tc::prefetch_l2(a.x + o);
+            gdn::tc::prefetch_l2(a.dy + o);
+        }
+    };
+    prefetch_head(h0);
 
     load_bc(sB, a.B, a, n, g, t0, nt, tid);
     load_bc(sC, a.C, a, n, g, t0, nt, tid);
@@ -683,6 +697,7 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
         const long long head = n * a.H + h;
         const long long slot = ((n * a.nch + ch) * a.H + h) * PS;
         __syncthreads();  // the previous head's reads (tiles, scalars, partials) are done
+        if (hh + 1 < a.HB) prefetch_head(h + 1);
         load_scalars(a, n, h, t0, nt, sc, tid);
         __syncthreads();
         for (int i = tid; i < L * P / 4; i += CT) {
@@ -903,7 +918,7 @@ static_assert(PS % (4 * CT) == 0, "state slices");
 int heads_per_block(long long N, long long nch, long long H, long long G)
 {
     const long long hpg = H / G;
-    for (int hb = 8; hb >= 1; hb >>= 1)
+    for (int hb = 4; hb >= 1; hb >>= 1)
         if (hpg % hb == 0 && N * nch * G * (hpg / hb) >= 3 * 152) return hb;
     return 1;
 }

@@ -22,12 +22,12 @@ struct Args {
     int n_ck;  // checkpoints (segments) per head
     int nch;   // chunks per sequence
     int m;     // chunks per segment (K / kChunk)
-    int HB;    // heads per CTA of the gradient kernel
+    int HB;    // heads per CTA of the head-blocked kernels
     int nhb;   // such blocks per group
 };
 
-// Heads per gradient CTA: the largest of 8, 4, 2, 1 dividing the heads of a group that still
-// leaves at least three CTAs per SM (else 1).
+// Heads per CTA of the head-blocked kernels: the largest of 4, 2, 1 dividing the heads of a
+// group that still leaves at least three CTAs per SM (else 1).
 int heads_per_block(long long N, long long nch, long long H, long long G);
 
 struct Workspace {
