@@ -169,6 +169,19 @@ __device__ __forceinline__ void load_xd(float* xd, float* xw, const Args& a, lon
     }
 }
 
+// L2 prefetches ahead of a head's loads, one 128-byte line a call and thread: the chunk's rows
+// of head h in a [.., P] slab (2 lines a row, threads < 2 nt), and a dense state (threads
+// < 256).
+__device__ __forceinline__ void prefetch_rows(const float* src, const Args& a, long long n, long long h,
+                                              long long t0, int nt, int tid)
+{
+    if (tid < 2 * nt) gdn::tc::prefetch_l2(src + ((n * a.T + t0 + (tid >> 1)) * a.H + h) * P + 32 * (tid & 1));
+}
+__device__ __forceinline__ void prefetch_state(const float* src, int tid)
+{
+    if (tid < PS / 32) gdn::tc::prefetch_l2(src + 32 * tid);
+}
+
 // A dense [P][S] state into a tile (ld LD128) and back.
 __device__ __forceinline__ void load_state(float* tile, const float* src, int tid)
 {
@@ -264,7 +277,7 @@ __device__ __forceinline__ float* decay_slot(const Args& a, long long n, long lo
 // ---------------------------------------------------------------------------------
 // Forward 1, one chunk a segment: dS of chunk ch for HB heads into the slot the chain turns
 // into checkpoint ch + 1 (the last chunk's into s_T), and g.  Grid (nch, G nhb, N).
-__global__ void __launch_bounds__(CT, 2) ssd_state_hb_kernel(const Args a)
+__global__ void __launch_bounds__(CT, 3) ssd_state_hb_kernel(const Args a)
 {
     extern __shared__ __align__(16) float sm[];
     float* sB = sm;
@@ -272,10 +285,12 @@ __global__ void __launch_bounds__(CT, 2) ssd_state_hb_kernel(const Args a)
     const Scal sc{sXw + T64};
     const int tid = threadIdx.x;
     const Blk b = blk_of(a);
+    prefetch_rows(a.x, a, b.n, b.h0, b.t0, b.nt, tid);
     load_bc(sB, a.B, a, b.n, b.g, b.t0, b.nt, tid);
     for (int hh = 0; hh < a.HB; ++hh) {
         const long long h = b.h0 + hh, head = b.n * a.H + h;
         __syncthreads();
+        if (hh + 1 < a.HB) prefetch_rows(a.x, a, b.n, h + 1, b.t0, b.nt, tid);
         load_scalars(a, b.n, h, b.t0, b.nt, sc, tid);
         __syncthreads();
         load_xd(nullptr, sXw, a, b.n, h, b.t0, b.nt, sc, tid);
@@ -378,6 +393,11 @@ __global__ void __launch_bounds__(CT, 1) ssd_output_hb_kernel(const Args a)
     const Scal sc{sM + T64};
     const int tid = threadIdx.x;
     const Blk b = blk_of(a);
+    auto prefetch_head = [&](long long h) {
+        prefetch_rows(a.x, a, b.n, h, b.t0, b.nt, tid);
+        prefetch_state(a.ckpt + ((b.n * a.H + h) * a.n_ck + b.ch) * PS, tid);
+    };
+    prefetch_head(b.h0);
     load_bc(sB, a.B, a, b.n, b.g, b.t0, b.nt, tid);
     load_bc(sC, a.C, a, b.n, b.g, b.t0, b.nt, tid);
     __syncthreads();
@@ -395,6 +415,7 @@ __global__ void __launch_bounds__(CT, 1) ssd_output_hb_kernel(const Args a)
     for (int hh = 0; hh < a.HB; ++hh) {
         const long long h = b.h0 + hh, head = b.n * a.H + h;
         __syncthreads();
+        if (hh + 1 < a.HB) prefetch_head(h + 1);
         load_scalars(a, b.n, h, b.t0, b.nt, sc, tid);
         __syncthreads();
         load_xd(sXd, nullptr, a, b.n, h, b.t0, b.nt, sc, tid);
@@ -513,7 +534,7 @@ __global__ void __launch_bounds__(CT, 1) ssd_output_kernel(const Args a)
 // ---------------------------------------------------------------------------------
 // Backward 1, one chunk a segment: (diag(e) dY)^T C of chunk ch for HB heads into their dd
 // slots, g into gvec.  Grid (nch, G nhb, N).
-__global__ void __launch_bounds__(CT, 2) ssd_dprep_hb_kernel(const Args a)
+__global__ void __launch_bounds__(CT, 3) ssd_dprep_hb_kernel(const Args a)
 {
     extern __shared__ __align__(16) float sm[];
     float* sC = sm;
@@ -521,11 +542,13 @@ __global__ void __launch_bounds__(CT, 2) ssd_dprep_hb_kernel(const Args a)
     const Scal sc{sYe + T64};
     const int tid = threadIdx.x;
     const Blk b = blk_of(a);
+    prefetch_rows(a.dy, a, b.n, b.h0, b.t0, b.nt, tid);
     load_bc(sC, a.C, a, b.n, b.g, b.t0, b.nt, tid);
     for (int hh = 0; hh < a.HB; ++hh) {
         const long long h = b.h0 + hh;
         const long long slot = ((b.n * a.nch + b.ch) * a.H + h) * PS;
         __syncthreads();
+        if (hh + 1 < a.HB) prefetch_rows(a.dy, a, b.n, h + 1, b.t0, b.nt, tid);
         load_scalars(a, b.n, h, b.t0, b.nt, sc, tid);
         __syncthreads();
         if (tid == 0) a.gvec[(b.n * a.nch + b.ch) * a.H + h] = sc.g();
@@ -663,14 +686,10 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
     // each next one's while the current one computes): 3 lines of 128 bytes a thread.
     auto prefetch_head = [&](long long h) {
         const long long slot = ((n * a.nch + ch) * a.H + h) * PS;
-        const float* si = at_ck ? a.ckpt_in + ((n * a.H + h) * a.n_ck + seg) * PS : a.sin_all + slot;
-        gdn::tc::prefetch_l2(si + 32 * tid);
-        gdn::tc::prefetch_l2(a.dd + slot + 32 * tid);
-        if (tid < 2 * nt) {
-            const long long o = ((n * a.T + t0 + (tid >> 1)) * a.H + h) * P + 32 * (tid & 1);
-            gdn::tc::prefetch_l2(a.x + o);
-            gdn::tc::prefetch_l2(a.dy + o);
-        }
+        prefetch_state(at_ck ? a.ckpt_in + ((n * a.H + h) * a.n_ck + seg) * PS : a.sin_all + slot, tid);
+        prefetch_state(a.dd + slot, tid);
+        prefetch_rows(a.x, a, n, h, t0, nt, tid);
+        prefetch_rows(a.dy, a, n, h, t0, nt, tid);
     };
     prefetch_head(h0);
 
