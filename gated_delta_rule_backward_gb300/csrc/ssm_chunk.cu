@@ -380,15 +380,15 @@ __global__ void __launch_bounds__(CT) ssd_chain_kernel(const Args a)
 }
 
 // Forward 3, one chunk a segment: y of chunk ch for HB heads from checkpoint ch, Q = C B^T
-// computed once.  Grid (nch, G nhb, N).
-__global__ void __launch_bounds__(CT, 1) ssd_output_hb_kernel(const Args a)
+// computed once and kept in registers (each thread masks the elements it owns), the state
+// tile over B's once Q is done: two CTAs an SM.  Grid (nch, G nhb, N).
+__global__ void __launch_bounds__(CT, 2) ssd_output_hb_kernel(const Args a)
 {
     extern __shared__ __align__(16) float sm[];
     float* sB = sm;
+    float* sS = sB;          // the state entering the chunk, rows p (after Q)
     float* sC = sB + T128;
-    float* sS = sC + T128;   // the state entering the chunk, rows p
-    float* sQ = sS + T128;   // C B^T
-    float* sXd = sQ + T64;
+    float* sXd = sC + T128;
     float* sM = sXd + T64;   // Lm (.) Q
     const Scal sc{sM + T64};
     const int tid = threadIdx.x;
@@ -401,20 +401,12 @@ __global__ void __launch_bounds__(CT, 1) ssd_output_hb_kernel(const Args a)
     load_bc(sB, a.B, a, b.n, b.g, b.t0, b.nt, tid);
     load_bc(sC, a.C, a, b.n, b.g, b.t0, b.nt, tid);
     __syncthreads();
-    {
-        Acc64 q;
-        zero_mma<64, 64>(q);
-        block_mma<64, 64, false, true>(q, sC, LD128, sB, LD128, S, tid);
-#pragma unroll
-        for (int i = 0; i < Map64::MT; ++i)
-#pragma unroll
-            for (int j = 0; j < Map64::NT; ++j)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) sQ[Map64::row(tid, i, r) * LD64 + Map64::col(tid, j, r)] = q[i][j][r];
-    }
+    Acc64 q;  // C B^T, rows t, columns tau
+    zero_mma<64, 64>(q);
+    block_mma<64, 64, false, true>(q, sC, LD128, sB, LD128, S, tid);
     for (int hh = 0; hh < a.HB; ++hh) {
         const long long h = b.h0 + hh, head = b.n * a.H + h;
-        __syncthreads();
+        __syncthreads();  // B (first head) or the previous head's tiles are no longer read
         if (hh + 1 < a.HB) prefetch_head(h + 1);
         load_scalars(a, b.n, h, b.t0, b.nt, sc, tid);
         __syncthreads();
@@ -433,8 +425,7 @@ __global__ void __launch_bounds__(CT, 1) ssd_output_hb_kernel(const Args a)
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
                         const int t = Map64::row(tid, i, r), tau = Map64::col(tid, j, r);
-                        sM[t * LD64 + tau] =
-                            tau <= t ? __fmul_rn(expf(__fsub_rn(c[t], c[tau])), sQ[t * LD64 + tau]) : 0.f;
+                        sM[t * LD64 + tau] = tau <= t ? __fmul_rn(expf(__fsub_rn(c[t], c[tau])), q[i][j][r]) : 0.f;
                     }
         }
         __syncthreads();
@@ -927,7 +918,7 @@ __global__ void __launch_bounds__(256) ssd_reduce_kernel(const Args a)
 
 constexpr size_t kSmemSegState = sizeof(float) * (T128 + T64 + NSCAL);
 constexpr size_t kSmemOutput = sizeof(float) * (3 * T128 + 2 * T64 + NSCAL);
-constexpr size_t kSmemOutputHb = sizeof(float) * (3 * T128 + 3 * T64 + NSCAL);
+constexpr size_t kSmemOutputHb = sizeof(float) * (2 * T128 + 2 * T64 + NSCAL);
 constexpr size_t kSmemDprep1 = sizeof(float) * (T128 + T64 + NSCAL);
 constexpr size_t kSmemDprepR = sizeof(float) * (3 * T128 + T64 + NSCAL);
 constexpr size_t kSmemGrad = sizeof(float) * (3 * T128 + 7 * T64 + 18 * L + L + 8 + NSCAL);
