@@ -74,14 +74,20 @@ __device__ __forceinline__ void block_mma(MmaAcc<M, N>& acc, const float* __rest
             tc::split_tf32(b_at(k0 + tq, n), bh[j][0], bl[j][0]);
             tc::split_tf32(b_at(k0 + tq + 4, n), bh[j][1], bl[j][1]);
         }
+        // pass-major: the MT x NT independent tiles lie between two passes on one accumulator
+        // (each element still sums hi hi, then hi lo, then lo hi)
 #pragma unroll
         for (int i = 0; i < Map::MT; ++i)
 #pragma unroll
-            for (int j = 0; j < Map::NT; ++j) {
-                tc::mma_warp_tf32(acc[i][j], ah[i], bh[j]);
-                tc::mma_warp_tf32(acc[i][j], ah[i], bl[j]);
-                tc::mma_warp_tf32(acc[i][j], al[i], bh[j]);
-            }
+            for (int j = 0; j < Map::NT; ++j) tc::mma_warp_tf32(acc[i][j], ah[i], bh[j]);
+#pragma unroll
+        for (int i = 0; i < Map::MT; ++i)
+#pragma unroll
+            for (int j = 0; j < Map::NT; ++j) tc::mma_warp_tf32(acc[i][j], ah[i], bl[j]);
+#pragma unroll
+        for (int i = 0; i < Map::MT; ++i)
+#pragma unroll
+            for (int j = 0; j < Map::NT; ++j) tc::mma_warp_tf32(acc[i][j], al[i], bh[j]);
     }
 }
 
