@@ -4,15 +4,15 @@
 //
 // C[M][N] += A(m, k) B(k, n) over k < K (K a multiple of 8), operands in shared memory with
 // the layouts of gdn_gemm.cuh (A_KMAJOR / B_KMAJOR select the transposed storage), computed
-// by the 256 threads (8 warps) of a CTA.  The warps tile the output 2 x 4; a warp tile of
-// (M / 2) x (N / 4) is MT x NT tiles of 16 x 8, and the accumulator of tile (mt, nt) is the
-// m16n8 fragment acc[mt][nt][r] at
-//   row    = wr (M / 2) + 16 mt + g + 8 (r / 2)
-//   column = wc (N / 4) + 8 nt + 2 tq + (r % 2)
-// (warp = 4 wr + wc, g = lane / 4, tq = lane % 4): a row lives in the 4 lanes of one g and
-// the 4 warps of one wr, a column in the 8 lanes of one tq and the 2 warps of one wc.  Every
-// output element is owned by one thread and its sum runs in a fixed order, so results do not
-// change from run to run.
+// by the WR x WC warps of a CTA (2 x 4 = 8 by default; a 4 x 4 grid runs 16).  The warps
+// tile the output WR x WC; a warp tile of (M / WR) x (N / WC) is MT x NT tiles of 16 x 8, and
+// the accumulator of tile (mt, nt) is the m16n8 fragment acc[mt][nt][r] at
+//   row    = wr (M / WR) + 16 mt + g + 8 (r / 2)
+//   column = wc (N / WC) + 8 nt + 2 tq + (r % 2)
+// (warp = WC wr + wc, g = lane / 4, tq = lane % 4): a row lives in the 4 lanes of one g and
+// the WC warps of one wr, a column in the 8 lanes of one tq and the WR warps of one wc.
+// Every output element is owned by one thread and its sum runs in a fixed order, so results
+// do not change from run to run.
 #pragma once
 
 #include <cstdint>
@@ -22,9 +22,9 @@
 
 namespace gdn {
 
-template <int M, int N>
+template <int M, int N, int WR_ = 2, int WC_ = 4>
 struct MmaMap {
-    static constexpr int WR = 2, WC = 4;
+    static constexpr int WR = WR_, WC = WC_;
     static constexpr int WTM = M / WR, WTN = N / WC;
     static constexpr int MT = WTM / 16, NT = WTN / 8;
     static_assert(MT * 16 * WR == M && NT * 8 * WC == N, "tile");
@@ -34,25 +34,25 @@ struct MmaMap {
     __device__ static int col(int tid, int nt, int r) { return wc(tid) * WTN + 8 * nt + 2 * (tid & 3) + (r & 1); }
 };
 
-template <int M, int N>
-using MmaAcc = float[MmaMap<M, N>::MT][MmaMap<M, N>::NT][4];
+template <int M, int N, int WR = 2, int WC = 4>
+using MmaAcc = float[MmaMap<M, N, WR, WC>::MT][MmaMap<M, N, WR, WC>::NT][4];
 
-template <int M, int N>
-__device__ __forceinline__ void zero_mma(MmaAcc<M, N>& acc)
+template <int M, int N, int WR = 2, int WC = 4>
+__device__ __forceinline__ void zero_mma(MmaAcc<M, N, WR, WC>& acc)
 {
 #pragma unroll
-    for (int i = 0; i < MmaMap<M, N>::MT; ++i)
+    for (int i = 0; i < MmaMap<M, N, WR, WC>::MT; ++i)
 #pragma unroll
-        for (int j = 0; j < MmaMap<M, N>::NT; ++j)
+        for (int j = 0; j < MmaMap<M, N, WR, WC>::NT; ++j)
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.f;
 }
 
-template <int M, int N, bool A_KMAJOR, bool B_KMAJOR>
-__device__ __forceinline__ void block_mma(MmaAcc<M, N>& acc, const float* __restrict__ A, int lda,
+template <int M, int N, bool A_KMAJOR, bool B_KMAJOR, int WR = 2, int WC = 4>
+__device__ __forceinline__ void block_mma(MmaAcc<M, N, WR, WC>& acc, const float* __restrict__ A, int lda,
                                           const float* __restrict__ B, int ldb, int K, int tid)
 {
-    using Map = MmaMap<M, N>;
+    using Map = MmaMap<M, N, WR, WC>;
     const int lane = tid & 31, g = lane >> 2, tq = lane & 3;
     const int m0 = Map::wr(tid) * Map::WTM + g, n0 = Map::wc(tid) * Map::WTN + g;
     auto a_at = [&](int m, int k) { return A_KMAJOR ? A[k * lda + m] : A[m * lda + k]; };

@@ -74,6 +74,12 @@ using Map64 = gdn::MmaMap<64, 64>;
 using Map128 = gdn::MmaMap<64, 128>;
 using Acc64 = MmaAcc<64, 64>;
 using Acc128 = MmaAcc<64, 128>;
+// The gradient kernel's: 16 warps on a 4 x 4 grid.
+constexpr int GT = 512;
+using G64 = gdn::MmaMap<64, 64, 4, 4>;
+using G128 = gdn::MmaMap<64, 128, 4, 4>;
+using GAcc64 = MmaAcc<64, 64, 4, 4>;
+using GAcc128 = MmaAcc<64, 128, 4, 4>;
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
@@ -138,10 +144,11 @@ __device__ __forceinline__ void load_scalars(const Args& a, long long n, long lo
 }
 
 // Rows [t0, t0 + L) of B or C (one group's [.., S] slab) into a tile, zero past the end.
+template <int NTH = CT>
 __device__ __forceinline__ void load_bc(float* tile, const float* src, const Args& a, long long n, long long g,
                                         long long t0, int nt, int tid)
 {
-    for (int i = tid; i < L * S / 4; i += CT) {
+    for (int i = tid; i < L * S / 4; i += NTH) {
         const int t = i / (S / 4), q = i - t * (S / 4);
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < nt) v = ld4(src + ((n * a.T + t0 + t) * a.G + g) * S + 4 * q);
@@ -183,9 +190,10 @@ __device__ __forceinline__ void prefetch_state(const float* src, int tid)
 }
 
 // A dense [P][S] state into a tile (ld LD128) and back.
+template <int NTH = CT>
 __device__ __forceinline__ void load_state(float* tile, const float* src, int tid)
 {
-    for (int i = tid; i < PS / 4; i += CT) {
+    for (int i = tid; i < PS / 4; i += NTH) {
         const int p = i / (S / 4), q = i - p * (S / 4);
         st4(tile + p * LD128 + 4 * q, ld4(src + p * S + 4 * q));
     }
@@ -636,10 +644,12 @@ __global__ void __launch_bounds__(CT) ssd_dchain_kernel(const Args a)
     st4(a.ds0 + head * PS + off, d);
 }
 
-// Backward 3: every gradient of one chunk for HB heads of one group.  Grid (nch, G nhb, N).
-// dx and ddt are complete per (chunk, head) and go straight out; dB and dC are summed over the
-// block's heads in registers (ascending) and written as the block's partial.
-__global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
+// Backward 3: every gradient of one chunk for HB heads of one group.  Grid (nch, G nhb, N),
+// 16 warps (the products on a 4 x 4 warp grid: one CTA fits an SM, and twice the warps of the
+// other kernels hide the latencies of its phases).  dx and ddt are complete per (chunk, head)
+// and go straight out; dB and dC are summed over the block's heads in registers (ascending)
+// and written as the block's partial.
+__global__ void __launch_bounds__(GT, 1) ssd_grad_kernel(const Args a)
 {
     extern __shared__ __align__(16) float sm[];
     float* sB = sm;
@@ -653,13 +663,13 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
     float* sdQ = sM + T64;   // Lm (.) dM
     float* sYe = sdQ + T64;  // diag(e) dY
     float* pRow = sYe + T64;      // [L][4] row sums of M (.) dM
-    float* pCol = pRow + 4 * L;   // [L][2] column sums of M (.) dM
-    float* pInt = pCol + 2 * L;   // [L][4] sum_p diag(e) dY (C s_in^T)
+    float* pCol = pRow + 4 * L;   // [L][4] column sums of M (.) dM
+    float* pInt = pCol + 4 * L;   // [L][4] sum_p diag(e) dY (C s_in^T)
     float* pV = pInt + 4 * L;     // [L][4] sum_p Xd u
     float* pX = pV + 4 * L;       // [L][4] sum_p x dXd
     float* dc = pX + 4 * L;       // [L]
-    float* red = dc + L;          // [8]
-    const Scal sc{red + 8};
+    float* red = dc + L;          // [16]
+    const Scal sc{red + 16};
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ch = blockIdx.x;
     const long long n = blockIdx.z;
@@ -670,7 +680,7 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
     const long long t0 = (long long)ch * L;
     const int nt = (int)min((long long)L, a.T - t0);
     const int gq = lane >> 2, tq = lane & 3;
-    const int wr = Map64::wr(tid), wc = Map64::wc(tid);  // the same for both output shapes
+    const int wr = G64::wr(tid), wc = G64::wc(tid);  // the same for both output shapes
     const int seg = ch / a.m;
     const bool at_ck = ch == seg * a.m;
     // A head's x, dy rows, s_in and dS_out into L2 ahead of their loads (the first head's now,
@@ -684,23 +694,23 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
     };
     prefetch_head(h0);
 
-    load_bc(sB, a.B, a, n, g, t0, nt, tid);
-    load_bc(sC, a.C, a, n, g, t0, nt, tid);
+    load_bc<GT>(sB, a.B, a, n, g, t0, nt, tid);
+    load_bc<GT>(sC, a.C, a, n, g, t0, nt, tid);
     __syncthreads();
     {  // Q = C B^T, shared by the block's heads
-        Acc64 q;
-        zero_mma<64, 64>(q);
-        block_mma<64, 64, false, true>(q, sC, LD128, sB, LD128, S, tid);
+        GAcc64 q;
+        zero_mma<64, 64, 4, 4>(q);
+        block_mma<64, 64, false, true, 4, 4>(q, sC, LD128, sB, LD128, S, tid);
 #pragma unroll
-        for (int i = 0; i < Map64::MT; ++i)
+        for (int i = 0; i < G64::MT; ++i)
 #pragma unroll
-            for (int j = 0; j < Map64::NT; ++j)
+            for (int j = 0; j < G64::NT; ++j)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) sQ[Map64::row(tid, i, r) * LD64 + Map64::col(tid, j, r)] = q[i][j][r];
+                for (int r = 0; r < 4; ++r) sQ[G64::row(tid, i, r) * LD64 + G64::col(tid, j, r)] = q[i][j][r];
     }
-    Acc128 accB, accC;
-    zero_mma<64, 128>(accB);
-    zero_mma<64, 128>(accC);
+    GAcc128 accB, accC;
+    zero_mma<64, 128, 4, 4>(accB);
+    zero_mma<64, 128, 4, 4>(accC);
 
     for (int hh = 0; hh < a.HB; ++hh) {
         const long long h = h0 + hh;
@@ -710,7 +720,7 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
         if (hh + 1 < a.HB) prefetch_head(h + 1);
         load_scalars(a, n, h, t0, nt, sc, tid);
         __syncthreads();
-        for (int i = tid; i < L * P / 4; i += CT) {
+        for (int i = tid; i < L * P / 4; i += GT) {
             const int t = i / (P / 4), q = i - t * (P / 4);
             const float4 xd = mul4(head_row4(a.x, a, n, h, t0, t, q, nt), sc.dt()[t]);
             const float4 dy = head_row4(a.dy, a, n, h, t0, t, q, nt);
@@ -719,25 +729,25 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
             st4(sdY + t * LD64 + 4 * q, dy);
             st4(sYe + t * LD64 + 4 * q, mul4(dy, sc.e()[t]));
         }
-        load_state(sSt, at_ck ? a.ckpt_in + (head * a.n_ck + seg) * PS : a.sin_all + slot, tid);
+        load_state<GT>(sSt, at_ck ? a.ckpt_in + (head * a.n_ck + seg) * PS : a.sin_all + slot, tid);
         __syncthreads();
         {  // with s_in: E = diag(e) dY s_in; dC += E, and sum_p diag(e) dY (C s_in^T) per row,
            // which is sum_j C (.) E
-            Acc128 E;
-            zero_mma<64, 128>(E);
-            block_mma<64, 128, false, false>(E, sYe, LD64, sSt, LD128, P, tid);
+            GAcc128 E;
+            zero_mma<64, 128, 4, 4>(E);
+            block_mma<64, 128, false, false, 4, 4>(E, sYe, LD64, sSt, LD128, P, tid);
 #pragma unroll
-            for (int i = 0; i < Map128::MT; ++i)
+            for (int i = 0; i < G128::MT; ++i)
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
-                    const int t = Map128::row(tid, i, 2 * hr);
+                    const int t = G128::row(tid, i, 2 * hr);
                     float v = 0.f;
 #pragma unroll
-                    for (int j = 0; j < Map128::NT; ++j)
+                    for (int j = 0; j < G128::NT; ++j)
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const int r = 2 * hr + e;
-                            v = __fmaf_rn(sC[t * LD128 + Map128::col(tid, j, r)], E[i][j][r], v);
+                            v = __fmaf_rn(sC[t * LD128 + G128::col(tid, j, r)], E[i][j][r], v);
                             accC[i][j][r] = __fadd_rn(accC[i][j][r], E[i][j][r]);
                         }
                     v = row_lanes(v);
@@ -748,7 +758,7 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
         {  // dS_out over s_in, and <dS_out, s_in>
             const float* dso = a.dd + slot;
             float v = 0.f;
-            for (int i = tid; i < PS / 4; i += CT) {
+            for (int i = tid; i < PS / 4; i += GT) {
                 const int p = i / (S / 4), q = i - p * (S / 4);
                 float* x = sSt + p * LD128 + 4 * q;
                 const float4 d = ld4(dso + p * S + 4 * q);
@@ -760,29 +770,29 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
             if (lane == 0) red[warp] = v;
         }
         __syncthreads();
-        Acc64 u;  // B dS_out^T: rows tokens, columns channels
+        GAcc64 u;  // B dS_out^T: rows tokens, columns channels
         {  // dM = dY Xd^T; M, dQ; the rows and columns of M (.) dM; u; sum_p Xd u
-            Acc64 dm;
-            zero_mma<64, 64>(dm);
-            zero_mma<64, 64>(u);
-            block_mma<64, 64, false, true>(dm, sdY, LD64, sXd, LD64, P, tid);
-            block_mma<64, 64, false, true>(u, sB, LD128, sSt, LD128, S, tid);
+            GAcc64 dm;
+            zero_mma<64, 64, 4, 4>(dm);
+            zero_mma<64, 64, 4, 4>(u);
+            block_mma<64, 64, false, true, 4, 4>(dm, sdY, LD64, sXd, LD64, P, tid);
+            block_mma<64, 64, false, true, 4, 4>(u, sB, LD128, sSt, LD128, S, tid);
             const float* c = sc.c();
-            float cs[Map64::NT][2];
+            float cs[G64::NT][2];
 #pragma unroll
-            for (int j = 0; j < Map64::NT; ++j) cs[j][0] = cs[j][1] = 0.f;
+            for (int j = 0; j < G64::NT; ++j) cs[j][0] = cs[j][1] = 0.f;
 #pragma unroll
-            for (int i = 0; i < Map64::MT; ++i)
+            for (int i = 0; i < G64::MT; ++i)
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
-                    const int t = Map64::row(tid, i, 2 * hr);
+                    const int t = G64::row(tid, i, 2 * hr);
                     float rs = 0.f, vs = 0.f;
 #pragma unroll
-                    for (int j = 0; j < Map64::NT; ++j)
+                    for (int j = 0; j < G64::NT; ++j)
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const int r = 2 * hr + e;
-                            const int tau = Map64::col(tid, j, r);
+                            const int tau = G64::col(tid, j, r);
                             const float lm = tau <= t ? expf(__fsub_rn(c[t], c[tau])) : 0.f;
                             const float m = __fmul_rn(lm, sQ[t * LD64 + tau]);
                             sM[t * LD64 + tau] = m;
@@ -801,29 +811,29 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
                     }
                 }
 #pragma unroll
-            for (int j = 0; j < Map64::NT; ++j)
+            for (int j = 0; j < G64::NT; ++j)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const float v = col_lanes(cs[j][e]);
-                    if (gq == 0) pCol[Map64::col(tid, j, e) * 2 + wr] = v;
+                    if (gq == 0) pCol[G64::col(tid, j, e) * 4 + wr] = v;
                 }
         }
         __syncthreads();
         {  // dXd = M^T dY + diag(w) u; dx; sum_p x dXd
-            Acc64 dxd;
-            zero_mma<64, 64>(dxd);
-            block_mma<64, 64, true, false>(dxd, sM, LD64, sdY, LD64, L, tid);
+            GAcc64 dxd;
+            zero_mma<64, 64, 4, 4>(dxd);
+            block_mma<64, 64, true, false, 4, 4>(dxd, sM, LD64, sdY, LD64, L, tid);
 #pragma unroll
-            for (int i = 0; i < Map64::MT; ++i)
+            for (int i = 0; i < G64::MT; ++i)
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
-                    const int tau = Map64::row(tid, i, 2 * hr);
+                    const int tau = G64::row(tid, i, 2 * hr);
                     const float w = sc.w()[tau], d = sc.dt()[tau];
                     float xs = 0.f;
                     const long long o = ((n * a.T + t0 + tau) * a.H + h) * P;
 #pragma unroll
-                    for (int j = 0; j < Map64::NT; ++j) {
-                        const int p = Map64::col(tid, j, 0);
+                    for (int j = 0; j < G64::NT; ++j) {
+                        const int p = G64::col(tid, j, 0);
                         const float g0 = __fmaf_rn(w, u[i][j][2 * hr], dxd[i][j][2 * hr]);
                         const float g1 = __fmaf_rn(w, u[i][j][2 * hr + 1], dxd[i][j][2 * hr + 1]);
                         if (tau < nt) {
@@ -837,9 +847,9 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
                 }
         }
         // dC += dQ B;  dB += dQ^T C + diag(w) Xd dS_out
-        block_mma<64, 128, false, false>(accC, sdQ, LD64, sB, LD128, L, tid);
-        block_mma<64, 128, true, false>(accB, sdQ, LD64, sC, LD128, L, tid);
-        block_mma<64, 128, false, false>(accB, sXw, LD64, sSt, LD128, P, tid);
+        block_mma<64, 128, false, false, 4, 4>(accC, sdQ, LD64, sB, LD128, L, tid);
+        block_mma<64, 128, true, false, 4, 4>(accB, sdQ, LD64, sC, LD128, L, tid);
+        block_mma<64, 128, false, false, 4, 4>(accB, sXw, LD64, sSt, LD128, P, tid);
         __syncthreads();
         if (warp == 0) {  // dc, its reverse running sum, ddt
 #pragma unroll
@@ -850,7 +860,8 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
                 const float* v4 = pV + 4 * t;
                 const float* x4 = pX + 4 * t;
                 const float rs = __fadd_rn(__fadd_rn(r4[0], r4[1]), __fadd_rn(r4[2], r4[3]));
-                const float cs = __fadd_rn(pCol[2 * t], pCol[2 * t + 1]);
+                const float* c4 = pCol + 4 * t;
+                const float cs = __fadd_rn(__fadd_rn(c4[0], c4[1]), __fadd_rn(c4[2], c4[3]));
                 const float it = __fadd_rn(__fadd_rn(i4[0], i4[1]), __fadd_rn(i4[2], i4[3]));
                 const float v = __fmul_rn(sc.w()[t], __fadd_rn(__fadd_rn(v4[0], v4[1]), __fadd_rn(v4[2], v4[3])));
                 const float xs = __fadd_rn(__fadd_rn(x4[0], x4[1]), __fadd_rn(x4[2], x4[3]));
@@ -861,7 +872,7 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
             __syncwarp();
             if (lane == 0) {
                 float dot = 0.f, vt = 0.f;
-                for (int k = 0; k < 8; ++k) dot = __fadd_rn(dot, red[k]);
+                for (int k = 0; k < GT / 32; ++k) dot = __fadd_rn(dot, red[k]);
                 for (int t = 0; t < L; ++t) vt = __fadd_rn(vt, pV[4 * t]);
                 dc[L - 1] = __fadd_rn(dc[L - 1], __fmaf_rn(sc.g(), dot, vt));
                 float run = 0.f;
@@ -882,15 +893,15 @@ __global__ void __launch_bounds__(CT, 1) ssd_grad_kernel(const Args a)
     // this block's dB, dC partial: rows t < nt
     float* part = a.partBC + (long long)hb * 2 * S;
 #pragma unroll
-    for (int i = 0; i < Map128::MT; ++i)
+    for (int i = 0; i < G128::MT; ++i)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
-            const int t = Map128::row(tid, i, 2 * hr);
+            const int t = G128::row(tid, i, 2 * hr);
             if (t >= nt) continue;
             float* row = part + ((n * a.T + t0 + t) * a.G + g) * (long long)a.nhb * 2 * S;
 #pragma unroll
-            for (int j = 0; j < Map128::NT; ++j) {
-                const int c = Map128::col(tid, j, 0);
+            for (int j = 0; j < G128::NT; ++j) {
+                const int c = G128::col(tid, j, 0);
                 st2(row + c, accB[i][j][2 * hr], accB[i][j][2 * hr + 1]);
                 st2(row + S + c, accC[i][j][2 * hr], accC[i][j][2 * hr + 1]);
             }
@@ -921,7 +932,7 @@ constexpr size_t kSmemOutput = sizeof(float) * (3 * T128 + 2 * T64 + NSCAL);
 constexpr size_t kSmemOutputHb = sizeof(float) * (2 * T128 + 2 * T64 + NSCAL);
 constexpr size_t kSmemDprep1 = sizeof(float) * (T128 + T64 + NSCAL);
 constexpr size_t kSmemDprepR = sizeof(float) * (3 * T128 + T64 + NSCAL);
-constexpr size_t kSmemGrad = sizeof(float) * (3 * T128 + 7 * T64 + 18 * L + L + 8 + NSCAL);
+constexpr size_t kSmemGrad = sizeof(float) * (3 * T128 + 7 * T64 + 20 * L + L + 16 + NSCAL);
 static_assert(kSmemGrad <= 232448, "the gradient kernel's shared memory");
 static_assert(PS % (4 * CT) == 0, "state slices");
 
@@ -955,13 +966,13 @@ Workspace workspace_layout(long long N, long long T, long long H, long long G, i
 }
 
 template <typename Kern>
-static int launch(Kern kern, dim3 grid, size_t smem, const Args& a, cudaStream_t st)
+static int launch(Kern kern, dim3 grid, size_t smem, const Args& a, cudaStream_t st, int threads = CT)
 {
     if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return (int)e;
     }
-    kern<<<grid, CT, smem, st>>>(a);
+    kern<<<grid, threads, smem, st>>>(a);
     return (int)cudaGetLastError();
 }
 
@@ -985,7 +996,7 @@ int backward(const Args& a, cudaStream_t st)
     int e = a.m == 1 ? launch(ssd_dprep_hb_kernel, blk, kSmemDprep1, a, st)
                      : launch(ssd_dprep_kernel, dim3(nck, H, N), kSmemDprepR, a, st);
     if (!e) e = launch(ssd_dchain_kernel, dim3(SLICES, H, N), 0, a, st);
-    if (!e) e = launch(ssd_grad_kernel, blk, kSmemGrad, a, st);
+    if (!e) e = launch(ssd_grad_kernel, blk, kSmemGrad, a, st, GT);
     if (!e) {
         ssd_reduce_kernel<<<(unsigned)(a.N * a.T), 256, 0, st>>>(a);
         e = (int)cudaGetLastError();
