@@ -139,6 +139,14 @@ def test_chunked_strong_decay():
     compare(run_gpu(prob), run_oracle(prob), _tol(prob.T))
 
 
+def test_chunked_head_blocks_groups_sequences():
+    """Head blocks over two groups and two sequences (N = 2, G = 2, 32 heads, 1024 tokens: two
+    heads a block), against the oracle on every output."""
+    prob = make_ssm_problem(N=2, T=1024, H=32, P=64, S=128, G=2, K=64, seed=21)
+    assert ssm.chunked(ssm.make_params(2, 1024, 32, 64, 128, 2, False, 64))
+    compare(run_gpu(prob), run_oracle(prob), _tol(prob.T))
+
+
 def test_mamba2_all_heads_chunked():
     """Every head of the Mamba-2 workload at 1024 tokens in chunked form: the gradient kernel
     takes two heads a block here, so dB and dC fold 40 block partials of 2 heads each."""
