@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libgdn.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["gdn_api.cu", "gdn_fwd.cu", "gdn_bwd.cu", "gdn_chunk.cu", "gdn_tc_chain.cu", "gdn_tc_grad.cu", "gdn_noalloc.cu", "gdn_widen.cu", "ssm_scan.cu", "ssm_chunk.cu"]
+SOURCES = ["gdn_api.cu", "gdn_fwd.cu", "gdn_bwd.cu", "gdn_chunk.cu", "gdn_tc_chain.cu", "gdn_tc_grad.cu", "gdn_noalloc.cu", "gdn_widen.cu", "ssm_scan.cu", "ssm_chunk.cu", "ssm_diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-cudart", "static", "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr"]

@@ -32,6 +32,7 @@
 
 #include "../../include/ssm.h"
 #include "ssm_chunk.h"
+#include "ssm_diag.h"
 
 namespace gdn {
 void set_last_error(const char* msg);
@@ -490,6 +491,7 @@ struct Plan {
     int per_state, SL, NSL, RPW, W, RPC, nb_g, nb_h, nsub, ctas;
     bool chunked;  // the chunked form (ssm_chunk.cu) runs
     int HB, nch;   // its heads per gradient CTA and chunks per sequence
+    bool diag;     // the segmented form for a decay per state (ssm_diag.cu) runs
 };
 
 // The chunked form takes one decay per head, 64 channels and 128 states (the Mamba-2 layer's
@@ -526,6 +528,10 @@ static int plan_of(const ssm_params_t* p, Plan& pl, std::string& why)
     pl.nch = (int)((pl.T + ssd::kChunk - 1) / ssd::kChunk);
     pl.HB = pl.chunked ? ssd::heads_per_block(pl.N, pl.nch, pl.H, pl.G) : 1;
     pl.n_ck = p->T <= 0 ? 1 : (p->T + pl.K - 1) / pl.K;
+    // a decay per state, one channel a head, 16 states, whole blocks of 16 channels in a group,
+    // and the segment decays' scratch (16 floats a segment and channel) inside y
+    pl.diag = p->a_per_state == 1 && p->P == 1 && p->S == diag::kS && p->T >= 1 && (p->H / p->G) % 16 == 0 &&
+              p->H % p->G == 0 && pl.n_ck * diag::kS <= p->T;
     if (pl.S != 16 && pl.S != 32 && pl.S != 64 && pl.S != 128 && pl.S != 256) {
         why = "S (d_state) must be 16, 32, 64, 128 or 256";
         return GDN_ERR_UNSUPPORTED;
@@ -569,6 +575,10 @@ static WsLayout ws_layout(const Plan& pl)
     WsLayout w{};
     if (pl.chunked) {
         w.total = ssd::workspace_layout(pl.N, pl.T, pl.H, pl.G, (int)pl.K, pl.HB).total;
+        return w;
+    }
+    if (pl.diag) {
+        w.total = diag::workspace_layout(pl.N, pl.T, pl.H, pl.G, (int)pl.K).total;
         return w;
     }
     size_t o = 0;
@@ -642,6 +652,15 @@ static ssd::Args chunk_args(const Plan& pl)
     return c;
 }
 
+static diag::Args diag_args(const Plan& pl)
+{
+    diag::Args c{};
+    c.N = pl.N; c.T = pl.T; c.H = pl.H; c.G = pl.G;
+    c.K = (int)pl.K; c.n_ck = (int)pl.n_ck; c.spk = (int)((pl.K + diag::kSB - 1) / diag::kSB);
+    c.nsb = c.n_ck * c.spk; c.nbg = (int)(pl.H / pl.G / 16);
+    return c;
+}
+
 static int fail(int code, const std::string& msg)
 {
     gdn::set_last_error(msg.c_str());
@@ -704,12 +723,20 @@ extern "C" int ssm_chunked(const ssm_params_t* p)
     return plan_of(p, pl, why) == GDN_OK && pl.chunked ? 1 : 0;
 }
 
+extern "C" int ssm_form(const ssm_params_t* p)
+{
+    Plan pl{};
+    std::string why;
+    if (plan_of(p, pl, why) != GDN_OK) return -1;
+    return pl.chunked ? 1 : pl.diag ? 2 : 0;
+}
+
 extern "C" int ssm_forward_launches(const ssm_params_t* p)
 {
     Plan pl{};
     std::string why;
     if (plan_of(p, pl, why) != GDN_OK || pl.N == 0) return 0;
-    return pl.chunked ? 3 : 1;
+    return pl.chunked || pl.diag ? 3 : 1;
 }
 
 extern "C" int ssm_backward_launches(const ssm_params_t* p)
@@ -717,7 +744,7 @@ extern "C" int ssm_backward_launches(const ssm_params_t* p)
     Plan pl{};
     std::string why;
     if (plan_of(p, pl, why) != GDN_OK || pl.N == 0 || pl.T == 0) return 0;
-    return pl.chunked ? 4 : 2;
+    return pl.chunked || pl.diag ? 4 : 2;
 }
 
 extern "C" int ssm_forward(const ssm_params_t* p, const float* s0, const float* x, const float* dt, const float* A,
@@ -758,6 +785,11 @@ extern "C" int ssm_forward(const ssm_params_t* p, const float* s0, const float* 
         c.x = x; c.dt = dt; c.A = A; c.B = B; c.C = C; c.s0 = s0;
         c.y = a.y; c.sT = a.sT; c.ckpt = ckpt;
         e = ssd::forward(c, (cudaStream_t)stream);
+    } else if (pl.diag) {
+        diag::Args c = diag_args(pl);
+        c.x = x; c.dt = dt; c.A = A; c.B = B; c.C = C; c.s0 = s0;
+        c.y = a.y; c.sT = a.sT; c.ckpt = ckpt;
+        e = diag::forward(c, (cudaStream_t)stream);
     } else {
         e = launch<true>(a, pl, (cudaStream_t)stream);
     }
@@ -828,6 +860,20 @@ extern "C" int ssm_backward(const ssm_params_t* p, const float* x, const float* 
         c.gvec = (float*)(ws + cw.gvec);
         c.partBC = (float*)(ws + cw.partBC);
         e = ssd::backward(c, st);
+        if (e) return fail(GDN_ERR_CUDA, std::string("ssm_backward: ") + cudaGetErrorString((cudaError_t)e));
+        return GDN_OK;
+    }
+    if (pl.diag) {
+        const diag::Workspace dw = diag::workspace_layout(pl.N, pl.T, pl.H, pl.G, (int)pl.K);
+        diag::Args c = diag_args(pl);
+        c.x = x; c.dt = dt; c.A = A; c.B = B; c.C = C; c.ckpt_in = ckpt; c.dy = a.dy; c.dsT = a.dsT;
+        c.ds0 = a.ds0; c.dx = a.dx; c.ddt = a.ddt; c.dB = a.dB; c.dC = a.dC;
+        c.sin_sb = (float*)(ws + dw.sin_sb);
+        c.U = (float*)(ws + dw.U);
+        c.Gb = (float*)(ws + dw.Gb);
+        c.carry = (float*)(ws + dw.carry);
+        c.partBC = (float*)(ws + dw.partBC);
+        e = diag::backward(c, st);
         if (e) return fail(GDN_ERR_CUDA, std::string("ssm_backward: ") + cudaGetErrorString((cudaError_t)e));
         return GDN_OK;
     }

@@ -16,7 +16,7 @@ _lib = gdn._lib
 
 # Every symbol include/ssm.h declares.
 EXPORTS = ["ssm_checkpoint_interval", "ssm_num_checkpoints", "ssm_packed_out_elems", "ssm_packed_grad_elems",
-           "ssm_backward_workspace_bytes", "ssm_supported", "ssm_chunked", "ssm_forward_launches",
+           "ssm_backward_workspace_bytes", "ssm_supported", "ssm_chunked", "ssm_form", "ssm_forward_launches",
            "ssm_backward_launches", "ssm_forward", "ssm_backward"]
 
 
@@ -51,6 +51,8 @@ _lib.ssm_supported.argtypes = [_PP]
 _lib.ssm_supported.restype = ctypes.c_int
 _lib.ssm_chunked.argtypes = [_PP]
 _lib.ssm_chunked.restype = ctypes.c_int
+_lib.ssm_form.argtypes = [_PP]
+_lib.ssm_form.restype = ctypes.c_int
 _lib.ssm_forward_launches.argtypes = [_PP]
 _lib.ssm_forward_launches.restype = ctypes.c_int
 _lib.ssm_backward_launches.argtypes = [_PP]
@@ -99,6 +101,17 @@ def supported(p) -> int:
 def chunked(p) -> bool:
     """True when these sizes run the chunked form."""
     return bool(_lib.ssm_chunked(ctypes.byref(p)))
+
+
+FORMS = {0: "token-serial", 1: "chunked", 2: "segmented"}
+
+
+def form(p) -> str:
+    """The form these sizes run: "token-serial", "chunked" or "segmented" (a decay per state)."""
+    f = int(_lib.ssm_form(ctypes.byref(p)))
+    if f < 0:
+        raise gdn.GdnError(int(_lib.ssm_supported(ctypes.byref(p))), "ssm_form")
+    return FORMS[f]
 
 
 def launches(p):

@@ -22,13 +22,20 @@
  * Arithmetic: fp32 throughout (FP32 pipe, expf); every sum over channels, heads and states
  * runs in a fixed order (no atomics), so a call's results do not change from run to run.
  *
- * Two forms compute this.  The token-serial walk follows the recurrences above token by token
- * (its results do not depend on K).  The chunked form (one decay per head, P = 64, S = 128,
- * K a multiple of 64; ssm_chunked() says which runs) groups 64 tokens into a chunk and writes
- * each chunk's part of the recurrence as dense products, with l_t = dt_t A, the running sum
- * c_t of l over the chunk, Q = C B^T and the mask exp(c_t - c_tau) for tau <= t: the chunk's
- * outputs and state change are those products, and only the state passes from chunk to chunk
- * (the same sums in another order; its results depend on K through the checkpoint segments).
+ * Three forms compute this (ssm_form() says which runs; each regroups the same sums, so
+ * results agree within rounding):
+ *   - the token-serial walk follows the recurrences above token by token (its results do not
+ *     depend on K);
+ *   - the chunked form (one decay per head, P = 64, S = 128, K a multiple of 64) groups 64
+ *     tokens into a chunk and writes each chunk's part of the recurrence as dense products,
+ *     with l_t = dt_t A, the running sum c_t of l over the chunk, Q = C B^T and the mask
+ *     exp(c_t - c_tau) for tau <= t; only the state passes from chunk to chunk;
+ *   - the segmented form (a decay per state, P = 1, S = 16, H / G a multiple of 16, and
+ *     ceil(T / K) * 16 <= T) runs every (channel, state) recurrence by checkpoint segments:
+ *     a segment maps its entry state s to G s + dS (G the product of its decays, dS its scan
+ *     from zero), and 32-token blocks of the reverse walk map the gradient arriving from the
+ *     right, c, to U + G c the same way.
+ * The last two forms' results depend on K through the segments.
  *
  * Layouts: dense, row-major, fp32, device memory, no strides:
  *     s0 [N][H][P][S]   x [N][T][H][P]   dt [N][T][H]   A [H] or [H][S]   B, C [N][T][G][S]
@@ -92,8 +99,11 @@ size_t ssm_backward_workspace_bytes(const ssm_params_t* p);
 /* GDN_OK when the sizes are supported, else the code ssm_forward / ssm_backward would return. */
 int ssm_supported(const ssm_params_t* p);
 /* 1 when these sizes run the chunked form (one decay per head, P = 64, S = 128, T >= 1, K a
- * multiple of 64), 0 when they run the token-serial walk or are unsupported. */
+ * multiple of 64), 0 when they run another form or are unsupported. */
 int ssm_chunked(const ssm_params_t* p);
+/* The form these sizes run: 0 token-serial walk, 1 chunked, 2 segmented (a decay per state);
+ * -1 when unsupported. */
+int ssm_form(const ssm_params_t* p);
 /* Kernels a forward / backward call with these params launches (0 when the call would
  * launch none: unsupported sizes, N = 0, or the backward at T = 0). */
 int ssm_forward_launches(const ssm_params_t* p);

@@ -8,9 +8,10 @@ float64).  The token-serial walk's results at different checkpoint intervals, an
 path's results over repeated calls, must agree bit for bit (the walk recomputes the
 forward's own states; every sum runs in a fixed order).
 
-Both forms run here: sizes with one decay per head, P = 64, S = 128 and K a multiple of 64
-take the chunked form (64-token chunks), every other the token-serial walk; each case
-asserts which one it exercises.
+All three forms run here: one decay per head with P = 64, S = 128 and K a multiple of 64
+takes the chunked form (64-token chunks); a decay per state with P = 1, S = 16, H / G a
+multiple of 16 and ceil(T / K) 16 <= T the segmented form; every other size the token-serial
+walk.  Each case asserts which one it exercises.
 """
 import numpy as np
 import pytest
@@ -84,7 +85,19 @@ CASES = [
     dict(N=1, T=50, H=2, P=8, S=256, G=2, mamba1=False, K=7),
     dict(N=1, T=64, H=64, P=2, S=16, G=2, mamba1=True, K=64),     # several heads per block
     dict(N=2, T=29, H=6, P=48, S=32, G=3, mamba1=False, K=4),
+    dict(N=2, T=300, H=32, P=1, S=16, G=2, mamba1=True, K=37),       # segmented: ragged segments
+    dict(N=1, T=200, H=16, P=1, S=16, G=1, mamba1=True, K=100),      # segmented: 4 sub-blocks a segment
+    dict(N=3, T=64, H=48, P=1, S=16, G=3, mamba1=True, K=16),        # segmented: n_ck 16 = T
 ]
+
+
+def expected_form(c):
+    n_ck = -(-c["T"] // c["K"])
+    if not c["mamba1"] and c["P"] == 64 and c["S"] == 128 and c["K"] % 64 == 0:
+        return "chunked"
+    if c["mamba1"] and c["P"] == 1 and c["S"] == 16 and (c["H"] // c["G"]) % 16 == 0 and n_ck * 16 <= c["T"]:
+        return "segmented"
+    return "token-serial"
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"N{c['N']}T{c['T']}H{c['H']}P{c['P']}S{c['S']}G{c['G']}"
@@ -92,7 +105,8 @@ CASES = [
 def test_parity(case):
     prob = make_ssm_problem(seed=7, **case)
     p = ssm.make_params(prob.N, prob.T, prob.H, prob.P, prob.S, prob.G, prob.mamba1, prob.K)
-    assert ssm.chunked(p) == (not prob.mamba1 and prob.P == 64 and prob.S == 128 and prob.K % 64 == 0)
+    assert ssm.form(p) == expected_form(case)
+    assert ssm.chunked(p) == (ssm.form(p) == "chunked")
     gpu = run_gpu(prob)
     ref = run_oracle(prob)
     compare(gpu, ref, _tol(prob.T))
@@ -108,10 +122,13 @@ def test_empty_sequence():
 
 @pytest.mark.parametrize("mamba1", [False, True], ids=["mamba2", "mamba1"])
 def test_checkpoint_interval_invariance_bitwise(mamba1):
-    prob = make_ssm_problem(N=1, T=77, H=8 if not mamba1 else 64, P=16 if not mamba1 else 1,
+    """The token-serial walk's results do not depend on K (two channels a head keep a decay per
+    state on the walk at every K)."""
+    prob = make_ssm_problem(N=1, T=77, H=8 if not mamba1 else 32, P=16 if not mamba1 else 2,
                             S=64 if not mamba1 else 16, G=2, mamba1=mamba1, K=8, seed=9)
     base = run_gpu(prob, K=1)
     for K in (3, 8, 77, 100):
+        assert ssm.form(ssm.make_params(1, 77, prob.H, prob.P, prob.S, 2, mamba1, K)) == "token-serial"
         got = run_gpu(prob, K=K)
         for k in NAMES:
             if k == "ckpt":
@@ -122,9 +139,11 @@ def test_checkpoint_interval_invariance_bitwise(mamba1):
             assert np.array_equal(ck[:, :, c], base["ckpt"][:, :, c * K]), f"K={K}: checkpoint {c}"
 
 
-@pytest.mark.parametrize("K", [16, 64], ids=["serial", "chunked"])
-def test_run_to_run_bitwise(K):
-    prob = ssm_workload("mamba2_small", K=K)
+@pytest.mark.parametrize("wl,K,form", [("mamba2_small", 16, "token-serial"), ("mamba2_small", 64, "chunked"),
+                                       ("mamba1_small", 20, "segmented")], ids=["serial", "chunked", "segmented"])
+def test_run_to_run_bitwise(wl, K, form):
+    prob = ssm_workload(wl, K=K)
+    assert ssm.form(ssm.make_params(prob.N, prob.T, prob.H, prob.P, prob.S, prob.G, prob.mamba1, prob.K)) == form
     a, b = run_gpu(prob), run_gpu(prob)
     for k in NAMES:
         assert np.array_equal(a[k], b[k]), k
@@ -157,8 +176,10 @@ def test_mamba2_all_heads_chunked():
 
 
 def test_mamba1_full_size():
-    """The Mamba-1 workload (1536 channels of 16 states, 4096 tokens) against the oracle."""
+    """The Mamba-1 workload (1536 channels of 16 states, 4096 tokens, segmented form) against
+    the oracle."""
     prob = ssm_workload("mamba1_d1536_T4096")
+    assert ssm.form(ssm.make_params(1, 4096, 1536, 1, 16, 1, True, 64)) == "segmented"
     compare(run_gpu(prob), run_oracle(prob), _tol(prob.T))
 
 

@@ -50,6 +50,16 @@ def test_chunked_dispatch():
     assert ssm.launches(ssm.make_params(1, 0, 8, 64, 128, K=64)) == (1, 0)
     assert ssm.launches(ssm.make_params(0, 10, 8, 64, 128, K=64)) == (0, 0)
     assert ssm.launches(ssm.make_params(1, 10, 8, 64, 24)) == (0, 0)
+    # the segmented form: a decay per state, one channel a head, 16 states, whole blocks of 16
+    # channels in a group, and ceil(T / K) 16 <= T
+    assert ssm.form(ssm.make_params(1, 4096, 1536, 1, 16, mamba1=True, K=64)) == "segmented"
+    assert ssm.launches(ssm.make_params(1, 4096, 1536, 1, 16, mamba1=True, K=64)) == (3, 4)
+    for p in (ssm.make_params(1, 100, 96, 1, 16, mamba1=True, K=6),     # 17 segments x 16 > 100
+              ssm.make_params(1, 100, 40, 1, 16, mamba1=True, K=20),    # 40 channels: not blocks of 16
+              ssm.make_params(1, 100, 96, 2, 16, mamba1=True, K=20),    # two channels a head
+              ssm.make_params(1, 100, 96, 1, 32, mamba1=True, K=20)):   # 32 states
+        assert ssm.form(p) == "token-serial"
+    assert ssm.form(ssm.make_params(1, 100, 8, 64, 128, K=64)) == "chunked"
     # the chunked workspace: the per-chunk state slabs (one, or two with inner chunks to
     # replay), the chunk decays and the dB/dC block partials
     st = 4 * 64 * 8 * 64 * 128
