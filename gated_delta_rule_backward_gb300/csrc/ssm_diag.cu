@@ -67,17 +67,26 @@ __device__ __forceinline__ float state_sum(float v)
     return v;
 }
 
-// One token's inputs for a thread.
-struct Tok {
-    float d, x, B;
+// A tile of up to SB tokens [t0, t0 + nt) of the CTA's 16 channels in shared memory, one
+// coalesced load a value: dt, x, dy [SB][16 channels] and B, C [SB][16 states] (the arrays
+// passed as null are skipped).  Ends with a barrier.
+struct Tile {
+    float *dt, *x, *dy, *B, *C;
 };
-__device__ __forceinline__ Tok tok_in(const Args& a, long long row, const Pos& p)
+__device__ __forceinline__ void stage(const Args& a, long long n, long long blk, long long g, long long t0, int nt,
+                                      const Tile& s, int tid)
 {
-    Tok k;
-    k.d = a.dt[row * a.H + p.h];
-    k.x = a.x[row * a.H + p.h];
-    k.B = a.B[(row * a.G + p.g) * S + p.j];
-    return k;
+    for (int i = tid; i < nt * CHB; i += TB) {
+        const int tt = i / CHB, c = i - tt * CHB;
+        const long long row = n * a.T + t0 + tt;
+        const long long hx = row * a.H + blk * CHB + c, bx = (row * a.G + g) * S + c;
+        if (s.dt) s.dt[i] = a.dt[hx];
+        if (s.x) s.x[i] = a.x[hx];
+        if (s.dy) s.dy[i] = a.dy[hx];
+        if (s.B) s.B[i] = a.B[bx];
+        if (s.C) s.C[i] = a.C[bx];
+    }
+    __syncthreads();
 }
 
 // ---------------------------------------------------------------------------------
@@ -86,19 +95,25 @@ __device__ __forceinline__ Tok tok_in(const Args& a, long long row, const Pos& p
 // output kernel overwrites afterwards).  Grid (n_ck, H / 16, N).
 __global__ void __launch_bounds__(TB) diag_fwd_local_kernel(const Args a)
 {
+    __shared__ float sdt[SB * CHB], sx[SB * CHB], sB[SB * S];
     const int tid = threadIdx.x;
     const int k = blockIdx.x;
     const long long n = blockIdx.z;
     const Pos p = pos_of(a, blockIdx.y, tid);
+    const int c = tid >> 4;
     const float Aj = a.A[p.h * S + p.j];
     const long long t0 = (long long)k * a.K, t1 = std::min(a.T, t0 + a.K);
     float s = 0.f, G = 1.f;
-#pragma unroll 4
-    for (long long t = t0; t < t1; ++t) {
-        const Tok v = tok_in(a, n * a.T + t, p);
-        const float av = expf(__fmul_rn(v.d, Aj));
-        s = __fmaf_rn(av, s, __fmul_rn(v.B, __fmul_rn(v.x, v.d)));
-        G = __fmul_rn(G, av);
+    for (long long tb = t0; tb < t1; tb += SB) {
+        const int nt = (int)std::min((long long)SB, t1 - tb);
+        if (tb > t0) __syncthreads();
+        stage(a, n, blockIdx.y, p.g, tb, nt, Tile{sdt, sx, nullptr, sB, nullptr}, tid);
+        for (int tt = 0; tt < nt; ++tt) {
+            const float d = sdt[tt * CHB + c];
+            const float av = expf(__fmul_rn(d, Aj));
+            s = __fmaf_rn(av, s, __fmul_rn(sB[tt * S + p.j], __fmul_rn(sx[tt * CHB + c], d)));
+            G = __fmul_rn(G, av);
+        }
     }
     const long long head = n * a.H + p.h;
     float* dst = k + 1 < a.n_ck ? a.ckpt + (head * a.n_ck + k + 1) * S : a.sT + head * S;
@@ -148,22 +163,26 @@ __global__ void __launch_bounds__(TB) diag_chain_kernel(const Args a)
 // Forward 3: y of the segment's tokens from its checkpoint.  Grid (n_ck, H / 16, N).
 __global__ void __launch_bounds__(TB) diag_fwd_out_kernel(const Args a)
 {
+    __shared__ float sdt[SB * CHB], sx[SB * CHB], sB[SB * S], sC[SB * S];
     const int tid = threadIdx.x;
+    const int c = tid >> 4;
     const int k = blockIdx.x;
     const long long n = blockIdx.z;
     const Pos p = pos_of(a, blockIdx.y, tid);
     const float Aj = a.A[p.h * S + p.j];
     const long long t0 = (long long)k * a.K, t1 = std::min(a.T, t0 + a.K);
     float s = a.ckpt[((n * a.H + p.h) * a.n_ck + k) * S + p.j];
-#pragma unroll 4
-    for (long long t = t0; t < t1; ++t) {
-        const long long row = n * a.T + t;
-        const Tok v = tok_in(a, row, p);
-        const float C = a.C[(row * a.G + p.g) * S + p.j];
-        const float av = expf(__fmul_rn(v.d, Aj));
-        s = __fmaf_rn(av, s, __fmul_rn(v.B, __fmul_rn(v.x, v.d)));
-        const float y = state_sum(__fmul_rn(s, C));
-        if (p.j == 0) a.y[row * a.H + p.h] = y;
+    for (long long tb = t0; tb < t1; tb += SB) {
+        const int nt = (int)std::min((long long)SB, t1 - tb);
+        if (tb > t0) __syncthreads();
+        stage(a, n, blockIdx.y, p.g, tb, nt, Tile{sdt, sx, nullptr, sB, sC}, tid);
+        for (int tt = 0; tt < nt; ++tt) {
+            const float d = sdt[tt * CHB + c];
+            const float av = expf(__fmul_rn(d, Aj));
+            s = __fmaf_rn(av, s, __fmul_rn(sB[tt * S + p.j], __fmul_rn(sx[tt * CHB + c], d)));
+            const float y = state_sum(__fmul_rn(s, sC[tt * S + p.j]));
+            if (p.j == 0) a.y[(n * a.T + tb + tt) * a.H + p.h] = y;
+        }
     }
 }
 
@@ -173,7 +192,9 @@ __global__ void __launch_bounds__(TB) diag_fwd_out_kernel(const Args a)
 // U = 0, G = 1.  Grid (n_ck, H / 16, N).
 __global__ void __launch_bounds__(TB) diag_bwd_prep_kernel(const Args a)
 {
+    __shared__ float sdt[SB * CHB], sx[SB * CHB], sdy[SB * CHB], sB[SB * S], sC[SB * S];
     const int tid = threadIdx.x;
+    const int c = tid >> 4;
     const int k = blockIdx.x;
     const long long n = blockIdx.z;
     const Pos p = pos_of(a, blockIdx.y, tid);
@@ -189,18 +210,18 @@ __global__ void __launch_bounds__(TB) diag_bwd_prep_kernel(const Args a)
             a.Gb[o] = 1.f;
             continue;
         }
-#pragma unroll 4
-        for (long long t = ts0; t < ts1; ++t) {
-            const Tok v = tok_in(a, n * a.T + t, p);
-            s = __fmaf_rn(expf(__fmul_rn(v.d, Aj)), s, __fmul_rn(v.B, __fmul_rn(v.x, v.d)));
+        const int nt = (int)(ts1 - ts0);
+        if (i > 0) __syncthreads();
+        stage(a, n, blockIdx.y, p.g, ts0, nt, Tile{sdt, sx, sdy, sB, sC}, tid);
+        for (int tt = 0; tt < nt; ++tt) {
+            const float d = sdt[tt * CHB + c];
+            s = __fmaf_rn(expf(__fmul_rn(d, Aj)), s, __fmul_rn(sB[tt * S + p.j], __fmul_rn(sx[tt * CHB + c], d)));
         }
         float gl = 0.f, G = 1.f, a_next = 1.f;
-#pragma unroll 4
-        for (long long t = ts1 - 1; t >= ts0; --t) {
-            const long long row = n * a.T + t;
-            const float av = expf(__fmul_rn(a.dt[row * a.H + p.h], Aj));
-            if (t < ts1 - 1) gl = __fmul_rn(a_next, gl);
-            gl = __fmaf_rn(a.dy[row * a.H + p.h], a.C[(row * a.G + p.g) * S + p.j], gl);
+        for (int tt = nt - 1; tt >= 0; --tt) {
+            const float av = expf(__fmul_rn(sdt[tt * CHB + c], Aj));
+            if (tt < nt - 1) gl = __fmul_rn(a_next, gl);
+            gl = __fmaf_rn(sdy[tt * CHB + c], sC[tt * S + p.j], gl);
             G = __fmul_rn(G, av);
             a_next = av;
         }
@@ -248,9 +269,15 @@ __global__ void __launch_bounds__(TB) diag_dchain_kernel(const Args a)
 __global__ void __launch_bounds__(TB) diag_bwd_grad_kernel(const Args a)
 {
     extern __shared__ __align__(16) float sm[];
-    float* ring = sm;             // [SB][TB]: the state entering each token
-    float* red = ring + SB * TB;  // [SB][NW][2 S]: warp sums of the dB, dC terms
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float* ring = sm;              // [SB][TB]: the state entering each token
+    float* aring = ring + SB * TB; // [SB][TB]: its decay
+    float* red = aring + SB * TB;  // [SB][NW][2 S]: warp sums of the dB, dC terms
+    float* sdt = red + SB * NW * 2 * S;  // the sub-block's inputs
+    float* sx = sdt + SB * CHB;
+    float* sdy = sx + SB * CHB;
+    float* sB = sdy + SB * CHB;
+    float* sC = sB + SB * S;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, c = tid >> 4;
     const int sb = blockIdx.x;
     const long long n = blockIdx.z;
     const Pos p = pos_of(a, blockIdx.y, tid);
@@ -262,28 +289,30 @@ __global__ void __launch_bounds__(TB) diag_bwd_grad_kernel(const Args a)
     const float Aj = a.A[p.h * S + p.j];
     const long long o = ((n * a.nsb + sb) * a.H + p.h) * S + p.j;
     float s = a.sin_sb[o];
+    float g = a.carry[o], a_next = 1.f;
+    stage(a, n, blockIdx.y, p.g, ts0, nt, Tile{sdt, sx, sdy, sB, sC}, tid);
     for (int tt = 0; tt < nt; ++tt) {
         ring[tt * TB + tid] = s;
-        const Tok v = tok_in(a, n * a.T + ts0 + tt, p);
-        s = __fmaf_rn(expf(__fmul_rn(v.d, Aj)), s, __fmul_rn(v.B, __fmul_rn(v.x, v.d)));
+        const float d = sdt[tt * CHB + c];
+        const float av = expf(__fmul_rn(d, Aj));
+        aring[tt * TB + tid] = av;
+        s = __fmaf_rn(av, s, __fmul_rn(sB[tt * S + p.j], __fmul_rn(sx[tt * CHB + c], d)));
     }
-    float g = a.carry[o], a_next = 1.f;
     for (int tt = nt - 1; tt >= 0; --tt) {
         const long long row = n * a.T + ts0 + tt;
-        const Tok v = tok_in(a, row, p);
-        const float dyv = a.dy[row * a.H + p.h];
-        const float C = a.C[(row * a.G + p.g) * S + p.j];
-        const float av = expf(__fmul_rn(v.d, Aj));
+        const float d = sdt[tt * CHB + c], xv = sx[tt * CHB + c], dyv = sdy[tt * CHB + c];
+        const float Bt = sB[tt * S + p.j], C = sC[tt * S + p.j];
+        const float av = aring[tt * TB + tid];
         if (tt < nt - 1) g = __fmul_rn(a_next, g);
         g = __fmaf_rn(dyv, C, g);  // the gradient reaching s_t
         const float sp = ring[tt * TB + tid];
-        const float xdt = __fmul_rn(v.x, v.d);
-        const float st = __fmaf_rn(av, sp, __fmul_rn(v.B, xdt));  // s_t, the forward's own step
+        const float xdt = __fmul_rn(xv, d);
+        const float st = __fmaf_rn(av, sp, __fmul_rn(Bt, xdt));  // s_t, the forward's own step
         float vB = __fmul_rn(g, xdt), vC = __fmul_rn(dyv, st);
-        const float dxp = state_sum(__fmul_rn(g, v.B));
-        const float ddtp = state_sum(__fmul_rn(g, __fmaf_rn(__fmul_rn(Aj, av), sp, __fmul_rn(v.B, v.x))));
+        const float dxp = state_sum(__fmul_rn(g, Bt));
+        const float ddtp = state_sum(__fmul_rn(g, __fmaf_rn(__fmul_rn(Aj, av), sp, __fmul_rn(Bt, xv))));
         if (p.j == 0) {
-            a.dx[row * a.H + p.h] = __fmul_rn(dxp, v.d);
+            a.dx[row * a.H + p.h] = __fmul_rn(dxp, d);
             a.ddt[row * a.H + p.h] = ddtp;
         }
         // the warp's two channels, then the warps in ascending order below
@@ -324,7 +353,7 @@ __global__ void __launch_bounds__(256) diag_reduce_kernel(const Args a)
 // ---------------------------------------------------------------------------------
 // Host side.
 
-constexpr size_t kSmemGrad = sizeof(float) * (SB * TB + SB * NW * 2 * S);
+constexpr size_t kSmemGrad = sizeof(float) * (2 * SB * TB + SB * NW * 2 * S + 3 * SB * CHB + 2 * SB * S);
 
 static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
