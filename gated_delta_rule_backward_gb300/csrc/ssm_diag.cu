@@ -58,15 +58,6 @@ __device__ __forceinline__ Pos pos_of(const Args& a, long long blk, int tid)
     return p;
 }
 
-// Sum over the 16 lanes of a channel (lane bits 0 .. 3).  A butterfly: every lane ends with the
-// same bits.
-__device__ __forceinline__ float state_sum(float v)
-{
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
 // A tile of up to SB tokens [t0, t0 + nt) of the CTA's 16 channels in shared memory, one
 // coalesced load a value: dt, x, dy [SB][16 channels] and B, C [SB][16 states] (the arrays
 // passed as null are skipped).  Ends with a barrier.
@@ -164,6 +155,7 @@ __global__ void __launch_bounds__(TB) diag_chain_kernel(const Args a)
 __global__ void __launch_bounds__(TB) diag_fwd_out_kernel(const Args a)
 {
     __shared__ float sdt[SB * CHB], sx[SB * CHB], sB[SB * S], sC[SB * S];
+    __shared__ float ysum[SB * TB];  // s_t C_t[j] per token and thread, summed over j after the tile
     const int tid = threadIdx.x;
     const int c = tid >> 4;
     const int k = blockIdx.x;
@@ -180,8 +172,16 @@ __global__ void __launch_bounds__(TB) diag_fwd_out_kernel(const Args a)
             const float d = sdt[tt * CHB + c];
             const float av = expf(__fmul_rn(d, Aj));
             s = __fmaf_rn(av, s, __fmul_rn(sB[tt * S + p.j], __fmul_rn(sx[tt * CHB + c], d)));
-            const float y = state_sum(__fmul_rn(s, sC[tt * S + p.j]));
-            if (p.j == 0) a.y[(n * a.T + tb + tt) * a.H + p.h] = y;
+            ysum[tt * TB + tid] = __fmul_rn(s, sC[tt * S + p.j]);
+        }
+        __syncthreads();
+        for (int i = tid; i < nt * CHB; i += TB) {  // (token, channel) pairs, states in order
+            const int tt = i / CHB, ch = i - tt * CHB;
+            const float* v = ysum + tt * TB + ch * S;
+            float y = 0.f;
+#pragma unroll
+            for (int e = 0; e < S; ++e) y = __fadd_rn(y, v[e]);
+            a.y[(n * a.T + tb + tt) * a.H + blockIdx.y * CHB + ch] = y;
         }
     }
 }
@@ -299,7 +299,6 @@ __global__ void __launch_bounds__(TB) diag_bwd_grad_kernel(const Args a)
         s = __fmaf_rn(av, s, __fmul_rn(sB[tt * S + p.j], __fmul_rn(sx[tt * CHB + c], d)));
     }
     for (int tt = nt - 1; tt >= 0; --tt) {
-        const long long row = n * a.T + ts0 + tt;
         const float d = sdt[tt * CHB + c], xv = sx[tt * CHB + c], dyv = sdy[tt * CHB + c];
         const float Bt = sB[tt * S + p.j], C = sC[tt * S + p.j];
         const float av = aring[tt * TB + tid];
@@ -309,12 +308,9 @@ __global__ void __launch_bounds__(TB) diag_bwd_grad_kernel(const Args a)
         const float xdt = __fmul_rn(xv, d);
         const float st = __fmaf_rn(av, sp, __fmul_rn(Bt, xdt));  // s_t, the forward's own step
         float vB = __fmul_rn(g, xdt), vC = __fmul_rn(dyv, st);
-        const float dxp = state_sum(__fmul_rn(g, Bt));
-        const float ddtp = state_sum(__fmul_rn(g, __fmaf_rn(__fmul_rn(Aj, av), sp, __fmul_rn(Bt, xv))));
-        if (p.j == 0) {
-            a.dx[row * a.H + p.h] = __fmul_rn(dxp, d);
-            a.ddt[row * a.H + p.h] = ddtp;
-        }
+        // this token's dx and ddt terms over the slots just read (summed over states below)
+        ring[tt * TB + tid] = __fmul_rn(g, Bt);
+        aring[tt * TB + tid] = __fmul_rn(g, __fmaf_rn(__fmul_rn(Aj, av), sp, __fmul_rn(Bt, xv)));
         // the warp's two channels, then the warps in ascending order below
         vB = __fadd_rn(vB, __shfl_xor_sync(0xffffffffu, vB, 16));
         vC = __fadd_rn(vC, __shfl_xor_sync(0xffffffffu, vC, 16));
@@ -325,6 +321,20 @@ __global__ void __launch_bounds__(TB) diag_bwd_grad_kernel(const Args a)
         a_next = av;
     }
     __syncthreads();
+    for (int i2 = tid; i2 < nt * CHB; i2 += TB) {  // (token, channel) pairs, states in order
+        const int tt = i2 / CHB, ch = i2 - tt * CHB;
+        const float* vx = ring + tt * TB + ch * S;
+        const float* vd = aring + tt * TB + ch * S;
+        float dxs = 0.f, dds = 0.f;
+#pragma unroll
+        for (int e = 0; e < S; ++e) {
+            dxs = __fadd_rn(dxs, vx[e]);
+            dds = __fadd_rn(dds, vd[e]);
+        }
+        const long long o2 = (n * a.T + ts0 + tt) * a.H + blockIdx.y * CHB + ch;
+        a.dx[o2] = __fmul_rn(dxs, sdt[tt * CHB + ch]);
+        a.ddt[o2] = dds;
+    }
     float* part = a.partBC + (long long)p.cb * 2 * S;
     for (int idx = tid; idx < nt * 2 * S; idx += TB) {
         const int tt = idx / (2 * S), c = idx - tt * 2 * S;
