@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(TB) diag_fwd_local_kernel(const Args a)
         const int nt = (int)std::min((long long)SB, t1 - tb);
         if (tb > t0) __syncthreads();
         stage(a, n, blockIdx.y, p.g, tb, nt, Tile{sdt, sx, nullptr, sB, nullptr}, tid);
+#pragma unroll 4
         for (int tt = 0; tt < nt; ++tt) {
             const float d = sdt[tt * CHB + c];
             const float av = expf(__fmul_rn(d, Aj));
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(TB) diag_fwd_out_kernel(const Args a)
         const int nt = (int)std::min((long long)SB, t1 - tb);
         if (tb > t0) __syncthreads();
         stage(a, n, blockIdx.y, p.g, tb, nt, Tile{sdt, sx, nullptr, sB, sC}, tid);
+#pragma unroll 4
         for (int tt = 0; tt < nt; ++tt) {
             const float d = sdt[tt * CHB + c];
             const float av = expf(__fmul_rn(d, Aj));
@@ -213,11 +215,13 @@ __global__ void __launch_bounds__(TB) diag_bwd_prep_kernel(const Args a)
         const int nt = (int)(ts1 - ts0);
         if (i > 0) __syncthreads();
         stage(a, n, blockIdx.y, p.g, ts0, nt, Tile{sdt, sx, sdy, sB, sC}, tid);
+#pragma unroll 4
         for (int tt = 0; tt < nt; ++tt) {
             const float d = sdt[tt * CHB + c];
             s = __fmaf_rn(expf(__fmul_rn(d, Aj)), s, __fmul_rn(sB[tt * S + p.j], __fmul_rn(sx[tt * CHB + c], d)));
         }
         float gl = 0.f, G = 1.f, a_next = 1.f;
+#pragma unroll 4
         for (int tt = nt - 1; tt >= 0; --tt) {
             const float av = expf(__fmul_rn(sdt[tt * CHB + c], Aj));
             if (tt < nt - 1) gl = __fmul_rn(a_next, gl);
@@ -291,6 +295,7 @@ __global__ void __launch_bounds__(TB) diag_bwd_grad_kernel(const Args a)
     float s = a.sin_sb[o];
     float g = a.carry[o], a_next = 1.f;
     stage(a, n, blockIdx.y, p.g, ts0, nt, Tile{sdt, sx, sdy, sB, sC}, tid);
+#pragma unroll 4
     for (int tt = 0; tt < nt; ++tt) {
         ring[tt * TB + tid] = s;
         const float d = sdt[tt * CHB + c];
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(TB) diag_bwd_grad_kernel(const Args a)
         aring[tt * TB + tid] = av;
         s = __fmaf_rn(av, s, __fmul_rn(sB[tt * S + p.j], __fmul_rn(sx[tt * CHB + c], d)));
     }
+#pragma unroll 4
     for (int tt = nt - 1; tt >= 0; --tt) {
         const float d = sdt[tt * CHB + c], xv = sx[tt * CHB + c], dyv = sdy[tt * CHB + c];
         const float Bt = sB[tt * S + p.j], C = sC[tt * S + p.j];
