@@ -177,12 +177,12 @@ __global__ void __launch_bounds__(TB) diag_fwd_out_kernel(const Args a)
             ysum[tt * TB + tid] = __fmul_rn(s, sC[tt * S + p.j]);
         }
         __syncthreads();
-        for (int i = tid; i < nt * CHB; i += TB) {  // (token, channel) pairs, states in order
+        for (int i = tid; i < nt * CHB; i += TB) {  // (token, channel) pairs
             const int tt = i / CHB, ch = i - tt * CHB;
             const float* v = ysum + tt * TB + ch * S;
             float y = 0.f;
 #pragma unroll
-            for (int e = 0; e < S; ++e) y = __fadd_rn(y, v[e]);
+            for (int e = 0; e < S; ++e) y = __fadd_rn(y, v[(e + ch) & (S - 1)]);  // rotated: no bank conflicts
             a.y[(n * a.T + tb + tt) * a.H + blockIdx.y * CHB + ch] = y;
         }
     }
@@ -327,15 +327,16 @@ __global__ void __launch_bounds__(TB) diag_bwd_grad_kernel(const Args a)
         a_next = av;
     }
     __syncthreads();
-    for (int i2 = tid; i2 < nt * CHB; i2 += TB) {  // (token, channel) pairs, states in order
+    for (int i2 = tid; i2 < nt * CHB; i2 += TB) {  // (token, channel) pairs
         const int tt = i2 / CHB, ch = i2 - tt * CHB;
         const float* vx = ring + tt * TB + ch * S;
         const float* vd = aring + tt * TB + ch * S;
         float dxs = 0.f, dds = 0.f;
 #pragma unroll
-        for (int e = 0; e < S; ++e) {
-            dxs = __fadd_rn(dxs, vx[e]);
-            dds = __fadd_rn(dds, vd[e]);
+        for (int e = 0; e < S; ++e) {  // states from j = ch on, rotated: no bank conflicts
+            const int j = (e + ch) & (S - 1);
+            dxs = __fadd_rn(dxs, vx[j]);
+            dds = __fadd_rn(dds, vd[j]);
         }
         const long long o2 = (n * a.T + ts0 + tt) * a.H + blockIdx.y * CHB + ch;
         a.dx[o2] = __fmul_rn(dxs, sdt[tt * CHB + ch]);
