@@ -41,6 +41,8 @@ constexpr int SB = kSB;
 constexpr int TB = 256;        // threads of the per-block kernels
 constexpr int CHB = TB / S;    // channels a CTA
 constexpr int NW = TB / 32;    // warps a CTA
+constexpr int TC = 64;         // threads of the chain kernels (a Mamba-1 layer's 1536 x 16
+                               // chains then spread over all SMs)
 
 struct Pos {
     long long h, g;
@@ -113,11 +115,11 @@ __global__ void __launch_bounds__(TB) diag_fwd_local_kernel(const Args a)
     a.y[((n * a.n_ck + k) * a.H + p.h) * S + p.j] = G;
 }
 
-// Forward 2: the chain over segments, one (channel, state) a thread.  Grid (ceil(16 H / 256), N).
+// Forward 2: the chain over segments, one (channel, state) a thread.  Grid (ceil(16 H / TC), N).
 // Checkpoint 0 is s0; slot k + 1 (or s_T) holds dS_k and becomes s_{k+1}.
-__global__ void __launch_bounds__(TB) diag_chain_kernel(const Args a)
+__global__ void __launch_bounds__(TC) diag_chain_kernel(const Args a)
 {
-    const long long i = (long long)blockIdx.x * TB + threadIdx.x;
+    const long long i = (long long)blockIdx.x * TC + threadIdx.x;
     const long long n = blockIdx.y;
     if (i >= a.H * S) return;
     const long long h = i / S;
@@ -235,10 +237,10 @@ __global__ void __launch_bounds__(TB) diag_bwd_prep_kernel(const Args a)
 }
 
 // Backward 2: the carry arriving at every sub-block from its right, last first, one (channel,
-// state) a thread; d_s the carry past token 0.  Grid (ceil(16 H / 256), N).
-__global__ void __launch_bounds__(TB) diag_dchain_kernel(const Args a)
+// state) a thread; d_s the carry past token 0.  Grid (ceil(16 H / TC), N).
+__global__ void __launch_bounds__(TC) diag_dchain_kernel(const Args a)
 {
-    const long long i = (long long)blockIdx.x * TB + threadIdx.x;
+    const long long i = (long long)blockIdx.x * TC + threadIdx.x;
     const long long n = blockIdx.y;
     if (i >= a.H * S) return;
     const long long gs = a.H * S;
@@ -397,9 +399,9 @@ Workspace workspace_layout(long long N, long long T, long long H, long long G, i
 int forward(const Args& a, cudaStream_t st)
 {
     const dim3 seg((unsigned)a.n_ck, (unsigned)(a.H / CHB), (unsigned)a.N);
-    const dim3 chain((unsigned)((a.H * S + TB - 1) / TB), (unsigned)a.N);
+    const dim3 chain((unsigned)((a.H * S + TC - 1) / TC), (unsigned)a.N);
     diag_fwd_local_kernel<<<seg, TB, 0, st>>>(a);
-    diag_chain_kernel<<<chain, TB, 0, st>>>(a);
+    diag_chain_kernel<<<chain, TC, 0, st>>>(a);
     diag_fwd_out_kernel<<<seg, TB, 0, st>>>(a);
     return (int)cudaGetLastError();
 }
@@ -407,13 +409,13 @@ int forward(const Args& a, cudaStream_t st)
 int backward(const Args& a, cudaStream_t st)
 {
     const dim3 seg((unsigned)a.n_ck, (unsigned)(a.H / CHB), (unsigned)a.N);
-    const dim3 chain((unsigned)((a.H * S + TB - 1) / TB), (unsigned)a.N);
+    const dim3 chain((unsigned)((a.H * S + TC - 1) / TC), (unsigned)a.N);
     const dim3 sub((unsigned)a.nsb, (unsigned)(a.H / CHB), (unsigned)a.N);
     cudaError_t e = cudaFuncSetAttribute(diag_bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemGrad);
     if (e != cudaSuccess) return (int)e;
     diag_bwd_prep_kernel<<<seg, TB, 0, st>>>(a);
-    diag_dchain_kernel<<<chain, TB, 0, st>>>(a);
+    diag_dchain_kernel<<<chain, TC, 0, st>>>(a);
     diag_bwd_grad_kernel<<<sub, TB, kSmemGrad, st>>>(a);
     diag_reduce_kernel<<<(unsigned)(a.N * a.T), 256, 0, st>>>(a);
     return (int)cudaGetLastError();
