@@ -946,7 +946,8 @@ def run_ssm(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl, "N": prob.N, "T": prob.T, "H": prob.H, "P": prob.P, "S": prob.S,
                    "G": prob.G, "decay": "per state (Mamba-1)" if prob.mamba1 else "per head (Mamba-2)",
-                   "K": prob.K, "form": "chunked (64-token chunks)" if ssm.chunked(p) else "token-serial",
+                   "K": prob.K, "form": {"chunked": "chunked (64-token chunks)", "segmented": "segmented (a decay per state, by "
+                            "checkpoint segments)", "token-serial": "token-serial"}[ssm.form(p)],
                    "arithmetic": "fp32 FP32-pipe, expf",
                    "l2": "flushed between timed steps (256 MiB write outside the events)"},
         "roofline": {"bound": "alu", "kernel": "whole step: ssm_forward + ssm_backward",
