@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         // memory, in (10) from global memory) only after that launch has completed
         if (m_unit) tc::grid_dep_wait();
         if (!tc::mbar_wait(bar_m, 0)) s_err = 1;
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < 8; ++q) {
             float4 a, b;
             if (m_unit) {
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         {  // M[j][row] for this thread's 64 j
             const float* mc = sM + (m_unit ? (row >> 2) * kLdU + (row & 3) : row);
             const int js = m_unit ? 4 : kLdM;
-#pragma unroll
+#pragma unroll 1
             for (int q = 0; q < 8; ++q) {
                 uint32_t hi[8], lo[8];
 #pragma unroll
@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         const float* dmc = sM + (row >> 2) * kLdU + (row & 3);  // dM[j][row] at dmc[4 j]
         {
             float dot = 0.f;
-#pragma unroll
+#pragma unroll 1
             for (int q = 0; q < 8; ++q) {
                 const int j0 = 64 * hc + 8 * q;
                 float mh[8], ml[8];
@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         tc::fence_before();
         tc::bar_sync_first(256);
         tc::fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < 8; ++q) {
             const int j0 = 64 * hc + 8 * q;
             uint32_t hi[4], lo[4];
@@ -788,7 +788,7 @@ __global__ void __launch_bounds__(GT, 1) gdn_tc_grad_kernel(const ChunkArgs A)
         const float* gyr = A.gy + (long long)n * A.gys0 + (long long)(t0 + lane) * A.gys1 + (long long)h * A.gys2 + 64 * hc;
         const float* sdd = sm + kDdStage + (lane >> 2) * kLdU + (lane & 3) + 4 * 64 * hc;  // dDelta[lane][j]
         const float* sdy = sm + kDyStage + lane * kLdM + 64 * hc;
-#pragma unroll
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {  // 32 of this thread's 64 columns at a time
             float v[32];
             if (quarter == 0) {  // rows 0..31: dY row t = lane

@@ -128,6 +128,8 @@ WORKLOADS = {
     # 4096 tokens, scalar gate): the FP32-pipe chunked path, for stage times and captures
     "d64_T4096_N4": dict(N=4, T=4096, H_k=16, H_v=48, d=64, kda=False, C=None, seed=1007, packed=True),
     "d32_T4096_N4": dict(N=4, T=4096, H_k=16, H_v=48, d=32, kda=False, C=None, seed=1008, packed=True),
+    # the head-size-64 shape at one sequence and 1024 tokens, for many-pass captures
+    "profile_d64_T1024": dict(N=1, T=1024, H_k=16, H_v=48, d=64, kda=False, C=64, seed=1009, packed=True),
 }
 
 
