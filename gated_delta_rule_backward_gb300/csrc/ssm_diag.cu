@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(TB) diag_fwd_out_kernel(const Args a)
 __global__ void __launch_bounds__(TB) diag_bwd_prep_kernel(const Args a)
 {
     __shared__ float sdt[SB * CHB], sx[SB * CHB], sdy[SB * CHB], sB[SB * S], sC[SB * S];
+    __shared__ float aring[SB * TB];  // the forward pass's decays, for the reverse pass
     const int tid = threadIdx.x;
     const int c = tid >> 4;
     const int k = blockIdx.x;
@@ -220,12 +221,14 @@ __global__ void __launch_bounds__(TB) diag_bwd_prep_kernel(const Args a)
 #pragma unroll 4
         for (int tt = 0; tt < nt; ++tt) {
             const float d = sdt[tt * CHB + c];
-            s = __fmaf_rn(expf(__fmul_rn(d, Aj)), s, __fmul_rn(sB[tt * S + p.j], __fmul_rn(sx[tt * CHB + c], d)));
+            const float av = expf(__fmul_rn(d, Aj));
+            aring[tt * TB + tid] = av;
+            s = __fmaf_rn(av, s, __fmul_rn(sB[tt * S + p.j], __fmul_rn(sx[tt * CHB + c], d)));
         }
         float gl = 0.f, G = 1.f, a_next = 1.f;
 #pragma unroll 4
         for (int tt = nt - 1; tt >= 0; --tt) {
-            const float av = expf(__fmul_rn(sdt[tt * CHB + c], Aj));
+            const float av = aring[tt * TB + tid];
             if (tt < nt - 1) gl = __fmul_rn(a_next, gl);
             gl = __fmaf_rn(sdy[tt * CHB + c], sC[tt * S + p.j], gl);
             G = __fmul_rn(G, av);
