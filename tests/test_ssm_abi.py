@@ -60,6 +60,14 @@ def test_chunked_dispatch():
               ssm.make_params(1, 100, 96, 1, 32, mamba1=True, K=20)):   # 32 states
         assert ssm.form(p) == "token-serial"
     assert ssm.form(ssm.make_params(1, 100, 8, 64, 128, K=64)) == "chunked"
+    # its workspace: four per-sub-block slabs (entry states, U, G, carries: 32-token sub-blocks
+    # of every segment, 16 states a channel) and the dB/dC partials of the 16-channel blocks
+    N, T, H, G, K = 2, 4096, 1536, 2, 100
+    nsb = -(-T // K) * -(-K // 32)
+    per = 4 * N * nsb * H * 16
+    parts = 4 * N * T * G * (H // G // 16) * 2 * 16
+    up = lambda b: (b + 255) // 256 * 256
+    assert ssm.backward_workspace_bytes(ssm.make_params(N, T, H, 1, 16, G, mamba1=True, K=K)) == 4 * up(per) + up(parts)
     # the chunked workspace: the per-chunk state slabs (one, or two with inner chunks to
     # replay), the chunk decays and the dB/dC block partials
     st = 4 * 64 * 8 * 64 * 128
