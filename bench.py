@@ -644,7 +644,7 @@ def run_ours(args):
     names = fwd_names + bwd_names
     single = [j for j in range(len(kern_ms)) if not (chunked and kinds[j] in PIPELINED_KINDS)]
     top = max(single, key=lambda j: kern_ms[j])
-    # The roofline of the method (the survey's measurement plan): its algorithmic flops, 27 d^2
+    # The roofline of the method: its algorithmic flops, 27 d^2
     # per head-token (forward 7, one recompute 5, backward 15), against the FP32 pipe of this
     # device; the compulsory bytes at the measured HBM bandwidth are the other floor, far lower.
     peak32, sms, mhz, peak32_src = fp32_peak(dev)
