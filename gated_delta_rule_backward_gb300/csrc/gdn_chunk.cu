@@ -363,6 +363,12 @@ __device__ void chunk_prep(const float* QKs, const float* gs, const float* bs, f
     unit_lower_inverse(Ts, Zs, Dm, bs, tid);  // Dm's strict upper half is zero
 }
 
+// L2 prefetches of [p, p + nf) (whole 128-byte lines), spread over the CTA's threads.
+__device__ __forceinline__ void prefetch_span(const float* p, long long nf, int tid)
+{
+    for (long long o = 32LL * tid; o < nf; o += 32LL * CT) tc::prefetch_l2(p + o);
+}
+
 __device__ __forceinline__ void load_gate_beta(const ChunkArgs& A, int n, int h, const ChunkPos& cp,
                                                float* gs, float* bs, int tid)
 {
@@ -1043,6 +1049,25 @@ __global__ void __launch_bounds__(CT, 1) gdn_chunk_grad_kernel(const ChunkArgs A
         const long long head = (long long)n * A.H_v + h;
         const long long ch = head * A.n_chunks + c;
         __syncthreads();
+        if (rho + 1 < r) {  // the next value head's rows and tiles into L2 while this one computes
+            const int h1 = h + A.H_k;
+            const long long head1 = (long long)n * A.H_v + h1, ch1 = head1 * A.n_chunks + c;
+            if (tid < cp.nb * (D / 32)) {
+                const int t = tid / (D / 32), q = tid - t * (D / 32);
+                tc::prefetch_l2(A.v + (long long)n * A.vs0 + (long long)(cp.t0 + t) * A.vs1 + (long long)h1 * A.vs2 + 32 * q);
+                tc::prefetch_l2(A.gy + (long long)n * A.gys0 + (long long)(cp.t0 + t) * A.gys1 + (long long)h1 * A.gys2 + 32 * q);
+            }
+            prefetch_span(A.ws + A.o_dX + ch1 * (BC * D), BC * D, tid);
+            prefetch_span(A.ws + A.o_dDel + ch1 * (BC * D), BC * D, tid);
+            prefetch_span(cp.loc == 0 ? A.ckpt + (head1 * A.n_ck + cp.seg) * (long long)(D * D)
+                                      : A.ws + A.o_Mc + ch1 * (long long)(D * D),
+                          D * D, tid);
+            prefetch_span(A.ws + A.o_Tr + ch1 * (BC * BC), BC * BC, tid);
+            prefetch_span(A.ws + A.o_Z + ch1 * (BC * BC), BC * BC, tid);
+            prefetch_span(A.ws + A.o_KK + ch1 * (BC * BC), BC * BC, tid);
+            prefetch_span(A.ws + A.o_QK + ch1 * (BC * BC), BC * BC, tid);
+            prefetch_span(A.ws + A.o_Dm + ch1 * (BC * BC), BC * BC, tid);
+        }
         load_gate_beta(A, n, h, cp, gs, bs, tid);
         {
             const long long tv = (long long)n * A.vs0 + (long long)cp.t0 * A.vs1 + (long long)h * A.vs2;
