@@ -453,11 +453,13 @@ namespace {
 // The backward's ranges and their shares of the segments, in the order the backward walks
 // them (the last segments first).  The first range is the smaller: its prep and dM chain
 // run with nothing beside them, while the second range's run beside the first range's
-// gradient step.  At the 4096-token, 64-segment workload, on one GB300, three runs each:
-// 40/60 1.833 ms per step, 45/55 1.840, 35/65 1.870, 30/70 1.880, 50/50 1.881 (three
-// ranges were 1.90-1.94 when last tried).
+// gradient step.  At the 4096-token, 64-segment workload, on one GB300: 40/60 1.833 ms per
+// step, 45/55 1.840, 35/65 1.870, 30/70 1.880, 50/50 1.881 (three runs each; three ranges
+// were 1.90-1.94 when last tried).  After the gradient step's code shrank (it shares its SMs
+// with the second range's prep and dM chain) 35/65 took the lead: 1.713-1.715 ms against
+// 1.714-1.740 for 40/60 (four alternating runs each), 45/55 1.726-1.747.
 constexpr int kBwdRanges = 2;
-constexpr int kBwdWalkPct[gdn::kMaxRanges] = {40, 60, 0, 0};
+constexpr int kBwdWalkPct[gdn::kMaxRanges] = {35, 65, 0, 0};
 }  // namespace
 
 int gdn::pipeline_ranges(int n_ck, bool backward)

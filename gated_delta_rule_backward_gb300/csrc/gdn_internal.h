@@ -181,7 +181,7 @@ int pipeline_ranges(int n_ck, bool backward);
 // Checkpoint segments [s_lo, s_hi) of range r of R.  The forward's 4 ranges grow (10, 20,
 // 30, 40 % of the segments, from 40 segments up): the state chain cannot start before the
 // first range's prep, and each later prep is shorter than the chain range it runs beside.
-// The backward's 2 ranges take 40 and 60 % of the segments in walk order (the last
+// The backward's 2 ranges take 35 and 65 % of the segments in walk order (the last
 // segments first), from 40 segments up.  Otherwise equal.
 void range_segments(int n_ck, int R, bool backward, int r, int* s_lo, int* s_hi);
 
